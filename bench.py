@@ -1,0 +1,405 @@
+#!/usr/bin/env python3
+"""Benchmark: split-K GEMM + reduce, BF16 M=256 N=1024 K=2048, 2 splits.
+
+One "step" is one pack of 8 complete operations (partial pass + accumulation),
+the pages' pack=8 mode ("Aligned shared rows for pipelined NAX on CUDA",
+section "Measurement protocol": device events over a captured complete-
+operation graph, weights prepared and resident, preparation outside timing).
+Each operation of a step works on its own seeded instance (A, B, out,
+workspace), drawn from a pool of 40 instances whose inputs (200 MB) exceed the
+129 MB L2, so every operation reads its operands from HBM.
+
+Printed (one JSON line, rank 0): value = microseconds per operation (lower is
+better), the roofline of the dominant kernel measured live with CUDA events,
+the end-to-end figure through the public API with host buffers, the clocks
+seen during the timed region, and the CPU oracle's time for the same work.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--mode fused|two_pass] [--pack 8] [--pool 40]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M, N, K, SPLITS, KPS = 256, 1024, 2048, 2, 1024
+DTYPE = "bf16"
+WORKLOAD = "BF16 split-K GEMM M=256 N=1024 K=2048 splits=2 (k_per_split=1024) + reduce"
+METRIC = BASE_METRIC = "split-K GEMM+reduce µs/op & TFLOP/s, % of roofline (BF16 M256/N1024/K2048)"
+FLOPS_PER_OP = 2 * M * N * K
+BYTES_2PASS = M * K * 2 + N * K * 2 + 2 * SPLITS * M * N * 4 + M * N * 4   # A+B, P write+read, out
+BYTES_FUSED = M * K * 2 + N * K * 2 + M * N * 4                             # A+B, out
+BYTES_GEMM = M * K * 2 + N * K * 2 + SPLITS * M * N * 4                     # A+B, P write
+BYTES_REDUCE = SPLITS * M * N * 4 + M * N * 4                               # P read, out write
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML during a region."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self.period = period_s
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:   # 1 = SM clock
+                self.max_mhz = mx.value
+            self.nv, self.h, self.ok = nv, h, True
+        except OSError:
+            pass
+
+    def _run(self):
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        names = [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+class OracleSample:
+    """The oracle's evaluation (every partial slab, plus the unsplit output and
+    its bounds) of `rows` output rows of the workload.  The work is linear in
+    the rows, so its time scales to one whole operation by M/rows."""
+
+    def __init__(self, rows: int = 32):
+        import oracle
+        import splitk_inputs as gen
+
+        self.oracle = oracle
+        ops = gen.uniform(M, N, K, DTYPE, seed=0)
+        self.A = ops.A[:rows].copy()
+        self.B = ops.B
+        self.rows = rows
+        self.threads = max(1, len(os.sched_getaffinity(0)))
+        self.cores = min(self.threads, rows)
+
+    def once(self) -> float:
+        """Seconds for one sample."""
+        t0 = time.perf_counter()
+        self.oracle.partials(self.A, self.B, DTYPE, K, SPLITS, KPS, threads=self.threads)
+        self.oracle.output(self.A, self.B, DTYPE, threads=self.threads)
+        return time.perf_counter() - t0
+
+    def us_per_op(self, seconds: float) -> float:
+        return seconds * (M / self.rows) * 1e6
+
+    def describe(self, reps: int) -> str:
+        return (f"{self.rows} of {M} output rows (all {N} columns, all of K), {reps} repetition(s) of "
+                f"the oracle's partials + unsplit output, scaled by {M}/{self.rows}")
+
+
+def oracle_rows_timing(seconds: float, rows: int = 32):
+    smp = OracleSample(rows)
+    smp.once()   # warm-up
+    reps, total = 0, 0.0
+    while total < seconds or reps == 0:
+        total += smp.once()
+        reps += 1
+    return smp.us_per_op(total / reps), smp.cores, smp.describe(reps)
+
+
+def nvml_index(torch, dev) -> int:
+    """NVML index of the CUDA device (matched by PCI bus id when possible)."""
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        nv.nvmlInit_v2()
+        h = ctypes.c_void_p()
+        if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0:
+            idx = ctypes.c_uint()
+            if nv.nvmlDeviceGetIndex(h, ctypes.byref(idx)) == 0:
+                return idx.value
+    except (OSError, AttributeError):
+        pass
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def make_pool(torch, n_inst, dev):
+    import numpy as np
+
+    import splitk_inputs as gen
+
+    pool = []
+    for i in range(n_inst):
+        ops = gen.uniform(M, N, K, DTYPE, seed=i)
+        A = torch.from_numpy(ops.A.view(np.int16)).to(dev).view(torch.bfloat16)
+        B = torch.from_numpy(ops.B.view(np.int16)).to(dev).view(torch.bfloat16)
+        pool.append({"A_host": torch.from_numpy(ops.A.view(np.int16)).view(torch.bfloat16).pin_memory(),
+                     "A": A, "B": B,
+                     "out": torch.empty((M, N), dtype=torch.float32, device=dev),
+                     "ws": torch.empty((SPLITS * M * N,), dtype=torch.float32, device=dev),
+                     "out_host": torch.empty((M, N), dtype=torch.float32).pin_memory()})
+    return pool
+
+
+def capture(torch, stream, fn):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def time_graphs(torch, stream, graphs, steps):
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for k in range(steps):
+            graphs[k % len(graphs)].replay()
+        stop.record(stream)
+    stop.synchronize()
+    return start.elapsed_time(stop)   # ms
+
+
+def run_ours(args, rank, world, dev, torch, dist):
+    import split_bf16_gemm_gb300 as sk
+
+    sk.build()
+    sk.lib()
+    pack = args.pack
+    n_inst = max(args.pool, pack)
+    n_inst -= n_inst % pack
+    pool = make_pool(torch, n_inst, dev)
+    nbytes = sk.gemm_bt_workspace_bytes(M, N, K, SPLITS, KPS)
+    fused = 1 if args.mode == "fused" else 0
+    plan = sk.splitk_describe_launch(M, N, K, SPLITS, KPS, DTYPE, fused=fused)
+    stream = torch.cuda.Stream(device=dev)
+    groups = [pool[g * pack:(g + 1) * pack] for g in range(n_inst // pack)]
+
+    def op(inst):
+        sk.gemm_bt(inst["A"], inst["B"], inst["out"], inst["ws"], nbytes, M, N, K, SPLITS, KPS,
+                   DTYPE, fused=fused, stream=stream)
+
+    def gemm_only(inst):
+        sk.gemm_splitk_bt(inst["A"], inst["B"], inst["ws"], M, N, K, SPLITS, KPS, DTYPE, stream=stream)
+
+    def reduce_only(inst):
+        sk.splitk_reduce(inst["ws"], inst["out"], SPLITS, M, N, stream=stream)
+
+    torch.cuda.synchronize()
+    graphs = [capture(torch, stream, lambda grp=grp: [op(i) for i in grp]) for grp in groups]
+
+    # sanity before timing: the fused and two-kernel paths agree bitwise
+    inst = pool[0]
+    sk.gemm_bt(inst["A"], inst["B"], inst["out"], inst["ws"], nbytes, M, N, K, SPLITS, KPS, DTYPE,
+               fused=0, stream=stream)
+    torch.cuda.synchronize()
+    ref = inst["out"].clone()
+    sk.gemm_bt(inst["A"], inst["B"], inst["out"], inst["ws"], nbytes, M, N, K, SPLITS, KPS, DTYPE,
+               fused=1, stream=stream)
+    torch.cuda.synchronize()
+    if not torch.equal(ref, inst["out"]):
+        raise RuntimeError("fused and two-kernel outputs differ")
+
+    time_graphs(torch, stream, graphs, max(args.warmup, 3))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(nvml_index(torch, dev)) as clocks:
+        ms = time_graphs(torch, stream, graphs, args.steps)
+    torch.cuda.synchronize()
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if sk.splitk_get_device_status(stream) != 0:
+        raise RuntimeError("a kernel's bounded wait ran out during the timed region")
+    ms_per_step = ms / args.steps
+    us_per_op = ms * 1e3 / (args.steps * pack * world)
+
+    # dominant kernel(s), timed alone over the same pool
+    gemm_graphs = [capture(torch, stream, lambda grp=grp: [gemm_only(i) for i in grp]) for grp in groups]
+    red_graphs = [capture(torch, stream, lambda grp=grp: [reduce_only(i) for i in grp]) for grp in groups]
+    reps = max(args.steps, 50)
+    time_graphs(torch, stream, gemm_graphs, 5)
+    gemm_us = time_graphs(torch, stream, gemm_graphs, reps) * 1e3 / (reps * pack)
+    time_graphs(torch, stream, red_graphs, 5)
+    red_us = time_graphs(torch, stream, red_graphs, reps) * 1e3 / (reps * pack)
+    two_pass_graphs = [capture(torch, stream, lambda grp=grp: [(gemm_only(i), reduce_only(i)) for i in grp])
+                       for grp in groups]
+    time_graphs(torch, stream, two_pass_graphs, 5)
+    two_pass_us = time_graphs(torch, stream, two_pass_graphs, reps) * 1e3 / (reps * pack)
+    if fused:
+        dom_name, dom_us, dom_bytes = "tc_splitk_kernel (fused: partials + split sum)", us_per_op * world, BYTES_FUSED
+    else:
+        dom_name, dom_us, dom_bytes = "tc_splitk_kernel (partial pass)", gemm_us, BYTES_GEMM
+
+    # end to end through the public API, host buffers: H2D of A, the call, D2H of out
+    e2e_steps = max(3, min(args.steps, 200))
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def e2e_step(k):
+        for inst in groups[k % len(groups)]:
+            inst["A"].copy_(inst["A_host"], non_blocking=True)
+            op(inst)
+            inst["out_host"].copy_(inst["out"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for k in range(3):
+            e2e_step(k)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for k in range(e2e_steps):
+            e2e_step(k)
+        stop.record(stream)
+    stop.synchronize()
+    e2e_us = start.elapsed_time(stop) * 1e3 / (e2e_steps * pack)
+
+    hbm, tflops, peak_kind = load_peaks()
+    achieved = dom_bytes / (dom_us * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": round(us_per_op, 4), "unit": "µs/op", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
+        "data": "synthetic (seeded uniform[-1,1], zero first A row, x4 last A row)",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "splits": SPLITS,
+                   "k_per_split": KPS, "mode": args.mode, "ops_per_step": pack,
+                   "instances": n_inst,
+                   "l2": f"inputs larger than L2: {n_inst} distinct instances, "
+                         f"{n_inst * (M * K + N * K) * 2 / 1e6:.0f} MB of A+B, cycled",
+                   "timing": "CUDA graph per step, CUDA events on the launching stream",
+                   "plan": plan},
+        "tflops": round(FLOPS_PER_OP / (us_per_op * 1e-6) / 1e12 / 1, 2),
+        "op_roofline": {
+            "t_roof_us_2pass_bytes": round(BYTES_2PASS / (hbm * 1e9) * 1e6, 4),
+            "frac_2pass_bytes": round(BYTES_2PASS / (hbm * 1e9) * 1e6 / us_per_op, 4),
+            "t_roof_us_min_bytes": round(BYTES_FUSED / (hbm * 1e9) * 1e6, 4),
+            "frac_min_bytes": round(BYTES_FUSED / (hbm * 1e9) * 1e6 / us_per_op, 4),
+            "peak": f"{peak_kind} {hbm} GB/s"},
+        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": None, "bytes_per_launch": dom_bytes,
+                     "launch_us": round(dom_us, 4), "peak_kind": peak_kind},
+        "kernels_us": {"partial_pass": round(gemm_us, 4), "reduce": round(red_us, 4),
+                       "two_pass_op": round(two_pass_us, 4),
+                       "fused_op" if fused else "two_pass_op_graph": round(us_per_op * world, 4)},
+        "e2e": {"value": round(e2e_us, 4), "unit": "µs/op", "h2d_bytes_per_step": pack * M * K * 2,
+                "d2h_bytes_per_step": pack * M * N * 4,
+                "how": "per op: pinned A -> device, gemm_bt via the Python binding, out -> pinned host; "
+                       "B resident (prepared weights); no graph"},
+        "gpu_launches": args.steps * pack * plan["kernels_per_call"],
+        "clocks": clocks.summary(),
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--mode", choices=["fused", "two_pass"], default="fused")
+    ap.add_argument("--pack", type=int, default=8)
+    ap.add_argument("--pool", type=int, default=40)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        # The reference arm is the oracle, timed on the host cores; rank 0 only.
+        if rank != 0:
+            return
+        smp = OracleSample()
+        for _ in range(args.warmup):
+            smp.once()
+        us_list = [smp.us_per_op(smp.once()) for _ in range(args.steps)]
+        cores, sample = smp.cores, smp.describe(1)
+        us = statistics.mean(us_list)
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": round(us, 2), "unit": "µs/op",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(us * 32 / M / 1e3, 4), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "splits": SPLITS,
+                       "k_per_split": KPS},
+            "cpu_baseline": {"value": round(us, 2), "unit": "µs/op", "cores": cores,
+                             "kind": "oracle", "sample": "per step: " + sample},
+            "e2e": {"value": round(us, 2), "unit": "µs/op", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}))
+        return
+
+    import torch
+
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+
+        tdist.init_process_group("nccl")
+        dist = tdist
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    line = run_ours(args, rank, world, dev, torch, dist)
+    if rank == 0 and world == 1:
+        us, cores, sample = oracle_rows_timing(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(us, 2), "unit": "µs/op", "cores": cores,
+                                "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+/*
+ * splitk.h -- C ABI of libsplitk: split-K GEMM with prepared, transposed
+ * weights, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (pages "Aligned shared rows for pipelined NAX on CUDA", section
+ * "Contract and correctness", and "Wider consecutive-weight NAX GEMM", section
+ * "Launch contract and correctness"):
+ *
+ *   A        row-major [M,K]          F32, F16 or BF16
+ *   B        row-major [N,K]          same element type; the prepared weight,
+ *                                     i.e. the transpose of a [K,N] weight
+ *   split s  covers k in [s*kps, min((s+1)*kps, K))
+ *   partials[s,m,n] = sum_{k in split s} A[m,k] * B[n,k]     F32, [splits,M,N]
+ *   out[m,n]        = sum_{s=0}^{splits-1} partials[s,m,n]   F32, [M,N]
+ *
+ * The second line is the separate accumulation pass the pages run after the
+ * partial pass ("an existing accumulation pass produces the final output").
+ *
+ * Contract enforced by every entry point before any device work:
+ *   - M, K and k_per_split are positive multiples of 32; N is a positive
+ *     multiple of 64;                                   else SPLITK_ERR_SHAPE
+ *   - every split starts below K and the splits cover K, i.e.
+ *     splits == ceil(K / k_per_split);                  else SPLITK_ERR_SPLIT
+ *   - M, N, K <= SPLITK_MAX_DIM and splits <= SPLITK_MAX_SPLITS
+ *     (implementation limits);                           else SPLITK_ERR_SHAPE
+ *   - no pointer is NULL;                                else SPLITK_ERR_NULL
+ *   - every pointer is 16-byte aligned;                  else SPLITK_ERR_ALIGN
+ *   - output byte ranges overlap neither the input ranges nor each other
+ *     (A and B may overlap each other: both are only read); else SPLITK_ERR_ALIAS
+ *
+ * Memory and ownership: every data pointer is a DEVICE pointer on the current
+ * CUDA device, owned by the caller.  The library allocates no device memory
+ * on any call path and keeps no pointer after a call returns.
+ *
+ * Asynchrony and errors: calls enqueue work on `stream` (a cudaStream_t, passed
+ * as void*; NULL means the legacy default stream) and return without
+ * synchronising.  A non-zero return means nothing was enqueued (validation
+ * failed) or the launch itself failed (SPLITK_ERR_CUDA).  No exception and no
+ * abort crosses the ABI.  Every wait inside a kernel has a time limit; a wait
+ * that runs out sets a device status word, which splitk_get_device_status()
+ * reads.  The three compute entry points (gemm_splitk_bt, splitk_reduce,
+ * gemm_bt) may be captured into a CUDA graph.
+ */
+#ifndef SPLITK_H
+#define SPLITK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of A and B.  Partials and the output are always F32. */
+typedef enum {
+    SPLITK_F32 = 0,
+    SPLITK_F16 = 1,
+    SPLITK_BF16 = 2
+} splitk_dtype;
+
+typedef enum {
+    SPLITK_OK = 0,
+    SPLITK_ERR_NULL = -1,           /* a required pointer is NULL */
+    SPLITK_ERR_SHAPE = -2,          /* M,K,kps not positive multiples of 32, N of 64, or too large */
+    SPLITK_ERR_SPLIT = -3,          /* splits != ceil(K/kps): a split starts at/after K or K is not covered */
+    SPLITK_ERR_ALIAS = -4,          /* an output range overlaps an input or another output */
+    SPLITK_ERR_ALIGN = -5,          /* a pointer is not 16-byte aligned */
+    SPLITK_ERR_DTYPE = -6,          /* unknown element type */
+    SPLITK_ERR_WORKSPACE = -7,      /* workspace smaller than gemm_bt_workspace_bytes() */
+    SPLITK_ERR_CUDA = -8,           /* a CUDA runtime call or launch failed */
+    SPLITK_ERR_DEVICE_TIMEOUT = -9, /* a kernel's bounded wait ran out (see splitk_get_device_status) */
+    SPLITK_ERR_CONFIG = -10         /* an invalid tile override */
+} splitk_status;
+
+#define SPLITK_MAX_DIM (1 << 22)
+#define SPLITK_MAX_SPLITS 4096
+
+/* Checks the contract's shape and split rules only (no pointers, no device
+ * work).  Returns SPLITK_OK, SPLITK_ERR_SHAPE or SPLITK_ERR_SPLIT; the shape
+ * rule is checked first. */
+int splitk_check_geometry(int64_t M, int64_t N, int64_t K, int64_t splits,
+                          int64_t k_per_split);
+
+/* The partial pass: partials[s,m,n] = sum over split s of A[m,k]*B[n,k].
+ *   A         device, [M,K] row-major, element type `dtype`
+ *   B         device, [N,K] row-major, element type `dtype`
+ *   partials  device, [splits,M,N] row-major F32; fully overwritten
+ * BF16/F16 operands run on the tensor cores (tcgen05, F32 accumulate in tensor
+ * memory, native operands); F32 operands run exact F32 FMA on the CUDA cores.
+ * Each element is a sum in F32 whose order is fixed for a given shape. */
+int gemm_splitk_bt(const void *A, const void *B, float *partials, int64_t M,
+                   int64_t N, int64_t K, int64_t splits, int64_t k_per_split,
+                   int dtype, void *stream);
+
+/* The accumulation pass: out[i] = (((P[0][i] + P[1][i]) + P[2][i]) + ...) in
+ * F32, in split order s = 0..splits-1.
+ *   partials  device, [splits,M,N] F32, read only
+ *   out       device, [M,N] F32; fully overwritten
+ * Requires M, N >= 1, splits >= 1, 16-byte aligned pointers and no overlap
+ * between the two ranges. */
+int splitk_reduce(const float *partials, float *out, int64_t splits, int64_t M,
+                  int64_t N, void *stream);
+
+/* Bytes of device workspace gemm_bt needs: room for the F32 partials
+ * [splits,M,N].  Returns 0 for a geometry that breaks the contract. */
+size_t gemm_bt_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t splits,
+                               int64_t k_per_split, int fused);
+
+/* One call: the partial pass then the accumulation pass, on one stream.
+ *   out        device, [M,N] F32; fully overwritten
+ *   workspace  device, >= gemm_bt_workspace_bytes() bytes, caller-owned
+ *              scratch; may not overlap A, B or out
+ *   fused      0: two kernels (gemm_splitk_bt, then splitk_reduce), the
+ *                 partials left in the workspace;
+ *              1: one kernel whose thread-block cluster also sums the splits
+ *                 (tensor-core types, splits <= 16); the workspace is left
+ *                 untouched; with F32 operands or more than 16 splits the
+ *                 two-kernel path runs instead;
+ *              3: as 1, and the partials are also written to the workspace.
+ * For a given shape, `out` is bitwise the same for every `fused` value. */
+int gemm_bt(const void *A, const void *B, float *out, void *workspace,
+            size_t workspace_bytes, int64_t M, int64_t N, int64_t K,
+            int64_t splits, int64_t k_per_split, int dtype, int fused,
+            void *stream);
+
+/* Reads and clears the device status word on the current device,
+ * synchronising `stream` first.  Returns SPLITK_OK, SPLITK_ERR_DEVICE_TIMEOUT
+ * (a kernel's bounded wait ran out since the last call; its outputs are not
+ * valid) or SPLITK_ERR_CUDA. */
+int splitk_get_device_status(void *stream);
+
+/* A short, static description of a status code. */
+const char *splitk_status_string(int status);
+
+/* Tile-shape override for tuning: every later tensor-core launch uses tile
+ * width `bn` (64, 128 or 256; must divide N, else the automatic choice is
+ * kept) and `chunks` thread blocks per split along K (1, 2, 4, 8 or 16),
+ * where that is legal for the shape.  bn = chunks = 0 restores the automatic
+ * choice.  Process-wide; not thread-safe against concurrent launches.
+ * Returns SPLITK_OK or SPLITK_ERR_CONFIG. */
+int splitk_set_tile_override(int bn, int chunks);
+
+/* Describes the launch gemm_bt would make, without launching: info[0..11] =
+ * {path (0 tensor-core, 1 F32 FMA), bn, chunks, chunk_len, stages,
+ *  cluster_size, grid_x, grid_y, grid_z, dynamic_smem_bytes,
+ *  fused_in_kernel (0/1), kernels_per_call}.  Returns a status as gemm_bt's
+ * validation would (pointers are not checked). */
+int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits,
+                           int64_t k_per_split, int dtype, int fused,
+                           int *info);
+
+/* Self-test of the bounded-wait machinery: launches one block that waits on a
+ * barrier nothing ever completes, with a limit of `limit_ns` nanoseconds
+ * (clamped to [1e3, 1e9]), synchronises `stream`, and returns what
+ * splitk_get_device_status() then reads (SPLITK_ERR_DEVICE_TIMEOUT expected). */
+int splitk_selftest_bounded_wait(int64_t limit_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPLITK_H */

@@ -1,0 +1,155 @@
+"""ctypes binding of libsplitk's C ABI (include/splitk.h), with the same names.
+
+Argument marshalling only: tensors become device pointers (``data_ptr()``),
+streams become ``cudaStream_t`` handles, a non-zero status becomes a
+``SplitKError``.  Every step of the computation runs in libsplitk's kernels;
+there is no fallback of any kind, and every call fails loudly when the
+library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsplitk.so")
+
+# Element types and status codes, as in include/splitk.h.
+F32, F16, BF16 = 0, 1, 2
+OK = 0
+ERR_NULL, ERR_SHAPE, ERR_SPLIT, ERR_ALIAS, ERR_ALIGN = -1, -2, -3, -4, -5
+ERR_DTYPE, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_CONFIG = -6, -7, -8, -9, -10
+
+EXPORTS = (
+    "splitk_check_geometry", "gemm_splitk_bt", "splitk_reduce", "gemm_bt_workspace_bytes",
+    "gemm_bt", "splitk_get_device_status", "splitk_status_string", "splitk_set_tile_override",
+    "splitk_describe_launch", "splitk_selftest_bounded_wait",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SplitKError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({status_string(status)})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libsplitk (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libsplitk is not built ({LIB_PATH} missing); "
+                                   "run split_bf16_gemm_gb300.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+            L.splitk_check_geometry.argtypes = [i64] * 5
+            L.gemm_splitk_bt.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, vp]
+            L.splitk_reduce.argtypes = [vp, vp, i64, i64, i64, vp]
+            L.gemm_bt_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i32]
+            L.gemm_bt_workspace_bytes.restype = sz
+            L.gemm_bt.argtypes = [vp, vp, vp, vp, sz, i64, i64, i64, i64, i64, i32, i32, vp]
+            L.splitk_get_device_status.argtypes = [vp]
+            L.splitk_status_string.argtypes = [i32]
+            L.splitk_status_string.restype = ctypes.c_char_p
+            L.splitk_set_tile_override.argtypes = [i32, i32]
+            L.splitk_describe_launch.argtypes = [i64, i64, i64, i64, i64, i32, i32, vp]
+            L.splitk_selftest_bounded_wait.argtypes = [i64, vp]
+            for name in ("splitk_check_geometry", "gemm_splitk_bt", "splitk_reduce", "gemm_bt",
+                         "splitk_get_device_status", "splitk_set_tile_override",
+                         "splitk_describe_launch", "splitk_selftest_bounded_wait"):
+                getattr(L, name).restype = i32
+            _lib = L
+    return _lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def dtype_code(dtype) -> int:
+    """Element-type code from a name ('bf16', 'f16', 'f32'), a torch dtype or an int."""
+    if isinstance(dtype, int):
+        return dtype
+    if isinstance(dtype, str):
+        return {"f32": F32, "f16": F16, "bf16": BF16}[dtype]
+    import torch
+
+    return {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}[dtype]
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise SplitKError(status, where)
+
+
+def status_string(status: int) -> str:
+    return lib().splitk_status_string(status).decode()
+
+
+splitk_status_string = status_string
+
+
+def splitk_check_geometry(M, N, K, splits, k_per_split) -> int:
+    """Contract status of a geometry (0 legal, ERR_SHAPE or ERR_SPLIT); never raises."""
+    return lib().splitk_check_geometry(M, N, K, splits, k_per_split)
+
+
+def gemm_splitk_bt(A, B, partials, M, N, K, splits, k_per_split, dtype, stream=None) -> None:
+    _check(lib().gemm_splitk_bt(_ptr(A), _ptr(B), _ptr(partials), M, N, K, splits, k_per_split,
+                                dtype_code(dtype), _stream(stream)), "gemm_splitk_bt")
+
+
+def splitk_reduce(partials, out, splits, M, N, stream=None) -> None:
+    _check(lib().splitk_reduce(_ptr(partials), _ptr(out), splits, M, N, _stream(stream)),
+           "splitk_reduce")
+
+
+def gemm_bt_workspace_bytes(M, N, K, splits, k_per_split, fused=0) -> int:
+    return int(lib().gemm_bt_workspace_bytes(M, N, K, splits, k_per_split, fused))
+
+
+def gemm_bt(A, B, out, workspace, workspace_bytes, M, N, K, splits, k_per_split, dtype, fused=0,
+            stream=None) -> None:
+    _check(lib().gemm_bt(_ptr(A), _ptr(B), _ptr(out), _ptr(workspace), workspace_bytes, M, N, K,
+                         splits, k_per_split, dtype_code(dtype), fused, _stream(stream)), "gemm_bt")
+
+
+def splitk_get_device_status(stream=None) -> int:
+    """Synchronises the stream, then reads and clears the device status word."""
+    return lib().splitk_get_device_status(_stream(stream))
+
+
+def splitk_set_tile_override(bn: int = 0, chunks: int = 0) -> None:
+    _check(lib().splitk_set_tile_override(bn, chunks), "splitk_set_tile_override")
+
+
+def splitk_describe_launch(M, N, K, splits, k_per_split, dtype, fused=0) -> dict:
+    info = (ctypes.c_int * 12)()
+    _check(lib().splitk_describe_launch(M, N, K, splits, k_per_split, dtype_code(dtype), fused,
+                                        ctypes.addressof(info)), "splitk_describe_launch")
+    keys = ("path", "bn", "chunks", "chunk_len", "stages", "cluster", "grid_x", "grid_y",
+            "grid_z", "smem_bytes", "fused_in_kernel", "kernels_per_call")
+    return dict(zip(keys, list(info)))
+
+
+def splitk_selftest_bounded_wait(limit_ns: int = 1_000_000, stream=None) -> int:
+    return lib().splitk_selftest_bounded_wait(limit_ns, _stream(stream))

@@ -1,0 +1,244 @@
+// splitk_api.cu -- the C ABI of libsplitk (declared in include/splitk.h).
+//
+// Every entry point validates its arguments completely on the host before any
+// CUDA call: the launch contract of the pages "Aligned shared rows for
+// pipelined NAX on CUDA" (section "Contract and correctness") and "Wider
+// consecutive-weight NAX GEMM" (section "Launch contract and correctness"),
+// plus NULL, alignment and aliasing checks on the pointers.  Nothing here
+// allocates device memory.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "../../include/splitk.h"
+#include "splitk_internal.h"
+
+namespace {
+
+using splitk::GemmProblem;
+using splitk::TilePlan;
+
+int geometry_status(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps)
+{
+    // shape rule: M, K, kps positive multiples of 32; N a positive multiple of 64
+    if (M <= 0 || M % 32 || K <= 0 || K % 32 || kps <= 0 || kps % 32 || N <= 0 || N % 64)
+        return SPLITK_ERR_SHAPE;
+    if (M > SPLITK_MAX_DIM || N > SPLITK_MAX_DIM || K > SPLITK_MAX_DIM) return SPLITK_ERR_SHAPE;
+    // split rule: every split starts below K, and together they cover K
+    if (S <= 0 || (S - 1) * kps >= K || S * kps < K) return SPLITK_ERR_SPLIT;
+    if (S > SPLITK_MAX_SPLITS) return SPLITK_ERR_SPLIT;
+    return SPLITK_OK;
+}
+
+int elem_bytes(int dtype)
+{
+    switch (dtype) {
+    case SPLITK_F32: return 4;
+    case SPLITK_F16: return 2;
+    case SPLITK_BF16: return 2;
+    default: return 0;
+    }
+}
+
+struct Range {
+    uintptr_t lo, hi;   // [lo, hi)
+};
+
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+Range range_of(const void *p, uint64_t bytes)
+{
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + static_cast<uintptr_t>(bytes)};
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPLITK_OK : SPLITK_ERR_CUDA; }
+
+// Checks shared by gemm_splitk_bt and gemm_bt.
+int validate_gemm(const void *A, const void *B, int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps,
+                  int dtype)
+{
+    int st = geometry_status(M, N, K, S, kps);
+    if (st != SPLITK_OK) return st;
+    if (elem_bytes(dtype) == 0) return SPLITK_ERR_DTYPE;
+    if (!A || !B) return SPLITK_ERR_NULL;
+    if (!aligned16(A) || !aligned16(B)) return SPLITK_ERR_ALIGN;
+    return SPLITK_OK;
+}
+
+// The partial pass into P (and, when `out` is given, the split sum too).
+int run_partial_pass(const void *A, const void *B, float *P, float *out, int64_t M, int64_t N, int64_t K, int64_t S,
+                     int64_t kps, int dtype, bool fused, cudaStream_t stream)
+{
+    if (dtype == SPLITK_F32) {
+        return cuda_status(splitk::launch_simt_f32(static_cast<const float *>(A), static_cast<const float *>(B), P,
+                                                   M, N, K, S, kps, stream));
+    }
+    GemmProblem pr{A, B, P, out, M, N, K, S, kps, dtype == SPLITK_BF16};
+    const TilePlan plan = splitk::plan_tc(M, N, K, S, kps, fused);
+    return cuda_status(splitk::launch_tc(pr, plan, stream));
+}
+
+bool fused_possible(int dtype, int64_t S) { return dtype != SPLITK_F32 && S <= 16; }
+
+}  // namespace
+
+extern "C" {
+
+int splitk_check_geometry(int64_t M, int64_t N, int64_t K, int64_t splits, int64_t k_per_split)
+{
+    return geometry_status(M, N, K, splits, k_per_split);
+}
+
+int gemm_splitk_bt(const void *A, const void *B, float *partials, int64_t M, int64_t N, int64_t K, int64_t splits,
+                   int64_t k_per_split, int dtype, void *stream)
+{
+    int st = validate_gemm(A, B, M, N, K, splits, k_per_split, dtype);
+    if (st != SPLITK_OK) return st;
+    if (!partials) return SPLITK_ERR_NULL;
+    if (!aligned16(partials)) return SPLITK_ERR_ALIGN;
+    const int e = elem_bytes(dtype);
+    const Range ra = range_of(A, static_cast<uint64_t>(M * K) * e);
+    const Range rb = range_of(B, static_cast<uint64_t>(N * K) * e);
+    const Range rp = range_of(partials, static_cast<uint64_t>(splits * M * N) * 4);
+    if (overlap(rp, ra) || overlap(rp, rb)) return SPLITK_ERR_ALIAS;
+    return run_partial_pass(A, B, partials, nullptr, M, N, K, splits, k_per_split, dtype, false,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int splitk_reduce(const float *partials, float *out, int64_t splits, int64_t M, int64_t N, void *stream)
+{
+    if (M <= 0 || N <= 0 || M > SPLITK_MAX_DIM || N > SPLITK_MAX_DIM) return SPLITK_ERR_SHAPE;
+    if (splits <= 0 || splits > SPLITK_MAX_SPLITS) return SPLITK_ERR_SPLIT;
+    if (!partials || !out) return SPLITK_ERR_NULL;
+    if (!aligned16(partials) || !aligned16(out)) return SPLITK_ERR_ALIGN;
+    const Range rp = range_of(partials, static_cast<uint64_t>(splits * M * N) * 4);
+    const Range ro = range_of(out, static_cast<uint64_t>(M * N) * 4);
+    if (overlap(rp, ro)) return SPLITK_ERR_ALIAS;
+    return cuda_status(splitk::launch_reduce(partials, out, splits, M * N, static_cast<cudaStream_t>(stream)));
+}
+
+size_t gemm_bt_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t splits, int64_t k_per_split, int fused)
+{
+    (void)fused;
+    if (geometry_status(M, N, K, splits, k_per_split) != SPLITK_OK) return 0;
+    return static_cast<size_t>(splits * M * N) * 4;
+}
+
+int gemm_bt(const void *A, const void *B, float *out, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
+            int64_t K, int64_t splits, int64_t k_per_split, int dtype, int fused, void *stream)
+{
+    int st = validate_gemm(A, B, M, N, K, splits, k_per_split, dtype);
+    if (st != SPLITK_OK) return st;
+    if (fused != 0 && fused != 1 && fused != 3) return SPLITK_ERR_CONFIG;
+    if (!out) return SPLITK_ERR_NULL;
+    if (!aligned16(out)) return SPLITK_ERR_ALIGN;
+    const bool in_kernel = fused != 0 && fused_possible(dtype, splits);
+    const bool need_ws = !in_kernel || fused == 3;
+    const size_t ws_need = gemm_bt_workspace_bytes(M, N, K, splits, k_per_split, fused);
+    if (need_ws) {
+        if (!workspace) return SPLITK_ERR_NULL;
+        if (!aligned16(workspace)) return SPLITK_ERR_ALIGN;
+        if (workspace_bytes < ws_need) return SPLITK_ERR_WORKSPACE;
+    }
+    const int e = elem_bytes(dtype);
+    const Range ra = range_of(A, static_cast<uint64_t>(M * K) * e);
+    const Range rb = range_of(B, static_cast<uint64_t>(N * K) * e);
+    const Range ro = range_of(out, static_cast<uint64_t>(M * N) * 4);
+    if (overlap(ro, ra) || overlap(ro, rb)) return SPLITK_ERR_ALIAS;
+    if (need_ws) {
+        const Range rw = range_of(workspace, ws_need);
+        if (overlap(rw, ra) || overlap(rw, rb) || overlap(rw, ro)) return SPLITK_ERR_ALIAS;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float *P = static_cast<float *>(workspace);
+    if (in_kernel)
+        return run_partial_pass(A, B, fused == 3 ? P : nullptr, out, M, N, K, splits, k_per_split, dtype, true, s);
+    st = run_partial_pass(A, B, P, nullptr, M, N, K, splits, k_per_split, dtype, false, s);
+    if (st != SPLITK_OK) return st;
+    return cuda_status(splitk::launch_reduce(P, out, splits, M * N, s));
+}
+
+int splitk_get_device_status(void *stream)
+{
+    unsigned status = 0;
+    if (splitk::read_and_clear_device_status(static_cast<cudaStream_t>(stream), &status) != cudaSuccess)
+        return SPLITK_ERR_CUDA;
+    return status ? SPLITK_ERR_DEVICE_TIMEOUT : SPLITK_OK;
+}
+
+const char *splitk_status_string(int status)
+{
+    switch (status) {
+    case SPLITK_OK: return "ok";
+    case SPLITK_ERR_NULL: return "a required pointer is NULL";
+    case SPLITK_ERR_SHAPE: return "M, K and k_per_split must be positive multiples of 32 and N of 64 (within limits)";
+    case SPLITK_ERR_SPLIT: return "splits must equal ceil(K / k_per_split): every split starts below K and they cover K";
+    case SPLITK_ERR_ALIAS: return "an output range overlaps an input or another output";
+    case SPLITK_ERR_ALIGN: return "pointers must be 16-byte aligned";
+    case SPLITK_ERR_DTYPE: return "unknown element type";
+    case SPLITK_ERR_WORKSPACE: return "workspace smaller than gemm_bt_workspace_bytes()";
+    case SPLITK_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case SPLITK_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    case SPLITK_ERR_CONFIG: return "invalid configuration value";
+    default: return "unknown status";
+    }
+}
+
+int splitk_set_tile_override(int bn, int chunks)
+{
+    if (bn != 0 && bn != 64 && bn != 128 && bn != 256) return SPLITK_ERR_CONFIG;
+    if (chunks != 0 && chunks != 1 && chunks != 2 && chunks != 4 && chunks != 8 && chunks != 16)
+        return SPLITK_ERR_CONFIG;
+    splitk::set_tile_override(bn, chunks);
+    return SPLITK_OK;
+}
+
+int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int64_t k_per_split, int dtype, int fused,
+                           int *info)
+{
+    int st = geometry_status(M, N, K, splits, k_per_split);
+    if (st != SPLITK_OK) return st;
+    if (elem_bytes(dtype) == 0) return SPLITK_ERR_DTYPE;
+    if (!info) return SPLITK_ERR_NULL;
+    std::fill(info, info + 12, 0);
+    if (dtype == SPLITK_F32) {
+        info[0] = 1;
+        info[1] = 64;
+        info[2] = 1;
+        info[3] = static_cast<int>(k_per_split);
+        info[5] = 1;
+        info[6] = static_cast<int>(N / 64);
+        info[7] = static_cast<int>((M + 63) / 64);
+        info[8] = static_cast<int>(splits);
+        info[11] = 2;
+        return SPLITK_OK;
+    }
+    const bool in_kernel = fused != 0 && fused_possible(dtype, splits);
+    const TilePlan p = splitk::plan_tc(M, N, K, splits, k_per_split, in_kernel);
+    info[0] = 0;
+    info[1] = p.bn;
+    info[2] = p.chunks;
+    info[3] = p.chunk_len;
+    info[4] = p.stages;
+    info[5] = p.cluster;
+    info[6] = static_cast<int>(p.grid.x);
+    info[7] = static_cast<int>(p.grid.y);
+    info[8] = static_cast<int>(p.grid.z);
+    info[9] = static_cast<int>(p.smem_bytes);
+    info[10] = in_kernel ? 1 : 0;
+    info[11] = in_kernel ? 1 : 2;
+    return SPLITK_OK;
+}
+
+int splitk_selftest_bounded_wait(int64_t limit_ns, void *stream)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (splitk::launch_wait_selftest(limit_ns, s) != cudaSuccess) return SPLITK_ERR_CUDA;
+    return splitk_get_device_status(stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,245 @@
+"""GPU parity: libsplitk through its C ABI against the F64 oracle.
+
+Every case poisons the partials and the output (7.0) and puts 64 guards of
+11.0 behind each; a NaN-poison pass removes the chance that a stale 7.0 lands
+within tolerance.  Shapes cover the pages' workloads (the single tile, M96,
+M256/N512, the M256/N1024 headline, the dtype x split sweep with the skinny,
+short-K and short-final-split shapes) and the pages' test categories
+(non-square, odd tile counts, long K, larger matrices).
+"""
+import numpy as np
+import pytest
+
+from harness import (TOL_FINAL, TOL_PARTIAL, Guarded, device_operand, max_scaled_error,
+                     oracle_case)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import split_bf16_gemm_gb300 as sk
+
+    sk.build()
+    sk.lib()
+    sk.splitk_set_tile_override(0, 0)
+    yield sk
+    sk.splitk_set_tile_override(0, 0)
+
+
+WORKLOADS = [  # (M, N, K, splits, kps, dtype): the pages' workloads
+    (32, 64, 128, 2, 64, "bf16"),
+    (96, 512, 2048, 4, 512, "bf16"),
+    (256, 512, 2048, 4, 512, "bf16"),
+    (256, 512, 2048, 2, 1024, "bf16"),
+    (256, 1024, 2048, 2, 1024, "bf16"),
+]
+SWEEP = []
+for _dt in ("f32", "f16", "bf16"):
+    for _S in (1, 2, 4, 8, 16):
+        SWEEP.append((32, 512, 2048, _S, 2048 // _S, _dt))
+        SWEEP.append((96, 512, 512, _S, 512 // _S, _dt))
+    SWEEP.append((64, 128, 160, 3, 64, _dt))
+CATEGORIES = [
+    (32, 64, 32, 1, 32, "bf16"),         # single tile, one split
+    (160, 192, 320, 3, 128, "bf16"),     # M tail past one 128-row tile, 3 N tiles, short final split
+    (96, 320, 1024, 2, 512, "f16"),      # odd tile count along N (5 x 64)
+    (64, 128, 8192, 4, 2048, "bf16"),    # long K
+    (512, 2048, 4096, 4, 1024, "bf16"),  # larger matrices
+    (32, 64, 64, 1, 128, "bf16"),        # k_per_split larger than K
+    (288, 256, 96, 3, 32, "f16"),        # 32-long splits everywhere
+]
+
+
+def ids(cases):
+    return [f"{dt}-M{M}N{N}K{K}S{S}" for M, N, K, S, kps, dt in cases]
+
+
+def run_two_pass(sk, ops, S, kps, poison=7.0):
+    M, N, K = ops.M, ops.N, ops.K
+    A = device_operand(ops.A, ops.dtype)
+    B = device_operand(ops.B, ops.dtype)
+    P = Guarded(S * M * N, poison)
+    out = Guarded(M * N, poison)
+    sk.gemm_splitk_bt(A, B, P.data, M, N, K, S, kps, ops.dtype)
+    sk.splitk_reduce(P.data, out.data, S, M, N)
+    assert sk.splitk_get_device_status() == 0
+    return A, B, P, out
+
+
+def check_case(sk, case, poison=7.0, recipe="uniform"):
+    M, N, K, S, kps, dt = case
+    ops, Pr, SP, Or, SO = oracle_case(M, N, K, S, kps, dt, recipe)
+    A, B, P, out = run_two_pass(sk, ops, S, kps, poison)
+    assert P.guards_intact() and out.guards_intact()
+    ep = max_scaled_error(P.numpy().reshape(S, M, N), Pr, SP)
+    eo = max_scaled_error(out.numpy().reshape(M, N), Or, SO)
+    assert ep <= TOL_PARTIAL, f"partials: max |err|/sum|ab| = {ep:.3e}"
+    assert eo <= TOL_FINAL[dt], f"output: max |err|/sum|ab| = {eo:.3e}"
+    return A, B, P, out
+
+
+@pytest.mark.parametrize("case", WORKLOADS + SWEEP + CATEGORIES, ids=ids(WORKLOADS + SWEEP + CATEGORIES))
+def test_two_pass_matches_oracle(lib, case):
+    check_case(lib, case)
+
+
+@pytest.mark.parametrize("case", WORKLOADS + CATEGORIES[:4] + SWEEP[-11:], ids=ids(WORKLOADS + CATEGORIES[:4] + SWEEP[-11:]))
+def test_nan_poison(lib, case):
+    check_case(lib, case, poison=float("nan"))
+
+
+@pytest.mark.parametrize("case", WORKLOADS + SWEEP[::3] + CATEGORIES, ids=ids(WORKLOADS + SWEEP[::3] + CATEGORIES))
+def test_gemm_bt_all_modes_bitwise(lib, case):
+    """gemm_bt with fused = 0, 1, 3 gives the two-kernel output bit for bit, and
+    fused = 3 writes the same partials as gemm_splitk_bt."""
+    sk = lib
+    M, N, K, S, kps, dt = case
+    ops, Pr, SP, Or, SO = oracle_case(M, N, K, S, kps, dt)
+    A, B, P, out = check_case(sk, case)
+    ref_out = out.numpy()
+    ref_P = P.numpy()
+    nbytes = sk.gemm_bt_workspace_bytes(M, N, K, S, kps)
+    for fused in (0, 1, 3):
+        ws = Guarded(nbytes // 4)
+        o = Guarded(M * N)
+        sk.gemm_bt(A, B, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=fused)
+        assert sk.splitk_get_device_status() == 0
+        assert o.guards_intact() and ws.guards_intact()
+        assert np.array_equal(o.numpy().view(np.uint32), ref_out.view(np.uint32)), f"fused={fused}"
+        if fused in (0, 3):
+            assert np.array_equal(ws.numpy().view(np.uint32), ref_P.view(np.uint32)), f"fused={fused}"
+        elif dt != "f32" and S <= 16:
+            assert np.all(ws.numpy() == 7.0), "fused=1 must leave the workspace untouched"
+
+
+INT_CASES = [
+    (32, 64, 32, 1, 32, "bf16"),
+    (32, 64, 128, 2, 64, "bf16"),
+    (64, 128, 160, 3, 64, "f16"),
+    (256, 1024, 2048, 2, 1024, "bf16"),
+    (96, 512, 2048, 4, 512, "f32"),
+]
+
+
+@pytest.mark.parametrize("case", INT_CASES, ids=ids(INT_CASES))
+def test_integer_inputs_bitwise(lib, case):
+    """Integer operands in [-8,8]: every product and partial sum is exact in
+    F32, so the GPU must equal the oracle exactly."""
+    sk = lib
+    M, N, K, S, kps, dt = case
+    ops, Pr, SP, Or, SO = oracle_case(M, N, K, S, kps, dt, "integers", 3)
+    _, _, P, out = run_two_pass(sk, ops, S, kps)
+    assert np.array_equal(P.numpy().reshape(S, M, N).astype(np.float64), Pr)
+    assert np.array_equal(out.numpy().reshape(M, N).astype(np.float64), Or)
+    assert P.guards_intact() and out.guards_intact()
+
+
+def test_golden_int_tile(lib):
+    from test_oracle_pins import load_int_tile
+
+    import splitk_inputs as gen
+
+    P_ref, O_ref = load_int_tile()
+    ops = gen.integers(32, 64, 128, "bf16", seed=3)
+    _, _, P, out = run_two_pass(lib, ops, 2, 64)
+    assert np.array_equal(P.numpy().reshape(2, 32, 64).astype(np.float64), P_ref)
+    assert np.array_equal(out.numpy().reshape(32, 64).astype(np.float64), O_ref)
+
+
+def test_closed_forms(lib):
+    sk = lib
+    ops, *_ = oracle_case(64, 128, 160, 3, 64, "bf16", "ones")
+    _, _, P, out = run_two_pass(sk, ops, 3, 64)
+    P = P.numpy().reshape(3, 64, 128)
+    assert np.all(P[0] == 64) and np.all(P[1] == 64) and np.all(P[2] == 32)
+    assert np.all(out.numpy() == 160)
+    ops, *_ = oracle_case(64, 128, 256, 2, 128, "f16", "identity_b", 4)
+    _, _, P, out = run_two_pass(sk, ops, 2, 128)
+    a = ops.A.view(np.float16).astype(np.float32)
+    assert np.array_equal(out.numpy().reshape(64, 128), a[:, :128])
+
+
+def test_zero_first_row_and_split_independence(lib):
+    sk = lib
+    outs = []
+    for S in (1, 2, 4, 8, 16):
+        ops, Pr, SP, Or, SO = oracle_case(96, 512, 512, S, 512 // S, "bf16")
+        _, _, P, out = run_two_pass(sk, ops, S, 512 // S)
+        o = out.numpy().reshape(96, 512)
+        assert np.all(o[0] == 0) and np.all(P.numpy().reshape(S, 96, 512)[:, 0] == 0)
+        outs.append(o.astype(np.float64))
+    for o in outs[1:]:
+        assert max_scaled_error(o, outs[0], SO) <= 2 * TOL_FINAL["bf16"]
+        assert max_scaled_error(o, outs[0], SO) <= 1e-5   # F32 accumulation, much tighter in practice
+
+
+TILINGS = [(bn, ch) for bn in (64, 128, 256) for ch in (1, 2, 4, 8)]
+
+
+@pytest.mark.parametrize("case", [(64, 128, 160, 3, 64, "bf16"), (256, 1024, 2048, 2, 1024, "bf16"),
+                                  (96, 512, 2048, 4, 512, "f16")], ids=["K160", "headline", "M96"])
+def test_every_tiling(lib, case):
+    """Each tile width and chunk count (including chunks past a short final
+    split, which hold no K at all) gives a correct result, and the fused path
+    matches the two-kernel path bitwise under the same tiling."""
+    sk = lib
+    M, N, K, S, kps, dt = case
+    ops, Pr, SP, Or, SO = oracle_case(M, N, K, S, kps, dt)
+    A = device_operand(ops.A, dt)
+    B = device_operand(ops.B, dt)
+    try:
+        for bn, ch in TILINGS:
+            sk.splitk_set_tile_override(bn, ch)
+            P = Guarded(S * M * N)
+            out = Guarded(M * N)
+            fused = Guarded(M * N)
+            sk.gemm_splitk_bt(A, B, P.data, M, N, K, S, kps, dt)
+            sk.splitk_reduce(P.data, out.data, S, M, N)
+            sk.gemm_bt(A, B, fused.data, None, 0, M, N, K, S, kps, dt, fused=1)
+            assert sk.splitk_get_device_status() == 0
+            assert P.guards_intact() and out.guards_intact() and fused.guards_intact()
+            assert max_scaled_error(P.numpy().reshape(S, M, N), Pr, SP) <= TOL_PARTIAL, (bn, ch)
+            assert max_scaled_error(out.numpy().reshape(M, N), Or, SO) <= TOL_FINAL[dt], (bn, ch)
+            assert np.array_equal(fused.numpy().view(np.uint32), out.numpy().view(np.uint32)), (bn, ch)
+    finally:
+        sk.splitk_set_tile_override(0, 0)
+
+
+def test_cuda_graph_capture_and_side_stream(lib):
+    sk = lib
+    M, N, K, S, kps, dt = 256, 1024, 2048, 2, 1024, "bf16"
+    ops, Pr, SP, Or, SO = oracle_case(M, N, K, S, kps, dt)
+    A = device_operand(ops.A, dt)
+    B = device_operand(ops.B, dt)
+    nbytes = sk.gemm_bt_workspace_bytes(M, N, K, S, kps)
+    ws = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+    outs = [torch.full((M, N), 7.0, device="cuda") for _ in range(2)]
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        sk.gemm_bt(A, B, outs[0], ws, nbytes, M, N, K, S, kps, dt, fused=0)
+        sk.gemm_bt(A, B, outs[1], None, 0, M, N, K, S, kps, dt, fused=1)
+    for _ in range(3):
+        outs[0].fill_(7.0)
+        outs[1].fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        for o in outs:
+            assert max_scaled_error(o.cpu().numpy(), Or, SO) <= TOL_FINAL[dt]
+        assert torch.equal(outs[0], outs[1])
+    assert sk.splitk_get_device_status() == 0
+
+
+def test_bounded_wait_reports_and_context_survives(lib):
+    sk = lib
+    from split_bf16_gemm_gb300 import binding as bd
+
+    assert sk.splitk_get_device_status() == 0
+    assert sk.splitk_selftest_bounded_wait(2_000_000) == bd.ERR_DEVICE_TIMEOUT
+    assert sk.splitk_get_device_status() == 0          # read-and-clear
+    check_case(sk, (32, 64, 128, 2, 64, "bf16"))        # the context is still usable

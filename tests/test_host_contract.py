@@ -1,0 +1,201 @@
+"""Host-side tests of libsplitk (no GPU): the library loads, exports every
+function include/splitk.h declares, and its validation agrees with the oracle's
+statement of the pages' contract.  Every call here fails validation before any
+CUDA call, so nothing touches a device (fake pointers are never dereferenced).
+"""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import split_bf16_gemm_gb300 as sk
+from split_bf16_gemm_gb300 import binding as bd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "splitk.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    sk.build()
+    return sk.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(bd.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_library_symbols_are_c_abi(L):
+    # nm -D lists the dynamic symbols; C linkage means unmangled names
+    import subprocess
+
+    out = subprocess.run(["nm", "-D", "--defined-only", sk.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in syms, name
+
+
+def test_geometry_matches_oracle_contract(L, orc):
+    """libsplitk's contract decision == the oracle's, bit for bit, over a grid."""
+    code = {0: 0, 1: bd.ERR_SHAPE, 2: bd.ERR_SPLIT}
+    for M in (-32, 0, 16, 32, 48, 96, 128, 256):
+        for N in (0, 32, 64, 96, 128, 512):
+            for K in (0, 32, 64, 96, 160, 2048):
+                for kps in (0, 16, 32, 64, 96, 512, 4096):
+                    for S in (0, 1, 2, 3, 4, 5, 16, 64):
+                        want = code[orc.contract(M, N, K, S, kps)]
+                        assert sk.splitk_check_geometry(M, N, K, S, kps) == want, (M, N, K, S, kps)
+
+
+def test_geometry_pages_cases(L):
+    with open(os.path.join(ROOT, "tests", "golden", "pages_contract.json")) as f:
+        cases = json.load(f)["contract_cases"]["cases"]
+    code = {0: 0, 1: bd.ERR_SHAPE, 2: bd.ERR_SPLIT}
+    for M, N, K, S, kps, expect in cases:
+        assert sk.splitk_check_geometry(M, N, K, S, kps) == code[expect]
+
+
+def test_implementation_limits(L):
+    big = (1 << 22) + 32
+    assert sk.splitk_check_geometry(big, 64, 64, 1, 64) == bd.ERR_SHAPE
+    assert sk.splitk_check_geometry(32, (1 << 22) + 64, 64, 1, 64) == bd.ERR_SHAPE
+    assert sk.splitk_check_geometry(32, 64, 32 * 5000, 5000, 32) == bd.ERR_SPLIT
+
+
+# fake device addresses: validation rejects every call below before any CUDA call
+A0, B0, P0, O0, W0 = 0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000
+GOOD = dict(M=32, N=64, K=128, S=2, kps=64)
+
+
+def call_gemm(L, A=A0, B=B0, P=P0, M=32, N=64, K=128, S=2, kps=64, dtype=bd.BF16):
+    return L.gemm_splitk_bt(A, B, P, M, N, K, S, kps, dtype, None)
+
+
+def test_gemm_rejections(L):
+    assert call_gemm(L, M=48) == bd.ERR_SHAPE
+    assert call_gemm(L, N=32) == bd.ERR_SHAPE
+    assert call_gemm(L, S=3) == bd.ERR_SPLIT
+    assert call_gemm(L, dtype=7) == bd.ERR_DTYPE
+    assert call_gemm(L, A=0) == bd.ERR_NULL
+    assert call_gemm(L, B=0) == bd.ERR_NULL
+    assert call_gemm(L, P=0) == bd.ERR_NULL
+    assert call_gemm(L, A=A0 + 8) == bd.ERR_ALIGN
+    assert call_gemm(L, P=P0 + 4) == bd.ERR_ALIGN
+    # partials [2,32,64] F32 = 16 KiB; A [32,128] BF16 = 8 KiB
+    assert call_gemm(L, P=A0) == bd.ERR_ALIAS
+    assert call_gemm(L, P=A0 + 8192 - 16) == bd.ERR_ALIAS
+    assert call_gemm(L, P=B0 - 16384 + 16) == bd.ERR_ALIAS
+    # the shape rule is reported before pointer problems
+    assert call_gemm(L, M=48, A=0) == bd.ERR_SHAPE
+
+
+def test_reduce_rejections(L):
+    assert L.splitk_reduce(P0, O0, 2, 0, 64, None) == bd.ERR_SHAPE
+    assert L.splitk_reduce(P0, O0, 0, 32, 64, None) == bd.ERR_SPLIT
+    assert L.splitk_reduce(0, O0, 2, 32, 64, None) == bd.ERR_NULL
+    assert L.splitk_reduce(P0, 0, 2, 32, 64, None) == bd.ERR_NULL
+    assert L.splitk_reduce(P0 + 4, O0, 2, 32, 64, None) == bd.ERR_ALIGN
+    assert L.splitk_reduce(P0, P0 + 16384 - 16, 2, 32, 64, None) == bd.ERR_ALIAS
+
+
+def test_gemm_bt_rejections(L):
+    need = sk.gemm_bt_workspace_bytes(32, 64, 128, 2, 64)
+    assert need == 2 * 32 * 64 * 4
+
+    def call(out=O0, ws=W0, wsb=need, fused=0, **kw):
+        g = dict(GOOD, **kw)
+        return L.gemm_bt(A0, B0, out, ws, wsb, g["M"], g["N"], g["K"], g["S"], g["kps"], bd.BF16,
+                         fused, None)
+
+    assert call(M=96, K=100) == bd.ERR_SHAPE
+    assert call(fused=2) == bd.ERR_CONFIG
+    assert call(out=0) == bd.ERR_NULL
+    assert call(ws=0) == bd.ERR_NULL
+    assert call(wsb=need - 4) == bd.ERR_WORKSPACE
+    assert call(ws=W0 + 8) == bd.ERR_ALIGN
+    assert call(out=A0) == bd.ERR_ALIAS
+    assert call(ws=O0) == bd.ERR_ALIAS
+    assert call(ws=B0 + 64) == bd.ERR_ALIAS
+    # fused=3 also keeps the partials, so it needs the workspace too
+    assert call(ws=0, fused=3) == bd.ERR_NULL
+    assert call(wsb=0, fused=3) == bd.ERR_WORKSPACE
+
+
+def test_workspace_bytes(L):
+    assert sk.gemm_bt_workspace_bytes(256, 1024, 2048, 2, 1024) == 2 * 256 * 1024 * 4
+    assert sk.gemm_bt_workspace_bytes(64, 128, 160, 3, 64) == 3 * 64 * 128 * 4
+    assert sk.gemm_bt_workspace_bytes(64, 128, 160, 2, 64) == 0
+
+
+def test_status_strings(L):
+    for code in range(-10, 1):
+        assert sk.splitk_status_string(code) != "unknown status"
+    assert sk.splitk_status_string(-99) == "unknown status"
+
+
+def test_tile_override_validation(L):
+    for bn, ch in [(32, 0), (0, 3), (512, 1), (64, 32)]:
+        with pytest.raises(sk.SplitKError):
+            sk.splitk_set_tile_override(bn, ch)
+    sk.splitk_set_tile_override(0, 0)
+
+
+def test_describe_launch_plans(L):
+    sk.splitk_set_tile_override(0, 0)
+    d = sk.splitk_describe_launch(256, 1024, 2048, 2, 1024, "bf16", fused=0)
+    assert d["path"] == 0 and d["kernels_per_call"] == 2
+    assert d["grid_x"] * d["bn"] == 1024 and d["grid_y"] == 2
+    assert d["grid_z"] == 2 * d["chunks"] and d["cluster"] == d["chunks"]
+    assert d["chunk_len"] * d["chunks"] >= 1024 and d["chunk_len"] % 32 == 0
+    assert d["smem_bytes"] <= 227 * 1024
+    f = sk.splitk_describe_launch(256, 1024, 2048, 2, 1024, "bf16", fused=1)
+    assert f["fused_in_kernel"] == 1 and f["kernels_per_call"] == 1
+    assert f["cluster"] == 2 * f["chunks"] <= 16
+    # same chunking in both modes: the fused output equals the two-kernel output bitwise
+    assert (f["bn"], f["chunks"], f["chunk_len"]) == (d["bn"], d["chunks"], d["chunk_len"])
+    # F32 runs the FMA path, two kernels even when fused is asked for
+    g = sk.splitk_describe_launch(96, 512, 2048, 4, 512, "f32", fused=1)
+    assert g["path"] == 1 and g["kernels_per_call"] == 2
+    # more than 16 splits: no single cluster holds them, two kernels
+    h = sk.splitk_describe_launch(32, 64, 32 * 32, 32, 32, "bf16", fused=1)
+    assert h["fused_in_kernel"] == 0 and h["kernels_per_call"] == 2
+    for S in (1, 2, 4, 8, 16):
+        e = sk.splitk_describe_launch(32, 512, 2048, S, 2048 // S, "f16", fused=1)
+        assert e["cluster"] == S * e["chunks"] <= 16
+
+
+def test_describe_launch_override(L):
+    try:
+        sk.splitk_set_tile_override(64, 2)
+        d = sk.splitk_describe_launch(64, 128, 160, 3, 64, "bf16")
+        assert d["bn"] == 64 and d["chunks"] == 2 and d["chunk_len"] == 32
+        # a width that does not divide N keeps the automatic width
+        sk.splitk_set_tile_override(256, 1)
+        d = sk.splitk_describe_launch(64, 128, 160, 3, 64, "bf16")
+        assert d["bn"] in (64, 128)
+    finally:
+        sk.splitk_set_tile_override(0, 0)
+
+
+def test_unbuilt_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(bd, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(bd, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        bd.lib()
