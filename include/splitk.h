@@ -101,23 +101,31 @@ int gemm_splitk_bt(const void *A, const void *B, float *partials, int64_t M,
 int splitk_reduce(const float *partials, float *out, int64_t splits, int64_t M,
                   int64_t N, void *stream);
 
-/* Bytes of device workspace gemm_bt needs: room for the F32 partials
- * [splits,M,N].  Returns 0 for a geometry that breaks the contract. */
+/* Bytes of device workspace gemm_bt needs: the F32 partials [splits,M,N]
+ * (the first splits*M*N*4 bytes) followed by the fused path's arrival
+ * counters.  The same size serves both values of `fused`.  Returns 0 for a
+ * geometry that breaks the contract. */
 size_t gemm_bt_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t splits,
                                int64_t k_per_split, int fused);
+
+/* Zeroes a workspace (cudaMemsetAsync on `stream`).  A workspace must be
+ * zeroed once before its first fused gemm_bt call; every fused call leaves
+ * its counters zero again, so later calls need no re-initialisation (unless
+ * a launch reported SPLITK_ERR_DEVICE_TIMEOUT). */
+int gemm_bt_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
 
 /* One call: the partial pass then the accumulation pass, on one stream.
  *   out        device, [M,N] F32; fully overwritten
  *   workspace  device, >= gemm_bt_workspace_bytes() bytes, caller-owned
- *              scratch; may not overlap A, B or out
- *   fused      0: two kernels (gemm_splitk_bt, then splitk_reduce), the
- *                 partials left in the workspace;
- *              1: one kernel whose thread-block cluster also sums the splits
- *                 (tensor-core types, splits <= 16); the workspace is left
- *                 untouched; with F32 operands or more than 16 splits the
- *                 two-kernel path runs instead;
- *              3: as 1, and the partials are also written to the workspace.
- * For a given shape, `out` is bitwise the same for every `fused` value. */
+ *              scratch; may not overlap A, B or out.  After the call it holds
+ *              the partials [splits,M,N] in its first bytes.
+ *   fused      0: two kernels (gemm_splitk_bt, then splitk_reduce);
+ *              1: one kernel: the last split to finish each piece of a tile
+ *                 adds the splits in split order and writes `out`; needs the
+ *                 workspace zeroed once (gemm_bt_workspace_init).  With F32
+ *                 operands the two-kernel path runs instead.
+ * For a given shape, `out` and the partials are bitwise the same for both
+ * values of `fused`. */
 int gemm_bt(const void *A, const void *B, float *out, void *workspace,
             size_t workspace_bytes, int64_t M, int64_t N, int64_t K,
             int64_t splits, int64_t k_per_split, int dtype, int fused,
@@ -129,20 +137,25 @@ int gemm_bt(const void *A, const void *B, float *out, void *workspace,
  * valid) or SPLITK_ERR_CUDA. */
 int splitk_get_device_status(void *stream);
 
+/* What the most recent SPLITK_ERR_CUDA on the calling host thread came from:
+ * the failing call and CUDA's name and description of its error.  The string
+ * is owned by the library and stays valid until the thread's next failure. */
+const char *splitk_last_error(void);
+
 /* A short, static description of a status code. */
 const char *splitk_status_string(int status);
 
 /* Tile-shape override for tuning: every later tensor-core launch uses tile
  * width `bn` (64, 128 or 256; must divide N, else the automatic choice is
- * kept) and `chunks` thread blocks per split along K (1, 2, 4, 8 or 16),
- * where that is legal for the shape.  bn = chunks = 0 restores the automatic
+ * kept) and `chunks` thread blocks per split along K (1, 2, 4 or 8; fewer
+ * when the shared memory of that many does not fit).  bn = chunks = 0 restores the automatic
  * choice.  Process-wide; not thread-safe against concurrent launches.
  * Returns SPLITK_OK or SPLITK_ERR_CONFIG. */
 int splitk_set_tile_override(int bn, int chunks);
 
 /* Describes the launch gemm_bt would make, without launching: info[0..11] =
  * {path (0 tensor-core, 1 F32 FMA), bn, chunks, chunk_len, stages,
- *  cluster_size, grid_x, grid_y, grid_z, dynamic_smem_bytes,
+ *  cluster_size (== chunks), grid_x, grid_y, grid_z, dynamic_smem_bytes,
  *  fused_in_kernel (0/1), kernels_per_call}.  Returns a status as gemm_bt's
  * validation would (pointers are not checked). */
 int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits,

@@ -24,7 +24,8 @@ ERR_DTYPE, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_CONFIG = -6, -7, -8,
 EXPORTS = (
     "splitk_check_geometry", "gemm_splitk_bt", "splitk_reduce", "gemm_bt_workspace_bytes",
     "gemm_bt", "splitk_get_device_status", "splitk_status_string", "splitk_set_tile_override",
-    "splitk_describe_launch", "splitk_selftest_bounded_wait",
+    "splitk_describe_launch", "splitk_selftest_bounded_wait", "splitk_last_error",
+    "gemm_bt_workspace_init",
 )
 
 _lock = threading.Lock()
@@ -34,7 +35,10 @@ _lib = None
 class SplitKError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: status {status} ({status_string(status)})")
+        msg = f"{where}: status {status} ({status_string(status)})"
+        if status == ERR_CUDA:
+            msg += ": " + last_error()
+        super().__init__(msg)
 
 
 def lib() -> ctypes.CDLL:
@@ -59,7 +63,11 @@ def lib() -> ctypes.CDLL:
             L.splitk_set_tile_override.argtypes = [i32, i32]
             L.splitk_describe_launch.argtypes = [i64, i64, i64, i64, i64, i32, i32, vp]
             L.splitk_selftest_bounded_wait.argtypes = [i64, vp]
+            L.gemm_bt_workspace_init.argtypes = [vp, sz, vp]
+            L.splitk_last_error.argtypes = []
+            L.splitk_last_error.restype = ctypes.c_char_p
             for name in ("splitk_check_geometry", "gemm_splitk_bt", "splitk_reduce", "gemm_bt",
+                         "gemm_bt_workspace_init",
                          "splitk_get_device_status", "splitk_set_tile_override",
                          "splitk_describe_launch", "splitk_selftest_bounded_wait"):
                 getattr(L, name).restype = i32
@@ -108,6 +116,14 @@ def status_string(status: int) -> str:
 splitk_status_string = status_string
 
 
+def last_error() -> str:
+    """The failing CUDA call behind the calling thread's latest ERR_CUDA."""
+    return lib().splitk_last_error().decode()
+
+
+splitk_last_error = last_error
+
+
 def splitk_check_geometry(M, N, K, splits, k_per_split) -> int:
     """Contract status of a geometry (0 legal, ERR_SHAPE or ERR_SPLIT); never raises."""
     return lib().splitk_check_geometry(M, N, K, splits, k_per_split)
@@ -125,6 +141,11 @@ def splitk_reduce(partials, out, splits, M, N, stream=None) -> None:
 
 def gemm_bt_workspace_bytes(M, N, K, splits, k_per_split, fused=0) -> int:
     return int(lib().gemm_bt_workspace_bytes(M, N, K, splits, k_per_split, fused))
+
+
+def gemm_bt_workspace_init(workspace, workspace_bytes, stream=None) -> None:
+    _check(lib().gemm_bt_workspace_init(_ptr(workspace), workspace_bytes, _stream(stream)),
+           "gemm_bt_workspace_init")
 
 
 def gemm_bt(A, B, out, workspace, workspace_bytes, M, N, K, splits, k_per_split, dtype, fused=0,

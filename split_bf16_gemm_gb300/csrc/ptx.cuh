@@ -43,6 +43,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
@@ -220,6 +225,12 @@ __device__ __forceinline__ void cluster_arrive()
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
+// Arrival that publishes nothing: only says "this CTA has reached here".
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_wait()
 {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -241,6 +252,28 @@ __device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr)
                  : "r"(addr)
                  : "memory");
     return v;
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to a
+// shared-memory address of a CTA in the cluster; completion is counted in
+// bytes on that CTA's mbarrier (`bar`, a cluster address).
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "r"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// 16-byte store into the shared memory of a CTA in the cluster (`dst`, a
+// cluster address); its bytes count toward that CTA's mbarrier `bar`.
+__device__ __forceinline__ void st_async_v4(uint32_t dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     dst),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
+                 : "memory");
 }
 
 __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr)

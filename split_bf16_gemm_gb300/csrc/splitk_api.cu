@@ -10,9 +10,33 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdio>
 
-#include "../../include/splitk.h"
+#include "splitk.h"
 #include "splitk_internal.h"
+
+namespace splitk {
+
+namespace {
+thread_local char g_last_error[256] = "no error";
+}
+
+cudaError_t note_error(cudaError_t e, const char *what)
+{
+    if (e != cudaSuccess)
+        std::snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", what, cudaGetErrorName(e),
+                      cudaGetErrorString(e));
+    return e;
+}
+
+void note_message(const char *what, int code)
+{
+    std::snprintf(g_last_error, sizeof g_last_error, "%s (code %d)", what, code);
+}
+
+const char *last_error_message() { return g_last_error; }
+
+}  // namespace splitk
 
 namespace {
 
@@ -70,19 +94,26 @@ int validate_gemm(const void *A, const void *B, int64_t M, int64_t N, int64_t K,
 }
 
 // The partial pass into P (and, when `out` is given, the split sum too).
-int run_partial_pass(const void *A, const void *B, float *P, float *out, int64_t M, int64_t N, int64_t K, int64_t S,
-                     int64_t kps, int dtype, bool fused, cudaStream_t stream)
+int run_partial_pass(const void *A, const void *B, float *P, float *out, unsigned *counters, int64_t M, int64_t N,
+                     int64_t K, int64_t S, int64_t kps, int dtype, bool fused, cudaStream_t stream)
 {
     if (dtype == SPLITK_F32) {
         return cuda_status(splitk::launch_simt_f32(static_cast<const float *>(A), static_cast<const float *>(B), P,
                                                    M, N, K, S, kps, stream));
     }
-    GemmProblem pr{A, B, P, out, M, N, K, S, kps, dtype == SPLITK_BF16};
+    GemmProblem pr{A, B, P, out, counters, M, N, K, S, kps, dtype == SPLITK_BF16};
     const TilePlan plan = splitk::plan_tc(M, N, K, S, kps, fused);
     return cuda_status(splitk::launch_tc(pr, plan, stream));
 }
 
-bool fused_possible(int dtype, int64_t S) { return dtype != SPLITK_F32 && S <= 16; }
+bool fused_possible(int dtype) { return dtype != SPLITK_F32; }
+
+size_t partials_bytes(int64_t M, int64_t N, int64_t S) { return static_cast<size_t>(S * M * N) * 4; }
+
+size_t counter_bytes(int64_t M, int64_t N)
+{
+    return (static_cast<size_t>(splitk::fused_counter_count(M, N)) * 4 + 15) / 16 * 16;
+}
 
 }  // namespace
 
@@ -105,7 +136,7 @@ int gemm_splitk_bt(const void *A, const void *B, float *partials, int64_t M, int
     const Range rb = range_of(B, static_cast<uint64_t>(N * K) * e);
     const Range rp = range_of(partials, static_cast<uint64_t>(splits * M * N) * 4);
     if (overlap(rp, ra) || overlap(rp, rb)) return SPLITK_ERR_ALIAS;
-    return run_partial_pass(A, B, partials, nullptr, M, N, K, splits, k_per_split, dtype, false,
+    return run_partial_pass(A, B, partials, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false,
                             static_cast<cudaStream_t>(stream));
 }
 
@@ -125,7 +156,15 @@ size_t gemm_bt_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t splits, 
 {
     (void)fused;
     if (geometry_status(M, N, K, splits, k_per_split) != SPLITK_OK) return 0;
-    return static_cast<size_t>(splits * M * N) * 4;
+    return partials_bytes(M, N, splits) + counter_bytes(M, N);
+}
+
+int gemm_bt_workspace_init(void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!workspace) return SPLITK_ERR_NULL;
+    if (!aligned16(workspace)) return SPLITK_ERR_ALIGN;
+    return cuda_status(splitk::note_error(
+        cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)), "cudaMemsetAsync(workspace)"));
 }
 
 int gemm_bt(const void *A, const void *B, float *out, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
@@ -133,40 +172,38 @@ int gemm_bt(const void *A, const void *B, float *out, void *workspace, size_t wo
 {
     int st = validate_gemm(A, B, M, N, K, splits, k_per_split, dtype);
     if (st != SPLITK_OK) return st;
-    if (fused != 0 && fused != 1 && fused != 3) return SPLITK_ERR_CONFIG;
-    if (!out) return SPLITK_ERR_NULL;
-    if (!aligned16(out)) return SPLITK_ERR_ALIGN;
-    const bool in_kernel = fused != 0 && fused_possible(dtype, splits);
-    const bool need_ws = !in_kernel || fused == 3;
+    if (fused != 0 && fused != 1) return SPLITK_ERR_CONFIG;
+    if (!out || !workspace) return SPLITK_ERR_NULL;
+    if (!aligned16(out) || !aligned16(workspace)) return SPLITK_ERR_ALIGN;
     const size_t ws_need = gemm_bt_workspace_bytes(M, N, K, splits, k_per_split, fused);
-    if (need_ws) {
-        if (!workspace) return SPLITK_ERR_NULL;
-        if (!aligned16(workspace)) return SPLITK_ERR_ALIGN;
-        if (workspace_bytes < ws_need) return SPLITK_ERR_WORKSPACE;
-    }
+    if (workspace_bytes < ws_need) return SPLITK_ERR_WORKSPACE;
     const int e = elem_bytes(dtype);
     const Range ra = range_of(A, static_cast<uint64_t>(M * K) * e);
     const Range rb = range_of(B, static_cast<uint64_t>(N * K) * e);
     const Range ro = range_of(out, static_cast<uint64_t>(M * N) * 4);
-    if (overlap(ro, ra) || overlap(ro, rb)) return SPLITK_ERR_ALIAS;
-    if (need_ws) {
-        const Range rw = range_of(workspace, ws_need);
-        if (overlap(rw, ra) || overlap(rw, rb) || overlap(rw, ro)) return SPLITK_ERR_ALIAS;
-    }
+    const Range rw = range_of(workspace, ws_need);
+    if (overlap(ro, ra) || overlap(ro, rb) || overlap(rw, ra) || overlap(rw, rb) || overlap(rw, ro))
+        return SPLITK_ERR_ALIAS;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float *P = static_cast<float *>(workspace);
-    if (in_kernel)
-        return run_partial_pass(A, B, fused == 3 ? P : nullptr, out, M, N, K, splits, k_per_split, dtype, true, s);
-    st = run_partial_pass(A, B, P, nullptr, M, N, K, splits, k_per_split, dtype, false, s);
+    unsigned *counters = reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + partials_bytes(M, N, splits));
+    if (fused && fused_possible(dtype))
+        return run_partial_pass(A, B, P, out, counters, M, N, K, splits, k_per_split, dtype, true, s);
+    st = run_partial_pass(A, B, P, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false, s);
     if (st != SPLITK_OK) return st;
     return cuda_status(splitk::launch_reduce(P, out, splits, M * N, s));
 }
 
+const char *splitk_last_error(void) { return splitk::last_error_message(); }
+
 int splitk_get_device_status(void *stream)
 {
     unsigned status = 0;
-    if (splitk::read_and_clear_device_status(static_cast<cudaStream_t>(stream), &status) != cudaSuccess)
+    const cudaError_t e = splitk::read_and_clear_device_status(static_cast<cudaStream_t>(stream), &status);
+    if (e != cudaSuccess) {
+        splitk::note_error(e, "reading the device status word");
         return SPLITK_ERR_CUDA;
+    }
     return status ? SPLITK_ERR_DEVICE_TIMEOUT : SPLITK_OK;
 }
 
@@ -191,7 +228,7 @@ const char *splitk_status_string(int status)
 int splitk_set_tile_override(int bn, int chunks)
 {
     if (bn != 0 && bn != 64 && bn != 128 && bn != 256) return SPLITK_ERR_CONFIG;
-    if (chunks != 0 && chunks != 1 && chunks != 2 && chunks != 4 && chunks != 8 && chunks != 16)
+    if (chunks != 0 && chunks != 1 && chunks != 2 && chunks != 4 && chunks != 8)
         return SPLITK_ERR_CONFIG;
     splitk::set_tile_override(bn, chunks);
     return SPLITK_OK;
@@ -217,7 +254,7 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
         info[11] = 2;
         return SPLITK_OK;
     }
-    const bool in_kernel = fused != 0 && fused_possible(dtype, splits);
+    const bool in_kernel = fused != 0 && fused_possible(dtype);
     const TilePlan p = splitk::plan_tc(M, N, K, splits, k_per_split, in_kernel);
     info[0] = 0;
     info[1] = p.bn;

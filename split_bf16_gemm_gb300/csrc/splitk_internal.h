@@ -14,21 +14,24 @@ struct GemmProblem {
     const void *B;      // [N,K] row-major, 16-bit elements
     float *P;           // [S,M,N] partials, or nullptr when not written
     float *out;         // [M,N] sum over splits, or nullptr (two-kernel path)
+    unsigned *counters; // fused: per (tile, cluster rank) arrival counters, zero between calls
     int64_t M, N, K, S, kps;
     bool bf16;          // operand type: BF16 (true) or F16 (false)
 };
 
 // How it is tiled.  One CTA computes a 128 x bn tile of one K-chunk of one
-// split; `chunks` CTAs share a split, and a thread-block cluster of `cluster`
-// CTAs (chunks, or splits*chunks when the kernel also sums the splits) adds
-// their accumulators through distributed shared memory.
+// split; the `chunks` CTAs of a split form a thread-block cluster and add
+// their accumulators through distributed shared memory, each rank owning
+// `share` 16-byte pieces of the tile.
 struct TilePlan {
     int bn;             // tile width: 64, 128 or 256
     int chunks;         // CTAs per split along K
     int chunk_len;      // K elements per chunk (multiple of 32)
     int stages;         // shared-memory pipeline depth
-    int cluster;        // CTAs per cluster along grid z
-    int fused;          // the cluster also sums over splits
+    int cluster;        // CTAs per cluster along grid z (== chunks)
+    int fused;          // the last split to finish a piece also sums over splits
+    int share;          // 16-byte pieces of the tile each cluster rank owns
+    uint32_t region0;   // bytes of the stage ring / accumulator staging
     dim3 grid;
     size_t smem_bytes;  // dynamic shared memory per CTA
 };
@@ -36,6 +39,11 @@ struct TilePlan {
 constexpr int kTileM = 128;   // rows per CTA tile (tcgen05 M)
 constexpr int kBlockK = 64;   // K elements per pipeline stage: one 128-byte swizzle row
 constexpr int kMaxStages = 8;
+constexpr int kMaxChunks = 8;  // portable cluster size
+
+// Arrival counters the fused path needs in the workspace, after the partials:
+// one per (128 x 64 tile column block, row block, chunk), the most any plan uses.
+inline int64_t fused_counter_count(int64_t M, int64_t N) { return (N / 64) * ((M + kTileM - 1) / kTileM) * kMaxChunks; }
 
 // Tile choice for a shape (automatic, or the process-wide override).
 TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused);
@@ -46,6 +54,12 @@ cudaError_t launch_tc(const GemmProblem &p, const TilePlan &plan, cudaStream_t s
 cudaError_t launch_simt_f32(const float *A, const float *B, float *P, int64_t M, int64_t N, int64_t K,
                             int64_t S, int64_t kps, cudaStream_t stream);
 cudaError_t launch_reduce(const float *P, float *out, int64_t S, int64_t count, cudaStream_t stream);
+
+// Last-error record (per host thread): what failed and the CUDA error or
+// driver result it returned.  note_error passes `e` through.
+cudaError_t note_error(cudaError_t e, const char *what);
+void note_message(const char *what, int code);
+const char *last_error_message();
 
 // Device status word (set by kernels whose bounded waits ran out).
 cudaError_t read_and_clear_device_status(cudaStream_t stream, unsigned *status);

@@ -86,7 +86,7 @@ cudaError_t launch_reduce(const float *P, float *out, int64_t S, int64_t count, 
     else
         reduce_scalar_kernel<<<static_cast<unsigned>(blocks), kReduceThreads, 0, stream>>>(P, out, static_cast<int>(S),
                                                                                            items);
-    return cudaGetLastError();
+    return note_error(cudaGetLastError(), "reduce kernel launch");
 }
 
 }  // namespace splitk

@@ -76,7 +76,7 @@ cudaError_t launch_simt_f32(const float *A, const float *B, float *P, int64_t M,
     dim3 grid(static_cast<unsigned>(N / kT), static_cast<unsigned>((M + kT - 1) / kT), static_cast<unsigned>(S));
     simt_f32_kernel<<<grid, kSimtThreads, 0, stream>>>(A, B, P, static_cast<int>(M), static_cast<int>(N),
                                                       static_cast<int>(K), static_cast<int>(kps));
-    return cudaGetLastError();
+    return note_error(cudaGetLastError(), "F32 FMA kernel launch");
 }
 
 }  // namespace splitk

@@ -7,24 +7,36 @@
 // "Launch contract and correctness").  Optionally the same launch also sums
 // the splits into out[m,n] (the pages' separate accumulation pass, fused).
 //
-// One CTA (128 threads, 4 warps) owns a 128 x BN output tile of one K-chunk:
-//   warp 0 lane 0  TMA producer: 128x64 A box + BNx64 B box per stage, both
-//                  128-byte swizzled, into a ring of `stages` buffers;
+// One CTA (256 threads, 8 warps) owns a 128 x BN output tile of one K-chunk:
+//   thread 0       TMA producer: 128x64 A box + BNx64 B box per stage, both
+//                  128-byte swizzled, into a ring of `stages` buffers; the
+//                  first `stages` loads go out before tensor memory is even
+//                  allocated;
 //   warp 1 lane 0  MMA issuer: 4 x tcgen05.mma (M=128, N=BN, K=16) per stage,
 //                  accumulating in tensor memory (BN 32-bit columns);
-//   all 4 warps    epilogue: tensor memory -> registers -> shared memory
-//                  (swizzled 32x32 float boxes), then the tile's F32 sums are
-//                  formed and stored with coalesced 16-byte stores.
-// A split's K range is cut into `chunks` CTAs; they form a thread-block
-// cluster and add their accumulators through distributed shared memory in
-// chunk order 0,1,2,..., so the result does not depend on which CTA finishes
-// first.  In fused mode the cluster holds every split of the tile and the
-// owner of each 16-byte piece also adds the split sums in split order, which
-// is exactly what the separate reduce kernel does with the same partials.
+//   all 8 warps    epilogue: tensor memory -> registers -> shared memory
+//                  (swizzled 32x32 float boxes, reusing the stage ring).
+// A split's K range is cut into `chunks` CTAs that form one thread-block
+// cluster.  Each cluster rank owns 1/chunks of the tile; every CTA pushes each
+// owner its share with one bulk shared-memory copy (cp.async.bulk into the
+// owner's shared memory, counted on the owner's mbarrier), and each owner adds
+// the chunks in chunk order 0,1,2,... from its own shared memory, so the sum
+// does not depend on arrival order.  Owners store their share of partials[s] with coalesced
+// 16-byte stores.
+// Fused mode: after storing its share of partials[s], the owner counts its
+// arrival on a per-(tile, rank) counter; the last of the `splits` owners of
+// that piece of the tile reads the other splits' partials back (L2) and adds
+// them in split order s = 0,1,..., exactly the separate reduce kernel's sums,
+// then stores out[m,n].  The counter wraps to zero, ready for the next call.
+//
+// Programmatic dependent launch: the kernel waits for the previous grid (whose
+// writes it may read) before its first load, and lets the next grid start its
+// own set-up as soon as every CTA has started.
 //
 // Every mbarrier wait has a time limit; on time-out the kernel records a bit
-// in g_device_status, drains its own loads in flight, frees its tensor memory
-// and finishes without touching the outputs' validity guarantees.
+// in g_device_status, drains its own loads in flight, still sends and awaits
+// every cluster message (so no peer waits on it), frees its tensor memory and
+// finishes; the outputs of that launch are then not valid.
 
 #include <cudaTypedefs.h>
 
@@ -41,15 +53,17 @@ __device__ unsigned g_device_status;
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s; a launch normally takes microseconds
-constexpr int kThreads = 128;
-constexpr int kMaxCluster = 16;
+constexpr int kThreads = 256;                     // 8 warps: two per tensor-memory lane quarter
+constexpr int kBatch = 8;                          // pieces per thread per pass of the split sum
 
 struct TcArgs {
-    float *P;
-    float *out;
+    float *P;              // [S,M,N] partials
+    float *out;            // [M,N], or nullptr when the splits are not summed here
+    unsigned *counters;    // per (tile, cluster rank) arrival counters when out != nullptr
     int M, N, K, S, kps;
-    int chunks, chunk_len, stages, cluster;
-    int fused;
+    int chunks, chunk_len, stages;
+    int share;             // 16-byte pieces owned by each cluster rank (a multiple of 8)
+    uint32_t region0;      // bytes of the stage ring / accumulator staging area
     int bf16;
     uint64_t wait_limit_ns;
 };
@@ -63,49 +77,101 @@ struct TcShape {
     static constexpr int kPieces = kTileM * BN / 4;               // 16-byte pieces per tile
 };
 
-template <int BN>
+// Piece g of the staged tile: 4 consecutive F32 of one row.  Box b = g >> 8
+// covers rows 32*(b&3).., columns 32*(b>>2)..; inside it, row rb = (g>>3)&31
+// is 128 bytes at (g >> 3) * 128 and holds its 16-byte piece j = g & 7 at
+// position j ^ (rb & 7).
+struct Piece {
+    uint32_t off;   // byte offset in the staging area
+    int row, col;   // tile-relative
+};
+
+__device__ __forceinline__ Piece piece_at(int g)
+{
+    const int b = g >> 8, rb = (g >> 3) & 31, j = g & 7;
+    Piece p;
+    p.off = (static_cast<uint32_t>(g >> 3) << 7) | (static_cast<uint32_t>(j ^ (rb & 7)) << 4);
+    p.row = (b & 3) * 32 + rb;
+    p.col = (b >> 2) * 32 + j * 4;
+    return p;
+}
+
+__device__ __forceinline__ void add4(float4 &a, const float4 &b)
+{
+    a.x += b.x;
+    a.y += b.y;
+    a.z += b.z;
+    a.w += b.w;
+}
+
+template <int BN, int C>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const TcArgs args)
 {
     using Sh = TcShape<BN>;
     extern __shared__ uint8_t dsmem[];
-    __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 1];
+    __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 2];
     __shared__ uint32_t tmem_slot;
     __shared__ int issued_s, consumed_s;
-    __shared__ unsigned abort_s;
+    __shared__ unsigned abort_s, last_s;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int stages = args.stages;
-    const uint32_t base = (ptx::smem_addr(dsmem) + 1023u) & ~1023u;   // swizzle atoms are 1 KB
+    const uint32_t raw = ptx::smem_addr(dsmem);
+    const uint32_t base = (raw + 1023u) & ~1023u;   // swizzle atoms are 1 KB
+    uint8_t *const gbase = dsmem + (base - raw);    // generic pointer to the same place
+    const uint32_t E = base;                        // accumulator staging, over the ring
+    const uint32_t recv = base + args.region0;      // the peers' shares of this CTA's pieces
 
     const int n_tile = blockIdx.x, m_tile = blockIdx.y;
-    const int s = blockIdx.z / args.chunks;
-    const int c = blockIdx.z - s * args.chunks;
+    const int s = blockIdx.z / C;
+    const int c = blockIdx.z - s * C;               // == rank in the 1 x 1 x C cluster
     const int ks = s * args.kps;
-    const int ke = min(ks + args.kps, args.K);            // the last split clamps to K
+    const int ke = min(ks + args.kps, args.K);      // the last split clamps to K
     const int k_lo = ks + c * args.chunk_len;
     const int k_hi = min(k_lo + args.chunk_len, ke);
-    const int klen = k_hi > k_lo ? k_hi - k_lo : 0;       // a chunk past a short split is empty
+    const int klen = k_hi > k_lo ? k_hi - k_lo : 0; // a chunk past a short split is empty
     const int nkb = (klen + kBlockK - 1) / kBlockK;
+    const int share = args.share;
+    const int my_lo = min(Sh::kPieces, c * share);
+    const int my_hi = min(Sh::kPieces, my_lo + share);
 
     const uint32_t bar0 = ptx::smem_addr(&bars[0]);
     auto full_bar = [&](int i) { return bar0 + 8u * i; };
     auto empty_bar = [&](int i) { return bar0 + 8u * (kMaxStages + i); };
     const uint32_t acc_bar = bar0 + 8u * (2 * kMaxStages);
+    const uint32_t recv_bar = bar0 + 8u * (2 * kMaxStages + 1);
 
+    const int pre = min(stages, nkb);               // loads that need no free slot
     if (tid == 0) {
         for (int i = 0; i < stages; ++i) {
             ptx::mbar_init(full_bar(i), 1);
             ptx::mbar_init(empty_bar(i), 1);
         }
         ptx::mbar_init(acc_bar, 1);
+        ptx::mbar_init(recv_bar, 1);
         issued_s = 0;
         consumed_s = 0;
         abort_s = 0;
+        last_s = 0;
         ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+        const uint32_t incoming = static_cast<uint32_t>((C - 1) * (my_hi - my_lo)) * 16u;
+        if (incoming)
+            ptx::mbar_arrive_expect_tx(recv_bar, incoming);
+        else
+            ptx::mbar_arrive(recv_bar);
         ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB);
+        ptx::grid_dependency_wait();                // A and B may be the previous grid's output
+        for (int kb = 0; kb < pre; ++kb) {
+            const uint32_t sa = base + kb * Sh::kStageBytes;
+            const int kx = k_lo + kb * kBlockK;
+            ptx::mbar_arrive_expect_tx(full_bar(kb), Sh::kStageBytes);
+            ptx::tma_load_2d(sa, &tmA, full_bar(kb), kx, m_tile * kTileM, ptx::l2_policy_evict_last());
+            ptx::tma_load_2d(sa + Sh::kABytes, &tmB, full_bar(kb), kx, n_tile * BN, ptx::l2_policy_evict_normal());
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(&tmem_slot), Sh::kTmemCols);
@@ -114,13 +180,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
+    if (C > 1) ptx::cluster_arrive();               // publishes this CTA's barrier set-up to the cluster
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
     const uint32_t tmem = tmem_slot;
 
     if (warp == 0 && lane == 0) {
-        // ---- TMA producer
-        const uint64_t pol_a = ptx::l2_policy_evict_last();    // A is re-read by every N tile
-        const uint64_t pol_b = ptx::l2_policy_evict_normal();
-        int kb = 0;
+        // ---- TMA producer: the loads that had to wait for a free stage
+        int kb = pre;
         for (; kb < nkb; ++kb) {
             const int st = kb % stages;
             const uint32_t ph = (kb / stages) & 1;
@@ -131,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sa = base + st * Sh::kStageBytes;
             const int kx = k_lo + kb * kBlockK;
             ptx::mbar_arrive_expect_tx(full_bar(st), Sh::kStageBytes);
-            ptx::tma_load_2d(sa, &tmA, full_bar(st), kx, m_tile * kTileM, pol_a);
-            ptx::tma_load_2d(sa + Sh::kABytes, &tmB, full_bar(st), kx, n_tile * BN, pol_b);
+            ptx::tma_load_2d(sa, &tmA, full_bar(st), kx, m_tile * kTileM, ptx::l2_policy_evict_last());
+            ptx::tma_load_2d(sa + Sh::kABytes, &tmB, full_bar(st), kx, n_tile * BN, ptx::l2_policy_evict_normal());
         }
         issued_s = kb;
     } else if (warp == 1 && lane == 0) {
@@ -160,28 +227,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
 
-    bool acc_ok = ptx::mbar_wait_bounded(acc_bar, 0, args.wait_limit_ns);
+    const bool acc_ok = ptx::mbar_wait_bounded(acc_bar, 0, args.wait_limit_ns);
     if (!acc_ok) atomicOr(&abort_s, 4u);
     __syncthreads();
     const bool aborted = abort_s != 0;
     if (aborted && tid == 0) {
         atomicOr(&g_device_status, abort_s);
-        for (int kb = consumed_s; kb < issued_s; ++kb)   // loads still in flight into our smem
+        const int issued = max(issued_s, pre);
+        for (int kb = consumed_s; kb < issued; ++kb)   // loads still in flight into our smem
             ptx::mbar_wait_bounded(full_bar(kb % stages), (kb / stages) & 1, args.wait_limit_ns);
     }
     ptx::tc_fence_after_sync();
 
-    // ---- epilogue 1: tensor memory -> shared memory (reuses the stage ring).
-    // Thread (warp w, lane l) holds tile row 32w+l.  Box b = jb*4 + w holds
-    // rows 32w..32w+31, columns 32jb..32jb+31 as 32 rows of 128 bytes; the
-    // 16-byte piece q of row r sits at position q ^ (r & 7), so the eight
-    // threads of a store phase hit eight different bank groups.
-    ptx::fence_proxy_async_smem();
-    const uint32_t E = base;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // ---- epilogue 1: tensor memory -> staging.  Warp w reads lane quarter
+    // q = w % 4 (tile rows 32q..32q+31, one per thread) and column half w / 4;
+    // the eight threads of a store phase hit eight bank groups.
+    const int quarter = warp & 3, half = warp >> 2;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const bool have_acc = nkb > 0 && !aborted;
 #pragma unroll 1
-    for (int jb = 0; jb < BN / 32; ++jb) {
+    for (int jb = half * (BN / 64); jb < (half + 1) * (BN / 64); ++jb) {
         uint32_t v[32];
         if (have_acc) {
             ptx::tmem_ld_32x32b_x32(lane_base + jb * 32, v);
@@ -189,12 +254,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
-        const uint32_t row_addr = E + static_cast<uint32_t>(jb * 4 + warp) * 4096u + lane * 128u;
+        const uint32_t row_addr = E + static_cast<uint32_t>(jb * 4 + quarter) * 4096u + lane * 128u;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
             ptx::st_shared_v4(row_addr + (static_cast<uint32_t>(q ^ (lane & 7)) << 4), v[4 * q],
                               v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     }
+    ptx::fence_proxy_async_smem();             // the staging is the source of bulk copies
     ptx::tc_fence_before_sync();
     __syncthreads();
     if (warp == 1) {
@@ -203,74 +269,101 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_dealloc(tmem, Sh::kTmemCols);
     }
 
-    // ---- epilogue 2: sums over the cluster, then coalesced global stores.
-    const int Q = args.cluster;
-    if (Q > 1) {
-        ptx::cluster_arrive();
-        ptx::cluster_wait();
-    }
-    const uint32_t rank = Q > 1 ? ptx::cluster_ctarank() : 0u;
-    const int per = (Sh::kPieces + Q - 1) / Q;   // Q = splits*chunks need not be a power of two
-    const int g_end = min(Sh::kPieces, static_cast<int>(rank + 1) * per);
-    const int row0 = m_tile * kTileM, col0 = n_tile * BN;
-    const int C = args.chunks;
-    const size_t MN = static_cast<size_t>(args.M) * args.N;
-    for (int g = static_cast<int>(rank) * per + tid; g < g_end; g += kThreads) {
-        const int b = g >> 8, i = g & 255, rb = i >> 3, j = i & 7;
-        const int jb = b >> 2, w = b & 3;
-        const uint32_t off = static_cast<uint32_t>(b) * 4096u + rb * 128u + (static_cast<uint32_t>(j ^ (rb & 7)) << 4);
-        const int row = row0 + w * 32 + rb;
-        const int col = col0 + jb * 32 + j * 4;
-        const bool in_rows = row < args.M;
-        float4 v[kMaxCluster];
-        if (Q == 1) {
-            v[0] = ptx::ld_shared_v4(E + off);
-        } else {
+    // ---- exchange: push every other rank its share of this CTA's chunk
+    if (C > 1) {
+        ptx::cluster_wait();                   // every peer's receive barrier is set up
+        if (tid == 0) {
 #pragma unroll
-            for (int r = 0; r < kMaxCluster; ++r)
-                if (r < Q) v[r] = ptx::ld_cluster_v4(ptx::mapa(E + off, r));
+            for (int r = 0; r < C; ++r) {
+                const int lo = min(Sh::kPieces, r * share), hi = min(Sh::kPieces, lo + share);
+                if (r == c || hi <= lo) continue;
+                const uint32_t slot = static_cast<uint32_t>(c - (c > r ? 1 : 0));
+                ptx::bulk_copy_to_cluster(ptx::mapa(recv + slot * static_cast<uint32_t>(share) * 16u, r),
+                                          E + static_cast<uint32_t>(lo) * 16u,
+                                          static_cast<uint32_t>(hi - lo) * 16u, ptx::mapa(recv_bar, r));
+            }
         }
-        const size_t elem = static_cast<size_t>(row) * args.N + col;
-        if (!args.fused) {
-            float4 acc = v[0];
+    }
+    if (!ptx::mbar_wait_bounded(recv_bar, 0, args.wait_limit_ns) && tid == 0) atomicOr(&g_device_status, 16u);
+    if (C > 1) ptx::cluster_arrive_relaxed();  // everything bound for this CTA has landed
+
+    // ---- epilogue 2: the chunk sum of each owned piece, in chunk order
+    const int row0 = m_tile * kTileM, col0 = n_tile * BN;
+    const size_t MN = static_cast<size_t>(args.M) * args.N;
+    auto chunk_sum = [&](const Piece &p) {
+        float4 v[C];
 #pragma unroll
-            for (int r = 1; r < kMaxCluster; ++r)
-                if (r < Q) {
-                    acc.x += v[r].x; acc.y += v[r].y; acc.z += v[r].z; acc.w += v[r].w;
-                }
-            if (in_rows) *reinterpret_cast<float4 *>(args.P + s * MN + elem) = acc;
-        } else {
-            // rank r = split * C + chunk: close each split's chunk sum, then
-            // add the split sums in split order.
-            float4 part = make_float4(0.f, 0.f, 0.f, 0.f), tot = part;
+        for (int r = 0; r < C; ++r) {
+            const uint32_t off = r == c ? p.off
+                                        : args.region0 + static_cast<uint32_t>(r - (r > c ? 1 : 0)) *
+                                                             static_cast<uint32_t>(share) * 16u +
+                                              (p.off - static_cast<uint32_t>(my_lo) * 16u);
+            v[r] = *reinterpret_cast<const float4 *>(gbase + off);
+        }
+        float4 acc = v[0];
 #pragma unroll
-            for (int r = 0; r < kMaxCluster; ++r) {
-                if (r < Q) {
-                    const int cc = r % C;
-                    if (cc == 0) {
-                        part = v[r];
-                    } else {
-                        part.x += v[r].x; part.y += v[r].y; part.z += v[r].z; part.w += v[r].w;
-                    }
-                    if (cc == C - 1) {
-                        const int sp = r / C;
-                        if (args.P != nullptr && in_rows)
-                            *reinterpret_cast<float4 *>(args.P + sp * MN + elem) = part;
-                        if (sp == 0) {
-                            tot = part;
-                        } else {
-                            tot.x += part.x; tot.y += part.y; tot.z += part.z; tot.w += part.w;
+        for (int r = 1; r < C; ++r) add4(acc, v[r]);
+        return acc;
+    };
+    float *const Ps = args.P + static_cast<size_t>(s) * MN;
+#pragma unroll 2
+    for (int g = my_lo + tid; g < my_hi; g += kThreads) {
+        const Piece p = piece_at(g);
+        const float4 acc = chunk_sum(p);
+        const int row = row0 + p.row;
+        if (row < args.M)
+            *reinterpret_cast<float4 *>(Ps + static_cast<size_t>(row) * args.N + col0 + p.col) = acc;
+    }
+
+    // ---- fused: the last split to finish this piece range adds all splits
+    if (args.out != nullptr) {
+        __threadfence();                       // this thread's partials, before the arrival count
+        __syncthreads();
+        if (tid == 0) {
+            const unsigned idx = (static_cast<unsigned>(m_tile) * gridDim.x + n_tile) * C + c;
+            const unsigned old = atomicInc(&args.counters[idx], static_cast<unsigned>(args.S - 1));
+            last_s = old == static_cast<unsigned>(args.S - 1) ? 1u : 0u;
+        }
+        __syncthreads();
+        if (last_s) {
+            __threadfence();
+            for (int g0 = my_lo + tid; g0 < my_hi; g0 += kBatch * kThreads) {
+                float4 tot[kBatch];
+                for (int sp = 0; sp < args.S; ++sp) {
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i) {
+                        const int g = g0 + i * kThreads;
+                        if (g < my_hi) {
+                            const Piece p = piece_at(g);
+                            const int row = row0 + p.row;
+                            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (sp == s)
+                                v = chunk_sum(p);
+                            else if (row < args.M)
+                                v = __ldcg(reinterpret_cast<const float4 *>(
+                                    args.P + sp * MN + static_cast<size_t>(row) * args.N + col0 + p.col));
+                            if (sp == 0)
+                                tot[i] = v;
+                            else
+                                add4(tot[i], v);
                         }
                     }
                 }
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i) {
+                    const int g = g0 + i * kThreads;
+                    if (g < my_hi) {
+                        const Piece p = piece_at(g);
+                        const int row = row0 + p.row;
+                        if (row < args.M)
+                            *reinterpret_cast<float4 *>(args.out + static_cast<size_t>(row) * args.N + col0 +
+                                                        p.col) = tot[i];
+                    }
+                }
             }
-            if (in_rows) *reinterpret_cast<float4 *>(args.out + elem) = tot;
         }
     }
-    if (Q > 1) {   // no CTA leaves while another may still read its shared memory
-        ptx::cluster_arrive();
-        ptx::cluster_wait();
-    }
+    if (C > 1) ptx::cluster_wait();            // no CTA leaves while its staging may still be copied from
 }
 
 __global__ void wait_selftest_kernel(uint64_t limit_ns)
@@ -306,15 +399,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 bool encode_operand(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows, bool bf16)
 {
     auto fn = encode_fn();
-    if (!fn) return false;
+    if (!fn) {
+        note_message("cuTensorMapEncodeTiled is not available from the driver", 0);
+        return false;
+    }
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+    const CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                     const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) note_message("cuTensorMapEncodeTiled failed", static_cast<int>(r));
     return r == CUDA_SUCCESS;
 }
 
@@ -322,40 +419,63 @@ int g_override_bn = 0, g_override_chunks = 0;
 
 size_t stage_bytes(int bn) { return static_cast<size_t>(kTileM + bn) * kBlockK * 2; }
 size_t epi_bytes(int bn) { return static_cast<size_t>(kTileM) * bn * 4; }
-constexpr size_t kSmemLimit = 227 * 1024;
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+constexpr size_t kSmemLimit = 226 * 1024;   // dynamic; leaves room for static shared memory
+// A GB300 keeps at most 15 clusters of 8 CTAs resident at once (measured with
+// cudaOccupancyMaxActiveClusters: one CTA per SM per cluster rank); clusters
+// of 4 fit 36 at once.
+constexpr int kResidentClustersOf8 = 15;
 
-template <int BN>
+// Dynamic shared memory of a plan: the stage ring (or the accumulator
+// staging, if larger), one receive slot per peer, and 1 KB of alignment slack.
+size_t smem_for(int bn, int stages, int chunks, int share)
+{
+    const size_t region0 = round_up(std::max(stages * stage_bytes(bn), epi_bytes(bn)), 1024);
+    return region0 + static_cast<size_t>(chunks - 1) * share * 16 + 1024;
+}
+
+// Opts the kernel into the device's full dynamic shared memory (what is left
+// of the per-block opt-in limit after its static shared memory); once per
+// device.
+template <int BN, int C>
 cudaError_t prepare_kernel_attrs()
 {
     static std::mutex mu;
     static bool done[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) return note_error(e, "cudaGetDevice");
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(tc_splitk_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemLimit));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(tc_splitk_kernel<BN>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return note_error(e, "cudaDeviceGetAttribute(MaxSharedMemoryPerBlockOptin)");
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, tc_splitk_kernel<BN, C>);
+    if (e != cudaSuccess) return note_error(e, "cudaFuncGetAttributes(tc_splitk_kernel)");
+    const int dyn = optin - static_cast<int>(fa.sharedSizeBytes);
+    e = cudaFuncSetAttribute(tc_splitk_kernel<BN, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    if (e != cudaSuccess) return note_error(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
     if (dev >= 0 && dev < 64) done[dev] = true;
     return cudaSuccess;
 }
 
-template <int BN>
+template <int BN, int C>
 cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args, const TilePlan &plan,
                       cudaStream_t stream)
 {
-    cudaError_t e = prepare_kernel_attrs<BN>();
+    cudaError_t e = prepare_kernel_attrs<BN, C>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = plan.grid;
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = plan.smem_bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     unsigned nattr = 0;
+    attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+    ++nattr;
     if (plan.cluster > 1) {
         attr[nattr].id = cudaLaunchAttributeClusterDimension;
         attr[nattr].val.clusterDim.x = 1;
@@ -365,14 +485,21 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
-    return cudaLaunchKernelEx(&cfg, tc_splitk_kernel<BN>, ta, tb, args);
+    return note_error(cudaLaunchKernelEx(&cfg, tc_splitk_kernel<BN, C>, ta, tb, args),
+                      "cudaLaunchKernelEx(tc_splitk_kernel)");
 }
 
-int pow2_floor(int64_t x)
+template <int BN>
+cudaError_t launch_chunks(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args, const TilePlan &plan,
+                          cudaStream_t stream)
 {
-    int p = 1;
-    while (static_cast<int64_t>(p) * 2 <= x) p *= 2;
-    return p;
+    switch (plan.chunks) {
+    case 1: return launch_bn<BN, 1>(ta, tb, args, plan, stream);
+    case 2: return launch_bn<BN, 2>(ta, tb, args, plan, stream);
+    case 4: return launch_bn<BN, 4>(ta, tb, args, plan, stream);
+    case 8: return launch_bn<BN, 8>(ta, tb, args, plan, stream);
+    default: return note_error(cudaErrorInvalidConfiguration, "chunk count");
+    }
 }
 
 }  // namespace
@@ -390,47 +517,57 @@ TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool f
     const int64_t mt = (M + kTileM - 1) / kTileM;
     int bn = (N % 128 == 0) ? 128 : 64;
     if (g_override_bn && N % g_override_bn == 0) bn = g_override_bn;
-    // Split each split's K range over `chunks` CTAs until the grid roughly
-    // fills the GPU (one CTA per SM), keeping chunks of at least 64 elements.
-    // The limit on `chunks` does not depend on `fused`, so the fused and the
-    // two-kernel paths add the same chunks in the same order.
-    const int64_t base = mt * (N / bn) * S;
-    int limit = 8;
-    if (S <= kMaxCluster) limit = std::min(limit, pow2_floor(kMaxCluster / S));
+    // Cut each split's K range into `chunks` CTAs (one cluster) until the grid
+    // roughly fills the GPU with one CTA per SM, keeping chunks at least 64
+    // long; clusters of 8 only while they all stay resident.  The choice does
+    // not depend on `fused`, so both paths add the same chunks in the same order.
+    const int64_t clusters = mt * (N / bn) * S;
     int chunks = 1;
     if (g_override_chunks) {
-        chunks = std::min(g_override_chunks, limit);
+        chunks = std::min(g_override_chunks, kMaxChunks);
     } else {
-        while (chunks * 2 <= limit && base * chunks * 2 <= 160 && kps / (chunks * 2) >= 64) chunks *= 2;
+        while (chunks * 2 <= kMaxChunks && clusters * chunks * 2 <= 160 && kps / (chunks * 2) >= 64) chunks *= 2;
+        if (chunks == 8 && clusters > kResidentClustersOf8) chunks = 4;
     }
-    (void)fused;
-    int64_t chunk_len = (kps + chunks - 1) / chunks;
-    chunk_len = (chunk_len + 31) / 32 * 32;
-    const int64_t nkb = (chunk_len + kBlockK - 1) / kBlockK;
-    int max_stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - 1024) / stage_bytes(bn)));
-    int stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(nkb, max_stages)));
+    int share = 0, stages = 2;
+    int64_t chunk_len = 0;
+    for (;; chunks /= 2) {
+        chunk_len = (kps + chunks - 1) / chunks;
+        chunk_len = (chunk_len + 31) / 32 * 32;
+        const int64_t nkb = (chunk_len + kBlockK - 1) / kBlockK;
+        const int pieces = kTileM * bn / 4;
+        share = static_cast<int>(round_up((pieces + chunks - 1) / chunks, 8));
+        stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(nkb, kMaxStages)));
+        while (stages > 2 && smem_for(bn, stages, chunks, share) > kSmemLimit) --stages;
+        if (smem_for(bn, stages, chunks, share) <= kSmemLimit || chunks == 1) break;
+    }
     p.bn = bn;
     p.chunks = chunks;
     p.chunk_len = static_cast<int>(chunk_len);
     p.stages = stages;
     p.fused = fused ? 1 : 0;
-    p.cluster = fused ? static_cast<int>(S) * chunks : chunks;
+    p.cluster = chunks;
+    p.share = share;
+    p.region0 = static_cast<uint32_t>(round_up(std::max(stages * stage_bytes(bn), epi_bytes(bn)), 1024));
     p.grid = dim3(static_cast<unsigned>(N / bn), static_cast<unsigned>(mt), static_cast<unsigned>(S * chunks));
-    p.smem_bytes = std::max(stages * stage_bytes(bn), epi_bytes(bn)) + 1024;
+    p.smem_bytes = smem_for(bn, stages, chunks, share);
     return p;
 }
 
 cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t stream)
 {
-    if (plan.cluster > kMaxCluster || plan.stages > kMaxStages || plan.smem_bytes > kSmemLimit)
-        return cudaErrorInvalidConfiguration;
+    if (plan.cluster > kMaxChunks || plan.stages > kMaxStages || plan.smem_bytes > kSmemLimit)
+        return note_error(cudaErrorInvalidConfiguration, "tile plan out of range");
+    if (plan.fused && (pr.out == nullptr || pr.counters == nullptr))
+        return note_error(cudaErrorInvalidValue, "fused launch without output or counters");
     CUtensorMap ta, tb;
     if (!encode_operand(&ta, pr.A, pr.M, pr.K, kTileM, pr.bf16) ||
         !encode_operand(&tb, pr.B, pr.N, pr.K, plan.bn, pr.bf16))
         return cudaErrorInvalidValue;
     TcArgs a = {};
     a.P = pr.P;
-    a.out = pr.out;
+    a.out = plan.fused ? pr.out : nullptr;
+    a.counters = plan.fused ? pr.counters : nullptr;
     a.M = static_cast<int>(pr.M);
     a.N = static_cast<int>(pr.N);
     a.K = static_cast<int>(pr.K);
@@ -439,15 +576,15 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
     a.chunks = plan.chunks;
     a.chunk_len = plan.chunk_len;
     a.stages = plan.stages;
-    a.cluster = plan.cluster;
-    a.fused = plan.fused;
+    a.share = plan.share;
+    a.region0 = plan.region0;
     a.bf16 = pr.bf16 ? 1 : 0;
     a.wait_limit_ns = kWaitLimitNs;
     switch (plan.bn) {
-    case 64: return launch_bn<64>(ta, tb, a, plan, stream);
-    case 128: return launch_bn<128>(ta, tb, a, plan, stream);
-    case 256: return launch_bn<256>(ta, tb, a, plan, stream);
-    default: return cudaErrorInvalidConfiguration;
+    case 64: return launch_chunks<64>(ta, tb, a, plan, stream);
+    case 128: return launch_chunks<128>(ta, tb, a, plan, stream);
+    case 256: return launch_chunks<256>(ta, tb, a, plan, stream);
+    default: return note_error(cudaErrorInvalidConfiguration, "tile width");
     }
 }
 
@@ -465,7 +602,7 @@ cudaError_t launch_wait_selftest(int64_t limit_ns, cudaStream_t stream)
 {
     limit_ns = std::max<int64_t>(1000, std::min<int64_t>(limit_ns, 1000000000));
     wait_selftest_kernel<<<1, 32, 0, stream>>>(static_cast<uint64_t>(limit_ns));
-    return cudaGetLastError();
+    return note_error(cudaGetLastError(), "wait_selftest_kernel launch");
 }
 
 }  // namespace splitk

@@ -76,6 +76,17 @@ def max_scaled_error(got: np.ndarray, ref: np.ndarray, bound: np.ndarray) -> flo
     return float(np.max(err[~zero] / bound[~zero]))
 
 
+def workspace(M, N, K, S, kps, poison: float = POISON):
+    """A gemm_bt workspace: partials poisoned, the fused path's counters zeroed
+    (the library's one-time requirement), guards behind."""
+    import split_bf16_gemm_gb300 as sk
+
+    nbytes = sk.gemm_bt_workspace_bytes(M, N, K, S, kps)
+    ws = Guarded(nbytes // 4, poison)
+    ws.buf[S * M * N: nbytes // 4] = 0.0
+    return ws, nbytes
+
+
 @lru_cache(maxsize=64)
 def oracle_case(M, N, K, S, kps, dtype, recipe="uniform", seed=0):
     """(operands, P*, SP, O*, SO) for a seeded case; cached per process."""

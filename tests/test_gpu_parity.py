@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 from harness import (TOL_FINAL, TOL_PARTIAL, Guarded, device_operand, max_scaled_error,
-                     oracle_case)
+                     oracle_case, workspace)
 
 pytestmark = pytest.mark.gpu
 
@@ -93,27 +93,67 @@ def test_nan_poison(lib, case):
 
 
 @pytest.mark.parametrize("case", WORKLOADS + SWEEP[::3] + CATEGORIES, ids=ids(WORKLOADS + SWEEP[::3] + CATEGORIES))
-def test_gemm_bt_all_modes_bitwise(lib, case):
-    """gemm_bt with fused = 0, 1, 3 gives the two-kernel output bit for bit, and
-    fused = 3 writes the same partials as gemm_splitk_bt."""
+def test_gemm_bt_both_modes_bitwise(lib, case):
+    """gemm_bt with fused = 0 and 1 gives the two-kernel output bit for bit and
+    leaves gemm_splitk_bt's partials in the workspace."""
     sk = lib
     M, N, K, S, kps, dt = case
-    ops, Pr, SP, Or, SO = oracle_case(M, N, K, S, kps, dt)
     A, B, P, out = check_case(sk, case)
     ref_out = out.numpy()
     ref_P = P.numpy()
-    nbytes = sk.gemm_bt_workspace_bytes(M, N, K, S, kps)
-    for fused in (0, 1, 3):
-        ws = Guarded(nbytes // 4)
+    for fused in (0, 1):
+        ws, nbytes = workspace(M, N, K, S, kps)
         o = Guarded(M * N)
         sk.gemm_bt(A, B, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=fused)
         assert sk.splitk_get_device_status() == 0
         assert o.guards_intact() and ws.guards_intact()
         assert np.array_equal(o.numpy().view(np.uint32), ref_out.view(np.uint32)), f"fused={fused}"
-        if fused in (0, 3):
-            assert np.array_equal(ws.numpy().view(np.uint32), ref_P.view(np.uint32)), f"fused={fused}"
-        elif dt != "f32" and S <= 16:
-            assert np.all(ws.numpy() == 7.0), "fused=1 must leave the workspace untouched"
+        w = ws.numpy()
+        assert np.array_equal(w[:S * M * N].view(np.uint32), ref_P.view(np.uint32)), f"fused={fused}"
+        assert np.all(w[S * M * N:] == 0), "the counters must be back at zero"
+
+
+def test_fused_repeated_calls_and_overwrite(lib):
+    """The counters reset themselves: many fused calls on one workspace stay
+    correct, and a later call with other operands overwrites the output."""
+    sk = lib
+    M, N, K, S, kps, dt = 96, 512, 2048, 4, 512, "bf16"
+    ops, Pr, SP, Or, SO = oracle_case(M, N, K, S, kps, dt)
+    ops2, _, _, Or2, SO2 = oracle_case(M, N, K, S, kps, dt, "uniform", 7)
+    A, B = device_operand(ops.A, dt), device_operand(ops.B, dt)
+    A2, B2 = device_operand(ops2.A, dt), device_operand(ops2.B, dt)
+    ws, nbytes = workspace(M, N, K, S, kps)
+    o = Guarded(M * N)
+    first = None
+    for i in range(6):
+        sk.gemm_bt(A, B, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=1)
+        r = o.numpy().copy()
+        first = r if first is None else first
+        assert np.array_equal(r.view(np.uint32), first.view(np.uint32))
+    assert max_scaled_error(first.reshape(M, N), Or, SO) <= TOL_FINAL[dt]
+    # back-to-back launches on one stream, same workspace and output
+    sk.gemm_bt(A, B, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=1)
+    sk.gemm_bt(A2, B2, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=1)
+    assert max_scaled_error(o.numpy().reshape(M, N), Or2, SO2) <= TOL_FINAL[dt]
+    assert sk.splitk_get_device_status() == 0
+    assert np.all(ws.numpy()[S * M * N:] == 0)
+
+
+def test_reads_follow_previous_kernel(lib):
+    """A kernel launched just before (here a torch copy into A) is complete
+    before the GEMM reads A: the dependent-launch wait covers it."""
+    sk = lib
+    M, N, K, S, kps, dt = 256, 1024, 2048, 2, 1024, "bf16"
+    ops, Pr, SP, Or, SO = oracle_case(M, N, K, S, kps, dt)
+    src = device_operand(ops.A, dt)
+    B = device_operand(ops.B, dt)
+    ws, nbytes = workspace(M, N, K, S, kps)
+    for _ in range(3):
+        A = torch.zeros_like(src)
+        o = Guarded(M * N)
+        A.copy_(src)
+        sk.gemm_bt(A, B, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=1)
+        assert max_scaled_error(o.numpy().reshape(M, N), Or, SO) <= TOL_FINAL[dt]
 
 
 INT_CASES = [
@@ -197,9 +237,10 @@ def test_every_tiling(lib, case):
             P = Guarded(S * M * N)
             out = Guarded(M * N)
             fused = Guarded(M * N)
+            ws, nbytes = workspace(M, N, K, S, kps)
             sk.gemm_splitk_bt(A, B, P.data, M, N, K, S, kps, dt)
             sk.splitk_reduce(P.data, out.data, S, M, N)
-            sk.gemm_bt(A, B, fused.data, None, 0, M, N, K, S, kps, dt, fused=1)
+            sk.gemm_bt(A, B, fused.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=1)
             assert sk.splitk_get_device_status() == 0
             assert P.guards_intact() and out.guards_intact() and fused.guards_intact()
             assert max_scaled_error(P.numpy().reshape(S, M, N), Pr, SP) <= TOL_PARTIAL, (bn, ch)
@@ -217,13 +258,15 @@ def test_cuda_graph_capture_and_side_stream(lib):
     B = device_operand(ops.B, dt)
     nbytes = sk.gemm_bt_workspace_bytes(M, N, K, S, kps)
     ws = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+    ws2 = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+    sk.gemm_bt_workspace_init(ws2, nbytes)
     outs = [torch.full((M, N), 7.0, device="cuda") for _ in range(2)]
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         sk.gemm_bt(A, B, outs[0], ws, nbytes, M, N, K, S, kps, dt, fused=0)
-        sk.gemm_bt(A, B, outs[1], None, 0, M, N, K, S, kps, dt, fused=1)
+        sk.gemm_bt(A, B, outs[1], ws2, nbytes, M, N, K, S, kps, dt, fused=1)
     for _ in range(3):
         outs[0].fill_(7.0)
         outs[1].fill_(7.0)

@@ -117,7 +117,7 @@ def test_reduce_rejections(L):
 
 def test_gemm_bt_rejections(L):
     need = sk.gemm_bt_workspace_bytes(32, 64, 128, 2, 64)
-    assert need == 2 * 32 * 64 * 4
+    assert need >= 2 * 32 * 64 * 4
 
     def call(out=O0, ws=W0, wsb=need, fused=0, **kw):
         g = dict(GOOD, **kw)
@@ -133,14 +133,19 @@ def test_gemm_bt_rejections(L):
     assert call(out=A0) == bd.ERR_ALIAS
     assert call(ws=O0) == bd.ERR_ALIAS
     assert call(ws=B0 + 64) == bd.ERR_ALIAS
-    # fused=3 also keeps the partials, so it needs the workspace too
-    assert call(ws=0, fused=3) == bd.ERR_NULL
-    assert call(wsb=0, fused=3) == bd.ERR_WORKSPACE
+    assert call(fused=3) == bd.ERR_CONFIG
+    # the fused path keeps the partials and its counters in the workspace too
+    assert call(ws=0, fused=1) == bd.ERR_NULL
+    assert call(wsb=0, fused=1) == bd.ERR_WORKSPACE
+    assert L.gemm_bt_workspace_init(0, 64, None) == bd.ERR_NULL
+    assert L.gemm_bt_workspace_init(W0 + 4, 64, None) == bd.ERR_ALIGN
 
 
 def test_workspace_bytes(L):
-    assert sk.gemm_bt_workspace_bytes(256, 1024, 2048, 2, 1024) == 2 * 256 * 1024 * 4
-    assert sk.gemm_bt_workspace_bytes(64, 128, 160, 3, 64) == 3 * 64 * 128 * 4
+    # partials, then one 4-byte counter per (64-column block, 128-row block, chunk <= 8)
+    assert sk.gemm_bt_workspace_bytes(256, 1024, 2048, 2, 1024) == 2 * 256 * 1024 * 4 + 16 * 2 * 8 * 4
+    assert sk.gemm_bt_workspace_bytes(64, 128, 160, 3, 64) == 3 * 64 * 128 * 4 + 2 * 1 * 8 * 4
+    assert sk.gemm_bt_workspace_bytes(64, 128, 160, 3, 64, 1) == sk.gemm_bt_workspace_bytes(64, 128, 160, 3, 64, 0)
     assert sk.gemm_bt_workspace_bytes(64, 128, 160, 2, 64) == 0
 
 
@@ -167,18 +172,18 @@ def test_describe_launch_plans(L):
     assert d["smem_bytes"] <= 227 * 1024
     f = sk.splitk_describe_launch(256, 1024, 2048, 2, 1024, "bf16", fused=1)
     assert f["fused_in_kernel"] == 1 and f["kernels_per_call"] == 1
-    assert f["cluster"] == 2 * f["chunks"] <= 16
+    assert f["cluster"] == f["chunks"] <= 8
     # same chunking in both modes: the fused output equals the two-kernel output bitwise
     assert (f["bn"], f["chunks"], f["chunk_len"]) == (d["bn"], d["chunks"], d["chunk_len"])
     # F32 runs the FMA path, two kernels even when fused is asked for
     g = sk.splitk_describe_launch(96, 512, 2048, 4, 512, "f32", fused=1)
     assert g["path"] == 1 and g["kernels_per_call"] == 2
-    # more than 16 splits: no single cluster holds them, two kernels
+    # any number of splits fuses: the splits meet through arrival counters
     h = sk.splitk_describe_launch(32, 64, 32 * 32, 32, 32, "bf16", fused=1)
-    assert h["fused_in_kernel"] == 0 and h["kernels_per_call"] == 2
+    assert h["fused_in_kernel"] == 1 and h["kernels_per_call"] == 1
     for S in (1, 2, 4, 8, 16):
         e = sk.splitk_describe_launch(32, 512, 2048, S, 2048 // S, "f16", fused=1)
-        assert e["cluster"] == S * e["chunks"] <= 16
+        assert e["cluster"] == e["chunks"] <= 8 and e["smem_bytes"] <= 226 * 1024
 
 
 def test_describe_launch_override(L):
