@@ -147,16 +147,22 @@ const char *splitk_status_string(int status);
 
 /* Tile-shape override for tuning: every later tensor-core launch uses tile
  * width `bn` (64, 128 or 256; must divide N, else the automatic choice is
- * kept) and `chunks` thread blocks per split along K (1, 2, 4 or 8; fewer
- * when the shared memory of that many does not fit).  bn = chunks = 0 restores the automatic
- * choice.  Process-wide; not thread-safe against concurrent launches.
- * Returns SPLITK_OK or SPLITK_ERR_CONFIG. */
-int splitk_set_tile_override(int bn, int chunks);
+ * kept), `chunks` thread blocks per split along K (1, 2, 4 or 8; fewer when
+ * the shared memory of that many does not fit) and `kblocks_per_stage`
+ * 64-wide k-blocks per pipeline stage (1, 2 or 4; more than 1 only when K and
+ * k_per_split are multiples of 64).  Zero keeps the automatic choice for that
+ * item.  Process-wide; not thread-safe against concurrent launches.  Returns
+ * SPLITK_OK or SPLITK_ERR_CONFIG. */
+int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
 
-/* Describes the launch gemm_bt would make, without launching: info[0..11] =
+/* Describes the launch gemm_bt would make, without launching: info[0..15] =
  * {path (0 tensor-core, 1 F32 FMA), bn, chunks, chunk_len, stages,
- *  cluster_size (== chunks), grid_x, grid_y, grid_z, dynamic_smem_bytes,
- *  fused_in_kernel (0/1), kernels_per_call}.  Returns a status as gemm_bt's
+ *  cluster_size (chunks, or splits * chunks), grid_x, grid_y, grid_z,
+ *  dynamic_smem_bytes,
+ *  fused_in_kernel (0/1), kernels_per_call, kblocks_per_stage,
+ *  three_d_loads (0/1), split_sum (0 none, 1 by arrival counters in the
+ *  workspace, 2 inside the thread-block cluster), 0}; `info` must hold 16
+ *  ints.  Returns a status as gemm_bt's
  * validation would (pointers are not checked). */
 int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits,
                            int64_t k_per_split, int dtype, int fused,

@@ -60,7 +60,7 @@ def lib() -> ctypes.CDLL:
             L.splitk_get_device_status.argtypes = [vp]
             L.splitk_status_string.argtypes = [i32]
             L.splitk_status_string.restype = ctypes.c_char_p
-            L.splitk_set_tile_override.argtypes = [i32, i32]
+            L.splitk_set_tile_override.argtypes = [i32, i32, i32]
             L.splitk_describe_launch.argtypes = [i64, i64, i64, i64, i64, i32, i32, vp]
             L.splitk_selftest_bounded_wait.argtypes = [i64, vp]
             L.gemm_bt_workspace_init.argtypes = [vp, sz, vp]
@@ -159,16 +159,17 @@ def splitk_get_device_status(stream=None) -> int:
     return lib().splitk_get_device_status(_stream(stream))
 
 
-def splitk_set_tile_override(bn: int = 0, chunks: int = 0) -> None:
-    _check(lib().splitk_set_tile_override(bn, chunks), "splitk_set_tile_override")
+def splitk_set_tile_override(bn: int = 0, chunks: int = 0, kblocks_per_stage: int = 0) -> None:
+    _check(lib().splitk_set_tile_override(bn, chunks, kblocks_per_stage), "splitk_set_tile_override")
 
 
 def splitk_describe_launch(M, N, K, splits, k_per_split, dtype, fused=0) -> dict:
-    info = (ctypes.c_int * 12)()
+    info = (ctypes.c_int * 16)()
     _check(lib().splitk_describe_launch(M, N, K, splits, k_per_split, dtype_code(dtype), fused,
                                         ctypes.addressof(info)), "splitk_describe_launch")
     keys = ("path", "bn", "chunks", "chunk_len", "stages", "cluster", "grid_x", "grid_y",
-            "grid_z", "smem_bytes", "fused_in_kernel", "kernels_per_call")
+            "grid_z", "smem_bytes", "fused_in_kernel", "kernels_per_call", "kblocks_per_stage",
+            "three_d", "split_sum")
     return dict(zip(keys, list(info)))
 
 

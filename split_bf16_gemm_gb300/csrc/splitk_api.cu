@@ -225,12 +225,14 @@ const char *splitk_status_string(int status)
     }
 }
 
-int splitk_set_tile_override(int bn, int chunks)
+int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage)
 {
     if (bn != 0 && bn != 64 && bn != 128 && bn != 256) return SPLITK_ERR_CONFIG;
     if (chunks != 0 && chunks != 1 && chunks != 2 && chunks != 4 && chunks != 8)
         return SPLITK_ERR_CONFIG;
-    splitk::set_tile_override(bn, chunks);
+    if (kblocks_per_stage != 0 && kblocks_per_stage != 1 && kblocks_per_stage != 2 && kblocks_per_stage != 4)
+        return SPLITK_ERR_CONFIG;
+    splitk::set_tile_override(bn, chunks, kblocks_per_stage);
     return SPLITK_OK;
 }
 
@@ -241,7 +243,7 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
     if (st != SPLITK_OK) return st;
     if (elem_bytes(dtype) == 0) return SPLITK_ERR_DTYPE;
     if (!info) return SPLITK_ERR_NULL;
-    std::fill(info, info + 12, 0);
+    std::fill(info, info + 16, 0);
     if (dtype == SPLITK_F32) {
         info[0] = 1;
         info[1] = 64;
@@ -252,6 +254,7 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
         info[7] = static_cast<int>((M + 63) / 64);
         info[8] = static_cast<int>(splits);
         info[11] = 2;
+        info[12] = 1;
         return SPLITK_OK;
     }
     const bool in_kernel = fused != 0 && fused_possible(dtype);
@@ -268,6 +271,9 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
     info[9] = static_cast<int>(p.smem_bytes);
     info[10] = in_kernel ? 1 : 0;
     info[11] = in_kernel ? 1 : 2;
+    info[12] = p.kbs;
+    info[13] = p.three_d;
+    info[14] = p.split_sum;
     return SPLITK_OK;
 }
 

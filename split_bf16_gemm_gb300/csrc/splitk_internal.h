@@ -20,16 +20,20 @@ struct GemmProblem {
 };
 
 // How it is tiled.  One CTA computes a 128 x bn tile of one K-chunk of one
-// split; the `chunks` CTAs of a split form a thread-block cluster and add
-// their accumulators through distributed shared memory, each rank owning
-// `share` 16-byte pieces of the tile.
+// split; the `chunks` CTAs of a split (or, when the splits are summed in the
+// cluster, all splits * chunks CTAs of the tile) form a thread-block cluster
+// and add their accumulators through distributed shared memory, each rank
+// owning `share` 16-byte pieces of the tile.
 struct TilePlan {
     int bn;             // tile width: 64, 128 or 256
     int chunks;         // CTAs per split along K
     int chunk_len;      // K elements per chunk (multiple of 32)
     int stages;         // shared-memory pipeline depth
-    int cluster;        // CTAs per cluster along grid z (== chunks)
-    int fused;          // the last split to finish a piece also sums over splits
+    int kbs;            // 64-wide k-blocks per stage
+    int three_d;        // stages loaded as one 3-D box per operand (K, kps, chunk_len multiples of 64)
+    int cluster;        // CTAs per cluster along grid z (chunks, or splits * chunks)
+    int fused;          // this launch also sums over splits
+    int split_sum;      // 0 none, 1 by arrival counters, 2 inside the cluster (cluster = splits * chunks)
     int share;          // 16-byte pieces of the tile each cluster rank owns
     uint32_t region0;   // bytes of the stage ring / accumulator staging
     dim3 grid;
@@ -47,7 +51,7 @@ inline int64_t fused_counter_count(int64_t M, int64_t N) { return (N / 64) * ((M
 
 // Tile choice for a shape (automatic, or the process-wide override).
 TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused);
-void set_tile_override(int bn, int chunks);
+void set_tile_override(int bn, int chunks, int kbs);
 
 // Kernel launches; each returns the launch's CUDA error.
 cudaError_t launch_tc(const GemmProblem &p, const TilePlan &plan, cudaStream_t stream);

@@ -59,9 +59,12 @@ constexpr int kBatch = 8;                          // pieces per thread per pass
 struct TcArgs {
     float *P;              // [S,M,N] partials
     float *out;            // [M,N], or nullptr when the splits are not summed here
-    unsigned *counters;    // per (tile, cluster rank) arrival counters when out != nullptr
+    unsigned *counters;    // per (tile, chunk) arrival counters (split sum by counters)
     int M, N, K, S, kps;
     int chunks, chunk_len, stages;
+    int split_sum;         // 0: none; 1: by arrival counters; 2: inside the cluster (cluster = splits x chunks)
+    int kbs;               // 64-wide k-blocks per pipeline stage
+    int three_d;           // operands loaded as 3-D boxes of kbs k-blocks (else 2-D, kbs == 1)
     int share;             // 16-byte pieces owned by each cluster rank (a multiple of 8)
     uint32_t region0;      // bytes of the stage ring / accumulator staging area
     int bf16;
@@ -70,9 +73,8 @@ struct TcArgs {
 
 template <int BN>
 struct TcShape {
-    static constexpr uint32_t kABytes = kTileM * kBlockK * 2;     // 16 KB
-    static constexpr uint32_t kBBytes = BN * kBlockK * 2;
-    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kABytes = kTileM * kBlockK * 2;     // one k-block of A: 16 KB
+    static constexpr uint32_t kBBytes = BN * kBlockK * 2;         // one k-block of B
     static constexpr uint32_t kTmemCols = BN;                     // power of two >= 32
     static constexpr int kPieces = kTileM * BN / 4;               // 16-byte pieces per tile
 };
@@ -104,7 +106,7 @@ __device__ __forceinline__ void add4(float4 &a, const float4 &b)
     a.w += b.w;
 }
 
-template <int BN, int C>
+template <int BN, int Q>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const TcArgs args)
@@ -125,8 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t recv = base + args.region0;      // the peers' shares of this CTA's pieces
 
     const int n_tile = blockIdx.x, m_tile = blockIdx.y;
+    const int C = args.chunks;
     const int s = blockIdx.z / C;
-    const int c = blockIdx.z - s * C;               // == rank in the 1 x 1 x C cluster
+    const int c = blockIdx.z - s * C;
+    const int rank = static_cast<int>(blockIdx.z) % Q;  // in the 1 x 1 x Q cluster: the chunk, or split*C+chunk
     const int ks = s * args.kps;
     const int ke = min(ks + args.kps, args.K);      // the last split clamps to K
     const int k_lo = ks + c * args.chunk_len;
@@ -134,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int klen = k_hi > k_lo ? k_hi - k_lo : 0; // a chunk past a short split is empty
     const int nkb = (klen + kBlockK - 1) / kBlockK;
     const int share = args.share;
-    const int my_lo = min(Sh::kPieces, c * share);
+    const int my_lo = min(Sh::kPieces, rank * share);
     const int my_hi = min(Sh::kPieces, my_lo + share);
 
     const uint32_t bar0 = ptx::smem_addr(&bars[0]);
@@ -143,7 +147,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t acc_bar = bar0 + 8u * (2 * kMaxStages);
     const uint32_t recv_bar = bar0 + 8u * (2 * kMaxStages + 1);
 
-    const int pre = min(stages, nkb);               // loads that need no free slot
+    // Stage i holds k-blocks i*kbs .. i*kbs+kbs-1 of the chunk: kbs slabs of A
+    // (128 rows x 128 bytes each) then kbs slabs of B (BN rows x 128 bytes).
+    const int kbs = args.kbs;
+    const uint32_t stage_bytes = static_cast<uint32_t>(kbs) * (Sh::kABytes + Sh::kBBytes);
+    const int nstg = (nkb + kbs - 1) / kbs;
+    const int pre = min(stages, nstg);              // stages that need no free slot
+    auto issue_stage = [&](int i, int slot) {
+        const uint32_t sa = base + slot * stage_bytes;
+        const uint32_t bar = full_bar(slot);
+        ptx::mbar_arrive_expect_tx(bar, stage_bytes);
+        if (args.three_d) {                         // one box per operand: kbs k-blocks at once
+            const int kb = k_lo / kBlockK + i * kbs;
+            ptx::tma_load_3d(sa, &tmA, bar, 0, m_tile * kTileM, kb, ptx::l2_policy_evict_last());
+            ptx::tma_load_3d(sa + kbs * Sh::kABytes, &tmB, bar, 0, n_tile * BN, kb, ptx::l2_policy_evict_normal());
+        } else {                                    // kbs == 1
+            const int kx = k_lo + i * kBlockK;
+            ptx::tma_load_2d(sa, &tmA, bar, kx, m_tile * kTileM, ptx::l2_policy_evict_last());
+            ptx::tma_load_2d(sa + Sh::kABytes, &tmB, bar, kx, n_tile * BN, ptx::l2_policy_evict_normal());
+        }
+    };
     if (tid == 0) {
         for (int i = 0; i < stages; ++i) {
             ptx::mbar_init(full_bar(i), 1);
@@ -157,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         last_s = 0;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
-        const uint32_t incoming = static_cast<uint32_t>((C - 1) * (my_hi - my_lo)) * 16u;
+        const uint32_t incoming = static_cast<uint32_t>((Q - 1) * (my_hi - my_lo)) * 16u;
         if (incoming)
             ptx::mbar_arrive_expect_tx(recv_bar, incoming);
         else
@@ -165,13 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB);
         ptx::grid_dependency_wait();                // A and B may be the previous grid's output
-        for (int kb = 0; kb < pre; ++kb) {
-            const uint32_t sa = base + kb * Sh::kStageBytes;
-            const int kx = k_lo + kb * kBlockK;
-            ptx::mbar_arrive_expect_tx(full_bar(kb), Sh::kStageBytes);
-            ptx::tma_load_2d(sa, &tmA, full_bar(kb), kx, m_tile * kTileM, ptx::l2_policy_evict_last());
-            ptx::tma_load_2d(sa + Sh::kABytes, &tmB, full_bar(kb), kx, n_tile * BN, ptx::l2_policy_evict_normal());
-        }
+        for (int i = 0; i < pre; ++i) issue_stage(i, i);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(&tmem_slot), Sh::kTmemCols);
@@ -180,49 +197,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
-    if (C > 1) ptx::cluster_arrive();               // publishes this CTA's barrier set-up to the cluster
+    if (Q > 1) ptx::cluster_arrive();               // publishes this CTA's barrier set-up to the cluster
     ptx::grid_dependency_wait();
     ptx::launch_dependents();
     const uint32_t tmem = tmem_slot;
 
     if (warp == 0 && lane == 0) {
-        // ---- TMA producer: the loads that had to wait for a free stage
-        int kb = pre;
-        for (; kb < nkb; ++kb) {
-            const int st = kb % stages;
-            const uint32_t ph = (kb / stages) & 1;
+        // ---- TMA producer: the stages that had to wait for a free slot
+        int i = pre;
+        for (; i < nstg; ++i) {
+            const int st = i % stages;
+            const uint32_t ph = (i / stages) & 1;
             if (!ptx::mbar_wait_bounded(empty_bar(st), ph ^ 1u, args.wait_limit_ns)) {
                 atomicOr(&abort_s, 1u);
                 break;
             }
-            const uint32_t sa = base + st * Sh::kStageBytes;
-            const int kx = k_lo + kb * kBlockK;
-            ptx::mbar_arrive_expect_tx(full_bar(st), Sh::kStageBytes);
-            ptx::tma_load_2d(sa, &tmA, full_bar(st), kx, m_tile * kTileM, ptx::l2_policy_evict_last());
-            ptx::tma_load_2d(sa + Sh::kABytes, &tmB, full_bar(st), kx, n_tile * BN, ptx::l2_policy_evict_normal());
+            issue_stage(i, st);
         }
-        issued_s = kb;
+        issued_s = i;
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
         const uint32_t idesc = ptx::idesc_f16_f32acc(args.bf16 != 0, kTileM, BN);
-        int kb = 0;
-        for (; kb < nkb; ++kb) {
-            const int st = kb % stages;
-            const uint32_t ph = (kb / stages) & 1;
+        int i = 0;
+        for (; i < nstg; ++i) {
+            const int st = i % stages;
+            const uint32_t ph = (i / stages) & 1;
             if (!ptx::mbar_wait_bounded(full_bar(st), ph, args.wait_limit_ns)) {
                 atomicOr(&abort_s, 2u);
                 break;
             }
             ptx::tc_fence_after_sync();
-            const uint32_t sa = base + st * Sh::kStageBytes;
-            const uint64_t ad = ptx::sdesc_kmajor_sw128(sa);
-            const uint64_t bd = ptx::sdesc_kmajor_sw128(sa + Sh::kABytes);
-            const int ksteps = min(kBlockK, klen - kb * kBlockK) / 16;   // 4, or 2 for a 32-long tail
-            for (int j = 0; j < ksteps; ++j)   // +32 bytes along K inside the swizzled row
-                ptx::mma_f16(tmem, ad + 2u * j, bd + 2u * j, idesc, (kb | j) != 0 ? 1u : 0u);
-            ptx::mma_commit(empty_bar(st));    // frees the stage once these MMAs have read it
+            const uint32_t sa = base + st * stage_bytes;
+            const uint32_t sb = sa + kbs * Sh::kABytes;
+            for (int j = 0; j < kbs; ++j) {
+                const int kb = i * kbs + j;
+                if (kb >= nkb) break;
+                const uint64_t ad = ptx::sdesc_kmajor_sw128(sa + j * Sh::kABytes);
+                const uint64_t bd = ptx::sdesc_kmajor_sw128(sb + j * Sh::kBBytes);
+                const int ksteps = min(kBlockK, klen - kb * kBlockK) / 16;   // 4, or 2 for a 32-long tail
+                for (int k = 0; k < ksteps; ++k)   // +32 bytes along K inside the swizzled row
+                    ptx::mma_f16(tmem, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(empty_bar(st));    // frees the slot once these MMAs have read it
         }
-        consumed_s = kb;
+        consumed_s = i;
         ptx::mma_commit(acc_bar);              // the accumulator is final
     }
     __syncthreads();
@@ -234,8 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (aborted && tid == 0) {
         atomicOr(&g_device_status, abort_s);
         const int issued = max(issued_s, pre);
-        for (int kb = consumed_s; kb < issued; ++kb)   // loads still in flight into our smem
-            ptx::mbar_wait_bounded(full_bar(kb % stages), (kb / stages) & 1, args.wait_limit_ns);
+        for (int i = consumed_s; i < issued; ++i)      // loads still in flight into our smem
+            ptx::mbar_wait_bounded(full_bar(i % stages), (i / stages) & 1, args.wait_limit_ns);
     }
     ptx::tc_fence_after_sync();
 
@@ -270,14 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- exchange: push every other rank its share of this CTA's chunk
-    if (C > 1) {
+    if (Q > 1) {
         ptx::cluster_wait();                   // every peer's receive barrier is set up
         if (tid == 0) {
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
+            for (int r = 0; r < Q; ++r) {
                 const int lo = min(Sh::kPieces, r * share), hi = min(Sh::kPieces, lo + share);
-                if (r == c || hi <= lo) continue;
-                const uint32_t slot = static_cast<uint32_t>(c - (c > r ? 1 : 0));
+                if (r == rank || hi <= lo) continue;
+                const uint32_t slot = static_cast<uint32_t>(rank - (rank > r ? 1 : 0));
                 ptx::bulk_copy_to_cluster(ptx::mapa(recv + slot * static_cast<uint32_t>(share) * 16u, r),
                                           E + static_cast<uint32_t>(lo) * 16u,
                                           static_cast<uint32_t>(hi - lo) * 16u, ptx::mapa(recv_bar, r));
@@ -285,42 +303,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     if (!ptx::mbar_wait_bounded(recv_bar, 0, args.wait_limit_ns) && tid == 0) atomicOr(&g_device_status, 16u);
-    if (C > 1) ptx::cluster_arrive_relaxed();  // everything bound for this CTA has landed
+    if (Q > 1) ptx::cluster_arrive_relaxed();  // everything bound for this CTA has landed
 
-    // ---- epilogue 2: the chunk sum of each owned piece, in chunk order
+    // ---- epilogue 2: sums of each owned piece over the cluster's ranks
     const int row0 = m_tile * kTileM, col0 = n_tile * BN;
     const size_t MN = static_cast<size_t>(args.M) * args.N;
-    auto chunk_sum = [&](const Piece &p) {
-        float4 v[C];
+    auto gather = [&](const Piece &p, float4 (&v)[Q]) {
 #pragma unroll
-        for (int r = 0; r < C; ++r) {
-            const uint32_t off = r == c ? p.off
-                                        : args.region0 + static_cast<uint32_t>(r - (r > c ? 1 : 0)) *
-                                                             static_cast<uint32_t>(share) * 16u +
-                                              (p.off - static_cast<uint32_t>(my_lo) * 16u);
+        for (int r = 0; r < Q; ++r) {
+            const uint32_t off = r == rank ? p.off
+                                           : args.region0 + static_cast<uint32_t>(r - (r > rank ? 1 : 0)) *
+                                                                static_cast<uint32_t>(share) * 16u +
+                                                 (p.off - static_cast<uint32_t>(my_lo) * 16u);
             v[r] = *reinterpret_cast<const float4 *>(gbase + off);
         }
+    };
+    // the chunk sum of one split (Q == C): chunks in order 0, 1, 2, ...
+    auto chunk_sum = [&](const Piece &p) {
+        float4 v[Q];
+        gather(p, v);
         float4 acc = v[0];
 #pragma unroll
-        for (int r = 1; r < C; ++r) add4(acc, v[r]);
+        for (int r = 1; r < Q; ++r) add4(acc, v[r]);
         return acc;
     };
-    float *const Ps = args.P + static_cast<size_t>(s) * MN;
+    if (args.split_sum != 2) {
+        float *const Ps = args.P + static_cast<size_t>(s) * MN;
 #pragma unroll 2
-    for (int g = my_lo + tid; g < my_hi; g += kThreads) {
-        const Piece p = piece_at(g);
-        const float4 acc = chunk_sum(p);
-        const int row = row0 + p.row;
-        if (row < args.M)
-            *reinterpret_cast<float4 *>(Ps + static_cast<size_t>(row) * args.N + col0 + p.col) = acc;
+        for (int g = my_lo + tid; g < my_hi; g += kThreads) {
+            const Piece p = piece_at(g);
+            const float4 acc = chunk_sum(p);
+            const int row = row0 + p.row;
+            if (row < args.M)
+                *reinterpret_cast<float4 *>(Ps + static_cast<size_t>(row) * args.N + col0 + p.col) = acc;
+        }
+    } else {
+        // the cluster holds every split of the tile (rank = split * C + chunk):
+        // each split's chunk sum in chunk order, then the splits in split order,
+        // the same additions the reduce kernel makes on the same partials
+        for (int g = my_lo + tid; g < my_hi; g += kThreads) {
+            const Piece p = piece_at(g);
+            const int row = row0 + p.row;
+            const size_t elem = static_cast<size_t>(row) * args.N + col0 + p.col;
+            float4 v[Q];
+            gather(p, v);
+            float4 part = v[0], tot = v[0];
+#pragma unroll
+            for (int r = 0; r < Q; ++r) {
+                const int cc = r % C;
+                if (cc == 0)
+                    part = v[r];
+                else
+                    add4(part, v[r]);
+                if (cc == C - 1) {
+                    const int sp = r / C;
+                    if (row < args.M) *reinterpret_cast<float4 *>(args.P + sp * MN + elem) = part;
+                    if (sp == 0)
+                        tot = part;
+                    else
+                        add4(tot, part);
+                }
+            }
+            if (row < args.M) *reinterpret_cast<float4 *>(args.out + elem) = tot;
+        }
     }
 
-    // ---- fused: the last split to finish this piece range adds all splits
-    if (args.out != nullptr) {
+    // ---- split sum by counters: the last split to finish this piece range
+    // adds all splits (Q == C here)
+    if (args.split_sum == 1) {
         __threadfence();                       // this thread's partials, before the arrival count
         __syncthreads();
         if (tid == 0) {
-            const unsigned idx = (static_cast<unsigned>(m_tile) * gridDim.x + n_tile) * C + c;
+            const unsigned idx = (static_cast<unsigned>(m_tile) * gridDim.x + n_tile) * C + c;   // c == rank
             const unsigned old = atomicInc(&args.counters[idx], static_cast<unsigned>(args.S - 1));
             last_s = old == static_cast<unsigned>(args.S - 1) ? 1u : 0u;
         }
@@ -363,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
-    if (C > 1) ptx::cluster_wait();            // no CTA leaves while its staging may still be copied from
+    if (Q > 1) ptx::cluster_wait();            // no CTA leaves while its staging may still be copied from
 }
 
 __global__ void wait_selftest_kernel(uint64_t limit_ns)
@@ -415,9 +469,34 @@ bool encode_operand(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, 
     return r == CUDA_SUCCESS;
 }
 
-int g_override_bn = 0, g_override_chunks = 0;
+// Row-major [rows, K] 16-bit matrix seen as 3-D (element within a 64-wide
+// k-block, row, k-block), box = 64 x box_rows x kbs, 128-byte swizzle: one
+// load brings kbs k-blocks of a tile.  Needs K % 64 == 0, so that no k-block
+// runs past the end of a row.
+bool encode_operand_3d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows, int kbs, bool bf16)
+{
+    auto fn = encode_fn();
+    if (!fn) {
+        note_message("cuTensorMapEncodeTiled is not available from the driver", 0);
+        return false;
+    }
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kBlockK), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(K / kBlockK)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(kBlockK) * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kBlockK), static_cast<cuuint32_t>(box_rows),
+                         static_cast<cuuint32_t>(kbs)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                          const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) note_message("cuTensorMapEncodeTiled (3-D) failed", static_cast<int>(r));
+    return r == CUDA_SUCCESS;
+}
 
-size_t stage_bytes(int bn) { return static_cast<size_t>(kTileM + bn) * kBlockK * 2; }
+int g_override_bn = 0, g_override_chunks = 0, g_override_kbs = 0;
+
+size_t stage_bytes(int bn, int kbs) { return static_cast<size_t>(kTileM + bn) * kBlockK * 2 * kbs; }
 size_t epi_bytes(int bn) { return static_cast<size_t>(kTileM) * bn * 4; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr size_t kSmemLimit = 226 * 1024;   // dynamic; leaves room for static shared memory
@@ -428,16 +507,16 @@ constexpr int kResidentClustersOf8 = 15;
 
 // Dynamic shared memory of a plan: the stage ring (or the accumulator
 // staging, if larger), one receive slot per peer, and 1 KB of alignment slack.
-size_t smem_for(int bn, int stages, int chunks, int share)
+size_t smem_for(int bn, int kbs, int stages, int chunks, int share)
 {
-    const size_t region0 = round_up(std::max(stages * stage_bytes(bn), epi_bytes(bn)), 1024);
+    const size_t region0 = round_up(std::max(stages * stage_bytes(bn, kbs), epi_bytes(bn)), 1024);
     return region0 + static_cast<size_t>(chunks - 1) * share * 16 + 1024;
 }
 
 // Opts the kernel into the device's full dynamic shared memory (what is left
 // of the per-block opt-in limit after its static shared memory); once per
 // device.
-template <int BN, int C>
+template <int BN, int Q>
 cudaError_t prepare_kernel_attrs()
 {
     static std::mutex mu;
@@ -451,20 +530,20 @@ cudaError_t prepare_kernel_attrs()
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return note_error(e, "cudaDeviceGetAttribute(MaxSharedMemoryPerBlockOptin)");
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, tc_splitk_kernel<BN, C>);
+    e = cudaFuncGetAttributes(&fa, tc_splitk_kernel<BN, Q>);
     if (e != cudaSuccess) return note_error(e, "cudaFuncGetAttributes(tc_splitk_kernel)");
     const int dyn = optin - static_cast<int>(fa.sharedSizeBytes);
-    e = cudaFuncSetAttribute(tc_splitk_kernel<BN, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    e = cudaFuncSetAttribute(tc_splitk_kernel<BN, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
     if (e != cudaSuccess) return note_error(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
     if (dev >= 0 && dev < 64) done[dev] = true;
     return cudaSuccess;
 }
 
-template <int BN, int C>
+template <int BN, int Q>
 cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args, const TilePlan &plan,
                       cudaStream_t stream)
 {
-    cudaError_t e = prepare_kernel_attrs<BN, C>();
+    cudaError_t e = prepare_kernel_attrs<BN, Q>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = plan.grid;
@@ -485,72 +564,174 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
-    return note_error(cudaLaunchKernelEx(&cfg, tc_splitk_kernel<BN, C>, ta, tb, args),
+    return note_error(cudaLaunchKernelEx(&cfg, tc_splitk_kernel<BN, Q>, ta, tb, args),
                       "cudaLaunchKernelEx(tc_splitk_kernel)");
 }
 
 template <int BN>
-cudaError_t launch_chunks(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args, const TilePlan &plan,
-                          cudaStream_t stream)
+cudaError_t launch_cluster(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args, const TilePlan &plan,
+                           cudaStream_t stream)
 {
-    switch (plan.chunks) {
+    switch (plan.cluster) {
     case 1: return launch_bn<BN, 1>(ta, tb, args, plan, stream);
     case 2: return launch_bn<BN, 2>(ta, tb, args, plan, stream);
     case 4: return launch_bn<BN, 4>(ta, tb, args, plan, stream);
     case 8: return launch_bn<BN, 8>(ta, tb, args, plan, stream);
-    default: return note_error(cudaErrorInvalidConfiguration, "chunk count");
+    default: return note_error(cudaErrorInvalidConfiguration, "cluster size");
     }
 }
 
 }  // namespace
 
-void set_tile_override(int bn, int chunks)
+void set_tile_override(int bn, int chunks, int kbs)
 {
     g_override_bn = bn;
     g_override_chunks = chunks;
+    g_override_kbs = kbs;
 }
+
+namespace {
+
+// Clusters of q CTAs (one per SM) a GB300 keeps resident at once, from
+// cudaOccupancyMaxActiveClusters: 36 of 4, 15 of 8; pairs and single CTAs are
+// limited by the SM count.
+int resident_clusters(int q)
+{
+    switch (q) {
+    case 1: return 148;
+    case 2: return 72;
+    case 4: return 36;
+    default: return 15;
+    }
+}
+
+struct StageChoice {
+    int kbs = 1, stages = 1;
+    bool ok = false;
+};
+
+// The largest stage (k-blocks per box) that keeps a chunk's loads double-
+// buffered, or all in flight, within shared memory, for a cluster of q.
+StageChoice pick_stages(int bn, int nkb, bool can3d, int q, int share)
+{
+    StageChoice r;
+    for (int cand : {4, 2, 1}) {
+        if (!can3d && cand > 1) continue;
+        if (g_override_kbs && cand != std::min(g_override_kbs, can3d ? 4 : 1)) continue;
+        const int want = (nkb + cand - 1) / cand;
+        int st = std::min(want, kMaxStages);
+        while (st > 1 && smem_for(bn, cand, st, q, share) > kSmemLimit) --st;
+        if (smem_for(bn, cand, st, q, share) > kSmemLimit) continue;
+        if (st < std::min(want, 2) && !g_override_kbs) continue;
+        r.kbs = std::min(cand, std::max(nkb, 1));
+        r.stages = st;
+        r.ok = true;
+        return r;
+    }
+    return r;
+}
+
+int share_for(int bn, int q)
+{
+    const int pieces = kTileM * bn / 4;
+    return static_cast<int>(round_up((pieces + q - 1) / q, 8));
+}
+
+// Time model of one launch (microseconds), from measurements on GB300: the
+// loads are bound by the L2 (about 10.5 TB/s for all SMs) or by one SM's TMA
+// intake (about 100 GB/s); staging the accumulator runs near 100 GB/s, the
+// distributed-shared-memory exchange and the final stores near 30 GB/s per SM.
+double model_us(int64_t M, int64_t N, int64_t S, int bn, int chunks, int64_t chunk_len, int q)
+{
+    const int64_t mt = (M + kTileM - 1) / kTileM;
+    const int64_t ctas = mt * (N / bn) * S * chunks;
+    const double load = static_cast<double>(kTileM + bn) * chunk_len * 2;     // bytes per CTA
+    const double acc = static_cast<double>(kTileM) * bn * 4;
+    const double t_load = std::max(load / 1.0e5, ctas * load / 1.05e7);
+    const double t_stage = acc / 1.0e5;
+    const double t_exchange = acc * (q - 1) / q / 3.0e4;
+    const double t_store = acc / q / 3.0e4;
+    const int64_t per_wave = q > 1 ? static_cast<int64_t>(resident_clusters(q)) * q : 148;
+    const int64_t waves = (ctas + per_wave - 1) / per_wave;
+    return static_cast<double>(waves) * (t_load + t_stage + t_exchange + t_store);
+}
+
+}  // namespace
 
 TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused)
 {
-    (void)K;
-    TilePlan p = {};
+    // Stages of several k-blocks load as one 3-D box per operand, which the
+    // TMA unit moves much faster than the same bytes in 16 KB boxes; that needs
+    // every chunk to start on a 64-element boundary.
+    const bool can3d = K % kBlockK == 0 && kps % kBlockK == 0;
+    const int64_t grain = can3d ? kBlockK : 32;
     const int64_t mt = (M + kTileM - 1) / kTileM;
-    int bn = (N % 128 == 0) ? 128 : 64;
-    if (g_override_bn && N % g_override_bn == 0) bn = g_override_bn;
-    // Cut each split's K range into `chunks` CTAs (one cluster) until the grid
-    // roughly fills the GPU with one CTA per SM, keeping chunks at least 64
-    // long; clusters of 8 only while they all stay resident.  The choice does
-    // not depend on `fused`, so both paths add the same chunks in the same order.
-    const int64_t clusters = mt * (N / bn) * S;
-    int chunks = 1;
-    if (g_override_chunks) {
-        chunks = std::min(g_override_chunks, kMaxChunks);
-    } else {
-        while (chunks * 2 <= kMaxChunks && clusters * chunks * 2 <= 160 && kps / (chunks * 2) >= 64) chunks *= 2;
-        if (chunks == 8 && clusters > kResidentClustersOf8) chunks = 4;
+    // Tile width and chunks per split: the cheapest by the model, with a
+    // penalty where the splits of a tile cannot share one resident cluster of
+    // a power-of-two size (the fused path then sums them through global
+    // memory).  The choice does not
+    // depend on `fused`, so both paths add the same chunks in the same order.
+    int best_bn = 0, best_c = 0;
+    double best = 1e30;
+    for (int bn : {64, 128, 256}) {
+        if (N % bn) continue;
+        if (g_override_bn && N % g_override_bn == 0 && bn != g_override_bn) continue;
+        for (int c : {1, 2, 4, 8}) {
+            if (g_override_chunks && c != g_override_chunks) continue;
+            int64_t len = (kps + c - 1) / c;
+            len = (len + grain - 1) / grain * grain;
+            if (!g_override_chunks && c > 1 && (c - 1) * len >= kps) continue;   // an always-empty chunk
+            const int nkb = static_cast<int>((len + kBlockK - 1) / kBlockK);
+            if (!pick_stages(bn, nkb, can3d, c, share_for(bn, c)).ok) continue;
+            const int64_t tiles = mt * (N / bn);
+            const int64_t sq = S * c;
+            const bool cluster_sum = sq <= kMaxChunks && (sq & (sq - 1)) == 0 &&
+                                     tiles <= resident_clusters(static_cast<int>(sq)) &&
+                                     pick_stages(bn, nkb, can3d, static_cast<int>(sq),
+                                                 share_for(bn, static_cast<int>(sq))).ok;
+            const double cost = model_us(M, N, S, bn, c, len, c) + (cluster_sum ? 0.0 : 1.5);
+            if (cost < best) {
+                best = cost;
+                best_bn = bn;
+                best_c = c;
+            }
+        }
     }
-    int share = 0, stages = 2;
-    int64_t chunk_len = 0;
-    for (;; chunks /= 2) {
-        chunk_len = (kps + chunks - 1) / chunks;
-        chunk_len = (chunk_len + 31) / 32 * 32;
-        const int64_t nkb = (chunk_len + kBlockK - 1) / kBlockK;
-        const int pieces = kTileM * bn / 4;
-        share = static_cast<int>(round_up((pieces + chunks - 1) / chunks, 8));
-        stages = static_cast<int>(std::max<int64_t>(2, std::min<int64_t>(nkb, kMaxStages)));
-        while (stages > 2 && smem_for(bn, stages, chunks, share) > kSmemLimit) --stages;
-        if (smem_for(bn, stages, chunks, share) <= kSmemLimit || chunks == 1) break;
+    if (best_bn == 0) {   // nothing fits the override: smallest tiles, one chunk
+        best_bn = 64;
+        best_c = 1;
     }
+    const int bn = best_bn, chunks = best_c;
+    int64_t chunk_len = (kps + chunks - 1) / chunks;
+    chunk_len = (chunk_len + grain - 1) / grain * grain;
+    const int nkb = static_cast<int>((chunk_len + kBlockK - 1) / kBlockK);
+    const int64_t tiles = mt * (N / bn);
+    int q = chunks, split_sum = 0;
+    if (fused) {
+        const int sq = static_cast<int>(S) * chunks;
+        split_sum = 1;
+        if (sq <= kMaxChunks && (sq & (sq - 1)) == 0 && tiles <= resident_clusters(sq) &&
+            pick_stages(bn, nkb, can3d, sq, share_for(bn, sq)).ok) {
+            q = sq;
+            split_sum = 2;
+        }
+    }
+    const int share = share_for(bn, q);
+    const StageChoice sc = pick_stages(bn, nkb, can3d, q, share);
+    TilePlan p = {};
     p.bn = bn;
     p.chunks = chunks;
     p.chunk_len = static_cast<int>(chunk_len);
-    p.stages = stages;
+    p.stages = sc.stages;
+    p.kbs = can3d ? sc.kbs : 1;
+    p.three_d = can3d && p.kbs > 1 ? 1 : 0;
     p.fused = fused ? 1 : 0;
-    p.cluster = chunks;
+    p.split_sum = split_sum;
+    p.cluster = q;
     p.share = share;
-    p.region0 = static_cast<uint32_t>(round_up(std::max(stages * stage_bytes(bn), epi_bytes(bn)), 1024));
+    p.region0 = static_cast<uint32_t>(round_up(std::max(p.stages * stage_bytes(bn, p.kbs), epi_bytes(bn)), 1024));
     p.grid = dim3(static_cast<unsigned>(N / bn), static_cast<unsigned>(mt), static_cast<unsigned>(S * chunks));
-    p.smem_bytes = smem_for(bn, stages, chunks, share);
+    p.smem_bytes = smem_for(bn, p.kbs, p.stages, q, share);
     return p;
 }
 
@@ -558,16 +739,19 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
 {
     if (plan.cluster > kMaxChunks || plan.stages > kMaxStages || plan.smem_bytes > kSmemLimit)
         return note_error(cudaErrorInvalidConfiguration, "tile plan out of range");
-    if (plan.fused && (pr.out == nullptr || pr.counters == nullptr))
+    if (plan.fused && (pr.out == nullptr || (plan.split_sum == 1 && pr.counters == nullptr)))
         return note_error(cudaErrorInvalidValue, "fused launch without output or counters");
     CUtensorMap ta, tb;
-    if (!encode_operand(&ta, pr.A, pr.M, pr.K, kTileM, pr.bf16) ||
-        !encode_operand(&tb, pr.B, pr.N, pr.K, plan.bn, pr.bf16))
-        return cudaErrorInvalidValue;
+    const bool ok = plan.three_d ? encode_operand_3d(&ta, pr.A, pr.M, pr.K, kTileM, plan.kbs, pr.bf16) &&
+                                       encode_operand_3d(&tb, pr.B, pr.N, pr.K, plan.bn, plan.kbs, pr.bf16)
+                                 : encode_operand(&ta, pr.A, pr.M, pr.K, kTileM, pr.bf16) &&
+                                       encode_operand(&tb, pr.B, pr.N, pr.K, plan.bn, pr.bf16);
+    if (!ok) return cudaErrorInvalidValue;
     TcArgs a = {};
     a.P = pr.P;
     a.out = plan.fused ? pr.out : nullptr;
-    a.counters = plan.fused ? pr.counters : nullptr;
+    a.counters = plan.split_sum == 1 ? pr.counters : nullptr;
+    a.split_sum = plan.split_sum;
     a.M = static_cast<int>(pr.M);
     a.N = static_cast<int>(pr.N);
     a.K = static_cast<int>(pr.K);
@@ -576,14 +760,16 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
     a.chunks = plan.chunks;
     a.chunk_len = plan.chunk_len;
     a.stages = plan.stages;
+    a.kbs = plan.kbs;
+    a.three_d = plan.three_d;
     a.share = plan.share;
     a.region0 = plan.region0;
     a.bf16 = pr.bf16 ? 1 : 0;
     a.wait_limit_ns = kWaitLimitNs;
     switch (plan.bn) {
-    case 64: return launch_chunks<64>(ta, tb, a, plan, stream);
-    case 128: return launch_chunks<128>(ta, tb, a, plan, stream);
-    case 256: return launch_chunks<256>(ta, tb, a, plan, stream);
+    case 64: return launch_cluster<64>(ta, tb, a, plan, stream);
+    case 128: return launch_cluster<128>(ta, tb, a, plan, stream);
+    case 256: return launch_cluster<256>(ta, tb, a, plan, stream);
     default: return note_error(cudaErrorInvalidConfiguration, "tile width");
     }
 }

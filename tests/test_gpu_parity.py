@@ -25,9 +25,9 @@ def lib():
 
     sk.build()
     sk.lib()
-    sk.splitk_set_tile_override(0, 0)
+    sk.splitk_set_tile_override(0, 0, 0)
     yield sk
-    sk.splitk_set_tile_override(0, 0)
+    sk.splitk_set_tile_override(0, 0, 0)
 
 
 WORKLOADS = [  # (M, N, K, splits, kps, dtype): the pages' workloads
@@ -217,7 +217,7 @@ def test_zero_first_row_and_split_independence(lib):
         assert max_scaled_error(o, outs[0], SO) <= 1e-5   # F32 accumulation, much tighter in practice
 
 
-TILINGS = [(bn, ch) for bn in (64, 128, 256) for ch in (1, 2, 4, 8)]
+TILINGS = [(bn, ch, kb) for bn in (64, 128, 256) for ch in (1, 2, 4, 8) for kb in (1, 2, 4)]
 
 
 @pytest.mark.parametrize("case", [(64, 128, 160, 3, 64, "bf16"), (256, 1024, 2048, 2, 1024, "bf16"),
@@ -232,8 +232,8 @@ def test_every_tiling(lib, case):
     A = device_operand(ops.A, dt)
     B = device_operand(ops.B, dt)
     try:
-        for bn, ch in TILINGS:
-            sk.splitk_set_tile_override(bn, ch)
+        for bn, ch, kb in TILINGS:
+            sk.splitk_set_tile_override(bn, ch, kb)
             P = Guarded(S * M * N)
             out = Guarded(M * N)
             fused = Guarded(M * N)
@@ -243,11 +243,11 @@ def test_every_tiling(lib, case):
             sk.gemm_bt(A, B, fused.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=1)
             assert sk.splitk_get_device_status() == 0
             assert P.guards_intact() and out.guards_intact() and fused.guards_intact()
-            assert max_scaled_error(P.numpy().reshape(S, M, N), Pr, SP) <= TOL_PARTIAL, (bn, ch)
-            assert max_scaled_error(out.numpy().reshape(M, N), Or, SO) <= TOL_FINAL[dt], (bn, ch)
-            assert np.array_equal(fused.numpy().view(np.uint32), out.numpy().view(np.uint32)), (bn, ch)
+            assert max_scaled_error(P.numpy().reshape(S, M, N), Pr, SP) <= TOL_PARTIAL, (bn, ch, kb)
+            assert max_scaled_error(out.numpy().reshape(M, N), Or, SO) <= TOL_FINAL[dt], (bn, ch, kb)
+            assert np.array_equal(fused.numpy().view(np.uint32), out.numpy().view(np.uint32)), (bn, ch, kb)
     finally:
-        sk.splitk_set_tile_override(0, 0)
+        sk.splitk_set_tile_override(0, 0, 0)
 
 
 def test_cuda_graph_capture_and_side_stream(lib):

@@ -156,14 +156,14 @@ def test_status_strings(L):
 
 
 def test_tile_override_validation(L):
-    for bn, ch in [(32, 0), (0, 3), (512, 1), (64, 32)]:
+    for bn, ch, kb in [(32, 0, 0), (0, 3, 0), (512, 1, 0), (64, 32, 0), (0, 0, 3), (0, 0, 8)]:
         with pytest.raises(sk.SplitKError):
-            sk.splitk_set_tile_override(bn, ch)
-    sk.splitk_set_tile_override(0, 0)
+            sk.splitk_set_tile_override(bn, ch, kb)
+    sk.splitk_set_tile_override(0, 0, 0)
 
 
 def test_describe_launch_plans(L):
-    sk.splitk_set_tile_override(0, 0)
+    sk.splitk_set_tile_override(0, 0, 0)
     d = sk.splitk_describe_launch(256, 1024, 2048, 2, 1024, "bf16", fused=0)
     assert d["path"] == 0 and d["kernels_per_call"] == 2
     assert d["grid_x"] * d["bn"] == 1024 and d["grid_y"] == 2
@@ -172,18 +172,27 @@ def test_describe_launch_plans(L):
     assert d["smem_bytes"] <= 227 * 1024
     f = sk.splitk_describe_launch(256, 1024, 2048, 2, 1024, "bf16", fused=1)
     assert f["fused_in_kernel"] == 1 and f["kernels_per_call"] == 1
-    assert f["cluster"] == f["chunks"] <= 8
+    # the headline's 2 splits x chunks share one cluster: the split sum stays on chip
+    assert f["split_sum"] == 2 and f["cluster"] == 2 * f["chunks"] <= 8
     # same chunking in both modes: the fused output equals the two-kernel output bitwise
     assert (f["bn"], f["chunks"], f["chunk_len"]) == (d["bn"], d["chunks"], d["chunk_len"])
     # F32 runs the FMA path, two kernels even when fused is asked for
     g = sk.splitk_describe_launch(96, 512, 2048, 4, 512, "f32", fused=1)
     assert g["path"] == 1 and g["kernels_per_call"] == 2
-    # any number of splits fuses: the splits meet through arrival counters
+    # any number of splits fuses: beyond one cluster the splits meet through
+    # arrival counters in the workspace
     h = sk.splitk_describe_launch(32, 64, 32 * 32, 32, 32, "bf16", fused=1)
-    assert h["fused_in_kernel"] == 1 and h["kernels_per_call"] == 1
+    assert h["fused_in_kernel"] == 1 and h["kernels_per_call"] == 1 and h["split_sum"] == 1
     for S in (1, 2, 4, 8, 16):
         e = sk.splitk_describe_launch(32, 512, 2048, S, 2048 // S, "f16", fused=1)
-        assert e["cluster"] == e["chunks"] <= 8 and e["smem_bytes"] <= 226 * 1024
+        assert e["smem_bytes"] <= 226 * 1024
+        if e["split_sum"] == 2:
+            assert e["cluster"] == S * e["chunks"] <= 8
+        else:
+            assert e["split_sum"] == 1 and e["cluster"] == e["chunks"] <= 8
+    # three splits: cluster sizes are powers of two, so the counters sum them
+    k = sk.splitk_describe_launch(64, 128, 160, 3, 64, "f16", fused=1)
+    assert k["split_sum"] == 1
 
 
 def test_describe_launch_override(L):
@@ -191,12 +200,18 @@ def test_describe_launch_override(L):
         sk.splitk_set_tile_override(64, 2)
         d = sk.splitk_describe_launch(64, 128, 160, 3, 64, "bf16")
         assert d["bn"] == 64 and d["chunks"] == 2 and d["chunk_len"] == 32
+        # K = 160 is not a multiple of 64: one k-block per stage, 2-D loads
+        assert d["kblocks_per_stage"] == 1 and d["three_d"] == 0
         # a width that does not divide N keeps the automatic width
         sk.splitk_set_tile_override(256, 1)
         d = sk.splitk_describe_launch(64, 128, 160, 3, 64, "bf16")
         assert d["bn"] in (64, 128)
+        # stages of 2 k-blocks as 3-D boxes where K and k_per_split allow it
+        sk.splitk_set_tile_override(128, 4, 2)
+        d = sk.splitk_describe_launch(256, 1024, 2048, 2, 1024, "bf16")
+        assert d["kblocks_per_stage"] == 2 and d["three_d"] == 1 and d["chunk_len"] % 64 == 0
     finally:
-        sk.splitk_set_tile_override(0, 0)
+        sk.splitk_set_tile_override(0, 0, 0)
 
 
 def test_unbuilt_library_fails_loudly(monkeypatch, tmp_path):
