@@ -74,6 +74,8 @@ typedef enum {
 
 #define SPLITK_MAX_DIM (1 << 22)
 #define SPLITK_MAX_SPLITS 4096
+/* Size of the scratch array gemm_bt_noalloc keeps in device memory. */
+#define SPLITK_NOALLOC_MAX_BYTES (32 << 20)
 
 /* Checks the contract's shape and split rules only (no pointers, no device
  * work).  Returns SPLITK_OK, SPLITK_ERR_SHAPE or SPLITK_ERR_SPLIT; the shape
@@ -130,6 +132,30 @@ int gemm_bt(const void *A, const void *B, float *out, void *workspace,
             size_t workspace_bytes, int64_t M, int64_t N, int64_t K,
             int64_t splits, int64_t k_per_split, int dtype, int fused,
             void *stream);
+
+/* gemm_bt for callers that cannot allocate device memory.  The paper has no
+ * counterpart of this entry point; it exists for hosts that hand an operator
+ * only its input and output buffers and forbid allocation while it runs (the
+ * execute callback of an inference-runtime plugin, for one) and for loops
+ * where cudaMalloc's implicit device synchronisation is not acceptable.
+ *   A, B, out, M, N, K, splits, k_per_split, dtype, fused, stream
+ *              as for gemm_bt; no workspace argument.
+ * Instead of a caller workspace it uses a scratch array of
+ * SPLITK_NOALLOC_MAX_BYTES (32 MiB) that the library keeps in device memory;
+ * every GPU that loads the library holds that array until the process exits.
+ * A shape whose gemm_bt_workspace_bytes() exceeds it is rejected with
+ * SPLITK_ERR_WORKSPACE before any device work (splitk_last_error() gives the
+ * sizes).  The call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.  Its first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Every call on a device
+ * shares the one array and leaves its contents behind (the partials); the
+ * fused path's counters are cleared at the start of each call.  Calls whose
+ * executions overlap on the GPU (on different streams, say) race on the
+ * array and must not be issued. */
+int gemm_bt_noalloc(const void *A, const void *B, float *out, int64_t M,
+                    int64_t N, int64_t K, int64_t splits, int64_t k_per_split,
+                    int dtype, int fused, void *stream);
 
 /* Reads and clears the device status word on the current device,
  * synchronising `stream` first.  Returns SPLITK_OK, SPLITK_ERR_DEVICE_TIMEOUT

@@ -25,8 +25,9 @@ EXPORTS = (
     "splitk_check_geometry", "gemm_splitk_bt", "splitk_reduce", "gemm_bt_workspace_bytes",
     "gemm_bt", "splitk_get_device_status", "splitk_status_string", "splitk_set_tile_override",
     "splitk_describe_launch", "splitk_selftest_bounded_wait", "splitk_last_error",
-    "gemm_bt_workspace_init",
+    "gemm_bt_workspace_init", "gemm_bt_noalloc",
 )
+NOALLOC_MAX_BYTES = 32 << 20   # SPLITK_NOALLOC_MAX_BYTES
 
 _lock = threading.Lock()
 _lib = None
@@ -64,10 +65,11 @@ def lib() -> ctypes.CDLL:
             L.splitk_describe_launch.argtypes = [i64, i64, i64, i64, i64, i32, i32, vp]
             L.splitk_selftest_bounded_wait.argtypes = [i64, vp]
             L.gemm_bt_workspace_init.argtypes = [vp, sz, vp]
+            L.gemm_bt_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, vp]
             L.splitk_last_error.argtypes = []
             L.splitk_last_error.restype = ctypes.c_char_p
             for name in ("splitk_check_geometry", "gemm_splitk_bt", "splitk_reduce", "gemm_bt",
-                         "gemm_bt_workspace_init",
+                         "gemm_bt_workspace_init", "gemm_bt_noalloc",
                          "splitk_get_device_status", "splitk_set_tile_override",
                          "splitk_describe_launch", "splitk_selftest_bounded_wait"):
                 getattr(L, name).restype = i32
@@ -152,6 +154,13 @@ def gemm_bt(A, B, out, workspace, workspace_bytes, M, N, K, splits, k_per_split,
             stream=None) -> None:
     _check(lib().gemm_bt(_ptr(A), _ptr(B), _ptr(out), _ptr(workspace), workspace_bytes, M, N, K,
                          splits, k_per_split, dtype_code(dtype), fused, _stream(stream)), "gemm_bt")
+
+
+def gemm_bt_noalloc(A, B, out, M, N, K, splits, k_per_split, dtype, fused=0, stream=None) -> None:
+    """gemm_bt without a workspace argument, for callers that cannot allocate:
+    the library's own device scratch array serves instead (see splitk.h)."""
+    _check(lib().gemm_bt_noalloc(_ptr(A), _ptr(B), _ptr(out), M, N, K, splits, k_per_split,
+                                 dtype_code(dtype), fused, _stream(stream)), "gemm_bt_noalloc")
 
 
 def splitk_get_device_status(stream=None) -> int:
