@@ -42,6 +42,29 @@ BYTES_GEMM = M * K * 2 + N * K * 2 + SPLITS * M * N * 4                     # A+
 BYTES_REDUCE = SPLITS * M * N * 4 + M * N * 4                               # P read, out write
 
 
+def kernel_traffic():
+    """DRAM bytes per launch of the tensor-core kernel from the committed ncu
+    record, or None when the kernel sources changed since it was taken."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "tc_splitk_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    rec = {}
+    with open(path) as f:
+        for line in f:
+            if "=" in line and not line.lstrip().startswith("#"):
+                k, v = line.split("=", 1)
+                rec[k.strip()] = v.strip()
+    h = hashlib.sha256()
+    for src in rec.get("sources", "").split():
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec.get("sources_sha256"):
+        return None
+    return int(rec["dram_bytes_per_launch"])
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -332,7 +355,7 @@ def run_ours(args, rank, world, dev, torch, dist):
             "peak": f"{peak_kind} {hbm} GB/s"},
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1),
                      "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "traffic": None, "bytes_per_launch": dom_bytes,
+                     "traffic": kernel_traffic() if fused else None, "bytes_per_launch": dom_bytes,
                      "launch_us": round(dom_us, 4), "peak_kind": peak_kind},
         "kernels_us": {"partial_pass": round(gemm_us, 4), "reduce": round(red_us, 4),
                        "two_pass_op": round(two_pass_us, 4),
