@@ -119,15 +119,21 @@ int gemm_bt_workspace_init(void *workspace, size_t workspace_bytes, void *stream
 /* One call: the partial pass then the accumulation pass, on one stream.
  *   out        device, [M,N] F32; fully overwritten
  *   workspace  device, >= gemm_bt_workspace_bytes() bytes, caller-owned
- *              scratch; may not overlap A, B or out.  After the call it holds
- *              the partials [splits,M,N] in its first bytes.
- *   fused      0: two kernels (gemm_splitk_bt, then splitk_reduce);
- *              1: one kernel: the last split to finish each piece of a tile
- *                 adds the splits in split order and writes `out`; needs the
- *                 workspace zeroed once (gemm_bt_workspace_init).  With F32
- *                 operands the two-kernel path runs instead.
- * For a given shape, `out` and the partials are bitwise the same for both
- * values of `fused`. */
+ *              scratch; may not overlap A, B or out.
+ *   fused      0: two kernels (gemm_splitk_bt, then splitk_reduce); the
+ *                 workspace then holds the partials [splits,M,N] in its
+ *                 first bytes;
+ *              1: one kernel: the splits are summed inside the launch (in the
+ *                 thread-block cluster when a tile's splits fit one cluster,
+ *                 else by the last split to finish each piece, through
+ *                 arrival counters in the workspace); the partials are not
+ *                 kept;
+ *              3: as 1, and the workspace also holds the partials afterwards.
+ *              Fused calls need the workspace zeroed once before the first
+ *              of them (gemm_bt_workspace_init).  With F32 operands the
+ *              two-kernel path runs instead.
+ * For a given shape, `out` (and the partials, where kept) are bitwise the
+ * same for every value of `fused`. */
 int gemm_bt(const void *A, const void *B, float *out, void *workspace,
             size_t workspace_bytes, int64_t M, int64_t N, int64_t K,
             int64_t splits, int64_t k_per_split, int dtype, int fused,

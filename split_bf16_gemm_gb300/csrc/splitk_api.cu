@@ -172,7 +172,7 @@ int gemm_bt(const void *A, const void *B, float *out, void *workspace, size_t wo
 {
     int st = validate_gemm(A, B, M, N, K, splits, k_per_split, dtype);
     if (st != SPLITK_OK) return st;
-    if (fused != 0 && fused != 1) return SPLITK_ERR_CONFIG;
+    if (fused != 0 && fused != 1 && fused != 3) return SPLITK_ERR_CONFIG;
     if (!out || !workspace) return SPLITK_ERR_NULL;
     if (!aligned16(out) || !aligned16(workspace)) return SPLITK_ERR_ALIGN;
     const size_t ws_need = gemm_bt_workspace_bytes(M, N, K, splits, k_per_split, fused);
@@ -187,8 +187,12 @@ int gemm_bt(const void *A, const void *B, float *out, void *workspace, size_t wo
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float *P = static_cast<float *>(workspace);
     unsigned *counters = reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + partials_bytes(M, N, splits));
-    if (fused && fused_possible(dtype))
-        return run_partial_pass(A, B, P, out, counters, M, N, K, splits, k_per_split, dtype, true, s);
+    if (fused && fused_possible(dtype)) {
+        // fused == 1 keeps no partials where the cluster sums the splits on chip
+        const TilePlan plan = splitk::plan_tc(M, N, K, splits, k_per_split, true);
+        float *keep = (fused == 1 && plan.split_sum == 2) ? nullptr : P;
+        return run_partial_pass(A, B, keep, out, counters, M, N, K, splits, k_per_split, dtype, true, s);
+    }
     st = run_partial_pass(A, B, P, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false, s);
     if (st != SPLITK_OK) return st;
     return cuda_status(splitk::launch_reduce(P, out, splits, M * N, s));

@@ -57,7 +57,7 @@ constexpr int kThreads = 256;                     // 8 warps: two per tensor-mem
 constexpr int kBatch = 8;                          // pieces per thread per pass of the split sum
 
 struct TcArgs {
-    float *P;              // [S,M,N] partials
+    float *P;              // [S,M,N] partials (nullptr: not kept, when the cluster sums the splits)
     float *out;            // [M,N], or nullptr when the splits are not summed here
     unsigned *counters;    // per (tile, chunk) arrival counters (split sum by counters)
     int M, N, K, S, kps;
@@ -197,7 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
-    if (Q > 1) ptx::cluster_arrive();               // publishes this CTA's barrier set-up to the cluster
+    // the barrier inits were published by thread 0's fence.mbarrier_init; the
+    // arrival itself needs no release semantics
+    if (Q > 1) ptx::cluster_arrive_relaxed();
     ptx::grid_dependency_wait();
     ptx::launch_dependents();
     const uint32_t tmem = tmem_slot;
@@ -338,9 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<float4 *>(Ps + static_cast<size_t>(row) * args.N + col0 + p.col) = acc;
         }
     } else {
+        const int cmask = C - 1, cshift = __ffs(C) - 1;
         // the cluster holds every split of the tile (rank = split * C + chunk):
         // each split's chunk sum in chunk order, then the splits in split order,
-        // the same additions the reduce kernel makes on the same partials
+        // the same additions the reduce kernel makes on the same partials (which
+        // are also stored when P is given)
         for (int g = my_lo + tid; g < my_hi; g += kThreads) {
             const Piece p = piece_at(g);
             const int row = row0 + p.row;
@@ -350,14 +354,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             float4 part = v[0], tot = v[0];
 #pragma unroll
             for (int r = 0; r < Q; ++r) {
-                const int cc = r % C;
+                const int cc = r & cmask;       // C is a power of two
                 if (cc == 0)
                     part = v[r];
                 else
                     add4(part, v[r]);
-                if (cc == C - 1) {
-                    const int sp = r / C;
-                    if (row < args.M) *reinterpret_cast<float4 *>(args.P + sp * MN + elem) = part;
+                if (cc == cmask) {
+                    const int sp = r >> cshift;
+                    if (args.P != nullptr && row < args.M) *reinterpret_cast<float4 *>(args.P + sp * MN + elem) = part;
                     if (sp == 0)
                         tot = part;
                     else
@@ -500,10 +504,6 @@ size_t stage_bytes(int bn, int kbs) { return static_cast<size_t>(kTileM + bn) * 
 size_t epi_bytes(int bn) { return static_cast<size_t>(kTileM) * bn * 4; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr size_t kSmemLimit = 226 * 1024;   // dynamic; leaves room for static shared memory
-// A GB300 keeps at most 15 clusters of 8 CTAs resident at once (measured with
-// cudaOccupancyMaxActiveClusters: one CTA per SM per cluster rank); clusters
-// of 4 fit 36 at once.
-constexpr int kResidentClustersOf8 = 15;
 
 // Dynamic shared memory of a plan: the stage ring (or the accumulator
 // staging, if larger), one receive slot per peer, and 1 KB of alignment slack.
@@ -741,6 +741,8 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
         return note_error(cudaErrorInvalidConfiguration, "tile plan out of range");
     if (plan.fused && (pr.out == nullptr || (plan.split_sum == 1 && pr.counters == nullptr)))
         return note_error(cudaErrorInvalidValue, "fused launch without output or counters");
+    if (pr.P == nullptr && plan.split_sum != 2)
+        return note_error(cudaErrorInvalidValue, "partials are needed unless the cluster sums the splits");
     CUtensorMap ta, tb;
     const bool ok = plan.three_d ? encode_operand_3d(&ta, pr.A, pr.M, pr.K, kTileM, plan.kbs, pr.bf16) &&
                                        encode_operand_3d(&tb, pr.B, pr.N, pr.K, plan.bn, plan.kbs, pr.bf16)

@@ -94,14 +94,15 @@ def test_nan_poison(lib, case):
 
 @pytest.mark.parametrize("case", WORKLOADS + SWEEP[::3] + CATEGORIES, ids=ids(WORKLOADS + SWEEP[::3] + CATEGORIES))
 def test_gemm_bt_both_modes_bitwise(lib, case):
-    """gemm_bt with fused = 0 and 1 gives the two-kernel output bit for bit and
-    leaves gemm_splitk_bt's partials in the workspace."""
+    """gemm_bt with fused = 0, 1 and 3 gives the two-kernel output bit for bit;
+    fused = 0 and 3 leave gemm_splitk_bt's partials in the workspace."""
     sk = lib
     M, N, K, S, kps, dt = case
     A, B, P, out = check_case(sk, case)
     ref_out = out.numpy()
     ref_P = P.numpy()
-    for fused in (0, 1):
+    plan = sk.splitk_describe_launch(M, N, K, S, kps, dt, fused=1)
+    for fused in (0, 1, 3):
         ws, nbytes = workspace(M, N, K, S, kps)
         o = Guarded(M * N)
         sk.gemm_bt(A, B, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=fused)
@@ -109,7 +110,10 @@ def test_gemm_bt_both_modes_bitwise(lib, case):
         assert o.guards_intact() and ws.guards_intact()
         assert np.array_equal(o.numpy().view(np.uint32), ref_out.view(np.uint32)), f"fused={fused}"
         w = ws.numpy()
-        assert np.array_equal(w[:S * M * N].view(np.uint32), ref_P.view(np.uint32)), f"fused={fused}"
+        if fused in (0, 3) or plan["split_sum"] != 2:
+            assert np.array_equal(w[:S * M * N].view(np.uint32), ref_P.view(np.uint32)), f"fused={fused}"
+        else:
+            assert np.all(w[:S * M * N] == 7.0), "fused=1 with the split sum on chip keeps no partials"
         assert np.all(w[S * M * N:] == 0), "the counters must be back at zero"
 
 

@@ -133,7 +133,8 @@ def test_gemm_bt_rejections(L):
     assert call(out=A0) == bd.ERR_ALIAS
     assert call(ws=O0) == bd.ERR_ALIAS
     assert call(ws=B0 + 64) == bd.ERR_ALIAS
-    assert call(fused=3) == bd.ERR_CONFIG
+    assert call(fused=2) == bd.ERR_CONFIG
+    assert call(fused=4) == bd.ERR_CONFIG
     # the fused path keeps the partials and its counters in the workspace too
     assert call(ws=0, fused=1) == bd.ERR_NULL
     assert call(wsb=0, fused=1) == bd.ERR_WORKSPACE
