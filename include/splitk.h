@@ -94,6 +94,17 @@ int gemm_splitk_bt(const void *A, const void *B, float *partials, int64_t M,
                    int64_t N, int64_t K, int64_t splits, int64_t k_per_split,
                    int dtype, void *stream);
 
+/* Weight preparation (pages: "Wider consecutive-weight NAX GEMM", section
+ * "Performance method" -- the transposed layout is prepared once, outside
+ * timing, and kept resident): B[n,k] = W[k,n].
+ *   W  device, [K,N] row-major, element type `dtype` (bits copied as they are)
+ *   B  device, [N,K] row-major, same type; fully overwritten
+ * K a positive multiple of 32 and N of 64 (the GEMM's contract for B),
+ * 16-byte aligned pointers, no overlap; else SPLITK_ERR_SHAPE / _DTYPE /
+ * _NULL / _ALIGN / _ALIAS before any device work. */
+int splitk_prepare_bt(const void *W, void *B, int64_t K, int64_t N, int dtype,
+                      void *stream);
+
 /* The accumulation pass: out[i] = (((P[0][i] + P[1][i]) + P[2][i]) + ...) in
  * F32, in split order s = 0..splits-1.
  *   partials  device, [splits,M,N] F32, read only

@@ -17,7 +17,10 @@ NAX GEMM" (section "Launch contract and correctness"):
 * ``contract``: 0 for a legal geometry, 1 when the shape rule fails (M, K, kps
   positive multiples of 32, N of 64), 2 when the split rule fails (each split
   starts below K, together they cover K);
-* ``decode``: the element formats' field definitions.
+* ``decode``: the element formats' field definitions;
+* ``transpose``: the weight preparation B[n,k] = W[k,n] ("Wider consecutive-
+  weight NAX GEMM", section "Performance method": the transposed layout is
+  prepared once, outside timing).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (brute force, closed forms, library cross-checks and invariants); none is
@@ -69,6 +72,8 @@ def _load():
             lib.oracle_decode.argtypes = [i32, vp, i64, vp]
             lib.oracle_contract.argtypes = [i64, i64, i64, i64, i64]
             lib.oracle_split_range.argtypes = [i64, i64, i64, vp, vp]
+            lib.oracle_transpose.argtypes = [i32, vp, i64, i64, vp]
+            lib.oracle_transpose.restype = i32
             lib.oracle_partials.argtypes = [i32, vp, vp, i64, i64, i64, i64, i64, vp, vp, i32]
             lib.oracle_output.argtypes = [i32, vp, vp, i64, i64, i64, vp, vp, i32]
             lib.oracle_points.argtypes = [i32, vp, vp, i64, i64, i64, i64, i64, i64,
@@ -109,6 +114,17 @@ def decode(bits: np.ndarray, dtype: str) -> np.ndarray:
     rc = _load().oracle_decode(code, _ptr(b), b.size, _ptr(out))
     if rc:
         raise ValueError(f"oracle_decode failed ({rc})")
+    return out
+
+
+def transpose(W: np.ndarray) -> np.ndarray:
+    """Row-major W[K,N] (2- or 4-byte elements) -> row-major B[N,K], bits copied."""
+    w = np.ascontiguousarray(W)
+    rows, cols = w.shape
+    out = np.empty((cols, rows), w.dtype)
+    rc = _load().oracle_transpose(w.dtype.itemsize, _ptr(w), rows, cols, _ptr(out))
+    if rc:
+        raise ValueError(f"oracle_transpose failed ({rc})")
     return out
 
 

@@ -22,6 +22,10 @@
  *   O[m,n]    = sum_{k=0}^{K-1}   A[m,k]*B[n,k]      unsplit product, in F64
  *   SO[m,n]   = sum_{k=0}^{K-1}   |A[m,k]*B[n,k]|
  *
+ * Weight preparation (the pages keep the transposed weight resident, prepared
+ * once outside timing: "Wider consecutive-weight NAX GEMM", section
+ * "Performance method") is the plain transpose B[n,k] = W[k,n], oracle_transpose.
+ *
  * Inputs arrive as the bit patterns the GPU sees (binary16, bfloat16 or
  * binary32) and are decoded here from each format's field definition
  * (sign, biased exponent, fraction), not by reinterpreting memory.
@@ -136,6 +140,24 @@ void oracle_split_range(int64_t K, int64_t kps, int64_t s, int64_t *k0, int64_t 
     if (lo > K) lo = K;
     *k0 = lo;
     *k1 = hi;
+}
+
+/* ------------------------------------------------------ weight preparation */
+
+/* dst[c][r] = src[r][c] for a row-major rows x cols matrix of elem_bytes-byte
+ * elements (copied as bits).  Returns 0, or -1 for an element size other than
+ * 2 or 4. */
+int oracle_transpose(int elem_bytes, const void *src, int64_t rows, int64_t cols, void *dst)
+{
+    const unsigned char *s = (const unsigned char *)src;
+    unsigned char *d = (unsigned char *)dst;
+    int64_t r, c;
+    if (elem_bytes != 2 && elem_bytes != 4) return -1;
+    for (r = 0; r < rows; ++r)
+        for (c = 0; c < cols; ++c)
+            memcpy(d + (size_t)(c * rows + r) * elem_bytes, s + (size_t)(r * cols + c) * elem_bytes,
+                   (size_t)elem_bytes);
+    return 0;
 }
 
 /* ---------------------------------------------------------------- products */

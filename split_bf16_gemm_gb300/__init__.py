@@ -12,6 +12,6 @@ from .binding import (  # noqa: F401
     gemm_bt_workspace_init,
     gemm_splitk_bt,
     lib, splitk_check_geometry, splitk_describe_launch, splitk_get_device_status, splitk_reduce,
-    splitk_last_error, splitk_selftest_bounded_wait, splitk_set_tile_override, splitk_status_string,
+    splitk_last_error, splitk_prepare_bt, splitk_selftest_bounded_wait, splitk_set_tile_override, splitk_status_string,
     status_string,
 )

@@ -25,7 +25,7 @@ EXPORTS = (
     "splitk_check_geometry", "gemm_splitk_bt", "splitk_reduce", "gemm_bt_workspace_bytes",
     "gemm_bt", "splitk_get_device_status", "splitk_status_string", "splitk_set_tile_override",
     "splitk_describe_launch", "splitk_selftest_bounded_wait", "splitk_last_error",
-    "gemm_bt_workspace_init", "gemm_bt_noalloc",
+    "gemm_bt_workspace_init", "gemm_bt_noalloc", "splitk_prepare_bt",
 )
 NOALLOC_MAX_BYTES = 32 << 20   # SPLITK_NOALLOC_MAX_BYTES
 
@@ -66,10 +66,11 @@ def lib() -> ctypes.CDLL:
             L.splitk_selftest_bounded_wait.argtypes = [i64, vp]
             L.gemm_bt_workspace_init.argtypes = [vp, sz, vp]
             L.gemm_bt_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, vp]
+            L.splitk_prepare_bt.argtypes = [vp, vp, i64, i64, i32, vp]
             L.splitk_last_error.argtypes = []
             L.splitk_last_error.restype = ctypes.c_char_p
             for name in ("splitk_check_geometry", "gemm_splitk_bt", "splitk_reduce", "gemm_bt",
-                         "gemm_bt_workspace_init", "gemm_bt_noalloc",
+                         "gemm_bt_workspace_init", "gemm_bt_noalloc", "splitk_prepare_bt",
                          "splitk_get_device_status", "splitk_set_tile_override",
                          "splitk_describe_launch", "splitk_selftest_bounded_wait"):
                 getattr(L, name).restype = i32
@@ -134,6 +135,12 @@ def splitk_check_geometry(M, N, K, splits, k_per_split) -> int:
 def gemm_splitk_bt(A, B, partials, M, N, K, splits, k_per_split, dtype, stream=None) -> None:
     _check(lib().gemm_splitk_bt(_ptr(A), _ptr(B), _ptr(partials), M, N, K, splits, k_per_split,
                                 dtype_code(dtype), _stream(stream)), "gemm_splitk_bt")
+
+
+def splitk_prepare_bt(W, B, K, N, dtype, stream=None) -> None:
+    """Weight preparation: B[n,k] = W[k,n] (W row-major [K,N], B row-major [N,K])."""
+    _check(lib().splitk_prepare_bt(_ptr(W), _ptr(B), K, N, dtype_code(dtype), _stream(stream)),
+           "splitk_prepare_bt")
 
 
 def splitk_reduce(partials, out, splits, M, N, stream=None) -> None:

@@ -152,6 +152,19 @@ int splitk_reduce(const float *partials, float *out, int64_t splits, int64_t M, 
     return cuda_status(splitk::launch_reduce(partials, out, splits, M * N, static_cast<cudaStream_t>(stream)));
 }
 
+int splitk_prepare_bt(const void *W, void *B, int64_t K, int64_t N, int dtype, void *stream)
+{
+    // the B that the GEMM's contract accepts: K a positive multiple of 32, N of 64
+    if (K <= 0 || K % 32 || N <= 0 || N % 64 || K > SPLITK_MAX_DIM || N > SPLITK_MAX_DIM) return SPLITK_ERR_SHAPE;
+    const int e = elem_bytes(dtype);
+    if (e == 0) return SPLITK_ERR_DTYPE;
+    if (!W || !B) return SPLITK_ERR_NULL;
+    if (!aligned16(W) || !aligned16(B)) return SPLITK_ERR_ALIGN;
+    const uint64_t bytes = static_cast<uint64_t>(K * N) * e;
+    if (overlap(range_of(W, bytes), range_of(B, bytes))) return SPLITK_ERR_ALIAS;
+    return cuda_status(splitk::launch_prepare(W, B, K, N, e, static_cast<cudaStream_t>(stream)));
+}
+
 size_t gemm_bt_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t splits, int64_t k_per_split, int fused)
 {
     (void)fused;

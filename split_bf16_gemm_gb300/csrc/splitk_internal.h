@@ -58,6 +58,7 @@ cudaError_t launch_tc(const GemmProblem &p, const TilePlan &plan, cudaStream_t s
 cudaError_t launch_simt_f32(const float *A, const float *B, float *P, int64_t M, int64_t N, int64_t K,
                             int64_t S, int64_t kps, cudaStream_t stream);
 cudaError_t launch_reduce(const float *P, float *out, int64_t S, int64_t count, cudaStream_t stream);
+cudaError_t launch_prepare(const void *W, void *B, int64_t K, int64_t N, int elem_bytes, cudaStream_t stream);
 
 // Last-error record (per host thread): what failed and the CUDA error or
 // driver result it returned.  note_error passes `e` through.

@@ -7,8 +7,11 @@
 // thread owns 16-byte pieces of the output, loads the S partial pieces
 // (independent 16-byte loads, all in flight together) and adds them in split
 // order s = 0, 1, ..., S-1 in F32, starting from P[0] itself.  The grid is a
-// multiple of the SM count with a grid-stride loop.
+// multiple of the SM count with a grid-stride loop.  Launched as a
+// programmatic dependent of the partial pass: its blocks start while the
+// partial pass finishes and wait (griddepcontrol.wait) for it before reading.
 
+#include "ptx.cuh"
 #include "splitk_internal.h"
 
 namespace splitk {
@@ -25,6 +28,8 @@ __device__ __forceinline__ float4 ld_stream(const float4 *p)
 __global__ void __launch_bounds__(kReduceThreads)
     reduce_v4_kernel(const float4 *__restrict__ P, float4 *__restrict__ out, int S, int64_t n4)
 {
+    ptx::grid_dependency_wait();   // the partials may be the previous grid's output
+    ptx::launch_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kReduceThreads;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kReduceThreads + threadIdx.x; i < n4; i += stride) {
         float4 acc = ld_stream(P + i);
@@ -50,6 +55,8 @@ __global__ void __launch_bounds__(kReduceThreads)
 __global__ void __launch_bounds__(kReduceThreads)
     reduce_scalar_kernel(const float *__restrict__ P, float *__restrict__ out, int S, int64_t n)
 {
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kReduceThreads;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kReduceThreads + threadIdx.x; i < n; i += stride) {
         float acc = P[i];
@@ -80,12 +87,22 @@ cudaError_t launch_reduce(const float *P, float *out, int64_t S, int64_t count, 
     int64_t blocks = want < cap ? want : cap;
     if (blocks > sms) blocks = (blocks + sms - 1) / sms * sms;
     if (blocks < 1) blocks = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(kReduceThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
     if (vec)
-        reduce_v4_kernel<<<static_cast<unsigned>(blocks), kReduceThreads, 0, stream>>>(
-            reinterpret_cast<const float4 *>(P), reinterpret_cast<float4 *>(out), static_cast<int>(S), items);
+        e = cudaLaunchKernelEx(&cfg, reduce_v4_kernel, reinterpret_cast<const float4 *>(P),
+                               reinterpret_cast<float4 *>(out), static_cast<int>(S), items);
     else
-        reduce_scalar_kernel<<<static_cast<unsigned>(blocks), kReduceThreads, 0, stream>>>(P, out, static_cast<int>(S),
-                                                                                           items);
+        e = cudaLaunchKernelEx(&cfg, reduce_scalar_kernel, P, out, static_cast<int>(S), items);
+    if (e != cudaSuccess) return note_error(e, "reduce kernel launch");
     return note_error(cudaGetLastError(), "reduce kernel launch");
 }
 

@@ -126,6 +126,13 @@ def unit_rows_a(M: int, N: int, K: int, dtype: str, seed: int = 0) -> Operands:
     return Operands(_round(a, dtype), u.B, dtype, seed, "A rows = e_(m mod K), uniform B")
 
 
+def weight_kn(K: int, N: int, dtype: str, seed: int = 0) -> np.ndarray:
+    """An unprepared weight W[K,N] (row-major), uniform[-1,1], rounded like
+    the operands: the input of the weight preparation B[n,k] = W[k,n]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return _round(rng.uniform(-1.0, 1.0, size=(K, N)).astype(np.float32), dtype)
+
+
 def to_f32(bits: np.ndarray, dtype: str) -> np.ndarray:
     """Widen bit patterns to float32 values (for building torch tensors)."""
     return _to_f32(np.asarray(bits), dtype)

@@ -290,3 +290,45 @@ def test_bounded_wait_reports_and_context_survives(lib):
     assert sk.splitk_selftest_bounded_wait(2_000_000) == bd.ERR_DEVICE_TIMEOUT
     assert sk.splitk_get_device_status() == 0          # read-and-clear
     check_case(sk, (32, 64, 128, 2, 64, "bf16"))        # the context is still usable
+
+
+PREP_CASES = [(32, 64, "bf16"), (160, 128, "f16"), (96, 320, "f32"), (2048, 1024, "bf16"), (4096, 2048, "f16")]
+
+
+@pytest.mark.parametrize("case", PREP_CASES, ids=[f"{c[2]}-K{c[0]}N{c[1]}" for c in PREP_CASES])
+def test_prepare_matches_oracle_bitwise(lib, case):
+    """Weight preparation B[n,k] = W[k,n] equals the oracle's transpose bit for
+    bit, leaves the guards behind B intact, and a GEMM on the prepared weight
+    equals one on the oracle-prepared weight bit for bit."""
+    import oracle
+    import splitk_inputs as gen
+
+    sk = lib
+    K, N, dt = case
+    w = gen.weight_kn(K, N, dt, seed=K ^ N)
+    ref = oracle.transpose(w)
+    W = device_operand(w, dt)
+    esz = 4 if dt == "f32" else 2
+    guard_words = 64
+    Bbuf = torch.full((N * K * esz // 4 + guard_words,), 7.0, dtype=torch.float32, device="cuda")
+    Bbuf[N * K * esz // 4:] = 11.0
+    B = Bbuf[:N * K * esz // 4].view(torch.int32)
+    sk.splitk_prepare_bt(W, B, K, N, dt)
+    torch.cuda.synchronize()
+    got = B.cpu().numpy().view(np.uint8)
+    assert np.array_equal(got, np.ascontiguousarray(ref).view(np.uint8).reshape(-1))
+    assert torch.all(Bbuf[N * K * esz // 4:] == 11.0)
+    if K >= 64 and dt != "f32":
+        M = 96
+        kps = -(-(K // 2) // 32) * 32          # two splits where K allows, k_per_split a multiple of 32
+        S = -(-K // kps)
+        ops = gen.uniform(M, N, K, dt, seed=1)
+        A = device_operand(ops.A, dt)
+        Bdev = B.view(torch.bfloat16 if dt == "bf16" else torch.float16).view(N, K)
+        Bref = device_operand(ref, dt)
+        o1, o2 = Guarded(M * N), Guarded(M * N)
+        ws, nbytes = workspace(M, N, K, S, kps)
+        sk.gemm_bt(A, Bdev, o1.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=0)
+        sk.gemm_bt(A, Bref, o2.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=0)
+        assert np.array_equal(o1.numpy().view(np.uint32), o2.numpy().view(np.uint32))
+    assert sk.splitk_get_device_status() == 0

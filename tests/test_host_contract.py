@@ -220,3 +220,16 @@ def test_unbuilt_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(bd, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         bd.lib()
+
+
+def test_prepare_rejections(L):
+    W, B = 0x10000000, 0x20000000
+    assert L.splitk_prepare_bt(W, B, 48, 64, bd.BF16, None) == bd.ERR_SHAPE
+    assert L.splitk_prepare_bt(W, B, 64, 96, bd.BF16, None) == bd.ERR_SHAPE
+    assert L.splitk_prepare_bt(W, B, 0, 64, bd.BF16, None) == bd.ERR_SHAPE
+    assert L.splitk_prepare_bt(W, B, 64, 64, 9, None) == bd.ERR_DTYPE
+    assert L.splitk_prepare_bt(0, B, 64, 64, bd.BF16, None) == bd.ERR_NULL
+    assert L.splitk_prepare_bt(W, 0, 64, 64, bd.BF16, None) == bd.ERR_NULL
+    assert L.splitk_prepare_bt(W + 2, B, 64, 64, bd.BF16, None) == bd.ERR_ALIGN
+    # W is 64 * 64 * 2 = 8 KiB; a B starting inside it overlaps
+    assert L.splitk_prepare_bt(W, W + 8192 - 16, 64, 64, bd.BF16, None) == bd.ERR_ALIAS

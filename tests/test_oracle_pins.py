@@ -361,3 +361,21 @@ def test_golden_int_tile(orc):
     assert np.array_equal(P, P_ref) and np.array_equal(O, O_ref)
     # exact integers: the two split slabs add up to the unsplit product
     assert np.array_equal(P_ref.sum(axis=0), O_ref)
+
+
+# ------------------------------------------------------- weight preparation
+
+
+def test_transpose_worked_example(orc):
+    w = np.array([[1, 2, 3, 4], [5, 6, 7, 8], [9, 10, 11, 12]], np.uint16)
+    assert orc.transpose(w).tolist() == [[1, 5, 9], [2, 6, 10], [3, 7, 11], [4, 8, 12]]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_transpose_matches_numpy_and_inverts(orc, dtype):
+    for K, N in [(32, 64), (160, 128), (96, 320), (2048, 1024)]:
+        w = gen.weight_kn(K, N, dtype, seed=K + N)
+        b = orc.transpose(w)
+        assert b.shape == (N, K)
+        assert np.array_equal(b, np.ascontiguousarray(w.T))           # library routine
+        assert np.array_equal(orc.transpose(b), w)                    # transposing twice
