@@ -212,6 +212,21 @@ def make_pool(torch, n_inst, dev):
     return pool
 
 
+def job_time(ms_local, steps, pack, world, dist=None, device="cpu"):
+    """The job's timed region is the slowest rank's (max over ranks); the
+    value is microseconds per operation over every rank's operations (each
+    rank runs `steps` steps of `pack` independent operations: weak scaling).
+    Returns (ms, us_per_op)."""
+    ms = float(ms_local)
+    if dist is not None and world > 1:
+        import torch
+
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, ms * 1e3 / (steps * pack * world)
+
+
 def capture(torch, stream, fn):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
@@ -281,14 +296,10 @@ def run_ours(args, rank, world, dev, torch, dist):
     with ClockSampler(nvml_index(torch, dev)) as clocks:
         ms = time_graphs(torch, stream, graphs, args.steps)
     torch.cuda.synchronize()
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, us_per_op = job_time(ms, args.steps, pack, world, dist, dev)
     if sk.splitk_get_device_status(stream) != 0:
         raise RuntimeError("a kernel's bounded wait ran out during the timed region")
     ms_per_step = ms / args.steps
-    us_per_op = ms * 1e3 / (args.steps * pack * world)
 
     if args.profile:
         return {"metric": METRIC, "value": round(us_per_op, 4), "unit": "µs/op", "profile_run": True,
