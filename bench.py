@@ -11,7 +11,8 @@ workspace), drawn from a pool of 40 instances whose inputs (200 MB) exceed the
 
 Printed (one JSON line, rank 0): value = microseconds per operation (lower is
 better), the roofline of the dominant kernel measured live with CUDA events,
-the end-to-end figure through the public API with host buffers, the clocks
+the end-to-end figure through the C ABI with host buffers (gemm_bt_host_batch:
+activations in and results out every step, pipelined), the clocks
 seen during the timed region, and the CPU oracle's time for the same work.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -204,11 +205,10 @@ def make_pool(torch, n_inst, dev):
         ops = gen.uniform(M, N, K, DTYPE, seed=i)
         A = torch.from_numpy(ops.A.view(np.int16)).to(dev).view(torch.bfloat16)
         B = torch.from_numpy(ops.B.view(np.int16)).to(dev).view(torch.bfloat16)
-        pool.append({"A_host": torch.from_numpy(ops.A.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        pool.append({"A_host": torch.from_numpy(ops.A.view(np.int16)).view(torch.bfloat16),
                      "A": A, "B": B,
                      "out": torch.empty((M, N), dtype=torch.float32, device=dev),
-                     "ws": torch.empty((SPLITS * M * N,), dtype=torch.float32, device=dev),
-                     "out_host": torch.empty((M, N), dtype=torch.float32).pin_memory()})
+                     "ws": torch.empty((SPLITS * M * N,), dtype=torch.float32, device=dev)})
     return pool
 
 
@@ -244,6 +244,66 @@ def time_graphs(torch, stream, graphs, steps):
         stop.record(stream)
     stop.synchronize()
     return start.elapsed_time(stop)   # ms
+
+
+def measure_e2e(sk, torch, stream, groups, pack, fused, steps):
+    """µs/op through gemm_bt_host_batch: per step one group's `pack`
+    activations come from pinned host memory and its results go back to
+    pinned host memory, all inside the timed region (CUDA events on the
+    caller's stream, which the call joins).  Also times the same batches with
+    one copy each way (no overlap of copies and kernels) and the host's
+    enqueue time per call."""
+    import time
+
+    dev = groups[0][0]["A"].device
+    hosts = []
+    for grp in groups:
+        a = torch.cat([inst["A_host"].reshape(-1) for inst in grp]).pin_memory()
+        o = torch.empty((pack * M * N,), dtype=torch.float32).pin_memory()
+        hosts.append((a, o, sk.pointer_array([inst["B"] for inst in grp])))
+    sb = sk.gemm_bt_host_staging_bytes(pack, M, N, K, SPLITS, KPS, DTYPE)
+    staging = torch.empty((sb // 4,), dtype=torch.float32, device=dev)
+    sk.gemm_bt_workspace_init(staging, sb, stream=stream)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(3, min(steps, 200))
+
+    def run(opc):
+        host_s = 0.0
+        with torch.cuda.stream(stream):
+            for k in range(3):
+                a, o, b = hosts[k % len(hosts)]
+                sk.gemm_bt_host_batch(a, b, o, pack, staging, sb, M, N, K, SPLITS, KPS, DTYPE, fused=fused,
+                                      ops_per_copy=opc, stream=stream)
+            torch.cuda.synchronize()
+            start.record(stream)
+            for k in range(n):
+                a, o, b = hosts[k % len(hosts)]
+                t0 = time.perf_counter()
+                sk.gemm_bt_host_batch(a, b, o, pack, staging, sb, M, N, K, SPLITS, KPS, DTYPE, fused=fused,
+                                      ops_per_copy=opc, stream=stream)
+                host_s += time.perf_counter() - t0
+            stop.record(stream)
+        stop.synchronize()
+        return start.elapsed_time(stop) * 1e3 / (n * pack), host_s * 1e6 / n
+
+    us, host_us = run(0)
+    # the step just timed ended on group (n-1) % len(groups): its host results
+    # must equal the resident-operand outputs of the same operations
+    last = (n - 1) % len(groups)
+    for i, inst in enumerate(groups[last]):
+        got = hosts[last][1][i * M * N:(i + 1) * M * N].view(M, N)
+        if not torch.equal(got, inst["out"].cpu()):
+            raise RuntimeError("host-buffer results differ from the resident-operand outputs")
+    serial_us, _ = run(pack)
+    if sk.splitk_get_device_status(stream) != 0:
+        raise RuntimeError("a kernel's bounded wait ran out during the end-to-end run")
+    return {"value": round(us, 4), "unit": "µs/op", "h2d_bytes_per_step": pack * M * K * 2,
+            "d2h_bytes_per_step": pack * M * N * 4,
+            "how": f"gemm_bt_host_batch per step: {pack} activations copied in from pinned host memory and "
+                   "results copied out to pinned host memory on two copy streams, pipelined against the "
+                   f"kernels; weights resident; CUDA events on the caller's stream over {n} steps",
+            "unpipelined": "the same with one copy each way for the whole step (no overlap of copies and kernels)",
+            "unpipelined_us": round(serial_us, 4), "host_enqueue_us_per_step": round(host_us, 2)}
 
 
 def run_ours(args, rank, world, dev, torch, dist):
@@ -322,28 +382,13 @@ def run_ours(args, rank, world, dev, torch, dist):
     else:
         dom_name, dom_us, dom_bytes = "tc_splitk_kernel (partial pass)", gemm_us, BYTES_GEMM
 
-    # end to end through the public API, host buffers: H2D of A, the call, D2H of out
-    e2e_steps = max(3, min(args.steps, 200))
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-
-    def e2e_step(k):
-        for inst in groups[k % len(groups)]:
-            inst["A"].copy_(inst["A_host"], non_blocking=True)
-            op(inst)
-            inst["out_host"].copy_(inst["out"], non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for k in range(3):
-            e2e_step(k)
-        torch.cuda.synchronize()
-        start.record(stream)
-        for k in range(e2e_steps):
-            e2e_step(k)
-        stop.record(stream)
-    stop.synchronize()
-    e2e_us = start.elapsed_time(stop) * 1e3 / (e2e_steps * pack)
+    # end to end through the C ABI with HOST buffers: every step copies its
+    # operations' activations in from pinned host memory and their results
+    # out to pinned host memory (gemm_bt_host_batch), weights resident
+    e2e = measure_e2e(sk, torch, stream, groups, pack, fused, args.steps)
 
     # weight preparation (B = W^T), a one-shot cost outside the operation
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     prep_n = 24
     Ws = [torch.empty((K, N), dtype=torch.bfloat16, device=dev).normal_() for _ in range(prep_n)]
     Bs = [torch.empty((N, K), dtype=torch.bfloat16, device=dev) for _ in range(prep_n)]
@@ -390,10 +435,7 @@ def run_ours(args, rank, world, dev, torch, dist):
         "kernels_us": {"partial_pass": round(gemm_us, 4), "reduce": round(red_us, 4),
                        "two_pass_op": round(two_pass_us, 4),
                        "fused_op" if fused else "two_pass_op_graph": round(us_per_op * world, 4)},
-        "e2e": {"value": round(e2e_us, 4), "unit": "µs/op", "h2d_bytes_per_step": pack * M * K * 2,
-                "d2h_bytes_per_step": pack * M * N * 4,
-                "how": "per op: pinned A -> device, gemm_bt via the Python binding, out -> pinned host; "
-                       "B resident (prepared weights); no graph"},
+        "e2e": e2e,
         "prepare": {"what": "weight preparation B[N,K] = W[K,N]^T (one-shot, outside the operation)",
                     "us": round(prep_us, 3), "bytes": 2 * K * N * 2,
                     "achieved_gbs": round(2 * K * N * 2 / (prep_us * 1e-6) / 1e9, 1),

@@ -29,8 +29,9 @@
  *     (A and B may overlap each other: both are only read); else SPLITK_ERR_ALIAS
  *
  * Memory and ownership: every data pointer is a DEVICE pointer on the current
- * CUDA device, owned by the caller.  The library allocates no device memory
- * on any call path and keeps no pointer after a call returns.
+ * CUDA device, owned by the caller, except the host activations and results
+ * of gemm_bt_host_batch.  The library allocates no device memory on any call
+ * path and keeps no pointer after a call returns.
  *
  * Asynchrony and errors: calls enqueue work on `stream` (a cudaStream_t, passed
  * as void*; NULL means the legacy default stream) and return without
@@ -173,6 +174,49 @@ int gemm_bt(const void *A, const void *B, float *out, void *workspace,
 int gemm_bt_noalloc(const void *A, const void *B, float *out, int64_t M,
                     int64_t N, int64_t K, int64_t splits, int64_t k_per_split,
                     int dtype, int fused, void *stream);
+
+/* Device staging bytes gemm_bt_host_batch needs for `count` operations of
+ * this shape: count A slots [M,K], count output slots [M,N] F32 and one
+ * gemm_bt workspace.  Returns 0 for a rejected geometry or element type, or
+ * count outside [1, 65536]. */
+size_t gemm_bt_host_staging_bytes(int64_t count, int64_t M, int64_t N,
+                                  int64_t K, int64_t splits,
+                                  int64_t k_per_split, int dtype);
+
+/* `count` operations out_i = gemm_bt(A_i, B_i) whose activations and results
+ * live in HOST memory.  The pages time operands already on the device; this
+ * entry point adds the copies a serving loop needs, pipelined so that they
+ * overlap the kernels.
+ *   A_host     host, [count,M,K] elements of `dtype`, operation i at
+ *              i*M*K; read by the copy engine (page-locked memory lets the
+ *              copies run asynchronously; any memory cudaMemcpyDefault
+ *              accepts works)
+ *   B          host array of `count` DEVICE pointers, each a prepared weight
+ *              [N,K] (16-byte aligned; entries may repeat)
+ *   out_host   host, [count,M,N] F32; fully overwritten once `stream`
+ *              reaches the end of the call's work
+ *   staging    device, >= gemm_bt_host_staging_bytes(), 16-byte aligned,
+ *              overlapping no B; zeroed once (gemm_bt_workspace_init) before
+ *              its first fused use, like a gemm_bt workspace
+ *   fused      as for gemm_bt (0, 1 or 3)
+ *   ops_per_copy  operations moved by one copy each way; 0 lets the library
+ *              choose (at least 2 MiB of A per copy, at most half the batch)
+ * Every operation is bitwise the gemm_bt result for its operands.  The copy
+ * in of group g+1 and the copy out of group g-1 run on two library streams
+ * while group g computes on `stream`; the copy in waits for the work already
+ * on `stream`, and `stream` waits for the last copy out, so synchronising
+ * `stream` completes the batch.  Host buffers must stay valid until then.
+ * The first call on a device creates those two streams and four events (kept
+ * until exit); a process-wide mutex serialises the enqueueing of concurrent
+ * calls.  Returns as gemm_bt's validation would (plus SPLITK_ERR_CONFIG for
+ * count outside [1, 65536] or ops_per_copy < 0, SPLITK_ERR_WORKSPACE for a
+ * small staging, SPLITK_ERR_ALIAS when A_host and out_host overlap or the
+ * staging overlaps a B or a host range) before enqueueing anything. */
+int gemm_bt_host_batch(const void *A_host, const void *const *B,
+                       float *out_host, int64_t count, void *staging,
+                       size_t staging_bytes, int64_t M, int64_t N, int64_t K,
+                       int64_t splits, int64_t k_per_split, int dtype,
+                       int fused, int64_t ops_per_copy, void *stream);
 
 /* Reads and clears the device status word on the current device,
  * synchronising `stream` first.  Returns SPLITK_OK, SPLITK_ERR_DEVICE_TIMEOUT

@@ -26,6 +26,7 @@ EXPORTS = (
     "gemm_bt", "splitk_get_device_status", "splitk_status_string", "splitk_set_tile_override",
     "splitk_describe_launch", "splitk_selftest_bounded_wait", "splitk_last_error",
     "gemm_bt_workspace_init", "gemm_bt_noalloc", "splitk_prepare_bt",
+    "gemm_bt_host_staging_bytes", "gemm_bt_host_batch",
 )
 NOALLOC_MAX_BYTES = 32 << 20   # SPLITK_NOALLOC_MAX_BYTES
 
@@ -67,11 +68,15 @@ def lib() -> ctypes.CDLL:
             L.gemm_bt_workspace_init.argtypes = [vp, sz, vp]
             L.gemm_bt_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, vp]
             L.splitk_prepare_bt.argtypes = [vp, vp, i64, i64, i32, vp]
+            L.gemm_bt_host_staging_bytes.argtypes = [i64] * 6 + [i32]
+            L.gemm_bt_host_staging_bytes.restype = sz
+            L.gemm_bt_host_batch.argtypes = [vp, vp, vp, i64, vp, sz, i64, i64, i64, i64, i64, i32, i32,
+                                             i64, vp]
             L.splitk_last_error.argtypes = []
             L.splitk_last_error.restype = ctypes.c_char_p
             for name in ("splitk_check_geometry", "gemm_splitk_bt", "splitk_reduce", "gemm_bt",
                          "gemm_bt_workspace_init", "gemm_bt_noalloc", "splitk_prepare_bt",
-                         "splitk_get_device_status", "splitk_set_tile_override",
+                         "gemm_bt_host_batch", "splitk_get_device_status", "splitk_set_tile_override",
                          "splitk_describe_launch", "splitk_selftest_bounded_wait"):
                 getattr(L, name).restype = i32
             _lib = L
@@ -168,6 +173,30 @@ def gemm_bt_noalloc(A, B, out, M, N, K, splits, k_per_split, dtype, fused=0, str
     the library's own device scratch array serves instead (see splitk.h)."""
     _check(lib().gemm_bt_noalloc(_ptr(A), _ptr(B), _ptr(out), M, N, K, splits, k_per_split,
                                  dtype_code(dtype), fused, _stream(stream)), "gemm_bt_noalloc")
+
+
+def gemm_bt_host_staging_bytes(count, M, N, K, splits, k_per_split, dtype) -> int:
+    return lib().gemm_bt_host_staging_bytes(count, M, N, K, splits, k_per_split, dtype_code(dtype))
+
+
+def pointer_array(items):
+    """A C array of device pointers (tensors or integer addresses); keep it
+    alive for the duration of the call that receives it."""
+    arr = (ctypes.c_void_p * max(len(items), 1))()
+    for i, x in enumerate(items):
+        arr[i] = _ptr(x)
+    return arr
+
+
+def gemm_bt_host_batch(A_host, B, out_host, count, staging, staging_bytes, M, N, K, splits, k_per_split,
+                       dtype, fused=0, ops_per_copy=0, stream=None) -> None:
+    """A_host and out_host: host tensors (pinned for overlap) or addresses; B:
+    a sequence of `count` device weights, or a prebuilt pointer_array()."""
+    arr = B if isinstance(B, ctypes.Array) else pointer_array(B)
+    _check(lib().gemm_bt_host_batch(_ptr(A_host), ctypes.cast(arr, ctypes.c_void_p), _ptr(out_host), count,
+                                    _ptr(staging), staging_bytes, M, N, K, splits, k_per_split,
+                                    dtype_code(dtype), fused, ops_per_copy, _stream(stream)),
+           "gemm_bt_host_batch")
 
 
 def splitk_get_device_status(stream=None) -> int:

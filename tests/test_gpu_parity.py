@@ -332,3 +332,95 @@ def test_prepare_matches_oracle_bitwise(lib, case):
         sk.gemm_bt(A, Bref, o2.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=0)
         assert np.array_equal(o1.numpy().view(np.uint32), o2.numpy().view(np.uint32))
     assert sk.splitk_get_device_status() == 0
+
+
+# (M, N, K, splits, kps, dtype, count, ops_per_copy)
+HOST_CASES = [(64, 128, 160, 3, 64, "bf16", 5, 2), (96, 512, 2048, 4, 512, "f16", 3, 0),
+              (32, 64, 128, 2, 64, "f32", 4, 1), (256, 1024, 2048, 2, 1024, "bf16", 4, 0)]
+
+
+def host_operand(bits_list, dtype, pinned):
+    flat = np.concatenate([np.ascontiguousarray(b).reshape(-1) for b in bits_list])
+    if dtype == "f32":
+        t = torch.from_numpy(flat.astype(np.float32))
+    else:
+        t = torch.from_numpy(flat.view(np.int16)).view(torch.bfloat16 if dtype == "bf16" else torch.float16)
+    return t.pin_memory() if pinned else t.clone()
+
+
+@pytest.mark.parametrize("case", HOST_CASES, ids=[f"{c[5]}-M{c[0]}N{c[1]}K{c[2]}S{c[3]}x{c[6]}g{c[7]}"
+                                                  for c in HOST_CASES])
+def test_host_batch_matches_device_call_and_oracle(lib, case):
+    """gemm_bt_host_batch: host activations in, host results out, each
+    operation bitwise the device-resident gemm_bt result for its operands and
+    within the pages' tolerance of the oracle; pinned and pageable host
+    memory; guards behind the host output intact."""
+    from harness import GUARD_VALUE, GUARDS
+
+    sk = lib
+    M, N, K, S, kps, dt, count, opc = case
+    cs = [oracle_case(M, N, K, S, kps, dt, "uniform", seed) for seed in range(count)]
+    Bs = [device_operand(c[0].B, dt) for c in cs]
+    ref = []
+    for c, B in zip(cs, Bs):
+        ws, nbytes = workspace(M, N, K, S, kps)
+        o = Guarded(M * N)
+        sk.gemm_bt(device_operand(c[0].A, dt), B, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=0)
+        ref.append(o.numpy().reshape(M, N))
+    sb = sk.gemm_bt_host_staging_bytes(count, M, N, K, S, kps, dt)
+    for pinned in (True, False):
+        A_host = host_operand([c[0].A for c in cs], dt, pinned)
+        for fused in (0, 1):
+            staging = torch.zeros(sb // 4 + 16, dtype=torch.float32, device="cuda")
+            out_host = torch.full((count * M * N + GUARDS,), 7.0, dtype=torch.float32)
+            out_host[count * M * N:] = GUARD_VALUE
+            out_host = out_host.pin_memory() if pinned else out_host
+            stream = torch.cuda.Stream()
+            sk.gemm_bt_host_batch(A_host, Bs, out_host, count, staging, sb, M, N, K, S, kps, dt,
+                                  fused=fused, ops_per_copy=opc, stream=stream)
+            stream.synchronize()
+            assert sk.splitk_get_device_status(stream) == 0
+            got = out_host.numpy()
+            assert np.all(got[count * M * N:] == GUARD_VALUE)
+            for i, c in enumerate(cs):
+                oi = got[i * M * N:(i + 1) * M * N].reshape(M, N)
+                assert np.array_equal(oi.view(np.uint32), ref[i].view(np.uint32)), (pinned, fused, i)
+                assert max_scaled_error(oi, c[3], c[4]) <= TOL_FINAL[dt]
+            # the results pass through the staging's output slots
+            esize = 4 if dt == "f32" else 2
+            off = (count * M * K * esize + 255) // 256 * 256 // 4
+            slots = staging[off:off + count * M * N].cpu().numpy()
+            assert np.array_equal(slots.view(np.uint32), got[:count * M * N].view(np.uint32))
+
+
+def test_host_batch_back_to_back_shared_staging(lib):
+    """Two batches on one stream share one staging with no synchronisation
+    between them; the second waits for the first's copies out, and both
+    results are right.  One weight serves every operation of a batch."""
+    sk = lib
+    M, N, K, S, kps, dt, count = 96, 512, 2048, 4, 512, "bf16", 6
+    c1 = [oracle_case(M, N, K, S, kps, dt, "uniform", 20 + i) for i in range(count)]
+    B = device_operand(c1[0][0].B, dt)
+    want = []
+    for c in c1:
+        ws, nbytes = workspace(M, N, K, S, kps)
+        o = Guarded(M * N)
+        sk.gemm_bt(device_operand(c[0].A, dt), B, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=1)
+        want.append(o.numpy())
+    sb = sk.gemm_bt_host_staging_bytes(count, M, N, K, S, kps, dt)
+    staging = torch.zeros(sb // 4, dtype=torch.float32, device="cuda")
+    a1 = host_operand([c[0].A for c in c1], dt, True)
+    a2 = host_operand([c[0].A for c in reversed(c1)], dt, True)
+    o1 = torch.zeros(count * M * N, dtype=torch.float32).pin_memory()
+    o2 = torch.zeros(count * M * N, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.Stream()
+    ptrs = sk.pointer_array([B] * count)
+    sk.gemm_bt_host_batch(a1, ptrs, o1, count, staging, sb, M, N, K, S, kps, dt, fused=1, stream=stream)
+    sk.gemm_bt_host_batch(a2, ptrs, o2, count, staging, sb, M, N, K, S, kps, dt, fused=1, stream=stream)
+    stream.synchronize()
+    assert sk.splitk_get_device_status(stream) == 0
+    for i in range(count):
+        r1 = o1.numpy()[i * M * N:(i + 1) * M * N]
+        r2 = o2.numpy()[(count - 1 - i) * M * N:(count - i) * M * N]
+        assert np.array_equal(r1.view(np.uint32), want[i].view(np.uint32)), i
+        assert np.array_equal(r2.view(np.uint32), want[i].view(np.uint32)), i

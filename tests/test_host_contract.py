@@ -233,3 +233,51 @@ def test_prepare_rejections(L):
     assert L.splitk_prepare_bt(W + 2, B, 64, 64, bd.BF16, None) == bd.ERR_ALIGN
     # W is 64 * 64 * 2 = 8 KiB; a B starting inside it overlaps
     assert L.splitk_prepare_bt(W, W + 8192 - 16, 64, 64, bd.BF16, None) == bd.ERR_ALIAS
+
+
+def test_host_staging_bytes(L):
+    # count A slots, count output slots (each group packed), one gemm_bt workspace
+    M, N, K, S, kps = 256, 1024, 2048, 2, 1024
+    ws = sk.gemm_bt_workspace_bytes(M, N, K, S, kps)
+    assert sk.gemm_bt_host_staging_bytes(8, M, N, K, S, kps, "bf16") == 8 * M * K * 2 + 8 * M * N * 4 + ws
+    assert sk.gemm_bt_host_staging_bytes(1, 32, 64, 128, 2, 64, "f32") == \
+        32 * 128 * 4 + 32 * 64 * 4 + sk.gemm_bt_workspace_bytes(32, 64, 128, 2, 64)
+    assert sk.gemm_bt_host_staging_bytes(0, M, N, K, S, kps, "bf16") == 0
+    assert sk.gemm_bt_host_staging_bytes((1 << 16) + 1, M, N, K, S, kps, "bf16") == 0
+    assert sk.gemm_bt_host_staging_bytes(2, 48, N, K, S, kps, "bf16") == 0
+    assert L.gemm_bt_host_staging_bytes(2, M, N, K, S, kps, 9) == 0
+
+
+def test_host_batch_rejections(L):
+    """Every rejection happens before the library touches CUDA (no GPU here)."""
+    M, N, K, S, kps = 32, 64, 128, 2, 64
+    need = sk.gemm_bt_host_staging_bytes(2, M, N, K, S, kps, "bf16")
+    Ah, Oh, ST = 0x50000000, 0x60000000, 0x70000000
+    Bs = bd.pointer_array([B0, B0])
+
+    def call(A=Ah, B=Bs, O=Oh, count=2, st=ST, stb=need, fused=0, opc=0, dtype=bd.BF16, **kw):
+        g = dict(GOOD, **kw)
+        b = ctypes.cast(B, ctypes.c_void_p) if isinstance(B, ctypes.Array) else B
+        return L.gemm_bt_host_batch(A, b, O, count, st, stb, g["M"], g["N"], g["K"], g["S"], g["kps"],
+                                    dtype, fused, opc, None)
+
+    assert call(M=48) == bd.ERR_SHAPE
+    assert call(S=3) == bd.ERR_SPLIT
+    assert call(dtype=5) == bd.ERR_DTYPE
+    assert call(count=0) == bd.ERR_CONFIG
+    assert call(count=(1 << 16) + 1) == bd.ERR_CONFIG
+    assert call(opc=-1) == bd.ERR_CONFIG
+    assert call(fused=2) == bd.ERR_CONFIG
+    assert call(A=0) == bd.ERR_NULL
+    assert call(B=0) == bd.ERR_NULL
+    assert call(O=0) == bd.ERR_NULL
+    assert call(st=0) == bd.ERR_NULL
+    assert call(B=bd.pointer_array([B0, 0])) == bd.ERR_NULL
+    assert call(st=ST + 8) == bd.ERR_ALIGN
+    assert call(B=bd.pointer_array([B0, B0 + 2])) == bd.ERR_ALIGN
+    assert call(stb=need - 16) == bd.ERR_WORKSPACE
+    # A_host [2,32,128] BF16 = 16 KiB; out_host [2,32,64] F32 = 16 KiB
+    assert call(O=Ah + 16384 - 16) == bd.ERR_ALIAS
+    assert call(B=bd.pointer_array([B0, ST + need - 64])) == bd.ERR_ALIAS
+    assert call(st=Oh - 64) == bd.ERR_ALIAS
+    assert call(M=48, A=0) == bd.ERR_SHAPE
