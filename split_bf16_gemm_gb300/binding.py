@@ -214,7 +214,7 @@ def splitk_describe_launch(M, N, K, splits, k_per_split, dtype, fused=0) -> dict
                                         ctypes.addressof(info)), "splitk_describe_launch")
     keys = ("path", "bn", "chunks", "chunk_len", "stages", "cluster", "grid_x", "grid_y",
             "grid_z", "smem_bytes", "fused_in_kernel", "kernels_per_call", "kblocks_per_stage",
-            "three_d", "split_sum")
+            "three_d", "split_sum", "prefetchers")
     return dict(zip(keys, list(info)))
 
 

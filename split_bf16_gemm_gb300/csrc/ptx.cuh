@@ -75,6 +75,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 
 // ------------------------------------------------------------------- TMA
 
+// Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned address, size a
+// multiple of 16); a hint only: no completion to wait for.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
+
+// Prefetch of the L2 line holding `p` (a hint: no completion).
+__device__ __forceinline__ void prefetch_l2_line(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

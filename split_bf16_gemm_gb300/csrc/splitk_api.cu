@@ -94,15 +94,20 @@ int validate_gemm(const void *A, const void *B, int64_t M, int64_t N, int64_t K,
 }
 
 // The partial pass into P (and, when `out` is given, the split sum too).
+// `prefetch` lets the CTAs that start beside the previous launch prefetch the
+// operands into L2; gemm_bt's two-kernel path turns it off, since the launch
+// before its partial pass is normally a reduce that leaves no SM free, and
+// prefetches issued once every CTA is running only compete with the loads.
 int run_partial_pass(const void *A, const void *B, float *P, float *out, unsigned *counters, int64_t M, int64_t N,
-                     int64_t K, int64_t S, int64_t kps, int dtype, bool fused, cudaStream_t stream)
+                     int64_t K, int64_t S, int64_t kps, int dtype, bool fused, bool prefetch, cudaStream_t stream)
 {
     if (dtype == SPLITK_F32) {
         return cuda_status(splitk::launch_simt_f32(static_cast<const float *>(A), static_cast<const float *>(B), P,
                                                    M, N, K, S, kps, stream));
     }
     GemmProblem pr{A, B, P, out, counters, M, N, K, S, kps, dtype == SPLITK_BF16};
-    const TilePlan plan = splitk::plan_tc(M, N, K, S, kps, fused);
+    TilePlan plan = splitk::plan_tc(M, N, K, S, kps, fused);
+    if (!prefetch) plan.prefetchers = 0;
     return cuda_status(splitk::launch_tc(pr, plan, stream));
 }
 
@@ -136,7 +141,7 @@ int gemm_splitk_bt(const void *A, const void *B, float *partials, int64_t M, int
     const Range rb = range_of(B, static_cast<uint64_t>(N * K) * e);
     const Range rp = range_of(partials, static_cast<uint64_t>(splits * M * N) * 4);
     if (overlap(rp, ra) || overlap(rp, rb)) return SPLITK_ERR_ALIAS;
-    return run_partial_pass(A, B, partials, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false,
+    return run_partial_pass(A, B, partials, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false, true,
                             static_cast<cudaStream_t>(stream));
 }
 
@@ -204,9 +209,9 @@ int gemm_bt(const void *A, const void *B, float *out, void *workspace, size_t wo
         // fused == 1 keeps no partials where the cluster sums the splits on chip
         const TilePlan plan = splitk::plan_tc(M, N, K, splits, k_per_split, true);
         float *keep = (fused == 1 && plan.split_sum == 2) ? nullptr : P;
-        return run_partial_pass(A, B, keep, out, counters, M, N, K, splits, k_per_split, dtype, true, s);
+        return run_partial_pass(A, B, keep, out, counters, M, N, K, splits, k_per_split, dtype, true, true, s);
     }
-    st = run_partial_pass(A, B, P, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false, s);
+    st = run_partial_pass(A, B, P, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false, false, s);
     if (st != SPLITK_OK) return st;
     return cuda_status(splitk::launch_reduce(P, out, splits, M * N, s));
 }
@@ -291,6 +296,7 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
     info[12] = p.kbs;
     info[13] = p.three_d;
     info[14] = p.split_sum;
+    info[15] = in_kernel ? p.prefetchers : 0;   // gemm_bt's two-kernel path does not prefetch
     return SPLITK_OK;
 }
 

@@ -36,6 +36,7 @@ struct TilePlan {
     int split_sum;      // 0 none, 1 by arrival counters, 2 inside the cluster (cluster = splits * chunks)
     int share;          // 16-byte pieces of the tile each cluster rank owns
     uint32_t region0;   // bytes of the stage ring / accumulator staging
+    int prefetchers;    // CTAs (the first in dispatch order) that prefetch A and B into L2
     dim3 grid;
     size_t smem_bytes;  // dynamic shared memory per CTA
 };

@@ -54,7 +54,8 @@ namespace {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s; a launch normally takes microseconds
 constexpr int kThreads = 256;                     // 8 warps: two per tensor-memory lane quarter
-constexpr int kBatch = 8;                          // pieces per thread per pass of the split sum
+constexpr int kPieceBatch = 2;                     // split sum by counters: pieces per thread per pass,
+constexpr int kSplitBatch = 8;                     //   and splits whose loads are in flight together
 
 struct TcArgs {
     float *P;              // [S,M,N] partials (nullptr: not kept, when the cluster sums the splits)
@@ -69,7 +70,22 @@ struct TcArgs {
     uint32_t region0;      // bytes of the stage ring / accumulator staging area
     int bf16;
     uint64_t wait_limit_ns;
+    const uint8_t *A, *B;  // operands, for the L2 prefetch
+    uint64_t a_bytes, b_bytes;
+    int prefetchers;       // CTAs, first in dispatch order, that prefetch A and B into L2
 };
+
+// Part j of `parts` (whole 128-byte lines) of [p, p + bytes) into L2, one
+// line per prefetch, spread over threads t = 0..nt-1.  Per-thread prefetches
+// keep the TMA unit free for the CTA's own loads.
+__device__ __forceinline__ void prefetch_part(const uint8_t *p, uint64_t bytes, int j, int parts, int t, int nt)
+{
+    const uint64_t part = ((bytes + parts - 1) / parts + 127) & ~uint64_t(127);
+    const uint64_t lo = static_cast<uint64_t>(j) * part;
+    const uint64_t hi = min(lo + part, bytes);
+    for (uint64_t off = lo + static_cast<uint64_t>(t) * 128u; off < hi; off += static_cast<uint64_t>(nt) * 128u)
+        ptx::prefetch_l2_line(p + off);
+}
 
 template <int BN>
 struct TcShape {
@@ -193,6 +209,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(&tmem_slot), Sh::kTmemCols);
         ptx::tmem_relinquish();
+    }
+    if (warp >= 2) {
+        // CTAs that start while the previous grid still runs (the first ones
+        // dispatched, on the SMs it leaves free) bring this launch's operands
+        // into L2 for everyone.  L2 is the point of coherence, so a line
+        // fetched before the previous grid writes it is updated, never stale.
+        const int disp = (blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * (blockIdx.z / Q))) * Q +
+                         static_cast<int>(blockIdx.z % Q);
+        if (disp < args.prefetchers) {
+            prefetch_part(args.A, args.a_bytes, disp, args.prefetchers, tid - 64, kThreads - 64);
+            prefetch_part(args.B, args.b_bytes, disp, args.prefetchers, tid - 64, kThreads - 64);
+        }
     }
     ptx::tc_fence_before_sync();
     __syncthreads();
@@ -385,33 +413,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         if (last_s) {
             __threadfence();
-            for (int g0 = my_lo + tid; g0 < my_hi; g0 += kBatch * kThreads) {
-                float4 tot[kBatch];
-                for (int sp = 0; sp < args.S; ++sp) {
+            // kPieceBatch pieces per thread, the loads of kSplitBatch splits
+            // in flight at once (one L2 round trip per kSplitBatch splits,
+            // not per split); the adds still run in split order 0..S-1.  With
+            // one CTA per split (Q == 1) it owns the whole tile and walks only
+            // the pieces of rows below M (a quarter of them when M is 32).
+            const int rows_here = Q == 1 ? min(kTileM, args.M - row0) : kTileM;
+            const int walk_hi = Q == 1 ? rows_here * (BN / 4) : my_hi;
+            auto owned = [&](int t) {           // t-th owned piece, as a piece index
+                if (Q > 1) return t;
+                const int r = t / (BN / 4), cq = t % (BN / 4);
+                return (((cq >> 3) << 2) | (r >> 5)) << 8 | (r & 31) << 3 | (cq & 7);
+            };
+            for (int g0 = (Q == 1 ? 0 : my_lo) + tid; g0 < walk_hi; g0 += kPieceBatch * kThreads) {
+                float4 tot[kPieceBatch];
+                for (int sp0 = 0; sp0 < args.S; sp0 += kSplitBatch) {
+                    float4 v[kSplitBatch][kPieceBatch];
 #pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        const int g = g0 + i * kThreads;
-                        if (g < my_hi) {
-                            const Piece p = piece_at(g);
-                            const int row = row0 + p.row;
-                            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (sp == s)
-                                v = chunk_sum(p);
-                            else if (row < args.M)
-                                v = __ldcg(reinterpret_cast<const float4 *>(
-                                    args.P + sp * MN + static_cast<size_t>(row) * args.N + col0 + p.col));
-                            if (sp == 0)
-                                tot[i] = v;
-                            else
-                                add4(tot[i], v);
+                    for (int j = 0; j < kSplitBatch; ++j) {
+#pragma unroll
+                        for (int i = 0; i < kPieceBatch; ++i) {
+                            const int t = g0 + i * kThreads, sp = sp0 + j;
+                            v[j][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (t < walk_hi && sp < args.S) {
+                                const Piece p = piece_at(owned(t));
+                                const int row = row0 + p.row;
+                                if (sp == s)
+                                    v[j][i] = chunk_sum(p);
+                                else if (row < args.M)
+                                    v[j][i] = __ldcg(reinterpret_cast<const float4 *>(
+                                        args.P + sp * MN + static_cast<size_t>(row) * args.N + col0 + p.col));
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < kSplitBatch; ++j) {
+#pragma unroll
+                        for (int i = 0; i < kPieceBatch; ++i) {
+                            if (sp0 + j == 0)
+                                tot[i] = v[j][i];
+                            else if (sp0 + j < args.S)
+                                add4(tot[i], v[j][i]);
                         }
                     }
                 }
 #pragma unroll
-                for (int i = 0; i < kBatch; ++i) {
-                    const int g = g0 + i * kThreads;
-                    if (g < my_hi) {
-                        const Piece p = piece_at(g);
+                for (int i = 0; i < kPieceBatch; ++i) {
+                    const int t = g0 + i * kThreads;
+                    if (t < walk_hi) {
+                        const Piece p = piece_at(owned(t));
                         const int row = row0 + p.row;
                         if (row < args.M)
                             *reinterpret_cast<float4 *>(args.out + static_cast<size_t>(row) * args.N + col0 +
@@ -731,6 +781,12 @@ TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool f
     p.share = share;
     p.region0 = static_cast<uint32_t>(round_up(std::max(p.stages * stage_bytes(bn, p.kbs), epi_bytes(bn)), 1024));
     p.grid = dim3(static_cast<unsigned>(N / bn), static_cast<unsigned>(mt), static_cast<unsigned>(S * chunks));
+    // CTAs of the next launch that fit beside this one (whole clusters): they
+    // start early under programmatic dependent launch and do the prefetch
+    const int64_t ctas = static_cast<int64_t>(p.grid.x) * p.grid.y * p.grid.z;
+    const int64_t clusters = ctas / q;
+    const int64_t spare = std::max<int64_t>(0, static_cast<int64_t>(resident_clusters(q)) - clusters) * q;
+    p.prefetchers = static_cast<int>(std::min(spare, ctas));
     p.smem_bytes = smem_for(bn, p.kbs, p.stages, q, share);
     return p;
 }
@@ -768,6 +824,11 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
     a.region0 = plan.region0;
     a.bf16 = pr.bf16 ? 1 : 0;
     a.wait_limit_ns = kWaitLimitNs;
+    a.A = static_cast<const uint8_t *>(pr.A);
+    a.B = static_cast<const uint8_t *>(pr.B);
+    a.a_bytes = static_cast<uint64_t>(pr.M * pr.K) * 2;
+    a.b_bytes = static_cast<uint64_t>(pr.N * pr.K) * 2;
+    a.prefetchers = plan.prefetchers;
     switch (plan.bn) {
     case 64: return launch_cluster<64>(ta, tb, a, plan, stream);
     case 128: return launch_cluster<128>(ta, tb, a, plan, stream);
