@@ -248,9 +248,9 @@ int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
  *  dynamic_smem_bytes,
  *  fused_in_kernel (0/1), kernels_per_call, kblocks_per_stage,
  *  three_d_loads (0/1), split_sum (0 none, 1 by arrival counters in the
- *  workspace, 2 inside the thread-block cluster), prefetchers (CTAs that
- *  fit beside a running launch and prefetch A and B into L2 before the
- *  dependency wait)}; `info` must hold 16 ints.  Returns a status as gemm_bt's
+ *  workspace, 2 inside the thread-block cluster), prefetchers (fused calls
+ *  only: CTAs that fit beside a running launch and prefetch A and B into L2
+ *  before the dependency wait)}; `info` must hold 16 ints.  Returns a status as gemm_bt's
  * validation would (pointers are not checked). */
 int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits,
                            int64_t k_per_split, int dtype, int fused,

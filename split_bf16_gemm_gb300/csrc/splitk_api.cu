@@ -95,9 +95,9 @@ int validate_gemm(const void *A, const void *B, int64_t M, int64_t N, int64_t K,
 
 // The partial pass into P (and, when `out` is given, the split sum too).
 // `prefetch` lets the CTAs that start beside the previous launch prefetch the
-// operands into L2; gemm_bt's two-kernel path turns it off, since the launch
-// before its partial pass is normally a reduce that leaves no SM free, and
-// prefetches issued once every CTA is running only compete with the loads.
+// operands into L2.  Only the fused launch uses it: before a partial pass
+// there is normally a reduce, which leaves no SM free, and prefetches issued
+// once every CTA is running only compete with the loads.
 int run_partial_pass(const void *A, const void *B, float *P, float *out, unsigned *counters, int64_t M, int64_t N,
                      int64_t K, int64_t S, int64_t kps, int dtype, bool fused, bool prefetch, cudaStream_t stream)
 {
@@ -141,7 +141,7 @@ int gemm_splitk_bt(const void *A, const void *B, float *partials, int64_t M, int
     const Range rb = range_of(B, static_cast<uint64_t>(N * K) * e);
     const Range rp = range_of(partials, static_cast<uint64_t>(splits * M * N) * 4);
     if (overlap(rp, ra) || overlap(rp, rb)) return SPLITK_ERR_ALIAS;
-    return run_partial_pass(A, B, partials, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false, true,
+    return run_partial_pass(A, B, partials, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false, false,
                             static_cast<cudaStream_t>(stream));
 }
 

@@ -309,28 +309,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                               v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     }
     ptx::fence_proxy_async_smem();             // the staging is the source of bulk copies
+    // ---- exchange: each warp pushes the boxes it staged to their owners
+    // (a box of 32 rows x 32 columns is 256 pieces; a rank's share is a
+    // whole number of boxes), so the copies start while other warps stage
+    if (Q > 1) {
+        ptx::cluster_wait();                   // every peer's receive barrier is set up
+        __syncwarp();
+        if (lane == 0) {
+            for (int jb = half * (BN / 64); jb < (half + 1) * (BN / 64); ++jb) {
+                const int b = jb * 4 + quarter;
+                const int r = (b * 256) / share;
+                if (r == rank) continue;
+                const uint32_t slot = static_cast<uint32_t>(rank - (rank > r ? 1 : 0));
+                ptx::bulk_copy_to_cluster(ptx::mapa(recv + (slot * static_cast<uint32_t>(share) +
+                                                             static_cast<uint32_t>(b * 256 - r * share)) * 16u, r),
+                                          E + static_cast<uint32_t>(b) * 4096u, 4096u, ptx::mapa(recv_bar, r));
+            }
+        }
+    }
     ptx::tc_fence_before_sync();
     __syncthreads();
     if (warp == 1) {
         if (!acc_ok) ptx::mbar_wait_bounded(acc_bar, 0, args.wait_limit_ns);
         ptx::tc_fence_after_sync();
         ptx::tmem_dealloc(tmem, Sh::kTmemCols);
-    }
-
-    // ---- exchange: push every other rank its share of this CTA's chunk
-    if (Q > 1) {
-        ptx::cluster_wait();                   // every peer's receive barrier is set up
-        if (tid == 0) {
-#pragma unroll
-            for (int r = 0; r < Q; ++r) {
-                const int lo = min(Sh::kPieces, r * share), hi = min(Sh::kPieces, lo + share);
-                if (r == rank || hi <= lo) continue;
-                const uint32_t slot = static_cast<uint32_t>(rank - (rank > r ? 1 : 0));
-                ptx::bulk_copy_to_cluster(ptx::mapa(recv + slot * static_cast<uint32_t>(share) * 16u, r),
-                                          E + static_cast<uint32_t>(lo) * 16u,
-                                          static_cast<uint32_t>(hi - lo) * 16u, ptx::mapa(recv_bar, r));
-            }
-        }
     }
     if (!ptx::mbar_wait_bounded(recv_bar, 0, args.wait_limit_ns) && tid == 0) atomicOr(&g_device_status, 16u);
     if (Q > 1) ptx::cluster_arrive_relaxed();  // everything bound for this CTA has landed
