@@ -218,6 +218,46 @@ int gemm_bt_host_batch(const void *A_host, const void *const *B,
                        int64_t splits, int64_t k_per_split, int dtype,
                        int fused, int64_t ops_per_copy, void *stream);
 
+/* Split count for a shape.  The pages sweep 1, 2, 4, 8 and 16 splits of fixed
+ * shapes ("Aligned shared rows for pipelined NAX on CUDA", section
+ * "Measurement protocol"; "Wider consecutive-weight NAX GEMM", section
+ * "Performance method"); these two entry points pick among the same
+ * candidates.  For a candidate n, k_per_split = ceil(K/n) rounded up to a
+ * multiple of 32 and splits = ceil(K/k_per_split) (below n when K is short).
+ *
+ * splitk_choose_splits: the library's cost model of gemm_bt with `fused`
+ * (the tile planner's estimate plus the reduce for the two-kernel path); no
+ * device work.  Writes the cheapest legal (splits, k_per_split) and, when
+ * model_us is not NULL, model_us[0..4] = the estimate in microseconds per
+ * call for candidates 1, 2, 4, 8, 16 (-1 for an illegal one).  M and K positive
+ * multiples of 32, N of 64 (else SPLITK_ERR_SHAPE), a known dtype
+ * (SPLITK_ERR_DTYPE), fused in {0, 1, 3} (SPLITK_ERR_CONFIG), non-NULL
+ * outputs (SPLITK_ERR_NULL). */
+int splitk_choose_splits(int64_t M, int64_t N, int64_t K, int dtype, int fused,
+                         int64_t *splits, int64_t *k_per_split,
+                         double *model_us);
+
+/* splitk_autotune_splits: measures each candidate on the caller's buffers
+ * (A, B, out, workspace as for gemm_bt) and writes the fastest legal
+ * (splits, k_per_split).  Per candidate: one untimed call, then a CUDA graph
+ * of `reps` calls (1..1000) replayed three times between CUDA events on a
+ * private stream that first waits for the work already on `stream`.
+ * us[0..4], when not NULL, receive the microseconds per call of candidates
+ * 1, 2, 4, 8, 16 (-1 where a candidate was not run: its workspace does not
+ * fit `workspace_bytes`, or it repeats an earlier candidate's split count).
+ * Every candidate's arguments are checked before anything is enqueued (the
+ * statuses of gemm_bt; SPLITK_ERR_WORKSPACE if no candidate fits).  On
+ * return the private stream has finished, `out` holds the chosen split's
+ * result, `stream` is ordered after it, and a fused workspace has the chosen
+ * split's counters zero, ready for gemm_bt with that split.  The inputs are
+ * read repeatedly, so they sit in L2 when they fit there: the timings rank
+ * the candidates, they are not cold-cache figures.  Not capturable. */
+int splitk_autotune_splits(const void *A, const void *B, float *out,
+                           void *workspace, size_t workspace_bytes, int64_t M,
+                           int64_t N, int64_t K, int dtype, int fused,
+                           int reps, void *stream, int64_t *splits,
+                           int64_t *k_per_split, float *us);
+
 /* Reads and clears the device status word on the current device,
  * synchronising `stream` first.  Returns SPLITK_OK, SPLITK_ERR_DEVICE_TIMEOUT
  * (a kernel's bounded wait ran out since the last call; its outputs are not

@@ -26,7 +26,7 @@ EXPORTS = (
     "gemm_bt", "splitk_get_device_status", "splitk_status_string", "splitk_set_tile_override",
     "splitk_describe_launch", "splitk_selftest_bounded_wait", "splitk_last_error",
     "gemm_bt_workspace_init", "gemm_bt_noalloc", "splitk_prepare_bt",
-    "gemm_bt_host_staging_bytes", "gemm_bt_host_batch",
+    "gemm_bt_host_staging_bytes", "gemm_bt_host_batch", "splitk_choose_splits", "splitk_autotune_splits",
 )
 NOALLOC_MAX_BYTES = 32 << 20   # SPLITK_NOALLOC_MAX_BYTES
 
@@ -72,11 +72,14 @@ def lib() -> ctypes.CDLL:
             L.gemm_bt_host_staging_bytes.restype = sz
             L.gemm_bt_host_batch.argtypes = [vp, vp, vp, i64, vp, sz, i64, i64, i64, i64, i64, i32, i32,
                                              i64, vp]
+            L.splitk_choose_splits.argtypes = [i64, i64, i64, i32, i32, vp, vp, vp]
+            L.splitk_autotune_splits.argtypes = [vp, vp, vp, vp, sz, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp]
             L.splitk_last_error.argtypes = []
             L.splitk_last_error.restype = ctypes.c_char_p
             for name in ("splitk_check_geometry", "gemm_splitk_bt", "splitk_reduce", "gemm_bt",
                          "gemm_bt_workspace_init", "gemm_bt_noalloc", "splitk_prepare_bt",
-                         "gemm_bt_host_batch", "splitk_get_device_status", "splitk_set_tile_override",
+                         "gemm_bt_host_batch", "splitk_choose_splits", "splitk_autotune_splits",
+                         "splitk_get_device_status", "splitk_set_tile_override",
                          "splitk_describe_launch", "splitk_selftest_bounded_wait"):
                 getattr(L, name).restype = i32
             _lib = L
@@ -197,6 +200,30 @@ def gemm_bt_host_batch(A_host, B, out_host, count, staging, staging_bytes, M, N,
                                     _ptr(staging), staging_bytes, M, N, K, splits, k_per_split,
                                     dtype_code(dtype), fused, ops_per_copy, _stream(stream)),
            "gemm_bt_host_batch")
+
+
+SPLIT_CANDIDATES = (1, 2, 4, 8, 16)
+
+
+def splitk_choose_splits(M, N, K, dtype, fused=0) -> tuple[int, int, dict]:
+    """(splits, k_per_split, {candidate: model microseconds or None}) from the
+    library's cost model."""
+    s, k = ctypes.c_int64(), ctypes.c_int64()
+    t = (ctypes.c_double * len(SPLIT_CANDIDATES))()
+    _check(lib().splitk_choose_splits(M, N, K, dtype_code(dtype), fused, ctypes.byref(s), ctypes.byref(k), t),
+           "splitk_choose_splits")
+    return s.value, k.value, {c: (None if t[i] < 0 else float(t[i])) for i, c in enumerate(SPLIT_CANDIDATES)}
+
+
+def splitk_autotune_splits(A, B, out, workspace, workspace_bytes, M, N, K, dtype, fused=0, reps=20,
+                           stream=None) -> tuple[int, int, dict]:
+    """(splits, k_per_split, {candidate: us per call or None}) measured on the device."""
+    s, k = ctypes.c_int64(), ctypes.c_int64()
+    us = (ctypes.c_float * len(SPLIT_CANDIDATES))()
+    _check(lib().splitk_autotune_splits(_ptr(A), _ptr(B), _ptr(out), _ptr(workspace), workspace_bytes, M, N, K,
+                                        dtype_code(dtype), fused, reps, _stream(stream), ctypes.byref(s),
+                                        ctypes.byref(k), us), "splitk_autotune_splits")
+    return s.value, k.value, {c: (None if us[i] < 0 else float(us[i])) for i, c in enumerate(SPLIT_CANDIDATES)}
 
 
 def splitk_get_device_status(stream=None) -> int:

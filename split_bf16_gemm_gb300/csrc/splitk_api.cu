@@ -122,6 +122,32 @@ size_t counter_bytes(int64_t M, int64_t N)
 
 }  // namespace
 
+namespace splitk {
+
+int check_gemm_bt(const void *A, const void *B, const float *out, const void *workspace, size_t workspace_bytes,
+                  int64_t M, int64_t N, int64_t K, int64_t splits, int64_t k_per_split, int dtype, int fused)
+{
+    int st = validate_gemm(A, B, M, N, K, splits, k_per_split, dtype);
+    if (st != SPLITK_OK) return st;
+    if (fused != 0 && fused != 1 && fused != 3) return SPLITK_ERR_CONFIG;
+    if (!out || !workspace) return SPLITK_ERR_NULL;
+    if (!aligned16(out) || !aligned16(workspace)) return SPLITK_ERR_ALIGN;
+    const size_t ws_need = gemm_bt_workspace_bytes(M, N, K, splits, k_per_split, fused);
+    if (workspace_bytes < ws_need) return SPLITK_ERR_WORKSPACE;
+    const int e = elem_bytes(dtype);
+    const Range ra = range_of(A, static_cast<uint64_t>(M * K) * e);
+    const Range rb = range_of(B, static_cast<uint64_t>(N * K) * e);
+    const Range ro = range_of(out, static_cast<uint64_t>(M * N) * 4);
+    const Range rw = range_of(workspace, ws_need);
+    if (overlap(ro, ra) || overlap(ro, rb) || overlap(rw, ra) || overlap(rw, rb) || overlap(rw, ro))
+        return SPLITK_ERR_ALIAS;
+    return SPLITK_OK;
+}
+
+size_t counters_offset(int64_t M, int64_t N, int64_t splits) { return partials_bytes(M, N, splits); }
+
+}  // namespace splitk
+
 extern "C" {
 
 int splitk_check_geometry(int64_t M, int64_t N, int64_t K, int64_t splits, int64_t k_per_split)
@@ -188,20 +214,8 @@ int gemm_bt_workspace_init(void *workspace, size_t workspace_bytes, void *stream
 int gemm_bt(const void *A, const void *B, float *out, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
             int64_t K, int64_t splits, int64_t k_per_split, int dtype, int fused, void *stream)
 {
-    int st = validate_gemm(A, B, M, N, K, splits, k_per_split, dtype);
+    int st = splitk::check_gemm_bt(A, B, out, workspace, workspace_bytes, M, N, K, splits, k_per_split, dtype, fused);
     if (st != SPLITK_OK) return st;
-    if (fused != 0 && fused != 1 && fused != 3) return SPLITK_ERR_CONFIG;
-    if (!out || !workspace) return SPLITK_ERR_NULL;
-    if (!aligned16(out) || !aligned16(workspace)) return SPLITK_ERR_ALIGN;
-    const size_t ws_need = gemm_bt_workspace_bytes(M, N, K, splits, k_per_split, fused);
-    if (workspace_bytes < ws_need) return SPLITK_ERR_WORKSPACE;
-    const int e = elem_bytes(dtype);
-    const Range ra = range_of(A, static_cast<uint64_t>(M * K) * e);
-    const Range rb = range_of(B, static_cast<uint64_t>(N * K) * e);
-    const Range ro = range_of(out, static_cast<uint64_t>(M * N) * 4);
-    const Range rw = range_of(workspace, ws_need);
-    if (overlap(ro, ra) || overlap(ro, rb) || overlap(rw, ra) || overlap(rw, rb) || overlap(rw, ro))
-        return SPLITK_ERR_ALIAS;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float *P = static_cast<float *>(workspace);
     unsigned *counters = reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + partials_bytes(M, N, splits));

@@ -52,6 +52,9 @@ inline int64_t fused_counter_count(int64_t M, int64_t N) { return (N / 64) * ((M
 
 // Tile choice for a shape (automatic, or the process-wide override).
 TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused);
+// The planner's estimate (microseconds) of one tensor-core launch of that
+// plan behind another launch, the in-launch split sum included when fused.
+double estimate_tc_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused);
 void set_tile_override(int bn, int chunks, int kbs);
 
 // Kernel launches; each returns the launch's CUDA error.
@@ -60,6 +63,12 @@ cudaError_t launch_simt_f32(const float *A, const float *B, float *P, int64_t M,
                             int64_t S, int64_t kps, cudaStream_t stream);
 cudaError_t launch_reduce(const float *P, float *out, int64_t S, int64_t count, cudaStream_t stream);
 cudaError_t launch_prepare(const void *W, void *B, int64_t K, int64_t N, int elem_bytes, cudaStream_t stream);
+
+// gemm_bt's argument checks (status as gemm_bt returns it; nothing launched),
+// and where the fused path's counters start in its workspace.
+int check_gemm_bt(const void *A, const void *B, const float *out, const void *workspace, size_t workspace_bytes,
+                  int64_t M, int64_t N, int64_t K, int64_t splits, int64_t k_per_split, int dtype, int fused);
+size_t counters_offset(int64_t M, int64_t N, int64_t splits);
 
 // Last-error record (per host thread): what failed and the CUDA error or
 // driver result it returned.  note_error passes `e` through.

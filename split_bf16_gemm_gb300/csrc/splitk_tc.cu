@@ -710,6 +710,23 @@ double model_us(int64_t M, int64_t N, int64_t S, int bn, int chunks, int64_t chu
 
 }  // namespace
 
+double estimate_tc_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused)
+{
+    const TilePlan p = plan_tc(M, N, K, S, kps, fused);
+    // fixed cost of a launch behind another: the dependency hand-off and the
+    // first stage landing (about 2.3 us on GB300)
+    double t = 2.3 + model_us(M, N, S, p.bn, p.chunks, p.chunk_len, p.cluster);
+    if (p.split_sum == 1) {
+        // the last split of each piece range reads the others' partials back:
+        // about 1 us of fence and arrival, one L2 round trip (0.7 us) per 8
+        // splits, and the bytes at about 60 GB/s into that CTA
+        const double rows = static_cast<double>(std::min<int64_t>(M, kTileM));
+        const double bytes = static_cast<double>(S - 1) * rows * p.bn * 4 / p.chunks;
+        t += 1.0 + 0.7 * static_cast<double>((S + 7) / 8) + bytes / 6.0e4;
+    }
+    return t;
+}
+
 TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused)
 {
     // Stages of several k-blocks load as one 3-D box per operand, which the

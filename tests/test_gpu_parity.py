@@ -424,3 +424,41 @@ def test_host_batch_back_to_back_shared_staging(lib):
         r2 = o2.numpy()[(count - 1 - i) * M * N:(count - i) * M * N]
         assert np.array_equal(r1.view(np.uint32), want[i].view(np.uint32)), i
         assert np.array_equal(r2.view(np.uint32), want[i].view(np.uint32)), i
+
+
+@pytest.mark.parametrize("case", [(96, 512, 512, "bf16", 1), (96, 512, 512, "bf16", 0), (64, 128, 160, "f16", 1),
+                                  (32, 512, 2048, "bf16", 1), (32, 64, 128, "f32", 0)],
+                         ids=lambda c: f"{c[3]}-M{c[0]}N{c[1]}K{c[2]}-fused{c[4]}")
+def test_autotune_splits(lib, case):
+    """The measured split choice is the fastest candidate it timed, a legal
+    geometry; `out` then holds a correct result, and a later gemm_bt with the
+    chosen split on the same workspace (counters re-zeroed) gives it again."""
+    sk = lib
+    M, N, K, dt, fused = case
+    cand = {}
+    for n in (1, 2, 4, 8, 16):
+        kps = -(-(-(-K // n)) // 32) * 32
+        cand[n] = (-(-K // kps), kps)
+    nbytes = max(sk.gemm_bt_workspace_bytes(M, N, K, S, kps) for S, kps in cand.values())
+    ops, _, _, Or, SO = oracle_case(M, N, K, cand[1][0], cand[1][1], dt)
+    A, B = device_operand(ops.A, dt), device_operand(ops.B, dt)
+    ws = Guarded(nbytes // 4, 0.0)
+    out = Guarded(M * N)
+    S, kps, us = sk.splitk_autotune_splits(A, B, out.data, ws.data, nbytes, M, N, K, dt, fused=fused, reps=10)
+    torch.cuda.synchronize()
+    assert (S, kps) in cand.values()
+    timed = {c: t for c, t in us.items() if t is not None}
+    assert timed and all(t > 0 for t in timed.values())
+    assert min(timed.values()) == timed[min(timed, key=timed.get)]
+    assert cand[min(timed, key=timed.get)] == (S, kps)
+    seen = set()
+    for n in (1, 2, 4, 8, 16):   # a repeated split count is timed once
+        assert (us[n] is None) == (cand[n][0] in seen)
+        seen.add(cand[n][0])
+    assert out.guards_intact() and ws.guards_intact()
+    got = out.numpy().reshape(M, N)
+    assert max_scaled_error(got, Or, SO) <= TOL_FINAL[dt]
+    again = Guarded(M * N)
+    sk.gemm_bt(A, B, again.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=fused)
+    assert sk.splitk_get_device_status() == 0
+    assert np.array_equal(again.numpy().view(np.uint32), out.numpy().view(np.uint32))

@@ -281,3 +281,61 @@ def test_host_batch_rejections(L):
     assert call(B=bd.pointer_array([B0, ST + need - 64])) == bd.ERR_ALIAS
     assert call(st=Oh - 64) == bd.ERR_ALIAS
     assert call(M=48, A=0) == bd.ERR_SHAPE
+
+
+def test_choose_splits_is_legal(L, orc):
+    """The model's choice is always a legal geometry drawn from the candidates."""
+    for M in (32, 96, 256):
+        for N in (64, 512, 1024):
+            for K in (32, 128, 160, 512, 2048, 4096):
+                for dt in ("bf16", "f16", "f32"):
+                    for fused in (0, 1):
+                        S, kps, t = sk.splitk_choose_splits(M, N, K, dt, fused)
+                        assert orc.contract(M, N, K, S, kps) == 0, (M, N, K, S, kps)
+                        assert kps % 32 == 0 and all(v is not None and v > 0 for v in t.values())
+                        best = min(t, key=t.get)
+                        k_best = -(-(-(-K // best)) // 32) * 32
+                        assert (S, kps) == (-(-K // k_best), k_best)
+                        legal = set()
+                        for n in (1, 2, 4, 8, 16):
+                            k = -(-(-(-K // n)) // 32) * 32
+                            legal.add((-(-K // k), k))
+                        assert (S, kps) in legal
+
+
+def test_choose_splits_rejections(L):
+    out = (ctypes.c_int64 * 2)()
+    assert L.splitk_choose_splits(48, 64, 128, bd.BF16, 0, ctypes.byref(out, 0), ctypes.byref(out, 8), None) \
+        == bd.ERR_SHAPE
+    assert L.splitk_choose_splits(32, 96, 128, bd.BF16, 0, ctypes.byref(out, 0), ctypes.byref(out, 8), None) \
+        == bd.ERR_SHAPE
+    assert L.splitk_choose_splits(32, 64, 128, 7, 0, ctypes.byref(out, 0), ctypes.byref(out, 8), None) \
+        == bd.ERR_DTYPE
+    assert L.splitk_choose_splits(32, 64, 128, bd.BF16, 2, ctypes.byref(out, 0), ctypes.byref(out, 8), None) \
+        == bd.ERR_CONFIG
+    assert L.splitk_choose_splits(32, 64, 128, bd.BF16, 0, None, ctypes.byref(out, 8), None) == bd.ERR_NULL
+
+
+def test_autotune_rejections(L):
+    """Every rejection happens before the library touches CUDA (no GPU here)."""
+    M, N, K = 32, 64, 128
+    need16 = max(sk.gemm_bt_workspace_bytes(M, N, K, -(-K // k), k) for k in (32, 64, 128))
+    s, k = ctypes.c_int64(), ctypes.c_int64()
+
+    def call(A=A0, B=B0, O=O0, W=W0, wsb=need16, M=M, N=N, K=K, dtype=bd.BF16, fused=0, reps=5):
+        return L.splitk_autotune_splits(A, B, O, W, wsb, M, N, K, dtype, fused, reps, None, ctypes.byref(s),
+                                        ctypes.byref(k), None)
+
+    assert call(M=48) == bd.ERR_SHAPE
+    assert call(dtype=9) == bd.ERR_DTYPE
+    assert call(fused=2) == bd.ERR_CONFIG
+    assert call(reps=0) == bd.ERR_CONFIG
+    assert call(reps=1001) == bd.ERR_CONFIG
+    assert call(A=0) == bd.ERR_NULL
+    assert call(O=0) == bd.ERR_NULL
+    assert call(W=0) == bd.ERR_NULL
+    assert call(A=A0 + 8) == bd.ERR_ALIGN
+    assert call(O=A0) == bd.ERR_ALIAS
+    assert call(wsb=16) == bd.ERR_WORKSPACE
+    assert L.splitk_autotune_splits(A0, B0, O0, W0, need16, M, N, K, bd.BF16, 0, 5, None, None, ctypes.byref(k),
+                                    None) == bd.ERR_NULL
