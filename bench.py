@@ -387,6 +387,31 @@ def run_ours(args, rank, world, dev, torch, dist):
     # out to pinned host memory (gemm_bt_host_batch), weights resident
     e2e = measure_e2e(sk, torch, stream, groups, pack, fused, args.steps)
 
+    # the same operations reading the weight in its [K,N] layout (gemm_kn):
+    # W = B^T, made on the device with the preparation kernel (B^T of an
+    # [N,K] matrix), so every operation has its own resident W
+    for inst in pool:
+        inst["W"] = torch.empty((K, N), dtype=torch.bfloat16, device=dev)
+        sk.splitk_prepare_bt(inst["B"], inst["W"], N, K, DTYPE, stream=stream)
+    torch.cuda.synchronize()
+
+    def op_kn(inst, f):
+        sk.gemm_kn(inst["A"], inst["W"], inst["out"], inst["ws"], nbytes, M, N, K, SPLITS, KPS, DTYPE,
+                   fused=f, stream=stream)
+
+    kn_us = {}
+    for f, name in ((1, "fused_op"), (0, "two_pass_op")):
+        kg = [capture(torch, stream, lambda grp=grp, f=f: [op_kn(i, f) for i in grp]) for grp in groups]
+        time_graphs(torch, stream, kg, 5)
+        kn_us[name] = round(time_graphs(torch, stream, kg, reps) * 1e3 / (reps * pack), 4)
+    ref = pool[0]["out"].clone()
+    op(pool[0])
+    torch.cuda.synchronize()
+    if not torch.equal(ref, pool[0]["out"]):
+        raise RuntimeError("the [K,N] and [N,K] weight layouts give different outputs")
+    for inst in pool:
+        del inst["W"]
+
     # weight preparation (B = W^T), a one-shot cost outside the operation
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     prep_n = 24
@@ -436,6 +461,8 @@ def run_ours(args, rank, world, dev, torch, dist):
                        "two_pass_op": round(two_pass_us, 4),
                        "fused_op" if fused else "two_pass_op_graph": round(us_per_op * world, 4)},
         "e2e": e2e,
+        "kn_layout": {"what": "the same operations with the weight in its [K,N] layout (gemm_kn, MN-major B)",
+                      "us": kn_us},
         "prepare": {"what": "weight preparation B[N,K] = W[K,N]^T (one-shot, outside the operation)",
                     "us": round(prep_us, 3), "bytes": 2 * K * N * 2,
                     "achieved_gbs": round(2 * K * N * 2 / (prep_us * 1e-6) / 1e9, 1),

@@ -151,6 +151,22 @@ int gemm_bt(const void *A, const void *B, float *out, void *workspace,
             int64_t splits, int64_t k_per_split, int dtype, int fused,
             void *stream);
 
+/* The same two operations with the weight in its own [K,N] layout, the other
+ * layout the pages keep resident ("Wider consecutive-weight NAX GEMM",
+ * section "Performance method": both layouts uploaded once); no preparation
+ * step.
+ *   W  device, [K,N] row-major, element type `dtype`; B[n,k] = W[k,n]
+ * Every other argument, the contract, the checks and the results are those of
+ * gemm_splitk_bt and gemm_bt with B = W^T; the tensor cores read W
+ * N-contiguous (MN-major operand). */
+int gemm_splitk_kn(const void *A, const void *W, float *partials, int64_t M,
+                   int64_t N, int64_t K, int64_t splits, int64_t k_per_split,
+                   int dtype, void *stream);
+int gemm_kn(const void *A, const void *W, float *out, void *workspace,
+            size_t workspace_bytes, int64_t M, int64_t N, int64_t K,
+            int64_t splits, int64_t k_per_split, int dtype, int fused,
+            void *stream);
+
 /* gemm_bt for callers that cannot allocate device memory.  The paper has no
  * counterpart of this entry point; it exists for hosts that hand an operator
  * only its input and output buffers and forbid allocation while it runs (the

@@ -27,6 +27,7 @@ EXPORTS = (
     "splitk_describe_launch", "splitk_selftest_bounded_wait", "splitk_last_error",
     "gemm_bt_workspace_init", "gemm_bt_noalloc", "splitk_prepare_bt",
     "gemm_bt_host_staging_bytes", "gemm_bt_host_batch", "splitk_choose_splits", "splitk_autotune_splits",
+    "gemm_splitk_kn", "gemm_kn",
 )
 NOALLOC_MAX_BYTES = 32 << 20   # SPLITK_NOALLOC_MAX_BYTES
 
@@ -59,6 +60,8 @@ def lib() -> ctypes.CDLL:
             L.gemm_bt_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i32]
             L.gemm_bt_workspace_bytes.restype = sz
             L.gemm_bt.argtypes = [vp, vp, vp, vp, sz, i64, i64, i64, i64, i64, i32, i32, vp]
+            L.gemm_splitk_kn.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, vp]
+            L.gemm_kn.argtypes = [vp, vp, vp, vp, sz, i64, i64, i64, i64, i64, i32, i32, vp]
             L.splitk_get_device_status.argtypes = [vp]
             L.splitk_status_string.argtypes = [i32]
             L.splitk_status_string.restype = ctypes.c_char_p
@@ -77,6 +80,7 @@ def lib() -> ctypes.CDLL:
             L.splitk_last_error.argtypes = []
             L.splitk_last_error.restype = ctypes.c_char_p
             for name in ("splitk_check_geometry", "gemm_splitk_bt", "splitk_reduce", "gemm_bt",
+                         "gemm_splitk_kn", "gemm_kn",
                          "gemm_bt_workspace_init", "gemm_bt_noalloc", "splitk_prepare_bt",
                          "gemm_bt_host_batch", "splitk_choose_splits", "splitk_autotune_splits",
                          "splitk_get_device_status", "splitk_set_tile_override",
@@ -143,6 +147,19 @@ def splitk_check_geometry(M, N, K, splits, k_per_split) -> int:
 def gemm_splitk_bt(A, B, partials, M, N, K, splits, k_per_split, dtype, stream=None) -> None:
     _check(lib().gemm_splitk_bt(_ptr(A), _ptr(B), _ptr(partials), M, N, K, splits, k_per_split,
                                 dtype_code(dtype), _stream(stream)), "gemm_splitk_bt")
+
+
+def gemm_splitk_kn(A, W, partials, M, N, K, splits, k_per_split, dtype, stream=None) -> None:
+    """gemm_splitk_bt with the weight W in its [K,N] layout."""
+    _check(lib().gemm_splitk_kn(_ptr(A), _ptr(W), _ptr(partials), M, N, K, splits, k_per_split,
+                                dtype_code(dtype), _stream(stream)), "gemm_splitk_kn")
+
+
+def gemm_kn(A, W, out, workspace, workspace_bytes, M, N, K, splits, k_per_split, dtype, fused=0,
+            stream=None) -> None:
+    """gemm_bt with the weight W in its [K,N] layout."""
+    _check(lib().gemm_kn(_ptr(A), _ptr(W), _ptr(out), _ptr(workspace), workspace_bytes, M, N, K,
+                         splits, k_per_split, dtype_code(dtype), fused, _stream(stream)), "gemm_kn")
 
 
 def splitk_prepare_bt(W, B, K, N, dtype, stream=None) -> None:

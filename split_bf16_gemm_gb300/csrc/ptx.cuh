@@ -188,14 +188,25 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
            (static_cast<uint64_t>(2) << 61);
 }
 
-// Instruction descriptor for tcgen05.mma .kind::f16 with F32 accumulation,
-// both operands K-major: D format F32 (bits 4-5 = 1), A and B format
-// (bits 7-9, 10-12: 0 = F16, 1 = BF16), N >> 3 (bits 17-22), M >> 4
-// (bits 24-28).
-__host__ __device__ constexpr uint32_t idesc_f16_f32acc(bool bf16, uint32_t m, uint32_t n)
+// Shared-memory descriptor of an MN-major operand in 128-byte swizzle: rows
+// of 128 bytes (64 consecutive MN elements) along K, 8-row (1 KB) groups
+// 1024 bytes apart along K (stride byte offset), groups of 64 MN elements
+// `lbo` bytes apart (leading byte offset); version 1, swizzle 2.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t lbo)
 {
-    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((n >> 3) << 17) |
-           ((m >> 4) << 24);
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor for tcgen05.mma .kind::f16 with F32 accumulation:
+// D format F32 (bits 4-5 = 1), A and B format (bits 7-9, 10-12: 0 = F16,
+// 1 = BF16), A K-major (bit 15 = 0), B K-major or, with `b_mn`, MN-major
+// (bit 16), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t idesc_f16_f32acc(bool bf16, uint32_t m, uint32_t n, bool b_mn = false)
+{
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn ? 1u : 0u) << 16) |
+           ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T for one K=16 slice, issued by one thread.

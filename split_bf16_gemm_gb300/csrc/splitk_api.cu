@@ -99,13 +99,15 @@ int validate_gemm(const void *A, const void *B, int64_t M, int64_t N, int64_t K,
 // there is normally a reduce, which leaves no SM free, and prefetches issued
 // once every CTA is running only compete with the loads.
 int run_partial_pass(const void *A, const void *B, float *P, float *out, unsigned *counters, int64_t M, int64_t N,
-                     int64_t K, int64_t S, int64_t kps, int dtype, bool fused, bool prefetch, cudaStream_t stream)
+                     int64_t K, int64_t S, int64_t kps, int dtype, bool fused, bool prefetch, bool b_kn,
+                     cudaStream_t stream)
 {
     if (dtype == SPLITK_F32) {
         return cuda_status(splitk::launch_simt_f32(static_cast<const float *>(A), static_cast<const float *>(B), P,
-                                                   M, N, K, S, kps, stream));
+                                                   M, N, K, S, kps, b_kn, stream));
     }
     GemmProblem pr{A, B, P, out, counters, M, N, K, S, kps, dtype == SPLITK_BF16};
+    pr.b_kn = b_kn;
     TilePlan plan = splitk::plan_tc(M, N, K, S, kps, fused);
     if (!prefetch) plan.prefetchers = 0;
     return cuda_status(splitk::launch_tc(pr, plan, stream));
@@ -155,8 +157,8 @@ int splitk_check_geometry(int64_t M, int64_t N, int64_t K, int64_t splits, int64
     return geometry_status(M, N, K, splits, k_per_split);
 }
 
-int gemm_splitk_bt(const void *A, const void *B, float *partials, int64_t M, int64_t N, int64_t K, int64_t splits,
-                   int64_t k_per_split, int dtype, void *stream)
+static int gemm_splitk_impl(const void *A, const void *B, float *partials, int64_t M, int64_t N, int64_t K,
+                            int64_t splits, int64_t k_per_split, int dtype, bool b_kn, void *stream)
 {
     int st = validate_gemm(A, B, M, N, K, splits, k_per_split, dtype);
     if (st != SPLITK_OK) return st;
@@ -168,7 +170,19 @@ int gemm_splitk_bt(const void *A, const void *B, float *partials, int64_t M, int
     const Range rp = range_of(partials, static_cast<uint64_t>(splits * M * N) * 4);
     if (overlap(rp, ra) || overlap(rp, rb)) return SPLITK_ERR_ALIAS;
     return run_partial_pass(A, B, partials, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false, false,
-                            static_cast<cudaStream_t>(stream));
+                            b_kn, static_cast<cudaStream_t>(stream));
+}
+
+int gemm_splitk_bt(const void *A, const void *B, float *partials, int64_t M, int64_t N, int64_t K, int64_t splits,
+                   int64_t k_per_split, int dtype, void *stream)
+{
+    return gemm_splitk_impl(A, B, partials, M, N, K, splits, k_per_split, dtype, false, stream);
+}
+
+int gemm_splitk_kn(const void *A, const void *W, float *partials, int64_t M, int64_t N, int64_t K, int64_t splits,
+                   int64_t k_per_split, int dtype, void *stream)
+{
+    return gemm_splitk_impl(A, W, partials, M, N, K, splits, k_per_split, dtype, true, stream);
 }
 
 int splitk_reduce(const float *partials, float *out, int64_t splits, int64_t M, int64_t N, void *stream)
@@ -211,8 +225,9 @@ int gemm_bt_workspace_init(void *workspace, size_t workspace_bytes, void *stream
         cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)), "cudaMemsetAsync(workspace)"));
 }
 
-int gemm_bt(const void *A, const void *B, float *out, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
-            int64_t K, int64_t splits, int64_t k_per_split, int dtype, int fused, void *stream)
+static int gemm_impl(const void *A, const void *B, float *out, void *workspace, size_t workspace_bytes, int64_t M,
+                     int64_t N, int64_t K, int64_t splits, int64_t k_per_split, int dtype, int fused, bool b_kn,
+                     void *stream)
 {
     int st = splitk::check_gemm_bt(A, B, out, workspace, workspace_bytes, M, N, K, splits, k_per_split, dtype, fused);
     if (st != SPLITK_OK) return st;
@@ -223,11 +238,23 @@ int gemm_bt(const void *A, const void *B, float *out, void *workspace, size_t wo
         // fused == 1 keeps no partials where the cluster sums the splits on chip
         const TilePlan plan = splitk::plan_tc(M, N, K, splits, k_per_split, true);
         float *keep = (fused == 1 && plan.split_sum == 2) ? nullptr : P;
-        return run_partial_pass(A, B, keep, out, counters, M, N, K, splits, k_per_split, dtype, true, true, s);
+        return run_partial_pass(A, B, keep, out, counters, M, N, K, splits, k_per_split, dtype, true, true, b_kn, s);
     }
-    st = run_partial_pass(A, B, P, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false, false, s);
+    st = run_partial_pass(A, B, P, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false, false, b_kn, s);
     if (st != SPLITK_OK) return st;
     return cuda_status(splitk::launch_reduce(P, out, splits, M * N, s));
+}
+
+int gemm_bt(const void *A, const void *B, float *out, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
+            int64_t K, int64_t splits, int64_t k_per_split, int dtype, int fused, void *stream)
+{
+    return gemm_impl(A, B, out, workspace, workspace_bytes, M, N, K, splits, k_per_split, dtype, fused, false, stream);
+}
+
+int gemm_kn(const void *A, const void *W, float *out, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
+            int64_t K, int64_t splits, int64_t k_per_split, int dtype, int fused, void *stream)
+{
+    return gemm_impl(A, W, out, workspace, workspace_bytes, M, N, K, splits, k_per_split, dtype, fused, true, stream);
 }
 
 const char *splitk_last_error(void) { return splitk::last_error_message(); }

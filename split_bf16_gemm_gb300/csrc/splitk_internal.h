@@ -11,12 +11,13 @@ namespace splitk {
 // What one tensor-core launch computes.
 struct GemmProblem {
     const void *A;      // [M,K] row-major, 16-bit elements
-    const void *B;      // [N,K] row-major, 16-bit elements
+    const void *B;      // [N,K] row-major, 16-bit elements; with b_kn, the weight [K,N] row-major
     float *P;           // [S,M,N] partials, or nullptr when not written
     float *out;         // [M,N] sum over splits, or nullptr (two-kernel path)
     unsigned *counters; // fused: per (tile, cluster rank) arrival counters, zero between calls
     int64_t M, N, K, S, kps;
     bool bf16;          // operand type: BF16 (true) or F16 (false)
+    bool b_kn = false;  // B given as the [K,N] weight itself (read MN-major)
 };
 
 // How it is tiled.  One CTA computes a 128 x bn tile of one K-chunk of one
@@ -60,7 +61,7 @@ void set_tile_override(int bn, int chunks, int kbs);
 // Kernel launches; each returns the launch's CUDA error.
 cudaError_t launch_tc(const GemmProblem &p, const TilePlan &plan, cudaStream_t stream);
 cudaError_t launch_simt_f32(const float *A, const float *B, float *P, int64_t M, int64_t N, int64_t K,
-                            int64_t S, int64_t kps, cudaStream_t stream);
+                            int64_t S, int64_t kps, bool b_kn, cudaStream_t stream);
 cudaError_t launch_reduce(const float *P, float *out, int64_t S, int64_t count, cudaStream_t stream);
 cudaError_t launch_prepare(const void *W, void *B, int64_t K, int64_t N, int elem_bytes, cudaStream_t stream);
 

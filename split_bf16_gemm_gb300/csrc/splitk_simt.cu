@@ -8,7 +8,9 @@
 //
 // Tiling: a 256-thread block owns a 64x64 tile of one split; each thread a
 // 4x4 sub-tile.  A and B are staged through shared memory 16 k at a time,
-// stored k-major so the inner loop reads broadcast-free rows.
+// stored k-major so the inner loop reads broadcast-free rows.  B is either the
+// prepared [N,K] weight or the [K,N] weight itself; both fill the same
+// shared-memory tile, so the products and their order are the same.
 
 #include "splitk_internal.h"
 
@@ -19,6 +21,8 @@ constexpr int kT = 64;     // tile rows and columns
 constexpr int kKs = 16;    // k per stage
 constexpr int kSimtThreads = 256;
 
+// KN: B is the weight W[K,N] itself (element (n,k) at k*N + n), else B[N,K].
+template <bool KN>
 __global__ void __launch_bounds__(kSimtThreads)
     simt_f32_kernel(const float *__restrict__ A, const float *__restrict__ B, float *__restrict__ P, int M, int N,
                     int K, int kps)
@@ -39,9 +43,15 @@ __global__ void __launch_bounds__(kSimtThreads)
     for (int k0 = ks; k0 < ke; k0 += kKs) {
         for (int idx = threadIdx.x; idx < kT * kKs; idx += kSimtThreads) {
             const int r = idx / kKs, kk = idx % kKs, k = k0 + kk;
-            const int m = m0 + r, n = n0 + r;
+            const int m = m0 + r;
             As[kk][r] = (m < M && k < ke) ? A[static_cast<size_t>(m) * K + k] : 0.f;
-            Bs[kk][r] = (n < N && k < ke) ? B[static_cast<size_t>(n) * K + k] : 0.f;
+            if (!KN) {
+                const int n = n0 + r;
+                Bs[kk][r] = (n < N && k < ke) ? B[static_cast<size_t>(n) * K + k] : 0.f;
+            } else {   // consecutive threads read consecutive n of one W row
+                const int kb = idx / kT, c = idx % kT, kw = k0 + kb;
+                Bs[kb][c] = (kw < ke) ? B[static_cast<size_t>(kw) * N + n0 + c] : 0.f;
+            }
         }
         __syncthreads();
 #pragma unroll
@@ -71,11 +81,15 @@ __global__ void __launch_bounds__(kSimtThreads)
 }  // namespace
 
 cudaError_t launch_simt_f32(const float *A, const float *B, float *P, int64_t M, int64_t N, int64_t K, int64_t S,
-                            int64_t kps, cudaStream_t stream)
+                            int64_t kps, bool b_kn, cudaStream_t stream)
 {
     dim3 grid(static_cast<unsigned>(N / kT), static_cast<unsigned>((M + kT - 1) / kT), static_cast<unsigned>(S));
-    simt_f32_kernel<<<grid, kSimtThreads, 0, stream>>>(A, B, P, static_cast<int>(M), static_cast<int>(N),
-                                                      static_cast<int>(K), static_cast<int>(kps));
+    if (b_kn)
+        simt_f32_kernel<true><<<grid, kSimtThreads, 0, stream>>>(A, B, P, static_cast<int>(M), static_cast<int>(N),
+                                                                static_cast<int>(K), static_cast<int>(kps));
+    else
+        simt_f32_kernel<false><<<grid, kSimtThreads, 0, stream>>>(A, B, P, static_cast<int>(M), static_cast<int>(N),
+                                                                 static_cast<int>(K), static_cast<int>(kps));
     return note_error(cudaGetLastError(), "F32 FMA kernel launch");
 }
 

@@ -73,6 +73,7 @@ struct TcArgs {
     const uint8_t *A, *B;  // operands, for the L2 prefetch
     uint64_t a_bytes, b_bytes;
     int prefetchers;       // CTAs, first in dispatch order, that prefetch A and B into L2
+    int b_kn;              // B is the [K,N] weight: loaded and read MN-major
 };
 
 // Part j of `parts` (whole 128-byte lines) of [p, p + bytes) into L2, one
@@ -176,11 +177,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (args.three_d) {                         // one box per operand: kbs k-blocks at once
             const int kb = k_lo / kBlockK + i * kbs;
             ptx::tma_load_3d(sa, &tmA, bar, 0, m_tile * kTileM, kb, ptx::l2_policy_evict_last());
-            ptx::tma_load_3d(sa + kbs * Sh::kABytes, &tmB, bar, 0, n_tile * BN, kb, ptx::l2_policy_evict_normal());
+            if (!args.b_kn)
+                ptx::tma_load_3d(sa + kbs * Sh::kABytes, &tmB, bar, 0, n_tile * BN, kb,
+                                 ptx::l2_policy_evict_normal());
         } else {                                    // kbs == 1
             const int kx = k_lo + i * kBlockK;
             ptx::tma_load_2d(sa, &tmA, bar, kx, m_tile * kTileM, ptx::l2_policy_evict_last());
-            ptx::tma_load_2d(sa + Sh::kABytes, &tmB, bar, kx, n_tile * BN, ptx::l2_policy_evict_normal());
+            if (!args.b_kn)
+                ptx::tma_load_2d(sa + Sh::kABytes, &tmB, bar, kx, n_tile * BN, ptx::l2_policy_evict_normal());
+        }
+        if (args.b_kn) {
+            // the [K,N] weight: BN/64 boxes of 64 columns x kbs*64 k-rows
+            // (128-byte rows, N contiguous), one after another
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+                ptx::tma_load_2d(sa + kbs * Sh::kABytes + static_cast<uint32_t>(j * kbs) * 8192u, &tmB, bar,
+                                 n_tile * BN + j * 64, k_lo + i * kbs * kBlockK, ptx::l2_policy_evict_normal());
         }
     };
     if (tid == 0) {
@@ -247,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued_s = i;
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
-        const uint32_t idesc = ptx::idesc_f16_f32acc(args.bf16 != 0, kTileM, BN);
+        const uint32_t idesc = ptx::idesc_f16_f32acc(args.bf16 != 0, kTileM, BN, args.b_kn != 0);
+        const uint32_t b_lbo = static_cast<uint32_t>(kbs) * 8192u;   // [K,N]: next 64 columns
         int i = 0;
         for (; i < nstg; ++i) {
             const int st = i % stages;
@@ -263,10 +276,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kb = i * kbs + j;
                 if (kb >= nkb) break;
                 const uint64_t ad = ptx::sdesc_kmajor_sw128(sa + j * Sh::kABytes);
-                const uint64_t bd = ptx::sdesc_kmajor_sw128(sb + j * Sh::kBBytes);
                 const int ksteps = min(kBlockK, klen - kb * kBlockK) / 16;   // 4, or 2 for a 32-long tail
-                for (int k = 0; k < ksteps; ++k)   // +32 bytes along K inside the swizzled row
-                    ptx::mma_f16(tmem, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                if (!args.b_kn) {
+                    const uint64_t bd = ptx::sdesc_kmajor_sw128(sb + j * Sh::kBBytes);
+                    for (int k = 0; k < ksteps; ++k)   // +32 bytes along K inside the swizzled row
+                        ptx::mma_f16(tmem, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                } else {
+                    for (int k = 0; k < ksteps; ++k)   // A: +32 bytes; B: 16 k-rows of 128 bytes further
+                        ptx::mma_f16(tmem, ad + 2u * k,
+                                     ptx::sdesc_mnmajor_sw128(sb + static_cast<uint32_t>(j * 64 + k * 16) * 128u,
+                                                              b_lbo),
+                                     idesc, (kb | k) != 0 ? 1u : 0u);
+                }
             }
             ptx::mma_commit(empty_bar(st));    // frees the slot once these MMAs have read it
         }
@@ -819,10 +840,15 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
     if (pr.P == nullptr && plan.split_sum != 2)
         return note_error(cudaErrorInvalidValue, "partials are needed unless the cluster sums the splits");
     CUtensorMap ta, tb;
-    const bool ok = plan.three_d ? encode_operand_3d(&ta, pr.A, pr.M, pr.K, kTileM, plan.kbs, pr.bf16) &&
-                                       encode_operand_3d(&tb, pr.B, pr.N, pr.K, plan.bn, plan.kbs, pr.bf16)
-                                 : encode_operand(&ta, pr.A, pr.M, pr.K, kTileM, pr.bf16) &&
-                                       encode_operand(&tb, pr.B, pr.N, pr.K, plan.bn, pr.bf16);
+    const int kbs = plan.three_d ? plan.kbs : 1;
+    const bool ok_a = plan.three_d ? encode_operand_3d(&ta, pr.A, pr.M, pr.K, kTileM, plan.kbs, pr.bf16)
+                                   : encode_operand(&ta, pr.A, pr.M, pr.K, kTileM, pr.bf16);
+    // the [K,N] weight is a row-major matrix of K rows of N: boxes of 64
+    // columns by kbs*64 rows
+    const bool ok_b = pr.b_kn ? encode_operand(&tb, pr.B, pr.K, pr.N, kbs * kBlockK, pr.bf16)
+                              : plan.three_d ? encode_operand_3d(&tb, pr.B, pr.N, pr.K, plan.bn, plan.kbs, pr.bf16)
+                                             : encode_operand(&tb, pr.B, pr.N, pr.K, plan.bn, pr.bf16);
+    const bool ok = ok_a && ok_b;
     if (!ok) return cudaErrorInvalidValue;
     TcArgs a = {};
     a.P = pr.P;
@@ -848,6 +874,7 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
     a.a_bytes = static_cast<uint64_t>(pr.M * pr.K) * 2;
     a.b_bytes = static_cast<uint64_t>(pr.N * pr.K) * 2;
     a.prefetchers = plan.prefetchers;
+    a.b_kn = pr.b_kn ? 1 : 0;
     switch (plan.bn) {
     case 64: return launch_cluster<64>(ta, tb, a, plan, stream);
     case 128: return launch_cluster<128>(ta, tb, a, plan, stream);

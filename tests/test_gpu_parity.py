@@ -462,3 +462,80 @@ def test_autotune_splits(lib, case):
     sk.gemm_bt(A, B, again.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=fused)
     assert sk.splitk_get_device_status() == 0
     assert np.array_equal(again.numpy().view(np.uint32), out.numpy().view(np.uint32))
+
+
+KN_CASES = WORKLOADS + [(64, 128, 160, 3, 64, "bf16"), (96, 512, 512, 4, 128, "f16"), (32, 512, 2048, 16, 128, "bf16"),
+                        (64, 128, 160, 3, 64, "f32"), (96, 512, 2048, 4, 512, "f32")]
+
+
+def kn_weight(orc, ops):
+    """W = B^T (the [K,N] weight whose prepared form is B), by the oracle's transpose."""
+    return device_operand(orc.transpose(ops.B.reshape(ops.N, ops.K)), ops.dtype)
+
+
+@pytest.mark.parametrize("case", KN_CASES, ids=ids(KN_CASES))
+def test_kn_layout_matches_oracle(lib, orc, case):
+    """gemm_splitk_kn / gemm_kn with W = B^T: partials and output against the
+    oracle, guards intact, and the fused and two-kernel calls bitwise equal."""
+    sk = lib
+    M, N, K, S, kps, dt = case
+    ops, Pr, SP, Or, SO = oracle_case(M, N, K, S, kps, dt)
+    A, W = device_operand(ops.A, dt), kn_weight(orc, ops)
+    P = Guarded(S * M * N)
+    out = Guarded(M * N)
+    sk.gemm_splitk_kn(A, W, P.data, M, N, K, S, kps, dt)
+    sk.splitk_reduce(P.data, out.data, S, M, N)
+    assert sk.splitk_get_device_status() == 0
+    assert P.guards_intact() and out.guards_intact()
+    assert max_scaled_error(P.numpy().reshape(S, M, N), Pr, SP) <= TOL_PARTIAL
+    assert max_scaled_error(out.numpy().reshape(M, N), Or, SO) <= TOL_FINAL[dt]
+    for fused in (0, 1, 3):
+        ws, nbytes = workspace(M, N, K, S, kps)
+        o = Guarded(M * N)
+        sk.gemm_kn(A, W, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=fused)
+        assert sk.splitk_get_device_status() == 0
+        assert o.guards_intact() and ws.guards_intact()
+        assert np.array_equal(o.numpy().view(np.uint32), out.numpy().view(np.uint32)), f"fused={fused}"
+
+
+@pytest.mark.parametrize("case", KN_CASES, ids=ids(KN_CASES))
+def test_kn_layout_bitwise_equals_prepared(lib, orc, case):
+    """Reading the weight N-contiguous gives the same bits as reading its
+    prepared transpose K-contiguous: same products, same accumulation."""
+    sk = lib
+    M, N, K, S, kps, dt = case
+    ops = oracle_case(M, N, K, S, kps, dt)[0]
+    A, B, W = device_operand(ops.A, dt), device_operand(ops.B, dt), kn_weight(orc, ops)
+    P1, P2 = Guarded(S * M * N), Guarded(S * M * N)
+    sk.gemm_splitk_bt(A, B, P1.data, M, N, K, S, kps, dt)
+    sk.gemm_splitk_kn(A, W, P2.data, M, N, K, S, kps, dt)
+    assert sk.splitk_get_device_status() == 0
+    assert np.array_equal(P1.numpy().view(np.uint32), P2.numpy().view(np.uint32))
+
+
+@pytest.mark.parametrize("case", [(64, 128, 160, 3, 64, "bf16"), (256, 1024, 2048, 2, 1024, "bf16")],
+                         ids=ids([(64, 128, 160, 3, 64, "bf16"), (256, 1024, 2048, 2, 1024, "bf16")]))
+def test_kn_every_tiling(lib, orc, case):
+    """Every tile width (one, two or four 64-column boxes of W per stage),
+    chunk count and stage depth reads W correctly."""
+    sk = lib
+    M, N, K, S, kps, dt = case
+    ops, Pr, SP, Or, SO = oracle_case(M, N, K, S, kps, dt)
+    A, W = device_operand(ops.A, dt), kn_weight(orc, ops)
+    seen = set()
+    try:
+        for bn, ch, kb in TILINGS:
+            sk.splitk_set_tile_override(bn, ch, kb)
+            d = sk.splitk_describe_launch(M, N, K, S, kps, dt, fused=0)
+            key = (d["bn"], d["chunks"], d["kblocks_per_stage"])
+            if key in seen:
+                continue
+            seen.add(key)
+            P = Guarded(S * M * N)
+            sk.gemm_splitk_kn(A, W, P.data, M, N, K, S, kps, dt)
+            assert sk.splitk_get_device_status() == 0
+            assert P.guards_intact()
+            assert max_scaled_error(P.numpy().reshape(S, M, N), Pr, SP) <= TOL_PARTIAL, key
+    finally:
+        sk.splitk_set_tile_override(0, 0, 0)
+    assert len(seen) > 4

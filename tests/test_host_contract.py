@@ -339,3 +339,19 @@ def test_autotune_rejections(L):
     assert call(wsb=16) == bd.ERR_WORKSPACE
     assert L.splitk_autotune_splits(A0, B0, O0, W0, need16, M, N, K, bd.BF16, 0, 5, None, None, ctypes.byref(k),
                                     None) == bd.ERR_NULL
+
+
+def test_kn_rejections(L):
+    """The [K,N] entry points check exactly what their [N,K] twins check."""
+    need = sk.gemm_bt_workspace_bytes(32, 64, 128, 2, 64)
+    for fn_bt, fn_kn in ((L.gemm_splitk_bt, L.gemm_splitk_kn),):
+        for kw in (dict(M=48), dict(N=32), dict(S=3), dict(dtype=7), dict(A=0), dict(B=0), dict(P=0),
+                   dict(A=A0 + 8), dict(P=P0 + 4), dict(P=A0), dict(P=B0 - 16384 + 16)):
+            g = dict(dict(A=A0, B=B0, P=P0, M=32, N=64, K=128, S=2, kps=64, dtype=bd.BF16), **kw)
+            args = (g["A"], g["B"], g["P"], g["M"], g["N"], g["K"], g["S"], g["kps"], g["dtype"], None)
+            assert fn_kn(*args) == fn_bt(*args) != 0, kw
+    for kw in (dict(out=0), dict(ws=0), dict(wsb=need - 4), dict(ws=W0 + 8), dict(out=A0), dict(ws=O0),
+               dict(fused=2), dict(M=96, K=100)):
+        g = dict(dict(out=O0, ws=W0, wsb=need, fused=0, M=32, N=64, K=128), **kw)
+        args = (A0, B0, g["out"], g["ws"], g["wsb"], g["M"], g["N"], g["K"], 2, 64, bd.BF16, g["fused"], None)
+        assert L.gemm_kn(*args) == L.gemm_bt(*args) != 0, kw
