@@ -8,26 +8,32 @@
 // the splits into out[m,n] (the pages' separate accumulation pass, fused).
 //
 // One CTA (256 threads, 8 warps) owns a 128 x BN output tile of one K-chunk:
-//   thread 0       TMA producer: 128x64 A box + BNx64 B box per stage, both
-//                  128-byte swizzled, into a ring of `stages` buffers; the
-//                  first `stages` loads go out before tensor memory is even
-//                  allocated;
-//   warp 1 lane 0  MMA issuer: 4 x tcgen05.mma (M=128, N=BN, K=16) per stage,
-//                  accumulating in tensor memory (BN 32-bit columns);
+//   thread 0       TMA producer: per stage, kbs 64-wide k-blocks of A (128
+//                  rows) and of B (BN rows), 128-byte swizzled, into a ring
+//                  of `stages` buffers; the first stages go out before tensor
+//                  memory is allocated;
+//   warp 1 lane 0  MMA issuer: tcgen05.mma (M=128, N=BN, K=16), accumulating
+//                  in tensor memory (BN 32-bit columns);
+//   warps 2-7      before the dependency wait, in the CTAs that start beside
+//                  the previous launch: L2 prefetch of this launch's A and B;
 //   all 8 warps    epilogue: tensor memory -> registers -> shared memory
 //                  (swizzled 32x32 float boxes, reusing the stage ring).
-// A split's K range is cut into `chunks` CTAs that form one thread-block
-// cluster.  Each cluster rank owns 1/chunks of the tile; every CTA pushes each
-// owner its share with one bulk shared-memory copy (cp.async.bulk into the
+// B is either the prepared [N,K] weight (K-major operand) or, with KN, the
+// [K,N] weight itself (MN-major operand: boxes of 64 columns by the stage's
+// k-rows); both give the same products in the same order.
+// The CTAs that share a tile (the chunks of a split, or every split and chunk
+// of the tile when the launch sums the splits) form one thread-block cluster.
+// Each cluster rank owns 1/Q of the tile; each warp pushes the boxes it staged
+// to their owners with bulk shared-memory copies (cp.async.bulk into the
 // owner's shared memory, counted on the owner's mbarrier), and each owner adds
-// the chunks in chunk order 0,1,2,... from its own shared memory, so the sum
-// does not depend on arrival order.  Owners store their share of partials[s] with coalesced
-// 16-byte stores.
-// Fused mode: after storing its share of partials[s], the owner counts its
-// arrival on a per-(tile, rank) counter; the last of the `splits` owners of
-// that piece of the tile reads the other splits' partials back (L2) and adds
-// them in split order s = 0,1,..., exactly the separate reduce kernel's sums,
-// then stores out[m,n].  The counter wraps to zero, ready for the next call.
+// the contributions in rank order from its own shared memory -- chunks in
+// chunk order, then splits in split order, the separate reduce kernel's sums
+// -- so the result does not depend on arrival order.
+// Fused mode with more splits than one cluster holds: after storing its share
+// of partials[s], the owner counts its arrival on a per-(tile, rank) counter;
+// the last of the `splits` owners of that piece of the tile reads the other
+// splits' partials back (L2) and adds them in split order, then stores
+// out[m,n].  The counter wraps to zero, ready for the next call.
 //
 // Programmatic dependent launch: the kernel waits for the previous grid (whose
 // writes it may read) before its first load, and lets the next grid start its
@@ -73,7 +79,6 @@ struct TcArgs {
     const uint8_t *A, *B;  // operands, for the L2 prefetch
     uint64_t a_bytes, b_bytes;
     int prefetchers;       // CTAs, first in dispatch order, that prefetch A and B into L2
-    int b_kn;              // B is the [K,N] weight: loaded and read MN-major
 };
 
 // Part j of `parts` (whole 128-byte lines) of [p, p + bytes) into L2, one
@@ -123,7 +128,7 @@ __device__ __forceinline__ void add4(float4 &a, const float4 &b)
     a.w += b.w;
 }
 
-template <int BN, int Q>
+template <int BN, int Q, bool KN>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const TcArgs args)
@@ -177,16 +182,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (args.three_d) {                         // one box per operand: kbs k-blocks at once
             const int kb = k_lo / kBlockK + i * kbs;
             ptx::tma_load_3d(sa, &tmA, bar, 0, m_tile * kTileM, kb, ptx::l2_policy_evict_last());
-            if (!args.b_kn)
+            if constexpr (!KN)
                 ptx::tma_load_3d(sa + kbs * Sh::kABytes, &tmB, bar, 0, n_tile * BN, kb,
                                  ptx::l2_policy_evict_normal());
         } else {                                    // kbs == 1
             const int kx = k_lo + i * kBlockK;
             ptx::tma_load_2d(sa, &tmA, bar, kx, m_tile * kTileM, ptx::l2_policy_evict_last());
-            if (!args.b_kn)
+            if constexpr (!KN)
                 ptx::tma_load_2d(sa + Sh::kABytes, &tmB, bar, kx, n_tile * BN, ptx::l2_policy_evict_normal());
         }
-        if (args.b_kn) {
+        if constexpr (KN) {
             // the [K,N] weight: BN/64 boxes of 64 columns x kbs*64 k-rows
             // (128-byte rows, N contiguous), one after another
 #pragma unroll
@@ -259,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued_s = i;
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
-        const uint32_t idesc = ptx::idesc_f16_f32acc(args.bf16 != 0, kTileM, BN, args.b_kn != 0);
+        const uint32_t idesc = ptx::idesc_f16_f32acc(args.bf16 != 0, kTileM, BN, KN);
         const uint32_t b_lbo = static_cast<uint32_t>(kbs) * 8192u;   // [K,N]: next 64 columns
         int i = 0;
         for (; i < nstg; ++i) {
@@ -277,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kb >= nkb) break;
                 const uint64_t ad = ptx::sdesc_kmajor_sw128(sa + j * Sh::kABytes);
                 const int ksteps = min(kBlockK, klen - kb * kBlockK) / 16;   // 4, or 2 for a 32-long tail
-                if (!args.b_kn) {
+                if constexpr (!KN) {
                     const uint64_t bd = ptx::sdesc_kmajor_sw128(sb + j * Sh::kBBytes);
                     for (int k = 0; k < ksteps; ++k)   // +32 bytes along K inside the swizzled row
                         ptx::mma_f16(tmem, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
@@ -589,7 +594,7 @@ size_t smem_for(int bn, int kbs, int stages, int chunks, int share)
 // Opts the kernel into the device's full dynamic shared memory (what is left
 // of the per-block opt-in limit after its static shared memory); once per
 // device.
-template <int BN, int Q>
+template <int BN, int Q, bool KN>
 cudaError_t prepare_kernel_attrs()
 {
     static std::mutex mu;
@@ -603,20 +608,20 @@ cudaError_t prepare_kernel_attrs()
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return note_error(e, "cudaDeviceGetAttribute(MaxSharedMemoryPerBlockOptin)");
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, tc_splitk_kernel<BN, Q>);
+    e = cudaFuncGetAttributes(&fa, tc_splitk_kernel<BN, Q, KN>);
     if (e != cudaSuccess) return note_error(e, "cudaFuncGetAttributes(tc_splitk_kernel)");
     const int dyn = optin - static_cast<int>(fa.sharedSizeBytes);
-    e = cudaFuncSetAttribute(tc_splitk_kernel<BN, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    e = cudaFuncSetAttribute(tc_splitk_kernel<BN, Q, KN>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
     if (e != cudaSuccess) return note_error(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
     if (dev >= 0 && dev < 64) done[dev] = true;
     return cudaSuccess;
 }
 
-template <int BN, int Q>
+template <int BN, int Q, bool KN>
 cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args, const TilePlan &plan,
                       cudaStream_t stream)
 {
-    cudaError_t e = prepare_kernel_attrs<BN, Q>();
+    cudaError_t e = prepare_kernel_attrs<BN, Q, KN>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = plan.grid;
@@ -637,19 +642,19 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
-    return note_error(cudaLaunchKernelEx(&cfg, tc_splitk_kernel<BN, Q>, ta, tb, args),
+    return note_error(cudaLaunchKernelEx(&cfg, tc_splitk_kernel<BN, Q, KN>, ta, tb, args),
                       "cudaLaunchKernelEx(tc_splitk_kernel)");
 }
 
-template <int BN>
+template <int BN, bool KN>
 cudaError_t launch_cluster(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args, const TilePlan &plan,
                            cudaStream_t stream)
 {
     switch (plan.cluster) {
-    case 1: return launch_bn<BN, 1>(ta, tb, args, plan, stream);
-    case 2: return launch_bn<BN, 2>(ta, tb, args, plan, stream);
-    case 4: return launch_bn<BN, 4>(ta, tb, args, plan, stream);
-    case 8: return launch_bn<BN, 8>(ta, tb, args, plan, stream);
+    case 1: return launch_bn<BN, 1, KN>(ta, tb, args, plan, stream);
+    case 2: return launch_bn<BN, 2, KN>(ta, tb, args, plan, stream);
+    case 4: return launch_bn<BN, 4, KN>(ta, tb, args, plan, stream);
+    case 8: return launch_bn<BN, 8, KN>(ta, tb, args, plan, stream);
     default: return note_error(cudaErrorInvalidConfiguration, "cluster size");
     }
 }
@@ -874,11 +879,13 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
     a.a_bytes = static_cast<uint64_t>(pr.M * pr.K) * 2;
     a.b_bytes = static_cast<uint64_t>(pr.N * pr.K) * 2;
     a.prefetchers = plan.prefetchers;
-    a.b_kn = pr.b_kn ? 1 : 0;
     switch (plan.bn) {
-    case 64: return launch_cluster<64>(ta, tb, a, plan, stream);
-    case 128: return launch_cluster<128>(ta, tb, a, plan, stream);
-    case 256: return launch_cluster<256>(ta, tb, a, plan, stream);
+    case 64: return pr.b_kn ? launch_cluster<64, true>(ta, tb, a, plan, stream)
+                            : launch_cluster<64, false>(ta, tb, a, plan, stream);
+    case 128: return pr.b_kn ? launch_cluster<128, true>(ta, tb, a, plan, stream)
+                             : launch_cluster<128, false>(ta, tb, a, plan, stream);
+    case 256: return pr.b_kn ? launch_cluster<256, true>(ta, tb, a, plan, stream)
+                             : launch_cluster<256, false>(ta, tb, a, plan, stream);
     default: return note_error(cudaErrorInvalidConfiguration, "tile width");
     }
 }
