@@ -89,8 +89,11 @@ int splitk_check_geometry(int64_t M, int64_t N, int64_t K, int64_t splits,
  *   B         device, [N,K] row-major, element type `dtype`
  *   partials  device, [splits,M,N] row-major F32; fully overwritten
  * BF16/F16 operands run on the tensor cores (tcgen05, F32 accumulate in tensor
- * memory, native operands); F32 operands run exact F32 FMA on the CUDA cores.
- * Each element is a sum in F32 whose order is fixed for a given shape. */
+ * memory, native operands).  F32 operands run on the tensor cores too, each
+ * product as three TF32 products (x = hi + lo with hi the top 19 bits and
+ * lo = x - hi; hi*lo + lo*hi + hi*hi; relative error per product about
+ * 2^-21).  Each element is a sum in F32 whose order is fixed for a given
+ * shape. */
 int gemm_splitk_bt(const void *A, const void *B, float *partials, int64_t M,
                    int64_t N, int64_t K, int64_t splits, int64_t k_per_split,
                    int dtype, void *stream);
@@ -142,8 +145,7 @@ int gemm_bt_workspace_init(void *workspace, size_t workspace_bytes, void *stream
  *                 kept;
  *              3: as 1, and the workspace also holds the partials afterwards.
  *              Fused calls need the workspace zeroed once before the first
- *              of them (gemm_bt_workspace_init).  With F32 operands the
- *              two-kernel path runs instead.
+ *              of them (gemm_bt_workspace_init).
  * For a given shape, `out` (and the partials, where kept) are bitwise the
  * same for every value of `fused`. */
 int gemm_bt(const void *A, const void *B, float *out, void *workspace,
@@ -156,9 +158,11 @@ int gemm_bt(const void *A, const void *B, float *out, void *workspace,
  * section "Performance method": both layouts uploaded once); no preparation
  * step.
  *   W  device, [K,N] row-major, element type `dtype`; B[n,k] = W[k,n]
- * Every other argument, the contract, the checks and the results are those of
- * gemm_splitk_bt and gemm_bt with B = W^T; the tensor cores read W
- * N-contiguous (MN-major operand). */
+ * Every other argument, the contract and the checks are those of
+ * gemm_splitk_bt and gemm_bt with B = W^T, and for BF16/F16 the results too
+ * (bitwise): the tensor cores read W N-contiguous (MN-major operand).  F32
+ * operands with W run exact F32 FMA on the CUDA cores (no fused variant: the
+ * two-kernel path runs for every `fused`). */
 int gemm_splitk_kn(const void *A, const void *W, float *partials, int64_t M,
                    int64_t N, int64_t K, int64_t splits, int64_t k_per_split,
                    int dtype, void *stream);
@@ -299,7 +303,7 @@ const char *splitk_status_string(int status);
 int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
 
 /* Describes the launch gemm_bt would make, without launching: info[0..15] =
- * {path (0 tensor-core, 1 F32 FMA), bn, chunks, chunk_len, stages,
+ * {path (0 tensor-core, 2 tensor-core 3xTF32 for F32), bn, chunks, chunk_len, stages,
  *  cluster_size (chunks, or splits * chunks), grid_x, grid_y, grid_z,
  *  dynamic_smem_bytes,
  *  fused_in_kernel (0/1), kernels_per_call, kblocks_per_stage,

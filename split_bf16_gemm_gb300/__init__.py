@@ -3,7 +3,7 @@
 A[M,K] (row-major) times the prepared weight B[N,K] (row-major, the transpose
 of a [K,N] weight), split along K into F32 partials[splits,M,N], then summed
 over splits into the F32 [M,N] output.  The compute runs in libsplitk, a C-ABI
-CUDA library for sm_103a (tcgen05 tensor cores for BF16/F16, exact F32 FMA for
+CUDA library for sm_103a (tcgen05 tensor cores: native BF16/F16, 3xTF32 for
 F32); this package is its build step and a thin ctypes binding.
 """
 from ._build import LIB_PATH, build  # noqa: F401

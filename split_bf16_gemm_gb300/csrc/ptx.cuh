@@ -209,6 +209,27 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32acc(bool bf16, uint32_t m, u
            ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
+// Instruction descriptor for tcgen05.mma .kind::tf32 with F32 accumulation:
+// D format F32 (bits 4-5 = 1), A and B format TF32 (bits 7-9, 10-12 = 2),
+// both K-major, N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t idesc_tf32_f32acc(uint32_t m, uint32_t n)
+{
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T for one K=8 slice of 32-bit operands (the
+// tensor cores read 19 bits of each: sign, exponent, 10 fraction bits).
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T for one K=16 slice, issued by one thread.
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                         uint32_t accumulate)

@@ -102,18 +102,21 @@ int run_partial_pass(const void *A, const void *B, float *P, float *out, unsigne
                      int64_t K, int64_t S, int64_t kps, int dtype, bool fused, bool prefetch, bool b_kn,
                      cudaStream_t stream)
 {
-    if (dtype == SPLITK_F32) {
+    if (dtype == SPLITK_F32 && b_kn) {   // exact FMA on the CUDA cores
         return cuda_status(splitk::launch_simt_f32(static_cast<const float *>(A), static_cast<const float *>(B), P,
                                                    M, N, K, S, kps, b_kn, stream));
     }
     GemmProblem pr{A, B, P, out, counters, M, N, K, S, kps, dtype == SPLITK_BF16};
     pr.b_kn = b_kn;
-    TilePlan plan = splitk::plan_tc(M, N, K, S, kps, fused);
+    pr.f32 = dtype == SPLITK_F32;   // 3xTF32 on the tensor cores
+    TilePlan plan = splitk::plan_tc(M, N, K, S, kps, fused, pr.f32);
     if (!prefetch) plan.prefetchers = 0;
     return cuda_status(splitk::launch_tc(pr, plan, stream));
 }
 
-bool fused_possible(int dtype) { return dtype != SPLITK_F32; }
+// The split sum runs inside the tensor-core launch; F32 with the [K,N] weight
+// runs on the CUDA cores and always takes the two-kernel path.
+bool fused_possible(int dtype, bool b_kn) { return !(dtype == SPLITK_F32 && b_kn); }
 
 size_t partials_bytes(int64_t M, int64_t N, int64_t S) { return static_cast<size_t>(S * M * N) * 4; }
 
@@ -234,9 +237,9 @@ static int gemm_impl(const void *A, const void *B, float *out, void *workspace, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float *P = static_cast<float *>(workspace);
     unsigned *counters = reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + partials_bytes(M, N, splits));
-    if (fused && fused_possible(dtype)) {
+    if (fused && fused_possible(dtype, b_kn)) {
         // fused == 1 keeps no partials where the cluster sums the splits on chip
-        const TilePlan plan = splitk::plan_tc(M, N, K, splits, k_per_split, true);
+        const TilePlan plan = splitk::plan_tc(M, N, K, splits, k_per_split, true, dtype == SPLITK_F32);
         float *keep = (fused == 1 && plan.split_sum == 2) ? nullptr : P;
         return run_partial_pass(A, B, keep, out, counters, M, N, K, splits, k_per_split, dtype, true, true, b_kn, s);
     }
@@ -307,22 +310,10 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
     if (elem_bytes(dtype) == 0) return SPLITK_ERR_DTYPE;
     if (!info) return SPLITK_ERR_NULL;
     std::fill(info, info + 16, 0);
-    if (dtype == SPLITK_F32) {
-        info[0] = 1;
-        info[1] = 64;
-        info[2] = 1;
-        info[3] = static_cast<int>(k_per_split);
-        info[5] = 1;
-        info[6] = static_cast<int>(N / 64);
-        info[7] = static_cast<int>((M + 63) / 64);
-        info[8] = static_cast<int>(splits);
-        info[11] = 2;
-        info[12] = 1;
-        return SPLITK_OK;
-    }
-    const bool in_kernel = fused != 0 && fused_possible(dtype);
-    const TilePlan p = splitk::plan_tc(M, N, K, splits, k_per_split, in_kernel);
-    info[0] = 0;
+    const bool x3 = dtype == SPLITK_F32;
+    const bool in_kernel = fused != 0 && fused_possible(dtype, false);
+    const TilePlan p = splitk::plan_tc(M, N, K, splits, k_per_split, in_kernel, x3);
+    info[0] = x3 ? 2 : 0;
     info[1] = p.bn;
     info[2] = p.chunks;
     info[3] = p.chunk_len;

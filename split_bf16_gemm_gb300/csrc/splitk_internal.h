@@ -18,6 +18,7 @@ struct GemmProblem {
     int64_t M, N, K, S, kps;
     bool bf16;          // operand type: BF16 (true) or F16 (false)
     bool b_kn = false;  // B given as the [K,N] weight itself (read MN-major)
+    bool f32 = false;   // F32 operands: 3xTF32 products on the tensor cores (bf16 ignored)
 };
 
 // How it is tiled.  One CTA computes a 128 x bn tile of one K-chunk of one
@@ -38,6 +39,7 @@ struct TilePlan {
     int share;          // 16-byte pieces of the tile each cluster rank owns
     uint32_t region0;   // bytes of the stage ring / accumulator staging
     int prefetchers;    // CTAs (the first in dispatch order) that prefetch A and B into L2
+    int x3;             // F32 operands as 3xTF32: 32-element k-blocks, stages twice the loaded bytes
     dim3 grid;
     size_t smem_bytes;  // dynamic shared memory per CTA
 };
@@ -52,10 +54,11 @@ constexpr int kMaxChunks = 8;  // portable cluster size
 inline int64_t fused_counter_count(int64_t M, int64_t N) { return (N / 64) * ((M + kTileM - 1) / kTileM) * kMaxChunks; }
 
 // Tile choice for a shape (automatic, or the process-wide override).
-TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused);
+// x3: F32 operands as 3xTF32 (else 16-bit operands).
+TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3 = false);
 // The planner's estimate (microseconds) of one tensor-core launch of that
 // plan behind another launch, the in-launch split sum included when fused.
-double estimate_tc_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused);
+double estimate_tc_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3 = false);
 void set_tile_override(int bn, int chunks, int kbs);
 
 // Kernel launches; each returns the launch's CUDA error.

@@ -1,10 +1,11 @@
-// splitk_simt.cu -- the split-K partial pass for F32 operands, in exact F32.
+// splitk_simt.cu -- the split-K partial pass in exact F32 on the CUDA cores,
+// for F32 operands with the [K,N] weight.
 //
-// The tensor cores' F32-input mode (TF32) keeps 10 fraction bits, about 5e-4
-// relative error per product, which cannot meet the pages' 1e-4 partial
-// tolerance for F32 ("Aligned shared rows for pipelined NAX on CUDA", section
-// "Contract and correctness").  So F32 runs on the CUDA cores: one FMA per
-// product, k ascending within the split, F32 accumulator.
+// One FMA per product, k ascending within the split, F32 accumulator: the
+// exact-F32 reference point for the pages' 1e-4 partial tolerance ("Aligned
+// shared rows for pipelined NAX on CUDA", section "Contract and
+// correctness").  F32 with the prepared [N,K] weight runs on the tensor cores
+// as 3xTF32 instead.
 //
 // Tiling: a 256-thread block owns a 64x64 tile of one split; each thread a
 // 4x4 sub-tile.  A and B are staged through shared memory 16 k at a time,

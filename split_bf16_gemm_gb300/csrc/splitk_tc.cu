@@ -128,14 +128,34 @@ __device__ __forceinline__ void add4(float4 &a, const float4 &b)
     a.w += b.w;
 }
 
-template <int BN, int Q, bool KN>
+// Split of an F32 value for the 3xTF32 products: hi keeps the 19 bits the
+// tensor cores read (sign, exponent, 10 fraction bits), lo = x - hi exactly
+// (at most 13 significant bits, of which the tensor cores keep the top 11).
+// Non-finite values pass whole in hi.
+__device__ __forceinline__ void split_tf32(uint32_t x, uint32_t &hi, uint32_t &lo)
+{
+    if ((x & 0x7F800000u) == 0x7F800000u) {
+        hi = x;
+        lo = 0u;
+        return;
+    }
+    hi = x & 0xFFFFE000u;
+    lo = __float_as_uint(__uint_as_float(x) - __uint_as_float(hi));
+}
+
+// KN: B is the [K,N] weight (MN-major operand).  X3: F32 operands, each
+// product formed as three TF32 products (hi*lo + lo*hi + hi*hi).
+template <int BN, int Q, bool KN, bool X3>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const TcArgs args)
 {
+    static_assert(!(KN && X3), "F32 operands with the [K,N] weight run on the CUDA cores");
+    constexpr int KB = X3 ? 32 : kBlockK;          // k elements per 128-byte swizzle row
+    constexpr int KSTEP = X3 ? 8 : 16;             // k per MMA instruction
     using Sh = TcShape<BN>;
     extern __shared__ uint8_t dsmem[];
-    __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 2];
+    __shared__ __align__(8) uint64_t bars[3 * kMaxStages + 2];
     __shared__ uint32_t tmem_slot;
     __shared__ int issued_s, consumed_s;
     __shared__ unsigned abort_s, last_s;
@@ -158,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int k_lo = ks + c * args.chunk_len;
     const int k_hi = min(k_lo + args.chunk_len, ke);
     const int klen = k_hi > k_lo ? k_hi - k_lo : 0; // a chunk past a short split is empty
-    const int nkb = (klen + kBlockK - 1) / kBlockK;
+    const int nkb = (klen + KB - 1) / KB;
     const int share = args.share;
     const int my_lo = min(Sh::kPieces, rank * share);
     const int my_hi = min(Sh::kPieces, my_lo + share);
@@ -168,25 +188,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto empty_bar = [&](int i) { return bar0 + 8u * (kMaxStages + i); };
     const uint32_t acc_bar = bar0 + 8u * (2 * kMaxStages);
     const uint32_t recv_bar = bar0 + 8u * (2 * kMaxStages + 1);
+    auto conv_bar = [&](int i) { return bar0 + 8u * (2 * kMaxStages + 2 + i); };   // X3: stage split
 
     // Stage i holds k-blocks i*kbs .. i*kbs+kbs-1 of the chunk: kbs slabs of A
     // (128 rows x 128 bytes each) then kbs slabs of B (BN rows x 128 bytes).
+    // With X3 the loaded half becomes the hi parts in place and a second half
+    // of the same layout holds the lo parts.
     const int kbs = args.kbs;
-    const uint32_t stage_bytes = static_cast<uint32_t>(kbs) * (Sh::kABytes + Sh::kBBytes);
+    const uint32_t load_bytes = static_cast<uint32_t>(kbs) * (Sh::kABytes + Sh::kBBytes);
+    const uint32_t stage_bytes = X3 ? 2u * load_bytes : load_bytes;
     const int nstg = (nkb + kbs - 1) / kbs;
     const int pre = min(stages, nstg);              // stages that need no free slot
     auto issue_stage = [&](int i, int slot) {
         const uint32_t sa = base + slot * stage_bytes;
         const uint32_t bar = full_bar(slot);
-        ptx::mbar_arrive_expect_tx(bar, stage_bytes);
+        ptx::mbar_arrive_expect_tx(bar, load_bytes);
         if (args.three_d) {                         // one box per operand: kbs k-blocks at once
-            const int kb = k_lo / kBlockK + i * kbs;
+            const int kb = k_lo / KB + i * kbs;
             ptx::tma_load_3d(sa, &tmA, bar, 0, m_tile * kTileM, kb, ptx::l2_policy_evict_last());
             if constexpr (!KN)
                 ptx::tma_load_3d(sa + kbs * Sh::kABytes, &tmB, bar, 0, n_tile * BN, kb,
                                  ptx::l2_policy_evict_normal());
         } else {                                    // kbs == 1
-            const int kx = k_lo + i * kBlockK;
+            const int kx = k_lo + i * KB;
             ptx::tma_load_2d(sa, &tmA, bar, kx, m_tile * kTileM, ptx::l2_policy_evict_last());
             if constexpr (!KN)
                 ptx::tma_load_2d(sa + Sh::kABytes, &tmB, bar, kx, n_tile * BN, ptx::l2_policy_evict_normal());
@@ -204,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < stages; ++i) {
             ptx::mbar_init(full_bar(i), 1);
             ptx::mbar_init(empty_bar(i), 1);
+            if (X3) ptx::mbar_init(conv_bar(i), kThreads / 32 - 2);   // one arrival per converting warp
         }
         ptx::mbar_init(acc_bar, 1);
         ptx::mbar_init(recv_bar, 1);
@@ -264,13 +289,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued_s = i;
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
-        const uint32_t idesc = ptx::idesc_f16_f32acc(args.bf16 != 0, kTileM, BN, KN);
+        const uint32_t idesc = X3 ? ptx::idesc_tf32_f32acc(kTileM, BN)
+                                  : ptx::idesc_f16_f32acc(args.bf16 != 0, kTileM, BN, KN);
         const uint32_t b_lbo = static_cast<uint32_t>(kbs) * 8192u;   // [K,N]: next 64 columns
         int i = 0;
         for (; i < nstg; ++i) {
             const int st = i % stages;
             const uint32_t ph = (i / stages) & 1;
-            if (!ptx::mbar_wait_bounded(full_bar(st), ph, args.wait_limit_ns)) {
+            if (!ptx::mbar_wait_bounded(X3 ? conv_bar(st) : full_bar(st), ph, args.wait_limit_ns)) {
                 atomicOr(&abort_s, 2u);
                 break;
             }
@@ -281,8 +307,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kb = i * kbs + j;
                 if (kb >= nkb) break;
                 const uint64_t ad = ptx::sdesc_kmajor_sw128(sa + j * Sh::kABytes);
-                const int ksteps = min(kBlockK, klen - kb * kBlockK) / 16;   // 4, or 2 for a 32-long tail
-                if constexpr (!KN) {
+                const int ksteps = min(KB, klen - kb * KB) / KSTEP;   // 4, or 2 for a 32-long 16-bit tail
+                if constexpr (X3) {
+                    // lo parts at the same offsets in the stage's second half;
+                    // the small products first, then hi*hi
+                    const uint64_t bd = ptx::sdesc_kmajor_sw128(sb + j * Sh::kBBytes);
+                    const uint64_t adl = ptx::sdesc_kmajor_sw128(sa + load_bytes + j * Sh::kABytes);
+                    const uint64_t bdl = ptx::sdesc_kmajor_sw128(sb + load_bytes + j * Sh::kBBytes);
+                    for (int k = 0; k < ksteps; ++k) {   // +32 bytes (8 F32) along K per step
+                        ptx::mma_tf32(tmem, ad + 2u * k, bdl + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                        ptx::mma_tf32(tmem, adl + 2u * k, bd + 2u * k, idesc, 1u);
+                        ptx::mma_tf32(tmem, ad + 2u * k, bd + 2u * k, idesc, 1u);
+                    }
+                } else if constexpr (!KN) {
                     const uint64_t bd = ptx::sdesc_kmajor_sw128(sb + j * Sh::kBBytes);
                     for (int k = 0; k < ksteps; ++k)   // +32 bytes along K inside the swizzled row
                         ptx::mma_f16(tmem, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
@@ -298,6 +335,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         consumed_s = i;
         ptx::mma_commit(acc_bar);              // the accumulator is final
+    } else if (X3 && warp >= 2) {
+        // ---- converters (warps 2-7): each landed stage becomes hi in place
+        // and lo in the second half, then is handed to the MMA issuer
+        const int t = tid - 64;
+        for (int i = 0; i < nstg; ++i) {
+            const int st = i % stages;
+            const uint32_t ph = (i / stages) & 1;
+            if (!ptx::mbar_wait_bounded(full_bar(st), ph, args.wait_limit_ns)) {
+                atomicOr(&abort_s, 8u);
+                break;
+            }
+            const uint32_t sa = base + st * stage_bytes;
+            for (uint32_t off = static_cast<uint32_t>(t) * 16u; off < load_bytes; off += (kThreads - 64) * 16u) {
+                const float4 v = ptx::ld_shared_v4(sa + off);
+                const uint32_t x[4] = {__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
+                                       __float_as_uint(v.w)};
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) split_tf32(x[q], hi[q], lo[q]);
+                ptx::st_shared_v4(sa + off, hi[0], hi[1], hi[2], hi[3]);
+                ptx::st_shared_v4(sa + load_bytes + off, lo[0], lo[1], lo[2], lo[3]);
+            }
+            ptx::fence_proxy_async_smem();     // the tensor cores read what these threads wrote
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(conv_bar(st));
+        }
     }
     __syncthreads();
 
@@ -532,18 +595,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 // Row-major [rows, K] 16-bit matrix, box = box_rows x 64 elements, 128-byte swizzle.
-bool encode_operand(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows, bool bf16)
+// Element type of an operand: 0 F16, 1 BF16, 2 F32.
+CUtensorMapDataType map_type(int et)
+{
+    return et == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                   : et == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+int elem_of(int et) { return et == 2 ? 4 : 2; }
+
+// Row-major [rows, K] matrix, box = box_rows x one 128-byte row (64 16-bit
+// or 32 F32 elements), 128-byte swizzle.
+bool encode_operand(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows, int et)
 {
     auto fn = encode_fn();
     if (!fn) {
         note_message("cuTensorMapEncodeTiled is not available from the driver", 0);
         return false;
     }
+    const int e = elem_of(et);
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), static_cast<cuuint32_t>(box_rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * e};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / e), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+    const CUresult r = fn(map, map_type(et), 2,
                     const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -551,24 +625,25 @@ bool encode_operand(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, 
     return r == CUDA_SUCCESS;
 }
 
-// Row-major [rows, K] 16-bit matrix seen as 3-D (element within a 64-wide
-// k-block, row, k-block), box = 64 x box_rows x kbs, 128-byte swizzle: one
-// load brings kbs k-blocks of a tile.  Needs K % 64 == 0, so that no k-block
-// runs past the end of a row.
-bool encode_operand_3d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows, int kbs, bool bf16)
+// Row-major [rows, K] matrix seen as 3-D (element within a k-block of one
+// 128-byte row, row, k-block), box = k-block x box_rows x kbs, 128-byte
+// swizzle: one load brings kbs k-blocks of a tile.  Needs K to be a whole
+// number of k-blocks, so that no k-block runs past the end of a row.
+bool encode_operand_3d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows, int kbs, int et)
 {
     auto fn = encode_fn();
     if (!fn) {
         note_message("cuTensorMapEncodeTiled is not available from the driver", 0);
         return false;
     }
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kBlockK), static_cast<cuuint64_t>(rows),
-                          static_cast<cuuint64_t>(K / kBlockK)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(kBlockK) * 2};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(kBlockK), static_cast<cuuint32_t>(box_rows),
+    const int e = elem_of(et), kb = 128 / e;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kb), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(K / kb)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * e, 128};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kb), static_cast<cuuint32_t>(box_rows),
                          static_cast<cuuint32_t>(kbs)};
     cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+    const CUresult r = fn(map, map_type(et), 3,
                           const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -578,23 +653,28 @@ bool encode_operand_3d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t 
 
 int g_override_bn = 0, g_override_chunks = 0, g_override_kbs = 0;
 
-size_t stage_bytes(int bn, int kbs) { return static_cast<size_t>(kTileM + bn) * kBlockK * 2 * kbs; }
+// One k-block is one 128-byte row of every operand row; a 3xTF32 stage holds
+// the lo parts too.
+size_t stage_bytes(int bn, int kbs, bool x3 = false)
+{
+    return static_cast<size_t>(kTileM + bn) * 128 * kbs * (x3 ? 2 : 1);
+}
 size_t epi_bytes(int bn) { return static_cast<size_t>(kTileM) * bn * 4; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr size_t kSmemLimit = 226 * 1024;   // dynamic; leaves room for static shared memory
 
 // Dynamic shared memory of a plan: the stage ring (or the accumulator
 // staging, if larger), one receive slot per peer, and 1 KB of alignment slack.
-size_t smem_for(int bn, int kbs, int stages, int chunks, int share)
+size_t smem_for(int bn, int kbs, int stages, int chunks, int share, bool x3 = false)
 {
-    const size_t region0 = round_up(std::max(stages * stage_bytes(bn, kbs), epi_bytes(bn)), 1024);
+    const size_t region0 = round_up(std::max(stages * stage_bytes(bn, kbs, x3), epi_bytes(bn)), 1024);
     return region0 + static_cast<size_t>(chunks - 1) * share * 16 + 1024;
 }
 
 // Opts the kernel into the device's full dynamic shared memory (what is left
 // of the per-block opt-in limit after its static shared memory); once per
 // device.
-template <int BN, int Q, bool KN>
+template <int BN, int Q, bool KN, bool X3>
 cudaError_t prepare_kernel_attrs()
 {
     static std::mutex mu;
@@ -608,20 +688,20 @@ cudaError_t prepare_kernel_attrs()
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return note_error(e, "cudaDeviceGetAttribute(MaxSharedMemoryPerBlockOptin)");
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, tc_splitk_kernel<BN, Q, KN>);
+    e = cudaFuncGetAttributes(&fa, tc_splitk_kernel<BN, Q, KN, X3>);
     if (e != cudaSuccess) return note_error(e, "cudaFuncGetAttributes(tc_splitk_kernel)");
     const int dyn = optin - static_cast<int>(fa.sharedSizeBytes);
-    e = cudaFuncSetAttribute(tc_splitk_kernel<BN, Q, KN>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    e = cudaFuncSetAttribute(tc_splitk_kernel<BN, Q, KN, X3>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
     if (e != cudaSuccess) return note_error(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
     if (dev >= 0 && dev < 64) done[dev] = true;
     return cudaSuccess;
 }
 
-template <int BN, int Q, bool KN>
+template <int BN, int Q, bool KN, bool X3>
 cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args, const TilePlan &plan,
                       cudaStream_t stream)
 {
-    cudaError_t e = prepare_kernel_attrs<BN, Q, KN>();
+    cudaError_t e = prepare_kernel_attrs<BN, Q, KN, X3>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = plan.grid;
@@ -642,19 +722,19 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
-    return note_error(cudaLaunchKernelEx(&cfg, tc_splitk_kernel<BN, Q, KN>, ta, tb, args),
+    return note_error(cudaLaunchKernelEx(&cfg, tc_splitk_kernel<BN, Q, KN, X3>, ta, tb, args),
                       "cudaLaunchKernelEx(tc_splitk_kernel)");
 }
 
-template <int BN, bool KN>
+template <int BN, bool KN, bool X3>
 cudaError_t launch_cluster(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args, const TilePlan &plan,
                            cudaStream_t stream)
 {
     switch (plan.cluster) {
-    case 1: return launch_bn<BN, 1, KN>(ta, tb, args, plan, stream);
-    case 2: return launch_bn<BN, 2, KN>(ta, tb, args, plan, stream);
-    case 4: return launch_bn<BN, 4, KN>(ta, tb, args, plan, stream);
-    case 8: return launch_bn<BN, 8, KN>(ta, tb, args, plan, stream);
+    case 1: return launch_bn<BN, 1, KN, X3>(ta, tb, args, plan, stream);
+    case 2: return launch_bn<BN, 2, KN, X3>(ta, tb, args, plan, stream);
+    case 4: return launch_bn<BN, 4, KN, X3>(ta, tb, args, plan, stream);
+    case 8: return launch_bn<BN, 8, KN, X3>(ta, tb, args, plan, stream);
     default: return note_error(cudaErrorInvalidConfiguration, "cluster size");
     }
 }
@@ -690,7 +770,7 @@ struct StageChoice {
 
 // The largest stage (k-blocks per box) that keeps a chunk's loads double-
 // buffered, or all in flight, within shared memory, for a cluster of q.
-StageChoice pick_stages(int bn, int nkb, bool can3d, int q, int share)
+StageChoice pick_stages(int bn, int nkb, bool can3d, int q, int share, bool x3 = false)
 {
     StageChoice r;
     for (int cand : {4, 2, 1}) {
@@ -698,8 +778,8 @@ StageChoice pick_stages(int bn, int nkb, bool can3d, int q, int share)
         if (g_override_kbs && cand != std::min(g_override_kbs, can3d ? 4 : 1)) continue;
         const int want = (nkb + cand - 1) / cand;
         int st = std::min(want, kMaxStages);
-        while (st > 1 && smem_for(bn, cand, st, q, share) > kSmemLimit) --st;
-        if (smem_for(bn, cand, st, q, share) > kSmemLimit) continue;
+        while (st > 1 && smem_for(bn, cand, st, q, share, x3) > kSmemLimit) --st;
+        if (smem_for(bn, cand, st, q, share, x3) > kSmemLimit) continue;
         if (st < std::min(want, 2) && !g_override_kbs) continue;
         r.kbs = std::min(cand, std::max(nkb, 1));
         r.stages = st;
@@ -719,11 +799,11 @@ int share_for(int bn, int q)
 // loads are bound by the L2 (about 10.5 TB/s for all SMs) or by one SM's TMA
 // intake (about 100 GB/s); staging the accumulator runs near 100 GB/s, the
 // distributed-shared-memory exchange and the final stores near 30 GB/s per SM.
-double model_us(int64_t M, int64_t N, int64_t S, int bn, int chunks, int64_t chunk_len, int q)
+double model_us(int64_t M, int64_t N, int64_t S, int bn, int chunks, int64_t chunk_len, int q, int elem = 2)
 {
     const int64_t mt = (M + kTileM - 1) / kTileM;
     const int64_t ctas = mt * (N / bn) * S * chunks;
-    const double load = static_cast<double>(kTileM + bn) * chunk_len * 2;     // bytes per CTA
+    const double load = static_cast<double>(kTileM + bn) * chunk_len * elem;  // bytes per CTA
     const double acc = static_cast<double>(kTileM) * bn * 4;
     const double t_load = std::max(load / 1.0e5, ctas * load / 1.05e7);
     const double t_stage = acc / 1.0e5;
@@ -736,12 +816,12 @@ double model_us(int64_t M, int64_t N, int64_t S, int bn, int chunks, int64_t chu
 
 }  // namespace
 
-double estimate_tc_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused)
+double estimate_tc_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3)
 {
-    const TilePlan p = plan_tc(M, N, K, S, kps, fused);
+    const TilePlan p = plan_tc(M, N, K, S, kps, fused, x3);
     // fixed cost of a launch behind another: the dependency hand-off and the
     // first stage landing (about 2.3 us on GB300)
-    double t = 2.3 + model_us(M, N, S, p.bn, p.chunks, p.chunk_len, p.cluster);
+    double t = 2.3 + model_us(M, N, S, p.bn, p.chunks, p.chunk_len, p.cluster, x3 ? 4 : 2);
     if (p.split_sum == 1) {
         // the last split of each piece range reads the others' partials back:
         // about 1 us of fence and arrival, one L2 round trip (0.7 us) per 8
@@ -753,13 +833,15 @@ double estimate_tc_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, b
     return t;
 }
 
-TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused)
+TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3)
 {
     // Stages of several k-blocks load as one 3-D box per operand, which the
     // TMA unit moves much faster than the same bytes in 16 KB boxes; that needs
-    // every chunk to start on a 64-element boundary.
-    const bool can3d = K % kBlockK == 0 && kps % kBlockK == 0;
-    const int64_t grain = can3d ? kBlockK : 32;
+    // every chunk to start on a k-block boundary (64 elements of 16 bits, or
+    // 32 F32, one 128-byte row).
+    const int kb_elems = x3 ? 32 : kBlockK;
+    const bool can3d = K % kb_elems == 0 && kps % kb_elems == 0;
+    const int64_t grain = can3d ? kb_elems : 32;
     const int64_t mt = (M + kTileM - 1) / kTileM;
     // Tile width and chunks per split: the cheapest by the model, with a
     // penalty where the splits of a tile cannot share one resident cluster of
@@ -776,15 +858,15 @@ TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool f
             int64_t len = (kps + c - 1) / c;
             len = (len + grain - 1) / grain * grain;
             if (!g_override_chunks && c > 1 && (c - 1) * len >= kps) continue;   // an always-empty chunk
-            const int nkb = static_cast<int>((len + kBlockK - 1) / kBlockK);
-            if (!pick_stages(bn, nkb, can3d, c, share_for(bn, c)).ok) continue;
+            const int nkb = static_cast<int>((len + kb_elems - 1) / kb_elems);
+            if (!pick_stages(bn, nkb, can3d, c, share_for(bn, c), x3).ok) continue;
             const int64_t tiles = mt * (N / bn);
             const int64_t sq = S * c;
             const bool cluster_sum = sq <= kMaxChunks && (sq & (sq - 1)) == 0 &&
                                      tiles <= resident_clusters(static_cast<int>(sq)) &&
                                      pick_stages(bn, nkb, can3d, static_cast<int>(sq),
-                                                 share_for(bn, static_cast<int>(sq))).ok;
-            const double cost = model_us(M, N, S, bn, c, len, c) + (cluster_sum ? 0.0 : 1.5);
+                                                 share_for(bn, static_cast<int>(sq)), x3).ok;
+            const double cost = model_us(M, N, S, bn, c, len, c, x3 ? 4 : 2) + (cluster_sum ? 0.0 : 1.5);
             if (cost < best) {
                 best = cost;
                 best_bn = bn;
@@ -799,20 +881,20 @@ TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool f
     const int bn = best_bn, chunks = best_c;
     int64_t chunk_len = (kps + chunks - 1) / chunks;
     chunk_len = (chunk_len + grain - 1) / grain * grain;
-    const int nkb = static_cast<int>((chunk_len + kBlockK - 1) / kBlockK);
+    const int nkb = static_cast<int>((chunk_len + kb_elems - 1) / kb_elems);
     const int64_t tiles = mt * (N / bn);
     int q = chunks, split_sum = 0;
     if (fused) {
         const int sq = static_cast<int>(S) * chunks;
         split_sum = 1;
         if (sq <= kMaxChunks && (sq & (sq - 1)) == 0 && tiles <= resident_clusters(sq) &&
-            pick_stages(bn, nkb, can3d, sq, share_for(bn, sq)).ok) {
+            pick_stages(bn, nkb, can3d, sq, share_for(bn, sq), x3).ok) {
             q = sq;
             split_sum = 2;
         }
     }
     const int share = share_for(bn, q);
-    const StageChoice sc = pick_stages(bn, nkb, can3d, q, share);
+    const StageChoice sc = pick_stages(bn, nkb, can3d, q, share, x3);
     TilePlan p = {};
     p.bn = bn;
     p.chunks = chunks;
@@ -824,7 +906,9 @@ TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool f
     p.split_sum = split_sum;
     p.cluster = q;
     p.share = share;
-    p.region0 = static_cast<uint32_t>(round_up(std::max(p.stages * stage_bytes(bn, p.kbs), epi_bytes(bn)), 1024));
+    p.x3 = x3 ? 1 : 0;
+    p.region0 =
+        static_cast<uint32_t>(round_up(std::max(p.stages * stage_bytes(bn, p.kbs, x3), epi_bytes(bn)), 1024));
     p.grid = dim3(static_cast<unsigned>(N / bn), static_cast<unsigned>(mt), static_cast<unsigned>(S * chunks));
     // CTAs of the next launch that fit beside this one (whole clusters): they
     // start early under programmatic dependent launch and do the prefetch
@@ -832,7 +916,7 @@ TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool f
     const int64_t clusters = ctas / q;
     const int64_t spare = std::max<int64_t>(0, static_cast<int64_t>(resident_clusters(q)) - clusters) * q;
     p.prefetchers = static_cast<int>(std::min(spare, ctas));
-    p.smem_bytes = smem_for(bn, p.kbs, p.stages, q, share);
+    p.smem_bytes = smem_for(bn, p.kbs, p.stages, q, share, x3);
     return p;
 }
 
@@ -844,15 +928,18 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
         return note_error(cudaErrorInvalidValue, "fused launch without output or counters");
     if (pr.P == nullptr && plan.split_sum != 2)
         return note_error(cudaErrorInvalidValue, "partials are needed unless the cluster sums the splits");
+    if (pr.f32 && (pr.b_kn || !plan.x3))
+        return note_error(cudaErrorInvalidValue, "F32 operands need a 3xTF32 plan and the [N,K] weight");
     CUtensorMap ta, tb;
+    const int et = pr.f32 ? 2 : pr.bf16 ? 1 : 0;
     const int kbs = plan.three_d ? plan.kbs : 1;
-    const bool ok_a = plan.three_d ? encode_operand_3d(&ta, pr.A, pr.M, pr.K, kTileM, plan.kbs, pr.bf16)
-                                   : encode_operand(&ta, pr.A, pr.M, pr.K, kTileM, pr.bf16);
+    const bool ok_a = plan.three_d ? encode_operand_3d(&ta, pr.A, pr.M, pr.K, kTileM, plan.kbs, et)
+                                   : encode_operand(&ta, pr.A, pr.M, pr.K, kTileM, et);
     // the [K,N] weight is a row-major matrix of K rows of N: boxes of 64
     // columns by kbs*64 rows
-    const bool ok_b = pr.b_kn ? encode_operand(&tb, pr.B, pr.K, pr.N, kbs * kBlockK, pr.bf16)
-                              : plan.three_d ? encode_operand_3d(&tb, pr.B, pr.N, pr.K, plan.bn, plan.kbs, pr.bf16)
-                                             : encode_operand(&tb, pr.B, pr.N, pr.K, plan.bn, pr.bf16);
+    const bool ok_b = pr.b_kn ? encode_operand(&tb, pr.B, pr.K, pr.N, kbs * kBlockK, et)
+                              : plan.three_d ? encode_operand_3d(&tb, pr.B, pr.N, pr.K, plan.bn, plan.kbs, et)
+                                             : encode_operand(&tb, pr.B, pr.N, pr.K, plan.bn, et);
     const bool ok = ok_a && ok_b;
     if (!ok) return cudaErrorInvalidValue;
     TcArgs a = {};
@@ -876,16 +963,21 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
     a.wait_limit_ns = kWaitLimitNs;
     a.A = static_cast<const uint8_t *>(pr.A);
     a.B = static_cast<const uint8_t *>(pr.B);
-    a.a_bytes = static_cast<uint64_t>(pr.M * pr.K) * 2;
-    a.b_bytes = static_cast<uint64_t>(pr.N * pr.K) * 2;
+    a.a_bytes = static_cast<uint64_t>(pr.M * pr.K) * elem_of(et);
+    a.b_bytes = static_cast<uint64_t>(pr.N * pr.K) * elem_of(et);
     a.prefetchers = plan.prefetchers;
-    switch (plan.bn) {
-    case 64: return pr.b_kn ? launch_cluster<64, true>(ta, tb, a, plan, stream)
-                            : launch_cluster<64, false>(ta, tb, a, plan, stream);
-    case 128: return pr.b_kn ? launch_cluster<128, true>(ta, tb, a, plan, stream)
-                             : launch_cluster<128, false>(ta, tb, a, plan, stream);
-    case 256: return pr.b_kn ? launch_cluster<256, true>(ta, tb, a, plan, stream)
-                             : launch_cluster<256, false>(ta, tb, a, plan, stream);
+    // operand variants: [N,K] weight, [K,N] weight, F32 as 3xTF32
+    const int variant = pr.f32 ? 2 : pr.b_kn ? 1 : 0;
+    switch (plan.bn * 4 + variant) {
+    case 64 * 4 + 0: return launch_cluster<64, false, false>(ta, tb, a, plan, stream);
+    case 64 * 4 + 1: return launch_cluster<64, true, false>(ta, tb, a, plan, stream);
+    case 64 * 4 + 2: return launch_cluster<64, false, true>(ta, tb, a, plan, stream);
+    case 128 * 4 + 0: return launch_cluster<128, false, false>(ta, tb, a, plan, stream);
+    case 128 * 4 + 1: return launch_cluster<128, true, false>(ta, tb, a, plan, stream);
+    case 128 * 4 + 2: return launch_cluster<128, false, true>(ta, tb, a, plan, stream);
+    case 256 * 4 + 0: return launch_cluster<256, false, false>(ta, tb, a, plan, stream);
+    case 256 * 4 + 1: return launch_cluster<256, true, false>(ta, tb, a, plan, stream);
+    case 256 * 4 + 2: return launch_cluster<256, false, true>(ta, tb, a, plan, stream);
     default: return note_error(cudaErrorInvalidConfiguration, "tile width");
     }
 }

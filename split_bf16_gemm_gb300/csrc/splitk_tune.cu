@@ -54,15 +54,8 @@ int elem_size(int dtype)
 double estimate_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, int dtype, int fused)
 {
     const double reduce = 1.0 + static_cast<double>(S + 1) * M * N * 4 / 6.0e6;   // bytes at ~6 TB/s
-    if (dtype == SPLITK_F32) {
-        // exact FMA: 64 x 64 tiles, about 0.5 TFLOP/s per SM, four blocks per SM
-        const int64_t blocks = (N / 64) * ((M + 63) / 64) * S;
-        const int64_t waves = (blocks + 4 * 148 - 1) / (4 * 148);
-        const double per_block = 2.0 * 64 * 64 * kps / 5.0e5 * 4;
-        return 2.3 + static_cast<double>(waves) * per_block + reduce;
-    }
     const bool in_kernel = fused != 0;
-    return splitk::estimate_tc_us(M, N, K, S, kps, in_kernel) + (in_kernel ? 0.0 : reduce);
+    return splitk::estimate_tc_us(M, N, K, S, kps, in_kernel, dtype == SPLITK_F32) + (in_kernel ? 0.0 : reduce);
 }
 
 }  // namespace

@@ -225,7 +225,9 @@ TILINGS = [(bn, ch, kb) for bn in (64, 128, 256) for ch in (1, 2, 4, 8) for kb i
 
 
 @pytest.mark.parametrize("case", [(64, 128, 160, 3, 64, "bf16"), (256, 1024, 2048, 2, 1024, "bf16"),
-                                  (96, 512, 2048, 4, 512, "f16")], ids=["K160", "headline", "M96"])
+                                  (96, 512, 2048, 4, 512, "f16"), (64, 128, 160, 3, 64, "f32"),
+                                  (256, 1024, 2048, 2, 1024, "f32")],
+                         ids=["K160", "headline", "M96", "K160-f32", "headline-f32"])
 def test_every_tiling(lib, case):
     """Each tile width and chunk count (including chunks past a short final
     split, which hold no K at all) gives a correct result, and the fused path
@@ -500,17 +502,25 @@ def test_kn_layout_matches_oracle(lib, orc, case):
 
 @pytest.mark.parametrize("case", KN_CASES, ids=ids(KN_CASES))
 def test_kn_layout_bitwise_equals_prepared(lib, orc, case):
-    """Reading the weight N-contiguous gives the same bits as reading its
-    prepared transpose K-contiguous: same products, same accumulation."""
+    """16-bit operands: reading the weight N-contiguous gives the same bits as
+    reading its prepared transpose K-contiguous (same products, same
+    accumulation).  F32: the [K,N] weight runs exact FMA, the prepared one
+    3xTF32; they agree to 3xTF32 accuracy (1e-5 of sum |a*b|, against the
+    exact oracle's 1e-4 bound)."""
     sk = lib
     M, N, K, S, kps, dt = case
-    ops = oracle_case(M, N, K, S, kps, dt)[0]
+    ops, Pr, SP, _, _ = oracle_case(M, N, K, S, kps, dt)
     A, B, W = device_operand(ops.A, dt), device_operand(ops.B, dt), kn_weight(orc, ops)
     P1, P2 = Guarded(S * M * N), Guarded(S * M * N)
     sk.gemm_splitk_bt(A, B, P1.data, M, N, K, S, kps, dt)
     sk.gemm_splitk_kn(A, W, P2.data, M, N, K, S, kps, dt)
     assert sk.splitk_get_device_status() == 0
-    assert np.array_equal(P1.numpy().view(np.uint32), P2.numpy().view(np.uint32))
+    if dt != "f32":
+        assert np.array_equal(P1.numpy().view(np.uint32), P2.numpy().view(np.uint32))
+    else:
+        diff = max_scaled_error(P1.numpy().reshape(S, M, N), P2.numpy().reshape(S, M, N).astype(np.float64), SP)
+        assert diff <= 1e-5
+        assert max_scaled_error(P2.numpy().reshape(S, M, N), Pr, SP) <= 1e-6   # exact FMA
 
 
 @pytest.mark.parametrize("case", [(64, 128, 160, 3, 64, "bf16"), (256, 1024, 2048, 2, 1024, "bf16")],

@@ -177,9 +177,13 @@ def test_describe_launch_plans(L):
     assert f["split_sum"] == 2 and f["cluster"] == 2 * f["chunks"] <= 8
     # same chunking in both modes: the fused output equals the two-kernel output bitwise
     assert (f["bn"], f["chunks"], f["chunk_len"]) == (d["bn"], d["chunks"], d["chunk_len"])
-    # F32 runs the FMA path, two kernels even when fused is asked for
+    # F32 runs 3xTF32 on the tensor cores: 32-element k-blocks, stages twice the loaded bytes,
+    # the split sum in the launch as for 16-bit operands
     g = sk.splitk_describe_launch(96, 512, 2048, 4, 512, "f32", fused=1)
-    assert g["path"] == 1 and g["kernels_per_call"] == 2
+    assert g["path"] == 2 and g["kernels_per_call"] == 1 and g["fused_in_kernel"] == 1
+    g0 = sk.splitk_describe_launch(96, 512, 2048, 4, 512, "f32", fused=0)
+    assert g0["path"] == 2 and g0["kernels_per_call"] == 2
+    assert g0["chunk_len"] % 32 == 0 and g0["smem_bytes"] <= 227 * 1024
     # any number of splits fuses: beyond one cluster the splits meet through
     # arrival counters in the workspace
     h = sk.splitk_describe_launch(32, 64, 32 * 32, 32, 32, "bf16", fused=1)
