@@ -223,9 +223,15 @@ size_t gemm_bt_host_staging_bytes(int64_t count, int64_t M, int64_t N,
  *              choose (at least 2 MiB of A per copy, at most half the batch)
  * Every operation is bitwise the gemm_bt result for its operands.  The copy
  * in of group g+1 and the copy out of group g-1 run on two library streams
- * while group g computes on `stream`; the copy in waits for the work already
- * on `stream`, and `stream` waits for the last copy out, so synchronising
- * `stream` completes the batch.  Host buffers must stay valid until then.
+ * while group g computes on `stream`, and `stream` waits for the last copy
+ * out, so synchronising `stream` completes the batch.  Host buffers must stay
+ * valid until then.  The copy in waits for the end of the previous call on
+ * the same staging (the library keeps one event per staging buffer, for the
+ * 32 most recently used), or, for a staging it has not seen, for the work
+ * already on `stream`: calls that alternate two staging buffers overlap one
+ * batch's copy in with the previous batch's kernels.  Between calls the
+ * staging belongs to them: other work must not write it, and one staging is
+ * used with one stream (its workspace part is used in stream order). 
  * The first call on a device creates those two streams and four events (kept
  * until exit); a process-wide mutex serialises the enqueueing of concurrent
  * calls.  Returns as gemm_bt's validation would (plus SPLITK_ERR_CONFIG for

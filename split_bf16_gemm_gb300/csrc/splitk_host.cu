@@ -15,8 +15,11 @@
 // so the copy-in of group g+1 and the copy-out of group g-1 run on the copy
 // engines while group g computes.  Events order the stages; the caller's
 // stream waits for the last copy-out before the call's work counts as done on
-// it, and the copy-in waits for everything the caller's stream held before the
-// call (the staging may still be in use there).
+// it.  The copy-in waits only for the previous call on the same staging (an
+// event the library keeps per staging buffer), or, the first time a staging
+// is seen, for everything the caller's stream held before the call.  A
+// caller alternating two staging buffers therefore gets the next batch's
+// activations in while the current batch computes.
 //
 // The two copy streams and four events per device are created on the first
 // call on that device and kept until the process exits.  One mutex per
@@ -43,8 +46,44 @@ struct Pipe {
     cudaEvent_t start = nullptr, loaded = nullptr, computed = nullptr, drained = nullptr;
 };
 
+// The end of the last call on each staging buffer (most recent first).
+constexpr int kTracked = 32;
+struct LastUse {
+    int device = -1;
+    const void *staging = nullptr;
+    cudaEvent_t done = nullptr;
+    uint64_t stamp = 0;
+};
+
 std::mutex g_mu;
 Pipe g_pipes[kMaxDevices];
+LastUse g_last[kTracked];
+uint64_t g_clock = 0;
+
+// The entry for (device, staging): found, or the least recently used slot
+// taken over (its event kept, its staging replaced).  *known says whether the
+// staging had an entry.
+LastUse *last_use(int device, const void *staging, bool *known)
+{
+    LastUse *lru = &g_last[0];
+    for (LastUse &e : g_last) {
+        if (e.device == device && e.staging == staging) {
+            *known = true;
+            e.stamp = ++g_clock;
+            return &e;
+        }
+        if (e.stamp < lru->stamp) lru = &e;
+    }
+    *known = false;
+    if (lru->done && lru->device != device) {   // an event belongs to its device
+        cudaEventDestroy(lru->done);
+        lru->done = nullptr;
+    }
+    lru->device = device;
+    lru->staging = staging;
+    lru->stamp = ++g_clock;
+    return lru;
+}
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -182,12 +221,27 @@ int gemm_bt_host_batch(const void *A_host, const void *const *B, float *out_host
     Pipe *p = nullptr;
     int rc = pipe_for_current_device(&p);
     if (rc != SPLITK_OK) return rc;
+    int dev = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return fail(ce, "cudaGetDevice");
+    bool known = false;
+    LastUse *use = last_use(dev, staging, &known);
+    if (!use->done && (ce = cudaEventCreateWithFlags(&use->done, cudaEventDisableTiming)) != cudaSuccess) {
+        use->device = -1;
+        return fail(ce, "cudaEventCreate(staging)");
+    }
 
-    cudaError_t ce;
-    // the staging may still be in use by work already on the caller's stream
-    if ((ce = cudaEventRecord(p->start, s)) != cudaSuccess) return fail(ce, "cudaEventRecord(start)");
-    if ((ce = cudaStreamWaitEvent(p->in, p->start, 0)) != cudaSuccess) return fail(ce, "cudaStreamWaitEvent(start)");
-    if ((ce = cudaStreamWaitEvent(p->out, p->start, 0)) != cudaSuccess) return fail(ce, "cudaStreamWaitEvent(start)");
+    // the copy-in overwrites the staging's A slots: after the previous call on
+    // this staging, or, for a staging not seen before, after everything
+    // already on the caller's stream (zeroing it, for one)
+    if (known) {
+        if ((ce = cudaStreamWaitEvent(p->in, use->done, 0)) != cudaSuccess)
+            return fail(ce, "cudaStreamWaitEvent(staging)");
+    } else {
+        if ((ce = cudaEventRecord(p->start, s)) != cudaSuccess) return fail(ce, "cudaEventRecord(start)");
+        if ((ce = cudaStreamWaitEvent(p->in, p->start, 0)) != cudaSuccess)
+            return fail(ce, "cudaStreamWaitEvent(start)");
+    }
 
     for (int64_t g0 = 0; g0 < count && rc == SPLITK_OK; g0 += g) {
         const int64_t n = (count - g0 < g) ? count - g0 : g;
@@ -215,6 +269,12 @@ int gemm_bt_host_batch(const void *A_host, const void *const *B, float *out_host
     const cudaError_t j4 = j3 == cudaSuccess ? cudaStreamWaitEvent(s, p->drained, 0) : j3;
     if (rc == SPLITK_OK && j2 != cudaSuccess) return fail(j2, "joining the copy-out stream");
     if (rc == SPLITK_OK && j4 != cudaSuccess) return fail(j4, "joining the copy-in stream");
+    // the end of this call's work on the staging, for the next call on it
+    ce = cudaEventRecord(use->done, s);
+    if (ce != cudaSuccess) {
+        use->device = -1;   // forget the staging: the next call waits on the caller's stream
+        if (rc == SPLITK_OK) return fail(ce, "cudaEventRecord(staging)");
+    }
     return rc;
 }
 

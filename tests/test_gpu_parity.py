@@ -374,6 +374,7 @@ def test_host_batch_matches_device_call_and_oracle(lib, case):
         A_host = host_operand([c[0].A for c in cs], dt, pinned)
         for fused in (0, 1):
             staging = torch.zeros(sb // 4 + 16, dtype=torch.float32, device="cuda")
+            torch.cuda.synchronize()
             out_host = torch.full((count * M * N + GUARDS,), 7.0, dtype=torch.float32)
             out_host[count * M * N:] = GUARD_VALUE
             out_host = out_host.pin_memory() if pinned else out_host
@@ -411,6 +412,7 @@ def test_host_batch_back_to_back_shared_staging(lib):
         want.append(o.numpy())
     sb = sk.gemm_bt_host_staging_bytes(count, M, N, K, S, kps, dt)
     staging = torch.zeros(sb // 4, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
     a1 = host_operand([c[0].A for c in c1], dt, True)
     a2 = host_operand([c[0].A for c in reversed(c1)], dt, True)
     o1 = torch.zeros(count * M * N, dtype=torch.float32).pin_memory()
@@ -549,3 +551,38 @@ def test_kn_every_tiling(lib, orc, case):
     finally:
         sk.splitk_set_tile_override(0, 0, 0)
     assert len(seen) > 4
+
+
+def test_host_batch_alternating_staging_in_flight(lib):
+    """Six batches on one stream over two alternating staging buffers, no
+    synchronisation until the end: each batch's copy in waits only for the
+    previous batch on the same staging, and every result is right."""
+    sk = lib
+    M, N, K, S, kps, dt, count, rounds = 128, 256, 1024, 2, 512, "bf16", 4, 6
+    cs = [oracle_case(M, N, K, S, kps, dt, "uniform", 40 + i) for i in range(count)]
+    Bs = [device_operand(c[0].B, dt) for c in cs]
+    want = []
+    for c, B in zip(cs, Bs):
+        ws, nbytes = workspace(M, N, K, S, kps)
+        o = Guarded(M * N)
+        sk.gemm_bt(device_operand(c[0].A, dt), B, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=1)
+        want.append(o.numpy())
+    sb = sk.gemm_bt_host_staging_bytes(count, M, N, K, S, kps, dt)
+    stagings = [torch.zeros(sb // 4, dtype=torch.float32, device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    ptrs = sk.pointer_array(Bs)
+    order = [list(range(count)) if r % 2 == 0 else list(reversed(range(count))) for r in range(rounds)]
+    hosts = [host_operand([cs[i][0].A for i in o], dt, True) for o in order]
+    outs = [torch.zeros(count * M * N, dtype=torch.float32).pin_memory() for _ in range(rounds)]
+    stream = torch.cuda.Stream()
+    for r in range(rounds):
+        bp = sk.pointer_array([Bs[i] for i in order[r]])
+        sk.gemm_bt_host_batch(hosts[r], bp, outs[r], count, stagings[r % 2], sb, M, N, K, S, kps, dt,
+                              fused=1, ops_per_copy=1, stream=stream)
+    stream.synchronize()
+    assert sk.splitk_get_device_status(stream) == 0
+    for r in range(rounds):
+        got = outs[r].numpy()
+        for j, i in enumerate(order[r]):
+            assert np.array_equal(got[j * M * N:(j + 1) * M * N].view(np.uint32), want[i].view(np.uint32)), (r, j)
+    del ptrs
