@@ -51,6 +51,10 @@ CATEGORIES = [
     (512, 2048, 4096, 4, 1024, "bf16"),  # larger matrices
     (32, 64, 64, 1, 128, "bf16"),        # k_per_split larger than K
     (288, 256, 96, 3, 32, "f16"),        # 32-long splits everywhere
+    (64, 128, 2048, 64, 32, "bf16"),     # 64 splits: fused sum by arrival counters, loads 8 splits at a time
+    (160, 192, 320, 3, 128, "f32"),      # F32 (3xTF32): M tail, short final split
+    (64, 128, 8192, 4, 2048, "f32"),     # F32, long K
+    (288, 256, 96, 3, 32, "f32"),        # F32, 32-long splits everywhere
 ]
 
 
