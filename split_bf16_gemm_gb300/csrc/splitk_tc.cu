@@ -128,19 +128,16 @@ __device__ __forceinline__ void add4(float4 &a, const float4 &b)
     a.w += b.w;
 }
 
-// Split of an F32 value for the 3xTF32 products: hi keeps the 19 bits the
-// tensor cores read (sign, exponent, 10 fraction bits), lo = x - hi exactly
-// (at most 13 significant bits, of which the tensor cores keep the top 11).
-// Non-finite values pass whole in hi.
-__device__ __forceinline__ void split_tf32(uint32_t x, uint32_t &hi, uint32_t &lo)
+// The low part of an F32 value for the 3xTF32 products.  The tensor cores
+// read an F32 operand as TF32 by dropping its 13 low fraction bits (checked
+// on GB300: every output of a one-hot product equals the truncated input), so
+// x itself serves as hi = x & ~0x1FFF, and lo = x - hi exactly (at most 13
+// significant bits, of which the tensor cores keep the top 11).  Non-finite
+// values get lo = 0.
+__device__ __forceinline__ uint32_t tf32_lo(uint32_t x)
 {
-    if ((x & 0x7F800000u) == 0x7F800000u) {
-        hi = x;
-        lo = 0u;
-        return;
-    }
-    hi = x & 0xFFFFE000u;
-    lo = __float_as_uint(__uint_as_float(x) - __uint_as_float(hi));
+    if ((x & 0x7F800000u) == 0x7F800000u) return 0u;
+    return __float_as_uint(__uint_as_float(x) - __uint_as_float(x & 0xFFFFE000u));
 }
 
 // KN: B is the [K,N] weight (MN-major operand).  X3: F32 operands, each
@@ -192,8 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Stage i holds k-blocks i*kbs .. i*kbs+kbs-1 of the chunk: kbs slabs of A
     // (128 rows x 128 bytes each) then kbs slabs of B (BN rows x 128 bytes).
-    // With X3 the loaded half becomes the hi parts in place and a second half
-    // of the same layout holds the lo parts.
+    // With X3 the loaded half serves as the hi parts as it is and a second
+    // half of the same layout holds the lo parts.
     const int kbs = args.kbs;
     const uint32_t load_bytes = static_cast<uint32_t>(kbs) * (Sh::kABytes + Sh::kBBytes);
     const uint32_t stage_bytes = X3 ? 2u * load_bytes : load_bytes;
@@ -336,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         consumed_s = i;
         ptx::mma_commit(acc_bar);              // the accumulator is final
     } else if (X3 && warp >= 2) {
-        // ---- converters (warps 2-7): each landed stage becomes hi in place
-        // and lo in the second half, then is handed to the MMA issuer
+        // ---- converters (warps 2-7): the lo parts of each landed stage go to
+        // the second half, then the stage is handed to the MMA issuer
         const int t = tid - 64;
         for (int i = 0; i < nstg; ++i) {
             const int st = i % stages;
@@ -349,13 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sa = base + st * stage_bytes;
             for (uint32_t off = static_cast<uint32_t>(t) * 16u; off < load_bytes; off += (kThreads - 64) * 16u) {
                 const float4 v = ptx::ld_shared_v4(sa + off);
-                const uint32_t x[4] = {__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
-                                       __float_as_uint(v.w)};
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) split_tf32(x[q], hi[q], lo[q]);
-                ptx::st_shared_v4(sa + off, hi[0], hi[1], hi[2], hi[3]);
-                ptx::st_shared_v4(sa + load_bytes + off, lo[0], lo[1], lo[2], lo[3]);
+                ptx::st_shared_v4(sa + load_bytes + off, tf32_lo(__float_as_uint(v.x)), tf32_lo(__float_as_uint(v.y)),
+                                  tf32_lo(__float_as_uint(v.z)), tf32_lo(__float_as_uint(v.w)));
             }
             ptx::fence_proxy_async_smem();     // the tensor cores read what these threads wrote
             __syncwarp();
