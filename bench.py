@@ -206,10 +206,41 @@ def make_pool(torch, n_inst, dev):
         A = torch.from_numpy(ops.A.view(np.int16)).to(dev).view(torch.bfloat16)
         B = torch.from_numpy(ops.B.view(np.int16)).to(dev).view(torch.bfloat16)
         pool.append({"A_host": torch.from_numpy(ops.A.view(np.int16)).view(torch.bfloat16),
+                     "A_bits": ops.A, "B_bits": ops.B,
                      "A": A, "B": B,
                      "out": torch.empty((M, N), dtype=torch.float32, device=dev),
                      "ws": torch.empty((SPLITS * M * N,), dtype=torch.float32, device=dev)})
     return pool
+
+
+TOL_BF16_FINAL = 2e-2   # the pages' final tolerance for BF16, times sum |a*b|
+
+
+def f64_check(insts, rows_per=8, seed=0):
+    """Sampled rows of each instance's output against an F64 product of its
+    BF16 operands (decoded from the same bits), as max |out - ref| / sum|ab|;
+    rows whose sum|ab| is 0 (the zero first row of A) must be exactly 0.
+    Returns (worst scaled error, outputs checked)."""
+    import numpy as np
+
+    def f64(bits):
+        return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+    rng = np.random.default_rng(seed)
+    worst, count = 0.0, 0
+    for inst in insts:
+        rows = sorted({0, 1, M // 2, M - 1, *rng.integers(0, M, rows_per - 4).tolist()})
+        a = f64(inst["A_bits"].reshape(M, K)[rows])
+        b = f64(inst["B_bits"].reshape(N, K))
+        ref, bound = a @ b.T, np.abs(a) @ np.abs(b).T
+        got = inst["out"][rows].cpu().numpy().astype(np.float64)
+        err = np.abs(got - ref)
+        zero = bound == 0
+        if not np.all(np.isfinite(err)) or np.any(err[zero] != 0):
+            return float("inf"), count + got.size
+        worst = max(worst, float(np.max(err[~zero] / bound[~zero])))
+        count += got.size
+    return worst, count
 
 
 def job_time(ms_local, steps, pack, world, dist=None, device="cpu"):
@@ -353,7 +384,16 @@ def run_ours(args, rank, world, dev, torch, dist):
     if not torch.equal(ref, inst["out"]):
         raise RuntimeError("fused and two-kernel outputs differ")
 
-    time_graphs(torch, stream, graphs, max(args.warmup, 3))
+    time_graphs(torch, stream, graphs, max(args.warmup, 3, len(graphs)))
+    torch.cuda.synchronize()
+    # F64 checks of sampled outputs right before and right after the timed
+    # region: two instances of every group of the pool
+    checked = [grp[j] for grp in groups for j in (0, len(grp) - 1)]
+    before = f64_check(checked)
+    if not before[0] <= TOL_BF16_FINAL:
+        raise RuntimeError(f"outputs before timing fail the F64 check: {before[0]:.3e}")
+    for inst in checked:   # poisoned, so that the check after timing sees the timed region's results
+        inst["out"].fill_(float("nan"))
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -363,6 +403,10 @@ def run_ours(args, rank, world, dev, torch, dist):
     ms, us_per_op = job_time(ms, args.steps, pack, world, dist, dev)
     if sk.splitk_get_device_status(stream) != 0:
         raise RuntimeError("a kernel's bounded wait ran out during the timed region")
+    ran = {id(i) for grp in groups[:min(args.steps, len(groups))] for i in grp}
+    after = f64_check([i for i in checked if id(i) in ran], seed=1)
+    if not after[0] <= TOL_BF16_FINAL:
+        raise RuntimeError(f"outputs after timing fail the F64 check: {after[0]:.3e}")
     ms_per_step = ms / args.steps
 
     if args.profile:
@@ -471,6 +515,11 @@ def run_ours(args, rank, world, dev, torch, dist):
                     "us": round(prep_us, 3), "bytes": 2 * K * N * 2,
                     "achieved_gbs": round(2 * K * N * 2 / (prep_us * 1e-6) / 1e9, 1),
                     "frac_of_hbm": round(2 * K * N * 2 / (prep_us * 1e-6) / 1e9 / hbm, 4)},
+        "checks": {"reference": "F64 product of the BF16 operands (numpy, from the same bits), sampled rows of "
+                                "two instances per group, max |out - ref| / sum|a*b|",
+                   "tolerance": TOL_BF16_FINAL,
+                   "before_timing": {"outputs": before[1], "max_scaled_err": float(f"{before[0]:.3e}")},
+                   "after_timing": {"outputs": after[1], "max_scaled_err": float(f"{after[0]:.3e}")}},
         "gpu_launches": args.steps * pack * plan["kernels_per_call"],
         "clocks": clocks.summary(),
     }
