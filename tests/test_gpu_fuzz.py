@@ -1,0 +1,123 @@
+"""GPU parity on seeded random legal geometries, and on large shapes checked at
+sampled points.
+
+The random cases draw M, N, K, the split length and the element type from the
+contract's legal space (M, K and k_per_split multiples of 32, N of 64,
+splits = ceil(K / k_per_split)), so that the tile planner meets shapes no
+hand-picked list holds: odd chunk counts, clusters that cannot hold every
+split, a short final split, chunks past its end.  Each is compared with the
+full oracle within the pages' tolerances, with guards, and the fused calls
+must give the two-kernel output bit for bit.
+
+The large shapes are too big for the full oracle in a test; the oracle's
+per-point evaluation checks partials and outputs at sampled (split, row,
+column) points, the rest of the output is checked for finiteness and the
+fused result against the two-kernel one.
+"""
+import numpy as np
+import pytest
+
+from harness import TOL_FINAL, TOL_PARTIAL, Guarded, device_operand, max_scaled_error, workspace
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import split_bf16_gemm_gb300 as sk
+
+    sk.build()
+    sk.lib()
+    sk.splitk_set_tile_override(0, 0, 0)
+    return sk
+
+
+def random_cases(n, seed=2024):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    cases = []
+    while len(cases) < n:
+        M = 32 * int(rng.integers(1, 21))          # 32 .. 640
+        N = 64 * int(rng.integers(1, 25))          # 64 .. 1536
+        K = 32 * int(rng.integers(1, 97))          # 32 .. 3072
+        kps = 32 * int(rng.integers(1, K // 32 + 1))
+        S = -(-K // kps)
+        dt = ("bf16", "f16", "f32")[int(rng.integers(0, 3))]
+        cases.append((M, N, K, S, kps, dt))
+    return cases
+
+
+RANDOM = random_cases(24)
+
+
+@pytest.mark.parametrize("case", RANDOM, ids=[f"{c[5]}-M{c[0]}N{c[1]}K{c[2]}S{c[3]}kps{c[4]}" for c in RANDOM])
+def test_random_geometry(lib, orc, case):
+    import splitk_inputs as gen
+
+    sk = lib
+    M, N, K, S, kps, dt = case
+    assert orc.contract(M, N, K, S, kps) == 0
+    ops = gen.uniform(M, N, K, dt, seed=M + N + K)
+    Pr, SP = orc.partials(ops.A, ops.B, dt, K, S, kps)
+    Or, SO = orc.output(ops.A, ops.B, dt)
+    A, B = device_operand(ops.A, dt), device_operand(ops.B, dt)
+    P, out = Guarded(S * M * N), Guarded(M * N)
+    sk.gemm_splitk_bt(A, B, P.data, M, N, K, S, kps, dt)
+    sk.splitk_reduce(P.data, out.data, S, M, N)
+    assert sk.splitk_get_device_status() == 0
+    assert P.guards_intact() and out.guards_intact()
+    assert max_scaled_error(P.numpy().reshape(S, M, N), Pr, SP) <= TOL_PARTIAL
+    assert max_scaled_error(out.numpy().reshape(M, N), Or, SO) <= TOL_FINAL[dt]
+    for fused in (1, 3):
+        ws, nbytes = workspace(M, N, K, S, kps)
+        o = Guarded(M * N)
+        sk.gemm_bt(A, B, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=fused)
+        assert sk.splitk_get_device_status() == 0
+        assert o.guards_intact() and ws.guards_intact()
+        assert np.array_equal(o.numpy().view(np.uint32), out.numpy().view(np.uint32)), fused
+
+
+LARGE = [(2048, 4096, 8192, 4, 2048, "bf16"), (1056, 2112, 5120, 5, 1024, "f16"),
+         (4096, 8192, 4096, 1, 4096, "bf16"), (1024, 2048, 8192, 2, 4096, "f32")]
+
+
+@pytest.mark.parametrize("case", LARGE, ids=[f"{c[5]}-M{c[0]}N{c[1]}K{c[2]}S{c[3]}" for c in LARGE])
+def test_large_shape_sampled(lib, orc, case):
+    import splitk_inputs as gen
+
+    sk = lib
+    M, N, K, S, kps, dt = case
+    ops = gen.uniform(M, N, K, dt, seed=7)
+    A, B = device_operand(ops.A, dt), device_operand(ops.B, dt)
+    P = Guarded(S * M * N)
+    out = Guarded(M * N)
+    sk.gemm_splitk_bt(A, B, P.data, M, N, K, S, kps, dt)
+    sk.splitk_reduce(P.data, out.data, S, M, N)
+    ws, nbytes = workspace(M, N, K, S, kps)
+    fused = torch.empty(M * N, dtype=torch.float32, device="cuda")
+    sk.gemm_bt(A, B, fused, ws.data, nbytes, M, N, K, S, kps, dt, fused=1)
+    assert sk.splitk_get_device_status() == 0
+    assert P.guards_intact() and out.guards_intact() and ws.guards_intact()
+    assert torch.equal(fused.view(torch.int32), out.data.view(torch.int32))
+    assert bool(torch.isfinite(out.data).all()) and bool(torch.isfinite(P.data).all())
+    rng = np.random.Generator(np.random.PCG64(M + K))
+    npts = 600
+    s = rng.integers(-1, S, npts)
+    m = rng.integers(0, M, npts)
+    n = rng.integers(0, N, npts)
+    m[:8] = [0, 0, M - 1, M - 1, 0, M - 1, M // 2, 1]     # the zero first row and the x4 last row
+    n[:8] = [0, N - 1, 0, N - 1, N // 2, N // 2, 0, N - 1]
+    val, bound = orc.points(ops.A, ops.B, dt, kps, S, s, m, n)
+    Pn = P.data.view(S, M, N)
+    On = out.data.view(M, N)
+    idx_s = torch.from_numpy(np.maximum(s, 0)).cuda()
+    idx_m = torch.from_numpy(m).cuda()
+    idx_n = torch.from_numpy(n).cuda()
+    got_p = Pn[idx_s, idx_m, idx_n].cpu().numpy()
+    got_o = On[idx_m, idx_n].cpu().numpy()
+    got = np.where(s >= 0, got_p, got_o)
+    part = s >= 0
+    assert max_scaled_error(got[part], val[part], bound[part]) <= TOL_PARTIAL
+    assert max_scaled_error(got[~part], val[~part], bound[~part]) <= TOL_FINAL[dt]
