@@ -199,6 +199,13 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t
            (static_cast<uint64_t>(2) << 61);
 }
 
+// A shared-memory descriptor from its two 32-bit halves (the start address
+// is in the low half).
+__device__ __forceinline__ uint64_t desc64(uint32_t lo, uint32_t hi)
+{
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
 // Instruction descriptor for tcgen05.mma .kind::f16 with F32 accumulation:
 // D format F32 (bits 4-5 = 1), A and B format (bits 7-9, 10-12: 0 = F16,
 // 1 = BF16), A K-major (bit 15 = 0), B K-major or, with `b_mn`, MN-major

@@ -47,6 +47,7 @@ struct TilePlan {
 constexpr int kTileM = 128;   // rows per CTA tile (tcgen05 M)
 constexpr int kBlockK = 64;   // K elements per pipeline stage: one 128-byte swizzle row
 constexpr int kMaxStages = 8;
+constexpr int kMaxKbs = 4;     // k-blocks in one pipeline stage (one TMA box per operand)
 constexpr int kMaxChunks = 8;  // portable cluster size
 
 // Arrival counters the fused path needs in the workspace, after the partials:

@@ -285,10 +285,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         issued_s = i;
     } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer
+        // ---- MMA issuer.  A single thread issues every MMA, and no other
+        // warp hides its scalar latency, so each tcgen05.mma must cost as few
+        // dependent instructions as possible: the stage's descriptors are
+        // built once, and each operand slice is reached by adding a constant
+        // to the descriptor's low word.  Its start-address field (bits 0-13,
+        // bytes >> 4) is the low end of that word and every shared-memory
+        // address is below 256 KB, so the addition never carries out of the
+        // field.  The k-blocks of a stage (at most kMaxKbs) and the K steps
+        // of a k-block are unrolled.  (A rolled loop with the descriptors
+        // rebuilt per MMA issued the 32 MMAs of a 128 x 64 x 512 chunk in
+        // about 3,600 cycles, against about 2,100 for the tensor core to run
+        // them.)
         const uint32_t idesc = X3 ? ptx::idesc_tf32_f32acc(kTileM, BN)
                                   : ptx::idesc_f16_f32acc(args.bf16 != 0, kTileM, BN, KN);
         const uint32_t b_lbo = static_cast<uint32_t>(kbs) * 8192u;   // [K,N]: next 64 columns
+        const uint32_t lo_half = load_bytes >> 4;                     // X3: the lo parts, in descriptor units
+        const bool short_tail = (klen % KB) != 0;   // a 2-D 16-bit chunk may end in a 32-long k-block
+        // one K step of k-block slice (a, b) (low descriptor words)
+        auto issue = [&](uint32_t a, uint32_t b, uint32_t ahi, uint32_t bhi, int k, uint32_t accumulate) {
+            if constexpr (X3) {
+                // the small products first, then hi*hi; +32 bytes (8 F32) along K per step
+                ptx::mma_tf32(tmem, ptx::desc64(a + 2u * k, ahi), ptx::desc64(b + lo_half + 2u * k, bhi), idesc,
+                              accumulate);
+                ptx::mma_tf32(tmem, ptx::desc64(a + lo_half + 2u * k, ahi), ptx::desc64(b + 2u * k, bhi), idesc, 1u);
+                ptx::mma_tf32(tmem, ptx::desc64(a + 2u * k, ahi), ptx::desc64(b + 2u * k, bhi), idesc, 1u);
+            } else if constexpr (KN) {
+                // A: +32 bytes along K; B: 16 k-rows of 128 bytes further (2 KB)
+                ptx::mma_f16(tmem, ptx::desc64(a + 2u * k, ahi), ptx::desc64(b + 128u * k, bhi), idesc, accumulate);
+            } else {
+                // +32 bytes along K inside the swizzled rows of both operands
+                ptx::mma_f16(tmem, ptx::desc64(a + 2u * k, ahi), ptx::desc64(b + 2u * k, bhi), idesc, accumulate);
+            }
+        };
         int i = 0;
         for (; i < nstg; ++i) {
             const int st = i % stages;
@@ -300,32 +329,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after_sync();
             const uint32_t sa = base + st * stage_bytes;
             const uint32_t sb = sa + kbs * Sh::kABytes;
-            for (int j = 0; j < kbs; ++j) {
-                const int kb = i * kbs + j;
-                if (kb >= nkb) break;
-                const uint64_t ad = ptx::sdesc_kmajor_sw128(sa + j * Sh::kABytes);
-                const int ksteps = min(KB, klen - kb * KB) / KSTEP;   // 4, or 2 for a 32-long 16-bit tail
-                if constexpr (X3) {
-                    // lo parts at the same offsets in the stage's second half;
-                    // the small products first, then hi*hi
-                    const uint64_t bd = ptx::sdesc_kmajor_sw128(sb + j * Sh::kBBytes);
-                    const uint64_t adl = ptx::sdesc_kmajor_sw128(sa + load_bytes + j * Sh::kABytes);
-                    const uint64_t bdl = ptx::sdesc_kmajor_sw128(sb + load_bytes + j * Sh::kBBytes);
-                    for (int k = 0; k < ksteps; ++k) {   // +32 bytes (8 F32) along K per step
-                        ptx::mma_tf32(tmem, ad + 2u * k, bdl + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
-                        ptx::mma_tf32(tmem, adl + 2u * k, bd + 2u * k, idesc, 1u);
-                        ptx::mma_tf32(tmem, ad + 2u * k, bd + 2u * k, idesc, 1u);
+            const uint64_t a0 = ptx::sdesc_kmajor_sw128(sa);
+            const uint64_t b0 = KN ? ptx::sdesc_mnmajor_sw128(sb, b_lbo) : ptx::sdesc_kmajor_sw128(sb);
+            const uint32_t alo = static_cast<uint32_t>(a0), ahi = static_cast<uint32_t>(a0 >> 32);
+            const uint32_t blo = static_cast<uint32_t>(b0), bhi = static_cast<uint32_t>(b0 >> 32);
+            const int kb0 = i * kbs;
+            const int nk = min(kbs, nkb - kb0);
+            uint32_t accumulate = i > 0 ? 1u : 0u;   // the chunk's first MMA starts the accumulator
+#pragma unroll
+            for (int j = 0; j < kMaxKbs; ++j) {
+                if (j >= nk) break;
+                const uint32_t a = alo + static_cast<uint32_t>(j) * (Sh::kABytes >> 4);
+                const uint32_t b = blo + static_cast<uint32_t>(j) * ((KN ? 8192u : Sh::kBBytes) >> 4);
+                if (short_tail && kb0 + j == nkb - 1) {
+                    // the 32-long tail: exactly two K steps (chunk lengths
+                    // are multiples of 32, so only a 16-bit 2-D chunk has
+                    // one).  The count is a constant on purpose: the same
+                    // two MMAs in a loop bounded by (klen % KB) / KSTEP
+                    // contributed only the first K step on GB300.
+#pragma unroll
+                    for (int k = 0; k < KB / KSTEP / 2; ++k) {
+                        issue(a, b, ahi, bhi, k, accumulate);
+                        accumulate = 1u;
                     }
-                } else if constexpr (!KN) {
-                    const uint64_t bd = ptx::sdesc_kmajor_sw128(sb + j * Sh::kBBytes);
-                    for (int k = 0; k < ksteps; ++k)   // +32 bytes along K inside the swizzled row
-                        ptx::mma_f16(tmem, ad + 2u * k, bd + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
                 } else {
-                    for (int k = 0; k < ksteps; ++k)   // A: +32 bytes; B: 16 k-rows of 128 bytes further
-                        ptx::mma_f16(tmem, ad + 2u * k,
-                                     ptx::sdesc_mnmajor_sw128(sb + static_cast<uint32_t>(j * 64 + k * 16) * 128u,
-                                                              b_lbo),
-                                     idesc, (kb | k) != 0 ? 1u : 0u);
+#pragma unroll
+                    for (int k = 0; k < KB / KSTEP; ++k) {
+                        issue(a, b, ahi, bhi, k, accumulate);
+                        accumulate = 1u;
+                    }
                 }
             }
             ptx::mma_commit(empty_bar(st));    // frees the slot once these MMAs have read it
@@ -765,9 +797,9 @@ struct StageChoice {
 StageChoice pick_stages(int bn, int nkb, bool can3d, int q, int share, bool x3 = false)
 {
     StageChoice r;
-    for (int cand : {4, 2, 1}) {
+    for (int cand : {kMaxKbs, 2, 1}) {
         if (!can3d && cand > 1) continue;
-        if (g_override_kbs && cand != std::min(g_override_kbs, can3d ? 4 : 1)) continue;
+        if (g_override_kbs && cand != std::min(g_override_kbs, can3d ? kMaxKbs : 1)) continue;
         const int want = (nkb + cand - 1) / cand;
         int st = std::min(want, kMaxStages);
         while (st > 1 && smem_for(bn, cand, st, q, share, x3) > kSmemLimit) --st;
@@ -914,7 +946,8 @@ TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool f
 
 cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t stream)
 {
-    if (plan.cluster > kMaxChunks || plan.stages > kMaxStages || plan.smem_bytes > kSmemLimit)
+    if (plan.cluster > kMaxChunks || plan.stages > kMaxStages || plan.kbs < 1 || plan.kbs > kMaxKbs ||
+        plan.smem_bytes > kSmemLimit)
         return note_error(cudaErrorInvalidConfiguration, "tile plan out of range");
     if (plan.fused && (pr.out == nullptr || (plan.split_sum == 1 && pr.counters == nullptr)))
         return note_error(cudaErrorInvalidValue, "fused launch without output or counters");
