@@ -161,7 +161,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int stages = args.stages;
     const uint32_t raw = ptx::smem_addr(dsmem);
     const uint32_t base = (raw + 1023u) & ~1023u;   // swizzle atoms are 1 KB
-    uint8_t *const gbase = dsmem + (base - raw);    // generic pointer to the same place
     const uint32_t E = base;                        // accumulator staging, over the ring
     const uint32_t recv = base + args.region0;      // the peers' shares of this CTA's pieces
 
@@ -450,23 +449,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ptx::mbar_wait_bounded(recv_bar, 0, args.wait_limit_ns) && tid == 0) atomicOr(&g_device_status, 16u);
     if (Q > 1) ptx::cluster_arrive_relaxed();  // everything bound for this CTA has landed
 
-    // ---- epilogue 2: sums of each owned piece over the cluster's ranks
+    // ---- epilogue 2: sums of each owned piece over the cluster's ranks.
+    // Eight warps do this part, so it is bound by latency, not bandwidth: the
+    // shared-memory base of every rank's contribution is computed once, and
+    // each thread loads both of its pieces (2 x Q float4) before it adds and
+    // stores, so the second piece's loads do not queue behind the first
+    // piece's stores.  (One piece at a time, with the offsets recomputed per
+    // rank and piece, this loop took about 0.5 us.)
     const int row0 = m_tile * kTileM, col0 = n_tile * BN;
     const size_t MN = static_cast<size_t>(args.M) * args.N;
+    const int rows_here = args.M - row0;                               // tile rows below M
+    const size_t tile0 = static_cast<size_t>(row0) * args.N + col0;   // the tile's first element
+    uint32_t rbase[Q];   // plus a piece's staging offset: that rank's contribution to the piece
+#pragma unroll
+    for (int r = 0; r < Q; ++r)
+        rbase[r] = r == rank ? E
+                             : recv + static_cast<uint32_t>(r - (r > rank ? 1 : 0)) * static_cast<uint32_t>(share) * 16u -
+                                   static_cast<uint32_t>(my_lo) * 16u;
     auto gather = [&](const Piece &p, float4 (&v)[Q]) {
 #pragma unroll
-        for (int r = 0; r < Q; ++r) {
-            const uint32_t off = r == rank ? p.off
-                                           : args.region0 + static_cast<uint32_t>(r - (r > rank ? 1 : 0)) *
-                                                                static_cast<uint32_t>(share) * 16u +
-                                                 (p.off - static_cast<uint32_t>(my_lo) * 16u);
-            v[r] = *reinterpret_cast<const float4 *>(gbase + off);
-        }
+        for (int r = 0; r < Q; ++r) v[r] = ptx::ld_shared_v4(rbase[r] + p.off);
     };
+    auto elem_of = [&](const Piece &p) { return tile0 + static_cast<size_t>(p.row) * args.N + p.col; };
     // the chunk sum of one split (Q == C): chunks in order 0, 1, 2, ...
-    auto chunk_sum = [&](const Piece &p) {
-        float4 v[Q];
-        gather(p, v);
+    auto chunk_sum = [&](const float4 (&v)[Q]) {
         float4 acc = v[0];
 #pragma unroll
         for (int r = 1; r < Q; ++r) add4(acc, v[r]);
@@ -474,13 +480,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (args.split_sum != 2) {
         float *const Ps = args.P + static_cast<size_t>(s) * MN;
-#pragma unroll 2
-        for (int g = my_lo + tid; g < my_hi; g += kThreads) {
-            const Piece p = piece_at(g);
-            const float4 acc = chunk_sum(p);
-            const int row = row0 + p.row;
-            if (row < args.M)
-                *reinterpret_cast<float4 *>(Ps + static_cast<size_t>(row) * args.N + col0 + p.col) = acc;
+        for (int g0 = my_lo + tid; g0 < my_hi; g0 += 2 * kThreads) {
+            const int g1 = g0 + kThreads;
+            const Piece p0 = piece_at(g0), p1 = piece_at(min(g1, my_hi - 1));
+            float4 v0[Q], v1[Q];
+            gather(p0, v0);
+            gather(p1, v1);
+            const float4 a0 = chunk_sum(v0), a1 = chunk_sum(v1);
+            if (p0.row < rows_here) *reinterpret_cast<float4 *>(Ps + elem_of(p0)) = a0;
+            if (g1 < my_hi && p1.row < rows_here) *reinterpret_cast<float4 *>(Ps + elem_of(p1)) = a1;
         }
     } else {
         const int cmask = C - 1, cshift = __ffs(C) - 1;
@@ -488,12 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // each split's chunk sum in chunk order, then the splits in split order,
         // the same additions the reduce kernel makes on the same partials (which
         // are also stored when P is given)
-        for (int g = my_lo + tid; g < my_hi; g += kThreads) {
-            const Piece p = piece_at(g);
-            const int row = row0 + p.row;
-            const size_t elem = static_cast<size_t>(row) * args.N + col0 + p.col;
-            float4 v[Q];
-            gather(p, v);
+        auto finish = [&](const Piece &p, const float4 (&v)[Q]) {
+            const size_t e = elem_of(p);
+            const bool live = p.row < rows_here;
             float4 part = v[0], tot = v[0];
 #pragma unroll
             for (int r = 0; r < Q; ++r) {
@@ -504,14 +509,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     add4(part, v[r]);
                 if (cc == cmask) {
                     const int sp = r >> cshift;
-                    if (args.P != nullptr && row < args.M) *reinterpret_cast<float4 *>(args.P + sp * MN + elem) = part;
+                    if (args.P != nullptr && live) *reinterpret_cast<float4 *>(args.P + sp * MN + e) = part;
                     if (sp == 0)
                         tot = part;
                     else
                         add4(tot, part);
                 }
             }
-            if (row < args.M) *reinterpret_cast<float4 *>(args.out + elem) = tot;
+            if (live) *reinterpret_cast<float4 *>(args.out + e) = tot;
+        };
+        for (int g0 = my_lo + tid; g0 < my_hi; g0 += 2 * kThreads) {
+            const int g1 = g0 + kThreads;
+            const Piece p0 = piece_at(g0), p1 = piece_at(min(g1, my_hi - 1));
+            float4 v0[Q], v1[Q];
+            gather(p0, v0);
+            gather(p1, v1);
+            finish(p0, v0);
+            if (g1 < my_hi) finish(p1, v1);
         }
     }
 
@@ -553,11 +567,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (t < walk_hi && sp < args.S) {
                                 const Piece p = piece_at(owned(t));
                                 const int row = row0 + p.row;
-                                if (sp == s)
-                                    v[j][i] = chunk_sum(p);
-                                else if (row < args.M)
+                                if (sp == s) {
+                                    float4 w[Q];
+                                    gather(p, w);
+                                    v[j][i] = chunk_sum(w);
+                                } else if (row < args.M) {
                                     v[j][i] = __ldcg(reinterpret_cast<const float4 *>(
                                         args.P + sp * MN + static_cast<size_t>(row) * args.N + col0 + p.col));
+                                }
                             }
                         }
                     }
