@@ -140,6 +140,70 @@ __device__ __forceinline__ uint32_t tf32_lo(uint32_t x)
     return __float_as_uint(__uint_as_float(x) - __uint_as_float(x & 0xFFFFE000u));
 }
 
+// The owner's sums when the cluster holds every split of the tile (rank =
+// split * CC + chunk): each split's chunks in chunk order, then the splits in
+// split order -- the additions the reduce kernel makes on the same partials,
+// which are also stored with HAS_P.  rbase[r] plus a piece's staging offset
+// addresses rank r's contribution to it.  The chunk count and HAS_P are
+// template parameters so that the grouping costs no branches: decided at run
+// time, the branches of this short sequence (resolved one after another in
+// every warp) about doubled the loop's time.  Each thread loads both of its
+// pieces (2 x Q float4) before it adds and stores.
+template <int Q, int CC, bool HAS_P>
+__device__ __forceinline__ void cluster_split_sum(const uint32_t (&rbase)[Q], int g_lo, int g_hi, int rows_here,
+                                                  size_t tile0, int N, size_t MN, float *P, float *out)
+{
+    static_assert(Q % CC == 0, "the cluster holds whole splits");
+    auto finish = [&](const Piece &p, const float4 (&v)[Q]) {
+        const size_t e = tile0 + static_cast<size_t>(p.row) * N + p.col;
+        const bool live = p.row < rows_here;
+        float4 tot = v[0];
+#pragma unroll
+        for (int sp = 0; sp < Q / CC; ++sp) {
+            float4 part = v[sp * CC];
+#pragma unroll
+            for (int c = 1; c < CC; ++c) add4(part, v[sp * CC + c]);
+            if (HAS_P && live) *reinterpret_cast<float4 *>(P + sp * MN + e) = part;
+            if (sp == 0)
+                tot = part;
+            else
+                add4(tot, part);
+        }
+        if (live) *reinterpret_cast<float4 *>(out + e) = tot;
+    };
+    for (int g0 = g_lo; g0 < g_hi; g0 += 2 * kThreads) {
+        const int g1 = g0 + kThreads;
+        const Piece p0 = piece_at(g0), p1 = piece_at(min(g1, g_hi - 1));
+        float4 v0[Q], v1[Q];
+#pragma unroll
+        for (int r = 0; r < Q; ++r) v0[r] = ptx::ld_shared_v4(rbase[r] + p0.off);
+#pragma unroll
+        for (int r = 0; r < Q; ++r) v1[r] = ptx::ld_shared_v4(rbase[r] + p1.off);
+        finish(p0, v0);
+        if (g1 < g_hi) finish(p1, v1);
+    }
+}
+
+template <int Q, bool HAS_P>
+__device__ __forceinline__ void cluster_split_sum_for(int C, const uint32_t (&rbase)[Q], int g_lo, int g_hi,
+                                                      int rows_here, size_t tile0, int N, size_t MN, float *P,
+                                                      float *out)
+{
+    switch (C) {   // the chunks of a split (a power of two dividing Q)
+    case 1: cluster_split_sum<Q, 1, HAS_P>(rbase, g_lo, g_hi, rows_here, tile0, N, MN, P, out); break;
+    case 2:
+        if constexpr (Q % 2 == 0) cluster_split_sum<Q, 2, HAS_P>(rbase, g_lo, g_hi, rows_here, tile0, N, MN, P, out);
+        break;
+    case 4:
+        if constexpr (Q % 4 == 0) cluster_split_sum<Q, 4, HAS_P>(rbase, g_lo, g_hi, rows_here, tile0, N, MN, P, out);
+        break;
+    case 8:
+        if constexpr (Q % 8 == 0) cluster_split_sum<Q, 8, HAS_P>(rbase, g_lo, g_hi, rows_here, tile0, N, MN, P, out);
+        break;
+    default: break;
+    }
+}
+
 // KN: B is the [K,N] weight (MN-major operand).  X3: F32 operands, each
 // product formed as three TF32 products (hi*lo + lo*hi + hi*hi).
 template <int BN, int Q, bool KN, bool X3>
@@ -453,9 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Eight warps do this part, so it is bound by latency, not bandwidth: the
     // shared-memory base of every rank's contribution is computed once, and
     // each thread loads both of its pieces (2 x Q float4) before it adds and
-    // stores, so the second piece's loads do not queue behind the first
-    // piece's stores.  (One piece at a time, with the offsets recomputed per
-    // rank and piece, this loop took about 0.5 us.)
+    // stores.
     const int row0 = m_tile * kTileM, col0 = n_tile * BN;
     const size_t MN = static_cast<size_t>(args.M) * args.N;
     const int rows_here = args.M - row0;                               // tile rows below M
@@ -470,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int r = 0; r < Q; ++r) v[r] = ptx::ld_shared_v4(rbase[r] + p.off);
     };
-    auto elem_of = [&](const Piece &p) { return tile0 + static_cast<size_t>(p.row) * args.N + p.col; };
+    auto tile_elem = [&](const Piece &p) { return tile0 + static_cast<size_t>(p.row) * args.N + p.col; };
     // the chunk sum of one split (Q == C): chunks in order 0, 1, 2, ...
     auto chunk_sum = [&](const float4 (&v)[Q]) {
         float4 acc = v[0];
@@ -487,46 +549,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             gather(p0, v0);
             gather(p1, v1);
             const float4 a0 = chunk_sum(v0), a1 = chunk_sum(v1);
-            if (p0.row < rows_here) *reinterpret_cast<float4 *>(Ps + elem_of(p0)) = a0;
-            if (g1 < my_hi && p1.row < rows_here) *reinterpret_cast<float4 *>(Ps + elem_of(p1)) = a1;
+            if (p0.row < rows_here) *reinterpret_cast<float4 *>(Ps + tile_elem(p0)) = a0;
+            if (g1 < my_hi && p1.row < rows_here) *reinterpret_cast<float4 *>(Ps + tile_elem(p1)) = a1;
         }
+    } else if (args.P != nullptr) {
+        cluster_split_sum_for<Q, true>(C, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, args.P, args.out);
     } else {
-        const int cmask = C - 1, cshift = __ffs(C) - 1;
-        // the cluster holds every split of the tile (rank = split * C + chunk):
-        // each split's chunk sum in chunk order, then the splits in split order,
-        // the same additions the reduce kernel makes on the same partials (which
-        // are also stored when P is given)
-        auto finish = [&](const Piece &p, const float4 (&v)[Q]) {
-            const size_t e = elem_of(p);
-            const bool live = p.row < rows_here;
-            float4 part = v[0], tot = v[0];
-#pragma unroll
-            for (int r = 0; r < Q; ++r) {
-                const int cc = r & cmask;       // C is a power of two
-                if (cc == 0)
-                    part = v[r];
-                else
-                    add4(part, v[r]);
-                if (cc == cmask) {
-                    const int sp = r >> cshift;
-                    if (args.P != nullptr && live) *reinterpret_cast<float4 *>(args.P + sp * MN + e) = part;
-                    if (sp == 0)
-                        tot = part;
-                    else
-                        add4(tot, part);
-                }
-            }
-            if (live) *reinterpret_cast<float4 *>(args.out + e) = tot;
-        };
-        for (int g0 = my_lo + tid; g0 < my_hi; g0 += 2 * kThreads) {
-            const int g1 = g0 + kThreads;
-            const Piece p0 = piece_at(g0), p1 = piece_at(min(g1, my_hi - 1));
-            float4 v0[Q], v1[Q];
-            gather(p0, v0);
-            gather(p1, v1);
-            finish(p0, v0);
-            if (g1 < my_hi) finish(p1, v1);
-        }
+        cluster_split_sum_for<Q, false>(C, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, nullptr, args.out);
     }
 
     // ---- split sum by counters: the last split to finish this piece range

@@ -121,3 +121,46 @@ def test_large_shape_sampled(lib, orc, case):
     part = s >= 0
     assert max_scaled_error(got[part], val[part], bound[part]) <= TOL_PARTIAL
     assert max_scaled_error(got[~part], val[~part], bound[~part]) <= TOL_FINAL[dt]
+
+
+GROUPINGS = [(1, 1), (2, 1), (1, 2), (4, 1), (2, 2), (1, 4), (8, 1), (4, 2), (2, 4), (1, 8)]
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("grouping", GROUPINGS, ids=[f"S{s}C{c}" for s, c in GROUPINGS])
+def test_cluster_split_sum_groupings(lib, orc, grouping, dt):
+    """Every (splits, chunks) grouping that one cluster sums on chip (splits x
+    chunks a power of two up to 8), with the partials discarded (fused=1) or
+    kept (fused=3): the output and kept partials equal the two-kernel path's
+    bit for bit, and the output is within the pages' tolerance of the oracle."""
+    import splitk_inputs as gen
+
+    sk = lib
+    S, C = grouping
+    M, N = 96, 128
+    kps = C * 64
+    K = S * kps
+    ops = gen.uniform(M, N, K, dt, seed=S * 16 + C)
+    Or, SO = orc.output(ops.A, ops.B, dt)
+    A, B = device_operand(ops.A, dt), device_operand(ops.B, dt)
+    try:
+        sk.splitk_set_tile_override(64, C, 0)
+        plan = sk.splitk_describe_launch(M, N, K, S, kps, dt, fused=1)
+        assert plan["chunks"] == C and plan["cluster"] == S * C and plan["split_sum"] == 2, plan
+        P, out = Guarded(S * M * N), Guarded(M * N)
+        sk.gemm_splitk_bt(A, B, P.data, M, N, K, S, kps, dt)
+        sk.splitk_reduce(P.data, out.data, S, M, N)
+        ref_bits = out.numpy().view(np.uint32)
+        assert max_scaled_error(out.numpy().reshape(M, N), Or, SO) <= TOL_FINAL[dt]
+        for fused in (1, 3):
+            ws, nbytes = workspace(M, N, K, S, kps)
+            o = Guarded(M * N)
+            sk.gemm_bt(A, B, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=fused)
+            assert sk.splitk_get_device_status() == 0
+            assert o.guards_intact() and ws.guards_intact()
+            assert np.array_equal(o.numpy().view(np.uint32), ref_bits), fused
+            if fused == 3:
+                kept = ws.numpy()[:S * M * N].view(np.uint32)
+                assert np.array_equal(kept, P.numpy().view(np.uint32))
+    finally:
+        sk.splitk_set_tile_override(0, 0, 0)
