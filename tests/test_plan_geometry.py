@@ -1,0 +1,155 @@
+"""Host-side geometry of every tile plan the library makes (no GPU needed).
+
+The tensor-core kernel trusts the plan that `splitk_describe_launch` reports:
+which K range each CTA loads, how its shared memory is laid out, which
+pieces of the output tile each cluster rank owns and where the peers'
+contributions land.  This test restates that index arithmetic on the CPU and
+checks, for hand-picked shapes, the seeded random geometries of the GPU
+tests, and every tile override:
+
+- the chunks of each split load every k of the split exactly once, each TMA
+  box starting on a 16-byte boundary and inside K;
+- the shared-memory size is the stage ring (or the accumulator staging, if
+  larger), one receive slot per peer and the alignment slack, within the
+  per-block limit;
+- a rank's share of the tile is a whole number of 32 x 32 boxes (each warp
+  pushes whole boxes), every 16-byte piece has exactly one owner, and every
+  contribution sent to or read from a receive slot stays inside that slot.
+"""
+import itertools
+
+import pytest
+
+from test_gpu_fuzz import LARGE, RANDOM
+
+SMEM_LIMIT = 226 * 1024
+TILE_M = 128
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import split_bf16_gemm_gb300 as sk
+
+    sk.build()
+    sk.lib()
+    return sk
+
+
+def piece(g):
+    """Staging offset, tile row and tile column of 16-byte piece g (the
+    kernel's layout: 32 x 32 float boxes, 128-byte rows, 16-byte pieces
+    swizzled by the row)."""
+    b, rb, j = g >> 8, (g >> 3) & 31, g & 7
+    return ((g >> 3) << 7) | ((j ^ (rb & 7)) << 4), (b & 3) * 32 + rb, (b >> 2) * 32 + j * 4
+
+
+def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
+    sk.splitk_set_tile_override(bn, ch, kbs)
+    try:
+        d = sk.splitk_describe_launch(M, N, K, S, kps, dt, fused=fused)
+    finally:
+        sk.splitk_set_tile_override(0, 0, 0)
+    x3 = dt == "f32"
+    kb_elems, elem = (32, 4) if x3 else (64, 2)
+    BN, C, CL, stages = d["bn"], d["chunks"], d["chunk_len"], d["stages"]
+    Q, KBS, T3, SS = d["cluster"], d["kblocks_per_stage"], d["three_d"], d["split_sum"]
+    assert d["path"] == (2 if x3 else 0)
+    assert C in (1, 2, 4, 8) and Q in (1, 2, 4, 8) and 1 <= stages <= 8 and 1 <= KBS <= 4
+    assert Q == C or (SS == 2 and Q == S * C)
+    assert (d["grid_x"], d["grid_y"], d["grid_z"]) == (N // BN, -(-M // TILE_M), S * C)
+    assert N % BN == 0 and d["grid_z"] % Q == 0
+    if T3:
+        assert K % kb_elems == 0 and kps % kb_elems == 0 and CL % kb_elems == 0
+    else:
+        assert KBS == 1
+
+    # shared memory: the ring (or the accumulator staging) + receive slots + slack
+    pieces = 32 * BN
+    share = -(-(-(-pieces // Q)) // 8) * 8
+    stage_bytes = (TILE_M + BN) * 128 * KBS * (2 if x3 else 1)
+    epi_bytes = TILE_M * BN * 4
+    region0 = -(-max(stages * stage_bytes, epi_bytes) // 1024) * 1024
+    assert d["smem_bytes"] == region0 + (Q - 1) * share * 16 + 1024 <= SMEM_LIMIT
+
+    # K coverage: every k of every split loaded exactly once, boxes aligned
+    for s in range(S):
+        ks, ke = s * kps, min(s * kps + kps, K)
+        covered = []
+        for c in range(C):
+            lo = ks + c * CL
+            hi = min(lo + CL, ke)
+            klen = max(0, hi - lo)
+            nkb = -(-klen // kb_elems)
+            if T3:
+                assert lo % kb_elems == 0
+            for i in range(-(-nkb // KBS)):
+                if T3:
+                    assert lo // kb_elems + i * KBS < K // kb_elems     # the box starts inside K
+                for j in range(KBS):
+                    kb = i * KBS + j
+                    if kb >= nkb:
+                        break
+                    kx = lo + kb * kb_elems
+                    valid = min(kb_elems, klen - kb * kb_elems)
+                    assert valid in (32, 64) and (kx * elem) % 16 == 0 and kx < K
+                    covered += range(kx, kx + valid)
+        assert covered == list(range(ks, ke)), (s, ks, ke)
+
+    # ownership and the exchange
+    if Q > 1:
+        assert share % 256 == 0, "a rank's share must be whole 32 x 32 boxes"
+    own = [(min(pieces, r * share), min(pieces, min(pieces, r * share) + share)) for r in range(Q)]
+    owner = {}
+    for r, (lo, hi) in enumerate(own):
+        assert lo % 8 == 0 and hi % 8 == 0
+        for g in range(lo, hi):
+            off, row, col = piece(g)
+            assert lo * 16 <= off < hi * 16 and off + 16 <= epi_bytes
+            assert (row, col) not in owner
+            owner[(row, col)] = r
+    assert len(owner) == pieces
+    recv = region0
+    for sender in range(Q):
+        for b in range(pieces // 256):              # the box a warp stages and pushes
+            r = (b * 256) // share
+            if r == sender:
+                continue
+            assert own[r][0] <= b * 256 and b * 256 + 256 <= own[r][1]
+            slot = sender - (1 if sender > r else 0)
+            dst = recv + (slot * share + (b * 256 - r * share)) * 16
+            assert recv + slot * share * 16 <= dst and dst + 4096 <= recv + (slot + 1) * share * 16
+            assert dst + 4096 <= d["smem_bytes"] - 1024
+    for me, (lo, hi) in enumerate(own):             # the owner's reads of its peers' slots
+        for r in range(Q):
+            if r == me:
+                continue
+            slot = r - (1 if r > me else 0)
+            base = recv + slot * share * 16 - lo * 16
+            for g in (lo, hi - 1) if hi > lo else ():
+                addr = base + piece(g)[0]
+                assert recv + slot * share * 16 <= addr and addr + 16 <= recv + (slot + 1) * share * 16
+
+
+CASES = [(32, 64, 128, 2, 64), (96, 512, 2048, 4, 512), (256, 512, 2048, 4, 512), (256, 1024, 2048, 2, 1024),
+         (64, 128, 160, 3, 64), (32, 64, 32, 1, 32), (160, 192, 320, 3, 128), (96, 320, 1024, 2, 512),
+         (64, 128, 8192, 4, 2048), (512, 2048, 4096, 4, 1024), (288, 256, 96, 3, 32)]
+CASES += [(32, 512, 2048, s, 2048 // s) for s in (1, 2, 4, 8, 16)] + [(96, 512, 512, s, 512 // s) for s in (1, 2, 4, 8, 16)]
+OVERRIDES = [(0, 0, 0)] + list(itertools.product((64, 128, 256), (1, 2, 4, 8), (0, 1, 2, 4)))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_plan_geometry_hand_picked(lib, dt):
+    n = 0
+    for case in CASES:
+        for fused in (0, 1):
+            for ov in OVERRIDES:
+                check_plan(lib, *case, fused, dt, *ov)
+                n += 1
+    assert n == len(CASES) * 2 * len(OVERRIDES)
+
+
+def test_plan_geometry_random_and_large(lib):
+    for c in RANDOM + LARGE:
+        for fused in (0, 1):
+            for ov in OVERRIDES:
+                check_plan(lib, *c[:5], fused, c[5], *ov)
