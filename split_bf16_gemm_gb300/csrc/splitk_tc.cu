@@ -673,9 +673,48 @@ CUtensorMapDataType map_type(int et)
 }
 int elem_of(int et) { return et == 2 ? 4 : 2; }
 
+// A tensor map depends only on the arguments that encode it (address, shape,
+// box, element type), not on the data, so calls that repeat them reuse it:
+// each host thread keeps the last kMapCache maps it encoded.
+struct MapKey {
+    const void *ptr;
+    int64_t rows, K;
+    int box_rows, kbs, et, rank;
+    bool operator==(const MapKey &o) const
+    {
+        return ptr == o.ptr && rows == o.rows && K == o.K && box_rows == o.box_rows && kbs == o.kbs &&
+               et == o.et && rank == o.rank;
+    }
+};
+constexpr int kMapCache = 16;
+struct MapEntry {
+    CUtensorMap map;
+    MapKey key;
+    bool valid;
+};
+thread_local MapEntry t_maps[kMapCache];
+thread_local int t_map_next = 0;
+
+template <typename Encode>
+bool cached_map(CUtensorMap *map, const MapKey &key, Encode encode)
+{
+    for (const MapEntry &e : t_maps)
+        if (e.valid && e.key == key) {
+            *map = e.map;
+            return true;
+        }
+    if (!encode(map)) return false;
+    MapEntry &slot = t_maps[t_map_next];
+    slot.map = *map;
+    slot.key = key;
+    slot.valid = true;
+    t_map_next = (t_map_next + 1) % kMapCache;
+    return true;
+}
+
 // Row-major [rows, K] matrix, box = box_rows x one 128-byte row (64 16-bit
 // or 32 F32 elements), 128-byte swizzle.
-bool encode_operand(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows, int et)
+bool encode_operand_uncached(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows, int et)
 {
     auto fn = encode_fn();
     if (!fn) {
@@ -695,11 +734,18 @@ bool encode_operand(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, 
     return r == CUDA_SUCCESS;
 }
 
+bool encode_operand(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows, int et)
+{
+    return cached_map(map, MapKey{ptr, rows, K, box_rows, 1, et, 2},
+                      [&](CUtensorMap *m) { return encode_operand_uncached(m, ptr, rows, K, box_rows, et); });
+}
+
 // Row-major [rows, K] matrix seen as 3-D (element within a k-block of one
 // 128-byte row, row, k-block), box = k-block x box_rows x kbs, 128-byte
 // swizzle: one load brings kbs k-blocks of a tile.  Needs K to be a whole
 // number of k-blocks, so that no k-block runs past the end of a row.
-bool encode_operand_3d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows, int kbs, int et)
+bool encode_operand_3d_uncached(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows, int kbs,
+                                int et)
 {
     auto fn = encode_fn();
     if (!fn) {
@@ -719,6 +765,12 @@ bool encode_operand_3d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t 
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) note_message("cuTensorMapEncodeTiled (3-D) failed", static_cast<int>(r));
     return r == CUDA_SUCCESS;
+}
+
+bool encode_operand_3d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows, int kbs, int et)
+{
+    return cached_map(map, MapKey{ptr, rows, K, box_rows, kbs, et, 3},
+                      [&](CUtensorMap *m) { return encode_operand_3d_uncached(m, ptr, rows, K, box_rows, kbs, et); });
 }
 
 int g_override_bn = 0, g_override_chunks = 0, g_override_kbs = 0;
@@ -903,7 +955,47 @@ double estimate_tc_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, b
     return t;
 }
 
+namespace {
+
+TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3);
+
+// The plan depends only on the problem's shape, the element width, `fused`
+// and the tile override, so each host thread keeps the last kPlanCache plans.
+struct PlanKey {
+    int64_t M, N, K, S, kps;
+    bool fused, x3;
+    int ov_bn, ov_chunks, ov_kbs;
+    bool operator==(const PlanKey &o) const
+    {
+        return M == o.M && N == o.N && K == o.K && S == o.S && kps == o.kps && fused == o.fused && x3 == o.x3 &&
+               ov_bn == o.ov_bn && ov_chunks == o.ov_chunks && ov_kbs == o.ov_kbs;
+    }
+};
+constexpr int kPlanCache = 8;
+struct PlanEntry {
+    PlanKey key;
+    TilePlan plan;
+    bool valid;
+};
+thread_local PlanEntry t_plans[kPlanCache];
+thread_local int t_plan_next = 0;
+
+}  // namespace
+
 TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3)
+{
+    const PlanKey key{M, N, K, S, kps, fused, x3, g_override_bn, g_override_chunks, g_override_kbs};
+    for (const PlanEntry &e : t_plans)
+        if (e.valid && e.key == key) return e.plan;
+    const TilePlan p = plan_tc_uncached(M, N, K, S, kps, fused, x3);
+    t_plans[t_plan_next] = PlanEntry{key, p, true};
+    t_plan_next = (t_plan_next + 1) % kPlanCache;
+    return p;
+}
+
+namespace {
+
+TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3)
 {
     // Stages of several k-blocks load as one 3-D box per operand, which the
     // TMA unit moves much faster than the same bytes in 16 KB boxes; that needs
@@ -989,6 +1081,8 @@ TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool f
     p.smem_bytes = smem_for(bn, p.kbs, p.stages, q, share, x3);
     return p;
 }
+
+}  // namespace
 
 cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t stream)
 {
