@@ -139,7 +139,7 @@ class OracleSample:
     its bounds) of `rows` output rows of the workload.  The work is linear in
     the rows, so its time scales to one whole operation by M/rows."""
 
-    def __init__(self, rows: int = 32):
+    def __init__(self, rows: int = 32, threads=None):
         import oracle
         import splitk_inputs as gen
 
@@ -148,7 +148,7 @@ class OracleSample:
         self.A = ops.A[:rows].copy()
         self.B = ops.B
         self.rows = rows
-        self.threads = max(1, len(os.sched_getaffinity(0)))
+        self.threads = threads or max(1, len(os.sched_getaffinity(0)))
         self.cores = min(self.threads, rows)
 
     def once(self) -> float:
@@ -166,8 +166,8 @@ class OracleSample:
                 f"the oracle's partials + unsplit output, scaled by {M}/{self.rows}")
 
 
-def oracle_rows_timing(seconds: float, rows: int = 32):
-    smp = OracleSample(rows)
+def oracle_rows_timing(seconds: float, rows: int = 32, threads=None):
+    smp = OracleSample(rows, threads)
     smp.once()   # warm-up
     reps, total = 0, 0.0
     while total < seconds or reps == 0:
@@ -595,8 +595,12 @@ def main():
     line = run_ours(args, rank, world, dev, torch, dist)
     if rank == 0 and world == 1 and not args.profile:
         us, cores, sample = oracle_rows_timing(args.cpu_seconds)
+        # the same oracle on one core
+        us1, _, sample1 = oracle_rows_timing(args.cpu_seconds / 3, threads=1)
         line["cpu_baseline"] = {"value": round(us, 2), "unit": "µs/op", "cores": cores,
-                                "kind": "oracle", "sample": sample}
+                                "kind": "oracle", "sample": sample,
+                                "single_thread": {"value": round(us1, 2), "unit": "µs/op", "cores": 1,
+                                                  "sample": sample1}}
     if rank == 0:
         print(json.dumps(line))
     if dist:
