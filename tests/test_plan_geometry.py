@@ -153,3 +153,27 @@ def test_plan_geometry_random_and_large(lib):
         for fused in (0, 1):
             for ov in OVERRIDES:
                 check_plan(lib, *c[:5], fused, c[5], *ov)
+
+
+def test_plan_follows_override_changes(lib):
+    """Plans are cached per host thread; a change of the tile override must
+    still give the plan for the new override, and clearing it the default."""
+    shape = (256, 1024, 2048, 2, 1024)
+    default = lib.splitk_describe_launch(*shape, "bf16", fused=1)
+    seen = []
+    try:
+        for ov in ((64, 4, 0), (64, 1, 0), (128, 2, 2), (64, 4, 0)):
+            lib.splitk_set_tile_override(*ov)
+            p = lib.splitk_describe_launch(*shape, "bf16", fused=1)
+            assert p["bn"] == ov[0] and p["chunks"] == ov[1], (ov, p)
+            if ov[2]:
+                assert p["kblocks_per_stage"] == ov[2]
+            seen.append(p)
+    finally:
+        lib.splitk_set_tile_override(0, 0, 0)
+    assert seen[0] == seen[3]
+    assert lib.splitk_describe_launch(*shape, "bf16", fused=1) == default
+    # other dtypes and fused flags of the same shape are distinct entries
+    assert lib.splitk_describe_launch(*shape, "f32", fused=1)["path"] == 2
+    assert lib.splitk_describe_launch(*shape, "bf16", fused=0)["fused_in_kernel"] == 0
+    assert default["fused_in_kernel"] == 1
