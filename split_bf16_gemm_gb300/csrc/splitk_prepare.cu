@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(kPrepThreads)
     // padded by one 32-bit word per row: the column reads spread over the banks
     __shared__ T tile[kTile][kTile + 4 / sizeof(T)];
     ptx::grid_dependency_wait();                         // W may be the previous grid's output
+    ptx::launch_dependents();                            // the next launch may start its blocks now
     const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kTile;
     const int64_t k0 = static_cast<int64_t>(blockIdx.y) * kTile;
     // W rows k0..k0+63, columns n0..n0+63  ->  tile[k - k0][n - n0]
