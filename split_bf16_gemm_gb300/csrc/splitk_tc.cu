@@ -189,19 +189,32 @@ __device__ __forceinline__ void cluster_split_sum_for(int C, const uint32_t (&rb
                                                       int rows_here, size_t tile0, int N, size_t MN, float *P,
                                                       float *out)
 {
-    switch (C) {   // the chunks of a split (a power of two dividing Q)
-    case 1: cluster_split_sum<Q, 1, HAS_P>(rbase, g_lo, g_hi, rows_here, tile0, N, MN, P, out); break;
-    case 2:
-        if constexpr (Q % 2 == 0) cluster_split_sum<Q, 2, HAS_P>(rbase, g_lo, g_hi, rows_here, tile0, N, MN, P, out);
-        break;
-    case 4:
-        if constexpr (Q % 4 == 0) cluster_split_sum<Q, 4, HAS_P>(rbase, g_lo, g_hi, rows_here, tile0, N, MN, P, out);
-        break;
-    case 8:
-        if constexpr (Q % 8 == 0) cluster_split_sum<Q, 8, HAS_P>(rbase, g_lo, g_hi, rows_here, tile0, N, MN, P, out);
-        break;
-    default: break;
+    // the chunks of a split: a power of two dividing Q (the host checks this
+    // before the launch; anything else would leave `out` unwritten, so it
+    // is reported in the status word rather than skipped silently)
+    if (C == 1) {
+        cluster_split_sum<Q, 1, HAS_P>(rbase, g_lo, g_hi, rows_here, tile0, N, MN, P, out);
+        return;
     }
+    if constexpr (Q % 2 == 0) {
+        if (C == 2) {
+            cluster_split_sum<Q, 2, HAS_P>(rbase, g_lo, g_hi, rows_here, tile0, N, MN, P, out);
+            return;
+        }
+    }
+    if constexpr (Q % 4 == 0) {
+        if (C == 4) {
+            cluster_split_sum<Q, 4, HAS_P>(rbase, g_lo, g_hi, rows_here, tile0, N, MN, P, out);
+            return;
+        }
+    }
+    if constexpr (Q % 8 == 0) {
+        if (C == 8) {
+            cluster_split_sum<Q, 8, HAS_P>(rbase, g_lo, g_hi, rows_here, tile0, N, MN, P, out);
+            return;
+        }
+    }
+    atomicOr(&g_device_status, 64u);
 }
 
 // KN: B is the [K,N] weight (MN-major operand).  X3: F32 operands, each
@@ -1086,8 +1099,10 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
 
 cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t stream)
 {
+    const bool chunks_ok = (plan.chunks & (plan.chunks - 1)) == 0 && plan.chunks >= 1 && plan.chunks <= kMaxChunks &&
+                           plan.cluster % plan.chunks == 0;
     if (plan.cluster > kMaxChunks || plan.stages > kMaxStages || plan.kbs < 1 || plan.kbs > kMaxKbs ||
-        plan.smem_bytes > kSmemLimit)
+        plan.smem_bytes > kSmemLimit || !chunks_ok)
         return note_error(cudaErrorInvalidConfiguration, "tile plan out of range");
     if (plan.fused && (pr.out == nullptr || (plan.split_sum == 1 && pr.counters == nullptr)))
         return note_error(cudaErrorInvalidValue, "fused launch without output or counters");
