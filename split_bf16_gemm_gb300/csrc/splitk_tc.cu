@@ -452,11 +452,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             const uint32_t sa = base + st * stage_bytes;
-            for (uint32_t off = static_cast<uint32_t>(t) * 16u; off < load_bytes; off += (kThreads - 64) * 16u) {
-                const float4 v = ptx::ld_shared_v4(sa + off);
+            // four 16-byte pieces per thread at a time: their loads are issued
+            // before any of their stores (the shared-memory accesses are
+            // ordered asm, so one piece at a time would wait out each load)
+            constexpr uint32_t kStep = (kThreads - 64) * 16u;
+            constexpr int kBatch = 4;
+            auto convert_store = [&](uint32_t off, const float4 &v) {
                 ptx::st_shared_v4(sa + load_bytes + off, tf32_lo(__float_as_uint(v.x)), tf32_lo(__float_as_uint(v.y)),
                                   tf32_lo(__float_as_uint(v.z)), tf32_lo(__float_as_uint(v.w)));
+            };
+            uint32_t off = static_cast<uint32_t>(t) * 16u;
+            for (; off + (kBatch - 1) * kStep < load_bytes; off += kBatch * kStep) {
+                float4 v[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) v[u] = ptx::ld_shared_v4(sa + off + u * kStep);
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) convert_store(off + u * kStep, v[u]);
             }
+            for (; off < load_bytes; off += kStep) convert_store(off, ptx::ld_shared_v4(sa + off));
             ptx::fence_proxy_async_smem();     // the tensor cores read what these threads wrote
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(conv_bar(st));
