@@ -945,8 +945,9 @@ int share_for(int bn, int q)
 
 // Time model of one launch (microseconds), from measurements on GB300: the
 // loads are bound by the L2 (about 10.5 TB/s for all SMs) or by one SM's TMA
-// intake (about 100 GB/s); staging the accumulator runs near 100 GB/s, the
-// distributed-shared-memory exchange and the final stores near 30 GB/s per SM.
+// intake (about 100 GB/s); staging the accumulator and the owners' stores to
+// L2 run near 100 GB/s, the distributed-shared-memory exchange near 30 GB/s
+// per SM.
 double model_us(int64_t M, int64_t N, int64_t S, int bn, int chunks, int64_t chunk_len, int q, int elem = 2)
 {
     const int64_t mt = (M + kTileM - 1) / kTileM;
@@ -956,7 +957,9 @@ double model_us(int64_t M, int64_t N, int64_t S, int bn, int chunks, int64_t chu
     const double t_load = std::max(load / 1.0e5, ctas * load / 1.05e7);
     const double t_stage = acc / 1.0e5;
     const double t_exchange = acc * (q - 1) / q / 3.0e4;
-    const double t_store = acc / q / 3.0e4;
+    // the owner's stores go to L2 (~100 GB/s per SM); the F32 plans were fitted with 30 GB/s,
+    // which stands in there for the converter warps' share of the stage time
+    const double t_store = acc / q / (elem == 4 ? 3.0e4 : 1.0e5);
     const int64_t per_wave = q > 1 ? static_cast<int64_t>(resident_clusters(q)) * q : 148;
     const int64_t waves = (ctas + per_wave - 1) / per_wave;
     return static_cast<double>(waves) * (t_load + t_stage + t_exchange + t_store);
