@@ -164,3 +164,48 @@ def test_cluster_split_sum_groupings(lib, orc, grouping, dt):
                 assert np.array_equal(kept, P.numpy().view(np.uint32))
     finally:
         sk.splitk_set_tile_override(0, 0, 0)
+
+
+@pytest.mark.parametrize("case", RANDOM, ids=[f"{c[5]}-M{c[0]}N{c[1]}K{c[2]}S{c[3]}kps{c[4]}" for c in RANDOM])
+def test_random_geometry_kn_and_prepare(lib, orc, case):
+    """The same random geometries with the weight in its [K,N] layout: weight
+    preparation gives the exact transpose; the [K,N] path gives the [N,K]
+    path's partials and outputs bit for bit with 16-bit operands (the same
+    products in the same order), and F32 (exact FMA there, 3xTF32 here)
+    within the pages' tolerances of the oracle."""
+    import splitk_inputs as gen
+
+    sk = lib
+    M, N, K, S, kps, dt = case
+    ops = gen.uniform(M, N, K, dt, seed=M + N + K)
+    A, B = device_operand(ops.A, dt), device_operand(ops.B, dt)
+    W = B.t().contiguous()
+    B2 = torch.full_like(B, 0)
+    sk.splitk_prepare_bt(W, B2, K, N, dt)
+    torch.cuda.synchronize()
+    assert torch.equal(B2.view(torch.int16 if dt != "f32" else torch.int32),
+                       B.view(torch.int16 if dt != "f32" else torch.int32))
+    P, out = Guarded(S * M * N), Guarded(M * N)
+    sk.gemm_splitk_bt(A, B, P.data, M, N, K, S, kps, dt)
+    sk.splitk_reduce(P.data, out.data, S, M, N)
+    Pk, outk = Guarded(S * M * N), Guarded(M * N)
+    sk.gemm_splitk_kn(A, W, Pk.data, M, N, K, S, kps, dt)
+    sk.splitk_reduce(Pk.data, outk.data, S, M, N)
+    fused = []
+    for f in (1, 3):
+        ws, nbytes = workspace(M, N, K, S, kps)
+        o = Guarded(M * N)
+        sk.gemm_kn(A, W, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=f)
+        fused.append((o, ws))
+    assert sk.splitk_get_device_status() == 0
+    assert all(g.guards_intact() for g in (P, out, Pk, outk)) and all(o.guards_intact() and w.guards_intact() for o, w in fused)
+    if dt != "f32":
+        assert np.array_equal(Pk.numpy().view(np.uint32), P.numpy().view(np.uint32))
+        assert np.array_equal(outk.numpy().view(np.uint32), out.numpy().view(np.uint32))
+    else:
+        Pr, SP = orc.partials(ops.A, ops.B, dt, K, S, kps)
+        Or, SO = orc.output(ops.A, ops.B, dt)
+        assert max_scaled_error(Pk.numpy().reshape(S, M, N), Pr, SP) <= TOL_PARTIAL
+        assert max_scaled_error(outk.numpy().reshape(M, N), Or, SO) <= TOL_FINAL[dt]
+    for o, _ in fused:   # the fused [K,N] call adds the [K,N] partials in the reduce kernel's order
+        assert np.array_equal(o.numpy().view(np.uint32), outk.numpy().view(np.uint32))
