@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 M, N, K, SPLITS, KPS = 256, 1024, 2048, 2, 1024
 DTYPE = "bf16"
 WORKLOAD = "BF16 split-K GEMM M=256 N=1024 K=2048 splits=2 (k_per_split=1024) + reduce"
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal
 METRIC = BASE_METRIC = "split-K GEMM+reduce µs/op & TFLOP/s, % of roofline (BF16 M256/N1024/K2048)"
 FLOPS_PER_OP = 2 * M * N * K
 BYTES_2PASS = M * K * 2 + N * K * 2 + 2 * SPLITS * M * N * 4 + M * N * 4   # A+B, P write+read, out
@@ -514,7 +515,11 @@ def run_ours(args, rank, world, dev, torch, dist):
             "frac_2pass_bytes": round(BYTES_2PASS / (hbm * 1e9) * 1e6 / us_per_op, 4),
             "t_roof_us_min_bytes": round(BYTES_FUSED / (hbm * 1e9) * 1e6, 4),
             "frac_min_bytes": round(BYTES_FUSED / (hbm * 1e9) * 1e6 / us_per_op, 4),
-            "peak": f"{peak_kind} {hbm} GB/s"},
+            "peak": f"{peak_kind} {hbm} GB/s",
+            # against the nominal HBM3e bandwidth as well
+            "nominal_gbs": NOMINAL_HBM_GBS,
+            "frac_2pass_bytes_nominal": round(BYTES_2PASS / (NOMINAL_HBM_GBS * 1e9) * 1e6 / us_per_op, 4),
+            "frac_min_bytes_nominal": round(BYTES_FUSED / (NOMINAL_HBM_GBS * 1e9) * 1e6 / us_per_op, 4)},
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1),
                      "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "traffic": kernel_traffic() if fused else None, "bytes_per_launch": dom_bytes,
