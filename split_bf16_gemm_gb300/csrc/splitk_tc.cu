@@ -1,7 +1,8 @@
 // splitk_tc.cu -- the split-K partial pass on the 5th-generation tensor cores.
 //
 // Computes partials[s,m,n] = sum over split s of A[m,k]*B[n,k] for 16-bit
-// operands (BF16 or F16, native, no staging through another type), the
+// operands (BF16 or F16, native, no staging through another type) and for
+// F32 operands as 3xTF32 products (X3), the
 // contract of the pages "Aligned shared rows for pipelined NAX on CUDA" and
 // "Wider consecutive-weight NAX GEMM" (sections "Contract and correctness" /
 // "Launch contract and correctness").  Optionally the same launch also sums
@@ -12,10 +13,13 @@
 //                  rows) and of B (BN rows), 128-byte swizzled, into a ring
 //                  of `stages` buffers; the first stages go out before tensor
 //                  memory is allocated;
-//   warp 1 lane 0  MMA issuer: tcgen05.mma (M=128, N=BN, K=16), accumulating
-//                  in tensor memory (BN 32-bit columns);
+//   warp 1 lane 0  MMA issuer: tcgen05.mma (M=128, N=BN, K=16; K=8 and three
+//                  products per step with X3) from descriptors built once
+//                  per stage, accumulating in tensor memory (BN 32-bit
+//                  columns);
 //   warps 2-7      before the dependency wait, in the CTAs that start beside
 //                  the previous launch: L2 prefetch of this launch's A and B;
+//                  with X3, after it: the lo parts of each landed stage;
 //   all 8 warps    epilogue: tensor memory -> registers -> shared memory
 //                  (swizzled 32x32 float boxes, reusing the stage ring).
 // B is either the prepared [N,K] weight (K-major operand) or, with KN, the
