@@ -276,6 +276,17 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 
+// Atomic increment with wrap (the value becomes 0 after `limit`), with
+// acquire-release semantics at GPU scope: it publishes what the calling
+// thread wrote or observed (through a preceding CTA barrier) before it, and
+// makes what other threads published the same way visible after it.
+__device__ __forceinline__ unsigned atom_inc_acq_rel_gpu(unsigned *p, unsigned limit)
+{
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(limit) : "memory");
+    return old;
+}
+
 // ------------------------------------------------------- cluster / DSMEM
 
 __device__ __forceinline__ uint32_t cluster_ctarank()

@@ -591,16 +591,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- split sum by counters: the last split to finish this piece range
     // adds all splits (Q == C here)
     if (args.split_sum == 1) {
-        __threadfence();                       // this thread's partials, before the arrival count
+        // the CTA's partials are all written (the barrier); thread 0's arrival
+        // count publishes them (release, cumulative over what the barrier
+        // ordered before it) and, for the last arriver, acquires the other
+        // splits' partials, which the second barrier passes on to all threads
         __syncthreads();
         if (tid == 0) {
             const unsigned idx = (static_cast<unsigned>(m_tile) * gridDim.x + n_tile) * C + c;   // c == rank
-            const unsigned old = atomicInc(&args.counters[idx], static_cast<unsigned>(args.S - 1));
+            const unsigned old = ptx::atom_inc_acq_rel_gpu(&args.counters[idx], static_cast<unsigned>(args.S - 1));
             last_s = old == static_cast<unsigned>(args.S - 1) ? 1u : 0u;
         }
         __syncthreads();
         if (last_s) {
-            __threadfence();
             // kPieceBatch pieces per thread, the loads of kSplitBatch splits
             // in flight at once (one L2 round trip per kSplitBatch splits,
             // not per split); the adds still run in split order 0..S-1.  With
