@@ -209,3 +209,50 @@ def test_random_geometry_kn_and_prepare(lib, orc, case):
         assert max_scaled_error(outk.numpy().reshape(M, N), Or, SO) <= TOL_FINAL[dt]
     for o, _ in fused:   # the fused [K,N] call adds the [K,N] partials in the reduce kernel's order
         assert np.array_equal(o.numpy().view(np.uint32), outk.numpy().view(np.uint32))
+
+
+def test_concurrent_host_threads(lib):
+    """Four host threads, each on its own stream, call gemm_bt (fused and not)
+    on different shapes and element types at the same time (ctypes releases
+    the GIL); every result equals the single-threaded one bit for bit."""
+    import threading
+
+    import splitk_inputs as gen
+
+    sk = lib
+    cases = [(256, 1024, 2048, 2, 1024, "bf16"), (96, 512, 2048, 4, 512, "f16"),
+             (160, 192, 320, 3, 128, "bf16"), (64, 256, 1024, 2, 512, "f32")]
+    prepared = []
+    for M, N, K, S, kps, dt in cases:
+        ops = gen.uniform(M, N, K, dt, seed=M + K)
+        A, B = device_operand(ops.A, dt), device_operand(ops.B, dt)
+        ws, nbytes = workspace(M, N, K, S, kps)
+        ref = torch.empty(M * N, dtype=torch.float32, device="cuda")
+        sk.gemm_bt(A, B, ref, ws.data, nbytes, M, N, K, S, kps, dt, fused=0)
+        torch.cuda.synchronize()
+        prepared.append((M, N, K, S, kps, dt, A, B, ref))
+    errors = []
+
+    def worker(idx):
+        try:
+            M, N, K, S, kps, dt, A, B, ref = prepared[idx]
+            stream = torch.cuda.Stream()
+            ws, nbytes = workspace(M, N, K, S, kps)
+            outs = [torch.empty(M * N, dtype=torch.float32, device="cuda") for _ in range(2)]
+            torch.cuda.synchronize()   # the workspace's set-up ran on torch's default stream
+            for it in range(20):
+                sk.gemm_bt(A, B, outs[it & 1], ws.data, nbytes, M, N, K, S, kps, dt, fused=it % 2, stream=stream)
+            stream.synchronize()
+            for o in outs:
+                if not torch.equal(o.view(torch.int32), ref.view(torch.int32)):
+                    errors.append((idx, "result differs"))
+        except Exception as e:   # reported below, in the main thread
+            errors.append((idx, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(prepared))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    assert sk.splitk_get_device_status() == 0
