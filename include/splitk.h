@@ -31,7 +31,10 @@
  * Memory and ownership: every data pointer is a DEVICE pointer on the current
  * CUDA device, owned by the caller, except the host activations and results
  * of gemm_bt_host_batch.  The library allocates no device memory on any call
- * path and keeps no pointer after a call returns.
+ * path and keeps no pointer to caller memory for use after a call returns.
+ * (Each host thread caches, in host memory, the last tile plans and TMA
+ * tensor maps it built; a cached map records an address and a shape and is
+ * reused only by a later call with the same address and shape.)
  *
  * Asynchrony and errors: calls enqueue work on `stream` (a cudaStream_t, passed
  * as void*; NULL means the legacy default stream) and return without
@@ -286,8 +289,9 @@ int splitk_autotune_splits(const void *A, const void *B, float *out,
 
 /* Reads and clears the device status word on the current device,
  * synchronising `stream` first.  Returns SPLITK_OK, SPLITK_ERR_DEVICE_TIMEOUT
- * (a kernel's bounded wait ran out since the last call; its outputs are not
- * valid) or SPLITK_ERR_CUDA. */
+ * (since the last call a kernel's bounded wait ran out, or a launch met a tile
+ * configuration it cannot run; that launch's outputs are not valid) or
+ * SPLITK_ERR_CUDA. */
 int splitk_get_device_status(void *stream);
 
 /* What the most recent SPLITK_ERR_CUDA on the calling host thread came from:
