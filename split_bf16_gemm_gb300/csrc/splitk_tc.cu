@@ -1059,8 +1059,9 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
             if (!pick_stages(bn, nkb, can3d, c, share_for(bn, c), x3).ok) continue;
             const int64_t tiles = mt * (N / bn);
             const int64_t sq = S * c;
+            // a single CTA per tile needs no cluster: its sum is its own tile
             const bool cluster_sum = sq <= kMaxChunks && (sq & (sq - 1)) == 0 &&
-                                     tiles <= resident_clusters(static_cast<int>(sq)) &&
+                                     (sq == 1 || tiles <= resident_clusters(static_cast<int>(sq))) &&
                                      pick_stages(bn, nkb, can3d, static_cast<int>(sq),
                                                  share_for(bn, static_cast<int>(sq)), x3).ok;
             const double cost = model_us(M, N, S, bn, c, len, c, x3 ? 4 : 2) + (cluster_sum ? 0.0 : 1.5);
@@ -1084,7 +1085,7 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     if (fused) {
         const int sq = static_cast<int>(S) * chunks;
         split_sum = 1;
-        if (sq <= kMaxChunks && (sq & (sq - 1)) == 0 && tiles <= resident_clusters(sq) &&
+        if (sq <= kMaxChunks && (sq & (sq - 1)) == 0 && (sq == 1 || tiles <= resident_clusters(sq)) &&
             pick_stages(bn, nkb, can3d, sq, share_for(bn, sq), x3).ok) {
             q = sq;
             split_sum = 2;
