@@ -80,7 +80,8 @@ def test_random_geometry(lib, orc, case):
 
 
 LARGE = [(2048, 4096, 8192, 4, 2048, "bf16"), (1056, 2112, 5120, 5, 1024, "f16"),
-         (4096, 8192, 4096, 1, 4096, "bf16"), (1024, 2048, 8192, 2, 4096, "f32")]
+         (4096, 8192, 4096, 1, 4096, "bf16"), (1024, 2048, 8192, 2, 4096, "f32"),
+         (2048, 8192, 8192, 2, 4096, "bf16")]
 
 
 @pytest.mark.parametrize("case", LARGE, ids=[f"{c[5]}-M{c[0]}N{c[1]}K{c[2]}S{c[3]}" for c in LARGE])

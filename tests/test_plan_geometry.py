@@ -12,6 +12,9 @@ tests, and every tile override:
 - the shared-memory size is the stage ring (or the accumulator staging, if
   larger), one receive slot per peer and the alignment slack, within the
   per-block limit;
+- the grid covers every tile once, with the row tiles along x exactly when
+  the launch is more than one wave, B's slab is over 32 MB and A's is the
+  smaller;
 - a rank's share of the tile is a whole number of 32 x 32 boxes (each warp
   pushes whole boxes), every 16-byte piece has exactly one owner, and every
   contribution sent to or read from a receive slot stays inside that slot.
@@ -24,6 +27,7 @@ from test_gpu_fuzz import LARGE, RANDOM
 
 SMEM_LIMIT = 226 * 1024
 TILE_M = 128
+RESIDENT_CLUSTERS = {1: 148, 2: 72, 4: 36, 8: 15}   # clusters of 1-8 CTAs a GB300 keeps resident
 
 
 @pytest.fixture(scope="module")
@@ -56,7 +60,15 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
     assert d["path"] == (2 if x3 else 0)
     assert C in (1, 2, 4, 8) and Q in (1, 2, 4, 8) and 1 <= stages <= 8 and 1 <= KBS <= 4
     assert Q == C or (SS == 2 and Q == S * C)
-    assert (d["grid_x"], d["grid_y"], d["grid_z"]) == (N // BN, -(-M // TILE_M), S * C)
+    mt = -(-M // TILE_M)
+    tiles_xy = (mt, N // BN) if d["rows_first"] else (N // BN, mt)
+    assert (d["grid_x"], d["grid_y"], d["grid_z"]) == (*tiles_xy, S * C)
+    assert d["grid_y"] <= 65535
+    # row tiles first only for launches of more than one wave whose B slab
+    # (one split of B) outgrows a quarter of L2, with A's slab the smaller
+    waves = mt * (N // BN) * S * C // Q > RESIDENT_CLUSTERS[Q]
+    b_slab = N * kps * (4 if x3 else 2)
+    assert d["rows_first"] == int(waves and mt * TILE_M < N and b_slab > 32 << 20 and N // BN <= 65535)
     assert N % BN == 0 and d["grid_z"] % Q == 0
     if T3:
         assert K % kb_elems == 0 and kps % kb_elems == 0 and CL % kb_elems == 0
