@@ -81,7 +81,31 @@ def test_random_geometry(lib, orc, case):
 
 LARGE = [(2048, 4096, 8192, 4, 2048, "bf16"), (1056, 2112, 5120, 5, 1024, "f16"),
          (4096, 8192, 4096, 1, 4096, "bf16"), (1024, 2048, 8192, 2, 4096, "f32"),
-         (2048, 8192, 8192, 2, 4096, "bf16")]
+         (2048, 8192, 8192, 2, 4096, "bf16"), (2048, 4096, 4096, 1, 4096, "f32")]
+
+
+def check_sampled(orc, ops, dt, M, N, S, kps, P, out, npts=600):
+    """Partials and outputs at seeded (split, row, column) points against the
+    oracle's per-point evaluation, the first eight on the zero first row, the
+    scaled last row and the corners."""
+    rng = np.random.Generator(np.random.PCG64(M + ops.A.shape[1]))
+    s = rng.integers(-1, S, npts)
+    m = rng.integers(0, M, npts)
+    n = rng.integers(0, N, npts)
+    m[:8] = [0, 0, M - 1, M - 1, 0, M - 1, M // 2, 1]     # the zero first row and the x4 last row
+    n[:8] = [0, N - 1, 0, N - 1, N // 2, N // 2, 0, N - 1]
+    val, bound = orc.points(ops.A, ops.B, dt, kps, S, s, m, n)
+    Pn = P.view(S, M, N)
+    On = out.view(M, N)
+    idx_s = torch.from_numpy(np.maximum(s, 0)).cuda()
+    idx_m = torch.from_numpy(m).cuda()
+    idx_n = torch.from_numpy(n).cuda()
+    got_p = Pn[idx_s, idx_m, idx_n].cpu().numpy()
+    got_o = On[idx_m, idx_n].cpu().numpy()
+    got = np.where(s >= 0, got_p, got_o)
+    part = s >= 0
+    assert max_scaled_error(got[part], val[part], bound[part]) <= TOL_PARTIAL
+    assert max_scaled_error(got[~part], val[~part], bound[~part]) <= TOL_FINAL[dt]
 
 
 @pytest.mark.parametrize("case", LARGE, ids=[f"{c[5]}-M{c[0]}N{c[1]}K{c[2]}S{c[3]}" for c in LARGE])
@@ -103,25 +127,43 @@ def test_large_shape_sampled(lib, orc, case):
     assert P.guards_intact() and out.guards_intact() and ws.guards_intact()
     assert torch.equal(fused.view(torch.int32), out.data.view(torch.int32))
     assert bool(torch.isfinite(out.data).all()) and bool(torch.isfinite(P.data).all())
-    rng = np.random.Generator(np.random.PCG64(M + K))
-    npts = 600
-    s = rng.integers(-1, S, npts)
-    m = rng.integers(0, M, npts)
-    n = rng.integers(0, N, npts)
-    m[:8] = [0, 0, M - 1, M - 1, 0, M - 1, M // 2, 1]     # the zero first row and the x4 last row
-    n[:8] = [0, N - 1, 0, N - 1, N // 2, N // 2, 0, N - 1]
-    val, bound = orc.points(ops.A, ops.B, dt, kps, S, s, m, n)
-    Pn = P.data.view(S, M, N)
-    On = out.data.view(M, N)
-    idx_s = torch.from_numpy(np.maximum(s, 0)).cuda()
-    idx_m = torch.from_numpy(m).cuda()
-    idx_n = torch.from_numpy(n).cuda()
-    got_p = Pn[idx_s, idx_m, idx_n].cpu().numpy()
-    got_o = On[idx_m, idx_n].cpu().numpy()
-    got = np.where(s >= 0, got_p, got_o)
-    part = s >= 0
-    assert max_scaled_error(got[part], val[part], bound[part]) <= TOL_PARTIAL
-    assert max_scaled_error(got[~part], val[~part], bound[~part]) <= TOL_FINAL[dt]
+    check_sampled(orc, ops, dt, M, N, S, kps, P.data, out.data)
+
+
+ROW_FIRST_KN = [(4096, 8192, 4096, 1, 4096, "bf16"), (2048, 4096, 4096, 1, 4096, "f32")]
+
+
+@pytest.mark.parametrize("case", ROW_FIRST_KN, ids=[f"{c[5]}-M{c[0]}N{c[1]}K{c[2]}S{c[3]}" for c in ROW_FIRST_KN])
+def test_large_kn_row_first(lib, orc, case):
+    """The [K,N] weight on large shapes that the planner puts in the row-first
+    tile order: 16-bit operands give the [N,K] path's partials and outputs bit
+    for bit, F32 the oracle's values at sampled points; the fused call gives
+    the two-kernel output bit for bit."""
+    import splitk_inputs as gen
+
+    sk = lib
+    M, N, K, S, kps, dt = case
+    assert sk.splitk_describe_launch(M, N, K, S, kps, dt, fused=0)["rows_first"] == 1
+    ops = gen.uniform(M, N, K, dt, seed=5)
+    A, B = device_operand(ops.A, dt), device_operand(ops.B, dt)
+    W = B.t().contiguous()
+    Pk, outk = Guarded(S * M * N), Guarded(M * N)
+    sk.gemm_splitk_kn(A, W, Pk.data, M, N, K, S, kps, dt)
+    sk.splitk_reduce(Pk.data, outk.data, S, M, N)
+    ws, nbytes = workspace(M, N, K, S, kps)
+    fused = Guarded(M * N)
+    sk.gemm_kn(A, W, fused.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=1)
+    assert sk.splitk_get_device_status() == 0
+    assert Pk.guards_intact() and outk.guards_intact() and fused.guards_intact() and ws.guards_intact()
+    assert torch.equal(fused.data.view(torch.int32), outk.data.view(torch.int32))
+    if dt != "f32":
+        del W
+        P, out = Guarded(S * M * N), Guarded(M * N)
+        sk.gemm_splitk_bt(A, B, P.data, M, N, K, S, kps, dt)
+        sk.splitk_reduce(P.data, out.data, S, M, N)
+        assert torch.equal(Pk.data.view(torch.int32), P.data.view(torch.int32))
+        assert torch.equal(outk.data.view(torch.int32), out.data.view(torch.int32))
+    check_sampled(orc, ops, dt, M, N, S, kps, Pk.data, outk.data)
 
 
 GROUPINGS = [(1, 1), (2, 1), (1, 2), (4, 1), (2, 2), (1, 4), (8, 1), (4, 2), (2, 4), (1, 8)]
