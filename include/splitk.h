@@ -312,7 +312,7 @@ const char *splitk_status_string(int status);
  * SPLITK_OK or SPLITK_ERR_CONFIG. */
 int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
 
-/* Describes the launch gemm_bt would make, without launching: info[0..16] =
+/* Describes the launch gemm_bt would make, without launching: info[0..17] =
  * {path (0 tensor-core, 2 tensor-core 3xTF32 for F32), bn, chunks, chunk_len, stages,
  *  cluster_size (chunks, or splits * chunks), grid_x, grid_y, grid_z,
  *  dynamic_smem_bytes,
@@ -323,7 +323,10 @@ int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
  *  before the dependency wait), rows_first (1: grid x walks the 128-row tiles
  *  and grid y the column tiles, so grid_x and grid_y are swapped; chosen for
  *  launches of more than one wave with M < N whose B slab per split,
- *  N * k_per_split elements, is over 32 MB)}; `info` must hold 17 ints.
+ *  N * k_per_split elements, is over 32 MB), tile_m (rows of A per thread
+ *  block: 128, or 256 for BN 256 plans with one block per tile, no cluster
+ *  and no arrival counters, chosen when it saves waves; grid_x or grid_y
+ *  then counts 256-row tiles)}; `info` must hold 18 ints.
  * Returns a status as gemm_bt's validation would (pointers are not checked). */
 int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits,
                            int64_t k_per_split, int dtype, int fused,

@@ -253,12 +253,12 @@ def splitk_set_tile_override(bn: int = 0, chunks: int = 0, kblocks_per_stage: in
 
 
 def splitk_describe_launch(M, N, K, splits, k_per_split, dtype, fused=0) -> dict:
-    info = (ctypes.c_int * 17)()
+    info = (ctypes.c_int * 18)()
     _check(lib().splitk_describe_launch(M, N, K, splits, k_per_split, dtype_code(dtype), fused,
                                         ctypes.addressof(info)), "splitk_describe_launch")
     keys = ("path", "bn", "chunks", "chunk_len", "stages", "cluster", "grid_x", "grid_y",
             "grid_z", "smem_bytes", "fused_in_kernel", "kernels_per_call", "kblocks_per_stage",
-            "three_d", "split_sum", "prefetchers", "rows_first")
+            "three_d", "split_sum", "prefetchers", "rows_first", "tile_m")
     return dict(zip(keys, list(info)))
 
 

@@ -309,7 +309,7 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
     if (st != SPLITK_OK) return st;
     if (elem_bytes(dtype) == 0) return SPLITK_ERR_DTYPE;
     if (!info) return SPLITK_ERR_NULL;
-    std::fill(info, info + 17, 0);
+    std::fill(info, info + 18, 0);
     const bool x3 = dtype == SPLITK_F32;
     const bool in_kernel = fused != 0 && fused_possible(dtype, false);
     const TilePlan p = splitk::plan_tc(M, N, K, splits, k_per_split, in_kernel, x3);
@@ -330,6 +330,7 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
     info[14] = p.split_sum;
     info[15] = in_kernel ? p.prefetchers : 0;   // gemm_bt's two-kernel path does not prefetch
     info[16] = p.rows_first;
+    info[17] = p.tile_m;
     return SPLITK_OK;
 }
 

@@ -41,6 +41,7 @@ struct TilePlan {
     int prefetchers;    // CTAs (the first in dispatch order) that prefetch A and B into L2
     int x3;             // F32 operands as 3xTF32: 32-element k-blocks, stages twice the loaded bytes
     int rows_first;     // grid x walks the row tiles, y the column tiles (else x columns, y rows)
+    int tile_m;         // rows of A per CTA: 128, or 256 (two accumulators; BN 256, one CTA per tile)
     dim3 grid;
     size_t smem_bytes;  // dynamic shared memory per CTA
 };

@@ -51,6 +51,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -98,12 +99,14 @@ __device__ __forceinline__ void prefetch_part(const uint8_t *p, uint64_t bytes, 
         ptx::prefetch_l2_line(p + off);
 }
 
-template <int BN>
+// TM: rows of A per CTA.  128 is one MMA's M; 256 (BN = 256 only) is two
+// accumulators, rows 0-127 and 128-255, which share every B operand.
+template <int BN, int TM = kTileM>
 struct TcShape {
-    static constexpr uint32_t kABytes = kTileM * kBlockK * 2;     // one k-block of A: 16 KB
+    static constexpr uint32_t kABytes = TM * kBlockK * 2;         // one k-block of A: 16 or 32 KB
     static constexpr uint32_t kBBytes = BN * kBlockK * 2;         // one k-block of B
-    static constexpr uint32_t kTmemCols = BN;                     // power of two >= 32
-    static constexpr int kPieces = kTileM * BN / 4;               // 16-byte pieces per tile
+    static constexpr uint32_t kTmemCols = BN * (TM / kTileM);     // power of two >= 32
+    static constexpr int kPieces = kTileM * BN / 4;               // 16-byte pieces per 128-row tile
 };
 
 // Piece g of the staged tile: 4 consecutive F32 of one row.  Box b = g >> 8
@@ -223,16 +226,20 @@ __device__ __forceinline__ void cluster_split_sum_for(int C, const uint32_t (&rb
 }
 
 // KN: B is the [K,N] weight (MN-major operand).  X3: F32 operands, each
-// product formed as three TF32 products (hi*lo + lo*hi + hi*hi).
-template <int BN, int Q, bool KN, bool X3>
+// product formed as three TF32 products (hi*lo + lo*hi + hi*hi).  TM: rows
+// of A per CTA; 256 only for 16-bit operands, BN = 256 and one CTA per tile
+// that keeps or sums its own partials (no cluster, no arrival counters).
+template <int BN, int Q, bool KN, bool X3, int TM = kTileM>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const TcArgs args)
 {
     static_assert(!(KN && X3), "F32 operands with the [K,N] weight run on the CUDA cores");
+    static_assert(TM == kTileM || (TM == 2 * kTileM && BN == 256 && Q == 1 && !X3), "256-row tiles");
     constexpr int KB = X3 ? 32 : kBlockK;          // k elements per 128-byte swizzle row
     constexpr int KSTEP = X3 ? 8 : 16;             // k per MMA instruction
-    using Sh = TcShape<BN>;
+    constexpr int kHalves = TM / kTileM;           // accumulators (128-row halves of the tile)
+    using Sh = TcShape<BN, TM>;
     extern __shared__ uint8_t dsmem[];
     __shared__ __align__(8) uint64_t bars[3 * kMaxStages + 2];
     __shared__ uint32_t tmem_slot;
@@ -284,13 +291,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive_expect_tx(bar, load_bytes);
         if (args.three_d) {                         // one box per operand: kbs k-blocks at once
             const int kb = k_lo / KB + i * kbs;
-            ptx::tma_load_3d(sa, &tmA, bar, 0, m_tile * kTileM, kb, ptx::l2_policy_evict_last());
+            ptx::tma_load_3d(sa, &tmA, bar, 0, m_tile * TM, kb, ptx::l2_policy_evict_last());
             if constexpr (!KN)
                 ptx::tma_load_3d(sa + kbs * Sh::kABytes, &tmB, bar, 0, n_tile * BN, kb,
                                  ptx::l2_policy_evict_normal());
         } else {                                    // kbs == 1
             const int kx = k_lo + i * KB;
-            ptx::tma_load_2d(sa, &tmA, bar, kx, m_tile * kTileM, ptx::l2_policy_evict_last());
+            ptx::tma_load_2d(sa, &tmA, bar, kx, m_tile * TM, ptx::l2_policy_evict_last());
             if constexpr (!KN)
                 ptx::tma_load_2d(sa + Sh::kABytes, &tmB, bar, kx, n_tile * BN, ptx::l2_policy_evict_normal());
         }
@@ -392,12 +399,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                               accumulate);
                 ptx::mma_tf32(tmem, ptx::desc64(a + lo_half + 2u * k, ahi), ptx::desc64(b + 2u * k, bhi), idesc, 1u);
                 ptx::mma_tf32(tmem, ptx::desc64(a + 2u * k, ahi), ptx::desc64(b + 2u * k, bhi), idesc, 1u);
-            } else if constexpr (KN) {
-                // A: +32 bytes along K; B: 16 k-rows of 128 bytes further (2 KB)
-                ptx::mma_f16(tmem, ptx::desc64(a + 2u * k, ahi), ptx::desc64(b + 128u * k, bhi), idesc, accumulate);
             } else {
-                // +32 bytes along K inside the swizzled rows of both operands
-                ptx::mma_f16(tmem, ptx::desc64(a + 2u * k, ahi), ptx::desc64(b + 2u * k, bhi), idesc, accumulate);
+                // A: +32 bytes along K inside its swizzled rows.  B: the same,
+                // or for the [K,N] weight 16 k-rows of 128 bytes further (2 KB)
+                const uint32_t bk = b + (KN ? 128u : 2u) * k;
+                ptx::mma_f16(tmem, ptx::desc64(a + 2u * k, ahi), ptx::desc64(bk, bhi), idesc, accumulate);
+                if constexpr (TM == 2 * kTileM)   // rows 128-255: 16 KB further, the second accumulator
+                    ptx::mma_f16(tmem + BN, ptx::desc64(a + 1024u + 2u * k, ahi), ptx::desc64(bk, bhi), idesc,
+                                 accumulate);
             }
         };
         int i = 0;
@@ -501,166 +510,176 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3, half = warp >> 2;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const bool have_acc = nkb > 0 && !aborted;
+    // With two accumulators (TM = 256) the staging, the stores and the sums
+    // below run once per 128-row half, the second after the first's stores
+    // have read the staging.
 #pragma unroll 1
-    for (int jb = half * (BN / 64); jb < (half + 1) * (BN / 64); ++jb) {
-        uint32_t v[32];
-        if (have_acc) {
-            ptx::tmem_ld_32x32b_x32(lane_base + jb * 32, v);
-        } else {
+    for (int h = 0; h < kHalves; ++h) {
+        if (h > 0) __syncthreads();
+#pragma unroll 1
+        for (int jb = half * (BN / 64); jb < (half + 1) * (BN / 64); ++jb) {
+            uint32_t v[32];
+            if (have_acc) {
+                ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(h * BN + jb * 32), v);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0u;
+                for (int i = 0; i < 32; ++i) v[i] = 0u;
+            }
+            const uint32_t row_addr = E + static_cast<uint32_t>(jb * 4 + quarter) * 4096u + lane * 128u;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                ptx::st_shared_v4(row_addr + (static_cast<uint32_t>(q ^ (lane & 7)) << 4), v[4 * q],
+                                  v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
-        const uint32_t row_addr = E + static_cast<uint32_t>(jb * 4 + quarter) * 4096u + lane * 128u;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            ptx::st_shared_v4(row_addr + (static_cast<uint32_t>(q ^ (lane & 7)) << 4), v[4 * q],
-                              v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-    }
-    ptx::fence_proxy_async_smem();             // the staging is the source of bulk copies
-    // ---- exchange: each warp pushes the boxes it staged to their owners
-    // (a box of 32 rows x 32 columns is 256 pieces; a rank's share is a
-    // whole number of boxes), so the copies start while other warps stage
-    if (Q > 1) {
-        ptx::cluster_wait();                   // every peer's receive barrier is set up
-        __syncwarp();
-        if (lane == 0) {
-            for (int jb = half * (BN / 64); jb < (half + 1) * (BN / 64); ++jb) {
-                const int b = jb * 4 + quarter;
-                const int r = (b * 256) / share;
-                if (r == rank) continue;
-                const uint32_t slot = static_cast<uint32_t>(rank - (rank > r ? 1 : 0));
-                ptx::bulk_copy_to_cluster(ptx::mapa(recv + (slot * static_cast<uint32_t>(share) +
-                                                             static_cast<uint32_t>(b * 256 - r * share)) * 16u, r),
-                                          E + static_cast<uint32_t>(b) * 4096u, 4096u, ptx::mapa(recv_bar, r));
+        ptx::fence_proxy_async_smem();             // the staging is the source of bulk copies
+        // ---- exchange: each warp pushes the boxes it staged to their owners
+        // (a box of 32 rows x 32 columns is 256 pieces; a rank's share is a
+        // whole number of boxes), so the copies start while other warps stage
+        if (Q > 1) {
+            ptx::cluster_wait();                   // every peer's receive barrier is set up
+            __syncwarp();
+            if (lane == 0) {
+                for (int jb = half * (BN / 64); jb < (half + 1) * (BN / 64); ++jb) {
+                    const int b = jb * 4 + quarter;
+                    const int r = (b * 256) / share;
+                    if (r == rank) continue;
+                    const uint32_t slot = static_cast<uint32_t>(rank - (rank > r ? 1 : 0));
+                    ptx::bulk_copy_to_cluster(ptx::mapa(recv + (slot * static_cast<uint32_t>(share) +
+                                                                 static_cast<uint32_t>(b * 256 - r * share)) * 16u, r),
+                                              E + static_cast<uint32_t>(b) * 4096u, 4096u, ptx::mapa(recv_bar, r));
+                }
             }
         }
-    }
-    ptx::tc_fence_before_sync();
-    __syncthreads();
-    if (warp == 1) {
-        if (!acc_ok) ptx::mbar_wait_bounded(acc_bar, 0, args.wait_limit_ns);
-        ptx::tc_fence_after_sync();
-        ptx::tmem_dealloc(tmem, Sh::kTmemCols);
-    }
-    if (!ptx::mbar_wait_bounded(recv_bar, 0, args.wait_limit_ns) && tid == 0) atomicOr(&g_device_status, 16u);
-    if (Q > 1) ptx::cluster_arrive_relaxed();  // everything bound for this CTA has landed
-
-    // ---- epilogue 2: sums of each owned piece over the cluster's ranks.
-    // Eight warps do this part, so it is bound by latency, not bandwidth: the
-    // shared-memory base of every rank's contribution is computed once, and
-    // each thread loads both of its pieces (2 x Q float4) before it adds and
-    // stores.
-    const int row0 = m_tile * kTileM, col0 = n_tile * BN;
-    const size_t MN = static_cast<size_t>(args.M) * args.N;
-    const int rows_here = args.M - row0;                               // tile rows below M
-    const size_t tile0 = static_cast<size_t>(row0) * args.N + col0;   // the tile's first element
-    uint32_t rbase[Q];   // plus a piece's staging offset: that rank's contribution to the piece
-#pragma unroll
-    for (int r = 0; r < Q; ++r)
-        rbase[r] = r == rank ? E
-                             : recv + static_cast<uint32_t>(r - (r > rank ? 1 : 0)) * static_cast<uint32_t>(share) * 16u -
-                                   static_cast<uint32_t>(my_lo) * 16u;
-    auto gather = [&](const Piece &p, float4 (&v)[Q]) {
-#pragma unroll
-        for (int r = 0; r < Q; ++r) v[r] = ptx::ld_shared_v4(rbase[r] + p.off);
-    };
-    auto tile_elem = [&](const Piece &p) { return tile0 + static_cast<size_t>(p.row) * args.N + p.col; };
-    // the chunk sum of one split (Q == C): chunks in order 0, 1, 2, ...
-    auto chunk_sum = [&](const float4 (&v)[Q]) {
-        float4 acc = v[0];
-#pragma unroll
-        for (int r = 1; r < Q; ++r) add4(acc, v[r]);
-        return acc;
-    };
-    if (args.split_sum != 2) {
-        float *const Ps = args.P + static_cast<size_t>(s) * MN;
-        for (int g0 = my_lo + tid; g0 < my_hi; g0 += 2 * kThreads) {
-            const int g1 = g0 + kThreads;
-            const Piece p0 = piece_at(g0), p1 = piece_at(min(g1, my_hi - 1));
-            float4 v0[Q], v1[Q];
-            gather(p0, v0);
-            gather(p1, v1);
-            const float4 a0 = chunk_sum(v0), a1 = chunk_sum(v1);
-            if (p0.row < rows_here) *reinterpret_cast<float4 *>(Ps + tile_elem(p0)) = a0;
-            if (g1 < my_hi && p1.row < rows_here) *reinterpret_cast<float4 *>(Ps + tile_elem(p1)) = a1;
-        }
-    } else if (args.P != nullptr) {
-        cluster_split_sum_for<Q, true>(C, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, args.P, args.out);
-    } else {
-        cluster_split_sum_for<Q, false>(C, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, nullptr, args.out);
-    }
-
-    // ---- split sum by counters: the last split to finish this piece range
-    // adds all splits (Q == C here)
-    if (args.split_sum == 1) {
-        // the CTA's partials are all written (the barrier); thread 0's arrival
-        // count publishes them (release, cumulative over what the barrier
-        // ordered before it) and, for the last arriver, acquires the other
-        // splits' partials, which the second barrier passes on to all threads
+        ptx::tc_fence_before_sync();
         __syncthreads();
-        if (tid == 0) {
-            const unsigned idx = (static_cast<unsigned>(m_tile) * (args.N / BN) + n_tile) * C + c;   // c == rank
-            const unsigned old = ptx::atom_inc_acq_rel_gpu(&args.counters[idx], static_cast<unsigned>(args.S - 1));
-            last_s = old == static_cast<unsigned>(args.S - 1) ? 1u : 0u;
+        if (warp == 1 && h == kHalves - 1) {
+            if (!acc_ok) ptx::mbar_wait_bounded(acc_bar, 0, args.wait_limit_ns);
+            ptx::tc_fence_after_sync();
+            ptx::tmem_dealloc(tmem, Sh::kTmemCols);
         }
-        __syncthreads();
-        if (last_s) {
-            // kPieceBatch pieces per thread, the loads of kSplitBatch splits
-            // in flight at once (one L2 round trip per kSplitBatch splits,
-            // not per split); the adds still run in split order 0..S-1.  With
-            // one CTA per split (Q == 1) it owns the whole tile and walks only
-            // the pieces of rows below M (a quarter of them when M is 32).
-            const int rows_here = Q == 1 ? min(kTileM, args.M - row0) : kTileM;
-            const int walk_hi = Q == 1 ? rows_here * (BN / 4) : my_hi;
-            auto owned = [&](int t) {           // t-th owned piece, as a piece index
-                if (Q > 1) return t;
-                const int r = t / (BN / 4), cq = t % (BN / 4);
-                return (((cq >> 3) << 2) | (r >> 5)) << 8 | (r & 31) << 3 | (cq & 7);
-            };
-            for (int g0 = (Q == 1 ? 0 : my_lo) + tid; g0 < walk_hi; g0 += kPieceBatch * kThreads) {
-                float4 tot[kPieceBatch];
-                for (int sp0 = 0; sp0 < args.S; sp0 += kSplitBatch) {
-                    float4 v[kSplitBatch][kPieceBatch];
+        if (!ptx::mbar_wait_bounded(recv_bar, 0, args.wait_limit_ns) && tid == 0) atomicOr(&g_device_status, 16u);
+        if (Q > 1) ptx::cluster_arrive_relaxed();  // everything bound for this CTA has landed
+
+        // ---- epilogue 2: sums of each owned piece over the cluster's ranks.
+        // Eight warps do this part, so it is bound by latency, not bandwidth: the
+        // shared-memory base of every rank's contribution is computed once, and
+        // each thread loads both of its pieces (2 x Q float4) before it adds and
+        // stores.
+        const int row0 = m_tile * TM + h * kTileM, col0 = n_tile * BN;
+        const size_t MN = static_cast<size_t>(args.M) * args.N;
+        const int rows_here = args.M - row0;                               // tile rows below M
+        const size_t tile0 = static_cast<size_t>(row0) * args.N + col0;   // the tile's first element
+        uint32_t rbase[Q];   // plus a piece's staging offset: that rank's contribution to the piece
+        const uint32_t slot_bytes = static_cast<uint32_t>(share) * 16u;
 #pragma unroll
-                    for (int j = 0; j < kSplitBatch; ++j) {
+        for (int r = 0; r < Q; ++r)
+            rbase[r] = r == rank ? E
+                                 : recv + static_cast<uint32_t>(r - (r > rank ? 1 : 0)) * slot_bytes -
+                                       static_cast<uint32_t>(my_lo) * 16u;
+        auto gather = [&](const Piece &p, float4 (&v)[Q]) {
 #pragma unroll
-                        for (int i = 0; i < kPieceBatch; ++i) {
-                            const int t = g0 + i * kThreads, sp = sp0 + j;
-                            v[j][i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (t < walk_hi && sp < args.S) {
-                                const Piece p = piece_at(owned(t));
-                                const int row = row0 + p.row;
-                                if (sp == s) {
-                                    float4 w[Q];
-                                    gather(p, w);
-                                    v[j][i] = chunk_sum(w);
-                                } else if (row < args.M) {
-                                    v[j][i] = __ldcg(reinterpret_cast<const float4 *>(
-                                        args.P + sp * MN + static_cast<size_t>(row) * args.N + col0 + p.col));
+            for (int r = 0; r < Q; ++r) v[r] = ptx::ld_shared_v4(rbase[r] + p.off);
+        };
+        auto tile_elem = [&](const Piece &p) { return tile0 + static_cast<size_t>(p.row) * args.N + p.col; };
+        // the chunk sum of one split (Q == C): chunks in order 0, 1, 2, ...
+        auto chunk_sum = [&](const float4 (&v)[Q]) {
+            float4 acc = v[0];
+#pragma unroll
+            for (int r = 1; r < Q; ++r) add4(acc, v[r]);
+            return acc;
+        };
+        if (args.split_sum != 2) {
+            float *const Ps = args.P + static_cast<size_t>(s) * MN;
+            for (int g0 = my_lo + tid; g0 < my_hi; g0 += 2 * kThreads) {
+                const int g1 = g0 + kThreads;
+                const Piece p0 = piece_at(g0), p1 = piece_at(min(g1, my_hi - 1));
+                float4 v0[Q], v1[Q];
+                gather(p0, v0);
+                gather(p1, v1);
+                const float4 a0 = chunk_sum(v0), a1 = chunk_sum(v1);
+                if (p0.row < rows_here) *reinterpret_cast<float4 *>(Ps + tile_elem(p0)) = a0;
+                if (g1 < my_hi && p1.row < rows_here) *reinterpret_cast<float4 *>(Ps + tile_elem(p1)) = a1;
+            }
+        } else if (args.P != nullptr) {
+            cluster_split_sum_for<Q, true>(C, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, args.P,
+                                           args.out);
+        } else {
+            cluster_split_sum_for<Q, false>(C, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, nullptr,
+                                            args.out);
+        }
+
+        // ---- split sum by counters: the last split to finish this piece range
+        // adds all splits (Q == C here)
+        if (args.split_sum == 1) {
+            // the CTA's partials are all written (the barrier); thread 0's arrival
+            // count publishes them (release, cumulative over what the barrier
+            // ordered before it) and, for the last arriver, acquires the other
+            // splits' partials, which the second barrier passes on to all threads
+            __syncthreads();
+            if (tid == 0) {
+                const unsigned idx = (static_cast<unsigned>(m_tile) * (args.N / BN) + n_tile) * C + c;   // c == rank
+                const unsigned old = ptx::atom_inc_acq_rel_gpu(&args.counters[idx], static_cast<unsigned>(args.S - 1));
+                last_s = old == static_cast<unsigned>(args.S - 1) ? 1u : 0u;
+            }
+            __syncthreads();
+            if (last_s) {
+                // kPieceBatch pieces per thread, the loads of kSplitBatch splits
+                // in flight at once (one L2 round trip per kSplitBatch splits,
+                // not per split); the adds still run in split order 0..S-1.  With
+                // one CTA per split (Q == 1) it owns the whole tile and walks only
+                // the pieces of rows below M (a quarter of them when M is 32).
+                const int rows_here = Q == 1 ? min(kTileM, args.M - row0) : kTileM;
+                const int walk_hi = Q == 1 ? rows_here * (BN / 4) : my_hi;
+                auto owned = [&](int t) {           // t-th owned piece, as a piece index
+                    if (Q > 1) return t;
+                    const int r = t / (BN / 4), cq = t % (BN / 4);
+                    return (((cq >> 3) << 2) | (r >> 5)) << 8 | (r & 31) << 3 | (cq & 7);
+                };
+                for (int g0 = (Q == 1 ? 0 : my_lo) + tid; g0 < walk_hi; g0 += kPieceBatch * kThreads) {
+                    float4 tot[kPieceBatch];
+                    for (int sp0 = 0; sp0 < args.S; sp0 += kSplitBatch) {
+                        float4 v[kSplitBatch][kPieceBatch];
+#pragma unroll
+                        for (int j = 0; j < kSplitBatch; ++j) {
+#pragma unroll
+                            for (int i = 0; i < kPieceBatch; ++i) {
+                                const int t = g0 + i * kThreads, sp = sp0 + j;
+                                v[j][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                if (t < walk_hi && sp < args.S) {
+                                    const Piece p = piece_at(owned(t));
+                                    const int row = row0 + p.row;
+                                    if (sp == s) {
+                                        float4 w[Q];
+                                        gather(p, w);
+                                        v[j][i] = chunk_sum(w);
+                                    } else if (row < args.M) {
+                                        v[j][i] = __ldcg(reinterpret_cast<const float4 *>(
+                                            args.P + sp * MN + static_cast<size_t>(row) * args.N + col0 + p.col));
+                                    }
                                 }
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < kSplitBatch; ++j) {
+#pragma unroll
+                            for (int i = 0; i < kPieceBatch; ++i) {
+                                if (sp0 + j == 0)
+                                    tot[i] = v[j][i];
+                                else if (sp0 + j < args.S)
+                                    add4(tot[i], v[j][i]);
                             }
                         }
                     }
 #pragma unroll
-                    for (int j = 0; j < kSplitBatch; ++j) {
-#pragma unroll
-                        for (int i = 0; i < kPieceBatch; ++i) {
-                            if (sp0 + j == 0)
-                                tot[i] = v[j][i];
-                            else if (sp0 + j < args.S)
-                                add4(tot[i], v[j][i]);
+                    for (int i = 0; i < kPieceBatch; ++i) {
+                        const int t = g0 + i * kThreads;
+                        if (t < walk_hi) {
+                            const Piece p = piece_at(owned(t));
+                            const int row = row0 + p.row;
+                            if (row < args.M)
+                                *reinterpret_cast<float4 *>(args.out + static_cast<size_t>(row) * args.N + col0 +
+                                                            p.col) = tot[i];
                         }
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < kPieceBatch; ++i) {
-                    const int t = g0 + i * kThreads;
-                    if (t < walk_hi) {
-                        const Piece p = piece_at(owned(t));
-                        const int row = row0 + p.row;
-                        if (row < args.M)
-                            *reinterpret_cast<float4 *>(args.out + static_cast<size_t>(row) * args.N + col0 +
-                                                        p.col) = tot[i];
                     }
                 }
             }
@@ -809,11 +828,11 @@ bool encode_operand_3d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t 
 
 int g_override_bn = 0, g_override_chunks = 0, g_override_kbs = 0;
 
-// One k-block is one 128-byte row of every operand row; a 3xTF32 stage holds
-// the lo parts too.
-size_t stage_bytes(int bn, int kbs, bool x3 = false)
+// One k-block is one 128-byte row of every operand row (tm rows of A, bn of
+// B); a 3xTF32 stage holds the lo parts too.
+size_t stage_bytes(int bn, int kbs, bool x3 = false, int tm = kTileM)
 {
-    return static_cast<size_t>(kTileM + bn) * 128 * kbs * (x3 ? 2 : 1);
+    return static_cast<size_t>(tm + bn) * 128 * kbs * (x3 ? 2 : 1);
 }
 size_t epi_bytes(int bn) { return static_cast<size_t>(kTileM) * bn * 4; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -821,16 +840,16 @@ constexpr size_t kSmemLimit = 226 * 1024;   // dynamic; leaves room for static s
 
 // Dynamic shared memory of a plan: the stage ring (or the accumulator
 // staging, if larger), one receive slot per peer, and 1 KB of alignment slack.
-size_t smem_for(int bn, int kbs, int stages, int chunks, int share, bool x3 = false)
+size_t smem_for(int bn, int kbs, int stages, int chunks, int share, bool x3 = false, int tm = kTileM)
 {
-    const size_t region0 = round_up(std::max(stages * stage_bytes(bn, kbs, x3), epi_bytes(bn)), 1024);
+    const size_t region0 = round_up(std::max(stages * stage_bytes(bn, kbs, x3, tm), epi_bytes(bn)), 1024);
     return region0 + static_cast<size_t>(chunks - 1) * share * 16 + 1024;
 }
 
 // Opts the kernel into the device's full dynamic shared memory (what is left
 // of the per-block opt-in limit after its static shared memory); once per
 // device.
-template <int BN, int Q, bool KN, bool X3>
+template <int BN, int Q, bool KN, bool X3, int TM>
 cudaError_t prepare_kernel_attrs()
 {
     static std::mutex mu;
@@ -844,20 +863,20 @@ cudaError_t prepare_kernel_attrs()
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return note_error(e, "cudaDeviceGetAttribute(MaxSharedMemoryPerBlockOptin)");
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, tc_splitk_kernel<BN, Q, KN, X3>);
+    e = cudaFuncGetAttributes(&fa, tc_splitk_kernel<BN, Q, KN, X3, TM>);
     if (e != cudaSuccess) return note_error(e, "cudaFuncGetAttributes(tc_splitk_kernel)");
     const int dyn = optin - static_cast<int>(fa.sharedSizeBytes);
-    e = cudaFuncSetAttribute(tc_splitk_kernel<BN, Q, KN, X3>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    e = cudaFuncSetAttribute(tc_splitk_kernel<BN, Q, KN, X3, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
     if (e != cudaSuccess) return note_error(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
     if (dev >= 0 && dev < 64) done[dev] = true;
     return cudaSuccess;
 }
 
-template <int BN, int Q, bool KN, bool X3>
+template <int BN, int Q, bool KN, bool X3, int TM = kTileM>
 cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args, const TilePlan &plan,
                       cudaStream_t stream)
 {
-    cudaError_t e = prepare_kernel_attrs<BN, Q, KN, X3>();
+    cudaError_t e = prepare_kernel_attrs<BN, Q, KN, X3, TM>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = plan.grid;
@@ -878,7 +897,7 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
-    return note_error(cudaLaunchKernelEx(&cfg, tc_splitk_kernel<BN, Q, KN, X3>, ta, tb, args),
+    return note_error(cudaLaunchKernelEx(&cfg, tc_splitk_kernel<BN, Q, KN, X3, TM>, ta, tb, args),
                       "cudaLaunchKernelEx(tc_splitk_kernel)");
 }
 
@@ -926,7 +945,7 @@ struct StageChoice {
 
 // The largest stage (k-blocks per box) that keeps a chunk's loads double-
 // buffered, or all in flight, within shared memory, for a cluster of q.
-StageChoice pick_stages(int bn, int nkb, bool can3d, int q, int share, bool x3 = false)
+StageChoice pick_stages(int bn, int nkb, bool can3d, int q, int share, bool x3 = false, int tm = kTileM)
 {
     StageChoice r;
     for (int cand : {kMaxKbs, 2, 1}) {
@@ -934,8 +953,8 @@ StageChoice pick_stages(int bn, int nkb, bool can3d, int q, int share, bool x3 =
         if (g_override_kbs && cand != std::min(g_override_kbs, can3d ? kMaxKbs : 1)) continue;
         const int want = (nkb + cand - 1) / cand;
         int st = std::min(want, kMaxStages);
-        while (st > 1 && smem_for(bn, cand, st, q, share, x3) > kSmemLimit) --st;
-        if (smem_for(bn, cand, st, q, share, x3) > kSmemLimit) continue;
+        while (st > 1 && smem_for(bn, cand, st, q, share, x3, tm) > kSmemLimit) --st;
+        if (smem_for(bn, cand, st, q, share, x3, tm) > kSmemLimit) continue;
         if (st < std::min(want, 2) && !g_override_kbs) continue;
         r.kbs = std::min(cand, std::max(nkb, 1));
         r.stages = st;
@@ -1094,8 +1113,24 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
         }
     }
     const int share = share_for(bn, q);
-    const StageChoice sc = pick_stages(bn, nkb, can3d, q, share, x3);
+    // 256-row tiles (two accumulators sharing each B operand) load 64 KB per
+    // k-block for twice the products of a 128-row tile's 48 KB.  A launch of
+    // many tiles is bound by the rate at which each SM takes in its loads, so
+    // a 256-row tile takes ~1.36x as long as a 128-row one (measured on
+    // GB300) and wins where halving the tile count saves more than that in
+    // waves of 148 CTAs.  Only for one CTA per tile that keeps or sums its
+    // own partials, with BN = 256 and 16-bit operands.
+    int tm = kTileM;
+    if (!x3 && bn == 256 && q == 1 && split_sum != 1 && mt > 1) {
+        const int64_t per_row_tile = (N / bn) * S;
+        const double waves1 = std::ceil(static_cast<double>(mt * per_row_tile) / resident_clusters(1));
+        const double waves2 = std::ceil(static_cast<double>((mt + 1) / 2 * per_row_tile) / resident_clusters(1));
+        if (waves1 > 1.0 && waves2 * 1.36 < waves1 && pick_stages(bn, nkb, can3d, 1, share, x3, 2 * kTileM).ok)
+            tm = 2 * kTileM;
+    }
+    const StageChoice sc = pick_stages(bn, nkb, can3d, q, share, x3, tm);
     TilePlan p = {};
+    p.tile_m = tm;
     p.bn = bn;
     p.chunks = chunks;
     p.chunk_len = static_cast<int>(chunk_len);
@@ -1108,7 +1143,7 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     p.share = share;
     p.x3 = x3 ? 1 : 0;
     p.region0 =
-        static_cast<uint32_t>(round_up(std::max(p.stages * stage_bytes(bn, p.kbs, x3), epi_bytes(bn)), 1024));
+        static_cast<uint32_t>(round_up(std::max(p.stages * stage_bytes(bn, p.kbs, x3, tm), epi_bytes(bn)), 1024));
     // CTAs are dispatched x first.  With x over the column tiles, each wave of
     // a launch of more than one wave sweeps B's whole split slab.  Once that
     // slab is more than a quarter of L2 it no longer stays there from wave to
@@ -1117,18 +1152,23 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     // On a GB300, M4096 N8192 K4096 (B slab 64 MB) went from 243.7 to 236.4 us
     // fused, while shapes whose slabs both fit (16 MB and less) ran 2-7%
     // slower in row order.
-    const int64_t ctas = mt * (N / bn) * S * chunks;
+    const int64_t row_tiles = (M + tm - 1) / tm;
+    const int64_t ctas = row_tiles * (N / bn) * S * chunks;
     const int64_t clusters = ctas / q;
     const int64_t b_slab = N * kps * (x3 ? 4 : 2);
     p.rows_first = clusters > resident_clusters(q) && mt * kTileM < N && b_slab > (int64_t(32) << 20) &&
                            N / bn <= 65535 ? 1 : 0;
-    p.grid = p.rows_first ? dim3(static_cast<unsigned>(mt), static_cast<unsigned>(N / bn), static_cast<unsigned>(S * chunks))
-                          : dim3(static_cast<unsigned>(N / bn), static_cast<unsigned>(mt), static_cast<unsigned>(S * chunks));
+    const unsigned gx = static_cast<unsigned>(N / bn), gy = static_cast<unsigned>(row_tiles);
+    const unsigned gz = static_cast<unsigned>(S * chunks);
+    p.grid = p.rows_first ? dim3(gy, gx, gz) : dim3(gx, gy, gz);
     // CTAs of the next launch that fit beside this one (whole clusters): they
     // start early under programmatic dependent launch and do the prefetch
     const int64_t spare = std::max<int64_t>(0, static_cast<int64_t>(resident_clusters(q)) - clusters) * q;
     p.prefetchers = static_cast<int>(std::min(spare, ctas));
-    p.smem_bytes = smem_for(bn, p.kbs, p.stages, q, share, x3);
+    // A 256-row tile's CTA takes all the shared memory a block may have, so
+    // that no other CTA of these kernels shares its SM: its two accumulators
+    // fill the SM's 512 tensor-memory columns.
+    p.smem_bytes = tm == 2 * kTileM ? kSmemLimit : smem_for(bn, p.kbs, p.stages, q, share, x3, tm);
     return p;
 }
 
@@ -1147,11 +1187,14 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
         return note_error(cudaErrorInvalidValue, "partials are needed unless the cluster sums the splits");
     if (pr.f32 && (pr.b_kn || !plan.x3))
         return note_error(cudaErrorInvalidValue, "F32 operands need a 3xTF32 plan and the [N,K] weight");
+    const bool tile_m_ok = plan.tile_m == kTileM || (plan.tile_m == 2 * kTileM && plan.bn == 256 &&
+                                                     plan.cluster == 1 && plan.split_sum != 1 && !plan.x3);
+    if (!tile_m_ok) return note_error(cudaErrorInvalidConfiguration, "256-row tile plan out of range");
     CUtensorMap ta, tb;
     const int et = pr.f32 ? 2 : pr.bf16 ? 1 : 0;
     const int kbs = plan.three_d ? plan.kbs : 1;
-    const bool ok_a = plan.three_d ? encode_operand_3d(&ta, pr.A, pr.M, pr.K, kTileM, plan.kbs, et)
-                                   : encode_operand(&ta, pr.A, pr.M, pr.K, kTileM, et);
+    const bool ok_a = plan.three_d ? encode_operand_3d(&ta, pr.A, pr.M, pr.K, plan.tile_m, plan.kbs, et)
+                                   : encode_operand(&ta, pr.A, pr.M, pr.K, plan.tile_m, et);
     // the [K,N] weight is a row-major matrix of K rows of N: boxes of 64
     // columns by kbs*64 rows
     const bool ok_b = pr.b_kn ? encode_operand(&tb, pr.B, pr.K, pr.N, kbs * kBlockK, et)
@@ -1186,6 +1229,9 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
     a.rows_first = plan.rows_first;
     // operand variants: [N,K] weight, [K,N] weight, F32 as 3xTF32
     const int variant = pr.f32 ? 2 : pr.b_kn ? 1 : 0;
+    if (plan.tile_m == 2 * kTileM)
+        return variant == 1 ? launch_bn<256, 1, true, false, 2 * kTileM>(ta, tb, a, plan, stream)
+                            : launch_bn<256, 1, false, false, 2 * kTileM>(ta, tb, a, plan, stream);
     switch (plan.bn * 4 + variant) {
     case 64 * 4 + 0: return launch_cluster<64, false, false>(ta, tb, a, plan, stream);
     case 64 * 4 + 1: return launch_cluster<64, true, false>(ta, tb, a, plan, stream);

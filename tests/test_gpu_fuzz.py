@@ -81,7 +81,10 @@ def test_random_geometry(lib, orc, case):
 
 LARGE = [(2048, 4096, 8192, 4, 2048, "bf16"), (1056, 2112, 5120, 5, 1024, "f16"),
          (4096, 8192, 4096, 1, 4096, "bf16"), (1024, 2048, 8192, 2, 4096, "f32"),
-         (2048, 8192, 8192, 2, 4096, "bf16"), (2048, 4096, 4096, 1, 4096, "f32")]
+         (2048, 8192, 8192, 2, 4096, "bf16"), (2048, 4096, 4096, 1, 4096, "f32"),
+         # 256-row tiles whose last tile is ragged: the second half empty (M = 3872),
+         # or partly below M (M = 4000)
+         (3872, 8192, 2048, 1, 2048, "bf16"), (4000, 8192, 2048, 1, 2048, "f16")]
 
 
 def check_sampled(orc, ops, dt, M, N, S, kps, P, out, npts=600):

@@ -14,7 +14,8 @@ tests, and every tile override:
   per-block limit;
 - the grid covers every tile once, with the row tiles along x exactly when
   the launch is more than one wave, B's slab is over 32 MB and A's is the
-  smaller;
+  smaller; 256-row tiles only where the planner's rule allows them, and
+  then with the whole shared memory of a block;
 - a rank's share of the tile is a whole number of 32 x 32 boxes (each warp
   pushes whole boxes), every 16-byte piece has exactly one owner, and every
   contribution sent to or read from a receive slot stays inside that slot.
@@ -56,17 +57,29 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
     x3 = dt == "f32"
     kb_elems, elem = (32, 4) if x3 else (64, 2)
     BN, C, CL, stages = d["bn"], d["chunks"], d["chunk_len"], d["stages"]
-    Q, KBS, T3, SS = d["cluster"], d["kblocks_per_stage"], d["three_d"], d["split_sum"]
+    Q, KBS, T3, SS, TM = d["cluster"], d["kblocks_per_stage"], d["three_d"], d["split_sum"], d["tile_m"]
     assert d["path"] == (2 if x3 else 0)
     assert C in (1, 2, 4, 8) and Q in (1, 2, 4, 8) and 1 <= stages <= 8 and 1 <= KBS <= 4
     assert Q == C or (SS == 2 and Q == S * C)
     mt = -(-M // TILE_M)
-    tiles_xy = (mt, N // BN) if d["rows_first"] else (N // BN, mt)
+    # 256-row tiles: BN 256, one CTA per tile keeping or summing its own
+    # partials, 16-bit operands, and fewer waves of 148 CTAs even at 1.36x
+    # the time per tile
+    assert TM in (TILE_M, 2 * TILE_M)
+    per_row_tile = (N // BN) * S
+    waves1 = -(-mt * per_row_tile // 148)
+    waves2 = -(-(-(-mt // 2)) * per_row_tile // 148)
+    wins = not x3 and BN == 256 and Q == 1 and SS != 1 and mt > 1 and waves1 > 1 and waves2 * 1.36 < waves1
+    if TM == 2 * TILE_M:
+        assert wins
+    elif not kbs:
+        assert not wins
+    tiles_xy = (-(-M // TM), N // BN) if d["rows_first"] else (N // BN, -(-M // TM))
     assert (d["grid_x"], d["grid_y"], d["grid_z"]) == (*tiles_xy, S * C)
     assert d["grid_y"] <= 65535
     # row tiles first only for launches of more than one wave whose B slab
     # (one split of B) outgrows a quarter of L2, with A's slab the smaller
-    waves = mt * (N // BN) * S * C // Q > RESIDENT_CLUSTERS[Q]
+    waves = -(-M // TM) * (N // BN) * S * C // Q > RESIDENT_CLUSTERS[Q]
     b_slab = N * kps * (4 if x3 else 2)
     assert d["rows_first"] == int(waves and mt * TILE_M < N and b_slab > 32 << 20 and N // BN <= 65535)
     assert N % BN == 0 and d["grid_z"] % Q == 0
@@ -78,10 +91,13 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
     # shared memory: the ring (or the accumulator staging) + receive slots + slack
     pieces = 32 * BN
     share = -(-(-(-pieces // Q)) // 8) * 8
-    stage_bytes = (TILE_M + BN) * 128 * KBS * (2 if x3 else 1)
+    stage_bytes = (TM + BN) * 128 * KBS * (2 if x3 else 1)
     epi_bytes = TILE_M * BN * 4
     region0 = -(-max(stages * stage_bytes, epi_bytes) // 1024) * 1024
-    assert d["smem_bytes"] == region0 + (Q - 1) * share * 16 + 1024 <= SMEM_LIMIT
+    if TM == TILE_M:
+        assert d["smem_bytes"] == region0 + (Q - 1) * share * 16 + 1024 <= SMEM_LIMIT
+    else:   # the whole per-block limit: no other CTA shares the SM's tensor memory
+        assert region0 + 1024 <= d["smem_bytes"] == SMEM_LIMIT
 
     # K coverage: every k of every split loaded exactly once, boxes aligned
     for s in range(S):
