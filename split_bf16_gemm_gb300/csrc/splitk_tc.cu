@@ -8,8 +8,9 @@
 // "Launch contract and correctness").  Optionally the same launch also sums
 // the splits into out[m,n] (the pages' separate accumulation pass, fused).
 //
-// One CTA (256 threads, 8 warps) owns a 128 x BN output tile of one K-chunk:
-//   thread 0       TMA producer: per stage, kbs 64-wide k-blocks of A (128
+// One CTA (256 threads, 8 warps) owns a TM x BN output tile of one K-chunk
+// (TM = 128, or 256 as below):
+//   thread 0       TMA producer: per stage, kbs 64-wide k-blocks of A (TM
 //                  rows) and of B (BN rows), 128-byte swizzled, into a ring
 //                  of `stages` buffers; the first stages go out before tensor
 //                  memory is allocated;
@@ -25,6 +26,13 @@
 // B is either the prepared [N,K] weight (K-major operand) or, with KN, the
 // [K,N] weight itself (MN-major operand: boxes of 64 columns by the stage's
 // k-rows); both give the same products in the same order.
+// 256-row tiles (BN = 256, one CTA per tile, 16-bit operands): each K step is
+// two MMAs, rows 0-127 and 128-255 of the stage's A, into two accumulators
+// (all 512 tensor-memory columns) with the same B descriptor, and the
+// epilogue runs once per 128-row half.  That loads a third fewer bytes per
+// product, and launches of many tiles are bound by each SM's TMA intake.
+// The grid walks the column tiles first, or the row tiles first where every
+// wave would otherwise sweep a B slab too large to stay in L2.
 // The CTAs that share a tile (the chunks of a split, or every split and chunk
 // of the tile when the launch sums the splits) form one thread-block cluster.
 // Each cluster rank owns 1/Q of the tile; each warp pushes the boxes it staged
