@@ -99,6 +99,18 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
     else:   # the whole per-block limit: no other CTA shares the SM's tensor memory
         assert region0 + 1024 <= d["smem_bytes"] == SMEM_LIMIT
 
+    # 256-row tiles: each k-block of A is 256 rows of 128 bytes; the second
+    # accumulator's MMAs read rows 128-255 (16 KB in, 1 KB-aligned for the
+    # swizzle), inside that k-block; the two accumulators (BN columns each)
+    # fill the 512 tensor-memory columns; each half is staged in turn through
+    # the same 128 x BN staging area
+    if TM == 2 * TILE_M:
+        a_kblock = TM * 128
+        assert BN == 256 and Q == 1 and not x3 and SS != 1
+        assert 16384 % 1024 == 0 and 16384 + TILE_M * 128 <= a_kblock
+        assert 2 * BN <= 512
+        assert epi_bytes <= region0 and stages * (a_kblock + BN * 128) * KBS <= region0
+
     # K coverage: every k of every split loaded exactly once, boxes aligned
     for s in range(S):
         ks, ke = s * kps, min(s * kps + kps, K)
