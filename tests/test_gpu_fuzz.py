@@ -129,6 +129,13 @@ def test_large_shape_sampled(lib, orc, case):
     assert sk.splitk_get_device_status() == 0
     assert P.guards_intact() and out.guards_intact() and ws.guards_intact()
     assert torch.equal(fused.view(torch.int32), out.data.view(torch.int32))
+    del fused
+    kept = torch.empty(M * N, dtype=torch.float32, device="cuda")
+    sk.gemm_bt(A, B, kept, ws.data, nbytes, M, N, K, S, kps, dt, fused=3)   # the partials kept too
+    assert sk.splitk_get_device_status() == 0 and ws.guards_intact()
+    assert torch.equal(kept.view(torch.int32), out.data.view(torch.int32))
+    assert torch.equal(ws.data[: S * M * N].view(torch.int32), P.data.view(torch.int32))
+    del kept
     assert bool(torch.isfinite(out.data).all()) and bool(torch.isfinite(P.data).all())
     check_sampled(orc, ops, dt, M, N, S, kps, P.data, out.data)
 
