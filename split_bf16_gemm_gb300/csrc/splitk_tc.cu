@@ -1124,10 +1124,11 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     // 256-row tiles (two accumulators sharing each B operand) load 64 KB per
     // k-block for twice the products of a 128-row tile's 48 KB.  A launch of
     // many tiles is bound by the rate at which each SM takes in its loads, so
-    // a 256-row tile takes ~1.36x as long as a 128-row one (measured on
-    // GB300) and wins where halving the tile count saves more than that in
-    // waves of 148 CTAs.  Only for one CTA per tile that keeps or sums its
-    // own partials, with BN = 256 and 16-bit operands.
+    // a 256-row tile takes ~1.36x as long as a 128-row one (the load bytes'
+    // ratio; per wave, GB300 measured 1.37-1.44) and wins where halving the
+    // tile count saves more than that in waves of 148 CTAs.  Only for one
+    // CTA per tile that keeps or sums its own partials, with BN = 256 and
+    // 16-bit operands.
     int tm = kTileM;
     if (!x3 && bn == 256 && q == 1 && split_sum != 1 && mt > 1) {
         const int64_t per_row_tile = (N / bn) * S;
