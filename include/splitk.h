@@ -44,6 +44,23 @@
  * that runs out sets a device status word, which splitk_get_device_status()
  * reads.  The three compute entry points (gemm_splitk_bt, splitk_reduce,
  * gemm_bt) may be captured into a CUDA graph.
+ *
+ * Consecutive launches inside a graph: every launch is a programmatic
+ * dependent of the one before it on its stream.  Eagerly, each launch waits
+ * for the previous grid to finish before it reads its operands.  While a
+ * stream is being captured, the library sees what the next launch depends on
+ * (cudaStreamGetCaptureInfo); when that is exactly its own previous launch on
+ * the stream, and the new launch reads (A and B; the partials, for the
+ * reduce) no byte that any of its launches still able to run writes, the new
+ * launch starts loading and multiplying at once and waits for the previous
+ * grid only before its first store ("overlap").  Its results are bitwise
+ * those of the same launch without overlap.  Launches that read what an
+ * earlier one writes (a chain of GEMMs, the reduce after the partial pass),
+ * launches after another kernel or a copy, and launches outside a capture
+ * wait as usual.  The decision is made at capture time from the pointers
+ * passed; a graph whose nodes are later given other buffers
+ * (cudaGraphExecKernelNodeSetParams) must keep the same pattern of overlaps
+ * between them.  splitk_set_overlap(0) turns this off for later captures.
  */
 #ifndef SPLITK_H
 #define SPLITK_H
@@ -93,10 +110,12 @@ int splitk_check_geometry(int64_t M, int64_t N, int64_t K, int64_t splits,
  *   partials  device, [splits,M,N] row-major F32; fully overwritten
  * BF16/F16 operands run on the tensor cores (tcgen05, F32 accumulate in tensor
  * memory, native operands).  F32 operands run on the tensor cores too, each
- * product as three TF32 products (x = hi + lo with hi the top 19 bits and
- * lo = x - hi; hi*lo + lo*hi + hi*hi; relative error per product about
- * 2^-21).  Each element is a sum in F32 whose order is fixed for a given
- * shape. */
+ * product as three TF32 products: x = hi + lo, where hi is the F32 operand as
+ * loaded, which the tensor cores read as TF32 by dropping its 13 low fraction
+ * bits (its top 19 bits; measured on GB300: truncation, not rounding), and
+ * lo = x - (x with those 13 bits cleared), exact in F32; hi*lo + lo*hi +
+ * hi*hi, relative error per product about 2^-21.  Each element is a sum in
+ * F32 whose order is fixed for a given shape. */
 int gemm_splitk_bt(const void *A, const void *B, float *partials, int64_t M,
                    int64_t N, int64_t K, int64_t splits, int64_t k_per_split,
                    int dtype, void *stream);
@@ -141,11 +160,14 @@ int gemm_bt_workspace_init(void *workspace, size_t workspace_bytes, void *stream
  *   fused      0: two kernels (gemm_splitk_bt, then splitk_reduce); the
  *                 workspace then holds the partials [splits,M,N] in its
  *                 first bytes;
- *              1: one kernel: the splits are summed inside the launch (in the
- *                 thread-block cluster when a tile's splits fit one cluster,
- *                 else by the last split to finish each piece, through
- *                 arrival counters in the workspace); the partials are not
- *                 kept;
+ *              1: one kernel where the tile plan holds all of a tile's
+ *                 splits in one resident thread-block cluster: the splits
+ *                 are summed inside the launch, over distributed shared
+ *                 memory, and the partials are not kept.  Where it cannot
+ *                 (too many splits for one cluster, or more tiles than
+ *                 resident clusters), the call runs the two kernels of 0,
+ *                 which measured faster there than summing through global
+ *                 memory (splitk_describe_launch reports which);
  *              3: as 1, and the workspace also holds the partials afterwards.
  *              Fused calls need the workspace zeroed once before the first
  *              of them (gemm_bt_workspace_init).
@@ -312,13 +334,14 @@ const char *splitk_status_string(int status);
  * SPLITK_OK or SPLITK_ERR_CONFIG. */
 int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
 
-/* Describes the launch gemm_bt would make, without launching: info[0..17] =
+/* Describes the launch gemm_bt would make, without launching: info[0..21] =
  * {path (0 tensor-core, 2 tensor-core 3xTF32 for F32), bn, chunks, chunk_len, stages,
  *  cluster_size (chunks, or splits * chunks), grid_x, grid_y, grid_z,
  *  dynamic_smem_bytes,
  *  fused_in_kernel (0/1), kernels_per_call, kblocks_per_stage,
- *  three_d_loads (0/1), split_sum (0 none, 1 by arrival counters in the
- *  workspace, 2 inside the thread-block cluster), prefetchers (fused calls
+ *  three_d_loads (0/1), split_sum (0 none, 2 inside the thread-block
+ *  cluster; a fused call whose splits do not fit one resident cluster
+ *  reports the two-kernel launch, fused_in_kernel 0), prefetchers (fused calls
  *  only: CTAs that fit beside a running launch and prefetch A and B into L2
  *  before the dependency wait), rows_first (1: grid x walks the 128-row tiles
  *  and grid y the column tiles, so grid_x and grid_y are swapped; chosen for
@@ -326,7 +349,13 @@ int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
  *  N * k_per_split elements, is over 32 MB), tile_m (rows of A per thread
  *  block: 128, or 256 for BN 256 plans with one block per tile, no cluster
  *  and no arrival counters, chosen when it saves waves; grid_x or grid_y
- *  then counts 256-row tiles)}; `info` must hold 18 ints.
+ *  then counts 256-row tiles),
+ *  compact (1: a fused call captured into a graph, when it starts beside the
+ *  launch before it or heads such a run, takes the compact layout: the same
+ *  tiles, chunks and sums, a stage ring cut so that two thread blocks fit on
+ *  an SM, the peers' shares received inside the ring),
+ *  compact_stages, compact_kblocks_per_stage, compact_dynamic_smem_bytes
+ *  (0 when compact is 0)}; `info` must hold 22 ints.
  * Returns a status as gemm_bt's validation would (pointers are not checked). */
 int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits,
                            int64_t k_per_split, int dtype, int fused,
@@ -337,6 +366,21 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits,
  * (clamped to [1e3, 1e9]), synchronises `stream`, and returns what
  * splitk_get_device_status() then reads (SPLITK_ERR_DEVICE_TIMEOUT expected). */
 int splitk_selftest_bounded_wait(int64_t limit_ns, void *stream);
+
+/* Turns the overlap of consecutive independent launches inside a graph
+ * capture (see the top of this header) on (1, the default) or off (0) for
+ * every later launch of the process.  Launches already captured keep what
+ * was decided for them.  Returns SPLITK_OK or SPLITK_ERR_CONFIG. */
+int splitk_set_overlap(int enable);
+
+/* What the calling host thread's most recent tensor-core launch did:
+ * info[0..7] = {overlap (it loaded before the previous grid finished),
+ * compact (its ring was cut so that two of its thread blocks fit on an SM,
+ * taken for such launches and for the first of a capture, when a
+ * one-wave plan allows it), capturing (the stream was being captured), bn,
+ * chunks, stages, kblocks_per_stage, dynamic_smem_bytes}.  Diagnostic;
+ * returns SPLITK_OK or SPLITK_ERR_NULL. */
+int splitk_last_launch(int *info);
 
 #ifdef __cplusplus
 }

@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     gemm_bt_noalloc, gemm_bt_workspace_bytes, gemm_bt_workspace_init, gemm_kn, gemm_splitk_kn, pointer_array,
     gemm_splitk_bt,
     lib, splitk_check_geometry, splitk_describe_launch, splitk_get_device_status, splitk_reduce,
-    splitk_autotune_splits, splitk_choose_splits, splitk_last_error, splitk_prepare_bt, splitk_selftest_bounded_wait, splitk_set_tile_override, splitk_status_string,
+    splitk_autotune_splits, splitk_choose_splits, splitk_last_error, splitk_last_launch, splitk_prepare_bt,
+    splitk_selftest_bounded_wait, splitk_set_overlap, splitk_set_tile_override, splitk_status_string,
     status_string,
 )

@@ -27,7 +27,7 @@ EXPORTS = (
     "splitk_describe_launch", "splitk_selftest_bounded_wait", "splitk_last_error",
     "gemm_bt_workspace_init", "gemm_bt_noalloc", "splitk_prepare_bt",
     "gemm_bt_host_staging_bytes", "gemm_bt_host_batch", "splitk_choose_splits", "splitk_autotune_splits",
-    "gemm_splitk_kn", "gemm_kn",
+    "gemm_splitk_kn", "gemm_kn", "splitk_set_overlap", "splitk_last_launch",
 )
 NOALLOC_MAX_BYTES = 32 << 20   # SPLITK_NOALLOC_MAX_BYTES
 
@@ -78,13 +78,16 @@ def lib() -> ctypes.CDLL:
             L.splitk_choose_splits.argtypes = [i64, i64, i64, i32, i32, vp, vp, vp]
             L.splitk_autotune_splits.argtypes = [vp, vp, vp, vp, sz, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp]
             L.splitk_last_error.argtypes = []
+            L.splitk_set_overlap.argtypes = [i32]
+            L.splitk_last_launch.argtypes = [vp]
             L.splitk_last_error.restype = ctypes.c_char_p
             for name in ("splitk_check_geometry", "gemm_splitk_bt", "splitk_reduce", "gemm_bt",
                          "gemm_splitk_kn", "gemm_kn",
                          "gemm_bt_workspace_init", "gemm_bt_noalloc", "splitk_prepare_bt",
                          "gemm_bt_host_batch", "splitk_choose_splits", "splitk_autotune_splits",
                          "splitk_get_device_status", "splitk_set_tile_override",
-                         "splitk_describe_launch", "splitk_selftest_bounded_wait"):
+                         "splitk_describe_launch", "splitk_selftest_bounded_wait", "splitk_set_overlap",
+                         "splitk_last_launch"):
                 getattr(L, name).restype = i32
             _lib = L
     return _lib
@@ -253,14 +256,29 @@ def splitk_set_tile_override(bn: int = 0, chunks: int = 0, kblocks_per_stage: in
 
 
 def splitk_describe_launch(M, N, K, splits, k_per_split, dtype, fused=0) -> dict:
-    info = (ctypes.c_int * 18)()
+    info = (ctypes.c_int * 22)()
     _check(lib().splitk_describe_launch(M, N, K, splits, k_per_split, dtype_code(dtype), fused,
                                         ctypes.addressof(info)), "splitk_describe_launch")
     keys = ("path", "bn", "chunks", "chunk_len", "stages", "cluster", "grid_x", "grid_y",
             "grid_z", "smem_bytes", "fused_in_kernel", "kernels_per_call", "kblocks_per_stage",
-            "three_d", "split_sum", "prefetchers", "rows_first", "tile_m")
+            "three_d", "split_sum", "prefetchers", "rows_first", "tile_m",
+            "compact", "compact_stages", "compact_kblocks_per_stage", "compact_smem_bytes")
     return dict(zip(keys, list(info)))
 
 
 def splitk_selftest_bounded_wait(limit_ns: int = 1_000_000, stream=None) -> int:
     return lib().splitk_selftest_bounded_wait(limit_ns, _stream(stream))
+
+
+def splitk_set_overlap(enable: bool) -> None:
+    """Overlap of consecutive independent launches inside graph captures: on
+    (the default) or off, for later captures of the whole process."""
+    _check(lib().splitk_set_overlap(1 if enable else 0), "splitk_set_overlap")
+
+
+def splitk_last_launch() -> dict:
+    """What the calling thread's most recent tensor-core launch did."""
+    info = (ctypes.c_int * 8)()
+    _check(lib().splitk_last_launch(ctypes.addressof(info)), "splitk_last_launch")
+    keys = ("overlap", "compact", "capturing", "bn", "chunks", "stages", "kblocks_per_stage", "smem_bytes")
+    return dict(zip(keys, list(info)))

@@ -93,14 +93,20 @@ int validate_gemm(const void *A, const void *B, int64_t M, int64_t N, int64_t K,
     return SPLITK_OK;
 }
 
+size_t counter_bytes(int64_t M, int64_t N);
+
 // The partial pass into P (and, when `out` is given, the split sum too).
 // `prefetch` lets the CTAs that start beside the previous launch prefetch the
 // operands into L2.  Only the fused launch uses it: before a partial pass
 // there is normally a reduce, which leaves no SM free, and prefetches issued
-// once every CTA is running only compete with the loads.
+// once every CTA is running only compete with the loads.  `allow_compact`:
+// inside a graph capture, the fused launch takes the compact layout (two CTAs
+// to an SM) when it may start beside the launch before it, or heads a run of
+// launches that may; a partial pass followed by the reduce keeps the full
+// ring, since the reduce's blocks leave no room for a second CTA.
 int run_partial_pass(const void *A, const void *B, float *P, float *out, unsigned *counters, int64_t M, int64_t N,
                      int64_t K, int64_t S, int64_t kps, int dtype, bool fused, bool prefetch, bool b_kn,
-                     cudaStream_t stream)
+                     bool allow_compact, cudaStream_t stream)
 {
     if (dtype == SPLITK_F32 && b_kn) {   // exact FMA on the CUDA cores
         return cuda_status(splitk::launch_simt_f32(static_cast<const float *>(A), static_cast<const float *>(B), P,
@@ -109,9 +115,37 @@ int run_partial_pass(const void *A, const void *B, float *P, float *out, unsigne
     GemmProblem pr{A, B, P, out, counters, M, N, K, S, kps, dtype == SPLITK_BF16};
     pr.b_kn = b_kn;
     pr.f32 = dtype == SPLITK_F32;   // 3xTF32 on the tensor cores
-    TilePlan plan = splitk::plan_tc(M, N, K, S, kps, fused, pr.f32);
+    const int e = elem_bytes(dtype);
+    // read before the wait for the previous grid: the operands only
+    const splitk::Span reads[2] = {splitk::span_of(A, static_cast<uint64_t>(M * K) * e),
+                                   splitk::span_of(B, static_cast<uint64_t>(N * K) * e)};
+    splitk::ChainGuard chain(stream, reads, 2);
+    const bool compact = allow_compact && chain.capturing() && (chain.overlap() || chain.fresh());
+    TilePlan plan = splitk::plan_tc(M, N, K, S, kps, fused, pr.f32, compact);
     if (!prefetch) plan.prefetchers = 0;
-    return cuda_status(splitk::launch_tc(pr, plan, stream));
+    pr.overlap = chain.overlap();
+    const cudaError_t err = splitk::launch_tc(pr, plan, stream);
+    splitk::Span writes[splitk::kMaxSpans];
+    int nw = 0;
+    if (P) writes[nw++] = splitk::span_of(P, static_cast<uint64_t>(S * M * N) * 4);
+    if (out) writes[nw++] = splitk::span_of(out, static_cast<uint64_t>(M * N) * 4);
+    if (counters && plan.split_sum == 1) writes[nw++] = splitk::span_of(counters, counter_bytes(M, N));
+    chain.commit(writes, nw, err == cudaSuccess);
+    splitk::note_launch({pr.overlap ? 1 : 0, plan.compact, chain.capturing() ? 1 : 0, plan.bn, plan.chunks,
+                         plan.stages, plan.kbs, static_cast<int>(plan.smem_bytes)});
+    return cuda_status(err);
+}
+
+// The accumulation pass, recorded in the capture chain as a launch that waits
+// at its start (it reads what the partial pass before it wrote).
+int run_reduce(const float *P, float *out, int64_t S, int64_t M, int64_t N, cudaStream_t stream)
+{
+    const splitk::Span reads[1] = {splitk::span_of(P, static_cast<uint64_t>(S * M * N) * 4)};
+    splitk::ChainGuard chain(stream, reads, 1);
+    const cudaError_t err = splitk::launch_reduce(P, out, S, M * N, stream);
+    const splitk::Span writes[1] = {splitk::span_of(out, static_cast<uint64_t>(M * N) * 4)};
+    chain.commit(writes, 1, err == cudaSuccess);
+    return cuda_status(err);
 }
 
 // The split sum runs inside the tensor-core launch; F32 with the [K,N] weight
@@ -173,7 +207,7 @@ static int gemm_splitk_impl(const void *A, const void *B, float *partials, int64
     const Range rp = range_of(partials, static_cast<uint64_t>(splits * M * N) * 4);
     if (overlap(rp, ra) || overlap(rp, rb)) return SPLITK_ERR_ALIAS;
     return run_partial_pass(A, B, partials, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false, false,
-                            b_kn, static_cast<cudaStream_t>(stream));
+                            b_kn, false, static_cast<cudaStream_t>(stream));
 }
 
 int gemm_splitk_bt(const void *A, const void *B, float *partials, int64_t M, int64_t N, int64_t K, int64_t splits,
@@ -197,7 +231,7 @@ int splitk_reduce(const float *partials, float *out, int64_t splits, int64_t M, 
     const Range rp = range_of(partials, static_cast<uint64_t>(splits * M * N) * 4);
     const Range ro = range_of(out, static_cast<uint64_t>(M * N) * 4);
     if (overlap(rp, ro)) return SPLITK_ERR_ALIAS;
-    return cuda_status(splitk::launch_reduce(partials, out, splits, M * N, static_cast<cudaStream_t>(stream)));
+    return run_reduce(partials, out, splits, M, N, static_cast<cudaStream_t>(stream));
 }
 
 int splitk_prepare_bt(const void *W, void *B, int64_t K, int64_t N, int dtype, void *stream)
@@ -237,15 +271,24 @@ static int gemm_impl(const void *A, const void *B, float *out, void *workspace, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float *P = static_cast<float *>(workspace);
     unsigned *counters = reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + partials_bytes(M, N, splits));
-    if (fused && fused_possible(dtype, b_kn)) {
-        // fused == 1 keeps no partials where the cluster sums the splits on chip
-        const TilePlan plan = splitk::plan_tc(M, N, K, splits, k_per_split, true, dtype == SPLITK_F32);
-        float *keep = (fused == 1 && plan.split_sum == 2) ? nullptr : P;
-        return run_partial_pass(A, B, keep, out, counters, M, N, K, splits, k_per_split, dtype, true, true, b_kn, s);
+    // The fused launch sums the splits inside its clusters.  Where the plan
+    // cannot hold a tile's splits in one resident cluster, the sum would go
+    // through arrival counters and an L2 read-back, which measured slower on
+    // GB300 than the separate reduce in every such case (for example BF16
+    // M256 N1024 K2048 with 8 splits: 17.9 against 7.0 us); those calls run as
+    // the two kernels instead.  The chunks do not depend on `fused`, so the
+    // result is the same either way, bit for bit.
+    if (fused && fused_possible(dtype, b_kn) &&
+        splitk::plan_tc(M, N, K, splits, k_per_split, true, dtype == SPLITK_F32).split_sum == 2) {
+        // fused == 1 keeps no partials
+        float *keep = fused == 1 ? nullptr : P;
+        return run_partial_pass(A, B, keep, out, counters, M, N, K, splits, k_per_split, dtype, true, true, b_kn,
+                                true, s);
     }
-    st = run_partial_pass(A, B, P, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false, false, b_kn, s);
+    st = run_partial_pass(A, B, P, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false, false, b_kn, false,
+                          s);
     if (st != SPLITK_OK) return st;
-    return cuda_status(splitk::launch_reduce(P, out, splits, M * N, s));
+    return run_reduce(P, out, splits, M, N, s);
 }
 
 int gemm_bt(const void *A, const void *B, float *out, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
@@ -309,9 +352,12 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
     if (st != SPLITK_OK) return st;
     if (elem_bytes(dtype) == 0) return SPLITK_ERR_DTYPE;
     if (!info) return SPLITK_ERR_NULL;
-    std::fill(info, info + 18, 0);
+    std::fill(info, info + 22, 0);
     const bool x3 = dtype == SPLITK_F32;
-    const bool in_kernel = fused != 0 && fused_possible(dtype, false);
+    // gemm_bt runs the two kernels where the fused launch could not sum a
+    // tile's splits inside one resident cluster
+    const bool in_kernel = fused != 0 && fused_possible(dtype, false) &&
+                           splitk::plan_tc(M, N, K, splits, k_per_split, true, x3).split_sum == 2;
     const TilePlan p = splitk::plan_tc(M, N, K, splits, k_per_split, in_kernel, x3);
     info[0] = x3 ? 2 : 0;
     info[1] = p.bn;
@@ -331,6 +377,37 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
     info[15] = in_kernel ? p.prefetchers : 0;   // gemm_bt's two-kernel path does not prefetch
     info[16] = p.rows_first;
     info[17] = p.tile_m;
+    // the layout a launch of this call takes inside a graph capture when it
+    // may start beside the launch before it (16-bit fused calls only)
+    if (in_kernel) {
+        const TilePlan c = splitk::plan_tc(M, N, K, splits, k_per_split, true, x3, true);
+        info[18] = c.compact;
+        info[19] = c.compact ? c.stages : 0;
+        info[20] = c.compact ? c.kbs : 0;
+        info[21] = c.compact ? static_cast<int>(c.smem_bytes) : 0;
+    }
+    return SPLITK_OK;
+}
+
+int splitk_set_overlap(int enable)
+{
+    if (enable != 0 && enable != 1) return SPLITK_ERR_CONFIG;
+    splitk::set_overlap_enabled(enable != 0);
+    return SPLITK_OK;
+}
+
+int splitk_last_launch(int *info)
+{
+    if (!info) return SPLITK_ERR_NULL;
+    const splitk::LaunchRecord r = splitk::last_launch();
+    info[0] = r.overlap;
+    info[1] = r.compact;
+    info[2] = r.capturing;
+    info[3] = r.bn;
+    info[4] = r.chunks;
+    info[5] = r.stages;
+    info[6] = r.kbs;
+    info[7] = r.smem_bytes;
     return SPLITK_OK;
 }
 

@@ -1,0 +1,147 @@
+// splitk_chain.cu -- which tensor-core launches may start before the launch
+// before them has finished.
+//
+// Every launch of this library is a programmatic dependent of the one before
+// it on its stream.  Normally a launch waits (griddepcontrol.wait) for that
+// grid to finish before it reads its operands, because the grid may have
+// written them.  Inside a CUDA graph capture the library can see what a new
+// launch depends on (cudaStreamGetCaptureInfo): when that is exactly the node
+// of its own previous launch, it knows which device memory every launch of
+// the chain since then writes.  If the new launch reads none of it, it may
+// load and multiply before the previous grid ends, waiting only before its
+// first store ("overlap").
+//
+// Which launches can still be running when an overlapping launch starts:
+// a launch that waited at its start (a "head") lets the next grid start only
+// after that wait returned, so everything before the head has finished; an
+// overlapping launch lets the next grid start as soon as its own CTAs have
+// started.  So a launch can meet every launch from the last head on, and the
+// window it is checked against is exactly that run: [head, ..., previous].
+// Every launch also waits for the previous grid before its first store, so
+// the grids finish in order and no launch overwrites what an earlier one
+// still reads.
+//
+// Eager launches (no capture) always wait: the library cannot see what else
+// the caller put on the stream.  splitk_set_overlap(0) turns the mechanism off.
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "splitk_internal.h"
+
+namespace splitk {
+namespace {
+
+constexpr int kChains = 16;    // capture sequences followed at once (least recently used replaced)
+constexpr int kWindow = 32;    // launches a new one is checked against, at most
+
+struct Entry {
+    cudaGraphNode_t node;
+    Span writes[kMaxSpans];
+    int n_writes;
+};
+
+struct Chain {
+    unsigned long long id = 0;
+    bool used = false;
+    uint64_t stamp = 0;
+    int n = 0;                 // entries e[0..n-1]; e[0] is the head
+    Entry e[kWindow];
+};
+
+std::mutex g_mu;
+Chain g_chains[kChains];
+uint64_t g_clock = 0;
+std::atomic<bool> g_enabled{true};
+
+Chain *find_chain(unsigned long long id)
+{
+    for (Chain &c : g_chains)
+        if (c.used && c.id == id) return &c;
+    return nullptr;
+}
+
+Chain *make_chain(unsigned long long id)
+{
+    Chain *victim = &g_chains[0];
+    for (Chain &c : g_chains) {
+        if (!c.used) {
+            victim = &c;
+            break;
+        }
+        if (c.stamp < victim->stamp) victim = &c;
+    }
+    victim->used = true;
+    victim->id = id;
+    victim->n = 0;
+    return victim;
+}
+
+bool meets(const Span &a, const Span &b) { return a.lo < b.hi && b.lo < a.hi; }
+
+}  // namespace
+
+void set_overlap_enabled(bool on) { g_enabled.store(on); }
+bool overlap_enabled() { return g_enabled.load(); }
+
+namespace {
+thread_local LaunchRecord t_last = {};
+}
+void note_launch(const LaunchRecord &r) { t_last = r; }
+LaunchRecord last_launch() { return t_last; }
+
+ChainGuard::ChainGuard(cudaStream_t stream, const Span *reads, int n_reads) : stream_(stream)
+{
+    if (!g_enabled.load()) return;
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    unsigned long long id = 0;
+    const cudaGraphNode_t *deps = nullptr;
+    size_t nd = 0;
+    if (cudaStreamGetCaptureInfo(stream, &st, &id, nullptr, &deps, nullptr, &nd) != cudaSuccess ||
+        st != cudaStreamCaptureStatusActive)
+        return;
+    lock_ = std::unique_lock<std::mutex>(g_mu);
+    capturing_ = true;
+    id_ = id;
+    fresh_ = true;
+    Chain *c = find_chain(id);
+    if (!c || c->n == 0 || nd != 1 || deps[0] != c->e[c->n - 1].node) return;   // not after our own launch
+    fresh_ = false;
+    for (int i = 0; i < c->n; ++i)
+        for (int w = 0; w < c->e[i].n_writes; ++w)
+            for (int r = 0; r < n_reads; ++r)
+                if (meets(c->e[i].writes[w], reads[r])) return;   // reads what a running launch may write
+    if (c->n >= kWindow) {
+        fresh_ = true;   // a long run: this launch waits and starts a new window
+        return;
+    }
+    overlap_ = true;
+}
+
+void ChainGuard::commit(const Span *writes, int n_writes, bool launched)
+{
+    if (!capturing_) return;
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    unsigned long long id = 0;
+    const cudaGraphNode_t *deps = nullptr;
+    size_t nd = 0;
+    Chain *c = find_chain(id_);
+    const bool ok = launched &&
+                    cudaStreamGetCaptureInfo(stream_, &st, &id, nullptr, &deps, nullptr, &nd) == cudaSuccess &&
+                    st == cudaStreamCaptureStatusActive && id == id_ && nd == 1 && n_writes <= kMaxSpans;
+    if (!ok) {
+        if (c) c->used = false;   // unknown state: the next launch waits and starts afresh
+        return;
+    }
+    if (!c) c = make_chain(id_);
+    if (!overlap_ || c->n >= kWindow) c->n = 0;   // a launch that waited at its start heads the window
+    Entry &e = c->e[c->n++];
+    e.node = deps[0];
+    e.n_writes = n_writes;
+    for (int w = 0; w < n_writes; ++w) e.writes[w] = writes[w];
+    c->stamp = ++g_clock;
+}
+
+}  // namespace splitk

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace splitk {
 
 // What one tensor-core launch computes.
@@ -19,6 +21,7 @@ struct GemmProblem {
     bool bf16;          // operand type: BF16 (true) or F16 (false)
     bool b_kn = false;  // B given as the [K,N] weight itself (read MN-major)
     bool f32 = false;   // F32 operands: 3xTF32 products on the tensor cores (bf16 ignored)
+    bool overlap = false; // no launch that may still run writes A or B: load before the previous grid ends
 };
 
 // How it is tiled.  One CTA computes a 128 x bn tile of one K-chunk of one
@@ -42,6 +45,8 @@ struct TilePlan {
     int x3;             // F32 operands as 3xTF32: 32-element k-blocks, stages twice the loaded bytes
     int rows_first;     // grid x walks the row tiles, y the column tiles (else x columns, y rows)
     int tile_m;         // rows of A per CTA: 128, or 256 (two accumulators; BN 256, one CTA per tile)
+    int compact;        // the ring cut so that two CTAs fit on an SM (same tiles, chunks and sums)
+    int recv_in_ring;   // the peers' shares land inside the stage ring once the MMAs are done
     dim3 grid;
     size_t smem_bytes;  // dynamic shared memory per CTA
 };
@@ -58,7 +63,10 @@ inline int64_t fused_counter_count(int64_t M, int64_t N) { return (N / 64) * ((M
 
 // Tile choice for a shape (automatic, or the process-wide override).
 // x3: F32 operands as 3xTF32 (else 16-bit operands).
-TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3 = false);
+// compact: the layout that lets two CTAs share an SM, where that plan exists
+// (plan.compact says whether it was taken).
+TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3 = false,
+                 bool compact = false);
 // The planner's estimate (microseconds) of one tensor-core launch of that
 // plan behind another launch, the in-launch split sum included when fused.
 double estimate_tc_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3 = false);
@@ -70,6 +78,51 @@ cudaError_t launch_simt_f32(const float *A, const float *B, float *P, int64_t M,
                             int64_t S, int64_t kps, bool b_kn, cudaStream_t stream);
 cudaError_t launch_reduce(const float *P, float *out, int64_t S, int64_t count, cudaStream_t stream);
 cudaError_t launch_prepare(const void *W, void *B, int64_t K, int64_t N, int elem_bytes, cudaStream_t stream);
+
+// A byte range [lo, hi) of device memory that a launch reads or writes.
+struct Span {
+    uintptr_t lo, hi;
+};
+inline Span span_of(const void *p, uint64_t bytes)
+{
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Span{lo, lo + static_cast<uintptr_t>(bytes)};
+}
+constexpr int kMaxSpans = 3;
+
+// Decides, for one launch, whether it may load before the previous grid on
+// its stream finishes (splitk_chain.cu), and records what it writes.  While a
+// capture is active the guard holds the chain table's lock from the decision
+// to commit(), so the two see the same chain.
+class ChainGuard {
+public:
+    ChainGuard(cudaStream_t stream, const Span *reads, int n_reads);
+    ChainGuard(const ChainGuard &) = delete;
+    ChainGuard &operator=(const ChainGuard &) = delete;
+    bool capturing() const { return capturing_; }
+    // no launch that may still be running writes what this one reads
+    bool overlap() const { return overlap_; }
+    // no earlier launch of this library precedes it in the capture (or the
+    // window was full): a head that independent launches may follow
+    bool fresh() const { return fresh_; }
+    // after the launch: record its writes (or forget the chain if it failed)
+    void commit(const Span *writes, int n_writes, bool launched);
+
+private:
+    cudaStream_t stream_;
+    std::unique_lock<std::mutex> lock_;
+    unsigned long long id_ = 0;
+    bool capturing_ = false, overlap_ = false, fresh_ = false;
+};
+void set_overlap_enabled(bool on);
+bool overlap_enabled();
+
+// What the last tensor-core launch of this host thread did (splitk_last_launch).
+struct LaunchRecord {
+    int overlap, compact, capturing, bn, chunks, stages, kbs, smem_bytes;
+};
+void note_launch(const LaunchRecord &r);
+LaunchRecord last_launch();
 
 // gemm_bt's argument checks (status as gemm_bt returns it; nothing launched),
 // and where the fused path's counters start in its workspace.

@@ -1,0 +1,296 @@
+"""GPU tests of launches that start beside the launch before them inside a
+CUDA graph capture ("overlap"; include/splitk.h, top comment).
+
+The library may let a launch load before the previous grid ends only where no
+launch that can still be running writes what the new one reads; every launch
+still waits for the previous grid before its first store.  Each test captures
+a sequence of calls, checks which launches overlapped (splitk_last_launch,
+read right after each call), replays the graph several times and compares
+every output bitwise with the same calls made eagerly, where each launch
+waits for the one before it.  The eager results themselves are pinned to the
+F64 oracle by test_gpu_parity.py; the headline case is checked against the
+oracle here too.
+"""
+import numpy as np
+import pytest
+
+from harness import TOL_FINAL, device_operand, max_scaled_error, oracle_case
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import split_bf16_gemm_gb300 as sk
+
+    sk.build()
+    sk.lib()
+    sk.splitk_set_tile_override(0, 0, 0)
+    sk.splitk_set_overlap(True)
+    yield sk
+    sk.splitk_set_overlap(True)
+
+
+def operands(M, N, K, dt, seed):
+    import splitk_inputs as gen
+
+    ops = gen.uniform(M, N, K, dt, seed)
+    return device_operand(ops.A, dt), device_operand(ops.B, dt)
+
+
+def capture(body):
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        body()
+    return g
+
+
+def bitwise(a, b) -> bool:
+    return torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def instances(sk, M, N, K, S, kps, dt, n, seed0=0):
+    out = []
+    for i in range(n):
+        A, B = operands(M, N, K, dt, seed0 + i)
+        nb = sk.gemm_bt_workspace_bytes(M, N, K, S, kps)
+        ws = torch.zeros(nb // 4, dtype=torch.float32, device="cuda")
+        out.append(dict(A=A, B=B, ws=ws, nb=nb, out=torch.full((M, N), 7.0, device="cuda"),
+                        ref=torch.full((M, N), 7.0, device="cuda")))
+    return out
+
+
+@pytest.mark.parametrize("shape", [
+    (256, 1024, 2048, 2, 1024),   # the headline
+    (96, 512, 2048, 4, 512),      # a cluster of 8 CTAs
+    (256, 512, 2048, 4, 512),
+    (32, 64, 128, 2, 64),         # the single tile
+    (160, 192, 320, 3, 128),      # M tail, three splits (two kernels)
+])
+@pytest.mark.parametrize("fused", [1, 3])
+def test_independent_calls_overlap_bitwise(lib, shape, fused):
+    sk = lib
+    M, N, K, S, kps = shape
+    dt = "bf16"
+    insts = instances(sk, M, N, K, S, kps, dt, 6)
+    for it in insts:   # eager: every launch waits for the one before
+        sk.gemm_bt(it["A"], it["B"], it["ref"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=fused)
+    torch.cuda.synchronize()
+    refs_ws = [it["ws"].clone() for it in insts]
+    in_kernel = sk.splitk_describe_launch(M, N, K, S, kps, dt, fused=fused)["fused_in_kernel"]
+    seen = []
+
+    def body():
+        for it in insts:
+            sk.gemm_bt(it["A"], it["B"], it["out"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=fused)
+            seen.append(sk.splitk_last_launch())
+
+    g = capture(body)
+    assert all(d["capturing"] == 1 for d in seen)
+    assert seen[0]["overlap"] == 0                       # nothing of ours precedes it
+    # fused in one launch: each call reads only its own A and B, which no
+    # earlier call writes.  Two kernels: each call's partial pass follows the
+    # previous call's reduce, whose output it does not read.
+    assert all(d["overlap"] == 1 for d in seen[1:]), seen
+    if in_kernel and (M, N, K) == (256, 1024, 2048):
+        assert all(d["compact"] == 1 for d in seen), seen
+    for _ in range(3):
+        for it in insts:
+            it["out"].fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        for it in insts:
+            assert bitwise(it["out"], it["ref"])
+    if fused == 3:   # the kept partials too
+        for it, w in zip(insts, refs_ws):
+            P = S * M * N
+            assert bitwise(it["ws"][:P], w[:P])
+    assert sk.splitk_get_device_status() == 0
+    if (M, N, K, S) == (256, 1024, 2048, 2):
+        ops, Pr, SP, Or, SO = oracle_case(M, N, K, S, kps, dt)
+        assert max_scaled_error(insts[0]["out"].cpu().numpy(), Or, SO) <= TOL_FINAL[dt]
+
+
+def test_dependent_chain_waits(lib):
+    """F32 operands, so that an output can be the next call's A.  Expected:
+    a: X -> Y          head (no call of ours before it): waits
+    b: P -> Q          independent of a: overlaps
+    c: Y -> Z          reads Y, which a (still in b's window) writes: waits
+    d: Z -> W          reads what c writes: waits
+    e: R -> T          independent of d: overlaps
+    f: (U, Q) -> V     reads Q, written by b before the wait in c: overlaps
+    g: W -> Y2         reads W, written by d (in the window d, e, f): waits"""
+    sk = lib
+    dt = "f32"
+    M, K = 128, 256
+    S, kps = 2, 128
+
+    def mat(rows, cols, seed):
+        g = torch.Generator(device="cpu").manual_seed(seed)
+        return (torch.rand(rows, cols, generator=g) * 2 - 1).cuda()
+
+    X, P, R, U = mat(M, K, 1), mat(M, K, 2), mat(M, K, 3), mat(M, K, 4)
+    Bs = {k: mat(256, K, 10 + i) for i, k in enumerate("abcdeg")}
+    nb = sk.gemm_bt_workspace_bytes(M, 256, K, S, kps)
+    ws = {k: torch.zeros(nb // 4, device="cuda") for k in "abcdefg"}
+    outs = {k: torch.full((M, 256), 7.0, device="cuda") for k in "abcdeg"}
+    outs["f"] = torch.full((M, 128), 7.0, device="cuda")
+    Y, Q, Z, W, T, V, Y2 = outs["a"], outs["b"], outs["c"], outs["d"], outs["e"], outs["f"], outs["g"]
+    calls = [
+        ("a", X, Bs["a"], Y, 256), ("b", P, Bs["b"], Q, 256), ("c", Y, Bs["c"], Z, 256),
+        ("d", Z, Bs["d"], W, 256), ("e", R, Bs["e"], T, 256), ("f", U, Q, V, 128), ("g", W, Bs["g"], Y2, 256),
+    ]
+
+    def run(record=None):
+        for name, A, B, O, N in calls:
+            sk.gemm_bt(A, B, O, ws[name], nb, M, N, K, S, kps, dt, fused=1)
+            if record is not None:
+                record.append((name, sk.splitk_last_launch()["overlap"]))
+
+    run()
+    torch.cuda.synchronize()
+    ref = {k: v.clone() for k, v in outs.items()}
+    seen = []
+    g = capture(lambda: run(seen))
+    assert seen == [("a", 0), ("b", 1), ("c", 0), ("d", 0), ("e", 1), ("f", 1), ("g", 0)], seen
+    for _ in range(3):
+        for v in outs.values():
+            v.fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        for k in outs:
+            assert bitwise(outs[k], ref[k]), k
+    assert sk.splitk_get_device_status() == 0
+
+
+def test_store_waits_for_previous_reader(lib):
+    """b overlaps a (it reads neither Y nor anything a writes), but b's output
+    is a's input X: b may load early, yet must not store before a has read X.
+    The graph is replayed from the same starting X each time."""
+    sk = lib
+    dt = "f32"
+    M, N, K, S, kps = 128, 256, 256, 2, 128
+    g0 = torch.Generator(device="cpu").manual_seed(5)
+    X0 = (torch.rand(M, K, generator=g0) * 2 - 1).cuda()
+    B1 = (torch.rand(N, K, generator=g0) * 2 - 1).cuda()
+    A2 = (torch.rand(M, K, generator=g0) * 2 - 1).cuda()
+    B2 = (torch.rand(N, K, generator=g0) * 2 - 1).cuda()
+    X = X0.clone()
+    Y = torch.empty(M, N, device="cuda")
+    nb = sk.gemm_bt_workspace_bytes(M, N, K, S, kps)
+    w1 = torch.zeros(nb // 4, device="cuda")
+    w2 = torch.zeros(nb // 4, device="cuda")
+    seen = []
+
+    def run(record=None):
+        sk.gemm_bt(X, B1, Y, w1, nb, M, N, K, S, kps, dt, fused=1)
+        if record is not None:
+            record.append(sk.splitk_last_launch()["overlap"])
+        sk.gemm_bt(A2, B2, X, w2, nb, M, N, K, S, kps, dt, fused=1)   # overwrites a's input
+        if record is not None:
+            record.append(sk.splitk_last_launch()["overlap"])
+
+    run()
+    torch.cuda.synchronize()
+    Y_ref, X_ref = Y.clone(), X.clone()
+    g = capture(lambda: run(seen))
+    assert seen == [0, 1]
+    for _ in range(5):
+        X.copy_(X0)
+        Y.fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert bitwise(Y, Y_ref) and bitwise(X, X_ref)
+    assert sk.splitk_get_device_status() == 0
+
+
+def test_other_work_between_calls_waits(lib):
+    """A copy captured between two calls writes the second call's A: the second
+    call follows that node, not the library's launch, so it waits; the call
+    after it overlaps again."""
+    sk = lib
+    M, N, K, S, kps, dt = 256, 1024, 2048, 2, 1024, "bf16"
+    insts = instances(sk, M, N, K, S, kps, dt, 3)
+    src = operands(M, N, K, dt, 99)[0]
+    seen = []
+
+    def run(record=None):
+        it0, it1, it2 = insts
+        sk.gemm_bt(it0["A"], it0["B"], it0["out"], it0["ws"], it0["nb"], M, N, K, S, kps, dt, fused=1)
+        it1["A"].copy_(src)
+        sk.gemm_bt(it1["A"], it1["B"], it1["out"], it1["ws"], it1["nb"], M, N, K, S, kps, dt, fused=1)
+        if record is not None:
+            record.append(sk.splitk_last_launch()["overlap"])
+        sk.gemm_bt(it2["A"], it2["B"], it2["out"], it2["ws"], it2["nb"], M, N, K, S, kps, dt, fused=1)
+        if record is not None:
+            record.append(sk.splitk_last_launch()["overlap"])
+
+    g = capture(lambda: run(seen))
+    assert seen == [0, 1]
+    for rep in range(3):
+        src.copy_(operands(M, N, K, dt, 100 + rep)[0])
+        for it in insts:
+            it["out"].fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        got = [it["out"].clone() for it in insts]
+        run()   # eagerly, from the same state
+        torch.cuda.synchronize()
+        for a, it in zip(got, insts):
+            assert bitwise(a, it["out"])
+    assert sk.splitk_get_device_status() == 0
+
+
+def test_overlap_switch(lib):
+    sk = lib
+    M, N, K, S, kps, dt = 256, 1024, 2048, 2, 1024, "bf16"
+    insts = instances(sk, M, N, K, S, kps, dt, 4)
+    for it in insts:
+        sk.gemm_bt(it["A"], it["B"], it["ref"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=1)
+    torch.cuda.synchronize()
+    seen = []
+
+    def body():
+        for it in insts:
+            sk.gemm_bt(it["A"], it["B"], it["out"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=1)
+            seen.append(sk.splitk_last_launch())
+
+    try:
+        sk.splitk_set_overlap(False)
+        g = capture(body)
+    finally:
+        sk.splitk_set_overlap(True)
+    assert all(d["overlap"] == 0 and d["compact"] == 0 and d["capturing"] == 0 for d in seen)
+    g.replay()
+    torch.cuda.synchronize()
+    for it in insts:
+        assert bitwise(it["out"], it["ref"])
+
+
+def test_kn_layout_overlap_bitwise(lib):
+    sk = lib
+    M, N, K, S, kps, dt = 256, 1024, 2048, 2, 1024, "bf16"
+    insts = instances(sk, M, N, K, S, kps, dt, 4)
+    for it in insts:
+        it["W"] = it["B"].t().contiguous()
+        sk.gemm_bt(it["A"], it["B"], it["ref"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=1)
+    torch.cuda.synchronize()
+    seen = []
+
+    def body():
+        for it in insts:
+            sk.gemm_kn(it["A"], it["W"], it["out"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=1)
+            seen.append(sk.splitk_last_launch()["overlap"])
+
+    g = capture(body)
+    assert seen == [0, 1, 1, 1]
+    g.replay()
+    torch.cuda.synchronize()
+    for it in insts:
+        assert bitwise(it["out"], it["ref"])   # the [K,N] path is bitwise the [N,K] path
+    assert sk.splitk_get_device_status() == 0

@@ -18,7 +18,11 @@ tests, and every tile override:
   then with the whole shared memory of a block;
 - a rank's share of the tile is a whole number of 32 x 32 boxes (each warp
   pushes whole boxes), every 16-byte piece has exactly one owner, and every
-  contribution sent to or read from a receive slot stays inside that slot.
+  contribution sent to or read from a receive slot stays inside that slot;
+- the compact layout (taken inside graph captures): the same tiles, chunks
+  and cluster, a ring that still covers every k once, the receive slots
+  inside the ring after the staging area, and two thread blocks' shared and
+  tensor memory within one SM's.
 """
 import itertools
 
@@ -27,6 +31,9 @@ import pytest
 from test_gpu_fuzz import LARGE, RANDOM
 
 SMEM_LIMIT = 226 * 1024
+COMPACT_LIMIT = 112 * 1024
+SM_SMEM = 228 * 1024          # per SM; 1 KB of it reserved per thread block
+STATIC_SMEM = 240             # the kernel's barriers and flags (nvcc -Xptxas -v)
 TILE_M = 128
 RESIDENT_CLUSTERS = {1: 148, 2: 72, 4: 36, 8: 15}   # clusters of 1-8 CTAs a GB300 keeps resident
 
@@ -111,7 +118,33 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
         assert 2 * BN <= 512
         assert epi_bytes <= region0 and stages * (a_kblock + BN * 128) * KBS <= region0
 
-    # K coverage: every k of every split loaded exactly once, boxes aligned
+    check_k_coverage(K, S, kps, C, CL, KBS, T3, kb_elems, elem)
+    check_exchange(BN, Q, region0, d["smem_bytes"] - 1024)
+
+    # the compact layout: same tiles and sums, a ring two blocks to an SM,
+    # the receive slots inside it after the staging area
+    if d["compact"]:
+        assert d["fused_in_kernel"] == 1 and not x3 and TM == TILE_M and BN <= 128
+        assert -(-M // TM) * (N // BN) * S * C // Q <= RESIDENT_CLUSTERS[Q]   # one wave
+        cst, ckbs, csmem = d["compact_stages"], d["compact_kblocks_per_stage"], d["compact_smem_bytes"]
+        assert 1 <= cst <= 8 and ckbs in (1, 2, 4) and (ckbs == 1 or T3)
+        cstage = (TM + BN) * 128 * ckbs
+        nkb = -(-CL // kb_elems)
+        assert cst >= min(2, -(-nkb // ckbs))            # double-buffered unless one stage holds the chunk
+        recv_bytes = (Q - 1) * share * 16
+        cregion = -(-max(cst * cstage, epi_bytes + recv_bytes) // 1024) * 1024
+        assert csmem == cregion + 1024 <= COMPACT_LIMIT
+        assert 2 * (csmem + STATIC_SMEM + 1024) <= SM_SMEM   # two blocks to an SM
+        assert 2 * BN <= 512 and BN <= csmem // 512          # tensor memory: theirs fits, by the smem rule
+        check_k_coverage(K, S, kps, C, CL, ckbs, int(ckbs > 1), kb_elems, elem)
+        if Q > 1:
+            check_exchange(BN, Q, epi_bytes, cregion)
+    else:
+        assert d["compact_stages"] == d["compact_kblocks_per_stage"] == d["compact_smem_bytes"] == 0
+
+
+def check_k_coverage(K, S, kps, C, CL, KBS, T3, kb_elems, elem):
+    """Every k of every split loaded exactly once, boxes aligned."""
     for s in range(S):
         ks, ke = s * kps, min(s * kps + kps, K)
         covered = []
@@ -135,7 +168,13 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
                     covered += range(kx, kx + valid)
         assert covered == list(range(ks, ke)), (s, ks, ke)
 
-    # ownership and the exchange
+
+def check_exchange(BN, Q, recv, limit):
+    """Ownership of the tile's pieces, and every push into and read of the
+    receive slots (which start at `recv`) inside its slot and below `limit`."""
+    pieces = 32 * BN
+    share = -(-(-(-pieces // Q)) // 8) * 8
+    epi_bytes = TILE_M * BN * 4
     if Q > 1:
         assert share % 256 == 0, "a rank's share must be whole 32 x 32 boxes"
     own = [(min(pieces, r * share), min(pieces, min(pieces, r * share) + share)) for r in range(Q)]
@@ -148,7 +187,6 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
             assert (row, col) not in owner
             owner[(row, col)] = r
     assert len(owner) == pieces
-    recv = region0
     for sender in range(Q):
         for b in range(pieces // 256):              # the box a warp stages and pushes
             r = (b * 256) // share
@@ -158,7 +196,7 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
             slot = sender - (1 if sender > r else 0)
             dst = recv + (slot * share + (b * 256 - r * share)) * 16
             assert recv + slot * share * 16 <= dst and dst + 4096 <= recv + (slot + 1) * share * 16
-            assert dst + 4096 <= d["smem_bytes"] - 1024
+            assert dst + 4096 <= limit
     for me, (lo, hi) in enumerate(own):             # the owner's reads of its peers' slots
         for r in range(Q):
             if r == me:
