@@ -76,6 +76,106 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+# Nominal dense tensor rates of a GB300 (PFLOP/s): BF16/F16 2.25, TF32 1.1.  F32
+# operands run as three TF32 products each, so their tensor term is the BF16
+# measured peak x 1.1 / 2.25 / 3 per useful FLOP.
+TF32_OVER_BF16 = 1.1 / 2.25
+
+
+def op_roofline(M_, N_, K_, S_, dt, hbm_gbs, bf16_tflops):
+    """Roofline times (us) of one operation: the slower of its FLOPs at the
+    tensor peak for its element type and its bytes at the HBM bandwidth, for
+    the two-pass bytes (A, B, partials written and read, output) and for the
+    fused kernel's minimal bytes (A, B, output)."""
+    e = 4 if dt == "f32" else 2
+    flops = 2 * M_ * N_ * K_
+    peak = bf16_tflops * (TF32_OVER_BF16 / 3 if dt == "f32" else 1.0)
+    t_flop = flops / (peak * 1e12) * 1e6
+    b2 = M_ * K_ * e + N_ * K_ * e + 2 * S_ * M_ * N_ * 4 + M_ * N_ * 4
+    bmin = M_ * K_ * e + N_ * K_ * e + M_ * N_ * 4
+    t2, tmin = b2 / (hbm_gbs * 1e9) * 1e6, bmin / (hbm_gbs * 1e9) * 1e6
+    return {"flops": flops, "bytes_2pass": b2, "bytes_min": bmin, "tensor_peak_tflops": round(peak, 1),
+            "t_flop_us": round(t_flop, 4), "t_roof_us_2pass": round(max(t_flop, t2), 4),
+            "t_roof_us_min": round(max(t_flop, tmin), 4),
+            "bound_2pass": "tensor" if t_flop > t2 else "hbm", "bound_min": "tensor" if t_flop > tmin else "hbm"}
+
+
+# The pages' workloads beside the headline: the M96 and M256/N512 shapes, the
+# single tile, and the dtype x split sweep over the skinny and short-K shapes
+# with the short-final-split case ("Wider consecutive-weight NAX GEMM",
+# section "Performance method"; "Aligned shared rows for pipelined NAX on
+# CUDA", section "Measurement protocol").
+CONFIGS = [("bf16", 32, 64, 128, 2, 64), ("bf16", 96, 512, 2048, 4, 512), ("bf16", 256, 512, 2048, 4, 512)]
+for _dt in ("bf16", "f16", "f32"):
+    for _S in (1, 2, 4, 8, 16):
+        CONFIGS.append((_dt, 32, 512, 2048, _S, 2048 // _S))
+        CONFIGS.append((_dt, 96, 512, 512, _S, 512 // _S))
+    CONFIGS.append((_dt, 64, 128, 160, 3, 64))
+
+
+def measure_configs(sk, torch, stream, dev, hbm, tflops, pool_bytes=160 << 20, max_inst=128):
+    """Per workload: fused and two-kernel us per operation (graphs of 8 calls,
+    CUDA events), TFLOP/s and the roofline fractions.  Each workload cycles a
+    pool of seeded instances of at least `pool_bytes` of A + B where
+    `max_inst` instances reach that (else the pool is L2-resident, and the
+    entry says so).  The fused and two-kernel outputs of one instance must be
+    equal bit for bit."""
+    import numpy as np
+
+    import splitk_inputs as gen
+
+    res = []
+    for dt, M_, N_, K_, S_, kps_ in CONFIGS:
+        e = 4 if dt == "f32" else 2
+        ab = (M_ * K_ + N_ * K_) * e
+        n = max(8, min(max_inst, -(-pool_bytes // ab)))
+        n -= n % 8
+        nb = sk.gemm_bt_workspace_bytes(M_, N_, K_, S_, kps_)
+        pool = []
+        for i in range(n):
+            ops = gen.uniform(M_, N_, K_, dt, seed=i)
+            if dt == "f32":
+                A_ = torch.from_numpy(np.ascontiguousarray(ops.A, np.float32)).to(dev)
+                B_ = torch.from_numpy(np.ascontiguousarray(ops.B, np.float32)).to(dev)
+            else:
+                tdt = torch.bfloat16 if dt == "bf16" else torch.float16
+                A_ = torch.from_numpy(ops.A.view(np.int16)).to(dev).view(tdt)
+                B_ = torch.from_numpy(ops.B.view(np.int16)).to(dev).view(tdt)
+            pool.append((A_, B_, torch.empty((M_, N_), dtype=torch.float32, device=dev),
+                         torch.empty((nb // 4,), dtype=torch.float32, device=dev)))
+        groups = [pool[g * 8:(g + 1) * 8] for g in range(n // 8)]
+        entry = {"workload": f"{dt.upper()} M{M_} N{N_} K{K_} splits={S_} (k_per_split={kps_})",
+                 "instances": n, "pool_mb": round(n * ab / 1e6, 1),
+                 "l2": "cold (pool larger than L2)" if n * ab > 129e6 else "warm (pool fits in L2)"}
+        plan = sk.splitk_describe_launch(M_, N_, K_, S_, kps_, dt, fused=1)
+        entry["fused_in_kernel"] = plan["fused_in_kernel"]
+        for fused, key in ((1, "fused_us"), (0, "two_pass_us")):
+            graphs = [capture(torch, stream, lambda grp=grp, f=fused: [
+                sk.gemm_bt(a, b, o, w, nb, M_, N_, K_, S_, kps_, dt, fused=f, stream=stream) for a, b, o, w in grp])
+                for grp in groups]
+            time_graphs(torch, stream, graphs, max(3, len(graphs)))
+            reps = max(len(graphs), 40)
+            entry[key] = round(min(time_graphs(torch, stream, graphs, reps) for _ in range(3)) * 1e3 / (reps * 8), 4)
+        a, b, o, w = pool[0]
+        sk.gemm_bt(a, b, o, w, nb, M_, N_, K_, S_, kps_, dt, fused=0, stream=stream)
+        torch.cuda.synchronize()
+        ref = o.clone()
+        sk.gemm_bt(a, b, o, w, nb, M_, N_, K_, S_, kps_, dt, fused=1, stream=stream)
+        torch.cuda.synchronize()
+        entry["fused_bitwise_two_pass"] = bool(torch.equal(ref.view(torch.int32), o.view(torch.int32)))
+        r = op_roofline(M_, N_, K_, S_, dt, hbm, tflops)
+        entry["tflops_fused"] = round(r["flops"] / (entry["fused_us"] * 1e-6) / 1e12, 2)
+        entry["frac_min_bytes_fused"] = round(r["t_roof_us_min"] / entry["fused_us"], 4)
+        entry["frac_2pass_fused"] = round(r["t_roof_us_2pass"] / entry["fused_us"], 4)
+        entry["frac_2pass_two_pass"] = round(r["t_roof_us_2pass"] / entry["two_pass_us"], 4)
+        entry["roofline"] = r
+        res.append(entry)
+        del pool, groups
+    if sk.splitk_get_device_status(stream) != 0:
+        raise RuntimeError("a kernel's bounded wait ran out during the per-workload runs")
+    return res
+
+
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -86,7 +186,7 @@ class ClockSampler:
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
                0x100: "display_clock_setting"}
 
-    def __init__(self, device_index: int, period_s: float = 0.002):
+    def __init__(self, device_index: int, period_s: float = 0.0005):
         self.samples, self.reasons, self.max_mhz = [], 0, None
         self.period = period_s
         self.ok = False
@@ -419,8 +519,9 @@ def run_ours(args, rank, world, dev, torch, dist):
     # 9 rounds of 40 replays of the same graphs, the median round; and pack=1
     # (one operation per replay, over the same pool)
     round_us = []
-    for _ in range(9):
-        round_us.append(time_graphs(torch, stream, graphs, 40) * 1e3 / (40 * pack))
+    with ClockSampler(nvml_index(torch, dev), period_s=0.0005) as round_clocks:
+        for _ in range(9):
+            round_us.append(time_graphs(torch, stream, graphs, 40) * 1e3 / (40 * pack))
     single = [capture(torch, stream, lambda i=i: op(i)) for i in pool]
     time_graphs(torch, stream, single, 10)
     pack1_us = time_graphs(torch, stream, single, 400) * 1e3 / 400
@@ -496,6 +597,15 @@ def run_ours(args, rank, world, dev, torch, dist):
     del Ws, Bs
 
     hbm, tflops, peak_kind = load_peaks()
+    # the same fused graphs with every launch waiting for the one before (the
+    # overlap of independent launches inside a capture turned off)
+    sk.splitk_set_overlap(False)
+    strict_graphs = [capture(torch, stream, lambda grp=grp: [op(i) for i in grp]) for grp in groups]
+    sk.splitk_set_overlap(True)
+    time_graphs(torch, stream, strict_graphs, 5)
+    strict_us = time_graphs(torch, stream, strict_graphs, reps) * 1e3 / (reps * pack)
+    configs = measure_configs(sk, torch, stream, dev, hbm, tflops) if args.configs else None
+    roof = op_roofline(M, N, K, SPLITS, DTYPE, hbm, tflops)
     achieved = dom_bytes / (dom_us * 1e-6) / 1e9
     line = {
         "metric": METRIC, "value": round(us_per_op, 4), "unit": "µs/op", "n_gpus": world,
@@ -511,16 +621,20 @@ def run_ours(args, rank, world, dev, torch, dist):
                    "plan": plan},
         "tflops": round(FLOPS_PER_OP / (us_per_op * 1e-6) / 1e12 / 1, 2),
         "op_roofline": {
-            "t_roof_us_2pass_bytes": round(BYTES_2PASS / (hbm * 1e9) * 1e6, 4),
-            "frac_2pass_bytes": round(BYTES_2PASS / (hbm * 1e9) * 1e6 / us_per_op, 4),
-            "t_roof_us_min_bytes": round(BYTES_FUSED / (hbm * 1e9) * 1e6, 4),
-            "frac_min_bytes": round(BYTES_FUSED / (hbm * 1e9) * 1e6 / us_per_op, 4),
+            "what": "the slower of the FLOPs at the measured dense BF16 peak and the bytes at the measured "
+                    "HBM bandwidth, for the two-pass bytes and for the fused kernel's minimal bytes",
+            "t_flop_us": roof["t_flop_us"], "bound": roof["bound_2pass"],
+            "t_roof_us_2pass_bytes": roof["t_roof_us_2pass"],
+            "frac_2pass_bytes": round(roof["t_roof_us_2pass"] / us_per_op, 4),
+            "t_roof_us_min_bytes": roof["t_roof_us_min"],
+            "frac_min_bytes": round(roof["t_roof_us_min"] / us_per_op, 4),
             "peak": f"{peak_kind} {hbm} GB/s",
             # against the nominal HBM3e bandwidth as well
             "nominal_gbs": NOMINAL_HBM_GBS,
             "frac_2pass_bytes_nominal": round(BYTES_2PASS / (NOMINAL_HBM_GBS * 1e9) * 1e6 / us_per_op, 4),
             "frac_min_bytes_nominal": round(BYTES_FUSED / (NOMINAL_HBM_GBS * 1e9) * 1e6 / us_per_op, 4)},
-        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1),
+        "roofline": {"bound": roof["bound_min"] if fused else roof["bound_2pass"], "kernel": dom_name,
+                     "t_flop_us": roof["t_flop_us"], "achieved": round(achieved, 1),
                      "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "traffic": kernel_traffic() if fused else None, "bytes_per_launch": dom_bytes,
                      "launch_us": round(dom_us, 4), "peak_kind": peak_kind},
@@ -528,10 +642,15 @@ def run_ours(args, rank, world, dev, torch, dist):
                      "rounds_min_max_us": [round(min(round_us), 4), round(max(round_us), 4)],
                      "pack1_us": round(pack1_us, 4),
                      "pack1": "one operation per graph replay, the pool's instances in turn (each replay "
-                              "pays a graph launch; no dependent-launch overlap across replays)"},
+                              "pays a graph launch; no dependent-launch overlap across replays)",
+                     "clocks": round_clocks.summary()},
         "kernels_us": {"partial_pass": round(gemm_us, 4), "reduce": round(red_us, 4),
                        "two_pass_op": round(two_pass_us, 4),
-                       "fused_op" if fused else "two_pass_op_graph": round(us_per_op * world, 4)},
+                       "fused_op" if fused else "two_pass_op_graph": round(us_per_op * world, 4),
+                       "fused_op_every_launch_waits": round(strict_us, 4)},
+        "overlap": "inside each captured graph, a call whose operands no running launch writes loads "
+                   "before the previous launch ends and waits only before its first store; "
+                   "kernels_us.fused_op_every_launch_waits is the same graphs with that turned off",
         "e2e": e2e,
         "kn_layout": {"what": "the same operations with the weight in its [K,N] layout (gemm_kn, MN-major B)",
                       "us": kn_us},
@@ -545,6 +664,7 @@ def run_ours(args, rank, world, dev, torch, dist):
                    "tolerance": TOL_BF16_FINAL,
                    "before_timing": {"outputs": before[1], "max_scaled_err": float(f"{before[0]:.3e}")},
                    "after_timing": {"outputs": after[1], "max_scaled_err": float(f"{after[0]:.3e}")}},
+        "configs": configs,
         "gpu_launches": args.steps * pack * plan["kernels_per_call"],
         "clocks": clocks.summary(),
     }
@@ -561,6 +681,8 @@ def main():
     ap.add_argument("--pack", type=int, default=8)
     ap.add_argument("--pool", type=int, default=40)
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the per-workload measurements of the pages' other shapes")
     ap.add_argument("--profile", action="store_true",
                     help="short run for ncu: the timed graphs only, no secondary timings, no CPU leg")
     args = ap.parse_args()

@@ -140,17 +140,15 @@ int splitk_prepare_bt(const void *W, void *B, int64_t K, int64_t N, int dtype,
 int splitk_reduce(const float *partials, float *out, int64_t splits, int64_t M,
                   int64_t N, void *stream);
 
-/* Bytes of device workspace gemm_bt needs: the F32 partials [splits,M,N]
- * (the first splits*M*N*4 bytes) followed by the fused path's arrival
- * counters.  The same size serves both values of `fused`.  Returns 0 for a
- * geometry that breaks the contract. */
+/* Bytes of device workspace gemm_bt needs: the F32 partials [splits,M,N],
+ * splits*M*N*4 bytes.  The same size serves every value of `fused`.  Returns
+ * 0 for a geometry that breaks the contract. */
 size_t gemm_bt_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t splits,
                                int64_t k_per_split, int fused);
 
-/* Zeroes a workspace (cudaMemsetAsync on `stream`).  A workspace must be
- * zeroed once before its first fused gemm_bt call; every fused call leaves
- * its counters zero again, so later calls need no re-initialisation (unless
- * a launch reported SPLITK_ERR_DEVICE_TIMEOUT). */
+/* Zeroes a workspace (cudaMemsetAsync on `stream`).  gemm_bt needs no
+ * particular workspace contents (every byte it reads it wrote in the same
+ * call); this gives callers a defined starting state. */
 int gemm_bt_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
 
 /* One call: the partial pass then the accumulation pass, on one stream.
@@ -167,10 +165,11 @@ int gemm_bt_workspace_init(void *workspace, size_t workspace_bytes, void *stream
  *                 (too many splits for one cluster, or more tiles than
  *                 resident clusters), the call runs the two kernels of 0,
  *                 which measured faster there than summing through global
- *                 memory (splitk_describe_launch reports which);
+ *                 memory; so it does for F32 operands with M <= 32 where the
+ *                 cluster summing the splits would be larger than the
+ *                 partial pass's own (measured faster too).
+ *                 splitk_describe_launch reports which;
  *              3: as 1, and the workspace also holds the partials afterwards.
- *              Fused calls need the workspace zeroed once before the first
- *              of them (gemm_bt_workspace_init).
  * For a given shape, `out` (and the partials, where kept) are bitwise the
  * same for every value of `fused`. */
 int gemm_bt(const void *A, const void *B, float *out, void *workspace,
@@ -209,13 +208,13 @@ int gemm_kn(const void *A, const void *W, float *out, void *workspace,
  * A shape whose gemm_bt_workspace_bytes() exceeds it is rejected with
  * SPLITK_ERR_WORKSPACE before any device work (splitk_last_error() gives the
  * sizes).  The call allocates nothing: no cudaMalloc, no cudaFree, no
- * allocating library routine.  Its first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  Every call on a device
- * shares the one array and leaves its contents behind (the partials); the
- * fused path's counters are cleared at the start of each call.  Calls whose
- * executions overlap on the GPU (on different streams, say) race on the
- * array and must not be issued. */
+ * allocating library routine.  Each call looks up the array's device
+ * address on the current device (cudaGetSymbolAddress, a lookup that
+ * allocates nothing); the first call on a device also loads the library's
+ * device code there, so make that first call before any stream capture.
+ * Every call on a device shares the one array and leaves its contents behind
+ * (the partials).  Calls whose executions overlap on the GPU (on different
+ * streams, say) race on the array and must not be issued. */
 int gemm_bt_noalloc(const void *A, const void *B, float *out, int64_t M,
                     int64_t N, int64_t K, int64_t splits, int64_t k_per_split,
                     int dtype, int fused, void *stream);
@@ -241,8 +240,7 @@ size_t gemm_bt_host_staging_bytes(int64_t count, int64_t M, int64_t N,
  *   out_host   host, [count,M,N] F32; fully overwritten once `stream`
  *              reaches the end of the call's work
  *   staging    device, >= gemm_bt_host_staging_bytes(), 16-byte aligned,
- *              overlapping no B; zeroed once (gemm_bt_workspace_init) before
- *              its first fused use, like a gemm_bt workspace
+ *              overlapping no B
  *   fused      as for gemm_bt (0, 1 or 3)
  *   ops_per_copy  operations moved by one copy each way; 0 lets the library
  *              choose (at least 2 MiB of A per copy, at most half the batch)
@@ -299,8 +297,7 @@ int splitk_choose_splits(int64_t M, int64_t N, int64_t K, int dtype, int fused,
  * Every candidate's arguments are checked before anything is enqueued (the
  * statuses of gemm_bt; SPLITK_ERR_WORKSPACE if no candidate fits).  On
  * return the private stream has finished, `out` holds the chosen split's
- * result, `stream` is ordered after it, and a fused workspace has the chosen
- * split's counters zero, ready for gemm_bt with that split.  The inputs are
+ * result and `stream` is ordered after it.  The inputs are
  * read repeatedly, so they sit in L2 when they fit there: the timings rank
  * the candidates, they are not cold-cache figures.  Not capturable. */
 int splitk_autotune_splits(const void *A, const void *B, float *out,
@@ -348,7 +345,7 @@ int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
  *  launches of more than one wave with M < N whose B slab per split,
  *  N * k_per_split elements, is over 32 MB), tile_m (rows of A per thread
  *  block: 128, or 256 for BN 256 plans with one block per tile, no cluster
- *  and no arrival counters, chosen when it saves waves; grid_x or grid_y
+ *  chosen when it saves waves; grid_x or grid_y
  *  then counts 256-row tiles),
  *  compact (1: a fused call captured into a graph, when it starts beside the
  *  launch before it or heads such a run, takes the compact layout: the same

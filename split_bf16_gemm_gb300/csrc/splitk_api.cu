@@ -93,8 +93,6 @@ int validate_gemm(const void *A, const void *B, int64_t M, int64_t N, int64_t K,
     return SPLITK_OK;
 }
 
-size_t counter_bytes(int64_t M, int64_t N);
-
 // The partial pass into P (and, when `out` is given, the split sum too).
 // `prefetch` lets the CTAs that start beside the previous launch prefetch the
 // operands into L2.  Only the fused launch uses it: before a partial pass
@@ -104,7 +102,7 @@ size_t counter_bytes(int64_t M, int64_t N);
 // to an SM) when it may start beside the launch before it, or heads a run of
 // launches that may; a partial pass followed by the reduce keeps the full
 // ring, since the reduce's blocks leave no room for a second CTA.
-int run_partial_pass(const void *A, const void *B, float *P, float *out, unsigned *counters, int64_t M, int64_t N,
+int run_partial_pass(const void *A, const void *B, float *P, float *out, int64_t M, int64_t N,
                      int64_t K, int64_t S, int64_t kps, int dtype, bool fused, bool prefetch, bool b_kn,
                      bool allow_compact, cudaStream_t stream)
 {
@@ -112,7 +110,7 @@ int run_partial_pass(const void *A, const void *B, float *P, float *out, unsigne
         return cuda_status(splitk::launch_simt_f32(static_cast<const float *>(A), static_cast<const float *>(B), P,
                                                    M, N, K, S, kps, b_kn, stream));
     }
-    GemmProblem pr{A, B, P, out, counters, M, N, K, S, kps, dtype == SPLITK_BF16};
+    GemmProblem pr{A, B, P, out, M, N, K, S, kps, dtype == SPLITK_BF16};
     pr.b_kn = b_kn;
     pr.f32 = dtype == SPLITK_F32;   // 3xTF32 on the tensor cores
     const int e = elem_bytes(dtype);
@@ -129,22 +127,27 @@ int run_partial_pass(const void *A, const void *B, float *P, float *out, unsigne
     int nw = 0;
     if (P) writes[nw++] = splitk::span_of(P, static_cast<uint64_t>(S * M * N) * 4);
     if (out) writes[nw++] = splitk::span_of(out, static_cast<uint64_t>(M * N) * 4);
-    if (counters && plan.split_sum == 1) writes[nw++] = splitk::span_of(counters, counter_bytes(M, N));
-    chain.commit(writes, nw, err == cudaSuccess);
+    chain.commit(writes, nw, err == cudaSuccess, !pr.overlap);
     splitk::note_launch({pr.overlap ? 1 : 0, plan.compact, chain.capturing() ? 1 : 0, plan.bn, plan.chunks,
                          plan.stages, plan.kbs, static_cast<int>(plan.smem_bytes)});
     return cuda_status(err);
 }
 
-// The accumulation pass, recorded in the capture chain as a launch that waits
-// at its start (it reads what the partial pass before it wrote).
+// The accumulation pass.  After the partial pass it reads what that pass
+// wrote, so it waits for it; a reduce whose partials no running launch
+// writes (inside a capture) loads them at once.  It lets the next launch
+// start as soon as its own blocks have started (the next partial pass then
+// loads under it), except where no run of this library's launches precedes
+// it in a capture: there it releases the next launch after its wait and
+// heads a new run.
 int run_reduce(const float *P, float *out, int64_t S, int64_t M, int64_t N, cudaStream_t stream)
 {
     const splitk::Span reads[1] = {splitk::span_of(P, static_cast<uint64_t>(S * M * N) * 4)};
     splitk::ChainGuard chain(stream, reads, 1);
-    const cudaError_t err = splitk::launch_reduce(P, out, S, M * N, stream);
+    const bool head = chain.capturing() && chain.fresh();
+    const cudaError_t err = splitk::launch_reduce(P, out, S, M * N, chain.overlap(), !head, stream);
     const splitk::Span writes[1] = {splitk::span_of(out, static_cast<uint64_t>(M * N) * 4)};
-    chain.commit(writes, 1, err == cudaSuccess);
+    chain.commit(writes, 1, err == cudaSuccess, head);
     return cuda_status(err);
 }
 
@@ -152,12 +155,24 @@ int run_reduce(const float *P, float *out, int64_t S, int64_t M, int64_t N, cuda
 // runs on the CUDA cores and always takes the two-kernel path.
 bool fused_possible(int dtype, bool b_kn) { return !(dtype == SPLITK_F32 && b_kn); }
 
-size_t partials_bytes(int64_t M, int64_t N, int64_t S) { return static_cast<size_t>(S * M * N) * 4; }
-
-size_t counter_bytes(int64_t M, int64_t N)
+// Whether gemm_bt(fused != 0) sums the splits inside its launch.  It does
+// where the tile plan holds all of a tile's splits in one resident cluster,
+// except for F32 operands (3xTF32) with M <= 32: there the cluster that sums
+// the splits is larger than the partial pass's own (every split's chunks,
+// against one split's), its exchange moves the whole 128-row accumulator of
+// which at most 32 rows are live, and on GB300 the two kernels measured
+// faster (M32 N512 K2048, 2 to 8 splits: 5.6-5.8 against 7.0-7.2 us).
+bool sums_in_kernel(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, int dtype, bool b_kn)
 {
-    return (static_cast<size_t>(splitk::fused_counter_count(M, N)) * 4 + 15) / 16 * 16;
+    if (!fused_possible(dtype, b_kn)) return false;
+    const bool x3 = dtype == SPLITK_F32;
+    const TilePlan f = splitk::plan_tc(M, N, K, S, kps, true, x3);
+    if (f.split_sum != 2) return false;
+    if (x3 && M <= 32 && f.cluster > splitk::plan_tc(M, N, K, S, kps, false, x3).cluster) return false;
+    return true;
 }
+
+size_t partials_bytes(int64_t M, int64_t N, int64_t S) { return static_cast<size_t>(S * M * N) * 4; }
 
 }  // namespace
 
@@ -183,8 +198,6 @@ int check_gemm_bt(const void *A, const void *B, const float *out, const void *wo
     return SPLITK_OK;
 }
 
-size_t counters_offset(int64_t M, int64_t N, int64_t splits) { return partials_bytes(M, N, splits); }
-
 }  // namespace splitk
 
 extern "C" {
@@ -206,8 +219,8 @@ static int gemm_splitk_impl(const void *A, const void *B, float *partials, int64
     const Range rb = range_of(B, static_cast<uint64_t>(N * K) * e);
     const Range rp = range_of(partials, static_cast<uint64_t>(splits * M * N) * 4);
     if (overlap(rp, ra) || overlap(rp, rb)) return SPLITK_ERR_ALIAS;
-    return run_partial_pass(A, B, partials, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false, false,
-                            b_kn, false, static_cast<cudaStream_t>(stream));
+    return run_partial_pass(A, B, partials, nullptr, M, N, K, splits, k_per_split, dtype, false, false, b_kn,
+                            false, static_cast<cudaStream_t>(stream));
 }
 
 int gemm_splitk_bt(const void *A, const void *B, float *partials, int64_t M, int64_t N, int64_t K, int64_t splits,
@@ -251,7 +264,7 @@ size_t gemm_bt_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t splits, 
 {
     (void)fused;
     if (geometry_status(M, N, K, splits, k_per_split) != SPLITK_OK) return 0;
-    return partials_bytes(M, N, splits) + counter_bytes(M, N);
+    return partials_bytes(M, N, splits);
 }
 
 int gemm_bt_workspace_init(void *workspace, size_t workspace_bytes, void *stream)
@@ -270,22 +283,20 @@ static int gemm_impl(const void *A, const void *B, float *out, void *workspace, 
     if (st != SPLITK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float *P = static_cast<float *>(workspace);
-    unsigned *counters = reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + partials_bytes(M, N, splits));
     // The fused launch sums the splits inside its clusters.  Where the plan
-    // cannot hold a tile's splits in one resident cluster, the sum would go
-    // through arrival counters and an L2 read-back, which measured slower on
-    // GB300 than the separate reduce in every such case (for example BF16
-    // M256 N1024 K2048 with 8 splits: 17.9 against 7.0 us); those calls run as
-    // the two kernels instead.  The chunks do not depend on `fused`, so the
-    // result is the same either way, bit for bit.
-    if (fused && fused_possible(dtype, b_kn) &&
-        splitk::plan_tc(M, N, K, splits, k_per_split, true, dtype == SPLITK_F32).split_sum == 2) {
+    // cannot hold a tile's splits in one resident cluster, the call runs the
+    // two kernels: summing through global memory instead (arrival counters,
+    // the last split reading the others' partials back from L2) measured
+    // slower on GB300 than the separate reduce in every such case (BF16 M256
+    // N1024 K2048 with 8 splits: 17.9 against 7.0 us).  The chunks do not
+    // depend on `fused`, so the result is the same either way, bit for bit.
+    if (fused && sums_in_kernel(M, N, K, splits, k_per_split, dtype, b_kn)) {
         // fused == 1 keeps no partials
         float *keep = fused == 1 ? nullptr : P;
-        return run_partial_pass(A, B, keep, out, counters, M, N, K, splits, k_per_split, dtype, true, true, b_kn,
+        return run_partial_pass(A, B, keep, out, M, N, K, splits, k_per_split, dtype, true, true, b_kn,
                                 true, s);
     }
-    st = run_partial_pass(A, B, P, nullptr, nullptr, M, N, K, splits, k_per_split, dtype, false, false, b_kn, false,
+    st = run_partial_pass(A, B, P, nullptr, M, N, K, splits, k_per_split, dtype, false, false, b_kn, false,
                           s);
     if (st != SPLITK_OK) return st;
     return run_reduce(P, out, splits, M, N, s);
@@ -356,8 +367,7 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
     const bool x3 = dtype == SPLITK_F32;
     // gemm_bt runs the two kernels where the fused launch could not sum a
     // tile's splits inside one resident cluster
-    const bool in_kernel = fused != 0 && fused_possible(dtype, false) &&
-                           splitk::plan_tc(M, N, K, splits, k_per_split, true, x3).split_sum == 2;
+    const bool in_kernel = fused != 0 && sums_in_kernel(M, N, K, splits, k_per_split, dtype, false);
     const TilePlan p = splitk::plan_tc(M, N, K, splits, k_per_split, in_kernel, x3);
     info[0] = x3 ? 2 : 0;
     info[1] = p.bn;

@@ -12,14 +12,16 @@
 // first store ("overlap").
 //
 // Which launches can still be running when an overlapping launch starts:
-// a launch that waited at its start (a "head") lets the next grid start only
-// after that wait returned, so everything before the head has finished; an
-// overlapping launch lets the next grid start as soon as its own CTAs have
-// started.  So a launch can meet every launch from the last head on, and the
-// window it is checked against is exactly that run: [head, ..., previous].
-// Every launch also waits for the previous grid before its first store, so
-// the grids finish in order and no launch overwrites what an earlier one
-// still reads.
+// a "head" -- a launch that waits at its start and lets the next grid start
+// only after that wait returned -- guarantees that everything before it has
+// finished when its successor starts; every other launch (an overlapping
+// one, or a reduce after a partial pass, which waits for its partials but
+// lets the next grid start at once) lets the next grid start as soon as its
+// own CTAs have started.  So a launch can meet
+// every launch from the last head on, and the window it is checked against
+// is exactly that run: [head, ..., previous].  Every launch also waits for
+// the previous grid before its first store, so the grids finish in order and
+// no launch overwrites what an earlier one still reads.
 //
 // Eager launches (no capture) always wait: the library cannot see what else
 // the caller put on the stream.  splitk_set_overlap(0) turns the mechanism off.
@@ -120,7 +122,7 @@ ChainGuard::ChainGuard(cudaStream_t stream, const Span *reads, int n_reads) : st
     overlap_ = true;
 }
 
-void ChainGuard::commit(const Span *writes, int n_writes, bool launched)
+void ChainGuard::commit(const Span *writes, int n_writes, bool launched, bool head)
 {
     if (!capturing_) return;
     cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
@@ -135,8 +137,17 @@ void ChainGuard::commit(const Span *writes, int n_writes, bool launched)
         if (c) c->used = false;   // unknown state: the next launch waits and starts afresh
         return;
     }
-    if (!c) c = make_chain(id_);
-    if (!overlap_ || c->n >= kWindow) c->n = 0;   // a launch that waited at its start heads the window
+    if (head) {
+        if (!c) c = make_chain(id_);
+        c->n = 0;                  // everything before it has finished when its successor starts
+    } else if (!c || fresh_ || c->n >= kWindow) {
+        // A launch that lets its successor start early can only extend a run
+        // that a head began: after anything else (another kernel, a copy) its
+        // successor could meet work the library cannot see.  The next launch
+        // then waits and heads a new run.
+        if (c) c->used = false;
+        return;
+    }
     Entry &e = c->e[c->n++];
     e.node = deps[0];
     e.n_writes = n_writes;

@@ -16,7 +16,6 @@ struct GemmProblem {
     const void *B;      // [N,K] row-major, 16-bit elements; with b_kn, the weight [K,N] row-major
     float *P;           // [S,M,N] partials, or nullptr when not written
     float *out;         // [M,N] sum over splits, or nullptr (two-kernel path)
-    unsigned *counters; // fused: per (tile, cluster rank) arrival counters, zero between calls
     int64_t M, N, K, S, kps;
     bool bf16;          // operand type: BF16 (true) or F16 (false)
     bool b_kn = false;  // B given as the [K,N] weight itself (read MN-major)
@@ -38,7 +37,7 @@ struct TilePlan {
     int three_d;        // stages loaded as one 3-D box per operand (K, kps, chunk_len multiples of 64)
     int cluster;        // CTAs per cluster along grid z (chunks, or splits * chunks)
     int fused;          // this launch also sums over splits
-    int split_sum;      // 0 none, 1 by arrival counters, 2 inside the cluster (cluster = splits * chunks)
+    int split_sum;      // 0 none, 2 inside the cluster (cluster = splits * chunks)
     int share;          // 16-byte pieces of the tile each cluster rank owns
     uint32_t region0;   // bytes of the stage ring / accumulator staging
     int prefetchers;    // CTAs (the first in dispatch order) that prefetch A and B into L2
@@ -57,10 +56,6 @@ constexpr int kMaxStages = 8;
 constexpr int kMaxKbs = 4;     // k-blocks in one pipeline stage (one TMA box per operand)
 constexpr int kMaxChunks = 8;  // portable cluster size
 
-// Arrival counters the fused path needs in the workspace, after the partials:
-// one per (128 x 64 tile column block, row block, chunk), the most any plan uses.
-inline int64_t fused_counter_count(int64_t M, int64_t N) { return (N / 64) * ((M + kTileM - 1) / kTileM) * kMaxChunks; }
-
 // Tile choice for a shape (automatic, or the process-wide override).
 // x3: F32 operands as 3xTF32 (else 16-bit operands).
 // compact: the layout that lets two CTAs share an SM, where that plan exists
@@ -76,7 +71,10 @@ void set_tile_override(int bn, int chunks, int kbs);
 cudaError_t launch_tc(const GemmProblem &p, const TilePlan &plan, cudaStream_t stream);
 cudaError_t launch_simt_f32(const float *A, const float *B, float *P, int64_t M, int64_t N, int64_t K,
                             int64_t S, int64_t kps, bool b_kn, cudaStream_t stream);
-cudaError_t launch_reduce(const float *P, float *out, int64_t S, int64_t count, cudaStream_t stream);
+// overlap: nothing that can still be running writes P (splitk_chain.cu);
+// release_first: let the next grid start before waiting for the previous one
+cudaError_t launch_reduce(const float *P, float *out, int64_t S, int64_t count, bool overlap, bool release_first,
+                          cudaStream_t stream);
 cudaError_t launch_prepare(const void *W, void *B, int64_t K, int64_t N, int elem_bytes, cudaStream_t stream);
 
 // A byte range [lo, hi) of device memory that a launch reads or writes.
@@ -105,8 +103,10 @@ public:
     // no earlier launch of this library precedes it in the capture (or the
     // window was full): a head that independent launches may follow
     bool fresh() const { return fresh_; }
-    // after the launch: record its writes (or forget the chain if it failed)
-    void commit(const Span *writes, int n_writes, bool launched);
+    // after the launch: record its writes (or forget the chain if it
+    // failed); `head`: it waited for the previous grid before letting the
+    // next one start, so nothing before it can still be running then
+    void commit(const Span *writes, int n_writes, bool launched, bool head);
 
 private:
     cudaStream_t stream_;
@@ -125,10 +125,9 @@ void note_launch(const LaunchRecord &r);
 LaunchRecord last_launch();
 
 // gemm_bt's argument checks (status as gemm_bt returns it; nothing launched),
-// and where the fused path's counters start in its workspace.
+
 int check_gemm_bt(const void *A, const void *B, const float *out, const void *workspace, size_t workspace_bytes,
                   int64_t M, int64_t N, int64_t K, int64_t splits, int64_t k_per_split, int dtype, int fused);
-size_t counters_offset(int64_t M, int64_t N, int64_t splits);
 
 // Last-error record (per host thread): what failed and the CUDA error or
 // driver result it returned.  note_error passes `e` through.

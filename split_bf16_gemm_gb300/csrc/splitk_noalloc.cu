@@ -9,14 +9,14 @@
 // every GPU loading the library holds until the process exits.
 //
 // The array is shared by every call on a device and keeps the last call's
-// contents; the parts that must start at zero (the fused path's arrival
-// counters) are cleared at the start of each call.  Calls whose executions
-// overlap on the GPU (for instance on two streams) race on the array.
+// contents (the partials; gemm_bt needs nothing zeroed).  Calls on one stream
+// stay ordered (every launch waits for the one before it before its first
+// store, inside graph captures too); calls whose executions overlap on the
+// GPU (for instance on two streams) race on the array.
 
 #include <cuda_runtime.h>
 
 #include <cstdio>
-#include <mutex>
 
 #include "splitk.h"
 #include "splitk_internal.h"
@@ -25,37 +25,23 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SPLITK_NOALLOC_MAX_BYTES];
 
-// Device address of the array on each device.  In host code the array's name
-// is only a host-side stand-in, so the address comes from
-// cudaGetSymbolAddress, called once per device with that device current.
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void *g_scratch[kMaxDevices] = {};
-
+// Device address of the array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress with the device current.  It is looked up on every
+// call (a lookup; it allocates nothing) rather than kept: after a device
+// reset, or once the primary context is torn down and made again, the array
+// may sit at another address.  The first call on a device also loads the
+// library's device code there.
 int scratch_for_current_device(void **ptr)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
-        splitk::note_error(e, "cudaGetDevice");
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+        splitk::note_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol,
+                           "cudaGetSymbolAddress(no-allocation scratch)");
         return SPLITK_ERR_CUDA;
     }
-    if (dev < 0 || dev >= kMaxDevices) {
-        splitk::note_message("gemm_bt_noalloc: device index beyond the supported range", dev);
-        return SPLITK_ERR_CUDA;
-    }
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p) {
-            splitk::note_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol,
-                               "cudaGetSymbolAddress(no-allocation scratch)");
-            return SPLITK_ERR_CUDA;
-        }
-        g_scratch[dev] = p;
-    }
-    *ptr = g_scratch[dev];
+    *ptr = p;
     return SPLITK_OK;
 }
 
@@ -77,15 +63,5 @@ extern "C" int gemm_bt_noalloc(const void *A, const void *B, float *out, int64_t
     void *scratch = nullptr;
     const int st = scratch_for_current_device(&scratch);
     if (st != SPLITK_OK) return st;
-    if (fused) {
-        // the arrival counters follow the partials and must start at zero
-        const size_t partials = static_cast<size_t>(splits * M * N) * 4;
-        const cudaError_t e = cudaMemsetAsync(static_cast<char *>(scratch) + partials, 0, need - partials,
-                                              static_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) {
-            splitk::note_error(e, "cudaMemsetAsync(no-allocation counters)");
-            return SPLITK_ERR_CUDA;
-        }
-    }
     return gemm_bt(A, B, out, scratch, need, M, N, K, splits, k_per_split, dtype, fused, stream);
 }

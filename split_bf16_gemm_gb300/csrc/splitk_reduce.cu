@@ -10,6 +10,12 @@
 // multiple of the SM count with a grid-stride loop.  Launched as a
 // programmatic dependent of the partial pass: its blocks start while the
 // partial pass finishes and wait (griddepcontrol.wait) for it before reading.
+// With `release_first` each block lets the next grid start at once (the
+// next partial pass then loads its operands while this one sums, where it
+// may: splitk_chain.cu); otherwise only after its wait, which makes it the
+// head of a run of launches that may overlap.  With `overlap` (no running
+// launch writes P) the blocks load at once and wait for the previous grid
+// only before their stores.
 
 #include "ptx.cuh"
 #include "splitk_internal.h"
@@ -26,10 +32,12 @@ __device__ __forceinline__ float4 ld_stream(const float4 *p)
 }
 
 __global__ void __launch_bounds__(kReduceThreads)
-    reduce_v4_kernel(const float4 *__restrict__ P, float4 *__restrict__ out, int S, int64_t n4)
+    reduce_v4_kernel(const float4 *__restrict__ P, float4 *__restrict__ out, int S, int64_t n4, int overlap,
+                     int release_first)
 {
-    ptx::grid_dependency_wait();   // the partials may be the previous grid's output
-    ptx::launch_dependents();
+    if (release_first) ptx::launch_dependents();
+    if (!overlap) ptx::grid_dependency_wait();   // the partials may be the previous grid's output
+    ptx::launch_dependents();                    // (a second invocation changes nothing)
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kReduceThreads;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kReduceThreads + threadIdx.x; i < n4; i += stride) {
         float4 acc = ld_stream(P + i);
@@ -47,20 +55,24 @@ __global__ void __launch_bounds__(kReduceThreads)
             const float4 v = ld_stream(P + static_cast<int64_t>(s) * n4 + i);
             acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
         }
+        if (overlap) ptx::grid_dependency_wait();   // the previous grid may still read `out`
         out[i] = acc;
     }
 }
 
 // Any element count: the same sums one float at a time.
 __global__ void __launch_bounds__(kReduceThreads)
-    reduce_scalar_kernel(const float *__restrict__ P, float *__restrict__ out, int S, int64_t n)
+    reduce_scalar_kernel(const float *__restrict__ P, float *__restrict__ out, int S, int64_t n, int overlap,
+                         int release_first)
 {
-    ptx::grid_dependency_wait();
+    if (release_first) ptx::launch_dependents();
+    if (!overlap) ptx::grid_dependency_wait();
     ptx::launch_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kReduceThreads;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kReduceThreads + threadIdx.x; i < n; i += stride) {
         float acc = P[i];
         for (int s = 1; s < S; ++s) acc += P[static_cast<int64_t>(s) * n + i];
+        if (overlap) ptx::grid_dependency_wait();
         out[i] = acc;
     }
 }
@@ -75,7 +87,8 @@ int sm_count()
 
 }  // namespace
 
-cudaError_t launch_reduce(const float *P, float *out, int64_t S, int64_t count, cudaStream_t stream)
+cudaError_t launch_reduce(const float *P, float *out, int64_t S, int64_t count, bool overlap, bool release_first,
+                          cudaStream_t stream)
 {
     static thread_local int sms = 0;
     if (sms == 0) sms = sm_count();
@@ -99,9 +112,11 @@ cudaError_t launch_reduce(const float *P, float *out, int64_t S, int64_t count, 
     cudaError_t e;
     if (vec)
         e = cudaLaunchKernelEx(&cfg, reduce_v4_kernel, reinterpret_cast<const float4 *>(P),
-                               reinterpret_cast<float4 *>(out), static_cast<int>(S), items);
+                               reinterpret_cast<float4 *>(out), static_cast<int>(S), items, overlap ? 1 : 0,
+                               release_first ? 1 : 0);
     else
-        e = cudaLaunchKernelEx(&cfg, reduce_scalar_kernel, P, out, static_cast<int>(S), items);
+        e = cudaLaunchKernelEx(&cfg, reduce_scalar_kernel, P, out, static_cast<int>(S), items, overlap ? 1 : 0,
+                               release_first ? 1 : 0);
     if (e != cudaSuccess) return note_error(e, "reduce kernel launch");
     return note_error(cudaGetLastError(), "reduce kernel launch");
 }

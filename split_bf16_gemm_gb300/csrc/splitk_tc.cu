@@ -41,11 +41,6 @@
 // the contributions in rank order from its own shared memory -- chunks in
 // chunk order, then splits in split order, the separate reduce kernel's sums
 // -- so the result does not depend on arrival order.
-// Fused mode with more splits than one cluster holds: after storing its share
-// of partials[s], the owner counts its arrival on a per-(tile, rank) counter;
-// the last of the `splits` owners of that piece of the tile reads the other
-// splits' partials back (L2) and adds them in split order, then stores
-// out[m,n].  The counter wraps to zero, ready for the next call.
 //
 // Programmatic dependent launch: the kernel waits for the previous grid (whose
 // writes it may read) before its first load, and lets the next grid start its
@@ -79,16 +74,13 @@ namespace {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s; a launch normally takes microseconds
 constexpr int kThreads = 256;                     // 8 warps: two per tensor-memory lane quarter
-constexpr int kPieceBatch = 2;                     // split sum by counters: pieces per thread per pass,
-constexpr int kSplitBatch = 8;                     //   and splits whose loads are in flight together
 
 struct TcArgs {
     float *P;              // [S,M,N] partials (nullptr: not kept, when the cluster sums the splits)
     float *out;            // [M,N], or nullptr when the splits are not summed here
-    unsigned *counters;    // per (tile, chunk) arrival counters (split sum by counters)
     int M, N, K, S, kps;
     int chunks, chunk_len, stages;
-    int split_sum;         // 0: none; 1: by arrival counters; 2: inside the cluster (cluster = splits x chunks)
+    int split_sum;         // 0: none; 2: inside the cluster (cluster = splits x chunks)
     int kbs;               // 64-wide k-blocks per pipeline stage
     int three_d;           // operands loaded as 3-D boxes of kbs k-blocks (else 2-D, kbs == 1)
     int share;             // 16-byte pieces owned by each cluster rank (a multiple of 8)
@@ -244,7 +236,7 @@ __device__ __forceinline__ void cluster_split_sum_for(int C, const uint32_t (&rb
 // KN: B is the [K,N] weight (MN-major operand).  X3: F32 operands, each
 // product formed as three TF32 products (hi*lo + lo*hi + hi*hi).  TM: rows
 // of A per CTA; 256 only for 16-bit operands, BN = 256 and one CTA per tile
-// that keeps or sums its own partials (no cluster, no arrival counters).
+// that keeps or sums its own partials (no cluster).
 template <int BN, int Q, bool KN, bool X3, int TM = kTileM>
 __global__ void __launch_bounds__(kThreads, 2)
     tc_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -260,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ __align__(8) uint64_t bars[3 * kMaxStages + 2];
     __shared__ uint32_t tmem_slot;
     __shared__ int issued_s, consumed_s;
-    __shared__ unsigned abort_s, last_s;
+    __shared__ unsigned abort_s;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int stages = args.stages;
@@ -339,7 +331,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         issued_s = 0;
         consumed_s = 0;
         abort_s = 0;
-        last_s = 0;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
         const uint32_t incoming = static_cast<uint32_t>((Q - 1) * (my_hi - my_lo)) * 16u;
@@ -375,12 +366,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     // arrival itself needs no release semantics.  With the receive slots in
     // the ring, this CTA arrives only once its MMAs have read the ring.
     if (Q > 1 && !args.recv_in_ring) ptx::cluster_arrive_relaxed();
-    if (args.overlap) {
-        if (tid == 0) ptx::launch_dependents();   // the first invocation in a CTA counts
-    } else {
-        ptx::grid_dependency_wait();
-        ptx::launch_dependents();
-    }
+    // Overlapping, the next grid is released at once; otherwise after the
+    // wait.  (Written as one conditional wait and an unconditional release:
+    // the same choice as two branches measured 0.1-0.4 us slower per launch
+    // on GB300, in both modes.)
+    if (!args.overlap) ptx::grid_dependency_wait();
+    ptx::launch_dependents();
     const uint32_t tmem = tmem_slot;
 
     if (warp == 0 && lane == 0) {
@@ -635,83 +626,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         } else {
             cluster_split_sum_for<Q, false>(C, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, nullptr,
                                             args.out);
-        }
-
-        // ---- split sum by counters: the last split to finish this piece range
-        // adds all splits (Q == C here)
-        if (args.split_sum == 1) {
-            // the CTA's partials are all written (the barrier); thread 0's arrival
-            // count publishes them (release, cumulative over what the barrier
-            // ordered before it) and, for the last arriver, acquires the other
-            // splits' partials, which the second barrier passes on to all threads
-            __syncthreads();
-            if (tid == 0) {
-                const unsigned idx = (static_cast<unsigned>(m_tile) * (args.N / BN) + n_tile) * C + c;   // c == rank
-                const unsigned old = ptx::atom_inc_acq_rel_gpu(&args.counters[idx], static_cast<unsigned>(args.S - 1));
-                last_s = old == static_cast<unsigned>(args.S - 1) ? 1u : 0u;
-            }
-            __syncthreads();
-            if (last_s) {
-                // kPieceBatch pieces per thread, the loads of kSplitBatch splits
-                // in flight at once (one L2 round trip per kSplitBatch splits,
-                // not per split); the adds still run in split order 0..S-1.  With
-                // one CTA per split (Q == 1) it owns the whole tile and walks only
-                // the pieces of rows below M (a quarter of them when M is 32).
-                const int rows_here = Q == 1 ? min(kTileM, args.M - row0) : kTileM;
-                const int walk_hi = Q == 1 ? rows_here * (BN / 4) : my_hi;
-                auto owned = [&](int t) {           // t-th owned piece, as a piece index
-                    if (Q > 1) return t;
-                    const int r = t / (BN / 4), cq = t % (BN / 4);
-                    return (((cq >> 3) << 2) | (r >> 5)) << 8 | (r & 31) << 3 | (cq & 7);
-                };
-                for (int g0 = (Q == 1 ? 0 : my_lo) + tid; g0 < walk_hi; g0 += kPieceBatch * kThreads) {
-                    float4 tot[kPieceBatch];
-                    for (int sp0 = 0; sp0 < args.S; sp0 += kSplitBatch) {
-                        float4 v[kSplitBatch][kPieceBatch];
-#pragma unroll
-                        for (int j = 0; j < kSplitBatch; ++j) {
-#pragma unroll
-                            for (int i = 0; i < kPieceBatch; ++i) {
-                                const int t = g0 + i * kThreads, sp = sp0 + j;
-                                v[j][i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                                if (t < walk_hi && sp < args.S) {
-                                    const Piece p = piece_at(owned(t));
-                                    const int row = row0 + p.row;
-                                    if (sp == s) {
-                                        float4 w[Q];
-                                        gather(p, w);
-                                        v[j][i] = chunk_sum(w);
-                                    } else if (row < args.M) {
-                                        v[j][i] = __ldcg(reinterpret_cast<const float4 *>(
-                                            args.P + sp * MN + static_cast<size_t>(row) * args.N + col0 + p.col));
-                                    }
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int j = 0; j < kSplitBatch; ++j) {
-#pragma unroll
-                            for (int i = 0; i < kPieceBatch; ++i) {
-                                if (sp0 + j == 0)
-                                    tot[i] = v[j][i];
-                                else if (sp0 + j < args.S)
-                                    add4(tot[i], v[j][i]);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < kPieceBatch; ++i) {
-                        const int t = g0 + i * kThreads;
-                        if (t < walk_hi) {
-                            const Piece p = piece_at(owned(t));
-                            const int row = row0 + p.row;
-                            if (row < args.M)
-                                *reinterpret_cast<float4 *>(args.out + static_cast<size_t>(row) * args.N + col0 +
-                                                            p.col) = tot[i];
-                        }
-                    }
-                }
-            }
         }
     }
     if (Q > 1) ptx::cluster_wait();            // no CTA leaves while its staging may still be copied from
@@ -1039,16 +953,7 @@ double estimate_tc_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, b
     const TilePlan p = plan_tc(M, N, K, S, kps, fused, x3);
     // fixed cost of a launch behind another: the dependency hand-off and the
     // first stage landing (about 2.3 us on GB300)
-    double t = 2.3 + model_us(M, N, S, p.bn, p.chunks, p.chunk_len, p.cluster, x3 ? 4 : 2);
-    if (p.split_sum == 1) {
-        // the last split of each piece range reads the others' partials back:
-        // about 1 us of fence and arrival, one L2 round trip (0.7 us) per 8
-        // splits, and the bytes at about 60 GB/s into that CTA
-        const double rows = static_cast<double>(std::min<int64_t>(M, kTileM));
-        const double bytes = static_cast<double>(S - 1) * rows * p.bn * 4 / p.chunks;
-        t += 1.0 + 0.7 * static_cast<double>((S + 7) / 8) + bytes / 6.0e4;
-    }
-    return t;
+    return 2.3 + model_us(M, N, S, p.bn, p.chunks, p.chunk_len, p.cluster, x3 ? 4 : 2);
 }
 
 namespace {
@@ -1104,9 +1009,9 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     const int64_t mt = (M + kTileM - 1) / kTileM;
     // Tile width and chunks per split: the cheapest by the model, with a
     // penalty where the splits of a tile cannot share one resident cluster of
-    // a power-of-two size (the fused path then sums them through global
-    // memory).  The choice does not
-    // depend on `fused`, so both paths add the same chunks in the same order.
+    // a power-of-two size (a fused call then runs the separate reduce).  The
+    // choice does not depend on `fused`, so both paths add the same chunks in
+    // the same order.
     int best_bn = 0, best_c = 0;
     double best = 1e30;
     for (int bn : {64, 128, 256}) {
@@ -1143,10 +1048,12 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     chunk_len = (chunk_len + grain - 1) / grain * grain;
     const int nkb = static_cast<int>((chunk_len + kb_elems - 1) / kb_elems);
     const int64_t tiles = mt * (N / bn);
+    // A fused launch sums the splits inside its clusters, which must then hold
+    // every split and chunk of a tile and all be resident at once; where that
+    // fails the plan is not fused (split_sum 0) and gemm_bt runs the reduce.
     int q = chunks, split_sum = 0;
     if (fused) {
         const int sq = static_cast<int>(S) * chunks;
-        split_sum = 1;
         if (sq <= kMaxChunks && (sq & (sq - 1)) == 0 && (sq == 1 || tiles <= resident_clusters(sq)) &&
             pick_stages(bn, nkb, can3d, sq, share_for(bn, sq), x3).ok) {
             q = sq;
@@ -1163,7 +1070,7 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     // CTA per tile that keeps or sums its own partials, with BN = 256 and
     // 16-bit operands.
     int tm = kTileM;
-    if (!x3 && bn == 256 && q == 1 && split_sum != 1 && mt > 1) {
+    if (!x3 && bn == 256 && q == 1 && mt > 1) {
         const int64_t per_row_tile = (N / bn) * S;
         const double waves1 = std::ceil(static_cast<double>(mt * per_row_tile) / resident_clusters(1));
         const double waves2 = std::ceil(static_cast<double>((mt + 1) / 2 * per_row_tile) / resident_clusters(1));
@@ -1179,7 +1086,7 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     p.stages = sc.stages;
     p.kbs = can3d ? sc.kbs : 1;
     p.three_d = can3d && p.kbs > 1 ? 1 : 0;
-    p.fused = fused ? 1 : 0;
+    p.fused = split_sum == 2 ? 1 : 0;
     p.split_sum = split_sum;
     p.cluster = q;
     p.share = share;
@@ -1252,14 +1159,14 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
     if (plan.cluster > kMaxChunks || plan.stages > kMaxStages || plan.kbs < 1 || plan.kbs > kMaxKbs ||
         plan.smem_bytes > kSmemLimit || !chunks_ok)
         return note_error(cudaErrorInvalidConfiguration, "tile plan out of range");
-    if (plan.fused && (pr.out == nullptr || (plan.split_sum == 1 && pr.counters == nullptr)))
-        return note_error(cudaErrorInvalidValue, "fused launch without output or counters");
+    if (plan.fused && (pr.out == nullptr || plan.split_sum != 2))
+        return note_error(cudaErrorInvalidValue, "fused launch without output or cluster split sum");
     if (pr.P == nullptr && plan.split_sum != 2)
         return note_error(cudaErrorInvalidValue, "partials are needed unless the cluster sums the splits");
     if (pr.f32 && (pr.b_kn || !plan.x3))
         return note_error(cudaErrorInvalidValue, "F32 operands need a 3xTF32 plan and the [N,K] weight");
     const bool tile_m_ok = plan.tile_m == kTileM || (plan.tile_m == 2 * kTileM && plan.bn == 256 &&
-                                                     plan.cluster == 1 && plan.split_sum != 1 && !plan.x3);
+                                                     plan.cluster == 1 && !plan.x3);
     if (!tile_m_ok) return note_error(cudaErrorInvalidConfiguration, "256-row tile plan out of range");
     if (plan.recv_in_ring && static_cast<size_t>(kTileM) * plan.bn * 4 +
                                  static_cast<size_t>(plan.cluster - 1) * plan.share * 16 >
@@ -1280,7 +1187,6 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
     TcArgs a = {};
     a.P = pr.P;
     a.out = plan.fused ? pr.out : nullptr;
-    a.counters = plan.split_sum == 1 ? pr.counters : nullptr;
     a.split_sum = plan.split_sum;
     a.M = static_cast<int>(pr.M);
     a.N = static_cast<int>(pr.N);

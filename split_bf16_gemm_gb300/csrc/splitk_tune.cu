@@ -133,17 +133,10 @@ int splitk_autotune_splits(const void *A, const void *B, float *out, void *works
         !cuda(cudaStreamWaitEvent(ts, ready, 0), "cudaStreamWaitEvent")) {
         // fall through to clean-up
     }
-    char *const ws = static_cast<char *>(workspace);
-    auto zero_counters = [&](int i) {
-        const size_t off = splitk::counters_offset(M, N, cs[i]);
-        const size_t need = gemm_bt_workspace_bytes(M, N, K, cs[i], ck[i], fused);
-        return cuda(cudaMemsetAsync(ws + off, 0, need - off, ts), "cudaMemsetAsync(counters)");
-    };
     float best = 3.0e38f;
     int bi = -1;
     for (int i = 0; i < kCandidates && rc == SPLITK_OK; ++i) {
         if (!run[i]) continue;
-        if (fused && !zero_counters(i)) break;
         const int w = gemm_bt(A, B, out, workspace, workspace_bytes, M, N, K, cs[i], ck[i], dtype, fused, ts);
         if (w != SPLITK_OK) {
             rc = w;
@@ -179,12 +172,9 @@ int splitk_autotune_splits(const void *A, const void *B, float *out, void *works
         if (rc == SPLITK_OK && splitk_get_device_status(ts) != SPLITK_OK) rc = SPLITK_ERR_DEVICE_TIMEOUT;
     }
     if (rc == SPLITK_OK && bi >= 0) {
-        // leave `out` holding the chosen split's result and, for the fused
-        // path, the chosen split's counters zero for later gemm_bt calls
-        if (!fused || zero_counters(bi)) {
-            const int w = gemm_bt(A, B, out, workspace, workspace_bytes, M, N, K, cs[bi], ck[bi], dtype, fused, ts);
-            if (w != SPLITK_OK) rc = w;
-        }
+        // leave `out` holding the chosen split's result
+        const int w = gemm_bt(A, B, out, workspace, workspace_bytes, M, N, K, cs[bi], ck[bi], dtype, fused, ts);
+        if (w != SPLITK_OK) rc = w;
         cuda(cudaEventRecord(e1, ts), "cudaEventRecord");
         cuda(cudaStreamWaitEvent(user, e1, 0), "cudaStreamWaitEvent");   // `stream` sees the final call
         cuda(cudaStreamSynchronize(ts), "cudaStreamSynchronize");

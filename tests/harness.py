@@ -77,14 +77,11 @@ def max_scaled_error(got: np.ndarray, ref: np.ndarray, bound: np.ndarray) -> flo
 
 
 def workspace(M, N, K, S, kps, poison: float = POISON):
-    """A gemm_bt workspace: partials poisoned, the fused path's counters zeroed
-    (the library's one-time requirement), guards behind."""
+    """A gemm_bt workspace (the partials), poisoned, guards behind."""
     import split_bf16_gemm_gb300 as sk
 
     nbytes = sk.gemm_bt_workspace_bytes(M, N, K, S, kps)
-    ws = Guarded(nbytes // 4, poison)
-    ws.buf[S * M * N: nbytes // 4] = 0.0
-    return ws, nbytes
+    return Guarded(nbytes // 4, poison), nbytes
 
 
 @lru_cache(maxsize=64)

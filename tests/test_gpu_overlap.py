@@ -294,3 +294,55 @@ def test_kn_layout_overlap_bitwise(lib):
     for it in insts:
         assert bitwise(it["out"], it["ref"])   # the [K,N] path is bitwise the [N,K] path
     assert sk.splitk_get_device_status() == 0
+
+
+def test_reduce_heads_or_extends_runs(lib):
+    """A reduce after foreign work waits for it and only then lets the next
+    launch start, so it heads a run: the fused call after it overlaps, and so
+    does the partial pass after that.  The reduces that follow (of partials
+    no running launch writes) load at once and let their successors start
+    early.  Every result is the eager one, bit for bit."""
+    sk = lib
+    M, N, K, S, kps, dt = 96, 512, 2048, 4, 512, "bf16"
+    insts = instances(sk, M, N, K, S, kps, dt, 4)
+    # partials to reduce: from eager partial passes
+    Ps = []
+    for it in insts:
+        P = torch.empty(S * M * N, device="cuda")
+        sk.gemm_splitk_bt(it["A"], it["B"], P, M, N, K, S, kps, dt)
+        Ps.append(P)
+    outs_ref = [torch.empty(M, N, device="cuda") for _ in range(4)]
+    outs = [torch.full((M, N), 7.0, device="cuda") for _ in range(4)]
+    fused_ref = torch.empty(M, N, device="cuda")
+    fused_out = torch.full((M, N), 7.0, device="cuda")
+    side = torch.zeros(16, device="cuda")
+    Pfresh = torch.empty(S * M * N, device="cuda")
+
+    def run(o, fo, record=None):
+        side.add_(1.0)                                          # foreign work first
+        sk.splitk_reduce(Ps[0], o[0], S, M, N)                  # heads a run
+        it = insts[1]
+        sk.gemm_bt(it["A"], it["B"], fo, it["ws"], it["nb"], M, N, K, S, kps, dt, fused=1)
+        if record is not None:
+            record.append(sk.splitk_last_launch()["overlap"])
+        sk.gemm_splitk_bt(insts[2]["A"], insts[2]["B"], Pfresh, M, N, K, S, kps, dt)   # overlaps the fused call
+        if record is not None:
+            record.append(sk.splitk_last_launch()["overlap"])
+        for j in (1, 2, 3):                                     # partials nothing running writes
+            sk.splitk_reduce(Ps[j], o[j], S, M, N)
+
+    run(outs_ref, fused_ref)
+    torch.cuda.synchronize()
+    seen = []
+    g = capture(lambda: run(outs, fused_out, seen))
+    assert seen == [1, 1], seen
+    for _ in range(3):
+        for o in outs:
+            o.fill_(7.0)
+        fused_out.fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(outs, outs_ref):
+            assert bitwise(a, b)
+        assert bitwise(fused_out, fused_ref)
+    assert sk.splitk_get_device_status() == 0

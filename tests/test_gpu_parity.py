@@ -51,7 +51,7 @@ CATEGORIES = [
     (512, 2048, 4096, 4, 1024, "bf16"),  # larger matrices
     (32, 64, 64, 1, 128, "bf16"),        # k_per_split larger than K
     (288, 256, 96, 3, 32, "f16"),        # 32-long splits everywhere
-    (64, 128, 2048, 64, 32, "bf16"),     # 64 splits: fused sum by arrival counters, loads 8 splits at a time
+    (64, 128, 2048, 64, 32, "bf16"),     # 64 splits: a fused call runs the two kernels
     (160, 192, 320, 3, 128, "f32"),      # F32 (3xTF32): M tail, short final split
     (64, 128, 8192, 4, 2048, "f32"),     # F32, long K
     (288, 256, 96, 3, 32, "f32"),        # F32, 32-long splits everywhere
@@ -118,12 +118,11 @@ def test_gemm_bt_both_modes_bitwise(lib, case):
             assert np.array_equal(w[:S * M * N].view(np.uint32), ref_P.view(np.uint32)), f"fused={fused}"
         else:
             assert np.all(w[:S * M * N] == 7.0), "fused=1 with the split sum on chip keeps no partials"
-        assert np.all(w[S * M * N:] == 0), "the counters must be back at zero"
 
 
 def test_fused_repeated_calls_and_overwrite(lib):
-    """The counters reset themselves: many fused calls on one workspace stay
-    correct, and a later call with other operands overwrites the output."""
+    """Many fused calls on one workspace and output stay bitwise the same, and a
+    later call with other operands overwrites the output."""
     sk = lib
     M, N, K, S, kps, dt = 96, 512, 2048, 4, 512, "bf16"
     ops, Pr, SP, Or, SO = oracle_case(M, N, K, S, kps, dt)
@@ -144,7 +143,6 @@ def test_fused_repeated_calls_and_overwrite(lib):
     sk.gemm_bt(A2, B2, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=1)
     assert max_scaled_error(o.numpy().reshape(M, N), Or2, SO2) <= TOL_FINAL[dt]
     assert sk.splitk_get_device_status() == 0
-    assert np.all(ws.numpy()[S * M * N:] == 0)
 
 
 def test_reads_follow_previous_kernel(lib):
@@ -440,7 +438,7 @@ def test_host_batch_back_to_back_shared_staging(lib):
 def test_autotune_splits(lib, case):
     """The measured split choice is the fastest candidate it timed, a legal
     geometry; `out` then holds a correct result, and a later gemm_bt with the
-    chosen split on the same workspace (counters re-zeroed) gives it again."""
+    chosen split on the same workspace gives it again."""
     sk = lib
     M, N, K, dt, fused = case
     cand = {}

@@ -135,7 +135,7 @@ def test_gemm_bt_rejections(L):
     assert call(ws=B0 + 64) == bd.ERR_ALIAS
     assert call(fused=2) == bd.ERR_CONFIG
     assert call(fused=4) == bd.ERR_CONFIG
-    # the fused path keeps the partials and its counters in the workspace too
+    # the fused calls take the same workspace (the two-kernel path runs where no cluster sums)
     assert call(ws=0, fused=1) == bd.ERR_NULL
     assert call(wsb=0, fused=1) == bd.ERR_WORKSPACE
     assert L.gemm_bt_workspace_init(0, 64, None) == bd.ERR_NULL
@@ -143,9 +143,9 @@ def test_gemm_bt_rejections(L):
 
 
 def test_workspace_bytes(L):
-    # partials, then one 4-byte counter per (64-column block, 128-row block, chunk <= 8)
-    assert sk.gemm_bt_workspace_bytes(256, 1024, 2048, 2, 1024) == 2 * 256 * 1024 * 4 + 16 * 2 * 8 * 4
-    assert sk.gemm_bt_workspace_bytes(64, 128, 160, 3, 64) == 3 * 64 * 128 * 4 + 2 * 1 * 8 * 4
+    # the F32 partials [splits, M, N]
+    assert sk.gemm_bt_workspace_bytes(256, 1024, 2048, 2, 1024) == 2 * 256 * 1024 * 4
+    assert sk.gemm_bt_workspace_bytes(64, 128, 160, 3, 64) == 3 * 64 * 128 * 4
     assert sk.gemm_bt_workspace_bytes(64, 128, 160, 3, 64, 1) == sk.gemm_bt_workspace_bytes(64, 128, 160, 3, 64, 0)
     assert sk.gemm_bt_workspace_bytes(64, 128, 160, 2, 64) == 0
 

@@ -255,3 +255,35 @@ def test_plan_follows_override_changes(lib):
     assert lib.splitk_describe_launch(*shape, "f32", fused=1)["path"] == 2
     assert lib.splitk_describe_launch(*shape, "bf16", fused=0)["fused_in_kernel"] == 0
     assert default["fused_in_kernel"] == 1
+
+
+def test_fused_routing(lib):
+    """gemm_bt(fused=1) sums the splits in its launch only where one resident
+    cluster holds all of a tile's splits and chunks; elsewhere it runs the two
+    kernels (the same chunks, so the same result bit for bit), which measured
+    faster on GB300 than summing through global memory.  F32 operands with
+    M <= 32 also run the two kernels where the summing cluster would be larger
+    than the partial pass's own."""
+    sk = lib
+    fused_in_kernel = [
+        (256, 1024, 2048, 2, 1024, "bf16"), (256, 1024, 2048, 4, 512, "bf16"), (96, 512, 2048, 4, 512, "bf16"),
+        (256, 512, 2048, 4, 512, "bf16"), (32, 64, 128, 2, 64, "bf16"), (32, 512, 2048, 8, 256, "f16"),
+        (96, 512, 512, 2, 256, "f32"), (32, 512, 2048, 1, 2048, "f32"),
+    ]
+    two_kernels = [
+        (256, 1024, 2048, 8, 256, "bf16"), (256, 1024, 2048, 16, 128, "bf16"),   # more than one cluster holds
+        (96, 512, 2048, 16, 128, "bf16"), (32, 512, 2048, 16, 128, "f16"),
+        (64, 128, 160, 3, 64, "bf16"),                                          # three splits
+        (4096, 8192, 4096, 2, 2048, "bf16"),                                    # more tiles than resident clusters
+        (32, 512, 2048, 2, 1024, "f32"), (32, 512, 2048, 8, 256, "f32"),        # F32, M <= 32
+    ]
+    for c in fused_in_kernel:
+        d = sk.splitk_describe_launch(*c, fused=1)
+        assert d["fused_in_kernel"] == 1 and d["kernels_per_call"] == 1 and d["split_sum"] == 2, c
+    for c in two_kernels:
+        d = sk.splitk_describe_launch(*c, fused=1)
+        assert d["fused_in_kernel"] == 0 and d["kernels_per_call"] == 2 and d["split_sum"] == 0, c
+        # the partial pass of the fused call is the two-kernel call's partial pass
+        d0 = sk.splitk_describe_launch(*c, fused=0)
+        assert {k: d[k] for k in ("bn", "chunks", "chunk_len", "cluster", "stages")} == \
+               {k: d0[k] for k in ("bn", "chunks", "chunk_len", "cluster", "stages")}, c

@@ -31,7 +31,7 @@ def sk():
 
 CASES = [
     (256, 1024, 2048, 2, 1024, "bf16"),   # the benchmark workload: splits summed inside the cluster
-    (64, 128, 160, 3, 64, "f16"),         # three splits: summed through the arrival counters
+    (64, 128, 160, 3, 64, "f16"),         # three splits: no cluster holds them, two kernels
     (96, 512, 512, 16, 32, "bf16"),       # sixteen splits
     (96, 512, 2048, 4, 512, "f32"),       # F32 operands: two kernels
 ]
@@ -63,10 +63,12 @@ def test_noalloc_matches_gemm_bt_on_two_calls(sk, case, fused):
 def test_noalloc_rejects_shapes_beyond_its_scratch(sk):
     from split_bf16_gemm_gb300 import binding as bd
 
-    # partials alone: 1 * 2048 * 4096 * 4 bytes = 32 MiB, plus counters: too big
-    M, N, K = 2048, 4096, 2048
-    assert sk.gemm_bt_workspace_bytes(M, N, K, 1, K) > bd.NOALLOC_MAX_BYTES
-    st = sk.lib().gemm_bt_noalloc(0x10000000, 0x20000000, 0x30000000, M, N, K, 1, K, bd.BF16, 0, None)
+    # partials: 2 * 2048 * 4096 * 4 bytes = 64 MiB, twice the scratch; one split
+    # (exactly 32 MiB) still fits
+    M, N, K = 2048, 4096, 4096
+    assert sk.gemm_bt_workspace_bytes(M, N, K, 1, K) == bd.NOALLOC_MAX_BYTES
+    assert sk.gemm_bt_workspace_bytes(M, N, K, 2, K // 2) > bd.NOALLOC_MAX_BYTES
+    st = sk.lib().gemm_bt_noalloc(0x10000000, 0x20000000, 0x30000000, M, N, K, 2, K // 2, bd.BF16, 0, None)
     assert st == bd.ERR_WORKSPACE
     assert "scratch" in sk.splitk_last_error()
     # a shape that fits is accepted (and computed) right after the rejection
