@@ -237,8 +237,10 @@ __device__ __forceinline__ void cluster_split_sum_for(int C, const uint32_t (&rb
 // product formed as three TF32 products (hi*lo + lo*hi + hi*hi).  TM: rows
 // of A per CTA; 256 only for 16-bit operands, BN = 256 and one CTA per tile
 // that keeps or sums its own partials (no cluster).
+// Registers: at most 85 per thread for clusters of up to 4 (three CTAs per
+// SM in the compact layout), else 128 (two); no instantiation spills.
 template <int BN, int Q, bool KN, bool X3, int TM = kTileM>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
     tc_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const TcArgs args)
 {
@@ -780,10 +782,11 @@ size_t stage_bytes(int bn, int kbs, bool x3 = false, int tm = kTileM)
 size_t epi_bytes(int bn) { return static_cast<size_t>(kTileM) * bn * 4; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr size_t kSmemLimit = 226 * 1024;   // dynamic; leaves room for static shared memory
-// The compact layout: two CTAs to an SM (228 KB of shared memory, 1 KB of it
-// reserved per CTA, plus the kernel's static barriers), so that the next
-// operation's CTAs can start beside this one's.
+// The compact layout: two or three CTAs to an SM (228 KB of shared memory,
+// 1 KB of it reserved per CTA, plus the kernel's static barriers), so that
+// the next operations' CTAs can start beside this one's.
 constexpr size_t kCompactSmemLimit = 112 * 1024;
+constexpr size_t kCompact3SmemLimit = 74 * 1024;
 
 // Dynamic shared memory of a plan: the stage ring (or the accumulator
 // staging, if larger), one receive slot per peer, and 1 KB of alignment slack.
@@ -1123,16 +1126,28 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     // sums in the same order, with the ring cut to what two CTAs per SM
     // allow and the peers' shares received inside it.  Only for launches of
     // one wave (where the next operation's CTAs would otherwise find no room)
-    // and tiles of at most 128 columns (two CTAs' accumulators then use at
-    // most half of an SM's tensor memory).  On GB300, a graph of eight
+    // and tiles of at most 128 columns (three CTAs' accumulators then fit in
+    // an SM's 512 tensor-memory columns).  On GB300, a graph of eight
     // independent BF16 M256 N1024 K2048 operations went from 5.9 to 4.2 us
     // per operation with this layout and the early start; the layout alone,
     // with every launch waiting for the one before, was slower (6.7 us).
+    // Launches of more CTAs than half the SMs, with clusters of at most 4
+    // (whose kernels keep to 85 registers), cut the ring further, to three
+    // CTAs per SM: the headline shape went from 4.05 to 3.80 us per
+    // operation; launches of 64 CTAs already hold four operations at once
+    // with two per SM and ran slower with the smaller ring (M256 N512 K2048
+    // S4: 3.55 against 3.28 us).
     p.compact = 0;
     p.recv_in_ring = 0;
     if (compact && !x3 && tm == kTileM && bn <= 128 && clusters <= resident_clusters(q)) {
-        const StageChoice cc = pick_stages(bn, nkb, can3d, q, share, x3, tm, kCompactSmemLimit, q > 1);
-        if (cc.ok && cc.stages >= std::min(2, (nkb + cc.kbs - 1) / cc.kbs)) {
+        const auto double_buffered = [&](const StageChoice &c) {
+            return c.ok && c.stages >= std::min(2, (nkb + c.kbs - 1) / c.kbs);
+        };
+        StageChoice cc;
+        if (q <= 4 && ctas > resident_clusters(1) / 2)
+            cc = pick_stages(bn, nkb, can3d, q, share, x3, tm, kCompact3SmemLimit, q > 1);
+        if (!double_buffered(cc)) cc = pick_stages(bn, nkb, can3d, q, share, x3, tm, kCompactSmemLimit, q > 1);
+        if (double_buffered(cc)) {
             p.compact = 1;
             p.recv_in_ring = q > 1 ? 1 : 0;
             p.stages = cc.stages;
@@ -1142,7 +1157,7 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
             p.region0 = static_cast<uint32_t>(
                 round_up(std::max(p.stages * stage_bytes(bn, p.kbs, x3, tm), in_ring), 1024));
             p.smem_bytes = smem_for(bn, p.kbs, p.stages, q, share, x3, tm, q > 1);
-            // two CTAs to an SM: as many start beside a running launch as it has CTAs
+            // two or three CTAs to an SM: as many start beside a running launch as it has CTAs
             p.prefetchers = static_cast<int>(std::min<int64_t>(ctas, 2 * resident_clusters(q) * q - ctas));
             if (p.prefetchers < 0) p.prefetchers = 0;
         }

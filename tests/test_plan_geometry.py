@@ -32,6 +32,7 @@ from test_gpu_fuzz import LARGE, RANDOM
 
 SMEM_LIMIT = 226 * 1024
 COMPACT_LIMIT = 112 * 1024
+COMPACT3_LIMIT = 74 * 1024    # three thread blocks to an SM
 SM_SMEM = 228 * 1024          # per SM; 1 KB of it reserved per thread block
 STATIC_SMEM = 240             # the kernel's barriers and flags (nvcc -Xptxas -v)
 TILE_M = 128
@@ -136,6 +137,15 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
         assert csmem == cregion + 1024 <= COMPACT_LIMIT
         assert 2 * (csmem + STATIC_SMEM + 1024) <= SM_SMEM   # two blocks to an SM
         assert 2 * BN <= 512 and BN <= csmem // 512          # tensor memory: theirs fits, by the smem rule
+        # three to an SM for launches of more CTAs than half the SMs with
+        # clusters of at most 4, wherever a double-buffered ring of single
+        # k-block stages and the staging plus receive slots fit in 74 KB
+        ctas = -(-M // TM) * (N // BN) * S * C
+        kmin = kbs if (kbs and T3) else 1                    # the smallest stage the override allows
+        stage1 = (TM + BN) * 128 * kmin
+        fits3 = max(min(2, -(-nkb // kmin)) * stage1, epi_bytes + recv_bytes) + 1024 <= COMPACT3_LIMIT
+        if Q <= 4 and ctas > 74 and fits3:
+            assert csmem <= COMPACT3_LIMIT and 3 * (csmem + STATIC_SMEM + 1024) <= SM_SMEM and 3 * BN <= 512
         check_k_coverage(K, S, kps, C, CL, ckbs, int(ckbs > 1), kb_elems, elem)
         if Q > 1:
             check_exchange(BN, Q, epi_bytes, cregion)
