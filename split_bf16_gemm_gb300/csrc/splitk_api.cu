@@ -155,6 +155,8 @@ int run_reduce(const float *P, float *out, int64_t S, int64_t M, int64_t N, cuda
 // runs on the CUDA cores and always takes the two-kernel path.
 bool fused_possible(int dtype, bool b_kn) { return !(dtype == SPLITK_F32 && b_kn); }
 
+}  // namespace
+
 // Whether gemm_bt(fused != 0) sums the splits inside its launch.  It does
 // where the tile plan holds all of a tile's splits in one resident cluster,
 // except for F32 operands (3xTF32) with M <= 32: there the cluster that sums
@@ -162,7 +164,7 @@ bool fused_possible(int dtype, bool b_kn) { return !(dtype == SPLITK_F32 && b_kn
 // against one split's), its exchange moves the whole 128-row accumulator of
 // which at most 32 rows are live, and on GB300 the two kernels measured
 // faster (M32 N512 K2048, 2 to 8 splits: 5.6-5.8 against 7.0-7.2 us).
-bool sums_in_kernel(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, int dtype, bool b_kn)
+bool splitk::fused_in_kernel(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, int dtype, bool b_kn)
 {
     if (!fused_possible(dtype, b_kn)) return false;
     const bool x3 = dtype == SPLITK_F32;
@@ -171,6 +173,8 @@ bool sums_in_kernel(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, int
     if (x3 && M <= 32 && f.cluster > splitk::plan_tc(M, N, K, S, kps, false, x3).cluster) return false;
     return true;
 }
+
+namespace {
 
 size_t partials_bytes(int64_t M, int64_t N, int64_t S) { return static_cast<size_t>(S * M * N) * 4; }
 
@@ -290,7 +294,7 @@ static int gemm_impl(const void *A, const void *B, float *out, void *workspace, 
     // slower on GB300 than the separate reduce in every such case (BF16 M256
     // N1024 K2048 with 8 splits: 17.9 against 7.0 us).  The chunks do not
     // depend on `fused`, so the result is the same either way, bit for bit.
-    if (fused && sums_in_kernel(M, N, K, splits, k_per_split, dtype, b_kn)) {
+    if (fused && splitk::fused_in_kernel(M, N, K, splits, k_per_split, dtype, b_kn)) {
         // fused == 1 keeps no partials
         float *keep = fused == 1 ? nullptr : P;
         return run_partial_pass(A, B, keep, out, M, N, K, splits, k_per_split, dtype, true, true, b_kn,
@@ -367,7 +371,7 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
     const bool x3 = dtype == SPLITK_F32;
     // gemm_bt runs the two kernels where the fused launch could not sum a
     // tile's splits inside one resident cluster
-    const bool in_kernel = fused != 0 && sums_in_kernel(M, N, K, splits, k_per_split, dtype, false);
+    const bool in_kernel = fused != 0 && splitk::fused_in_kernel(M, N, K, splits, k_per_split, dtype, false);
     const TilePlan p = splitk::plan_tc(M, N, K, splits, k_per_split, in_kernel, x3);
     info[0] = x3 ? 2 : 0;
     info[1] = p.bn;

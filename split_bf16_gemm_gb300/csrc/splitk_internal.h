@@ -124,6 +124,10 @@ struct LaunchRecord {
 void note_launch(const LaunchRecord &r);
 LaunchRecord last_launch();
 
+// Whether gemm_bt(fused != 0) sums the splits inside its tensor-core launch
+// (else it runs the partial pass and the reduce); dtype as in splitk.h.
+bool fused_in_kernel(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, int dtype, bool b_kn);
+
 // gemm_bt's argument checks (status as gemm_bt returns it; nothing launched),
 
 int check_gemm_bt(const void *A, const void *B, const float *out, const void *workspace, size_t workspace_bytes,

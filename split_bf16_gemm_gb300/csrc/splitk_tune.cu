@@ -18,6 +18,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 
 #include "splitk.h"
 #include "splitk_internal.h"
@@ -50,11 +51,14 @@ int elem_size(int dtype)
     }
 }
 
-// Estimated microseconds of one gemm_bt call behind another.
+// Estimated microseconds per gemm_bt call in a graph of such calls: the
+// tensor-core launch, plus for the two-kernel path (fused == 0, or a fused
+// call that runs the two kernels) the reduce: 0.85 us, its bytes at ~3.1 TB/s
+// and 0.046 us per split (fitted with the launch model in splitk_tc.cu).
 double estimate_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, int dtype, int fused)
 {
-    const double reduce = 1.0 + static_cast<double>(S + 1) * M * N * 4 / 6.0e6;   // bytes at ~6 TB/s
-    const bool in_kernel = fused != 0;
+    const bool in_kernel = fused != 0 && splitk::fused_in_kernel(M, N, K, S, kps, dtype, false);
+    const double reduce = 0.85 + static_cast<double>(S + 1) * M * N * 4 / 3.1e6 + 0.046 * static_cast<double>(S);
     return splitk::estimate_tc_us(M, N, K, S, kps, in_kernel, dtype == SPLITK_F32) + (in_kernel ? 0.0 : reduce);
 }
 
@@ -78,8 +82,11 @@ int splitk_choose_splits(int64_t M, int64_t N, int64_t K, int dtype, int fused, 
         if (splitk_check_geometry(M, N, K, S, kps) != SPLITK_OK) continue;
         const double t = estimate_us(M, N, K, S, kps, dtype, fused);
         if (model_us) model_us[i] = t;
-        if (t < best) {
-            best = t;
+        // candidates within 1% count as ties, won by the larger split count
+        // (the measured curves are flat there, and more splits cost least
+        // where the model misses a fixed cost)
+        if (t <= best * 1.01) {
+            best = std::min(best, t);
             bs = S;
             bk = kps;
         }
