@@ -364,6 +364,23 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits,
  * splitk_get_device_status() then reads (SPLITK_ERR_DEVICE_TIMEOUT expected). */
 int splitk_selftest_bounded_wait(int64_t limit_ns, void *stream);
 
+/* Self-test of the tensor-core kernel's own time-out path: one fused launch
+ * (arguments as for gemm_bt with fused = 1, no workspace; the shape must sum
+ * its splits inside the launch, else SPLITK_ERR_CONFIG) whose wait for the
+ * final accumulator gives up at once: the warps that wait for it test it
+ * once, before the MMA issuer has finished, as a wait that ran out would.  The
+ * kernel then records the time-out, still sends and awaits every cluster
+ * message, waits for the MMAs (normal limit) before it frees its tensor
+ * memory, and finishes; `out` is not valid.  Synchronises `stream` and
+ * returns what splitk_get_device_status() reads (SPLITK_ERR_DEVICE_TIMEOUT
+ * expected).  At that wait every TMA load of the launch has landed, and the
+ * waits after it keep their normal limits, so no copy is in flight when a
+ * block exits. */
+int splitk_selftest_kernel_timeout(const void *A, const void *B, float *out,
+                                   int64_t M, int64_t N, int64_t K,
+                                   int64_t splits, int64_t k_per_split,
+                                   int dtype, void *stream);
+
 /* Turns the overlap of consecutive independent launches inside a graph
  * capture (see the top of this header) on (1, the default) or off (0) for
  * every later launch of the process.  Launches already captured keep what

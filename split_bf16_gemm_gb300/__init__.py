@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     gemm_splitk_bt,
     lib, splitk_check_geometry, splitk_describe_launch, splitk_get_device_status, splitk_reduce,
     splitk_autotune_splits, splitk_choose_splits, splitk_last_error, splitk_last_launch, splitk_prepare_bt,
-    splitk_selftest_bounded_wait, splitk_set_overlap, splitk_set_tile_override, splitk_status_string,
+    splitk_selftest_bounded_wait, splitk_selftest_kernel_timeout, splitk_set_overlap, splitk_set_tile_override,
+    splitk_status_string,
     status_string,
 )

@@ -27,7 +27,7 @@ EXPORTS = (
     "splitk_describe_launch", "splitk_selftest_bounded_wait", "splitk_last_error",
     "gemm_bt_workspace_init", "gemm_bt_noalloc", "splitk_prepare_bt",
     "gemm_bt_host_staging_bytes", "gemm_bt_host_batch", "splitk_choose_splits", "splitk_autotune_splits",
-    "gemm_splitk_kn", "gemm_kn", "splitk_set_overlap", "splitk_last_launch",
+    "gemm_splitk_kn", "gemm_kn", "splitk_set_overlap", "splitk_last_launch", "splitk_selftest_kernel_timeout",
 )
 NOALLOC_MAX_BYTES = 32 << 20   # SPLITK_NOALLOC_MAX_BYTES
 
@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
             L.splitk_last_error.argtypes = []
             L.splitk_set_overlap.argtypes = [i32]
             L.splitk_last_launch.argtypes = [vp]
+            L.splitk_selftest_kernel_timeout.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, vp]
             L.splitk_last_error.restype = ctypes.c_char_p
             for name in ("splitk_check_geometry", "gemm_splitk_bt", "splitk_reduce", "gemm_bt",
                          "gemm_splitk_kn", "gemm_kn",
@@ -87,7 +88,7 @@ def lib() -> ctypes.CDLL:
                          "gemm_bt_host_batch", "splitk_choose_splits", "splitk_autotune_splits",
                          "splitk_get_device_status", "splitk_set_tile_override",
                          "splitk_describe_launch", "splitk_selftest_bounded_wait", "splitk_set_overlap",
-                         "splitk_last_launch"):
+                         "splitk_last_launch", "splitk_selftest_kernel_timeout"):
                 getattr(L, name).restype = i32
             _lib = L
     return _lib
@@ -282,3 +283,11 @@ def splitk_last_launch() -> dict:
     _check(lib().splitk_last_launch(ctypes.addressof(info)), "splitk_last_launch")
     keys = ("overlap", "compact", "capturing", "bn", "chunks", "stages", "kblocks_per_stage", "smem_bytes")
     return dict(zip(keys, list(info)))
+
+
+def splitk_selftest_kernel_timeout(A, B, out, M, N, K, splits, k_per_split, dtype, stream=None) -> int:
+    """One fused launch whose wait for the final accumulator gives up at once
+    (the kernel's own time-out path); returns the device status it leaves
+    (ERR_DEVICE_TIMEOUT expected).  Never raises."""
+    return lib().splitk_selftest_kernel_timeout(_ptr(A), _ptr(B), _ptr(out), M, N, K, splits, k_per_split,
+                                                dtype_code(dtype), _stream(stream))

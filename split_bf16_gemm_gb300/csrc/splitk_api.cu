@@ -425,6 +425,29 @@ int splitk_last_launch(int *info)
     return SPLITK_OK;
 }
 
+int splitk_selftest_kernel_timeout(const void *A, const void *B, float *out, int64_t M, int64_t N, int64_t K,
+                                   int64_t splits, int64_t k_per_split, int dtype, void *stream)
+{
+    int st = validate_gemm(A, B, M, N, K, splits, k_per_split, dtype);
+    if (st != SPLITK_OK) return st;
+    if (!out) return SPLITK_ERR_NULL;
+    if (!aligned16(out)) return SPLITK_ERR_ALIGN;
+    const int e = elem_bytes(dtype);
+    const Range ro = range_of(out, static_cast<uint64_t>(M * N) * 4);
+    if (overlap(ro, range_of(A, static_cast<uint64_t>(M * K) * e)) ||
+        overlap(ro, range_of(B, static_cast<uint64_t>(N * K) * e)))
+        return SPLITK_ERR_ALIAS;
+    if (!splitk::fused_in_kernel(M, N, K, splits, k_per_split, dtype, false)) return SPLITK_ERR_CONFIG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    GemmProblem pr{A, B, nullptr, out, M, N, K, splits, k_per_split, dtype == SPLITK_BF16};
+    pr.f32 = dtype == SPLITK_F32;
+    pr.acc_probe = true;
+    TilePlan plan = splitk::plan_tc(M, N, K, splits, k_per_split, true, pr.f32);
+    plan.prefetchers = 0;
+    if (splitk::launch_tc(pr, plan, s) != cudaSuccess) return SPLITK_ERR_CUDA;
+    return splitk_get_device_status(stream);
+}
+
 int splitk_selftest_bounded_wait(int64_t limit_ns, void *stream)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -21,6 +21,7 @@ struct GemmProblem {
     bool b_kn = false;  // B given as the [K,N] weight itself (read MN-major)
     bool f32 = false;   // F32 operands: 3xTF32 products on the tensor cores (bf16 ignored)
     bool overlap = false; // no launch that may still run writes A or B: load before the previous grid ends
+    bool acc_probe = false; // time-out self-test: the wait for the accumulator gives up at once
 };
 
 // How it is tiled.  One CTA computes a 128 x bn tile of one K-chunk of one

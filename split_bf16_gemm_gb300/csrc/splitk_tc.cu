@@ -87,6 +87,7 @@ struct TcArgs {
     uint32_t region0;      // bytes of the stage ring / accumulator staging area
     int bf16;
     uint64_t wait_limit_ns;
+    int acc_probe;         // time-out self-test: the wait for the final accumulator gives up at once
     const uint8_t *A, *B;  // operands, for the L2 prefetch
     uint64_t a_bytes, b_bytes;
     int prefetchers;       // CTAs, first in dispatch order, that prefetch A and B into L2
@@ -506,6 +507,10 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
             if (lane == 0) ptx::mbar_arrive(conv_bar(st));
         }
     }
+    // time-out self-test: the warps that wait for the accumulator and take no
+    // part in the main loop (2-7) test it once, before the MMA issuer has
+    // finished, and give up as a wait that ran out would
+    if (args.acc_probe && warp >= 2 && !ptx::mbar_test_wait(acc_bar, 0)) atomicOr(&abort_s, 4u);
     __syncthreads();
 
     const bool acc_ok = ptx::mbar_wait_bounded(acc_bar, 0, args.wait_limit_ns);
@@ -572,7 +577,12 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
         ptx::tc_fence_before_sync();
         __syncthreads();
         if (warp == 1 && h == kHalves - 1) {
-            if (!acc_ok) ptx::mbar_wait_bounded(acc_bar, 0, args.wait_limit_ns);
+            // after a time-out the MMAs may still run: wait for them (normal
+            // limit) before freeing their tensor memory.  `aborted` is the
+            // same in every thread (acc_ok is per thread), and the warp
+            // reconverges before the warp-wide deallocation.
+            if (aborted) ptx::mbar_wait_bounded(acc_bar, 0, args.wait_limit_ns);
+            __syncwarp();
             ptx::tc_fence_after_sync();
             ptx::tmem_dealloc(tmem, Sh::kTmemCols);
         }
@@ -1237,6 +1247,7 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
     a.region0 = plan.region0;
     a.bf16 = pr.bf16 ? 1 : 0;
     a.wait_limit_ns = kWaitLimitNs;
+    a.acc_probe = pr.acc_probe ? 1 : 0;
     a.A = static_cast<const uint8_t *>(pr.A);
     a.B = static_cast<const uint8_t *>(pr.B);
     a.a_bytes = static_cast<uint64_t>(pr.M * pr.K) * elem_of(et);

@@ -296,6 +296,37 @@ def test_bounded_wait_reports_and_context_survives(lib):
     check_case(sk, (32, 64, 128, 2, 64, "bf16"))        # the context is still usable
 
 
+def test_kernel_timeout_path_reports_and_context_survives(lib):
+    """The tensor-core kernel's own time-out path: in a fused launch the wait
+    for the final accumulator gives up at once, while the last MMAs still run
+    (a self-test entry point).  The launch records the time-out, still sends
+    and awaits every cluster message, waits for its MMAs before freeing its
+    tensor memory and finishes inside its output's bounds; the context stays
+    usable: the next calls match the oracle, and a run of launches after it
+    still gets its tensor memory."""
+    sk = lib
+    from split_bf16_gemm_gb300 import binding as bd
+
+    M, N, K, S, kps, dt = 256, 1024, 2048, 2, 1024, "bf16"
+    ops, Pr, SP, Or, SO = oracle_case(M, N, K, S, kps, dt)
+    A, B = device_operand(ops.A, dt), device_operand(ops.B, dt)
+    assert sk.splitk_get_device_status() == 0
+    for _ in range(3):
+        out = Guarded(M * N)
+        assert sk.splitk_selftest_kernel_timeout(A, B, out.data, M, N, K, S, kps, dt) == bd.ERR_DEVICE_TIMEOUT
+        assert out.guards_intact()
+    assert sk.splitk_get_device_status() == 0          # read-and-clear
+    check_case(sk, (M, N, K, S, kps, dt))               # parity on the same context
+    ws, nbytes = workspace(M, N, K, S, kps)
+    o = Guarded(M * N)
+    for _ in range(20):
+        sk.gemm_bt(A, B, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=1)
+    assert sk.splitk_get_device_status() == 0
+    assert max_scaled_error(o.numpy().reshape(M, N), Or, SO) <= TOL_FINAL[dt] and o.guards_intact()
+    # a call that would not sum its splits inside the launch is refused
+    assert sk.splitk_selftest_kernel_timeout(A, B, o.data, M, N, K, 8, 256, dt) == bd.ERR_CONFIG
+
+
 PREP_CASES = [(32, 64, "bf16"), (160, 128, "f16"), (96, 320, "f32"), (2048, 1024, "bf16"), (4096, 2048, "f16")]
 
 
