@@ -53,8 +53,13 @@
  * the stream, and the new launch reads (A and B; the partials, for the
  * reduce) no byte that any of its launches still able to run writes, the new
  * launch starts loading and multiplying at once and waits for the previous
- * grid only before its first store ("overlap").  Its results are bitwise
- * those of the same launch without overlap.  Launches that read what an
+ * grid only before its first store ("overlap"); if none of them reads or
+ * writes what the new launch writes either, it also stores at once and
+ * waits only before it finishes, so the grids still finish in launch order.
+ * Such a fused launch may also give each thread block all the chunks of its
+ * split, each in its own accumulator, added in chunk order inside the block.
+ * Its results are bitwise those of the same launch without overlap.
+ * Launches that read what an
  * earlier one writes (a chain of GEMMs, the reduce after the partial pass),
  * launches after another kernel or a copy, and launches outside a capture
  * wait as usual.  The decision is made at capture time from the pointers
@@ -331,7 +336,7 @@ const char *splitk_status_string(int status);
  * SPLITK_OK or SPLITK_ERR_CONFIG. */
 int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
 
-/* Describes the launch gemm_bt would make, without launching: info[0..21] =
+/* Describes the launch gemm_bt would make, without launching: info[0..24] =
  * {path (0 tensor-core, 2 tensor-core 3xTF32 for F32), bn, chunks, chunk_len, stages,
  *  cluster_size (chunks, or splits * chunks), grid_x, grid_y, grid_z,
  *  dynamic_smem_bytes,
@@ -349,10 +354,13 @@ int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
  *  then counts 256-row tiles),
  *  compact (1: a fused call captured into a graph, when it starts beside the
  *  launch before it or heads such a run, takes the compact layout: the same
- *  tiles, chunks and sums, a stage ring cut so that two thread blocks fit on
- *  an SM, the peers' shares received inside the ring),
- *  compact_stages, compact_kblocks_per_stage, compact_dynamic_smem_bytes
- *  (0 when compact is 0)}; `info` must hold 22 ints.
+ *  tiles, chunks and sums, a stage ring cut so that two or three thread
+ *  blocks fit on an SM, the peers' shares received inside the ring),
+ *  compact_stages, compact_kblocks_per_stage, compact_dynamic_smem_bytes,
+ *  compact_chunks_per_block (1, or every chunk of a split in one thread
+ *  block, each in its own accumulator, added in chunk order before the
+ *  exchange: the same sums), compact_cluster_size, compact_grid_z
+ *  (0 when compact is 0)}; `info` must hold 25 ints.
  * Returns a status as gemm_bt's validation would (pointers are not checked). */
 int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits,
                            int64_t k_per_split, int dtype, int fused,
@@ -388,12 +396,16 @@ int splitk_selftest_kernel_timeout(const void *A, const void *B, float *out,
 int splitk_set_overlap(int enable);
 
 /* What the calling host thread's most recent tensor-core launch did:
- * info[0..7] = {overlap (it loaded before the previous grid finished),
- * compact (its ring was cut so that two of its thread blocks fit on an SM,
- * taken for such launches and for the first of a capture, when a
- * one-wave plan allows it), capturing (the stream was being captured), bn,
- * chunks, stages, kblocks_per_stage, dynamic_smem_bytes}.  Diagnostic;
- * returns SPLITK_OK or SPLITK_ERR_NULL. */
+ * info[0..9] = {overlap (0: it waited for the previous grid before loading;
+ * 1: it loaded before that grid finished and waited before its first store;
+ * 2: it also stored before, waiting only before it finished), compact (its
+ * ring was cut so that two or three of its thread blocks fit on an SM,
+ * taken for such launches and for the first of a capture, when a one-wave
+ * plan allows it), capturing (the stream was being captured), bn, chunks,
+ * stages, kblocks_per_stage, dynamic_smem_bytes, chunks_per_block (1, or
+ * all the chunks of a split, each in its own accumulator and added in chunk
+ * order inside the block: the same sums), cluster_size}.  `info` must hold
+ * 10 ints.  Diagnostic; returns SPLITK_OK or SPLITK_ERR_NULL. */
 int splitk_last_launch(int *info);
 
 #ifdef __cplusplus

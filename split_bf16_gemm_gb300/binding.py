@@ -257,13 +257,14 @@ def splitk_set_tile_override(bn: int = 0, chunks: int = 0, kblocks_per_stage: in
 
 
 def splitk_describe_launch(M, N, K, splits, k_per_split, dtype, fused=0) -> dict:
-    info = (ctypes.c_int * 22)()
+    info = (ctypes.c_int * 25)()
     _check(lib().splitk_describe_launch(M, N, K, splits, k_per_split, dtype_code(dtype), fused,
                                         ctypes.addressof(info)), "splitk_describe_launch")
     keys = ("path", "bn", "chunks", "chunk_len", "stages", "cluster", "grid_x", "grid_y",
             "grid_z", "smem_bytes", "fused_in_kernel", "kernels_per_call", "kblocks_per_stage",
             "three_d", "split_sum", "prefetchers", "rows_first", "tile_m",
-            "compact", "compact_stages", "compact_kblocks_per_stage", "compact_smem_bytes")
+            "compact", "compact_stages", "compact_kblocks_per_stage", "compact_smem_bytes",
+            "compact_chunks_per_block", "compact_cluster", "compact_grid_z")
     return dict(zip(keys, list(info)))
 
 
@@ -279,9 +280,10 @@ def splitk_set_overlap(enable: bool) -> None:
 
 def splitk_last_launch() -> dict:
     """What the calling thread's most recent tensor-core launch did."""
-    info = (ctypes.c_int * 8)()
+    info = (ctypes.c_int * 10)()
     _check(lib().splitk_last_launch(ctypes.addressof(info)), "splitk_last_launch")
-    keys = ("overlap", "compact", "capturing", "bn", "chunks", "stages", "kblocks_per_stage", "smem_bytes")
+    keys = ("overlap", "compact", "capturing", "bn", "chunks", "stages", "kblocks_per_stage", "smem_bytes",
+            "chunks_per_block", "cluster")
     return dict(zip(keys, list(info)))
 
 

@@ -114,22 +114,23 @@ int run_partial_pass(const void *A, const void *B, float *P, float *out, int64_t
     pr.b_kn = b_kn;
     pr.f32 = dtype == SPLITK_F32;   // 3xTF32 on the tensor cores
     const int e = elem_bytes(dtype);
-    // read before the wait for the previous grid: the operands only
     const splitk::Span reads[2] = {splitk::span_of(A, static_cast<uint64_t>(M * K) * e),
                                    splitk::span_of(B, static_cast<uint64_t>(N * K) * e)};
-    splitk::ChainGuard chain(stream, reads, 2);
+    splitk::Span writes[2];
+    int nw = 0;
+    if (P) writes[nw++] = splitk::span_of(P, static_cast<uint64_t>(S * M * N) * 4);
+    if (out) writes[nw++] = splitk::span_of(out, static_cast<uint64_t>(M * N) * 4);
+    splitk::ChainGuard chain(stream, reads, 2, writes, nw);
     const bool compact = allow_compact && chain.capturing() && (chain.overlap() || chain.fresh());
     TilePlan plan = splitk::plan_tc(M, N, K, S, kps, fused, pr.f32, compact);
     if (!prefetch) plan.prefetchers = 0;
     pr.overlap = chain.overlap();
+    pr.store_early = chain.store_early();
     const cudaError_t err = splitk::launch_tc(pr, plan, stream);
-    splitk::Span writes[splitk::kMaxSpans];
-    int nw = 0;
-    if (P) writes[nw++] = splitk::span_of(P, static_cast<uint64_t>(S * M * N) * 4);
-    if (out) writes[nw++] = splitk::span_of(out, static_cast<uint64_t>(M * N) * 4);
-    chain.commit(writes, nw, err == cudaSuccess, !pr.overlap);
-    splitk::note_launch({pr.overlap ? 1 : 0, plan.compact, chain.capturing() ? 1 : 0, plan.bn, plan.chunks,
-                         plan.stages, plan.kbs, static_cast<int>(plan.smem_bytes)});
+    chain.commit(err == cudaSuccess, !pr.overlap);
+    splitk::note_launch({pr.overlap ? (pr.store_early ? 2 : 1) : 0, plan.compact, chain.capturing() ? 1 : 0, plan.bn,
+                         plan.chunks, plan.stages, plan.kbs, static_cast<int>(plan.smem_bytes), plan.cpc,
+                         plan.cluster});
     return cuda_status(err);
 }
 
@@ -143,11 +144,11 @@ int run_partial_pass(const void *A, const void *B, float *P, float *out, int64_t
 int run_reduce(const float *P, float *out, int64_t S, int64_t M, int64_t N, cudaStream_t stream)
 {
     const splitk::Span reads[1] = {splitk::span_of(P, static_cast<uint64_t>(S * M * N) * 4)};
-    splitk::ChainGuard chain(stream, reads, 1);
+    const splitk::Span writes[1] = {splitk::span_of(out, static_cast<uint64_t>(M * N) * 4)};
+    splitk::ChainGuard chain(stream, reads, 1, writes, 1);
     const bool head = chain.capturing() && chain.fresh();
     const cudaError_t err = splitk::launch_reduce(P, out, S, M * N, chain.overlap(), !head, stream);
-    const splitk::Span writes[1] = {splitk::span_of(out, static_cast<uint64_t>(M * N) * 4)};
-    chain.commit(writes, 1, err == cudaSuccess, head);
+    chain.commit(err == cudaSuccess, head);
     return cuda_status(err);
 }
 
@@ -367,7 +368,7 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
     if (st != SPLITK_OK) return st;
     if (elem_bytes(dtype) == 0) return SPLITK_ERR_DTYPE;
     if (!info) return SPLITK_ERR_NULL;
-    std::fill(info, info + 22, 0);
+    std::fill(info, info + 25, 0);
     const bool x3 = dtype == SPLITK_F32;
     // gemm_bt runs the two kernels where the fused launch could not sum a
     // tile's splits inside one resident cluster
@@ -399,6 +400,9 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
         info[19] = c.compact ? c.stages : 0;
         info[20] = c.compact ? c.kbs : 0;
         info[21] = c.compact ? static_cast<int>(c.smem_bytes) : 0;
+        info[22] = c.compact ? c.cpc : 0;
+        info[23] = c.compact ? c.cluster : 0;
+        info[24] = c.compact ? static_cast<int>(c.grid.z) : 0;
     }
     return SPLITK_OK;
 }
@@ -422,6 +426,8 @@ int splitk_last_launch(int *info)
     info[5] = r.stages;
     info[6] = r.kbs;
     info[7] = r.smem_bytes;
+    info[8] = r.cpc;
+    info[9] = r.cluster;
     return SPLITK_OK;
 }
 

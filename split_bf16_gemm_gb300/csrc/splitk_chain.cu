@@ -9,7 +9,10 @@
 // of its own previous launch, it knows which device memory every launch of
 // the chain since then writes.  If the new launch reads none of it, it may
 // load and multiply before the previous grid ends, waiting only before its
-// first store ("overlap").
+// first store ("overlap").  If no launch of the chain reads or writes what
+// the new one writes either, it stores at once too and waits for the
+// previous grid only before it finishes ("store early"): the grids still
+// finish in launch order.
 //
 // Which launches can still be running when an overlapping launch starts:
 // a "head" -- a launch that waits at its start and lets the next grid start
@@ -20,8 +23,9 @@
 // own CTAs have started.  So a launch can meet
 // every launch from the last head on, and the window it is checked against
 // is exactly that run: [head, ..., previous].  Every launch also waits for
-// the previous grid before its first store, so the grids finish in order and
-// no launch overwrites what an earlier one still reads.
+// the previous grid before it finishes, so the grids finish in order, and
+// before its first store unless nothing in that run reads or writes what it
+// writes, so no launch overwrites what an earlier one still reads or writes.
 //
 // Eager launches (no capture) always wait: the library cannot see what else
 // the caller put on the stream.  splitk_set_overlap(0) turns the mechanism off.
@@ -41,8 +45,8 @@ constexpr int kWindow = 32;    // launches a new one is checked against, at most
 
 struct Entry {
     cudaGraphNode_t node;
-    Span writes[kMaxSpans];
-    int n_writes;
+    Span reads[kMaxSpans], writes[kMaxSpans];
+    int n_reads, n_writes;
 };
 
 struct Chain {
@@ -94,8 +98,14 @@ thread_local LaunchRecord t_last = {};
 void note_launch(const LaunchRecord &r) { t_last = r; }
 LaunchRecord last_launch() { return t_last; }
 
-ChainGuard::ChainGuard(cudaStream_t stream, const Span *reads, int n_reads) : stream_(stream)
+ChainGuard::ChainGuard(cudaStream_t stream, const Span *reads, int n_reads, const Span *writes, int n_writes)
+    : stream_(stream)
 {
+    if (n_reads > kMaxSpans || n_writes > kMaxSpans) return;   // not followed: the launch waits
+    n_reads_ = n_reads;
+    n_writes_ = n_writes;
+    for (int r = 0; r < n_reads; ++r) reads_[r] = reads[r];
+    for (int w = 0; w < n_writes; ++w) writes_[w] = writes[w];
     if (!g_enabled.load()) return;
     cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
     unsigned long long id = 0;
@@ -120,9 +130,17 @@ ChainGuard::ChainGuard(cudaStream_t stream, const Span *reads, int n_reads) : st
         return;
     }
     overlap_ = true;
+    store_early_ = true;
+    for (int i = 0; i < c->n && store_early_; ++i)
+        for (int w = 0; w < n_writes && store_early_; ++w) {
+            for (int x = 0; x < c->e[i].n_writes; ++x)
+                if (meets(c->e[i].writes[x], writes[w])) store_early_ = false;
+            for (int x = 0; x < c->e[i].n_reads; ++x)
+                if (meets(c->e[i].reads[x], writes[w])) store_early_ = false;
+        }
 }
 
-void ChainGuard::commit(const Span *writes, int n_writes, bool launched, bool head)
+void ChainGuard::commit(bool launched, bool head)
 {
     if (!capturing_) return;
     cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
@@ -132,7 +150,7 @@ void ChainGuard::commit(const Span *writes, int n_writes, bool launched, bool he
     Chain *c = find_chain(id_);
     const bool ok = launched &&
                     cudaStreamGetCaptureInfo(stream_, &st, &id, nullptr, &deps, nullptr, &nd) == cudaSuccess &&
-                    st == cudaStreamCaptureStatusActive && id == id_ && nd == 1 && n_writes <= kMaxSpans;
+                    st == cudaStreamCaptureStatusActive && id == id_ && nd == 1;
     if (!ok) {
         if (c) c->used = false;   // unknown state: the next launch waits and starts afresh
         return;
@@ -150,8 +168,10 @@ void ChainGuard::commit(const Span *writes, int n_writes, bool launched, bool he
     }
     Entry &e = c->e[c->n++];
     e.node = deps[0];
-    e.n_writes = n_writes;
-    for (int w = 0; w < n_writes; ++w) e.writes[w] = writes[w];
+    e.n_reads = n_reads_;
+    e.n_writes = n_writes_;
+    for (int r = 0; r < n_reads_; ++r) e.reads[r] = reads_[r];
+    for (int w = 0; w < n_writes_; ++w) e.writes[w] = writes_[w];
     c->stamp = ++g_clock;
 }
 

@@ -21,6 +21,7 @@ struct GemmProblem {
     bool b_kn = false;  // B given as the [K,N] weight itself (read MN-major)
     bool f32 = false;   // F32 operands: 3xTF32 products on the tensor cores (bf16 ignored)
     bool overlap = false; // no launch that may still run writes A or B: load before the previous grid ends
+    bool store_early = false; // (with overlap) none reads or writes P or out either: store before that too
     bool acc_probe = false; // time-out self-test: the wait for the accumulator gives up at once
 };
 
@@ -47,6 +48,7 @@ struct TilePlan {
     int tile_m;         // rows of A per CTA: 128, or 256 (two accumulators; BN 256, one CTA per tile)
     int compact;        // the ring cut so that two CTAs fit on an SM (same tiles, chunks and sums)
     int recv_in_ring;   // the peers' shares land inside the stage ring once the MMAs are done
+    int cpc;            // chunks per CTA: 1, or (merged compact plans) every chunk of the split
     dim3 grid;
     size_t smem_bytes;  // dynamic shared memory per CTA
 };
@@ -59,8 +61,10 @@ constexpr int kMaxChunks = 8;  // portable cluster size
 
 // Tile choice for a shape (automatic, or the process-wide override).
 // x3: F32 operands as 3xTF32 (else 16-bit operands).
-// compact: the layout that lets two CTAs share an SM, where that plan exists
-// (plan.compact says whether it was taken).
+// compact: the layout that lets two or three CTAs share an SM, where that
+// plan exists (plan.compact says whether it was taken).
+// A fused compact plan may give each CTA all the chunks of its split
+// (plan.cpc > 1).
 TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3 = false,
                  bool compact = false);
 // The planner's estimate (microseconds) of one tensor-core launch of that
@@ -95,32 +99,36 @@ constexpr int kMaxSpans = 3;
 // to commit(), so the two see the same chain.
 class ChainGuard {
 public:
-    ChainGuard(cudaStream_t stream, const Span *reads, int n_reads);
+    ChainGuard(cudaStream_t stream, const Span *reads, int n_reads, const Span *writes, int n_writes);
     ChainGuard(const ChainGuard &) = delete;
     ChainGuard &operator=(const ChainGuard &) = delete;
     bool capturing() const { return capturing_; }
     // no launch that may still be running writes what this one reads
     bool overlap() const { return overlap_; }
+    // (with overlap) none reads or writes what this one writes either
+    bool store_early() const { return store_early_; }
     // no earlier launch of this library precedes it in the capture (or the
     // window was full): a head that independent launches may follow
     bool fresh() const { return fresh_; }
-    // after the launch: record its writes (or forget the chain if it
-    // failed); `head`: it waited for the previous grid before letting the
-    // next one start, so nothing before it can still be running then
-    void commit(const Span *writes, int n_writes, bool launched, bool head);
+    // after the launch: record its reads and writes (or forget the chain if
+    // it failed); `head`: it waited for the previous grid before letting
+    // the next one start, so nothing before it can still be running then
+    void commit(bool launched, bool head);
 
 private:
     cudaStream_t stream_;
     std::unique_lock<std::mutex> lock_;
     unsigned long long id_ = 0;
-    bool capturing_ = false, overlap_ = false, fresh_ = false;
+    bool capturing_ = false, overlap_ = false, fresh_ = false, store_early_ = false;
+    Span reads_[kMaxSpans], writes_[kMaxSpans];
+    int n_reads_ = 0, n_writes_ = 0;
 };
 void set_overlap_enabled(bool on);
 bool overlap_enabled();
 
 // What the last tensor-core launch of this host thread did (splitk_last_launch).
 struct LaunchRecord {
-    int overlap, compact, capturing, bn, chunks, stages, kbs, smem_bytes;
+    int overlap, compact, capturing, bn, chunks, stages, kbs, smem_bytes, cpc, cluster;
 };
 void note_launch(const LaunchRecord &r);
 LaunchRecord last_launch();

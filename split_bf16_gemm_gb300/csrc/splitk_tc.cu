@@ -92,8 +92,11 @@ struct TcArgs {
     uint64_t a_bytes, b_bytes;
     int prefetchers;       // CTAs, first in dispatch order, that prefetch A and B into L2
     int rows_first;        // blockIdx.x is the row tile and blockIdx.y the column tile
-    int overlap;           // load before the previous grid ends (nothing in flight writes A or B)
+    int overlap;           // 0: wait for the previous grid before the first load; 1: load at once,
+                           // wait before the first store; 2: load and store at once, wait
+                           // before finishing (no launch in flight reads or writes the outputs)
     int recv_in_ring;      // the peers' shares land in the stage ring, once its MMAs are done
+    int cpc;               // chunks per CTA: 1, or every chunk of a split, each in its own accumulator
 };
 
 // Part j of `parts` (whole 128-byte lines) of [p, p + bytes) into L2, one
@@ -257,6 +260,11 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
     __shared__ int issued_s, consumed_s;
     __shared__ unsigned abort_s;
 
+    // An overlapping launch lets the next grid start at once: its CTAs then
+    // take the slots that free up while this grid runs.  (On GB300 the
+    // headline shape went from 3.84 to 3.60 us per operation in graphs of
+    // eight against releasing after the set-up.)
+    if (args.overlap) ptx::launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int stages = args.stages;
     const uint32_t raw = ptx::smem_addr(dsmem);
@@ -268,14 +276,20 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
 
     const int n_tile = args.rows_first ? blockIdx.y : blockIdx.x;
     const int m_tile = args.rows_first ? blockIdx.x : blockIdx.y;
-    const int C = args.chunks;
-    const int s = blockIdx.z / C;
-    const int c = blockIdx.z - s * C;
-    const int rank = static_cast<int>(blockIdx.z) % Q;  // in the 1 x 1 x Q cluster: the chunk, or split*C+chunk
+    // A CTA covers cpc consecutive chunks of one split, each summed in its
+    // own accumulator (cpc > 1 only for 16-bit, 128-row plans whose chunks
+    // are whole k-blocks of whole stages): the same products, chunk sums and
+    // order as one CTA per chunk, with the chunk sum taken before the
+    // exchange.  CC CTAs cover a split.
+    const int cpc = args.cpc;
+    const int CC = args.chunks / cpc;
+    const int s = blockIdx.z / CC;
+    const int c = (blockIdx.z - s * CC) * cpc;      // its first chunk
+    const int rank = static_cast<int>(blockIdx.z) % Q;  // in the 1 x 1 x Q cluster: split*CC + CTA of the split
     const int ks = s * args.kps;
     const int ke = min(ks + args.kps, args.K);      // the last split clamps to K
     const int k_lo = ks + c * args.chunk_len;
-    const int k_hi = min(k_lo + args.chunk_len, ke);
+    const int k_hi = min(k_lo + cpc * args.chunk_len, ke);
     const int klen = k_hi > k_lo ? k_hi - k_lo : 0; // a chunk past a short split is empty
     const int nkb = (klen + KB - 1) / KB;
     const int share = args.share;
@@ -347,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
         for (int i = 0; i < pre; ++i) issue_stage(i, i);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_addr(&tmem_slot), Sh::kTmemCols);
+        ptx::tmem_alloc(ptx::smem_addr(&tmem_slot), Sh::kTmemCols * static_cast<uint32_t>(cpc));
         ptx::tmem_relinquish();
     }
     if (warp >= 2) {
@@ -369,25 +383,32 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
     // arrival itself needs no release semantics.  With the receive slots in
     // the ring, this CTA arrives only once its MMAs have read the ring.
     if (Q > 1 && !args.recv_in_ring) ptx::cluster_arrive_relaxed();
-    // Overlapping, the next grid is released at once; otherwise after the
-    // wait.  (Written as one conditional wait and an unconditional release:
-    // the same choice as two branches measured 0.1-0.4 us slower per launch
-    // on GB300, in both modes.)
+    // Without overlap the next grid is released after the wait (an
+    // overlapping launch released it at its start; a second release is a
+    // no-op).  (Written as one conditional wait and an unconditional
+    // release: the same choice as two branches measured 0.1-0.4 us slower
+    // per launch on GB300, in both modes.)
     if (!args.overlap) ptx::grid_dependency_wait();
     ptx::launch_dependents();
     const uint32_t tmem = tmem_slot;
 
     if (warp == 0 && lane == 0) {
-        // ---- TMA producer: the stages that had to wait for a free slot
+        // ---- TMA producer: the stages that had to wait for a free slot.
+        // Slot and phase advance by counting (no division per stage: the
+        // loops below are on the path from a landing to the next load).
         int i = pre;
+        int st = pre == stages ? 0 : pre;
+        uint32_t ph = pre == stages ? 1u : 0u;
         for (; i < nstg; ++i) {
-            const int st = i % stages;
-            const uint32_t ph = (i / stages) & 1;
             if (!ptx::mbar_wait_bounded(empty_bar(st), ph ^ 1u, args.wait_limit_ns)) {
                 atomicOr(&abort_s, 1u);
                 break;
             }
             issue_stage(i, st);
+            if (++st == stages) {
+                st = 0;
+                ph ^= 1u;
+            }
         }
         issued_s = i;
     } else if (warp == 1 && lane == 0) {
@@ -408,28 +429,29 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
         const uint32_t b_lbo = static_cast<uint32_t>(kbs) * 8192u;   // [K,N]: next 64 columns
         const uint32_t lo_half = load_bytes >> 4;                     // X3: the lo parts, in descriptor units
         const bool short_tail = (klen % KB) != 0;   // a 2-D 16-bit chunk may end in a 32-long k-block
+        const int kpc = args.chunk_len / KB;        // k-blocks per chunk (a multiple of kbs when cpc > 1)
         // one K step of k-block slice (a, b) (low descriptor words)
-        auto issue = [&](uint32_t a, uint32_t b, uint32_t ahi, uint32_t bhi, int k, uint32_t accumulate) {
+        auto issue = [&](uint32_t d, uint32_t a, uint32_t b, uint32_t ahi, uint32_t bhi, int k, uint32_t accumulate) {
             if constexpr (X3) {
                 // the small products first, then hi*hi; +32 bytes (8 F32) along K per step
-                ptx::mma_tf32(tmem, ptx::desc64(a + 2u * k, ahi), ptx::desc64(b + lo_half + 2u * k, bhi), idesc,
+                ptx::mma_tf32(d, ptx::desc64(a + 2u * k, ahi), ptx::desc64(b + lo_half + 2u * k, bhi), idesc,
                               accumulate);
-                ptx::mma_tf32(tmem, ptx::desc64(a + lo_half + 2u * k, ahi), ptx::desc64(b + 2u * k, bhi), idesc, 1u);
-                ptx::mma_tf32(tmem, ptx::desc64(a + 2u * k, ahi), ptx::desc64(b + 2u * k, bhi), idesc, 1u);
+                ptx::mma_tf32(d, ptx::desc64(a + lo_half + 2u * k, ahi), ptx::desc64(b + 2u * k, bhi), idesc, 1u);
+                ptx::mma_tf32(d, ptx::desc64(a + 2u * k, ahi), ptx::desc64(b + 2u * k, bhi), idesc, 1u);
             } else {
                 // A: +32 bytes along K inside its swizzled rows.  B: the same,
                 // or for the [K,N] weight 16 k-rows of 128 bytes further (2 KB)
                 const uint32_t bk = b + (KN ? 128u : 2u) * k;
-                ptx::mma_f16(tmem, ptx::desc64(a + 2u * k, ahi), ptx::desc64(bk, bhi), idesc, accumulate);
+                ptx::mma_f16(d, ptx::desc64(a + 2u * k, ahi), ptx::desc64(bk, bhi), idesc, accumulate);
                 if constexpr (TM == 2 * kTileM)   // rows 128-255: 16 KB further, the second accumulator
-                    ptx::mma_f16(tmem + BN, ptx::desc64(a + 1024u + 2u * k, ahi), ptx::desc64(bk, bhi), idesc,
+                    ptx::mma_f16(d + BN, ptx::desc64(a + 1024u + 2u * k, ahi), ptx::desc64(bk, bhi), idesc,
                                  accumulate);
             }
         };
-        int i = 0;
+        int i = 0, st = 0;
+        uint32_t ph = 0;
+        int jc = 0, kb_in = 0;   // cpc > 1: the chunk (accumulator) of the stage, its first k-block in it
         for (; i < nstg; ++i) {
-            const int st = i % stages;
-            const uint32_t ph = (i / stages) & 1;
             if (!ptx::mbar_wait_bounded(X3 ? conv_bar(st) : full_bar(st), ph, args.wait_limit_ns)) {
                 atomicOr(&abort_s, 2u);
                 break;
@@ -443,7 +465,13 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
             const uint32_t blo = static_cast<uint32_t>(b0), bhi = static_cast<uint32_t>(b0 >> 32);
             const int kb0 = i * kbs;
             const int nk = min(kbs, nkb - kb0);
-            uint32_t accumulate = i > 0 ? 1u : 0u;   // the chunk's first MMA starts the accumulator
+            // the chunk's first MMA starts its accumulator
+            const uint32_t d = tmem + static_cast<uint32_t>(jc * BN);
+            uint32_t accumulate = (cpc > 1 ? kb_in : i) > 0 ? 1u : 0u;
+            if (cpc > 1 && (kb_in += kbs) == kpc) {
+                kb_in = 0;
+                ++jc;
+            }
 #pragma unroll
             for (int j = 0; j < kMaxKbs; ++j) {
                 if (j >= nk) break;
@@ -457,18 +485,22 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
                     // contributed only the first K step on GB300.
 #pragma unroll
                     for (int k = 0; k < KB / KSTEP / 2; ++k) {
-                        issue(a, b, ahi, bhi, k, accumulate);
+                        issue(d, a, b, ahi, bhi, k, accumulate);
                         accumulate = 1u;
                     }
                 } else {
 #pragma unroll
                     for (int k = 0; k < KB / KSTEP; ++k) {
-                        issue(a, b, ahi, bhi, k, accumulate);
+                        issue(d, a, b, ahi, bhi, k, accumulate);
                         accumulate = 1u;
                     }
                 }
             }
             ptx::mma_commit(empty_bar(st));    // frees the slot once these MMAs have read it
+            if (++st == stages) {
+                st = 0;
+                ph ^= 1u;
+            }
         }
         consumed_s = i;
         ptx::mma_commit(acc_bar);              // the accumulator is final
@@ -476,9 +508,9 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
         // ---- converters (warps 2-7): the lo parts of each landed stage go to
         // the second half, then the stage is handed to the MMA issuer
         const int t = tid - 64;
+        int st = 0;
+        uint32_t ph = 0;
         for (int i = 0; i < nstg; ++i) {
-            const int st = i % stages;
-            const uint32_t ph = (i / stages) & 1;
             if (!ptx::mbar_wait_bounded(full_bar(st), ph, args.wait_limit_ns)) {
                 atomicOr(&abort_s, 8u);
                 break;
@@ -505,6 +537,10 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
             ptx::fence_proxy_async_smem();     // the tensor cores read what these threads wrote
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(conv_bar(st));
+            if (++st == stages) {
+                st = 0;
+                ph ^= 1u;
+            }
         }
     }
     // time-out self-test: the warps that wait for the accumulator and take no
@@ -542,18 +578,52 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
         if (h > 0) __syncthreads();
 #pragma unroll 1
         for (int jb = half * (BN / 64); jb < (half + 1) * (BN / 64); ++jb) {
-            uint32_t v[32];
-            if (have_acc) {
-                ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(h * BN + jb * 32), v);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0u;
-            }
             const uint32_t row_addr = E + static_cast<uint32_t>(jb * 4 + quarter) * 4096u + lane * 128u;
+            if (cpc == 1) {
+                uint32_t v[32];
+                if (have_acc) {
+                    ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(h * BN + jb * 32), v);
+                } else {
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                ptx::st_shared_v4(row_addr + (static_cast<uint32_t>(q ^ (lane & 7)) << 4), v[4 * q],
-                                  v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    for (int i = 0; i < 32; ++i) v[i] = 0u;
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    ptx::st_shared_v4(row_addr + (static_cast<uint32_t>(q ^ (lane & 7)) << 4), v[4 * q],
+                                      v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
+                // the chunk sum: chunk 0 + chunk 1 + ... in order, a chunk
+                // past the split's end adding +0 -- what the owner adds when
+                // each chunk has its own CTA.  16 columns at a time.
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t v[16];
+                    const uint32_t col = static_cast<uint32_t>(jb * 32 + hh * 16);
+                    if (have_acc) {
+                        ptx::tmem_ld_32x32b_x16(lane_base + col, v);
+#pragma unroll 1
+                        for (int j = 1; j < cpc; ++j) {
+                            uint32_t w[16];
+                            if (k_lo + j * args.chunk_len < k_hi) {
+                                ptx::tmem_ld_32x32b_x16(lane_base + static_cast<uint32_t>(j * BN) + col, w);
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) w[i] = 0u;
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(w[i]));
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = 0u;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        ptx::st_shared_v4(row_addr + (static_cast<uint32_t>((hh * 4 + q) ^ (lane & 7)) << 4),
+                                          v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
+            }
         }
         ptx::fence_proxy_async_smem();             // the staging is the source of bulk copies
         // ---- exchange: each warp pushes the boxes it staged to their owners
@@ -584,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
             if (aborted) ptx::mbar_wait_bounded(acc_bar, 0, args.wait_limit_ns);
             __syncwarp();
             ptx::tc_fence_after_sync();
-            ptx::tmem_dealloc(tmem, Sh::kTmemCols);
+            ptx::tmem_dealloc(tmem, Sh::kTmemCols * static_cast<uint32_t>(cpc));
         }
         if (!ptx::mbar_wait_bounded(recv_bar, 0, args.wait_limit_ns) && tid == 0) atomicOr(&g_device_status, 16u);
         if (Q > 1) ptx::cluster_arrive_relaxed();  // everything bound for this CTA has landed
@@ -595,8 +665,9 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
         // each thread loads both of its pieces (2 x Q float4) before it adds and
         // stores.
         // the first global stores: the previous grid must have finished (it
-        // may still read what these overwrite, or write the same outputs)
-        if (args.overlap) ptx::grid_dependency_wait();
+        // may still read what these overwrite, or write the same outputs),
+        // unless no launch in flight reads or writes them (overlap 2)
+        if (args.overlap == 1) ptx::grid_dependency_wait();
         const int row0 = m_tile * TM + h * kTileM, col0 = n_tile * BN;
         const size_t MN = static_cast<size_t>(args.M) * args.N;
         const int rows_here = args.M - row0;                               // tile rows below M
@@ -613,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
             for (int r = 0; r < Q; ++r) v[r] = ptx::ld_shared_v4(rbase[r] + p.off);
         };
         auto tile_elem = [&](const Piece &p) { return tile0 + static_cast<size_t>(p.row) * args.N + p.col; };
-        // the chunk sum of one split (Q == C): chunks in order 0, 1, 2, ...
+        // the chunk sum of one split (Q == CC): chunks in order 0, 1, 2, ...
         auto chunk_sum = [&](const float4 (&v)[Q]) {
             float4 acc = v[0];
 #pragma unroll
@@ -633,13 +704,16 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
                 if (g1 < my_hi && p1.row < rows_here) *reinterpret_cast<float4 *>(Ps + tile_elem(p1)) = a1;
             }
         } else if (args.P != nullptr) {
-            cluster_split_sum_for<Q, true>(C, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, args.P,
+            cluster_split_sum_for<Q, true>(CC, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, args.P,
                                            args.out);
         } else {
-            cluster_split_sum_for<Q, false>(C, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, nullptr,
+            cluster_split_sum_for<Q, false>(CC, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, nullptr,
                                             args.out);
         }
     }
+    // overlap 2 stored without waiting: the grid still finishes after the
+    // previous one, so that grids finish in launch order
+    if (args.overlap == 2) ptx::grid_dependency_wait();
     if (Q > 1) ptx::cluster_wait();            // no CTA leaves while its staging may still be copied from
 }
 
@@ -1112,6 +1186,7 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     }
     const StageChoice sc = pick_stages(bn, nkb, can3d, q, share, x3, tm);
     TilePlan p = {};
+    p.cpc = 1;
     p.tile_m = tm;
     p.bn = bn;
     p.chunks = chunks;
@@ -1167,30 +1242,59 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     // operation; launches of 64 CTAs already hold four operations at once
     // with two per SM and ran slower with the smaller ring (M256 N512 K2048
     // S4: 3.55 against 3.28 us).
+    //
+    // Merged chunks: a fused compact plan whose chunks are whole k-blocks
+    // gives each CTA all the chunks of its split, each in its own
+    // accumulator, and the CTA adds them in chunk order before the exchange
+    // -- the same sums as one CTA per chunk, with 1/chunks of the CTAs, each
+    // loading its split's whole K range, and a cluster of the splits only.
+    // Launched back to back in a graph such CTAs spend less of their time on
+    // the fixed parts (set-up, staging, exchange, stores), exchange a
+    // quarter of the bytes, and keep three to an SM: on GB300 the headline
+    // shape went from 3.61 to 3.21 us per operation in graphs of eight, with
+    // the stores made before the wait for the previous grid.
     p.compact = 0;
     p.recv_in_ring = 0;
-    if (compact && !x3 && tm == kTileM && bn <= 128 && clusters <= resident_clusters(q)) {
+    const auto try_compact = [&](int cpc) {
+        const int qc = q / cpc;
+        const int64_t cctas = ctas / cpc;
+        if (clusters > resident_clusters(qc)) return false;
+        const int cshare = share_for(bn, qc);
+        const int cnkb = nkb * cpc;   // k-blocks of a CTA
         const auto double_buffered = [&](const StageChoice &c) {
-            return c.ok && c.stages >= std::min(2, (nkb + c.kbs - 1) / c.kbs);
+            return c.ok && c.stages >= std::min(2, (cnkb + c.kbs - 1) / c.kbs) && (cpc == 1 || nkb % c.kbs == 0);
         };
         StageChoice cc;
-        if (q <= 4 && ctas > resident_clusters(1) / 2)
-            cc = pick_stages(bn, nkb, can3d, q, share, x3, tm, kCompact3SmemLimit, q > 1);
-        if (!double_buffered(cc)) cc = pick_stages(bn, nkb, can3d, q, share, x3, tm, kCompactSmemLimit, q > 1);
-        if (double_buffered(cc)) {
-            p.compact = 1;
-            p.recv_in_ring = q > 1 ? 1 : 0;
-            p.stages = cc.stages;
-            p.kbs = can3d ? cc.kbs : 1;
-            p.three_d = can3d && p.kbs > 1 ? 1 : 0;
-            const size_t in_ring = epi_bytes(bn) + (q > 1 ? static_cast<size_t>(q - 1) * share * 16 : 0);
-            p.region0 = static_cast<uint32_t>(
-                round_up(std::max(p.stages * stage_bytes(bn, p.kbs, x3, tm), in_ring), 1024));
-            p.smem_bytes = smem_for(bn, p.kbs, p.stages, q, share, x3, tm, q > 1);
-            // two or three CTAs to an SM: as many start beside a running launch as it has CTAs
-            p.prefetchers = static_cast<int>(std::min<int64_t>(ctas, 2 * resident_clusters(q) * q - ctas));
-            if (p.prefetchers < 0) p.prefetchers = 0;
-        }
+        if (qc <= 4 && (cctas > resident_clusters(1) / 2 || cpc > 1))
+            cc = pick_stages(bn, cnkb, can3d, qc, cshare, x3, tm, kCompact3SmemLimit, qc > 1);
+        if (!double_buffered(cc)) cc = pick_stages(bn, cnkb, can3d, qc, cshare, x3, tm, kCompactSmemLimit, qc > 1);
+        if (!double_buffered(cc)) return false;
+        p.compact = 1;
+        p.cpc = cpc;
+        p.cluster = qc;
+        p.share = cshare;
+        p.recv_in_ring = qc > 1 ? 1 : 0;
+        p.stages = cc.stages;
+        p.kbs = can3d ? cc.kbs : 1;
+        p.three_d = can3d && p.kbs > 1 ? 1 : 0;
+        // the staging area and the receive slots inside the ring; and at
+        // least 512 bytes per tensor-memory column (cpc accumulators), so
+        // that the CTAs that fit on an SM by shared memory, of any of these
+        // launches, always fit in its 512 columns
+        const size_t in_ring = epi_bytes(bn) + (qc > 1 ? static_cast<size_t>(qc - 1) * cshare * 16 : 0);
+        const size_t tmem_floor = static_cast<size_t>(bn) * cpc * 512;
+        p.region0 = static_cast<uint32_t>(
+            round_up(std::max({p.stages * stage_bytes(bn, p.kbs, x3, tm), in_ring, tmem_floor}), 1024));
+        p.smem_bytes = static_cast<size_t>(p.region0) + 1024;
+        p.grid.z = static_cast<unsigned>(S * chunks / cpc);
+        // two or three CTAs to an SM: as many start beside a running launch as it has CTAs
+        p.prefetchers = static_cast<int>(std::min<int64_t>(cctas, 2 * resident_clusters(qc) * qc - cctas));
+        if (p.prefetchers < 0) p.prefetchers = 0;
+        return true;
+    };
+    if (compact && !x3 && tm == kTileM && bn <= 128) {
+        const bool mergeable = split_sum == 2 && chunks > 1 && bn * chunks <= 128 && can3d && chunk_len % kBlockK == 0;
+        if (!(mergeable && try_compact(chunks))) try_compact(1);
     }
     return p;
 }
@@ -1200,7 +1304,14 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
 cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t stream)
 {
     const bool chunks_ok = (plan.chunks & (plan.chunks - 1)) == 0 && plan.chunks >= 1 && plan.chunks <= kMaxChunks &&
-                           plan.cluster % plan.chunks == 0;
+                           (plan.cluster * plan.cpc) % plan.chunks == 0;
+    // several chunks per CTA: each its own accumulator (at most 128 tensor-
+    // memory columns in all), its chunks whole k-blocks of whole stages
+    const bool cpc_ok = plan.cpc == 1 ||
+                        (plan.cpc == plan.chunks && !plan.x3 && plan.tile_m == kTileM && plan.bn * plan.cpc <= 128 &&
+                         plan.chunk_len % kBlockK == 0 && (plan.chunk_len / kBlockK) % plan.kbs == 0 &&
+                         static_cast<int64_t>(plan.grid.z) * plan.cpc == pr.S * plan.chunks);
+    if (!cpc_ok) return note_error(cudaErrorInvalidConfiguration, "chunks per CTA out of range");
     if (plan.cluster > kMaxChunks || plan.stages > kMaxStages || plan.kbs < 1 || plan.kbs > kMaxKbs ||
         plan.smem_bytes > kSmemLimit || !chunks_ok)
         return note_error(cudaErrorInvalidConfiguration, "tile plan out of range");
@@ -1256,8 +1367,9 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
     // once; prefetching them into L2 only adds requests
     a.prefetchers = pr.overlap ? 0 : plan.prefetchers;
     a.rows_first = plan.rows_first;
-    a.overlap = pr.overlap ? 1 : 0;
+    a.overlap = pr.overlap ? (pr.store_early ? 2 : 1) : 0;
     a.recv_in_ring = plan.recv_in_ring && plan.cluster > 1 ? 1 : 0;
+    a.cpc = plan.cpc;
     // operand variants: [N,K] weight, [K,N] weight, F32 as 3xTF32
     const int variant = pr.f32 ? 2 : pr.b_kn ? 1 : 0;
     if (plan.tile_m == 2 * kTileM)

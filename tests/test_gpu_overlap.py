@@ -2,12 +2,15 @@
 CUDA graph capture ("overlap"; include/splitk.h, top comment).
 
 The library may let a launch load before the previous grid ends only where no
-launch that can still be running writes what the new one reads; every launch
-still waits for the previous grid before its first store.  Each test captures
-a sequence of calls, checks which launches overlapped (splitk_last_launch,
-read right after each call), replays the graph several times and compares
-every output bitwise with the same calls made eagerly, where each launch
-waits for the one before it.  The eager results themselves are pinned to the
+launch that can still be running writes what the new one reads (overlap 1);
+it also stores before that grid ends only where none of them reads or
+writes what the new one writes (overlap 2), and every launch still waits for
+the previous grid before it finishes.  A fused launch that overlaps may give
+each thread block all the chunks of its split (chunks_per_block > 1), with
+the same sums.  Each test captures a sequence of calls, checks which launches
+overlapped (splitk_last_launch, read right after each call), replays the
+graph several times and compares every output bitwise with the same calls
+made eagerly, where each launch waits for the one before it.  The eager results themselves are pinned to the
 F64 oracle by test_gpu_parity.py; the headline case is checked against the
 oracle here too.
 """
@@ -71,6 +74,8 @@ def instances(sk, M, N, K, S, kps, dt, n, seed0=0):
     (256, 512, 2048, 4, 512),
     (32, 64, 128, 2, 64),         # the single tile
     (160, 192, 320, 3, 128),      # M tail, three splits (two kernels)
+    (256, 1024, 1920, 2, 1024),   # the last split's second chunk short
+    (256, 1024, 1536, 2, 1024),   # ... and empty
 ])
 @pytest.mark.parametrize("fused", [1, 3])
 def test_independent_calls_overlap_bitwise(lib, shape, fused):
@@ -94,11 +99,15 @@ def test_independent_calls_overlap_bitwise(lib, shape, fused):
     assert all(d["capturing"] == 1 for d in seen)
     assert seen[0]["overlap"] == 0                       # nothing of ours precedes it
     # fused in one launch: each call reads only its own A and B, which no
-    # earlier call writes.  Two kernels: each call's partial pass follows the
-    # previous call's reduce, whose output it does not read.
-    assert all(d["overlap"] == 1 for d in seen[1:]), seen
-    if in_kernel and (M, N, K) == (256, 1024, 2048):
+    # earlier call writes, and writes only its own output and workspace.
+    # Two kernels: each call's partial pass follows the previous call's
+    # reduce, whose output it neither reads nor writes.
+    assert all(d["overlap"] == 2 for d in seen[1:]), seen
+    if in_kernel and N == 1024:
         assert all(d["compact"] == 1 for d in seen), seen
+        # every compact launch takes both chunks of its split (512 each,
+        # 64-column tiles) into one block: a cluster of the splits only
+        assert all(d["chunks_per_block"] == 2 and d["cluster"] == S for d in seen), seen
     for _ in range(3):
         for it in insts:
             it["out"].fill_(7.0)
@@ -119,10 +128,10 @@ def test_independent_calls_overlap_bitwise(lib, shape, fused):
 def test_dependent_chain_waits(lib):
     """F32 operands, so that an output can be the next call's A.  Expected:
     a: X -> Y          head (no call of ours before it): waits
-    b: P -> Q          independent of a: overlaps
+    b: P -> Q          independent of a: overlaps, stores early
     c: Y -> Z          reads Y, which a (still in b's window) writes: waits
     d: Z -> W          reads what c writes: waits
-    e: R -> T          independent of d: overlaps
+    e: R -> T          independent of d: overlaps, stores early
     f: (U, Q) -> V     reads Q, written by b before the wait in c: overlaps
     g: W -> Y2         reads W, written by d (in the window d, e, f): waits"""
     sk = lib
@@ -157,7 +166,7 @@ def test_dependent_chain_waits(lib):
     ref = {k: v.clone() for k, v in outs.items()}
     seen = []
     g = capture(lambda: run(seen))
-    assert seen == [("a", 0), ("b", 1), ("c", 0), ("d", 0), ("e", 1), ("f", 1), ("g", 0)], seen
+    assert seen == [("a", 0), ("b", 2), ("c", 0), ("d", 0), ("e", 2), ("f", 2), ("g", 0)], seen
     for _ in range(3):
         for v in outs.values():
             v.fill_(7.0)
@@ -170,8 +179,9 @@ def test_dependent_chain_waits(lib):
 
 def test_store_waits_for_previous_reader(lib):
     """b overlaps a (it reads neither Y nor anything a writes), but b's output
-    is a's input X: b may load early, yet must not store before a has read X.
-    The graph is replayed from the same starting X each time."""
+    is a's input X: b may load early, yet must not store before a has read X
+    (overlap 1, not 2).  The graph is replayed from the same starting X each
+    time."""
     sk = lib
     dt = "f32"
     M, N, K, S, kps = 128, 256, 256, 2, 128
@@ -231,7 +241,7 @@ def test_other_work_between_calls_waits(lib):
             record.append(sk.splitk_last_launch()["overlap"])
 
     g = capture(lambda: run(seen))
-    assert seen == [0, 1]
+    assert seen == [0, 2]
     for rep in range(3):
         src.copy_(operands(M, N, K, dt, 100 + rep)[0])
         for it in insts:
@@ -288,7 +298,7 @@ def test_kn_layout_overlap_bitwise(lib):
             seen.append(sk.splitk_last_launch()["overlap"])
 
     g = capture(body)
-    assert seen == [0, 1, 1, 1]
+    assert seen == [0, 2, 2, 2]
     g.replay()
     torch.cuda.synchronize()
     for it in insts:
@@ -335,7 +345,7 @@ def test_reduce_heads_or_extends_runs(lib):
     torch.cuda.synchronize()
     seen = []
     g = capture(lambda: run(outs, fused_out, seen))
-    assert seen == [1, 1], seen
+    assert seen == [2, 2], seen
     for _ in range(3):
         for o in outs:
             o.fill_(7.0)
@@ -345,4 +355,33 @@ def test_reduce_heads_or_extends_runs(lib):
         for a, b in zip(outs, outs_ref):
             assert bitwise(a, b)
         assert bitwise(fused_out, fused_ref)
+    assert sk.splitk_get_device_status() == 0
+
+
+def test_store_waits_for_previous_writer(lib):
+    """b writes the output a writes (its own operands are independent): b may
+    load early but stores only after a has finished (overlap 1), so the
+    output holds b's result, as eagerly."""
+    sk = lib
+    M, N, K, S, kps, dt = 256, 1024, 2048, 2, 1024, "bf16"
+    insts = instances(sk, M, N, K, S, kps, dt, 2)
+    O = torch.full((M, N), 7.0, device="cuda")
+    seen = []
+
+    def run(record=None):
+        for it in insts:
+            sk.gemm_bt(it["A"], it["B"], O, it["ws"], it["nb"], M, N, K, S, kps, dt, fused=1)
+            if record is not None:
+                record.append(sk.splitk_last_launch()["overlap"])
+
+    run()
+    torch.cuda.synchronize()
+    ref = O.clone()
+    g = capture(lambda: run(seen))
+    assert seen == [0, 1]
+    for _ in range(5):
+        O.fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert bitwise(O, ref)
     assert sk.splitk_get_device_status() == 0

@@ -20,9 +20,12 @@ tests, and every tile override:
   pushes whole boxes), every 16-byte piece has exactly one owner, and every
   contribution sent to or read from a receive slot stays inside that slot;
 - the compact layout (taken inside graph captures): the same tiles, chunks
-  and cluster, a ring that still covers every k once, the receive slots
-  inside the ring after the staging area, and two thread blocks' shared and
-  tensor memory within one SM's.
+  and sums, a ring that still covers every k once, the receive slots inside
+  the ring after the staging area, and two or three thread blocks' shared
+  and tensor memory within one SM's; where a block takes every chunk of its
+  split (chunks_per_block > 1), each chunk starts on a stage boundary, its
+  accumulators fit the block's share of tensor memory, and the cluster
+  holds the splits only.
 """
 import itertools
 
@@ -128,46 +131,70 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
         assert d["fused_in_kernel"] == 1 and not x3 and TM == TILE_M and BN <= 128
         assert -(-M // TM) * (N // BN) * S * C // Q <= RESIDENT_CLUSTERS[Q]   # one wave
         cst, ckbs, csmem = d["compact_stages"], d["compact_kblocks_per_stage"], d["compact_smem_bytes"]
+        cpc, qc = d["compact_chunks_per_block"], d["compact_cluster"]
         assert 1 <= cst <= 8 and ckbs in (1, 2, 4) and (ckbs == 1 or T3)
+        # every chunk of a split in one block: only where the chunks are whole
+        # stages of whole k-blocks and the accumulators fit 128 columns
+        can3d = K % kb_elems == 0 and kps % kb_elems == 0
+        mergeable = SS == 2 and C > 1 and BN * C <= 128 and can3d and CL % 64 == 0
+        assert cpc in (1, C) and (cpc == 1 or mergeable)
+        assert qc == Q // cpc and d["compact_grid_z"] == S * C // cpc and d["compact_grid_z"] % qc == 0
+        assert -(-M // TM) * (N // BN) * S * C // Q <= RESIDENT_CLUSTERS[qc]
         cstage = (TM + BN) * 128 * ckbs
         nkb = -(-CL // kb_elems)
-        assert cst >= min(2, -(-nkb // ckbs))            # double-buffered unless one stage holds the chunk
-        recv_bytes = (Q - 1) * share * 16
-        cregion = -(-max(cst * cstage, epi_bytes + recv_bytes) // 1024) * 1024
+        cnkb = nkb * cpc                                  # k-blocks of a block
+        assert cst >= min(2, -(-cnkb // ckbs))            # double-buffered unless one stage holds them all
+        if cpc > 1:
+            assert nkb % ckbs == 0                        # a chunk's first k-block starts a stage
+        cshare = -(-(-(-pieces // qc)) // 8) * 8
+        recv_bytes = (qc - 1) * cshare * 16
+        cols = BN * cpc                                   # tensor memory: a power of two >= 32
+        cregion = -(-max(cst * cstage, epi_bytes + recv_bytes, cols * 512) // 1024) * 1024
         assert csmem == cregion + 1024 <= COMPACT_LIMIT
         assert 2 * (csmem + STATIC_SMEM + 1024) <= SM_SMEM   # two blocks to an SM
-        assert 2 * BN <= 512 and BN <= csmem // 512          # tensor memory: theirs fits, by the smem rule
-        # three to an SM for launches of more CTAs than half the SMs with
-        # clusters of at most 4, wherever a double-buffered ring of single
-        # k-block stages and the staging plus receive slots fit in 74 KB
-        ctas = -(-M // TM) * (N // BN) * S * C
+        assert cols & (cols - 1) == 0 and 2 * cols <= 512 and cols <= csmem // 512
+        # three to an SM for merged launches and for launches of more CTAs
+        # than half the SMs, with clusters of at most 4, wherever a
+        # double-buffered ring of single k-block stages and the staging plus
+        # receive slots fit in 74 KB
+        cctas = -(-M // TM) * (N // BN) * S * C // cpc
         kmin = kbs if (kbs and T3) else 1                    # the smallest stage the override allows
         stage1 = (TM + BN) * 128 * kmin
-        fits3 = max(min(2, -(-nkb // kmin)) * stage1, epi_bytes + recv_bytes) + 1024 <= COMPACT3_LIMIT
-        if Q <= 4 and ctas > 74 and fits3:
-            assert csmem <= COMPACT3_LIMIT and 3 * (csmem + STATIC_SMEM + 1024) <= SM_SMEM and 3 * BN <= 512
-        check_k_coverage(K, S, kps, C, CL, ckbs, int(ckbs > 1), kb_elems, elem)
-        if Q > 1:
-            check_exchange(BN, Q, epi_bytes, cregion)
+        fits3 = max(min(2, -(-cnkb // kmin)) * stage1, epi_bytes + recv_bytes, cols * 512) + 1024 <= COMPACT3_LIMIT
+        if qc <= 4 and (cctas > 74 or cpc > 1) and fits3:
+            assert csmem <= COMPACT3_LIMIT and 3 * (csmem + STATIC_SMEM + 1024) <= SM_SMEM and 3 * cols <= 512
+        check_k_coverage(K, S, kps, C, CL, ckbs, int(ckbs > 1), kb_elems, elem, cpc)
+        if qc > 1:
+            check_exchange(BN, qc, epi_bytes, cregion)
     else:
         assert d["compact_stages"] == d["compact_kblocks_per_stage"] == d["compact_smem_bytes"] == 0
+        assert d["compact_chunks_per_block"] == d["compact_cluster"] == d["compact_grid_z"] == 0
 
 
-def check_k_coverage(K, S, kps, C, CL, KBS, T3, kb_elems, elem):
-    """Every k of every split loaded exactly once, boxes aligned."""
+def check_k_coverage(K, S, kps, C, CL, KBS, T3, kb_elems, elem, cpc=1):
+    """Every k of every split loaded exactly once, boxes aligned; with cpc
+    chunks per block, each chunk's k-blocks in their own accumulator, in
+    order, the first of each chunk starting it."""
     for s in range(S):
         ks, ke = s * kps, min(s * kps + kps, K)
         covered = []
-        for c in range(C):
-            lo = ks + c * CL
-            hi = min(lo + CL, ke)
+        for cb in range(C // cpc):                    # the blocks of the split
+            lo = ks + cb * cpc * CL
+            hi = min(lo + cpc * CL, ke)
             klen = max(0, hi - lo)
             nkb = -(-klen // kb_elems)
             if T3:
                 assert lo % kb_elems == 0
+            kpc = CL // kb_elems
+            jc, kb_in = 0, 0                          # the kernel's accumulator bookkeeping
             for i in range(-(-nkb // KBS)):
                 if T3:
                     assert lo // kb_elems + i * KBS < K // kb_elems     # the box starts inside K
+                if cpc > 1:
+                    assert jc == (i * KBS) // kpc and kb_in == (i * KBS) % kpc
+                    kb_in += KBS
+                    if kb_in == kpc:
+                        kb_in, jc = 0, jc + 1
                 for j in range(KBS):
                     kb = i * KBS + j
                     if kb >= nkb:
@@ -175,6 +202,8 @@ def check_k_coverage(K, S, kps, C, CL, KBS, T3, kb_elems, elem):
                     kx = lo + kb * kb_elems
                     valid = min(kb_elems, klen - kb * kb_elems)
                     assert valid in (32, 64) and (kx * elem) % 16 == 0 and kx < K
+                    if cpc > 1:                       # inside the chunk its accumulator holds
+                        assert lo + (kb // kpc) * CL <= kx < lo + (kb // kpc + 1) * CL
                     covered += range(kx, kx + valid)
         assert covered == list(range(ks, ke)), (s, ks, ke)
 
