@@ -134,21 +134,21 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
 __device__ __forceinline__ uint64_t l2_policy_evict_last()
 {
     uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_normal()
 {
     uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    asm("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {
     uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 
@@ -402,9 +402,12 @@ __device__ __forceinline__ void grid_dependency_wait()
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// No memory clobber: releasing the next grid orders nothing (the next grid's
+// griddepcontrol.wait waits for this whole grid), and without it the
+// compiler may keep the kernel's parameter loads ahead of the release.
 __device__ __forceinline__ void launch_dependents()
 {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
 }
 
 }  // namespace ptx

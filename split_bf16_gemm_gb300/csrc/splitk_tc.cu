@@ -338,6 +338,9 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
         }
     };
     if (tid == 0) {
+        // the tensor maps first: the first load waits for their fetch
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
         for (int i = 0; i < stages; ++i) {
             ptx::mbar_init(full_bar(i), 1);
             ptx::mbar_init(empty_bar(i), 1);
@@ -355,9 +358,12 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
             ptx::mbar_arrive_expect_tx(recv_bar, incoming);
         else
             ptx::mbar_arrive(recv_bar);
-        ptx::prefetch_tensormap(&tmA);
-        ptx::prefetch_tensormap(&tmB);
-        if (!args.overlap) ptx::grid_dependency_wait();   // A and B may be the previous grid's output
+        if (!args.overlap) {
+            ptx::grid_dependency_wait();   // A and B may be the previous grid's output
+            // the previous grid has finished: the next one may start (this
+            // thread's release counts for the CTA; the others' below are no-ops)
+            ptx::launch_dependents();
+        }
         for (int i = 0; i < pre; ++i) issue_stage(i, i);
     }
     if (warp == 1) {
@@ -712,8 +718,12 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
         }
     }
     // overlap 2 stored without waiting: the grid still finishes after the
-    // previous one, so that grids finish in launch order
-    if (args.overlap == 2) ptx::grid_dependency_wait();
+    // previous one, so that grids finish in launch order.  One CTA waiting
+    // is enough for that; the others leave at once and free their SM for
+    // the next launches.
+    if (args.overlap == 2 && blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1 &&
+        blockIdx.z == gridDim.z - 1)
+        ptx::grid_dependency_wait();
     if (Q > 1) ptx::cluster_wait();            // no CTA leaves while its staging may still be copied from
 }
 
