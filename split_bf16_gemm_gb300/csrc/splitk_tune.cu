@@ -53,12 +53,12 @@ int elem_size(int dtype)
 
 // Estimated microseconds per gemm_bt call in a graph of such calls: the
 // tensor-core launch, plus for the two-kernel path (fused == 0, or a fused
-// call that runs the two kernels) the reduce: 0.85 us, its bytes at ~3.1 TB/s
-// and 0.046 us per split (fitted with the launch model in splitk_tc.cu).
+// call that runs the two kernels) the reduce: 0.95 us, its bytes at ~3.0 TB/s
+// and 0.062 us per split (fitted with the launch model in splitk_tc.cu).
 double estimate_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, int dtype, int fused)
 {
     const bool in_kernel = fused != 0 && splitk::fused_in_kernel(M, N, K, S, kps, dtype, false);
-    const double reduce = 0.85 + static_cast<double>(S + 1) * M * N * 4 / 3.1e6 + 0.046 * static_cast<double>(S);
+    const double reduce = 0.953 + static_cast<double>(S + 1) * M * N * 4 / 2.978e6 + 0.0623 * static_cast<double>(S);
     return splitk::estimate_tc_us(M, N, K, S, kps, in_kernel, dtype == SPLITK_F32) + (in_kernel ? 0.0 : reduce);
 }
 
@@ -82,10 +82,10 @@ int splitk_choose_splits(int64_t M, int64_t N, int64_t K, int dtype, int fused, 
         if (splitk_check_geometry(M, N, K, S, kps) != SPLITK_OK) continue;
         const double t = estimate_us(M, N, K, S, kps, dtype, fused);
         if (model_us) model_us[i] = t;
-        // candidates within 1% count as ties, won by the larger split count
+        // candidates within 2% count as ties, won by the larger split count
         // (the measured curves are flat there, and more splits cost least
         // where the model misses a fixed cost)
-        if (t <= best * 1.01) {
+        if (t <= best * 1.02) {
             best = std::min(best, t);
             bs = S;
             bk = kps;

@@ -289,7 +289,7 @@ def test_host_batch_rejections(L):
 
 def test_choose_splits_is_legal(L, orc):
     """The model's choice is always a legal geometry drawn from the candidates:
-    the largest candidate whose estimate is within 1% of the smallest."""
+    the largest candidate whose estimate is within 2% of the smallest."""
     for M in (32, 96, 256):
         for N in (64, 512, 1024):
             for K in (32, 128, 160, 512, 2048, 4096):
@@ -299,7 +299,7 @@ def test_choose_splits_is_legal(L, orc):
                         assert orc.contract(M, N, K, S, kps) == 0, (M, N, K, S, kps)
                         assert kps % 32 == 0 and all(v is not None and v > 0 for v in t.values())
                         low = min(t.values())
-                        best = max(c for c, v in t.items() if v <= low * 1.01)
+                        best = max(c for c, v in t.items() if v <= low * 1.02)
                         k_best = -(-(-(-K // best)) // 32) * 32
                         assert (S, kps) == (-(-K // k_best), k_best)
                         legal = set()
