@@ -160,18 +160,20 @@ bool fused_possible(int dtype, bool b_kn) { return !(dtype == SPLITK_F32 && b_kn
 
 // Whether gemm_bt(fused != 0) sums the splits inside its launch.  It does
 // where the tile plan holds all of a tile's splits in one resident cluster,
-// except for F32 operands (3xTF32) with M <= 32: there the cluster that sums
-// the splits is larger than the partial pass's own (every split's chunks,
-// against one split's), its exchange moves the whole 128-row accumulator of
-// which at most 32 rows are live, and on GB300 the two kernels measured
-// faster (M32 N512 K2048, 2 to 8 splits: 5.6-5.8 against 7.0-7.2 us).
+// except for F32 operands (3xTF32) with M <= 32 or 8 splits or more, where
+// the cluster that sums the splits is larger than the partial pass's own
+// (every split's chunks, against one split's): its exchange moves the whole
+// 128-row accumulator, of which at most 32 rows are live for M <= 32, and
+// the F32 stages leave little room for the receive slots; on GB300 the two
+// kernels measured faster (M32 N512 K2048, 2 to 8 splits: 5.6-5.8 against
+// 7.0-7.2 us; M96 N512 K512, 8 splits: 4.0 against 4.5 us).
 bool splitk::fused_in_kernel(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, int dtype, bool b_kn)
 {
     if (!fused_possible(dtype, b_kn)) return false;
     const bool x3 = dtype == SPLITK_F32;
     const TilePlan f = splitk::plan_tc(M, N, K, S, kps, true, x3);
     if (f.split_sum != 2) return false;
-    if (x3 && M <= 32 && f.cluster > splitk::plan_tc(M, N, K, S, kps, false, x3).cluster) return false;
+    if (x3 && (M <= 32 || S >= 8) && f.cluster > splitk::plan_tc(M, N, K, S, kps, false, x3).cluster) return false;
     return true;
 }
 

@@ -301,8 +301,8 @@ def test_fused_routing(lib):
     cluster holds all of a tile's splits and chunks; elsewhere it runs the two
     kernels (the same chunks, so the same result bit for bit), which measured
     faster on GB300 than summing through global memory.  F32 operands with
-    M <= 32 also run the two kernels where the summing cluster would be larger
-    than the partial pass's own."""
+    M <= 32 or 8 splits or more also run the two kernels where the summing
+    cluster would be larger than the partial pass's own."""
     sk = lib
     fused_in_kernel = [
         (256, 1024, 2048, 2, 1024, "bf16"), (256, 1024, 2048, 4, 512, "bf16"), (96, 512, 2048, 4, 512, "bf16"),
@@ -315,6 +315,7 @@ def test_fused_routing(lib):
         (64, 128, 160, 3, 64, "bf16"),                                          # three splits
         (4096, 8192, 4096, 2, 2048, "bf16"),                                    # more tiles than resident clusters
         (32, 512, 2048, 2, 1024, "f32"), (32, 512, 2048, 8, 256, "f32"),        # F32, M <= 32
+        (96, 512, 512, 8, 64, "f32"),                                           # F32, 8 splits
     ]
     for c in fused_in_kernel:
         d = sk.splitk_describe_launch(*c, fused=1)
