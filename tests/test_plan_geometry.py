@@ -19,8 +19,8 @@ tests, and every tile override:
 - a rank's share of the tile is a whole number of 32 x 32 boxes (each warp
   pushes whole boxes), every 16-byte piece has exactly one owner, and every
   contribution sent to or read from a receive slot stays inside that slot;
-- the compact layout (taken inside graph captures): the same tiles, chunks
-  and sums, a ring that still covers every k once, the receive slots inside
+- the compact layout (taken inside graph captures, by fused calls and by
+  the partial pass of the two-kernel call): the same tiles, chunks and sums, a ring that still covers every k once, the receive slots inside
   the ring after the staging area, and two or three thread blocks' shared
   and tensor memory within one SM's; where a block takes every chunk of its
   split (chunks_per_block > 1), each chunk starts on a stage boundary, its
@@ -128,11 +128,11 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
     # the compact layout: same tiles and sums, a ring two blocks to an SM,
     # the receive slots inside it after the staging area
     if d["compact"]:
-        assert d["fused_in_kernel"] == 1 and not x3 and TM == TILE_M and BN <= 128
+        assert not x3 and TM == TILE_M and BN <= 128
         assert -(-M // TM) * (N // BN) * S * C // Q <= RESIDENT_CLUSTERS[Q]   # one wave
         cst, ckbs, csmem = d["compact_stages"], d["compact_kblocks_per_stage"], d["compact_smem_bytes"]
         cpc, qc = d["compact_chunks_per_block"], d["compact_cluster"]
-        assert 1 <= cst <= 8 and ckbs in (1, 2, 4) and (ckbs == 1 or T3)
+        assert 1 <= cst <= 8 and 1 <= ckbs <= 4 and (ckbs == 1 or T3 or (K % kb_elems == 0 and kps % kb_elems == 0))
         # every chunk of a split in one block: only where the chunks are whole
         # stages of whole k-blocks and the accumulators fit 128 columns
         can3d = K % kb_elems == 0 and kps % kb_elems == 0
