@@ -649,8 +649,10 @@ def run_ours(args, rank, world, dev, torch, dist):
                        "fused_op" if fused else "two_pass_op_graph": round(us_per_op * world, 4),
                        "fused_op_every_launch_waits": round(strict_us, 4)},
         "overlap": "inside each captured graph, a call whose operands no running launch writes loads "
-                   "before the previous launch ends and waits only before its first store; "
-                   "kernels_us.fused_op_every_launch_waits is the same graphs with that turned off",
+                   "before the previous launch ends and waits only before its first store, or (nothing "
+                   "in flight touching its outputs either) stores at once and has one block wait before "
+                   "the grid finishes; kernels_us.fused_op_every_launch_waits is the same graphs with "
+                   "that turned off",
         "e2e": e2e,
         "kn_layout": {"what": "the same operations with the weight in its [K,N] layout (gemm_kn, MN-major B)",
                       "us": kn_us},
