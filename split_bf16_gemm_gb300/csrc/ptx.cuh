@@ -88,14 +88,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 
 // ------------------------------------------------------------------- TMA
 
-// Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned address, size a
-// multiple of 16); a hint only: no completion to wait for.
-__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
-                 : "memory");
-}
-
 // Prefetch of the L2 line holding `p` (a hint: no completion).
 __device__ __forceinline__ void prefetch_l2_line(const void *p)
 {
@@ -142,13 +134,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_normal()
 {
     uint64_t p;
     asm("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_first()
-{
-    uint64_t p;
-    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 
@@ -302,30 +287,7 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 
-// Atomic increment with wrap (the value becomes 0 after `limit`), with
-// acquire-release semantics at GPU scope: it publishes what the calling
-// thread wrote or observed (through a preceding CTA barrier) before it, and
-// makes what other threads published the same way visible after it.
-__device__ __forceinline__ unsigned atom_inc_acq_rel_gpu(unsigned *p, unsigned limit)
-{
-    unsigned old;
-    asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(limit) : "memory");
-    return old;
-}
-
 // ------------------------------------------------------- cluster / DSMEM
-
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_arrive()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
 
 // Arrival that publishes nothing: only says "this CTA has reached here".
 __device__ __forceinline__ void cluster_arrive_relaxed()
@@ -346,16 +308,6 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank)
     return r;
 }
 
-__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr)
-{
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-
 // Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to a
 // shared-memory address of a CTA in the cluster; completion is counted in
 // bytes on that CTA's mbarrier (`bar`, a cluster address).
@@ -364,17 +316,6 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src,
     asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      dst),
                  "r"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
-// 16-byte store into the shared memory of a CTA in the cluster (`dst`, a
-// cluster address); its bytes count toward that CTA's mbarrier `bar`.
-__device__ __forceinline__ void st_async_v4(uint32_t dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
-                                            uint32_t bar)
-{
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-                     dst),
-                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
                  : "memory");
 }
 
