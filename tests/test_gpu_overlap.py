@@ -77,7 +77,7 @@ def instances(sk, M, N, K, S, kps, dt, n, seed0=0):
     (256, 1024, 1920, 2, 1024),   # the last split's second chunk short
     (256, 1024, 1536, 2, 1024),   # ... and empty
 ])
-@pytest.mark.parametrize("fused", [1, 3])
+@pytest.mark.parametrize("fused", [0, 1, 3])
 def test_independent_calls_overlap_bitwise(lib, shape, fused):
     sk = lib
     M, N, K, S, kps = shape
@@ -115,7 +115,7 @@ def test_independent_calls_overlap_bitwise(lib, shape, fused):
         torch.cuda.synchronize()
         for it in insts:
             assert bitwise(it["out"], it["ref"])
-    if fused == 3:   # the kept partials too
+    if fused != 1:   # the kept partials too (fused=0: the workspace holds them)
         for it, w in zip(insts, refs_ws):
             P = S * M * N
             assert bitwise(it["ws"][:P], w[:P])
@@ -384,4 +384,35 @@ def test_store_waits_for_previous_writer(lib):
         g.replay()
         torch.cuda.synchronize()
         assert bitwise(O, ref)
+    assert sk.splitk_get_device_status() == 0
+
+
+def test_long_run_starts_a_new_window(lib):
+    """40 independent calls in one capture: the library follows at most 32
+    launches of a run, so the 33rd waits for the previous grid and heads a
+    new run, and the calls after it overlap again; every output is the eager
+    one, bit for bit."""
+    sk = lib
+    M, N, K, S, kps, dt = 256, 512, 2048, 4, 512, "bf16"
+    insts = instances(sk, M, N, K, S, kps, dt, 40)
+    for it in insts:
+        sk.gemm_bt(it["A"], it["B"], it["ref"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=1)
+    torch.cuda.synchronize()
+    seen = []
+
+    def body():
+        for it in insts:
+            sk.gemm_bt(it["A"], it["B"], it["out"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=1)
+            seen.append(sk.splitk_last_launch()["overlap"])
+
+    g = capture(body)
+    assert seen[0] == 0 and seen[32] == 0, seen
+    assert all(v == 2 for i, v in enumerate(seen) if i not in (0, 32)), seen
+    for _ in range(2):
+        for it in insts:
+            it["out"].fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        for it in insts:
+            assert bitwise(it["out"], it["ref"])
     assert sk.splitk_get_device_status() == 0
