@@ -357,7 +357,7 @@ int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
  *  starts beside the launch before it or heads such a run, takes the compact
  *  layout: the same tiles, chunks and sums, a stage ring cut so that two or
  *  three thread blocks fit on an SM, the peers' shares received inside the
- *  ring; 16-bit operands, one-wave plans),
+ *  ring; one-wave plans),
  *  compact_stages, compact_kblocks_per_stage, compact_dynamic_smem_bytes,
  *  compact_chunks_per_block (1, or every chunk of a split in one thread
  *  block, each in its own accumulator, added in chunk order before the

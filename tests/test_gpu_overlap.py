@@ -416,3 +416,38 @@ def test_long_run_starts_a_new_window(lib):
         for it in insts:
             assert bitwise(it["out"], it["ref"])
     assert sk.splitk_get_device_status() == 0
+
+
+@pytest.mark.parametrize("shape", [(96, 512, 512, 4, 128), (256, 1024, 2048, 2, 1024), (160, 192, 320, 3, 128)])
+@pytest.mark.parametrize("fused", [0, 1])
+def test_f32_calls_overlap_bitwise(lib, shape, fused):
+    """F32 operands (3xTF32) in graphs: the calls after the first overlap and
+    take the compact layout (two CTAs per SM, one chunk per CTA), and every
+    output is the eager one, bit for bit."""
+    sk = lib
+    M, N, K, S, kps = shape
+    dt = "f32"
+    insts = instances(sk, M, N, K, S, kps, dt, 5)
+    for it in insts:
+        sk.gemm_bt(it["A"], it["B"], it["ref"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=fused)
+    torch.cuda.synchronize()
+    seen = []
+
+    def body():
+        for it in insts:
+            sk.gemm_bt(it["A"], it["B"], it["out"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=fused)
+            seen.append(sk.splitk_last_launch())
+
+    g = capture(body)
+    assert seen[0]["overlap"] == 0 and all(d["overlap"] == 2 for d in seen[1:]), seen
+    assert all(d["chunks_per_block"] == 1 for d in seen), seen
+    if M * N <= 256 * 1024:
+        assert all(d["compact"] == 1 for d in seen), seen
+    for _ in range(2):
+        for it in insts:
+            it["out"].fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        for it in insts:
+            assert bitwise(it["out"], it["ref"])
+    assert sk.splitk_get_device_status() == 0

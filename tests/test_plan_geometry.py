@@ -128,7 +128,7 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
     # the compact layout: same tiles and sums, a ring two blocks to an SM,
     # the receive slots inside it after the staging area
     if d["compact"]:
-        assert not x3 and TM == TILE_M and BN <= 128
+        assert TM == TILE_M and BN <= 128
         assert -(-M // TM) * (N // BN) * S * C // Q <= RESIDENT_CLUSTERS[Q]   # one wave
         cst, ckbs, csmem = d["compact_stages"], d["compact_kblocks_per_stage"], d["compact_smem_bytes"]
         cpc, qc = d["compact_chunks_per_block"], d["compact_cluster"]
@@ -136,11 +136,11 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
         # every chunk of a split in one block: only where the chunks are whole
         # stages of whole k-blocks and the accumulators fit 128 columns
         can3d = K % kb_elems == 0 and kps % kb_elems == 0
-        mergeable = SS == 2 and C > 1 and BN * C <= 128 and can3d and CL % 64 == 0
+        mergeable = not x3 and SS == 2 and C > 1 and BN * C <= 128 and can3d and CL % 64 == 0
         assert cpc in (1, C) and (cpc == 1 or mergeable)
         assert qc == Q // cpc and d["compact_grid_z"] == S * C // cpc and d["compact_grid_z"] % qc == 0
         assert -(-M // TM) * (N // BN) * S * C // Q <= RESIDENT_CLUSTERS[qc]
-        cstage = (TM + BN) * 128 * ckbs
+        cstage = (TM + BN) * 128 * ckbs * (2 if x3 else 1)
         nkb = -(-CL // kb_elems)
         cnkb = nkb * cpc                                  # k-blocks of a block
         assert cst >= min(2, -(-cnkb // ckbs))            # double-buffered unless one stage holds them all
@@ -159,7 +159,7 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
         # receive slots fit in 74 KB
         cctas = -(-M // TM) * (N // BN) * S * C // cpc
         kmin = kbs if (kbs and T3) else 1                    # the smallest stage the override allows
-        stage1 = (TM + BN) * 128 * kmin
+        stage1 = (TM + BN) * 128 * kmin * (2 if x3 else 1)
         fits3 = max(min(2, -(-cnkb // kmin)) * stage1, epi_bytes + recv_bytes, cols * 512) + 1024 <= COMPACT3_LIMIT
         if qc <= 4 and (cctas > 74 or cpc > 1) and fits3:
             assert csmem <= COMPACT3_LIMIT and 3 * (csmem + STATIC_SMEM + 1024) <= SM_SMEM and 3 * cols <= 512
