@@ -8,8 +8,9 @@
 // "Launch contract and correctness").  Optionally the same launch also sums
 // the splits into out[m,n] (the pages' separate accumulation pass, fused).
 //
-// One CTA (256 threads, 8 warps) owns a TM x BN output tile of one K-chunk
-// (TM = 128, or 256 as below):
+// One CTA (256 threads, 8 warps) owns a TM x BN output tile of one K-chunk, or
+// of both chunks of its split, each in its own accumulator (TM = 128, or 256
+// as below):
 //   thread 0       TMA producer: per stage, kbs 64-wide k-blocks of A (TM
 //                  rows) and of B (BN rows), 128-byte swizzled, into a ring
 //                  of `stages` buffers; the first stages go out before tensor
@@ -17,7 +18,7 @@
 //   warp 1 lane 0  MMA issuer: tcgen05.mma (M=128, N=BN, K=16; K=8 and three
 //                  products per step with X3) from descriptors built once
 //                  per stage, accumulating in tensor memory (BN 32-bit
-//                  columns);
+//                  columns per chunk);
 //   warps 2-7      before the dependency wait, in the CTAs that start beside
 //                  the previous launch: L2 prefetch of this launch's A and B;
 //                  with X3, after it: the lo parts of each landed stage;
@@ -47,15 +48,19 @@
 // own set-up once that wait has returned.  With `overlap` the host has
 // established that no launch that can still be running writes A or B (the
 // chain of launches inside one graph capture, splitk_chain.cu): the loads then
-// start at once, the next grid is released right after set-up, and the wait
-// for the previous grid comes only before the first global store.  Consecutive
-// independent operations then run side by side, two CTAs to an SM when the
-// compact layout (a 2-stage ring that also receives the peers' shares) fits.
+// start at once, the next grid is released at the kernel's start, and the
+// wait for the previous grid comes only before the first global store -- or,
+// where none of those launches reads or writes this one's outputs either, only
+// before one CTA of the grid finishes (the grids still finish in launch
+// order).  Consecutive independent operations then run side by side, two or
+// three CTAs to an SM in the compact layout (a ring cut to fit, that also
+// receives the peers' shares), where a CTA may take both chunks of its split.
 //
 // Every mbarrier wait has a time limit; on time-out the kernel records a bit
 // in g_device_status, drains its own loads in flight, still sends and awaits
-// every cluster message (so no peer waits on it), frees its tensor memory and
-// finishes; the outputs of that launch are then not valid.
+// every cluster message (so no peer waits on it), waits for its MMAs, frees
+// its tensor memory and finishes; the outputs of that launch are then not
+// valid.
 
 #include <cudaTypedefs.h>
 
