@@ -44,9 +44,34 @@ BYTES_GEMM = M * K * 2 + N * K * 2 + SPLITS * M * N * 4                     # A+
 BYTES_REDUCE = SPLITS * M * N * 4 + M * N * 4                               # P read, out write
 
 
+def code_of(text: str) -> str:
+    """C/C++/CUDA source without its comments and blank lines (string and
+    character literals kept as they are), so that a comment-only edit leaves
+    the traffic record valid."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":                       # a literal, escapes included
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            while i < n and text[i] != "\n":
+                i += 1
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_traffic():
     """DRAM bytes per launch of the tensor-core kernel from the committed ncu
-    record, or None when the kernel sources changed since it was taken."""
+    record, or None when the kernel's code changed since it was taken."""
     import hashlib
 
     path = os.path.join(ROOT, "profiles", "tc_splitk_traffic.txt")
@@ -60,9 +85,9 @@ def kernel_traffic():
                 rec[k.strip()] = v.strip()
     h = hashlib.sha256()
     for src in rec.get("sources", "").split():
-        with open(os.path.join(ROOT, src), "rb") as f:
-            h.update(f.read())
-    if h.hexdigest() != rec.get("sources_sha256"):
+        with open(os.path.join(ROOT, src)) as f:
+            h.update(code_of(f.read()).encode())
+    if h.hexdigest() != rec.get("code_sha256"):
         return None
     return int(rec["dram_bytes_per_launch"])
 
