@@ -58,14 +58,18 @@
  * waits only before it finishes, so the grids still finish in launch order.
  * Such a fused launch may also give each thread block all the chunks of its
  * split, each in its own accumulator, added in chunk order inside the block.
- * Its results are bitwise those of the same launch without overlap.
+ * A call that may store early and has the same shape and plan as the launch
+ * before it joins that launch instead of adding one: the launch's graph
+ * node then computes both calls (up to 8), whose blocks may run in any
+ * order.  Its results are bitwise those of the same launch without overlap.
  * Launches that read what an
  * earlier one writes (a chain of GEMMs, the reduce after the partial pass),
  * launches after another kernel or a copy, and launches outside a capture
  * wait as usual.  The decision is made at capture time from the pointers
  * passed; a graph whose nodes are later given other buffers
  * (cudaGraphExecKernelNodeSetParams) must keep the same pattern of overlaps
- * between them.  splitk_set_overlap(0) turns this off for later captures.
+ * between them, and the calls grouped into one node stay in that node.
+ * splitk_set_overlap turns the grouping, or both, off for later captures.
  */
 #ifndef SPLITK_H
 #define SPLITK_H
@@ -337,7 +341,7 @@ const char *splitk_status_string(int status);
  * SPLITK_OK or SPLITK_ERR_CONFIG. */
 int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
 
-/* Describes the launch gemm_bt would make, without launching: info[0..24] =
+/* Describes the launch gemm_bt would make, without launching: info[0..25] =
  * {path (0 tensor-core, 2 tensor-core 3xTF32 for F32), bn, chunks, chunk_len, stages,
  *  cluster_size (chunks, or splits * chunks), grid_x, grid_y, grid_z,
  *  dynamic_smem_bytes,
@@ -361,8 +365,10 @@ int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
  *  compact_stages, compact_kblocks_per_stage, compact_dynamic_smem_bytes,
  *  compact_chunks_per_block (1, or every chunk of a split in one thread
  *  block, each in its own accumulator, added in chunk order before the
- *  exchange: the same sums), compact_cluster_size, compact_grid_z
- *  (0 when compact is 0)}; `info` must hold 25 ints.
+ *  exchange: the same sums), compact_cluster_size, compact_grid_z,
+ *  compact_bn (the compact plan's tile width, which may be wider than bn:
+ *  the products of an output element do not depend on it)
+ *  (0 when compact is 0)}; `info` must hold 26 ints.
  * Returns a status as gemm_bt's validation would (pointers are not checked). */
 int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits,
                            int64_t k_per_split, int dtype, int fused,
@@ -391,14 +397,16 @@ int splitk_selftest_kernel_timeout(const void *A, const void *B, float *out,
                                    int64_t splits, int64_t k_per_split,
                                    int dtype, void *stream);
 
-/* Turns the overlap of consecutive independent launches inside a graph
- * capture (see the top of this header) on (1, the default) or off (0) for
- * every later launch of the process.  Launches already captured keep what
- * was decided for them.  Returns SPLITK_OK or SPLITK_ERR_CONFIG. */
-int splitk_set_overlap(int enable);
+/* What the library does with consecutive independent calls inside a graph
+ * capture (see the top of this header), for every later call of the
+ * process: 2 (the default) overlap them and group them into one launch
+ * where they can be; 1 overlap them only (one launch per call); 0 neither
+ * (every launch waits for the one before).  Launches already captured keep
+ * what was decided for them.  Returns SPLITK_OK or SPLITK_ERR_CONFIG. */
+int splitk_set_overlap(int mode);
 
 /* What the calling host thread's most recent tensor-core launch did:
- * info[0..9] = {overlap (0: it waited for the previous grid before loading;
+ * info[0..10] = {overlap (0: it waited for the previous grid before loading;
  * 1: it loaded before that grid finished and waited before its first store;
  * 2: it also stored before, waiting only before it finished), compact (its
  * ring was cut so that two or three of its thread blocks fit on an SM,
@@ -406,8 +414,10 @@ int splitk_set_overlap(int enable);
  * plan allows it), capturing (the stream was being captured), bn, chunks,
  * stages, kblocks_per_stage, dynamic_smem_bytes, chunks_per_block (1, or
  * all the chunks of a split, each in its own accumulator and added in chunk
- * order inside the block: the same sums), cluster_size}.  `info` must hold
- * 10 ints.  Diagnostic; returns SPLITK_OK or SPLITK_ERR_NULL. */
+ * order inside the block: the same sums), cluster_size, group (the calls
+ * the launch computes so far: 1, or more where the call joined the launch
+ * of the calls before it)}.  `info` must hold 11 ints.  Diagnostic;
+ * returns SPLITK_OK or SPLITK_ERR_NULL. */
 int splitk_last_launch(int *info);
 
 #ifdef __cplusplus

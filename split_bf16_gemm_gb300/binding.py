@@ -257,14 +257,14 @@ def splitk_set_tile_override(bn: int = 0, chunks: int = 0, kblocks_per_stage: in
 
 
 def splitk_describe_launch(M, N, K, splits, k_per_split, dtype, fused=0) -> dict:
-    info = (ctypes.c_int * 25)()
+    info = (ctypes.c_int * 26)()
     _check(lib().splitk_describe_launch(M, N, K, splits, k_per_split, dtype_code(dtype), fused,
                                         ctypes.addressof(info)), "splitk_describe_launch")
     keys = ("path", "bn", "chunks", "chunk_len", "stages", "cluster", "grid_x", "grid_y",
             "grid_z", "smem_bytes", "fused_in_kernel", "kernels_per_call", "kblocks_per_stage",
             "three_d", "split_sum", "prefetchers", "rows_first", "tile_m",
             "compact", "compact_stages", "compact_kblocks_per_stage", "compact_smem_bytes",
-            "compact_chunks_per_block", "compact_cluster", "compact_grid_z")
+            "compact_chunks_per_block", "compact_cluster", "compact_grid_z", "compact_bn")
     return dict(zip(keys, list(info)))
 
 
@@ -272,18 +272,21 @@ def splitk_selftest_bounded_wait(limit_ns: int = 1_000_000, stream=None) -> int:
     return lib().splitk_selftest_bounded_wait(limit_ns, _stream(stream))
 
 
-def splitk_set_overlap(enable: bool) -> None:
-    """Overlap of consecutive independent launches inside graph captures: on
-    (the default) or off, for later captures of the whole process."""
-    _check(lib().splitk_set_overlap(1 if enable else 0), "splitk_set_overlap")
+def splitk_set_overlap(mode=2) -> None:
+    """Consecutive independent calls inside graph captures, for later
+    captures of the whole process: 2 (or True, the default) overlap and group
+    them, 1 overlap only, 0 (or False) neither."""
+    if isinstance(mode, bool):
+        mode = 2 if mode else 0
+    _check(lib().splitk_set_overlap(int(mode)), "splitk_set_overlap")
 
 
 def splitk_last_launch() -> dict:
     """What the calling thread's most recent tensor-core launch did."""
-    info = (ctypes.c_int * 10)()
+    info = (ctypes.c_int * 11)()
     _check(lib().splitk_last_launch(ctypes.addressof(info)), "splitk_last_launch")
     keys = ("overlap", "compact", "capturing", "bn", "chunks", "stages", "kblocks_per_stage", "smem_bytes",
-            "chunks_per_block", "cluster")
+            "chunks_per_block", "cluster", "group")
     return dict(zip(keys, list(info)))
 
 

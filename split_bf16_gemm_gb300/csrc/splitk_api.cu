@@ -127,11 +127,22 @@ int run_partial_pass(const void *A, const void *B, float *P, float *out, int64_t
     if (!prefetch) plan.prefetchers = 0;
     pr.overlap = chain.overlap();
     pr.store_early = chain.store_early();
-    const cudaError_t err = splitk::launch_tc(pr, plan, stream);
+    // a call that touches nothing in flight, with the same shape and plan as
+    // the launch before it, joins that launch (no node added)
+    int group = 1, mode = pr.overlap ? (pr.store_early ? 2 : 1) : 0;
+    if (pr.store_early && splitk::grouping_enabled() &&
+        splitk::join_group(pr, plan, chain.capture_id(), chain.dep_node(), &group, &mode)) {
+        chain.commit_joined();
+        splitk::note_launch({mode, plan.compact, 1, plan.bn, plan.chunks, plan.stages, plan.kbs,
+                             static_cast<int>(plan.smem_bytes), plan.cpc, plan.cluster, group});
+        return SPLITK_OK;
+    }
+    const cudaError_t err = chain.capturing() && splitk::grouping_enabled()
+                                ? splitk::launch_tc_grouped(pr, plan, stream, chain.capture_id())
+                                : splitk::launch_tc(pr, plan, stream);
     chain.commit(err == cudaSuccess, !pr.overlap);
-    splitk::note_launch({pr.overlap ? (pr.store_early ? 2 : 1) : 0, plan.compact, chain.capturing() ? 1 : 0, plan.bn,
-                         plan.chunks, plan.stages, plan.kbs, static_cast<int>(plan.smem_bytes), plan.cpc,
-                         plan.cluster});
+    splitk::note_launch({mode, plan.compact, chain.capturing() ? 1 : 0, plan.bn, plan.chunks, plan.stages, plan.kbs,
+                         static_cast<int>(plan.smem_bytes), plan.cpc, plan.cluster, 1});
     return cuda_status(err);
 }
 
@@ -369,7 +380,7 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
     if (st != SPLITK_OK) return st;
     if (elem_bytes(dtype) == 0) return SPLITK_ERR_DTYPE;
     if (!info) return SPLITK_ERR_NULL;
-    std::fill(info, info + 25, 0);
+    std::fill(info, info + 26, 0);
     const bool x3 = dtype == SPLITK_F32;
     // gemm_bt runs the two kernels where the fused launch could not sum a
     // tile's splits inside one resident cluster
@@ -404,14 +415,15 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
         info[22] = c.compact ? c.cpc : 0;
         info[23] = c.compact ? c.cluster : 0;
         info[24] = c.compact ? static_cast<int>(c.grid.z) : 0;
+        info[25] = c.compact ? c.bn : 0;
     }
     return SPLITK_OK;
 }
 
-int splitk_set_overlap(int enable)
+int splitk_set_overlap(int mode)
 {
-    if (enable != 0 && enable != 1) return SPLITK_ERR_CONFIG;
-    splitk::set_overlap_enabled(enable != 0);
+    if (mode < 0 || mode > 2) return SPLITK_ERR_CONFIG;
+    splitk::set_overlap_mode(mode);
     return SPLITK_OK;
 }
 
@@ -429,6 +441,7 @@ int splitk_last_launch(int *info)
     info[7] = r.smem_bytes;
     info[8] = r.cpc;
     info[9] = r.cluster;
+    info[10] = r.group;
     return SPLITK_OK;
 }
 

@@ -43,9 +43,12 @@ namespace {
 constexpr int kChains = 16;    // capture sequences followed at once (least recently used replaced)
 constexpr int kWindow = 32;    // launches a new one is checked against, at most
 
+// a launch's byte ranges: two of each kind per call, for every call grouped into it
+constexpr int kEntrySpans = kMaxSpans * kMaxGroup;
+
 struct Entry {
     cudaGraphNode_t node;
-    Span reads[kMaxSpans], writes[kMaxSpans];
+    Span reads[kEntrySpans], writes[kEntrySpans];
     int n_reads, n_writes;
 };
 
@@ -60,7 +63,7 @@ struct Chain {
 std::mutex g_mu;
 Chain g_chains[kChains];
 uint64_t g_clock = 0;
-std::atomic<bool> g_enabled{true};
+std::atomic<int> g_mode{2};
 
 Chain *find_chain(unsigned long long id)
 {
@@ -89,8 +92,9 @@ bool meets(const Span &a, const Span &b) { return a.lo < b.hi && b.lo < a.hi; }
 
 }  // namespace
 
-void set_overlap_enabled(bool on) { g_enabled.store(on); }
-bool overlap_enabled() { return g_enabled.load(); }
+void set_overlap_mode(int mode) { g_mode.store(mode); }
+bool overlap_enabled() { return g_mode.load() >= 1; }
+bool grouping_enabled() { return g_mode.load() >= 2; }
 
 namespace {
 thread_local LaunchRecord t_last = {};
@@ -106,7 +110,7 @@ ChainGuard::ChainGuard(cudaStream_t stream, const Span *reads, int n_reads, cons
     n_writes_ = n_writes;
     for (int r = 0; r < n_reads; ++r) reads_[r] = reads[r];
     for (int w = 0; w < n_writes; ++w) writes_[w] = writes[w];
-    if (!g_enabled.load()) return;
+    if (!overlap_enabled()) return;
     cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
     unsigned long long id = 0;
     const cudaGraphNode_t *deps = nullptr;
@@ -121,6 +125,7 @@ ChainGuard::ChainGuard(cudaStream_t stream, const Span *reads, int n_reads, cons
     Chain *c = find_chain(id);
     if (!c || c->n == 0 || nd != 1 || deps[0] != c->e[c->n - 1].node) return;   // not after our own launch
     fresh_ = false;
+    dep_ = deps[0];
     for (int i = 0; i < c->n; ++i)
         for (int w = 0; w < c->e[i].n_writes; ++w)
             for (int r = 0; r < n_reads; ++r)
@@ -172,6 +177,21 @@ void ChainGuard::commit(bool launched, bool head)
     e.n_writes = n_writes_;
     for (int r = 0; r < n_reads_; ++r) e.reads[r] = reads_[r];
     for (int w = 0; w < n_writes_; ++w) e.writes[w] = writes_[w];
+    c->stamp = ++g_clock;
+}
+
+void ChainGuard::commit_joined()
+{
+    if (!capturing_) return;
+    Chain *c = find_chain(id_);
+    if (!c || c->n == 0) return;
+    Entry &e = c->e[c->n - 1];
+    if (e.n_reads + n_reads_ > kEntrySpans || e.n_writes + n_writes_ > kEntrySpans) {
+        c->used = false;   // cannot record it: the next launch waits and starts afresh
+        return;
+    }
+    for (int r = 0; r < n_reads_; ++r) e.reads[e.n_reads++] = reads_[r];
+    for (int w = 0; w < n_writes_; ++w) e.writes[e.n_writes++] = writes_[w];
     c->stamp = ++g_clock;
 }
 

@@ -58,6 +58,7 @@ constexpr int kBlockK = 64;   // K elements per pipeline stage: one 128-byte swi
 constexpr int kMaxStages = 8;
 constexpr int kMaxKbs = 4;     // k-blocks in one pipeline stage (one TMA box per operand)
 constexpr int kMaxChunks = 8;  // portable cluster size
+constexpr int kMaxGroup = 8;   // independent calls one launch may compute (graph capture)
 
 // Tile choice for a shape (automatic, or the process-wide override).
 // x3: F32 operands as 3xTF32 (else 16-bit operands).
@@ -74,6 +75,15 @@ void set_tile_override(int bn, int chunks, int kbs);
 
 // Kernel launches; each returns the launch's CUDA error.
 cudaError_t launch_tc(const GemmProblem &p, const TilePlan &plan, cudaStream_t stream);
+// The same, inside the capture `capture` (0: not capturing): a launch that
+// later calls may join (join_group), where the plan allows grouping.
+cudaError_t launch_tc_grouped(const GemmProblem &p, const TilePlan &plan, cudaStream_t stream,
+                              unsigned long long capture);
+// Adds the call to the grouped launch captured as `dep` (the capture's
+// current dependency), if it has the same shape and plan and room; returns
+// whether it did (and the launch's problem count in *group_size).
+bool join_group(const GemmProblem &p, const TilePlan &plan, unsigned long long capture, cudaGraphNode_t dep,
+                int *group_size, int *mode);
 cudaError_t launch_simt_f32(const float *A, const float *B, float *P, int64_t M, int64_t N, int64_t K,
                             int64_t S, int64_t kps, bool b_kn, cudaStream_t stream);
 // overlap: nothing that can still be running writes P (splitk_chain.cu);
@@ -107,6 +117,10 @@ public:
     bool overlap() const { return overlap_; }
     // (with overlap) none reads or writes what this one writes either
     bool store_early() const { return store_early_; }
+    // the capture, and the node the launch depends on (its chain's last
+    // launch, when overlap() holds)
+    unsigned long long capture_id() const { return id_; }
+    cudaGraphNode_t dep_node() const { return dep_; }
     // no earlier launch of this library precedes it in the capture (or the
     // window was full): a head that independent launches may follow
     bool fresh() const { return fresh_; }
@@ -114,21 +128,27 @@ public:
     // it failed); `head`: it waited for the previous grid before letting
     // the next one start, so nothing before it can still be running then
     void commit(bool launched, bool head);
+    // instead of commit: the call joined the chain's last launch (no node
+    // added); its reads and writes are added to that launch's
+    void commit_joined();
 
 private:
     cudaStream_t stream_;
     std::unique_lock<std::mutex> lock_;
     unsigned long long id_ = 0;
     bool capturing_ = false, overlap_ = false, fresh_ = false, store_early_ = false;
+    cudaGraphNode_t dep_ = nullptr;
     Span reads_[kMaxSpans], writes_[kMaxSpans];
     int n_reads_ = 0, n_writes_ = 0;
 };
-void set_overlap_enabled(bool on);
+// 0: every launch waits; 1: overlap in captures; 2: overlap and grouping
+void set_overlap_mode(int mode);
 bool overlap_enabled();
+bool grouping_enabled();
 
 // What the last tensor-core launch of this host thread did (splitk_last_launch).
 struct LaunchRecord {
-    int overlap, compact, capturing, bn, chunks, stages, kbs, smem_bytes, cpc, cluster;
+    int overlap, compact, capturing, bn, chunks, stages, kbs, smem_bytes, cpc, cluster, group;
 };
 void note_launch(const LaunchRecord &r);
 LaunchRecord last_launch();

@@ -80,10 +80,21 @@ namespace {
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s; a launch normally takes microseconds
 constexpr int kThreads = 256;                     // 8 warps: two per tensor-memory lane quarter
 
+// The operands of the problems one launch computes: one, or (G > 1) up to G
+// independent problems of the same shape and plan, the group index taken
+// from blockIdx.y (blockIdx.y = group * m_tiles + row tile).
+template <int G>
+struct TcOperands {
+    CUtensorMap tm[G][2];       // A and B of each problem
+    float *P[G];                // [S,M,N] partials (nullptr: not kept, when the cluster sums the splits)
+    float *out[G];              // [M,N], or nullptr when the splits are not summed here
+    const uint8_t *A[G], *B[G]; // operands, for the L2 prefetch
+};
+
 struct TcArgs {
-    float *P;              // [S,M,N] partials (nullptr: not kept, when the cluster sums the splits)
-    float *out;            // [M,N], or nullptr when the splits are not summed here
     int M, N, K, S, kps;
+    int group;             // problems in the launch (G > 1 only)
+    int m_tiles;           // row tiles of one problem
     int chunks, chunk_len, stages;
     int split_sum;         // 0: none; 2: inside the cluster (cluster = splits x chunks)
     int kbs;               // 64-wide k-blocks per pipeline stage
@@ -93,7 +104,6 @@ struct TcArgs {
     int bf16;
     uint64_t wait_limit_ns;
     int acc_probe;         // time-out self-test: the wait for the final accumulator gives up at once
-    const uint8_t *A, *B;  // operands, for the L2 prefetch
     uint64_t a_bytes, b_bytes;
     int prefetchers;       // CTAs, first in dispatch order, that prefetch A and B into L2
     int rows_first;        // blockIdx.x is the row tile and blockIdx.y the column tile
@@ -248,10 +258,9 @@ __device__ __forceinline__ void cluster_split_sum_for(int C, const uint32_t (&rb
 // that keeps or sums its own partials (no cluster).
 // Registers: at most 85 per thread for clusters of up to 4 (three CTAs per
 // SM in the compact layout), else 128 (two); no instantiation spills.
-template <int BN, int Q, bool KN, bool X3, int TM = kTileM>
+template <int BN, int Q, bool KN, bool X3, int TM = kTileM, int G = 1>
 __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
-    tc_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const TcArgs args)
+    tc_splitk_kernel(const __grid_constant__ TcOperands<G> ops, const TcArgs args)
 {
     static_assert(!(KN && X3), "F32 operands with the [K,N] weight run on the CUDA cores");
     static_assert(TM == kTileM || (TM == 2 * kTileM && BN == 256 && Q == 1 && !X3), "256-row tiles");
@@ -280,7 +289,16 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
     const uint32_t recv = base + (args.recv_in_ring ? static_cast<uint32_t>(kTileM * BN * 4) : args.region0);
 
     const int n_tile = args.rows_first ? blockIdx.y : blockIdx.x;
-    const int m_tile = args.rows_first ? blockIdx.x : blockIdx.y;
+    int m_tile = args.rows_first ? blockIdx.x : blockIdx.y;
+    int grp = 0;                                    // the problem (grouped launches walk columns first)
+    if constexpr (G > 1) {
+        grp = m_tile / args.m_tiles;
+        m_tile -= grp * args.m_tiles;
+    }
+    const CUtensorMap *const tmA = &ops.tm[grp][0];
+    const CUtensorMap *const tmB = &ops.tm[grp][1];
+    float *const P = ops.P[grp];
+    float *const out = ops.out[grp];
     // A CTA covers cpc consecutive chunks of one split, each summed in its
     // own accumulator (cpc > 1 only for 16-bit, 128-row plans whose chunks
     // are whole k-blocks of whole stages): the same products, chunk sums and
@@ -323,29 +341,29 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
         ptx::mbar_arrive_expect_tx(bar, load_bytes);
         if (args.three_d) {                         // one box per operand: kbs k-blocks at once
             const int kb = k_lo / KB + i * kbs;
-            ptx::tma_load_3d(sa, &tmA, bar, 0, m_tile * TM, kb, ptx::l2_policy_evict_last());
+            ptx::tma_load_3d(sa, tmA, bar, 0, m_tile * TM, kb, ptx::l2_policy_evict_last());
             if constexpr (!KN)
-                ptx::tma_load_3d(sa + kbs * Sh::kABytes, &tmB, bar, 0, n_tile * BN, kb,
+                ptx::tma_load_3d(sa + kbs * Sh::kABytes, tmB, bar, 0, n_tile * BN, kb,
                                  ptx::l2_policy_evict_normal());
         } else {                                    // kbs == 1
             const int kx = k_lo + i * KB;
-            ptx::tma_load_2d(sa, &tmA, bar, kx, m_tile * TM, ptx::l2_policy_evict_last());
+            ptx::tma_load_2d(sa, tmA, bar, kx, m_tile * TM, ptx::l2_policy_evict_last());
             if constexpr (!KN)
-                ptx::tma_load_2d(sa + Sh::kABytes, &tmB, bar, kx, n_tile * BN, ptx::l2_policy_evict_normal());
+                ptx::tma_load_2d(sa + Sh::kABytes, tmB, bar, kx, n_tile * BN, ptx::l2_policy_evict_normal());
         }
         if constexpr (KN) {
             // the [K,N] weight: BN/64 boxes of 64 columns x kbs*64 k-rows
             // (128-byte rows, N contiguous), one after another
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
-                ptx::tma_load_2d(sa + kbs * Sh::kABytes + static_cast<uint32_t>(j * kbs) * 8192u, &tmB, bar,
+                ptx::tma_load_2d(sa + kbs * Sh::kABytes + static_cast<uint32_t>(j * kbs) * 8192u, tmB, bar,
                                  n_tile * BN + j * 64, k_lo + i * kbs * kBlockK, ptx::l2_policy_evict_normal());
         }
     };
     if (tid == 0) {
         // the tensor maps first: the first load waits for their fetch
-        ptx::prefetch_tensormap(&tmA);
-        ptx::prefetch_tensormap(&tmB);
+        ptx::prefetch_tensormap(tmA);
+        ptx::prefetch_tensormap(tmB);
         for (int i = 0; i < stages; ++i) {
             ptx::mbar_init(full_bar(i), 1);
             ptx::mbar_init(empty_bar(i), 1);
@@ -383,8 +401,8 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
         const int disp = (blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * (blockIdx.z / Q))) * Q +
                          static_cast<int>(blockIdx.z % Q);
         if (disp < args.prefetchers) {
-            prefetch_part(args.A, args.a_bytes, disp, args.prefetchers, tid - 64, kThreads - 64);
-            prefetch_part(args.B, args.b_bytes, disp, args.prefetchers, tid - 64, kThreads - 64);
+            prefetch_part(ops.A[grp], args.a_bytes, disp, args.prefetchers, tid - 64, kThreads - 64);
+            prefetch_part(ops.B[grp], args.b_bytes, disp, args.prefetchers, tid - 64, kThreads - 64);
         }
     }
     ptx::tc_fence_before_sync();
@@ -703,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
             return acc;
         };
         if (args.split_sum != 2) {
-            float *const Ps = args.P + static_cast<size_t>(s) * MN;
+            float *const Ps = P + static_cast<size_t>(s) * MN;
             for (int g0 = my_lo + tid; g0 < my_hi; g0 += 2 * kThreads) {
                 const int g1 = g0 + kThreads;
                 const Piece p0 = piece_at(g0), p1 = piece_at(min(g1, my_hi - 1));
@@ -714,12 +732,11 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
                 if (p0.row < rows_here) *reinterpret_cast<float4 *>(Ps + tile_elem(p0)) = a0;
                 if (g1 < my_hi && p1.row < rows_here) *reinterpret_cast<float4 *>(Ps + tile_elem(p1)) = a1;
             }
-        } else if (args.P != nullptr) {
-            cluster_split_sum_for<Q, true>(CC, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, args.P,
-                                           args.out);
+        } else if (P != nullptr) {
+            cluster_split_sum_for<Q, true>(CC, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, P, out);
         } else {
             cluster_split_sum_for<Q, false>(CC, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, nullptr,
-                                            args.out);
+                                            out);
         }
     }
     // overlap 2 stored without waiting: the grid still finishes after the
@@ -887,6 +904,22 @@ constexpr size_t kSmemLimit = 226 * 1024;   // dynamic; leaves room for static s
 constexpr size_t kCompactSmemLimit = 112 * 1024;
 constexpr size_t kCompact3SmemLimit = 74 * 1024;
 
+// Tensor-memory columns a CTA may allocate for its shared memory, so that the
+// CTAs of these kernels that fit on an SM by shared memory (228 KB, 1 KB of
+// it reserved per CTA) always fit in its 512 columns and no allocation waits
+// on a CTA that may wait in turn: at most one column per 512 bytes, or 256
+// columns from 100 KB on.  Every plan has at least 32 KB per 64 columns (its
+// accumulator staging area), so the CTAs beside a 256-column one (at least
+// 101 KB with the reserve) hold at most 256 columns more: two 256-column
+// CTAs leave no room for a third CTA, one beside a 128-column CTA (66 KB)
+// leaves room for at most one of 64 (34 KB), and 64-column CTAs alone keep
+// to 2 columns per KB.
+constexpr size_t kTmem256Smem = 100 * 1024;
+bool tmem_fits(int cols, size_t smem)
+{
+    return static_cast<size_t>(cols) * 512 <= smem || (cols == 256 && smem >= kTmem256Smem);
+}
+
 // Dynamic shared memory of a plan: the stage ring (or the accumulator
 // staging, if larger), one receive slot per peer, and 1 KB of alignment slack.
 // With the receive slots in the ring (rir) they follow the staging area
@@ -903,7 +936,7 @@ size_t smem_for(int bn, int kbs, int stages, int chunks, int share, bool x3 = fa
 // Opts the kernel into the device's full dynamic shared memory (what is left
 // of the per-block opt-in limit after its static shared memory); once per
 // device.
-template <int BN, int Q, bool KN, bool X3, int TM>
+template <int BN, int Q, bool KN, bool X3, int TM, int G>
 cudaError_t prepare_kernel_attrs()
 {
     static std::mutex mu;
@@ -917,20 +950,20 @@ cudaError_t prepare_kernel_attrs()
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return note_error(e, "cudaDeviceGetAttribute(MaxSharedMemoryPerBlockOptin)");
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, tc_splitk_kernel<BN, Q, KN, X3, TM>);
+    e = cudaFuncGetAttributes(&fa, tc_splitk_kernel<BN, Q, KN, X3, TM, G>);
     if (e != cudaSuccess) return note_error(e, "cudaFuncGetAttributes(tc_splitk_kernel)");
     const int dyn = optin - static_cast<int>(fa.sharedSizeBytes);
-    e = cudaFuncSetAttribute(tc_splitk_kernel<BN, Q, KN, X3, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    e = cudaFuncSetAttribute(tc_splitk_kernel<BN, Q, KN, X3, TM, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dyn);
     if (e != cudaSuccess) return note_error(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
     if (dev >= 0 && dev < 64) done[dev] = true;
     return cudaSuccess;
 }
 
-template <int BN, int Q, bool KN, bool X3, int TM = kTileM>
-cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args, const TilePlan &plan,
-                      cudaStream_t stream)
+template <int BN, int Q, bool KN, bool X3, int TM = kTileM, int G = 1>
+cudaError_t launch_bn(const TcOperands<G> &ops, const TcArgs &args, const TilePlan &plan, cudaStream_t stream)
 {
-    cudaError_t e = prepare_kernel_attrs<BN, Q, KN, X3, TM>();
+    cudaError_t e = prepare_kernel_attrs<BN, Q, KN, X3, TM, G>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = plan.grid;
@@ -951,19 +984,18 @@ cudaError_t launch_bn(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
-    return note_error(cudaLaunchKernelEx(&cfg, tc_splitk_kernel<BN, Q, KN, X3, TM>, ta, tb, args),
+    return note_error(cudaLaunchKernelEx(&cfg, tc_splitk_kernel<BN, Q, KN, X3, TM, G>, ops, args),
                       "cudaLaunchKernelEx(tc_splitk_kernel)");
 }
 
-template <int BN, bool KN, bool X3>
-cudaError_t launch_cluster(const CUtensorMap &ta, const CUtensorMap &tb, const TcArgs &args, const TilePlan &plan,
-                           cudaStream_t stream)
+template <int BN, bool KN, bool X3, int G = 1>
+cudaError_t launch_cluster(const TcOperands<G> &ops, const TcArgs &args, const TilePlan &plan, cudaStream_t stream)
 {
     switch (plan.cluster) {
-    case 1: return launch_bn<BN, 1, KN, X3>(ta, tb, args, plan, stream);
-    case 2: return launch_bn<BN, 2, KN, X3>(ta, tb, args, plan, stream);
-    case 4: return launch_bn<BN, 4, KN, X3>(ta, tb, args, plan, stream);
-    case 8: return launch_bn<BN, 8, KN, X3>(ta, tb, args, plan, stream);
+    case 1: return launch_bn<BN, 1, KN, X3, kTileM, G>(ops, args, plan, stream);
+    case 2: return launch_bn<BN, 2, KN, X3, kTileM, G>(ops, args, plan, stream);
+    case 4: return launch_bn<BN, 4, KN, X3, kTileM, G>(ops, args, plan, stream);
+    case 8: return launch_bn<BN, 8, KN, X3, kTileM, G>(ops, args, plan, stream);
     default: return note_error(cudaErrorInvalidConfiguration, "cluster size");
     }
 }
@@ -1271,21 +1303,35 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     // the stores made before the wait for the previous grid.
     p.compact = 0;
     p.recv_in_ring = 0;
-    const auto try_compact = [&](int cpc) {
+    // cbn: the compact plan's tile width.  The products of an output element
+    // do not depend on it (the same K steps in the same MMA order; checked
+    // bitwise on GB300 for widths 64, 128 and 256), so a compact plan may be
+    // wider than the plan it stands for and still give the same bits.
+    const auto try_compact = [&](int cpc, int cbn) {
+        if (N % cbn) return false;
         const int qc = q / cpc;
-        const int64_t cctas = ctas / cpc;
-        if (clusters > resident_clusters(qc)) return false;
-        const int cshare = share_for(bn, qc);
+        const int64_t cctas = row_tiles * (N / cbn) * S * chunks / cpc;
+        if (cctas / qc > resident_clusters(qc)) return false;
+        const int cols = cbn * cpc;   // tensor-memory columns of a CTA
+        const int cshare = share_for(cbn, qc);
         const int cnkb = nkb * cpc;   // k-blocks of a CTA
         const auto double_buffered = [&](const StageChoice &c) {
             return c.ok && c.stages >= std::min(2, (cnkb + c.kbs - 1) / c.kbs) && (cpc == 1 || nkb % c.kbs == 0);
         };
         StageChoice cc;
-        if (qc <= 4 && (cctas > resident_clusters(1) / 2 || cpc > 1))
-            cc = pick_stages(bn, cnkb, can3d, qc, cshare, x3, tm, kCompact3SmemLimit, qc > 1);
-        if (!double_buffered(cc)) cc = pick_stages(bn, cnkb, can3d, qc, cshare, x3, tm, kCompactSmemLimit, qc > 1);
+        if (qc <= 4 && cols <= 128 && (cctas > resident_clusters(1) / 2 || cpc > 1))
+            cc = pick_stages(cbn, cnkb, can3d, qc, cshare, x3, tm, kCompact3SmemLimit, qc > 1);
+        if (!double_buffered(cc)) cc = pick_stages(cbn, cnkb, can3d, qc, cshare, x3, tm, kCompactSmemLimit, qc > 1);
         if (!double_buffered(cc)) return false;
+        // the staging area and the receive slots inside the ring, and the
+        // shared memory the tensor-memory rule asks for (tmem_fits)
+        const size_t in_ring = epi_bytes(cbn) + (qc > 1 ? static_cast<size_t>(qc - 1) * cshare * 16 : 0);
+        const size_t tmem_floor = cols <= 128 ? static_cast<size_t>(cols) * 512 : kTmem256Smem;
+        const size_t region0 =
+            round_up(std::max({cc.stages * stage_bytes(cbn, can3d ? cc.kbs : 1, x3, tm), in_ring, tmem_floor}), 1024);
+        if (region0 + 1024 > kCompactSmemLimit || !tmem_fits(cols, region0 + 1024)) return false;
         p.compact = 1;
+        p.bn = cbn;
         p.cpc = cpc;
         p.cluster = qc;
         p.share = cshare;
@@ -1293,16 +1339,11 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
         p.stages = cc.stages;
         p.kbs = can3d ? cc.kbs : 1;
         p.three_d = can3d && p.kbs > 1 ? 1 : 0;
-        // the staging area and the receive slots inside the ring; and at
-        // least 512 bytes per tensor-memory column (cpc accumulators), so
-        // that the CTAs that fit on an SM by shared memory, of any of these
-        // launches, always fit in its 512 columns
-        const size_t in_ring = epi_bytes(bn) + (qc > 1 ? static_cast<size_t>(qc - 1) * cshare * 16 : 0);
-        const size_t tmem_floor = static_cast<size_t>(bn) * cpc * 512;
-        p.region0 = static_cast<uint32_t>(
-            round_up(std::max({p.stages * stage_bytes(bn, p.kbs, x3, tm), in_ring, tmem_floor}), 1024));
-        p.smem_bytes = static_cast<size_t>(p.region0) + 1024;
-        p.grid.z = static_cast<unsigned>(S * chunks / cpc);
+        p.region0 = static_cast<uint32_t>(region0);
+        p.smem_bytes = region0 + 1024;
+        p.grid = dim3(static_cast<unsigned>(N / cbn), static_cast<unsigned>(row_tiles),
+                      static_cast<unsigned>(S * chunks / cpc));
+        p.rows_first = 0;
         // two or three CTAs to an SM: as many start beside a running launch as it has CTAs
         p.prefetchers = static_cast<int>(std::min<int64_t>(cctas, 2 * resident_clusters(qc) * qc - cctas));
         if (p.prefetchers < 0) p.prefetchers = 0;
@@ -1312,23 +1353,99 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     // stages, with the lo halves, are twice as large), never merged: on
     // GB300 F32 M96 N512 K512 went from 3.98 to 2.36 us per operation in
     // graphs of eight, M256 N1024 K2048 S2 from 14.5 to 10.7 us.
+    //
+    // A fused plan of 64-column tiles and two chunks first tries 128-column
+    // tiles with both chunks in a CTA (two 128-column accumulators, two CTAs
+    // per SM): a third less shared-memory traffic per product, half the CTAs.
+    // The headline shape went from 3.23 to 2.48 us per operation in graphs of
+    // eight calls grouped into one launch.
     if (compact && tm == kTileM && bn <= 128) {
-        const bool mergeable = !x3 && split_sum == 2 && chunks > 1 && bn * chunks <= 128 && can3d && chunk_len % kBlockK == 0;
-        if (!(mergeable && try_compact(chunks))) try_compact(1);
+        const bool mergeable = !x3 && split_sum == 2 && chunks > 1 && can3d && chunk_len % kBlockK == 0;
+        if (!(mergeable && chunks == 2 && bn == 64 && try_compact(2, 128)) &&
+            !(mergeable && bn * chunks <= 128 && try_compact(chunks, bn)))
+            try_compact(1, bn);
     }
     return p;
 }
 
 }  // namespace
 
-cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t stream)
+namespace {
+
+int elem_code(const GemmProblem &pr) { return pr.f32 ? 2 : pr.bf16 ? 1 : 0; }
+
+// The TMA maps of one problem's A and B for a plan.
+bool encode_problem(const GemmProblem &pr, const TilePlan &plan, CUtensorMap *ta, CUtensorMap *tb)
+{
+    const int et = elem_code(pr);
+    const int kbs = plan.three_d ? plan.kbs : 1;
+    const bool ok_a = plan.three_d ? encode_operand_3d(ta, pr.A, pr.M, pr.K, plan.tile_m, plan.kbs, et)
+                                   : encode_operand(ta, pr.A, pr.M, pr.K, plan.tile_m, et);
+    // the [K,N] weight is a row-major matrix of K rows of N: boxes of 64
+    // columns by kbs*64 rows
+    const bool ok_b = pr.b_kn ? encode_operand(tb, pr.B, pr.K, pr.N, kbs * kBlockK, et)
+                              : plan.three_d ? encode_operand_3d(tb, pr.B, pr.N, pr.K, plan.bn, plan.kbs, et)
+                                             : encode_operand(tb, pr.B, pr.N, pr.K, plan.bn, et);
+    return ok_a && ok_b;
+}
+
+template <int G>
+void set_problem(TcOperands<G> &ops, int g, const GemmProblem &pr, const TilePlan &plan)
+{
+    ops.P[g] = pr.P;
+    ops.out[g] = plan.fused ? pr.out : nullptr;
+    ops.A[g] = static_cast<const uint8_t *>(pr.A);
+    ops.B[g] = static_cast<const uint8_t *>(pr.B);
+}
+
+TcArgs make_args(const GemmProblem &pr, const TilePlan &plan)
+{
+    const int et = elem_code(pr);
+    TcArgs a = {};
+    a.split_sum = plan.split_sum;
+    a.M = static_cast<int>(pr.M);
+    a.N = static_cast<int>(pr.N);
+    a.K = static_cast<int>(pr.K);
+    a.S = static_cast<int>(pr.S);
+    a.kps = static_cast<int>(pr.kps);
+    a.group = 1;
+    a.m_tiles = static_cast<int>((pr.M + plan.tile_m - 1) / plan.tile_m);
+    a.chunks = plan.chunks;
+    a.chunk_len = plan.chunk_len;
+    a.stages = plan.stages;
+    a.kbs = plan.kbs;
+    a.three_d = plan.three_d;
+    a.share = plan.share;
+    a.region0 = plan.region0;
+    a.bf16 = pr.bf16 ? 1 : 0;
+    a.wait_limit_ns = kWaitLimitNs;
+    a.acc_probe = pr.acc_probe ? 1 : 0;
+    a.a_bytes = static_cast<uint64_t>(pr.M * pr.K) * elem_of(et);
+    a.b_bytes = static_cast<uint64_t>(pr.N * pr.K) * elem_of(et);
+    // a launch that starts beside the previous one loads its own operands at
+    // once; prefetching them into L2 only adds requests
+    a.prefetchers = pr.overlap ? 0 : plan.prefetchers;
+    a.rows_first = plan.rows_first;
+    a.overlap = pr.overlap ? (pr.store_early ? 2 : 1) : 0;
+    a.recv_in_ring = plan.recv_in_ring && plan.cluster > 1 ? 1 : 0;
+    a.cpc = plan.cpc;
+    return a;
+}
+
+}  // namespace
+
+namespace {
+
+// The plan and problem checks every launch makes before encoding anything.
+cudaError_t check_plan(const GemmProblem &pr, const TilePlan &plan)
 {
     const bool chunks_ok = (plan.chunks & (plan.chunks - 1)) == 0 && plan.chunks >= 1 && plan.chunks <= kMaxChunks &&
                            (plan.cluster * plan.cpc) % plan.chunks == 0;
     // several chunks per CTA: each its own accumulator (at most 128 tensor-
     // memory columns in all), its chunks whole k-blocks of whole stages
     const bool cpc_ok = plan.cpc == 1 ||
-                        (plan.cpc == plan.chunks && !plan.x3 && plan.tile_m == kTileM && plan.bn * plan.cpc <= 128 &&
+                        (plan.cpc == 2 && plan.cpc == plan.chunks && !plan.x3 && plan.tile_m == kTileM &&
+                         tmem_fits(plan.bn * plan.cpc, plan.smem_bytes) &&
                          plan.chunk_len % kBlockK == 0 && (plan.chunk_len / kBlockK) % plan.kbs == 0 &&
                          static_cast<int64_t>(plan.grid.z) * plan.cpc == pr.S * plan.chunks);
     if (!cpc_ok) return note_error(cudaErrorInvalidConfiguration, "chunks per CTA out of range");
@@ -1348,65 +1465,211 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
                                  static_cast<size_t>(plan.cluster - 1) * plan.share * 16 >
                              plan.region0)
         return note_error(cudaErrorInvalidConfiguration, "receive slots outside the stage ring");
-    CUtensorMap ta, tb;
-    const int et = pr.f32 ? 2 : pr.bf16 ? 1 : 0;
-    const int kbs = plan.three_d ? plan.kbs : 1;
-    const bool ok_a = plan.three_d ? encode_operand_3d(&ta, pr.A, pr.M, pr.K, plan.tile_m, plan.kbs, et)
-                                   : encode_operand(&ta, pr.A, pr.M, pr.K, plan.tile_m, et);
-    // the [K,N] weight is a row-major matrix of K rows of N: boxes of 64
-    // columns by kbs*64 rows
-    const bool ok_b = pr.b_kn ? encode_operand(&tb, pr.B, pr.K, pr.N, kbs * kBlockK, et)
-                              : plan.three_d ? encode_operand_3d(&tb, pr.B, pr.N, pr.K, plan.bn, plan.kbs, et)
-                                             : encode_operand(&tb, pr.B, pr.N, pr.K, plan.bn, et);
-    const bool ok = ok_a && ok_b;
-    if (!ok) return cudaErrorInvalidValue;
-    TcArgs a = {};
-    a.P = pr.P;
-    a.out = plan.fused ? pr.out : nullptr;
-    a.split_sum = plan.split_sum;
-    a.M = static_cast<int>(pr.M);
-    a.N = static_cast<int>(pr.N);
-    a.K = static_cast<int>(pr.K);
-    a.S = static_cast<int>(pr.S);
-    a.kps = static_cast<int>(pr.kps);
-    a.chunks = plan.chunks;
-    a.chunk_len = plan.chunk_len;
-    a.stages = plan.stages;
-    a.kbs = plan.kbs;
-    a.three_d = plan.three_d;
-    a.share = plan.share;
-    a.region0 = plan.region0;
-    a.bf16 = pr.bf16 ? 1 : 0;
-    a.wait_limit_ns = kWaitLimitNs;
-    a.acc_probe = pr.acc_probe ? 1 : 0;
-    a.A = static_cast<const uint8_t *>(pr.A);
-    a.B = static_cast<const uint8_t *>(pr.B);
-    a.a_bytes = static_cast<uint64_t>(pr.M * pr.K) * elem_of(et);
-    a.b_bytes = static_cast<uint64_t>(pr.N * pr.K) * elem_of(et);
-    // a launch that starts beside the previous one loads its own operands at
-    // once; prefetching them into L2 only adds requests
-    a.prefetchers = pr.overlap ? 0 : plan.prefetchers;
-    a.rows_first = plan.rows_first;
-    a.overlap = pr.overlap ? (pr.store_early ? 2 : 1) : 0;
-    a.recv_in_ring = plan.recv_in_ring && plan.cluster > 1 ? 1 : 0;
-    a.cpc = plan.cpc;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t stream)
+{
+    const cudaError_t ce = check_plan(pr, plan);
+    if (ce != cudaSuccess) return ce;
+    TcOperands<1> ops = {};
+    if (!encode_problem(pr, plan, &ops.tm[0][0], &ops.tm[0][1])) return cudaErrorInvalidValue;
+    set_problem(ops, 0, pr, plan);
+    const TcArgs a = make_args(pr, plan);
     // operand variants: [N,K] weight, [K,N] weight, F32 as 3xTF32
     const int variant = pr.f32 ? 2 : pr.b_kn ? 1 : 0;
     if (plan.tile_m == 2 * kTileM)
-        return variant == 1 ? launch_bn<256, 1, true, false, 2 * kTileM>(ta, tb, a, plan, stream)
-                            : launch_bn<256, 1, false, false, 2 * kTileM>(ta, tb, a, plan, stream);
+        return variant == 1 ? launch_bn<256, 1, true, false, 2 * kTileM>(ops, a, plan, stream)
+                            : launch_bn<256, 1, false, false, 2 * kTileM>(ops, a, plan, stream);
     switch (plan.bn * 4 + variant) {
-    case 64 * 4 + 0: return launch_cluster<64, false, false>(ta, tb, a, plan, stream);
-    case 64 * 4 + 1: return launch_cluster<64, true, false>(ta, tb, a, plan, stream);
-    case 64 * 4 + 2: return launch_cluster<64, false, true>(ta, tb, a, plan, stream);
-    case 128 * 4 + 0: return launch_cluster<128, false, false>(ta, tb, a, plan, stream);
-    case 128 * 4 + 1: return launch_cluster<128, true, false>(ta, tb, a, plan, stream);
-    case 128 * 4 + 2: return launch_cluster<128, false, true>(ta, tb, a, plan, stream);
-    case 256 * 4 + 0: return launch_cluster<256, false, false>(ta, tb, a, plan, stream);
-    case 256 * 4 + 1: return launch_cluster<256, true, false>(ta, tb, a, plan, stream);
-    case 256 * 4 + 2: return launch_cluster<256, false, true>(ta, tb, a, plan, stream);
+    case 64 * 4 + 0: return launch_cluster<64, false, false>(ops, a, plan, stream);
+    case 64 * 4 + 1: return launch_cluster<64, true, false>(ops, a, plan, stream);
+    case 64 * 4 + 2: return launch_cluster<64, false, true>(ops, a, plan, stream);
+    case 128 * 4 + 0: return launch_cluster<128, false, false>(ops, a, plan, stream);
+    case 128 * 4 + 1: return launch_cluster<128, true, false>(ops, a, plan, stream);
+    case 128 * 4 + 2: return launch_cluster<128, false, true>(ops, a, plan, stream);
+    case 256 * 4 + 0: return launch_cluster<256, false, false>(ops, a, plan, stream);
+    case 256 * 4 + 1: return launch_cluster<256, true, false>(ops, a, plan, stream);
+    case 256 * 4 + 2: return launch_cluster<256, false, true>(ops, a, plan, stream);
     default: return note_error(cudaErrorInvalidConfiguration, "tile width");
     }
+}
+
+// ---- grouping consecutive independent calls into one launch (graph capture)
+//
+// Inside a capture, a call that may store before the launch before it ends
+// (splitk_chain.cu: nothing in flight reads or writes its operands or outputs)
+// and that has the same shape and plan as that launch joins it: the launch's
+// kernel node gets the call's operands as one more problem (the group index
+// is the high part of blockIdx.y) and a grid that covers it, and no node is
+// added.  The problems of a group are independent, so their CTAs may run in
+// any order; the node keeps its place in the chain.  A group holds at most
+// kMaxGroup problems; grouped launches use the kernel instantiated for
+// kMaxGroup problems (16-bit operands, 128-row tiles, BN <= 128, clusters of
+// at most 4).
+namespace {
+
+struct GroupState {
+    bool valid = false;
+    unsigned long long capture = 0;
+    cudaGraphNode_t node = nullptr;
+    uint64_t stamp = 0;
+    // what every problem of the group shares
+    int64_t M = 0, N = 0, K = 0, S = 0, kps = 0;
+    bool bf16 = false, b_kn = false, keep_p = false, overlap = false, store_early = false;
+    TilePlan plan = {};
+    // the node's launch
+    void *func = nullptr;
+    size_t smem = 0;
+    TcOperands<kMaxGroup> ops = {};
+    TcArgs args = {};
+    int n = 0;
+};
+
+constexpr int kGroupSlots = 16;
+std::mutex g_group_mu;
+GroupState g_groups[kGroupSlots];
+uint64_t g_group_clock = 0;
+
+bool same_plan(const TilePlan &a, const TilePlan &b)
+{
+    return a.bn == b.bn && a.chunks == b.chunks && a.chunk_len == b.chunk_len && a.stages == b.stages &&
+           a.kbs == b.kbs && a.three_d == b.three_d && a.cluster == b.cluster && a.fused == b.fused &&
+           a.split_sum == b.split_sum && a.share == b.share && a.region0 == b.region0 && a.x3 == b.x3 &&
+           a.rows_first == b.rows_first && a.tile_m == b.tile_m && a.compact == b.compact &&
+           a.recv_in_ring == b.recv_in_ring && a.cpc == b.cpc && a.grid.x == b.grid.x && a.grid.y == b.grid.y &&
+           a.grid.z == b.grid.z && a.smem_bytes == b.smem_bytes;
+}
+
+bool groupable(const GemmProblem &pr, const TilePlan &plan)
+{
+    return plan.compact && !plan.x3 && !pr.f32 && !pr.acc_probe && plan.tile_m == kTileM && plan.bn <= 128 &&
+           plan.cluster <= 4 && !plan.rows_first;
+}
+
+template <int BN, bool KN>
+void *grouped_kernel(int q)
+{
+    switch (q) {
+    case 1: return reinterpret_cast<void *>(tc_splitk_kernel<BN, 1, KN, false, kTileM, kMaxGroup>);
+    case 2: return reinterpret_cast<void *>(tc_splitk_kernel<BN, 2, KN, false, kTileM, kMaxGroup>);
+    case 4: return reinterpret_cast<void *>(tc_splitk_kernel<BN, 4, KN, false, kTileM, kMaxGroup>);
+    default: return nullptr;
+    }
+}
+
+template <int BN, bool KN>
+cudaError_t launch_grouped_bn(const TcOperands<kMaxGroup> &ops, const TcArgs &a, const TilePlan &plan,
+                              cudaStream_t stream)
+{
+    switch (plan.cluster) {
+    case 1: return launch_bn<BN, 1, KN, false, kTileM, kMaxGroup>(ops, a, plan, stream);
+    case 2: return launch_bn<BN, 2, KN, false, kTileM, kMaxGroup>(ops, a, plan, stream);
+    case 4: return launch_bn<BN, 4, KN, false, kTileM, kMaxGroup>(ops, a, plan, stream);
+    default: return note_error(cudaErrorInvalidConfiguration, "cluster size");
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_tc_grouped(const GemmProblem &pr, const TilePlan &plan, cudaStream_t stream,
+                              unsigned long long capture)
+{
+    if (!groupable(pr, plan) || capture == 0) return launch_tc(pr, plan, stream);
+    cudaError_t e = check_plan(pr, plan);
+    if (e != cudaSuccess) return e;
+    GroupState st;
+    if (!encode_problem(pr, plan, &st.ops.tm[0][0], &st.ops.tm[0][1])) return cudaErrorInvalidValue;
+    set_problem(st.ops, 0, pr, plan);
+    st.args = make_args(pr, plan);
+    st.args.group = 1;
+    switch (plan.bn * 2 + (pr.b_kn ? 1 : 0)) {
+    case 64 * 2 + 0: e = launch_grouped_bn<64, false>(st.ops, st.args, plan, stream); st.func = grouped_kernel<64, false>(plan.cluster); break;
+    case 64 * 2 + 1: e = launch_grouped_bn<64, true>(st.ops, st.args, plan, stream); st.func = grouped_kernel<64, true>(plan.cluster); break;
+    case 128 * 2 + 0: e = launch_grouped_bn<128, false>(st.ops, st.args, plan, stream); st.func = grouped_kernel<128, false>(plan.cluster); break;
+    case 128 * 2 + 1: e = launch_grouped_bn<128, true>(st.ops, st.args, plan, stream); st.func = grouped_kernel<128, true>(plan.cluster); break;
+    default: return note_error(cudaErrorInvalidConfiguration, "tile width");
+    }
+    if (e != cudaSuccess) return e;
+    // the node just captured, which later calls may join
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    unsigned long long id = 0;
+    const cudaGraphNode_t *deps = nullptr;
+    size_t nd = 0;
+    if (cudaStreamGetCaptureInfo(stream, &cs, &id, nullptr, &deps, nullptr, &nd) != cudaSuccess ||
+        cs != cudaStreamCaptureStatusActive || id != capture || nd != 1 || st.func == nullptr)
+        return cudaSuccess;   // launched; just not joinable
+    st.valid = true;
+    st.capture = capture;
+    st.node = deps[0];
+    st.M = pr.M; st.N = pr.N; st.K = pr.K; st.S = pr.S; st.kps = pr.kps;
+    st.bf16 = pr.bf16; st.b_kn = pr.b_kn; st.keep_p = pr.P != nullptr;
+    st.overlap = pr.overlap; st.store_early = pr.store_early;
+    st.plan = plan;
+    st.smem = plan.smem_bytes;
+    st.n = 1;
+    std::lock_guard<std::mutex> lock(g_group_mu);
+    // the capture's slot, else a free one, else the least recently used
+    GroupState *slot = nullptr;
+    for (GroupState &g : g_groups)
+        if (g.valid && g.capture == capture) slot = &g;
+    if (!slot)
+        for (GroupState &g : g_groups)
+            if (!g.valid) {
+                slot = &g;
+                break;
+            }
+    if (!slot) {
+        slot = &g_groups[0];
+        for (GroupState &g : g_groups)
+            if (g.stamp < slot->stamp) slot = &g;
+    }
+    st.stamp = ++g_group_clock;
+    *slot = st;
+    return cudaSuccess;
+}
+
+bool join_group(const GemmProblem &pr, const TilePlan &plan, unsigned long long capture, cudaGraphNode_t dep,
+                int *group_size, int *mode)
+{
+    if (!groupable(pr, plan) || capture == 0 || dep == nullptr) return false;
+    if (check_plan(pr, plan) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(g_group_mu);
+    GroupState *st = nullptr;
+    for (GroupState &g : g_groups)
+        if (g.valid && g.capture == capture) st = &g;
+    if (!st || st->node != dep || st->n >= kMaxGroup) return false;
+    const bool same = st->M == pr.M && st->N == pr.N && st->K == pr.K && st->S == pr.S && st->kps == pr.kps &&
+                      st->bf16 == pr.bf16 && st->b_kn == pr.b_kn && st->keep_p == (pr.P != nullptr) &&
+                      same_plan(st->plan, plan);
+    if (!same) return false;
+    const int g = st->n;
+    if (!encode_problem(pr, plan, &st->ops.tm[g][0], &st->ops.tm[g][1])) return false;
+    set_problem(st->ops, g, pr, plan);
+    TcArgs a = st->args;
+    a.group = g + 1;
+    a.prefetchers = 0;   // several problems: no early CTAs prefetch one of them
+    cudaKernelNodeParams kp = {};
+    kp.func = st->func;
+    kp.gridDim = dim3(plan.grid.x, plan.grid.y * static_cast<unsigned>(g + 1), plan.grid.z);
+    kp.blockDim = dim3(kThreads, 1, 1);
+    kp.sharedMemBytes = static_cast<unsigned>(st->smem);
+    void *params[2] = {&st->ops, &a};
+    kp.kernelParams = params;
+    kp.extra = nullptr;
+    if (cudaGraphKernelNodeSetParams(st->node, &kp) != cudaSuccess) {
+        (void)cudaGetLastError();
+        st->valid = false;   // leave the node as it was; the call launches on its own
+        return false;
+    }
+    st->args = a;
+    st->n = g + 1;
+    st->stamp = ++g_group_clock;
+    if (group_size) *group_size = st->n;
+    if (mode) *mode = st->overlap ? (st->store_early ? 2 : 1) : 0;
+    return true;
 }
 
 cudaError_t read_and_clear_device_status(cudaStream_t stream, unsigned *status)

@@ -32,9 +32,9 @@ def lib():
     sk.build()
     sk.lib()
     sk.splitk_set_tile_override(0, 0, 0)
-    sk.splitk_set_overlap(True)
+    sk.splitk_set_overlap(1)   # overlap, one launch per call (grouping: its own tests below)
     yield sk
-    sk.splitk_set_overlap(True)
+    sk.splitk_set_overlap(2)
 
 
 def operands(M, N, K, dt, seed):
@@ -274,7 +274,7 @@ def test_overlap_switch(lib):
         sk.splitk_set_overlap(False)
         g = capture(body)
     finally:
-        sk.splitk_set_overlap(True)
+        sk.splitk_set_overlap(1)
     assert all(d["overlap"] == 0 and d["compact"] == 0 and d["capturing"] == 0 for d in seen)
     g.replay()
     torch.cuda.synchronize()
@@ -450,4 +450,142 @@ def test_f32_calls_overlap_bitwise(lib, shape, fused):
         torch.cuda.synchronize()
         for it in insts:
             assert bitwise(it["out"], it["ref"])
+    assert sk.splitk_get_device_status() == 0
+
+
+# ---- grouping: consecutive independent calls of one shape in one launch
+
+@pytest.fixture
+def grouping(lib):
+    lib.splitk_set_overlap(2)
+    yield lib
+    lib.splitk_set_overlap(1)
+
+
+@pytest.mark.parametrize("shape", [
+    (256, 1024, 2048, 2, 1024),   # the headline: both chunks of a split per block, clusters of 2
+    (96, 512, 2048, 4, 512),      # clusters of 4
+    (256, 512, 2048, 4, 512),     # one chunk per split
+    (256, 1024, 1536, 2, 1024),   # an empty last chunk
+])
+@pytest.mark.parametrize("fused", [1, 3])
+def test_grouped_calls_bitwise(grouping, shape, fused):
+    """12 independent calls of one shape: the first launches (heading the
+    run), the next 7 join its launch, the 9th launches again and the last 3
+    join that one.  Every output (and kept partials) is the eager one, bit
+    for bit."""
+    sk = grouping
+    M, N, K, S, kps = shape
+    dt = "bf16"
+    insts = instances(sk, M, N, K, S, kps, dt, 12)
+    for it in insts:
+        sk.gemm_bt(it["A"], it["B"], it["ref"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=fused)
+    torch.cuda.synchronize()
+    refs_ws = [it["ws"].clone() for it in insts]
+    seen = []
+
+    def body():
+        for it in insts:
+            sk.gemm_bt(it["A"], it["B"], it["out"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=fused)
+            seen.append(sk.splitk_last_launch())
+
+    g = capture(body)
+    assert [d["group"] for d in seen] == [1, 2, 3, 4, 5, 6, 7, 8, 1, 2, 3, 4], seen
+    assert seen[0]["overlap"] == 0 and seen[8]["overlap"] == 2, seen
+    for _ in range(3):
+        for it in insts:
+            it["out"].fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        for it in insts:
+            assert bitwise(it["out"], it["ref"])
+    if fused == 3:
+        for it, w in zip(insts, refs_ws):
+            P = S * M * N
+            assert bitwise(it["ws"][:P], w[:P])
+    assert sk.splitk_get_device_status() == 0
+
+
+def test_grouping_only_same_shape_and_independent(grouping):
+    """Calls of two shapes in turn never group; a call that reads the output
+    of the call before it does not join it (it waits), and the independent
+    call after it joins that one."""
+    sk = grouping
+    dt = "bf16"
+    s1, s2 = (256, 1024, 2048, 2, 1024), (256, 512, 2048, 4, 512)
+    a = instances(sk, *s1, dt, 3)
+    b = instances(sk, *s2, dt, 3)
+    seen = []
+
+    def alternate(record=None):
+        for x, y in zip(a, b):
+            sk.gemm_bt(x["A"], x["B"], x["out"], x["ws"], x["nb"], *s1, dt, fused=1)
+            if record is not None:
+                record.append(sk.splitk_last_launch()["group"])
+            sk.gemm_bt(y["A"], y["B"], y["out"], y["ws"], y["nb"], *s2, dt, fused=1)
+            if record is not None:
+                record.append(sk.splitk_last_launch()["group"])
+
+    g = capture(lambda: alternate(seen))
+    assert seen == [1] * 6, seen
+    for x, y in zip(a, b):
+        x["out"].fill_(7.0)
+        y["out"].fill_(7.0)
+    g.replay()
+    torch.cuda.synchronize()
+    got = [t["out"].clone() for t in a + b]
+    alternate()
+    torch.cuda.synchronize()
+    assert all(bitwise(u, t["out"]) for u, t in zip(got, a + b))
+
+    # a call writing what the call before it writes does not join it (it
+    # stores only after that launch has finished); the call after it, touching
+    # nothing in flight, joins it
+    c = instances(sk, *s1, dt, 3)
+    O = torch.empty(s1[0], s1[1], device="cuda")
+    rec = []
+
+    def waw(record=None):
+        for k, it in enumerate(c):
+            o = O if k < 2 else it["out"]
+            sk.gemm_bt(it["A"], it["B"], o, it["ws"], it["nb"], *s1, dt, fused=1)
+            if record is not None:
+                d = sk.splitk_last_launch()
+                record.append((d["overlap"], d["group"]))
+
+    waw()
+    torch.cuda.synchronize()
+    ref_o, ref_c = O.clone(), c[2]["out"].clone()
+    g2 = capture(lambda: waw(rec))
+    assert rec == [(0, 1), (1, 1), (1, 2)], rec
+    O.fill_(7.0)
+    c[2]["out"].fill_(7.0)
+    g2.replay()
+    torch.cuda.synchronize()
+    assert bitwise(O, ref_o) and bitwise(c[2]["out"], ref_c)
+    assert sk.splitk_get_device_status() == 0
+
+
+def test_grouped_kn_bitwise(grouping):
+    """The [K,N] weight groups the same way, bitwise the [N,K] path."""
+    sk = grouping
+    M, N, K, S, kps, dt = 256, 1024, 2048, 2, 1024, "bf16"
+    insts = instances(sk, M, N, K, S, kps, dt, 8)
+    for it in insts:
+        it["W"] = it["B"].t().contiguous()
+        sk.gemm_bt(it["A"], it["B"], it["ref"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=1)
+    torch.cuda.synchronize()
+    seen = []
+
+    def body():
+        for it in insts:
+            sk.gemm_kn(it["A"], it["W"], it["out"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=1)
+            seen.append(sk.splitk_last_launch()["group"])
+
+    g = capture(body)
+    assert seen == list(range(1, 9)), seen
+    g.replay()
+    torch.cuda.synchronize()
+    for it in insts:
+        assert bitwise(it["out"], it["ref"])
     assert sk.splitk_get_device_status() == 0

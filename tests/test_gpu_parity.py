@@ -258,6 +258,41 @@ def test_every_tiling(lib, case):
         sk.splitk_set_tile_override(0, 0, 0)
 
 
+@pytest.mark.parametrize("case", [(256, 1024, 2048, 2, 1024, "bf16"), (96, 512, 2048, 4, 512, "bf16"),
+                                  (256, 512, 2048, 4, 512, "f16"), (160, 512, 640, 2, 320, "bf16"),
+                                  (128, 512, 1024, 2, 512, "f32")],
+                         ids=["headline", "M96", "M256N512-f16", "M160-tail", "f32"])
+def test_tile_width_does_not_change_bits(lib, case):
+    """For a given chunking, the tile width (64, 128 or 256 columns) does not
+    change one bit of the partials: each output element gets the same MMA K
+    steps in the same order.  The compact layout inside graph captures relies
+    on this when it widens a plan's tiles."""
+    sk = lib
+    M, N, K, S, kps, dt = case
+    ops, Pr, SP, Or, SO = oracle_case(M, N, K, S, kps, dt)
+    A = device_operand(ops.A, dt)
+    B = device_operand(ops.B, dt)
+    try:
+        for ch in (1, 2, 4):
+            got = {}
+            for bn in (64, 128, 256):
+                sk.splitk_set_tile_override(bn, ch, 0)
+                d = sk.splitk_describe_launch(M, N, K, S, kps, dt, fused=0)
+                if d["bn"] != bn or d["chunks"] != ch:
+                    continue
+                P = Guarded(S * M * N)
+                sk.gemm_splitk_bt(A, B, P.data, M, N, K, S, kps, dt)
+                assert sk.splitk_get_device_status() == 0 and P.guards_intact()
+                got[bn] = P.numpy().view(np.uint32).copy()
+                assert max_scaled_error(P.numpy().reshape(S, M, N), Pr, SP) <= TOL_PARTIAL, (bn, ch)
+            widths = sorted(got)
+            assert len(widths) >= 2, (ch, widths)
+            for w in widths[1:]:
+                assert np.array_equal(got[widths[0]], got[w]), (ch, widths[0], w)
+    finally:
+        sk.splitk_set_tile_override(0, 0, 0)
+
+
 def test_cuda_graph_capture_and_side_stream(lib):
     sk = lib
     M, N, K, S, kps, dt = 256, 1024, 2048, 2, 1024, "bf16"

@@ -34,6 +34,7 @@ import pytest
 from test_gpu_fuzz import LARGE, RANDOM
 
 SMEM_LIMIT = 226 * 1024
+TMEM256_SMEM = 100 * 1024     # a 256-column block's shared memory, at least (the tensor-memory rule)
 COMPACT_LIMIT = 112 * 1024
 COMPACT3_LIMIT = 74 * 1024    # three thread blocks to an SM
 SM_SMEM = 228 * 1024          # per SM; 1 KB of it reserved per thread block
@@ -49,6 +50,40 @@ def lib():
     sk.build()
     sk.lib()
     return sk
+
+
+def tmem_fits(cols, smem):
+    """The tensor-memory rule of the planner: one column per 512 bytes of
+    shared memory, or 256 columns from 100 KB on."""
+    return cols * 512 <= smem or (cols == 256 and smem >= TMEM256_SMEM)
+
+
+def test_tmem_rule_never_oversubscribes():
+    """Whatever mix of these kernels' blocks fits on an SM by shared memory
+    (228 KB, 1 KB reserved per block and the static part), their tensor-
+    memory columns fit in its 512.  Each plan's shared memory is at least its
+    accumulator staging area, 512 bytes per 128-row column: 32 KB for 64
+    columns, 64 KB for 128; the smallest footprint for each column count
+    that the rule allows is enumerated, and every multiset of them that fits
+    is checked."""
+    import functools
+
+    per_sm = SM_SMEM
+    kinds = [(512, SMEM_LIMIT + 1024 + STATIC_SMEM)]   # 256-row tiles take all of a block's shared memory
+    for cols in (64, 128, 256):
+        smem = min(s for s in range(1024, SMEM_LIMIT + 1, 1024) if tmem_fits(cols, s) and s >= cols * 256)
+        kinds.append((cols, smem + 1024 + STATIC_SMEM))
+
+    @functools.lru_cache(maxsize=None)
+    def most(room, start):
+        best = 0
+        for i in range(start, len(kinds)):
+            cols, foot = kinds[i]
+            if foot <= room:
+                best = max(best, cols + most(room - foot, i))
+        return best
+
+    assert most(per_sm, 0) <= 512, kinds
 
 
 def piece(g):
@@ -129,43 +164,48 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
     # the receive slots inside it after the staging area
     if d["compact"]:
         assert TM == TILE_M and BN <= 128
-        assert -(-M // TM) * (N // BN) * S * C // Q <= RESIDENT_CLUSTERS[Q]   # one wave
         cst, ckbs, csmem = d["compact_stages"], d["compact_kblocks_per_stage"], d["compact_smem_bytes"]
-        cpc, qc = d["compact_chunks_per_block"], d["compact_cluster"]
+        cpc, qc, CB = d["compact_chunks_per_block"], d["compact_cluster"], d["compact_bn"]
         assert 1 <= cst <= 8 and 1 <= ckbs <= 4 and (ckbs == 1 or T3 or (K % kb_elems == 0 and kps % kb_elems == 0))
         # every chunk of a split in one block: only where the chunks are whole
-        # stages of whole k-blocks and the accumulators fit 128 columns
+        # stages of whole k-blocks; 128-column tiles (from 64) only so, with
+        # two chunks
         can3d = K % kb_elems == 0 and kps % kb_elems == 0
-        mergeable = not x3 and SS == 2 and C > 1 and BN * C <= 128 and can3d and CL % 64 == 0
-        assert cpc in (1, C) and (cpc == 1 or mergeable)
+        mergeable = not x3 and SS == 2 and C > 1 and can3d and CL % 64 == 0
+        assert CB == BN or (CB == 128 and BN == 64 and C == 2 and cpc == 2 and mergeable), (BN, CB, cpc)
+        assert cpc in (1, C) and (cpc == 1 or (mergeable and CB * C <= 256))
         assert qc == Q // cpc and d["compact_grid_z"] == S * C // cpc and d["compact_grid_z"] % qc == 0
-        assert -(-M // TM) * (N // BN) * S * C // Q <= RESIDENT_CLUSTERS[qc]
-        cstage = (TM + BN) * 128 * ckbs * (2 if x3 else 1)
+        assert N % CB == 0
+        cctas = -(-M // TM) * (N // CB) * S * C // cpc
+        assert cctas // qc <= RESIDENT_CLUSTERS[qc]       # one wave
+        cstage = (TM + CB) * 128 * ckbs * (2 if x3 else 1)
         nkb = -(-CL // kb_elems)
         cnkb = nkb * cpc                                  # k-blocks of a block
         assert cst >= min(2, -(-cnkb // ckbs))            # double-buffered unless one stage holds them all
         if cpc > 1:
             assert nkb % ckbs == 0                        # a chunk's first k-block starts a stage
-        cshare = -(-(-(-pieces // qc)) // 8) * 8
+        cpieces = 32 * CB
+        cshare = -(-(-(-cpieces // qc)) // 8) * 8
+        cepi = TILE_M * CB * 4
         recv_bytes = (qc - 1) * cshare * 16
-        cols = BN * cpc                                   # tensor memory: a power of two >= 32
-        cregion = -(-max(cst * cstage, epi_bytes + recv_bytes, cols * 512) // 1024) * 1024
+        cols = CB * cpc                                   # tensor memory: a power of two >= 32
+        floor = cols * 512 if cols <= 128 else TMEM256_SMEM
+        cregion = -(-max(cst * cstage, cepi + recv_bytes, floor) // 1024) * 1024
         assert csmem == cregion + 1024 <= COMPACT_LIMIT
         assert 2 * (csmem + STATIC_SMEM + 1024) <= SM_SMEM   # two blocks to an SM
-        assert cols & (cols - 1) == 0 and 2 * cols <= 512 and cols <= csmem // 512
+        assert cols & (cols - 1) == 0 and 2 * cols <= 512 and tmem_fits(cols, csmem)
         # three to an SM for merged launches and for launches of more CTAs
-        # than half the SMs, with clusters of at most 4, wherever a
-        # double-buffered ring of single k-block stages and the staging plus
-        # receive slots fit in 74 KB
-        cctas = -(-M // TM) * (N // BN) * S * C // cpc
+        # than half the SMs, with clusters of at most 4 and at most 128
+        # columns, wherever a double-buffered ring of single k-block stages
+        # and the staging plus receive slots fit in 74 KB
         kmin = kbs if (kbs and T3) else 1                    # the smallest stage the override allows
-        stage1 = (TM + BN) * 128 * kmin * (2 if x3 else 1)
-        fits3 = max(min(2, -(-cnkb // kmin)) * stage1, epi_bytes + recv_bytes, cols * 512) + 1024 <= COMPACT3_LIMIT
-        if qc <= 4 and (cctas > 74 or cpc > 1) and fits3:
+        stage1 = (TM + CB) * 128 * kmin * (2 if x3 else 1)
+        fits3 = max(min(2, -(-cnkb // kmin)) * stage1, cepi + recv_bytes, floor) + 1024 <= COMPACT3_LIMIT
+        if qc <= 4 and cols <= 128 and (cctas > 74 or cpc > 1) and fits3:
             assert csmem <= COMPACT3_LIMIT and 3 * (csmem + STATIC_SMEM + 1024) <= SM_SMEM and 3 * cols <= 512
         check_k_coverage(K, S, kps, C, CL, ckbs, int(ckbs > 1), kb_elems, elem, cpc)
         if qc > 1:
-            check_exchange(BN, qc, epi_bytes, cregion)
+            check_exchange(CB, qc, cepi, cregion)
     else:
         assert d["compact_stages"] == d["compact_kblocks_per_stage"] == d["compact_smem_bytes"] == 0
         assert d["compact_chunks_per_block"] == d["compact_cluster"] == d["compact_grid_z"] == 0
