@@ -1507,8 +1507,7 @@ cudaError_t launch_tc(const GemmProblem &pr, const TilePlan &plan, cudaStream_t 
 // added.  The problems of a group are independent, so their CTAs may run in
 // any order; the node keeps its place in the chain.  A group holds at most
 // kMaxGroup problems; grouped launches use the kernel instantiated for
-// kMaxGroup problems (16-bit operands, 128-row tiles, BN <= 128, clusters of
-// at most 4).
+// kMaxGroup problems (16-bit operands, 128-row tiles, BN <= 128).
 namespace {
 
 struct GroupState {
@@ -1546,7 +1545,7 @@ bool same_plan(const TilePlan &a, const TilePlan &b)
 bool groupable(const GemmProblem &pr, const TilePlan &plan)
 {
     return plan.compact && !plan.x3 && !pr.f32 && !pr.acc_probe && plan.tile_m == kTileM && plan.bn <= 128 &&
-           plan.cluster <= 4 && !plan.rows_first;
+           !plan.rows_first;
 }
 
 template <int BN, bool KN>
@@ -1556,6 +1555,7 @@ void *grouped_kernel(int q)
     case 1: return reinterpret_cast<void *>(tc_splitk_kernel<BN, 1, KN, false, kTileM, kMaxGroup>);
     case 2: return reinterpret_cast<void *>(tc_splitk_kernel<BN, 2, KN, false, kTileM, kMaxGroup>);
     case 4: return reinterpret_cast<void *>(tc_splitk_kernel<BN, 4, KN, false, kTileM, kMaxGroup>);
+    case 8: return reinterpret_cast<void *>(tc_splitk_kernel<BN, 8, KN, false, kTileM, kMaxGroup>);
     default: return nullptr;
     }
 }
@@ -1568,6 +1568,7 @@ cudaError_t launch_grouped_bn(const TcOperands<kMaxGroup> &ops, const TcArgs &a,
     case 1: return launch_bn<BN, 1, KN, false, kTileM, kMaxGroup>(ops, a, plan, stream);
     case 2: return launch_bn<BN, 2, KN, false, kTileM, kMaxGroup>(ops, a, plan, stream);
     case 4: return launch_bn<BN, 4, KN, false, kTileM, kMaxGroup>(ops, a, plan, stream);
+    case 8: return launch_bn<BN, 8, KN, false, kTileM, kMaxGroup>(ops, a, plan, stream);
     default: return note_error(cudaErrorInvalidConfiguration, "cluster size");
     }
 }

@@ -467,6 +467,8 @@ def grouping(lib):
     (96, 512, 2048, 4, 512),      # clusters of 4
     (256, 512, 2048, 4, 512),     # one chunk per split
     (256, 1024, 1536, 2, 1024),   # an empty last chunk
+    (32, 512, 2048, 1, 2048),     # clusters of 8 (8 chunks)
+    (96, 512, 512, 2, 256),       # clusters of 8 (2 splits x 4 chunks)
 ])
 @pytest.mark.parametrize("fused", [1, 3])
 def test_grouped_calls_bitwise(grouping, shape, fused):
