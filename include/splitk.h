@@ -365,10 +365,17 @@ int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
  *  compact_stages, compact_kblocks_per_stage, compact_dynamic_smem_bytes,
  *  compact_chunks_per_block (1, or every chunk of a split in one thread
  *  block, each in its own accumulator, added in chunk order before the
- *  exchange: the same sums), compact_cluster_size, compact_grid_z,
+ *  exchange: the same sums; or, more than chunks, every chunk of every
+ *  split in one block of 128 x 128, no cluster and one block per SM, which
+ *  adds each split's chunks and then the splits in the same order: fused
+ *  16-bit calls whose splits are full and whose chunks tile them, where the
+ *  compact plan would take more than half the SMs), compact_cluster_size,
+ *  compact_grid_z,
  *  compact_bn (the compact plan's tile width, which may be wider than bn:
  *  the products of an output element do not depend on it)
- *  (0 when compact is 0)}; `info` must hold 26 ints.
+ *  (0 when compact is 0).  The compact fields describe a call that starts
+ *  beside the launch before it; the first call of a capture takes the
+ *  compact layout without whole-K blocks}; `info` must hold 26 ints.
  * Returns a status as gemm_bt's validation would (pointers are not checked). */
 int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits,
                            int64_t k_per_split, int dtype, int fused,
@@ -414,7 +421,8 @@ int splitk_set_overlap(int mode);
  * plan allows it), capturing (the stream was being captured), bn, chunks,
  * stages, kblocks_per_stage, dynamic_smem_bytes, chunks_per_block (1, or
  * all the chunks of a split, each in its own accumulator and added in chunk
- * order inside the block: the same sums), cluster_size, group (the calls
+ * order inside the block: the same sums; more than chunks: every chunk of
+ * every split, no cluster), cluster_size, group (the calls
  * the launch computes so far: 1, or more where the call joined the launch
  * of the calls before it)}.  `info` must hold 11 ints.  Diagnostic;
  * returns SPLITK_OK or SPLITK_ERR_NULL. */

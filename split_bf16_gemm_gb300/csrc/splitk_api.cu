@@ -123,7 +123,7 @@ int run_partial_pass(const void *A, const void *B, float *P, float *out, int64_t
     if (out) writes[nw++] = splitk::span_of(out, static_cast<uint64_t>(M * N) * 4);
     splitk::ChainGuard chain(stream, reads, 2, writes, nw);
     const bool compact = chain.capturing() && (chain.overlap() || chain.fresh());
-    TilePlan plan = splitk::plan_tc(M, N, K, S, kps, fused, pr.f32, compact);
+    TilePlan plan = splitk::plan_tc(M, N, K, S, kps, fused, pr.f32, compact, compact && chain.overlap());
     if (!prefetch) plan.prefetchers = 0;
     pr.overlap = chain.overlap();
     pr.store_early = chain.store_early();
@@ -405,9 +405,9 @@ int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits, int6
     info[16] = p.rows_first;
     info[17] = p.tile_m;
     // the layout a tensor-core launch of this call takes inside a graph
-    // capture when it may start beside the launch before it (16-bit only)
+    // capture when it may start beside the launch before it
     {
-        const TilePlan c = splitk::plan_tc(M, N, K, splits, k_per_split, in_kernel, x3, true);
+        const TilePlan c = splitk::plan_tc(M, N, K, splits, k_per_split, in_kernel, x3, true, true);
         info[18] = c.compact;
         info[19] = c.compact ? c.stages : 0;
         info[20] = c.compact ? c.kbs : 0;

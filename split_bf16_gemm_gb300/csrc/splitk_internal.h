@@ -65,9 +65,11 @@ constexpr int kMaxGroup = 8;   // independent calls one launch may compute (grap
 // compact: the layout that lets two or three CTAs share an SM, where that
 // plan exists (plan.compact says whether it was taken).
 // A fused compact plan may give each CTA all the chunks of its split
-// (plan.cpc > 1).
+// (plan.cpc > 1); with whole_k, for a launch that follows another, every
+// chunk of every split (plan.cpc > plan.chunks, no cluster) where the
+// compact plan would take more than half the SMs.
 TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3 = false,
-                 bool compact = false);
+                 bool compact = false, bool whole_k = false);
 // The planner's estimate (microseconds) of one tensor-core launch of that
 // plan behind another launch, the in-launch split sum included when fused.
 double estimate_tc_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3 = false);

@@ -299,18 +299,26 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
     const CUtensorMap *const tmB = &ops.tm[grp][1];
     float *const P = ops.P[grp];
     float *const out = ops.out[grp];
-    // A CTA covers cpc consecutive chunks of one split, each summed in its
+    // A CTA covers cpc consecutive (split, chunk) units, each summed in its
     // own accumulator (cpc > 1 only for 16-bit, 128-row plans whose chunks
-    // are whole k-blocks of whole stages): the same products, chunk sums and
-    // order as one CTA per chunk, with the chunk sum taken before the
-    // exchange.  CC CTAs cover a split.
+    // are whole k-blocks of whole stages): one chunk, every chunk of a
+    // split, or (whole_k) every chunk of every split, where the splits are
+    // full and their chunks tile them.  The same products, chunk sums and
+    // order as one CTA per chunk: the chunk sums (and with whole_k the split
+    // sum) are taken before the exchange.  CC CTAs cover a split.
     const int cpc = args.cpc;
-    const int CC = args.chunks / cpc;
-    const int s = blockIdx.z / CC;
-    const int c = (blockIdx.z - s * CC) * cpc;      // its first chunk
+    const int C = args.chunks;
+    // (whole_k only in the kernels a whole-K plan launches: 16-bit, 128 x 128
+    // tiles, no cluster; the others keep their registers)
+    constexpr bool kWholeK = Q == 1 && BN == 128 && !X3 && TM == kTileM;
+    const bool whole_k = kWholeK && cpc > C;
+    const int CC = whole_k ? 1 : C / cpc;
+    const int u0 = static_cast<int>(blockIdx.z) * cpc;
+    const int s = u0 / C;                           // its first split
+    const int c = u0 - s * C;                       // its first chunk there
     const int rank = static_cast<int>(blockIdx.z) % Q;  // in the 1 x 1 x Q cluster: split*CC + CTA of the split
     const int ks = s * args.kps;
-    const int ke = min(ks + args.kps, args.K);      // the last split clamps to K
+    const int ke = whole_k ? args.K : min(ks + args.kps, args.K);   // the last split clamps to K
     const int k_lo = ks + c * args.chunk_len;
     const int k_hi = min(k_lo + cpc * args.chunk_len, ke);
     const int klen = k_hi > k_lo ? k_hi - k_lo : 0; // a chunk past a short split is empty
@@ -621,36 +629,94 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
                     ptx::st_shared_v4(row_addr + (static_cast<uint32_t>(q ^ (lane & 7)) << 4), v[4 * q],
                                       v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             } else {
-                // the chunk sum: chunk 0 + chunk 1 + ... in order, a chunk
-                // past the split's end adding +0 -- what the owner adds when
-                // each chunk has its own CTA.  16 columns at a time.
+                if (!whole_k) {
+                    // the chunk sum: chunk 0 + chunk 1 + ... in order, a chunk
+                    // past the split's end adding +0 -- what the owner adds when
+                    // each chunk has its own CTA.  16 columns at a time.
 #pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t v[16];
-                    const uint32_t col = static_cast<uint32_t>(jb * 32 + hh * 16);
-                    if (have_acc) {
-                        ptx::tmem_ld_32x32b_x16(lane_base + col, v);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t v[16];
+                        const uint32_t col = static_cast<uint32_t>(jb * 32 + hh * 16);
+                        if (have_acc) {
+                            ptx::tmem_ld_32x32b_x16(lane_base + col, v);
 #pragma unroll 1
-                        for (int j = 1; j < cpc; ++j) {
+                            for (int j = 1; j < cpc; ++j) {
+                                uint32_t w[16];
+                                if (k_lo + j * args.chunk_len < k_hi) {
+                                    ptx::tmem_ld_32x32b_x16(lane_base + static_cast<uint32_t>(j * BN) + col, w);
+                                } else {
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) w[i] = 0u;
+                                }
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(w[i]));
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] = 0u;
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            ptx::st_shared_v4(row_addr + (static_cast<uint32_t>((hh * 4 + q) ^ (lane & 7)) << 4),
+                                              v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    }
+                } else {
+                    // whole_k: each split's chunk sum as above (stored as the
+                    // split's partials where they are kept), then the splits
+                    // in split order, the owner's sums.
+                    const int sps = cpc / C;                  // splits the CTA covers
+                    const int cps = C;                        // their chunks
+                    const int prow = quarter * 32 + lane;     // this thread's tile row
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t v[16];
+                        const uint32_t col = static_cast<uint32_t>(jb * 32 + hh * 16);
+#pragma unroll 1
+                        for (int sp = 0; sp < sps; ++sp) {
                             uint32_t w[16];
-                            if (k_lo + j * args.chunk_len < k_hi) {
-                                ptx::tmem_ld_32x32b_x16(lane_base + static_cast<uint32_t>(j * BN) + col, w);
+#pragma unroll 1
+                            for (int j = 0; j < cps; ++j) {
+                                const int a = sp * cps + j;
+                                uint32_t x[16];
+                                if (have_acc && k_lo + a * args.chunk_len < k_hi) {
+                                    ptx::tmem_ld_32x32b_x16(lane_base + static_cast<uint32_t>(a * BN) + col, x);
+                                } else {
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) x[i] = 0u;
+                                }
+                                if (j == 0) {
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) w[i] = x[i];
+                                } else {
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i)
+                                        w[i] = __float_as_uint(__uint_as_float(w[i]) + __uint_as_float(x[i]));
+                                }
+                            }
+                            if (P != nullptr && prow < args.M - m_tile * TM) {
+                                float *dst = P + static_cast<size_t>(s + sp) * args.M * args.N +
+                                             static_cast<size_t>(m_tile * TM + prow) * args.N + n_tile * BN + col;
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    *reinterpret_cast<float4 *>(dst + 4 * q) =
+                                        make_float4(__uint_as_float(w[4 * q]), __uint_as_float(w[4 * q + 1]),
+                                                    __uint_as_float(w[4 * q + 2]), __uint_as_float(w[4 * q + 3]));
+                            }
+                            if (sp == 0) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) v[i] = w[i];
                             } else {
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) w[i] = 0u;
+                                for (int i = 0; i < 16; ++i)
+                                    v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(w[i]));
                             }
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(w[i]));
                         }
-                    } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = 0u;
+                        for (int q = 0; q < 4; ++q)
+                            ptx::st_shared_v4(row_addr + (static_cast<uint32_t>((hh * 4 + q) ^ (lane & 7)) << 4),
+                                              v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                     }
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        ptx::st_shared_v4(row_addr + (static_cast<uint32_t>((hh * 4 + q) ^ (lane & 7)) << 4),
-                                          v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
             }
         }
@@ -732,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
                 if (p0.row < rows_here) *reinterpret_cast<float4 *>(Ps + tile_elem(p0)) = a0;
                 if (g1 < my_hi && p1.row < rows_here) *reinterpret_cast<float4 *>(Ps + tile_elem(p1)) = a1;
             }
-        } else if (P != nullptr) {
+        } else if (P != nullptr && !whole_k) {   // (whole_k: the partials were stored while staging)
             cluster_split_sum_for<Q, true>(CC, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, P, out);
         } else {
             cluster_split_sum_for<Q, false>(CC, rbase, my_lo + tid, my_hi, rows_here, tile0, args.N, MN, nullptr,
@@ -917,7 +983,8 @@ constexpr size_t kCompact3SmemLimit = 74 * 1024;
 constexpr size_t kTmem256Smem = 100 * 1024;
 bool tmem_fits(int cols, size_t smem)
 {
-    return static_cast<size_t>(cols) * 512 <= smem || (cols == 256 && smem >= kTmem256Smem);
+    return static_cast<size_t>(cols) * 512 <= smem || (cols == 256 && smem >= kTmem256Smem) ||
+           (cols == 512 && smem >= kSmemLimit);   // all of a block's shared memory: alone on its SM
 }
 
 // Dynamic shared memory of a plan: the stage ring (or the accumulator
@@ -1113,19 +1180,20 @@ double estimate_tc_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, b
 
 namespace {
 
-TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3, bool compact);
+TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3, bool compact,
+                          bool whole_ok);
 
 // The plan depends only on the problem's shape, the element width, `fused`,
 // the layout asked for and the tile override, so each host thread keeps the
 // last kPlanCache plans.
 struct PlanKey {
     int64_t M, N, K, S, kps;
-    bool fused, x3, compact;
+    bool fused, x3, compact, whole_ok;
     int ov_bn, ov_chunks, ov_kbs;
     bool operator==(const PlanKey &o) const
     {
         return M == o.M && N == o.N && K == o.K && S == o.S && kps == o.kps && fused == o.fused && x3 == o.x3 &&
-               compact == o.compact && ov_bn == o.ov_bn && ov_chunks == o.ov_chunks && ov_kbs == o.ov_kbs;
+               compact == o.compact && whole_ok == o.whole_ok && ov_bn == o.ov_bn && ov_chunks == o.ov_chunks && ov_kbs == o.ov_kbs;
     }
 };
 constexpr int kPlanCache = 8;
@@ -1139,12 +1207,14 @@ thread_local int t_plan_next = 0;
 
 }  // namespace
 
-TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3, bool compact)
+TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3, bool compact,
+                 bool whole_ok)
 {
-    const PlanKey key{M, N, K, S, kps, fused, x3, compact, g_override_bn, g_override_chunks, g_override_kbs};
+    whole_ok = whole_ok && compact;
+    const PlanKey key{M, N, K, S, kps, fused, x3, compact, whole_ok, g_override_bn, g_override_chunks, g_override_kbs};
     for (const PlanEntry &e : t_plans)
         if (e.valid && e.key == key) return e.plan;
-    const TilePlan p = plan_tc_uncached(M, N, K, S, kps, fused, x3, compact);
+    const TilePlan p = plan_tc_uncached(M, N, K, S, kps, fused, x3, compact, whole_ok);
     t_plans[t_plan_next] = PlanEntry{key, p, true};
     t_plan_next = (t_plan_next + 1) % kPlanCache;
     return p;
@@ -1152,7 +1222,8 @@ TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool f
 
 namespace {
 
-TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3, bool compact)
+TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3, bool compact,
+                          bool whole_ok)
 {
     // Stages of several k-blocks load as one 3-D box per operand, which the
     // TMA unit moves much faster than the same bytes in 16 KB boxes; that needs
@@ -1359,11 +1430,56 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     // per SM): a third less shared-memory traffic per product, half the CTAs.
     // The headline shape went from 3.23 to 2.48 us per operation in graphs of
     // eight calls grouped into one launch.
+    //
+    // Whole K in a CTA: where the splits are full and their chunks tile them,
+    // a fused plan for a launch that follows another may give one CTA every
+    // chunk of every split (S x chunks accumulators of 128 columns, at most
+    // 512 in all): no cluster and no exchange, the CTA adds its chunks and
+    // splits in the owners' order, one CTA per SM with all of its shared
+    // memory for the ring.  Only where the compact plan would take more than
+    // half the SMs (or there is none): with fewer CTAs a graph of such calls
+    // keeps two launches' CTAs on the SMs and ran faster with the compact
+    // plan.  On GB300, graphs of eight calls went from 5.19 to 4.63 us per
+    // call (M128 N2048 K4096 S4), 15.4 to 11.5 (M256 N2048 K8192 S4), 9.78
+    // to 6.48 (M512 N1024 K4096 S2) and 11.6 to 8.15 (M128 N4096 K4096 S2);
+    // M256 N512 K4096 S4 (64 compact CTAs) went from 3.09 to 3.60 and the
+    // M256 N1024 K2048 S2 headline (32) from 2.51 to 2.72.  A call heading a
+    // graph keeps the compact plan: alone, its few whole-K CTAs ran up to
+    // twice as long (M128 N2048 K4096 S4: 28.6 against 14.9 us).
+    const auto try_whole_k = [&](int cbn) {
+        const int units = static_cast<int>(S) * chunks;
+        const int cols = cbn * units;
+        const int64_t cctas = row_tiles * (N / cbn);
+        if (N % cbn || cols > 512 || (cols & (cols - 1)) || cctas > resident_clusters(1)) return false;
+        const int cnkb = nkb * units;
+        StageChoice cc = pick_stages(cbn, cnkb, can3d, 1, share_for(cbn, 1), x3, tm, kSmemLimit, false);
+        if (!cc.ok || cc.stages < std::min(2, (cnkb + cc.kbs - 1) / cc.kbs) || nkb % cc.kbs != 0) return false;
+        p.compact = 1;
+        p.bn = cbn;
+        p.cpc = units;
+        p.cluster = 1;
+        p.share = share_for(cbn, 1);
+        p.recv_in_ring = 0;
+        p.stages = cc.stages;
+        p.kbs = can3d ? cc.kbs : 1;
+        p.three_d = can3d && p.kbs > 1 ? 1 : 0;
+        p.region0 = static_cast<uint32_t>(
+            round_up(std::max(cc.stages * stage_bytes(cbn, p.kbs, x3, tm), epi_bytes(cbn)), 1024));
+        p.smem_bytes = kSmemLimit;   // alone on its SM: its accumulators may take all 512 columns
+        p.grid = dim3(static_cast<unsigned>(N / cbn), static_cast<unsigned>(row_tiles), 1);
+        p.rows_first = 0;
+        p.prefetchers = 0;
+        return true;
+    };
     if (compact && tm == kTileM && bn <= 128) {
         const bool mergeable = !x3 && split_sum == 2 && chunks > 1 && can3d && chunk_len % kBlockK == 0;
+        const bool whole = whole_ok && !x3 && split_sum == 2 && S > 1 && can3d && chunk_len % kBlockK == 0 &&
+                           K == S * kps && kps == static_cast<int64_t>(chunks) * chunk_len;
         if (!(mergeable && chunks == 2 && bn == 64 && try_compact(2, 128)) &&
             !(mergeable && bn * chunks <= 128 && try_compact(chunks, bn)))
             try_compact(1, bn);
+        const int64_t compact_ctas = p.compact ? static_cast<int64_t>(p.grid.x) * p.grid.y * p.grid.z : 0;
+        if (whole && (!p.compact || compact_ctas > resident_clusters(1) / 2)) try_whole_k(128);
     }
     return p;
 }
@@ -1443,9 +1559,13 @@ cudaError_t check_plan(const GemmProblem &pr, const TilePlan &plan)
                            (plan.cluster * plan.cpc) % plan.chunks == 0;
     // several chunks per CTA: each its own accumulator (at most 128 tensor-
     // memory columns in all), its chunks whole k-blocks of whole stages
+    // (or every chunk of every split: full splits that the chunks tile, no cluster)
+    const bool whole_k = plan.cpc > plan.chunks;
     const bool cpc_ok = plan.cpc == 1 ||
-                        (plan.cpc == 2 && plan.cpc == plan.chunks && !plan.x3 && plan.tile_m == kTileM &&
-                         tmem_fits(plan.bn * plan.cpc, plan.smem_bytes) &&
+                        ((plan.cpc == plan.chunks || (whole_k && plan.cpc == pr.S * plan.chunks && plan.cluster == 1 &&
+                                                      pr.K == pr.S * pr.kps &&
+                                                      pr.kps == static_cast<int64_t>(plan.chunks) * plan.chunk_len)) &&
+                         !plan.x3 && plan.tile_m == kTileM && tmem_fits(plan.bn * plan.cpc, plan.smem_bytes) &&
                          plan.chunk_len % kBlockK == 0 && (plan.chunk_len / kBlockK) % plan.kbs == 0 &&
                          static_cast<int64_t>(plan.grid.z) * plan.cpc == pr.S * plan.chunks);
     if (!cpc_ok) return note_error(cudaErrorInvalidConfiguration, "chunks per CTA out of range");

@@ -6,8 +6,9 @@ launch that can still be running writes what the new one reads (overlap 1);
 it also stores before that grid ends only where none of them reads or
 writes what the new one writes (overlap 2), and every launch still waits for
 the previous grid before it finishes.  A fused launch that overlaps may give
-each thread block all the chunks of its split (chunks_per_block > 1), with
-the same sums.  Each test captures a sequence of calls, checks which launches
+each thread block all the chunks of its split (chunks_per_block > 1), or
+where the splits are full, after the first call, every chunk of every split
+(no cluster), with the same sums.  Each test captures a sequence of calls, checks which launches
 overlapped (splitk_last_launch, read right after each call), replays the
 graph several times and compares every output bitwise with the same calls
 made eagerly, where each launch waits for the one before it.  The eager results themselves are pinned to the
@@ -590,4 +591,49 @@ def test_grouped_kn_bitwise(grouping):
     torch.cuda.synchronize()
     for it in insts:
         assert bitwise(it["out"], it["ref"])
+    assert sk.splitk_get_device_status() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    (128, 2048, 4096, 4, 1024),   # 16 whole-K blocks a call, one chunk per split
+    (512, 1024, 4096, 2, 2048),   # 32 a call, two chunks per split
+])
+@pytest.mark.parametrize("fused", [1, 3])
+def test_whole_k_calls_bitwise(grouping, shape, fused):
+    """Full splits whose compact plan takes more than half the SMs: the first
+    call of the capture keeps the compact plan (a cluster of the splits), the
+    calls after it take whole-K blocks (every chunk of every split in one
+    block, no cluster) and group among themselves.  Every output, and the
+    partials a call keeps, is the eager one, bit for bit."""
+    sk = grouping
+    M, N, K, S, kps = shape
+    dt = "bf16"
+    insts = instances(sk, M, N, K, S, kps, dt, 12)
+    for it in insts:
+        sk.gemm_bt(it["A"], it["B"], it["ref"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=fused)
+    torch.cuda.synchronize()
+    refs_ws = [it["ws"].clone() for it in insts]
+    C = sk.splitk_describe_launch(M, N, K, S, kps, dt, fused=fused)["chunks"]
+    seen = []
+
+    def body():
+        for it in insts:
+            sk.gemm_bt(it["A"], it["B"], it["out"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=fused)
+            seen.append(sk.splitk_last_launch())
+
+    g = capture(body)
+    assert seen[0]["chunks_per_block"] <= C and seen[0]["cluster"] > 1, seen[0]
+    assert all(d["chunks_per_block"] == S * C and d["cluster"] == 1 and d["bn"] == 128 for d in seen[1:]), seen
+    assert [d["group"] for d in seen] == [1, 1, 2, 3, 4, 5, 6, 7, 8, 1, 2, 3], seen
+    for _ in range(3):
+        for it in insts:
+            it["out"].fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        for it in insts:
+            assert bitwise(it["out"], it["ref"])
+    if fused == 3:
+        for it, w in zip(insts, refs_ws):
+            P = S * M * N
+            assert bitwise(it["ws"][:P], w[:P])
     assert sk.splitk_get_device_status() == 0

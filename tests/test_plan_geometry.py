@@ -54,8 +54,9 @@ def lib():
 
 def tmem_fits(cols, smem):
     """The tensor-memory rule of the planner: one column per 512 bytes of
-    shared memory, or 256 columns from 100 KB on."""
-    return cols * 512 <= smem or (cols == 256 and smem >= TMEM256_SMEM)
+    shared memory, 256 columns from 100 KB on, or all 512 for a block that
+    takes the whole per-block limit (alone on its SM)."""
+    return cols * 512 <= smem or (cols == 256 and smem >= TMEM256_SMEM) or (cols == 512 and smem >= SMEM_LIMIT)
 
 
 def test_tmem_rule_never_oversubscribes():
@@ -69,7 +70,8 @@ def test_tmem_rule_never_oversubscribes():
     import functools
 
     per_sm = SM_SMEM
-    kinds = [(512, SMEM_LIMIT + 1024 + STATIC_SMEM)]   # 256-row tiles take all of a block's shared memory
+    # 256-row tiles and whole-K blocks take all of a block's shared memory
+    kinds = [(512, SMEM_LIMIT + 1024 + STATIC_SMEM)]
     for cols in (64, 128, 256):
         smem = min(s for s in range(1024, SMEM_LIMIT + 1, 1024) if tmem_fits(cols, s) and s >= cols * 256)
         kinds.append((cols, smem + 1024 + STATIC_SMEM))
@@ -162,6 +164,37 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
 
     # the compact layout: same tiles and sums, a ring two blocks to an SM,
     # the receive slots inside it after the staging area
+    # whole K in a block (a call that follows another): full splits that the
+    # chunks tile, every chunk of every split in its own 128-column
+    # accumulator (at most 512 columns), no cluster, one block per SM with
+    # all of its shared memory; taken where the compact plan would take more
+    # than half the SMs, or there is none
+    can3d = K % kb_elems == 0 and kps % kb_elems == 0
+    whole = not x3 and SS == 2 and S > 1 and can3d and CL % 64 == 0 and K == S * kps and kps == C * CL
+    wcols = 128 * S * C
+    wctas = -(-M // TM) * (N // 128)
+    nkb = -(-CL // kb_elems)
+    kfix = kbs and min(kbs, 4)                            # an overridden stage depth
+    ring_ok = not kfix or (nkb % kfix == 0 and
+                           min(2, -(-nkb * S * C // kfix)) * (TM + 128) * 128 * kfix + 1024 <= SMEM_LIMIT)
+    whole_fits = whole and TM == TILE_M and BN <= 128 and N % 128 == 0 and wcols <= 512 and wctas <= 148 and ring_ok
+    if d["compact"] and d["compact_chunks_per_block"] > C:
+        cst, ckbs, csmem = d["compact_stages"], d["compact_kblocks_per_stage"], d["compact_smem_bytes"]
+        cpc, qc, CB = d["compact_chunks_per_block"], d["compact_cluster"], d["compact_bn"]
+        assert whole_fits and CB == 128 and cpc == S * C and qc == 1 and d["compact_grid_z"] == 1
+        assert wcols & (wcols - 1) == 0
+        assert nkb % ckbs == 0 and cst >= min(2, -(-nkb * cpc // ckbs))
+        assert csmem == SMEM_LIMIT and tmem_fits(wcols, csmem)
+        assert cst * (TM + 128) * 128 * ckbs + 1024 <= SMEM_LIMIT and TILE_M * 128 * 4 + 1024 <= SMEM_LIMIT
+        assert SMEM_LIMIT + 1024 + STATIC_SMEM + 1024 + 1024 > SM_SMEM   # nothing else fits beside it
+        # one block covers all of K: the splits' chunks back to back, each
+        # in its own accumulator, the first k-block of each starting a stage
+        check_k_coverage(K, 1, K, S * C, CL, ckbs, int(ckbs > 1), kb_elems, elem, S * C)
+        return
+    if whole_fits:   # not taken: the compact plan keeps to half the SMs
+        assert d["compact"], (M, N, K, S, kps, BN, C)
+        assert -(-M // TM) * (N // d["compact_bn"]) * d["compact_grid_z"] <= 74, (M, N, K, S, kps, BN, C)
+
     if d["compact"]:
         assert TM == TILE_M and BN <= 128
         cst, ckbs, csmem = d["compact_stages"], d["compact_kblocks_per_stage"], d["compact_smem_bytes"]
@@ -170,7 +203,6 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
         # every chunk of a split in one block: only where the chunks are whole
         # stages of whole k-blocks; 128-column tiles (from 64) only so, with
         # two chunks
-        can3d = K % kb_elems == 0 and kps % kb_elems == 0
         mergeable = not x3 and SS == 2 and C > 1 and can3d and CL % 64 == 0
         assert CB == BN or (CB == 128 and BN == 64 and C == 2 and cpc == 2 and mergeable), (BN, CB, cpc)
         assert cpc in (1, C) and (cpc == 1 or (mergeable and CB * C <= 256))
@@ -291,6 +323,8 @@ CASES = [(32, 64, 128, 2, 64), (96, 512, 2048, 4, 512), (256, 512, 2048, 4, 512)
          (64, 128, 160, 3, 64), (32, 64, 32, 1, 32), (160, 192, 320, 3, 128), (96, 320, 1024, 2, 512),
          (64, 128, 8192, 4, 2048), (512, 2048, 4096, 4, 1024), (288, 256, 96, 3, 32)]
 CASES += [(32, 512, 2048, s, 2048 // s) for s in (1, 2, 4, 8, 16)] + [(96, 512, 512, s, 512 // s) for s in (1, 2, 4, 8, 16)]
+# whole-K blocks where the compact plan is larger than half the SMs
+CASES += [(128, 2048, 4096, 4, 1024), (512, 1024, 4096, 2, 2048), (256, 2048, 8192, 4, 2048)]
 OVERRIDES = [(0, 0, 0)] + list(itertools.product((64, 128, 256), (1, 2, 4, 8), (0, 1, 2, 4)))
 
 
@@ -310,6 +344,30 @@ def test_plan_geometry_random_and_large(lib):
         for fused in (0, 1):
             for ov in OVERRIDES:
                 check_plan(lib, *c[:5], fused, c[5], *ov)
+
+
+@pytest.mark.parametrize("shape,whole", [
+    ((256, 1024, 2048, 2, 1024), False),   # 32 compact blocks: keeps two launches on the SMs
+    ((256, 512, 4096, 4, 1024), False),    # 64
+    ((256, 1024, 4096, 2, 2048), False),   # 32
+    ((128, 2048, 4096, 4, 1024), True),    # 128 compact blocks
+    ((256, 2048, 8192, 4, 2048), True),
+    ((512, 1024, 4096, 2, 2048), True),
+    ((128, 4096, 4096, 2, 2048), True),
+    ((128, 4096, 8192, 4, 2048), True),
+    ((256, 1024, 1536, 2, 1024), False),   # the last split short: not full splits
+    ((96, 512, 2048, 4, 512), False),      # 2 chunks x 4 splits: 1024 columns
+])
+def test_whole_k_choice(lib, shape, whole):
+    """Which fused BF16 calls that follow another in a capture get whole-K
+    blocks (the shapes the choice was measured on), with the same chunks as
+    the eager plan."""
+    d = lib.splitk_describe_launch(*shape, "bf16", fused=1)
+    M, N, K, S, kps = shape
+    assert d["fused_in_kernel"] == 1 and d["compact"] == 1
+    assert (d["compact_chunks_per_block"] == S * d["chunks"] and d["compact_cluster"] == 1) == whole, d
+    if whole:
+        assert d["compact_bn"] == 128 and d["compact_grid_z"] == 1
 
 
 def test_plan_follows_override_changes(lib):
