@@ -69,9 +69,10 @@ def code_of(text: str) -> str:
     return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
 
 
-def kernel_traffic():
+def kernel_traffic(ops_per_launch=1):
     """DRAM bytes per launch of the tensor-core kernel from the committed ncu
-    record, or None when the kernel's code changed since it was taken."""
+    record, or None when the kernel's code changed since it was taken or the
+    record's launches computed another number of operations."""
     import hashlib
 
     path = os.path.join(ROOT, "profiles", "tc_splitk_traffic.txt")
@@ -87,7 +88,7 @@ def kernel_traffic():
     for src in rec.get("sources", "").split():
         with open(os.path.join(ROOT, src)) as f:
             h.update(code_of(f.read()).encode())
-    if h.hexdigest() != rec.get("code_sha256"):
+    if h.hexdigest() != rec.get("code_sha256") or int(rec.get("ops_per_launch", 1)) != ops_per_launch:
         return None
     return int(rec["dram_bytes_per_launch"])
 
@@ -406,10 +407,12 @@ def time_graphs(torch, stream, graphs, steps):
 def measure_e2e(sk, torch, stream, groups, pack, fused, steps):
     """µs/op through gemm_bt_host_batch: per step one group's `pack`
     activations come from pinned host memory and its results go back to
-    pinned host memory, all inside the timed region (CUDA events on the
-    caller's stream, which the call joins).  Also times the same batches with
-    one copy each way (no overlap of copies and kernels) and the host's
-    enqueue time per call."""
+    pinned host memory, all inside the timed region.  Steps alternate two
+    staging buffers and two caller streams (each call joins its stream), so
+    that a step's kernels need not wait for the previous step's copy out;
+    the CUDA events bracket both streams.  Also times the same batches on one
+    stream with one copy each way (no overlap of copies and kernels) and the
+    host's enqueue time per call."""
     import time
 
     dev = groups[0][0]["A"].device
@@ -426,27 +429,30 @@ def measure_e2e(sk, torch, stream, groups, pack, fused, steps):
         sk.gemm_bt_workspace_init(st, sb, stream=stream)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n = max(3, min(steps, 200))
+    second = torch.cuda.Stream(device=dev)
 
-    def run(opc):
+    def run(opc, nstreams):
+        streams = [stream, second][:nstreams]
         host_s = 0.0
-        with torch.cuda.stream(stream):
-            for k in range(3):
-                a, o, b = hosts[k % len(hosts)]
-                sk.gemm_bt_host_batch(a, b, o, pack, stagings[k % 2], sb, M, N, K, SPLITS, KPS, DTYPE,
-                                      fused=fused, ops_per_copy=opc, stream=stream)
-            torch.cuda.synchronize()
-            start.record(stream)
-            for k in range(n):
-                a, o, b = hosts[k % len(hosts)]
-                t0 = time.perf_counter()
-                sk.gemm_bt_host_batch(a, b, o, pack, stagings[k % 2], sb, M, N, K, SPLITS, KPS, DTYPE,
-                                      fused=fused, ops_per_copy=opc, stream=stream)
-                host_s += time.perf_counter() - t0
-            stop.record(stream)
+        for k in range(3):
+            a, o, b = hosts[k % len(hosts)]
+            sk.gemm_bt_host_batch(a, b, o, pack, stagings[k % 2], sb, M, N, K, SPLITS, KPS, DTYPE,
+                                  fused=fused, ops_per_copy=opc, stream=streams[k % nstreams])
+        torch.cuda.synchronize()
+        start.record(stream)
+        second.wait_event(start)
+        for k in range(n):
+            a, o, b = hosts[k % len(hosts)]
+            t0 = time.perf_counter()
+            sk.gemm_bt_host_batch(a, b, o, pack, stagings[k % 2], sb, M, N, K, SPLITS, KPS, DTYPE,
+                                  fused=fused, ops_per_copy=opc, stream=streams[k % nstreams])
+            host_s += time.perf_counter() - t0
+        stream.wait_stream(second)
+        stop.record(stream)
         stop.synchronize()
         return start.elapsed_time(stop) * 1e3 / (n * pack), host_s * 1e6 / n
 
-    us, host_us = run(0)
+    us, host_us = run(0, 2)
     # the step just timed ended on group (n-1) % len(groups): its host results
     # must equal the resident-operand outputs of the same operations
     last = (n - 1) % len(groups)
@@ -454,16 +460,19 @@ def measure_e2e(sk, torch, stream, groups, pack, fused, steps):
         got = hosts[last][1][i * M * N:(i + 1) * M * N].view(M, N)
         if not torch.equal(got, inst["out"].cpu()):
             raise RuntimeError("host-buffer results differ from the resident-operand outputs")
-    serial_us, _ = run(pack)
+    one_stream_us, _ = run(0, 1)
+    serial_us, _ = run(pack, 1)
     if sk.splitk_get_device_status(stream) != 0:
         raise RuntimeError("a kernel's bounded wait ran out during the end-to-end run")
     return {"value": round(us, 4), "unit": "µs/op", "h2d_bytes_per_step": pack * M * K * 2,
             "d2h_bytes_per_step": pack * M * N * 4,
             "how": f"gemm_bt_host_batch per step: {pack} activations copied in from pinned host memory and "
                    "results copied out to pinned host memory on two copy streams, pipelined against the "
-                   "kernels, two staging buffers alternated so that a step's copy in overlaps the previous "
-                   f"step's kernels; weights resident; CUDA events on the caller's stream over {n} steps",
-            "unpipelined": "the same with one copy each way for the whole step (no overlap of copies and kernels)",
+                   "kernels (the operations of a copy group in one launch), two staging buffers and two "
+                   "caller streams alternated so that a step's copy in and its kernels overlap the previous "
+                   f"step's copy out; weights resident; CUDA events around both streams over {n} steps",
+            "one_stream_us": round(one_stream_us, 4),
+            "unpipelined": "one stream, one copy each way for the whole step (no overlap of copies and kernels)",
             "unpipelined_us": round(serial_us, 4), "host_enqueue_us_per_step": round(host_us, 2)}
 
 
@@ -497,6 +506,9 @@ def run_ours(args, rank, world, dev, torch, dist):
 
     torch.cuda.synchronize()
     graphs = [capture(torch, stream, lambda grp=grp: [op(i) for i in grp]) for grp in groups]
+    # the operations the last captured launch computes: a step's calls join
+    # one launch where they can (group), so a launch is a whole step
+    ops_per_launch = sk.splitk_last_launch()["group"]
 
     # sanity before timing: the fused and two-kernel paths agree bitwise
     inst = pool[0]
@@ -562,7 +574,8 @@ def run_ours(args, rank, world, dev, torch, dist):
     time_graphs(torch, stream, two_pass_graphs, 5)
     two_pass_us = time_graphs(torch, stream, two_pass_graphs, reps) * 1e3 / (reps * pack)
     if fused:
-        dom_name, dom_us, dom_bytes = "tc_splitk_kernel (fused: partials + split sum)", us_per_op * world, BYTES_FUSED
+        dom_name = f"tc_splitk_kernel (fused: partials + split sum; {ops_per_launch} operations per launch)"
+        dom_us, dom_bytes = us_per_op * world * ops_per_launch, BYTES_FUSED * ops_per_launch
     else:
         dom_name, dom_us, dom_bytes = "tc_splitk_kernel (partial pass)", gemm_us, BYTES_GEMM
 
@@ -661,7 +674,8 @@ def run_ours(args, rank, world, dev, torch, dist):
         "roofline": {"bound": roof["bound_min"] if fused else roof["bound_2pass"], "kernel": dom_name,
                      "t_flop_us": roof["t_flop_us"], "achieved": round(achieved, 1),
                      "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "traffic": kernel_traffic() if fused else None, "bytes_per_launch": dom_bytes,
+                     "traffic": kernel_traffic(ops_per_launch) if fused else None, "bytes_per_launch": dom_bytes,
+                     "ops_per_launch": ops_per_launch if fused else 1,
                      "launch_us": round(dom_us, 4), "peak_kind": peak_kind},
         "sampling": {"median_of_9_rounds_x_40_replays_us": round(statistics.median(round_us), 4),
                      "rounds_min_max_us": [round(min(round_us), 4), round(max(round_us), 4)],

@@ -253,8 +253,11 @@ size_t gemm_bt_host_staging_bytes(int64_t count, int64_t M, int64_t N,
  *              overlapping no B
  *   fused      as for gemm_bt (0, 1 or 3)
  *   ops_per_copy  operations moved by one copy each way; 0 lets the library
- *              choose (at least 2 MiB of A per copy, at most half the batch)
- * Every operation is bitwise the gemm_bt result for its operands.  The copy
+ *              choose (at least 4 MiB of A per copy, at most half the batch)
+ * Every operation is bitwise the gemm_bt result for its operands.  With
+ * fused = 1, 16-bit operands and a shape whose splits are summed inside the
+ * launch, the operations of a group run as one launch (up to 8 of them; the
+ * same tiles and sums as one call each); otherwise one gemm_bt each.  The copy
  * in of group g+1 and the copy out of group g-1 run on two library streams
  * while group g computes on `stream`, and `stream` waits for the last copy
  * out, so synchronising `stream` completes the batch.  Host buffers must stay
@@ -262,9 +265,12 @@ size_t gemm_bt_host_staging_bytes(int64_t count, int64_t M, int64_t N,
  * the same staging (the library keeps one event per staging buffer, for the
  * 32 most recently used), or, for a staging it has not seen, for the work
  * already on `stream`: calls that alternate two staging buffers overlap one
- * batch's copy in with the previous batch's kernels.  Between calls the
+ * batch's copy in with the previous batch's kernels.  On one stream a call's
+ * kernels still follow the previous call's copy out (stream order); calls
+ * that alternate two streams as well also overlap that copy out with the
+ * next batch's kernels.  Between calls the
  * staging belongs to them: other work must not write it, and one staging is
- * used with one stream (its workspace part is used in stream order). 
+ * used with one stream (its workspace part is used in stream order).
  * The first call on a device creates those two streams and four events (kept
  * until exit); a process-wide mutex serialises the enqueueing of concurrent
  * calls.  Returns as gemm_bt's validation would (plus SPLITK_ERR_CONFIG for

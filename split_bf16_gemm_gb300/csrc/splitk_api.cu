@@ -146,6 +146,36 @@ int run_partial_pass(const void *A, const void *B, float *P, float *out, int64_t
     return cuda_status(err);
 }
 
+}  // namespace
+
+namespace splitk {
+
+bool batch_possible(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps)
+{
+    const TilePlan plan = plan_tc(M, N, K, S, kps, true, false, true);
+    return plan.compact && plan.split_sum == 2 && !plan.x3 && plan.tile_m == kTileM && plan.bn <= 128 &&
+           !plan.rows_first;
+}
+
+int run_fused_batch(const void *const *A, const void *const *B, float *const *out, int n, int64_t M, int64_t N,
+                    int64_t K, int64_t S, int64_t kps, int dtype, cudaStream_t stream)
+{
+    if (n < 1 || n > kMaxGroup || dtype == SPLITK_F32 || !fused_in_kernel(M, N, K, S, kps, dtype, false))
+        return SPLITK_ERR_CONFIG;
+    if (!batch_possible(M, N, K, S, kps)) return SPLITK_ERR_CONFIG;
+    const TilePlan plan = plan_tc(M, N, K, S, kps, true, false, true);
+    GemmProblem prs[kMaxGroup];
+    for (int i = 0; i < n; ++i) prs[i] = GemmProblem{A[i], B[i], nullptr, out[i], M, N, K, S, kps, dtype == SPLITK_BF16};
+    const cudaError_t err = launch_tc_batch(prs, n, plan, stream);
+    note_launch({0, plan.compact, 0, plan.bn, plan.chunks, plan.stages, plan.kbs, static_cast<int>(plan.smem_bytes),
+                 plan.cpc, plan.cluster, n});
+    return err == cudaSuccess ? SPLITK_OK : (note_error(err, "batched launch"), SPLITK_ERR_CUDA);
+}
+
+}  // namespace splitk
+
+namespace {
+
 // The accumulation pass.  After the partial pass it reads what that pass
 // wrote, so it waits for it; a reduce whose partials no running launch
 // writes (inside a capture) loads them at once.  It lets the next launch

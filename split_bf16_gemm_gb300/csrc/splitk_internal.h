@@ -86,6 +86,10 @@ cudaError_t launch_tc_grouped(const GemmProblem &p, const TilePlan &plan, cudaSt
 // whether it did (and the launch's problem count in *group_size).
 bool join_group(const GemmProblem &p, const TilePlan &plan, unsigned long long capture, cudaGraphNode_t dep,
                 int *group_size, int *mode);
+// One launch computing n (1..kMaxGroup) independent problems of one shape
+// with the plan (compact, groupable), outside a capture: the grouped kernel
+// with every problem given at once.
+cudaError_t launch_tc_batch(const GemmProblem *p, int n, const TilePlan &plan, cudaStream_t stream);
 cudaError_t launch_simt_f32(const float *A, const float *B, float *P, int64_t M, int64_t N, int64_t K,
                             int64_t S, int64_t kps, bool b_kn, cudaStream_t stream);
 // overlap: nothing that can still be running writes P (splitk_chain.cu);
@@ -158,6 +162,14 @@ LaunchRecord last_launch();
 // Whether gemm_bt(fused != 0) sums the splits inside its tensor-core launch
 // (else it runs the partial pass and the reduce); dtype as in splitk.h.
 bool fused_in_kernel(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, int dtype, bool b_kn);
+// n (1..kMaxGroup) fused calls (fused = 1, [N,K] weights) of one shape in one
+// launch, where the shape sums its splits inside the launch and its compact
+// plan groups; returns SPLITK_ERR_CONFIG, launching nothing, where it does not.
+// Arguments as gemm_bt's, already validated, outputs distinct.
+int run_fused_batch(const void *const *A, const void *const *B, float *const *out, int n, int64_t M, int64_t N,
+                    int64_t K, int64_t S, int64_t kps, int dtype, cudaStream_t stream);
+// Whether the 16-bit fused plan of the shape allows such a launch.
+bool batch_possible(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps);
 
 // gemm_bt's argument checks (status as gemm_bt returns it; nothing launched),
 

@@ -1752,6 +1752,31 @@ cudaError_t launch_tc_grouped(const GemmProblem &pr, const TilePlan &plan, cudaS
     return cudaSuccess;
 }
 
+cudaError_t launch_tc_batch(const GemmProblem *prs, int n, const TilePlan &plan, cudaStream_t stream)
+{
+    if (n < 1 || n > kMaxGroup || !groupable(prs[0], plan)) return cudaErrorInvalidValue;
+    TcOperands<kMaxGroup> ops = {};
+    for (int i = 0; i < n; ++i) {
+        const cudaError_t e = check_plan(prs[i], plan);
+        if (e != cudaSuccess) return e;
+        if (!encode_problem(prs[i], plan, &ops.tm[i][0], &ops.tm[i][1])) return cudaErrorInvalidValue;
+        set_problem(ops, i, prs[i], plan);
+    }
+    TcArgs a = make_args(prs[0], plan);
+    a.group = n;
+    a.prefetchers = 0;
+    TilePlan bp = plan;
+    bp.grid.y *= static_cast<unsigned>(n);   // blockIdx.y = problem * row tiles + row tile
+    bp.prefetchers = 0;
+    switch (plan.bn * 2 + (prs[0].b_kn ? 1 : 0)) {
+    case 64 * 2 + 0: return launch_grouped_bn<64, false>(ops, a, bp, stream);
+    case 64 * 2 + 1: return launch_grouped_bn<64, true>(ops, a, bp, stream);
+    case 128 * 2 + 0: return launch_grouped_bn<128, false>(ops, a, bp, stream);
+    case 128 * 2 + 1: return launch_grouped_bn<128, true>(ops, a, bp, stream);
+    default: return note_error(cudaErrorInvalidConfiguration, "tile width");
+    }
+}
+
 bool join_group(const GemmProblem &pr, const TilePlan &plan, unsigned long long capture, cudaGraphNode_t dep,
                 int *group_size, int *mode)
 {

@@ -451,6 +451,9 @@ def test_host_batch_matches_device_call_and_oracle(lib, case):
                                   fused=fused, ops_per_copy=opc, stream=stream)
             stream.synchronize()
             assert sk.splitk_get_device_status(stream) == 0
+            if fused == 1 and dt == "bf16" and (M, N) == (256, 1024):
+                # two operations per copy, each pair in one launch
+                assert sk.splitk_last_launch()["group"] == 2
             got = out_host.numpy()
             assert np.all(got[count * M * N:] == GUARD_VALUE)
             for i, c in enumerate(cs):
@@ -621,10 +624,13 @@ def test_kn_every_tiling(lib, orc, case):
     assert len(seen) > 4
 
 
-def test_host_batch_alternating_staging_in_flight(lib):
-    """Six batches on one stream over two alternating staging buffers, no
-    synchronisation until the end: each batch's copy in waits only for the
-    previous batch on the same staging, and every result is right."""
+@pytest.mark.parametrize("nstreams,opc", [(1, 1), (2, 0), (2, 4)])
+def test_host_batch_alternating_staging_in_flight(lib, nstreams, opc):
+    """Six batches over two alternating staging buffers, on one stream or two
+    alternating streams, no synchronisation until the end: each batch's copy
+    in waits only for the previous batch on the same staging, and every
+    result is right (with ops_per_copy 0 and 4 the operations of a copy
+    group run as one launch)."""
     sk = lib
     M, N, K, S, kps, dt, count, rounds = 128, 256, 1024, 2, 512, "bf16", 4, 6
     cs = [oracle_case(M, N, K, S, kps, dt, "uniform", 40 + i) for i in range(count)]
@@ -642,13 +648,16 @@ def test_host_batch_alternating_staging_in_flight(lib):
     order = [list(range(count)) if r % 2 == 0 else list(reversed(range(count))) for r in range(rounds)]
     hosts = [host_operand([cs[i][0].A for i in o], dt, True) for o in order]
     outs = [torch.zeros(count * M * N, dtype=torch.float32).pin_memory() for _ in range(rounds)]
-    stream = torch.cuda.Stream()
+    streams = [torch.cuda.Stream() for _ in range(nstreams)]
     for r in range(rounds):
         bp = sk.pointer_array([Bs[i] for i in order[r]])
         sk.gemm_bt_host_batch(hosts[r], bp, outs[r], count, stagings[r % 2], sb, M, N, K, S, kps, dt,
-                              fused=1, ops_per_copy=1, stream=stream)
-    stream.synchronize()
-    assert sk.splitk_get_device_status(stream) == 0
+                              fused=1, ops_per_copy=opc, stream=streams[r % nstreams])
+        if opc == 4:
+            assert sk.splitk_last_launch()["group"] == 4
+    for st in streams:
+        st.synchronize()
+    assert sk.splitk_get_device_status(streams[0]) == 0
     for r in range(rounds):
         got = outs[r].numpy()
         for j, i in enumerate(order[r]):
