@@ -57,11 +57,14 @@
  * writes what the new launch writes either, it also stores at once and
  * waits only before it finishes, so the grids still finish in launch order.
  * Such a fused launch may also give each thread block all the chunks of its
- * split, each in its own accumulator, added in chunk order inside the block.
+ * split, each in its own accumulator, added in chunk order inside the block,
+ * or, for large shapes with full splits, every chunk of every split.
  * A call that may store early and has the same shape and plan as the launch
  * before it joins that launch instead of adding one: the launch's graph
  * node then computes both calls (up to 8), whose blocks may run in any
- * order.  Its results are bitwise those of the same launch without overlap.
+ * order; the first such call after a run's first launch may also switch
+ * that launch to its own (whole-K) plan.  Its results are bitwise those of
+ * the same launch without overlap.
  * Launches that read what an
  * earlier one writes (a chain of GEMMs, the reduce after the partial pass),
  * launches after another kernel or a copy, and launches outside a capture
@@ -380,8 +383,9 @@ int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
  *  compact_bn (the compact plan's tile width, which may be wider than bn:
  *  the products of an output element do not depend on it)
  *  (0 when compact is 0).  The compact fields describe a call that starts
- *  beside the launch before it; the first call of a capture takes the
- *  compact layout without whole-K blocks}; `info` must hold 26 ints.
+ *  beside the launch before it; the first call of a run launches without
+ *  whole-K blocks, and the next call that takes them converts that launch
+ *  and joins it}; `info` must hold 26 ints.
  * Returns a status as gemm_bt's validation would (pointers are not checked). */
 int splitk_describe_launch(int64_t M, int64_t N, int64_t K, int64_t splits,
                            int64_t k_per_split, int dtype, int fused,

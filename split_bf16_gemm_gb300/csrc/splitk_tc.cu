@@ -1439,13 +1439,15 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     // memory for the ring.  Only where the compact plan would take more than
     // half the SMs (or there is none): with fewer CTAs a graph of such calls
     // keeps two launches' CTAs on the SMs and ran faster with the compact
-    // plan.  On GB300, graphs of eight calls went from 5.19 to 4.63 us per
-    // call (M128 N2048 K4096 S4), 15.4 to 11.5 (M256 N2048 K8192 S4), 9.78
-    // to 6.48 (M512 N1024 K4096 S2) and 11.6 to 8.15 (M128 N4096 K4096 S2);
-    // M256 N512 K4096 S4 (64 compact CTAs) went from 3.09 to 3.60 and the
-    // M256 N1024 K2048 S2 headline (32) from 2.51 to 2.72.  A call heading a
-    // graph keeps the compact plan: alone, its few whole-K CTAs ran up to
-    // twice as long (M128 N2048 K4096 S4: 28.6 against 14.9 us).
+    // plan.  A call heading a run launches with its usual plan (alone, its
+    // few whole-K CTAs ran up to twice as long: M128 N2048 K4096 S4, 28.6
+    // against 14.9 us), and the first call after it converts that launch to
+    // whole-K blocks (convert_head).  On GB300, graphs of eight calls went
+    // from 5.19 to 4.64 us per call (M128 N2048 K4096 S4), 15.4 to 11.5
+    // (M256 N2048 K8192 S4), 9.78 to 6.55 (M512 N1024 K4096 S2) and 11.5 to
+    // 8.16 (M128 N4096 K4096 S2); with whole-K blocks M256 N512 K4096 S4 (64
+    // compact CTAs) went from 3.09 to 3.60 and the M256 N1024 K2048 S2
+    // headline (32) from 2.51 to 2.72, so those keep the compact plan.
     const auto try_whole_k = [&](int cbn) {
         const int units = static_cast<int>(S) * chunks;
         const int cols = cbn * units;
@@ -1645,6 +1647,7 @@ struct GroupState {
     TcOperands<kMaxGroup> ops = {};
     TcArgs args = {};
     int n = 0;
+    GemmProblem head = {};   // the first problem, as launched
 };
 
 constexpr int kGroupSlots = 16;
@@ -1660,6 +1663,17 @@ bool same_plan(const TilePlan &a, const TilePlan &b)
            a.rows_first == b.rows_first && a.tile_m == b.tile_m && a.compact == b.compact &&
            a.recv_in_ring == b.recv_in_ring && a.cpc == b.cpc && a.grid.x == b.grid.x && a.grid.y == b.grid.y &&
            a.grid.z == b.grid.z && a.smem_bytes == b.smem_bytes;
+}
+
+// A launch heads a group with a compact plan, or with the fused plan of a
+// shape whose later calls may take whole-K blocks (full splits), if its
+// tiles are 128 rows by at most 128 columns in column order (the grouped
+// kernels' instances); later calls join it only with the same compact plan,
+// or convert it (convert_head).
+bool head_groupable(const GemmProblem &pr, const TilePlan &plan)
+{
+    return (plan.compact || (plan.split_sum == 2 && pr.S > 1 && pr.K == pr.S * pr.kps)) && !plan.x3 && !pr.f32 &&
+           !pr.acc_probe && plan.tile_m == kTileM && plan.bn <= 128 && !plan.rows_first;
 }
 
 bool groupable(const GemmProblem &pr, const TilePlan &plan)
@@ -1698,7 +1712,7 @@ cudaError_t launch_grouped_bn(const TcOperands<kMaxGroup> &ops, const TcArgs &a,
 cudaError_t launch_tc_grouped(const GemmProblem &pr, const TilePlan &plan, cudaStream_t stream,
                               unsigned long long capture)
 {
-    if (!groupable(pr, plan) || capture == 0) return launch_tc(pr, plan, stream);
+    if (!head_groupable(pr, plan) || capture == 0) return launch_tc(pr, plan, stream);
     cudaError_t e = check_plan(pr, plan);
     if (e != cudaSuccess) return e;
     GroupState st;
@@ -1731,6 +1745,7 @@ cudaError_t launch_tc_grouped(const GemmProblem &pr, const TilePlan &plan, cudaS
     st.plan = plan;
     st.smem = plan.smem_bytes;
     st.n = 1;
+    st.head = pr;
     std::lock_guard<std::mutex> lock(g_group_mu);
     // the capture's slot, else a free one, else the least recently used
     GroupState *slot = nullptr;
@@ -1777,6 +1792,68 @@ cudaError_t launch_tc_batch(const GemmProblem *prs, int n, const TilePlan &plan,
     }
 }
 
+namespace {
+
+// The head of a run keeps the compact plan (alone in a graph it runs faster
+// so).  The first call after it that takes whole-K blocks, for the same
+// shape, converts the head's launch to that plan and joins it: the node gets
+// the whole-K kernel, both problems and no cluster.  Where a step fails the
+// node is left as it was (its cluster attribute restored) and the call
+// launches on its own.
+bool convert_head(GroupState &st, const GemmProblem &pr, const TilePlan &plan)
+{
+    if (st.n != 1 || plan.cpc <= plan.chunks || plan.cluster != 1 || plan.bn != 128) return false;
+    const GemmProblem &h = st.head;
+    if (check_plan(h, plan) != cudaSuccess) return false;
+    TcOperands<kMaxGroup> ops = {};
+    if (!encode_problem(h, plan, &ops.tm[0][0], &ops.tm[0][1]) ||
+        !encode_problem(pr, plan, &ops.tm[1][0], &ops.tm[1][1]))
+        return false;
+    set_problem(ops, 0, h, plan);
+    set_problem(ops, 1, pr, plan);
+    TcArgs a = make_args(h, plan);   // the head's overlap mode
+    a.group = 2;
+    a.prefetchers = 0;
+    void *const func = h.b_kn ? grouped_kernel<128, true>(1) : grouped_kernel<128, false>(1);
+    const cudaError_t pe = h.b_kn ? prepare_kernel_attrs<128, 1, true, false, kTileM, kMaxGroup>()
+                                  : prepare_kernel_attrs<128, 1, false, false, kTileM, kMaxGroup>();
+    if (pe != cudaSuccess || func == nullptr) return false;
+    cudaLaunchAttributeValue old = {}, one = {};
+    if (cudaGraphKernelNodeGetAttribute(st.node, cudaLaunchAttributeClusterDimension, &old) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    one.clusterDim.x = one.clusterDim.y = one.clusterDim.z = 1;
+    if (cudaGraphKernelNodeSetAttribute(st.node, cudaLaunchAttributeClusterDimension, &one) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    cudaKernelNodeParams kp = {};
+    kp.func = func;
+    kp.gridDim = dim3(plan.grid.x, plan.grid.y * 2u, plan.grid.z);
+    kp.blockDim = dim3(kThreads, 1, 1);
+    kp.sharedMemBytes = static_cast<unsigned>(plan.smem_bytes);
+    void *params[2] = {&ops, &a};
+    kp.kernelParams = params;
+    kp.extra = nullptr;
+    if (cudaGraphKernelNodeSetParams(st.node, &kp) != cudaSuccess) {
+        (void)cudaGetLastError();
+        if (cudaGraphKernelNodeSetAttribute(st.node, cudaLaunchAttributeClusterDimension, &old) != cudaSuccess)
+            (void)cudaGetLastError();
+        st.valid = false;
+        return false;
+    }
+    st.plan = plan;
+    st.func = func;
+    st.smem = plan.smem_bytes;
+    st.ops = ops;
+    st.args = a;
+    st.n = 2;
+    return true;
+}
+
+}  // namespace
+
 bool join_group(const GemmProblem &pr, const TilePlan &plan, unsigned long long capture, cudaGraphNode_t dep,
                 int *group_size, int *mode)
 {
@@ -1787,10 +1864,17 @@ bool join_group(const GemmProblem &pr, const TilePlan &plan, unsigned long long 
     for (GroupState &g : g_groups)
         if (g.valid && g.capture == capture) st = &g;
     if (!st || st->node != dep || st->n >= kMaxGroup) return false;
-    const bool same = st->M == pr.M && st->N == pr.N && st->K == pr.K && st->S == pr.S && st->kps == pr.kps &&
-                      st->bf16 == pr.bf16 && st->b_kn == pr.b_kn && st->keep_p == (pr.P != nullptr) &&
-                      same_plan(st->plan, plan);
-    if (!same) return false;
+    const bool same_shape = st->M == pr.M && st->N == pr.N && st->K == pr.K && st->S == pr.S &&
+                            st->kps == pr.kps && st->bf16 == pr.bf16 && st->b_kn == pr.b_kn &&
+                            st->keep_p == (pr.P != nullptr);
+    if (!same_shape) return false;
+    if (!same_plan(st->plan, plan)) {
+        if (!convert_head(*st, pr, plan)) return false;
+        st->stamp = ++g_group_clock;
+        if (group_size) *group_size = st->n;
+        if (mode) *mode = st->overlap ? (st->store_early ? 2 : 1) : 0;
+        return true;
+    }
     const int g = st->n;
     if (!encode_problem(pr, plan, &st->ops.tm[g][0], &st->ops.tm[g][1])) return false;
     set_problem(st->ops, g, pr, plan);

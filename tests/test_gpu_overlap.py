@@ -601,10 +601,11 @@ def test_grouped_kn_bitwise(grouping):
 @pytest.mark.parametrize("fused", [1, 3])
 def test_whole_k_calls_bitwise(grouping, shape, fused):
     """Full splits whose compact plan takes more than half the SMs: the first
-    call of the capture keeps the compact plan (a cluster of the splits), the
-    calls after it take whole-K blocks (every chunk of every split in one
-    block, no cluster) and group among themselves.  Every output, and the
-    partials a call keeps, is the eager one, bit for bit."""
+    call of the capture launches with the compact plan (a cluster of the
+    splits); the calls after it take whole-K blocks (every chunk of every
+    split in one block, no cluster), and the second converts the first's
+    launch to that plan and joins it.  Every output, and the partials a call
+    keeps, is the eager one, bit for bit."""
     sk = grouping
     M, N, K, S, kps = shape
     dt = "bf16"
@@ -624,7 +625,7 @@ def test_whole_k_calls_bitwise(grouping, shape, fused):
     g = capture(body)
     assert seen[0]["chunks_per_block"] <= C and seen[0]["cluster"] > 1, seen[0]
     assert all(d["chunks_per_block"] == S * C and d["cluster"] == 1 and d["bn"] == 128 for d in seen[1:]), seen
-    assert [d["group"] for d in seen] == [1, 1, 2, 3, 4, 5, 6, 7, 8, 1, 2, 3], seen
+    assert [d["group"] for d in seen] == [1, 2, 3, 4, 5, 6, 7, 8, 1, 2, 3, 4], seen
     for _ in range(3):
         for it in insts:
             it["out"].fill_(7.0)
