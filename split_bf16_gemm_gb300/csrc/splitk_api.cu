@@ -122,8 +122,21 @@ int run_partial_pass(const void *A, const void *B, float *P, float *out, int64_t
     if (P) writes[nw++] = splitk::span_of(P, static_cast<uint64_t>(S * M * N) * 4);
     if (out) writes[nw++] = splitk::span_of(out, static_cast<uint64_t>(M * N) * 4);
     splitk::ChainGuard chain(stream, reads, 2, writes, nw);
+    // Inside a capture the launches of a run take the compact layout (two or
+    // three CTAs to an SM).  With grouping, the run's first launch takes the
+    // usual plan instead where the grouped kernels can run it: alone in a
+    // graph that is faster, and the next call converts it to the compact plan
+    // when it joins (one call per graph on GB300: BF16 M256 N1024 K2048 S2
+    // 14.3 -> 10.4 us, M96 N512 K2048 S4 10.5 -> 9.6; graphs of eight and
+    // forty unchanged).
     const bool compact = chain.capturing() && (chain.overlap() || chain.fresh());
-    TilePlan plan = splitk::plan_tc(M, N, K, S, kps, fused, pr.f32, compact, compact && chain.overlap());
+    TilePlan plan;
+    if (compact && !chain.overlap() && splitk::grouping_enabled()) {
+        plan = splitk::plan_tc(M, N, K, S, kps, fused, pr.f32, false);
+        if (!splitk::head_groupable(pr, plan)) plan = splitk::plan_tc(M, N, K, S, kps, fused, pr.f32, true);
+    } else {
+        plan = splitk::plan_tc(M, N, K, S, kps, fused, pr.f32, compact, compact && chain.overlap());
+    }
     if (!prefetch) plan.prefetchers = 0;
     pr.overlap = chain.overlap();
     pr.store_early = chain.store_early();

@@ -81,6 +81,9 @@ cudaError_t launch_tc(const GemmProblem &p, const TilePlan &plan, cudaStream_t s
 // later calls may join (join_group), where the plan allows grouping.
 cudaError_t launch_tc_grouped(const GemmProblem &p, const TilePlan &plan, cudaStream_t stream,
                               unsigned long long capture);
+// Whether a launch with this plan can head a group (the grouped kernels
+// have an instance for it).
+bool head_groupable(const GemmProblem &p, const TilePlan &plan);
 // Adds the call to the grouped launch captured as `dep` (the capture's
 // current dependency), if it has the same shape and plan and room; returns
 // whether it did (and the launch's problem count in *group_size).

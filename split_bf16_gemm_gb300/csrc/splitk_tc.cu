@@ -1665,16 +1665,17 @@ bool same_plan(const TilePlan &a, const TilePlan &b)
            a.grid.z == b.grid.z && a.smem_bytes == b.smem_bytes;
 }
 
-// A launch heads a group with a compact plan, or with the fused plan of a
-// shape whose later calls may take whole-K blocks (full splits), if its
-// tiles are 128 rows by at most 128 columns in column order (the grouped
-// kernels' instances); later calls join it only with the same compact plan,
-// or convert it (convert_head).
+}  // namespace
+
+// A launch heads a group with any 16-bit plan of tiles 128 rows by at most
+// 128 columns in column order (the grouped kernels' instances); later calls
+// join it only with the same compact plan, or convert it (convert_head).
 bool head_groupable(const GemmProblem &pr, const TilePlan &plan)
 {
-    return (plan.compact || (plan.split_sum == 2 && pr.S > 1 && pr.K == pr.S * pr.kps)) && !plan.x3 && !pr.f32 &&
-           !pr.acc_probe && plan.tile_m == kTileM && plan.bn <= 128 && !plan.rows_first;
+    return !plan.x3 && !pr.f32 && !pr.acc_probe && plan.tile_m == kTileM && plan.bn <= 128 && !plan.rows_first;
 }
+
+namespace {
 
 bool groupable(const GemmProblem &pr, const TilePlan &plan)
 {
@@ -1794,16 +1795,33 @@ cudaError_t launch_tc_batch(const GemmProblem *prs, int n, const TilePlan &plan,
 
 namespace {
 
-// The head of a run keeps the compact plan (alone in a graph it runs faster
-// so).  The first call after it that takes whole-K blocks, for the same
-// shape, converts the head's launch to that plan and joins it: the node gets
-// the whole-K kernel, both problems and no cluster.  Where a step fails the
-// node is left as it was (its cluster attribute restored) and the call
-// launches on its own.
+// The first launch of a run takes its usual (eager) plan, which alone in a
+// graph runs fastest.  The first call after it with the same shape converts
+// that launch to its own plan (compact, or whole-K blocks) and joins it: the
+// node gets that plan's kernel, cluster size, grid and shared memory and both
+// problems.  Where a step fails the node is left as it was (its cluster
+// attribute restored) and the call launches on its own.
+template <bool KN>
+cudaError_t prepare_grouped(int bn, int q)
+{
+    switch (bn * 16 + q) {
+    case 64 * 16 + 1: return prepare_kernel_attrs<64, 1, KN, false, kTileM, kMaxGroup>();
+    case 64 * 16 + 2: return prepare_kernel_attrs<64, 2, KN, false, kTileM, kMaxGroup>();
+    case 64 * 16 + 4: return prepare_kernel_attrs<64, 4, KN, false, kTileM, kMaxGroup>();
+    case 64 * 16 + 8: return prepare_kernel_attrs<64, 8, KN, false, kTileM, kMaxGroup>();
+    case 128 * 16 + 1: return prepare_kernel_attrs<128, 1, KN, false, kTileM, kMaxGroup>();
+    case 128 * 16 + 2: return prepare_kernel_attrs<128, 2, KN, false, kTileM, kMaxGroup>();
+    case 128 * 16 + 4: return prepare_kernel_attrs<128, 4, KN, false, kTileM, kMaxGroup>();
+    case 128 * 16 + 8: return prepare_kernel_attrs<128, 8, KN, false, kTileM, kMaxGroup>();
+    default: return cudaErrorInvalidConfiguration;
+    }
+}
+
 bool convert_head(GroupState &st, const GemmProblem &pr, const TilePlan &plan)
 {
-    if (st.n != 1 || plan.cpc <= plan.chunks || plan.cluster != 1 || plan.bn != 128) return false;
+    if (st.n != 1 || !groupable(pr, plan)) return false;
     const GemmProblem &h = st.head;
+    if ((h.out != nullptr) != (plan.split_sum == 2) || (pr.out != nullptr) != (plan.split_sum == 2)) return false;
     if (check_plan(h, plan) != cudaSuccess) return false;
     TcOperands<kMaxGroup> ops = {};
     if (!encode_problem(h, plan, &ops.tm[0][0], &ops.tm[0][1]) ||
@@ -1814,16 +1832,20 @@ bool convert_head(GroupState &st, const GemmProblem &pr, const TilePlan &plan)
     TcArgs a = make_args(h, plan);   // the head's overlap mode
     a.group = 2;
     a.prefetchers = 0;
-    void *const func = h.b_kn ? grouped_kernel<128, true>(1) : grouped_kernel<128, false>(1);
-    const cudaError_t pe = h.b_kn ? prepare_kernel_attrs<128, 1, true, false, kTileM, kMaxGroup>()
-                                  : prepare_kernel_attrs<128, 1, false, false, kTileM, kMaxGroup>();
+    void *const func = plan.bn == 64 ? (h.b_kn ? grouped_kernel<64, true>(plan.cluster)
+                                               : grouped_kernel<64, false>(plan.cluster))
+                                     : (h.b_kn ? grouped_kernel<128, true>(plan.cluster)
+                                               : grouped_kernel<128, false>(plan.cluster));
+    const cudaError_t pe = h.b_kn ? prepare_grouped<true>(plan.bn, plan.cluster)
+                                  : prepare_grouped<false>(plan.bn, plan.cluster);
     if (pe != cudaSuccess || func == nullptr) return false;
     cudaLaunchAttributeValue old = {}, one = {};
     if (cudaGraphKernelNodeGetAttribute(st.node, cudaLaunchAttributeClusterDimension, &old) != cudaSuccess) {
         (void)cudaGetLastError();
         return false;
     }
-    one.clusterDim.x = one.clusterDim.y = one.clusterDim.z = 1;
+    one.clusterDim.x = one.clusterDim.y = 1;
+    one.clusterDim.z = static_cast<unsigned>(plan.cluster);
     if (cudaGraphKernelNodeSetAttribute(st.node, cudaLaunchAttributeClusterDimension, &one) != cudaSuccess) {
         (void)cudaGetLastError();
         return false;
@@ -1866,7 +1888,7 @@ bool join_group(const GemmProblem &pr, const TilePlan &plan, unsigned long long 
     if (!st || st->node != dep || st->n >= kMaxGroup) return false;
     const bool same_shape = st->M == pr.M && st->N == pr.N && st->K == pr.K && st->S == pr.S &&
                             st->kps == pr.kps && st->bf16 == pr.bf16 && st->b_kn == pr.b_kn &&
-                            st->keep_p == (pr.P != nullptr);
+                            st->keep_p == (pr.P != nullptr) && (st->head.out != nullptr) == (pr.out != nullptr);
     if (!same_shape) return false;
     if (!same_plan(st->plan, plan)) {
         if (!convert_head(*st, pr, plan)) return false;
