@@ -57,7 +57,8 @@
  * writes what the new launch writes either, it also stores at once and
  * waits only before it finishes, so the grids still finish in launch order.
  * Such a fused launch may also give each thread block all the chunks of its
- * split, each in its own accumulator, added in chunk order inside the block,
+ * split (or two consecutive chunks), each in its own accumulator, added in
+ * pairs inside the block (the owner adds a split's chunks in pairs too),
  * or, for large shapes with full splits, every chunk of every split.
  * A call that may store early and has the same shape and plan as the launch
  * before it joins that launch instead of adding one: the launch's graph
@@ -372,10 +373,10 @@ int splitk_set_tile_override(int bn, int chunks, int kblocks_per_stage);
  *  three thread blocks fit on an SM, the peers' shares received inside the
  *  ring; one-wave plans),
  *  compact_stages, compact_kblocks_per_stage, compact_dynamic_smem_bytes,
- *  compact_chunks_per_block (1, or every chunk of a split in one thread
- *  block, each in its own accumulator, added in chunk order before the
- *  exchange: the same sums; or, more than chunks, every chunk of every
- *  split in one block of 128 x 128, no cluster and one block per SM, which
+ *  compact_chunks_per_block (1, or two consecutive chunks of a split in one
+ *  thread block, each in its own accumulator, added before the exchange:
+ *  the same sums, since a split's chunks are added in pairs; or, more than
+ *  chunks, every chunk of every split in one block of 128 x 128, no cluster and one block per SM, which
  *  adds each split's chunks and then the splits in the same order: fused
  *  16-bit calls whose splits are full and whose chunks tile them, where the
  *  compact plan would take more than half the SMs), compact_cluster_size,
@@ -430,9 +431,9 @@ int splitk_set_overlap(int mode);
  * taken for such launches and for the first of a capture, when a one-wave
  * plan allows it), capturing (the stream was being captured), bn, chunks,
  * stages, kblocks_per_stage, dynamic_smem_bytes, chunks_per_block (1, or
- * all the chunks of a split, each in its own accumulator and added in chunk
- * order inside the block: the same sums; more than chunks: every chunk of
- * every split, no cluster), cluster_size, group (the calls
+ * two consecutive chunks of a split, each in its own accumulator and added
+ * inside the block: the same sums; more than chunks: every chunk of every
+ * split, no cluster), cluster_size, group (the calls
  * the launch computes so far: 1, or more where the call joined the launch
  * of the calls before it)}.  `info` must hold 11 ints.  Diagnostic;
  * returns SPLITK_OK or SPLITK_ERR_NULL. */

@@ -39,9 +39,10 @@
 // Each cluster rank owns 1/Q of the tile; each warp pushes the boxes it staged
 // to their owners with bulk shared-memory copies (cp.async.bulk into the
 // owner's shared memory, counted on the owner's mbarrier), and each owner adds
-// the contributions in rank order from its own shared memory -- chunks in
-// chunk order, then splits in split order, the separate reduce kernel's sums
-// -- so the result does not depend on arrival order.
+// the contributions in rank order from its own shared memory -- each split's
+// chunks in pairs ((c0 + c1) + (c2 + c3) ...), then the splits in split order,
+// the separate reduce kernel's sums -- so the result does not depend on
+// arrival order.
 //
 // Programmatic dependent launch: the kernel waits for the previous grid (whose
 // writes it may read) before its first load, and lets the next grid start its
@@ -163,6 +164,22 @@ __device__ __forceinline__ void add4(float4 &a, const float4 &b)
     a.w += b.w;
 }
 
+// The sum of n (a power of two) consecutive chunk contributions in pairs:
+// (v0 + v1) + (v2 + v3), and so on up the tree.  Any aligned run of 2^j
+// chunks is a subtree, so a CTA that sums two chunks itself and an owner that
+// adds such pair sums give the bits of an owner adding single chunks.
+template <int NV>
+__device__ __forceinline__ float4 pair_sum(const float4 *v)
+{
+    if constexpr (NV == 1) {
+        return v[0];
+    } else {
+        float4 a = pair_sum<NV / 2>(v);
+        add4(a, pair_sum<NV / 2>(v + NV / 2));
+        return a;
+    }
+}
+
 // The low part of an F32 value for the 3xTF32 products.  The tensor cores
 // read an F32 operand as TF32 by dropping its 13 low fraction bits (checked
 // on GB300: every output of a one-hot product equals the truncated input), so
@@ -176,9 +193,9 @@ __device__ __forceinline__ uint32_t tf32_lo(uint32_t x)
 }
 
 // The owner's sums when the cluster holds every split of the tile (rank =
-// split * CC + chunk): each split's chunks in chunk order, then the splits in
-// split order -- the additions the reduce kernel makes on the same partials,
-// which are also stored with HAS_P.  rbase[r] plus a piece's staging offset
+// split * CC + chunk): each split's chunks in pairs (pair_sum), then the
+// splits in split order -- the additions the reduce kernel makes on the same
+// partials, which are also stored with HAS_P.  rbase[r] plus a piece's staging offset
 // addresses rank r's contribution to it.  The chunk count and HAS_P are
 // template parameters so that the grouping costs no branches: decided at run
 // time, the branches of this short sequence (resolved one after another in
@@ -195,9 +212,7 @@ __device__ __forceinline__ void cluster_split_sum(const uint32_t (&rbase)[Q], in
         float4 tot = v[0];
 #pragma unroll
         for (int sp = 0; sp < Q / CC; ++sp) {
-            float4 part = v[sp * CC];
-#pragma unroll
-            for (int c = 1; c < CC; ++c) add4(part, v[sp * CC + c]);
+            const float4 part = pair_sum<CC>(&v[sp * CC]);
             if (HAS_P && live) *reinterpret_cast<float4 *>(P + sp * MN + e) = part;
             if (sp == 0)
                 tot = part;
@@ -630,9 +645,10 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
                                       v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             } else {
                 if (!whole_k) {
-                    // the chunk sum: chunk 0 + chunk 1 + ... in order, a chunk
-                    // past the split's end adding +0 -- what the owner adds when
-                    // each chunk has its own CTA.  16 columns at a time.
+                    // the chunk sum of a pair (cpc is 2 here): chunk 0 + chunk 1,
+                    // a chunk past the split's end adding +0 -- the pair sum
+                    // the owner adds when each chunk has its own CTA.  16
+                    // columns at a time.
 #pragma unroll 1
                     for (int hh = 0; hh < 2; ++hh) {
                         uint32_t v[16];
@@ -779,13 +795,8 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
             for (int r = 0; r < Q; ++r) v[r] = ptx::ld_shared_v4(rbase[r] + p.off);
         };
         auto tile_elem = [&](const Piece &p) { return tile0 + static_cast<size_t>(p.row) * args.N + p.col; };
-        // the chunk sum of one split (Q == CC): chunks in order 0, 1, 2, ...
-        auto chunk_sum = [&](const float4 (&v)[Q]) {
-            float4 acc = v[0];
-#pragma unroll
-            for (int r = 1; r < Q; ++r) add4(acc, v[r]);
-            return acc;
-        };
+        // the chunk sum of one split (Q == CC): the chunks in pairs
+        auto chunk_sum = [&](const float4 (&v)[Q]) { return pair_sum<Q>(v); };
         if (args.split_sum != 2) {
             float *const Ps = P + static_cast<size_t>(s) * MN;
             for (int g0 = my_lo + tid; g0 < my_hi; g0 += 2 * kThreads) {
@@ -1363,10 +1374,11 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
     // S4: 3.55 against 3.28 us).
     //
     // Merged chunks: a fused compact plan whose chunks are whole k-blocks
-    // gives each CTA all the chunks of its split, each in its own
-    // accumulator, and the CTA adds them in chunk order before the exchange
-    // -- the same sums as one CTA per chunk, with 1/chunks of the CTAs, each
-    // loading its split's whole K range, and a cluster of the splits only.
+    // gives each CTA two consecutive chunks of its split (all of them where
+    // there are two), each in its own accumulator, and the CTA adds the pair
+    // before the exchange -- the same sums as one CTA per chunk (the owner
+    // adds chunks in pairs), with half the CTAs, each loading twice the K
+    // range, and a cluster of half the size.
     // Launched back to back in a graph such CTAs spend less of their time on
     // the fixed parts (set-up, staging, exchange, stores), exchange a
     // quarter of the bytes, and keep three to an SM: on GB300 the headline
@@ -1477,8 +1489,7 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
         const bool mergeable = !x3 && split_sum == 2 && chunks > 1 && can3d && chunk_len % kBlockK == 0;
         const bool whole = whole_ok && !x3 && split_sum == 2 && S > 1 && can3d && chunk_len % kBlockK == 0 &&
                            K == S * kps && kps == static_cast<int64_t>(chunks) * chunk_len;
-        if (!(mergeable && chunks == 2 && bn == 64 && try_compact(2, 128)) &&
-            !(mergeable && bn * chunks <= 128 && try_compact(chunks, bn)))
+        if (!(mergeable && bn == 64 && try_compact(2, 128)) && !(mergeable && bn == 64 && try_compact(2, 64)))
             try_compact(1, bn);
         const int64_t compact_ctas = p.compact ? static_cast<int64_t>(p.grid.x) * p.grid.y * p.grid.z : 0;
         if (whole && (!p.compact || compact_ctas > resident_clusters(1) / 2)) try_whole_k(128);
@@ -1564,7 +1575,7 @@ cudaError_t check_plan(const GemmProblem &pr, const TilePlan &plan)
     // (or every chunk of every split: full splits that the chunks tile, no cluster)
     const bool whole_k = plan.cpc > plan.chunks;
     const bool cpc_ok = plan.cpc == 1 ||
-                        ((plan.cpc == plan.chunks || (whole_k && plan.cpc == pr.S * plan.chunks && plan.cluster == 1 &&
+                        (((plan.cpc == 2 && plan.chunks % 2 == 0) || (whole_k && plan.cpc == pr.S * plan.chunks && plan.cluster == 1 &&
                                                       pr.K == pr.S * pr.kps &&
                                                       pr.kps == static_cast<int64_t>(plan.chunks) * plan.chunk_len)) &&
                          !plan.x3 && plan.tile_m == kTileM && tmem_fits(plan.bn * plan.cpc, plan.smem_bytes) &&

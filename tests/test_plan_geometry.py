@@ -22,10 +22,11 @@ tests, and every tile override:
 - the compact layout (taken inside graph captures, by fused calls and by
   the partial pass of the two-kernel call): the same tiles, chunks and sums, a ring that still covers every k once, the receive slots inside
   the ring after the staging area, and two or three thread blocks' shared
-  and tensor memory within one SM's; where a block takes every chunk of its
-  split (chunks_per_block > 1), each chunk starts on a stage boundary, its
-  accumulators fit the block's share of tensor memory, and the cluster
-  holds the splits only.
+  and tensor memory within one SM's; where a block takes two consecutive
+  chunks of its split (chunks_per_block 2), each chunk starts on a stage
+  boundary, its accumulators fit the block's share of tensor memory, and
+  the cluster holds half as many blocks; where a block takes all of K
+  (whole-K), its chunks cover K once in order and it is alone on its SM.
 """
 import itertools
 
@@ -200,12 +201,12 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
         cst, ckbs, csmem = d["compact_stages"], d["compact_kblocks_per_stage"], d["compact_smem_bytes"]
         cpc, qc, CB = d["compact_chunks_per_block"], d["compact_cluster"], d["compact_bn"]
         assert 1 <= cst <= 8 and 1 <= ckbs <= 4 and (ckbs == 1 or T3 or (K % kb_elems == 0 and kps % kb_elems == 0))
-        # every chunk of a split in one block: only where the chunks are whole
-        # stages of whole k-blocks; 128-column tiles (from 64) only so, with
-        # two chunks
+        # two consecutive chunks of a split in one block: only where the
+        # chunks are whole stages of whole k-blocks, from 64-column tiles
+        # (widened to 128 or not)
         mergeable = not x3 and SS == 2 and C > 1 and can3d and CL % 64 == 0
-        assert CB == BN or (CB == 128 and BN == 64 and C == 2 and cpc == 2 and mergeable), (BN, CB, cpc)
-        assert cpc in (1, C) and (cpc == 1 or (mergeable and CB * C <= 256))
+        assert CB == BN or (CB == 128 and BN == 64 and cpc == 2 and mergeable), (BN, CB, cpc)
+        assert cpc in (1, 2) and (cpc == 1 or (mergeable and BN == 64 and C % 2 == 0))
         assert qc == Q // cpc and d["compact_grid_z"] == S * C // cpc and d["compact_grid_z"] % qc == 0
         assert N % CB == 0
         cctas = -(-M // TM) * (N // CB) * S * C // cpc
