@@ -1678,44 +1678,67 @@ bool same_plan(const TilePlan &a, const TilePlan &b)
 
 }  // namespace
 
-// A launch heads a group with any 16-bit plan of tiles 128 rows by at most
-// 128 columns in column order (the grouped kernels' instances); later calls
-// join it only with the same compact plan, or convert it (convert_head).
+// A launch heads a group with any tensor-core plan (16-bit operands, or F32
+// with the [N,K] weight) of tiles 128 rows by at most 128 columns in column
+// order (the grouped kernels' instances); later calls join it only with the
+// same compact plan, or convert it (convert_head).
 bool head_groupable(const GemmProblem &pr, const TilePlan &plan)
 {
-    return !plan.x3 && !pr.f32 && !pr.acc_probe && plan.tile_m == kTileM && plan.bn <= 128 && !plan.rows_first;
+    return plan.x3 == pr.f32 && !(pr.f32 && pr.b_kn) && !pr.acc_probe && plan.tile_m == kTileM && plan.bn <= 128 &&
+           !plan.rows_first;
 }
 
 namespace {
 
 bool groupable(const GemmProblem &pr, const TilePlan &plan)
 {
-    return plan.compact && !plan.x3 && !pr.f32 && !pr.acc_probe && plan.tile_m == kTileM && plan.bn <= 128 &&
-           !plan.rows_first;
+    return plan.compact && head_groupable(pr, plan);
 }
 
-template <int BN, bool KN>
-void *grouped_kernel(int q)
+// The grouped kernel of a plan: one instance per tile width (64, 128),
+// operand form (16-bit [N,K] or [K,N], F32 [N,K]) and cluster size.  `op`
+// asks for its function, its shared-memory attribute, or a launch.
+enum class GroupedOp { kFunc, kPrepare, kLaunch };
+
+template <int BN, int Q, bool KN, bool X3>
+cudaError_t grouped_op_q(GroupedOp op, void **func, const TcOperands<kMaxGroup> *ops, const TcArgs *a,
+                         const TilePlan *plan, cudaStream_t stream)
 {
-    switch (q) {
-    case 1: return reinterpret_cast<void *>(tc_splitk_kernel<BN, 1, KN, false, kTileM, kMaxGroup>);
-    case 2: return reinterpret_cast<void *>(tc_splitk_kernel<BN, 2, KN, false, kTileM, kMaxGroup>);
-    case 4: return reinterpret_cast<void *>(tc_splitk_kernel<BN, 4, KN, false, kTileM, kMaxGroup>);
-    case 8: return reinterpret_cast<void *>(tc_splitk_kernel<BN, 8, KN, false, kTileM, kMaxGroup>);
-    default: return nullptr;
+    switch (op) {
+    case GroupedOp::kFunc:
+        *func = reinterpret_cast<void *>(tc_splitk_kernel<BN, Q, KN, X3, kTileM, kMaxGroup>);
+        return cudaSuccess;
+    case GroupedOp::kPrepare: return prepare_kernel_attrs<BN, Q, KN, X3, kTileM, kMaxGroup>();
+    default: return launch_bn<BN, Q, KN, X3, kTileM, kMaxGroup>(*ops, *a, *plan, stream);
     }
 }
 
-template <int BN, bool KN>
-cudaError_t launch_grouped_bn(const TcOperands<kMaxGroup> &ops, const TcArgs &a, const TilePlan &plan,
-                              cudaStream_t stream)
+template <int BN, bool KN, bool X3>
+cudaError_t grouped_op_bn(GroupedOp op, int q, void **func, const TcOperands<kMaxGroup> *ops, const TcArgs *a,
+                          const TilePlan *plan, cudaStream_t stream)
 {
-    switch (plan.cluster) {
-    case 1: return launch_bn<BN, 1, KN, false, kTileM, kMaxGroup>(ops, a, plan, stream);
-    case 2: return launch_bn<BN, 2, KN, false, kTileM, kMaxGroup>(ops, a, plan, stream);
-    case 4: return launch_bn<BN, 4, KN, false, kTileM, kMaxGroup>(ops, a, plan, stream);
-    case 8: return launch_bn<BN, 8, KN, false, kTileM, kMaxGroup>(ops, a, plan, stream);
+    switch (q) {
+    case 1: return grouped_op_q<BN, 1, KN, X3>(op, func, ops, a, plan, stream);
+    case 2: return grouped_op_q<BN, 2, KN, X3>(op, func, ops, a, plan, stream);
+    case 4: return grouped_op_q<BN, 4, KN, X3>(op, func, ops, a, plan, stream);
+    case 8: return grouped_op_q<BN, 8, KN, X3>(op, func, ops, a, plan, stream);
     default: return note_error(cudaErrorInvalidConfiguration, "cluster size");
+    }
+}
+
+cudaError_t grouped_op(GroupedOp op, const TilePlan &plan, bool kn, void **func,
+                       const TcOperands<kMaxGroup> *ops = nullptr, const TcArgs *a = nullptr,
+                       cudaStream_t stream = nullptr)
+{
+    const int q = plan.cluster;
+    switch (plan.bn * 4 + (kn ? 2 : 0) + (plan.x3 ? 1 : 0)) {
+    case 64 * 4 + 0: return grouped_op_bn<64, false, false>(op, q, func, ops, a, &plan, stream);
+    case 64 * 4 + 2: return grouped_op_bn<64, true, false>(op, q, func, ops, a, &plan, stream);
+    case 64 * 4 + 1: return grouped_op_bn<64, false, true>(op, q, func, ops, a, &plan, stream);
+    case 128 * 4 + 0: return grouped_op_bn<128, false, false>(op, q, func, ops, a, &plan, stream);
+    case 128 * 4 + 2: return grouped_op_bn<128, true, false>(op, q, func, ops, a, &plan, stream);
+    case 128 * 4 + 1: return grouped_op_bn<128, false, true>(op, q, func, ops, a, &plan, stream);
+    default: return note_error(cudaErrorInvalidConfiguration, "tile width or operand form");
     }
 }
 
@@ -1732,14 +1755,9 @@ cudaError_t launch_tc_grouped(const GemmProblem &pr, const TilePlan &plan, cudaS
     set_problem(st.ops, 0, pr, plan);
     st.args = make_args(pr, plan);
     st.args.group = 1;
-    switch (plan.bn * 2 + (pr.b_kn ? 1 : 0)) {
-    case 64 * 2 + 0: e = launch_grouped_bn<64, false>(st.ops, st.args, plan, stream); st.func = grouped_kernel<64, false>(plan.cluster); break;
-    case 64 * 2 + 1: e = launch_grouped_bn<64, true>(st.ops, st.args, plan, stream); st.func = grouped_kernel<64, true>(plan.cluster); break;
-    case 128 * 2 + 0: e = launch_grouped_bn<128, false>(st.ops, st.args, plan, stream); st.func = grouped_kernel<128, false>(plan.cluster); break;
-    case 128 * 2 + 1: e = launch_grouped_bn<128, true>(st.ops, st.args, plan, stream); st.func = grouped_kernel<128, true>(plan.cluster); break;
-    default: return note_error(cudaErrorInvalidConfiguration, "tile width");
-    }
+    e = grouped_op(GroupedOp::kLaunch, plan, pr.b_kn, nullptr, &st.ops, &st.args, stream);
     if (e != cudaSuccess) return e;
+    if (grouped_op(GroupedOp::kFunc, plan, pr.b_kn, &st.func) != cudaSuccess) st.func = nullptr;
     // the node just captured, which later calls may join
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     unsigned long long id = 0;
@@ -1795,13 +1813,7 @@ cudaError_t launch_tc_batch(const GemmProblem *prs, int n, const TilePlan &plan,
     TilePlan bp = plan;
     bp.grid.y *= static_cast<unsigned>(n);   // blockIdx.y = problem * row tiles + row tile
     bp.prefetchers = 0;
-    switch (plan.bn * 2 + (prs[0].b_kn ? 1 : 0)) {
-    case 64 * 2 + 0: return launch_grouped_bn<64, false>(ops, a, bp, stream);
-    case 64 * 2 + 1: return launch_grouped_bn<64, true>(ops, a, bp, stream);
-    case 128 * 2 + 0: return launch_grouped_bn<128, false>(ops, a, bp, stream);
-    case 128 * 2 + 1: return launch_grouped_bn<128, true>(ops, a, bp, stream);
-    default: return note_error(cudaErrorInvalidConfiguration, "tile width");
-    }
+    return grouped_op(GroupedOp::kLaunch, bp, prs[0].b_kn, nullptr, &ops, &a, stream);
 }
 
 namespace {
@@ -1812,22 +1824,6 @@ namespace {
 // node gets that plan's kernel, cluster size, grid and shared memory and both
 // problems.  Where a step fails the node is left as it was (its cluster
 // attribute restored) and the call launches on its own.
-template <bool KN>
-cudaError_t prepare_grouped(int bn, int q)
-{
-    switch (bn * 16 + q) {
-    case 64 * 16 + 1: return prepare_kernel_attrs<64, 1, KN, false, kTileM, kMaxGroup>();
-    case 64 * 16 + 2: return prepare_kernel_attrs<64, 2, KN, false, kTileM, kMaxGroup>();
-    case 64 * 16 + 4: return prepare_kernel_attrs<64, 4, KN, false, kTileM, kMaxGroup>();
-    case 64 * 16 + 8: return prepare_kernel_attrs<64, 8, KN, false, kTileM, kMaxGroup>();
-    case 128 * 16 + 1: return prepare_kernel_attrs<128, 1, KN, false, kTileM, kMaxGroup>();
-    case 128 * 16 + 2: return prepare_kernel_attrs<128, 2, KN, false, kTileM, kMaxGroup>();
-    case 128 * 16 + 4: return prepare_kernel_attrs<128, 4, KN, false, kTileM, kMaxGroup>();
-    case 128 * 16 + 8: return prepare_kernel_attrs<128, 8, KN, false, kTileM, kMaxGroup>();
-    default: return cudaErrorInvalidConfiguration;
-    }
-}
-
 bool convert_head(GroupState &st, const GemmProblem &pr, const TilePlan &plan)
 {
     if (st.n != 1 || !groupable(pr, plan)) return false;
@@ -1843,13 +1839,10 @@ bool convert_head(GroupState &st, const GemmProblem &pr, const TilePlan &plan)
     TcArgs a = make_args(h, plan);   // the head's overlap mode
     a.group = 2;
     a.prefetchers = 0;
-    void *const func = plan.bn == 64 ? (h.b_kn ? grouped_kernel<64, true>(plan.cluster)
-                                               : grouped_kernel<64, false>(plan.cluster))
-                                     : (h.b_kn ? grouped_kernel<128, true>(plan.cluster)
-                                               : grouped_kernel<128, false>(plan.cluster));
-    const cudaError_t pe = h.b_kn ? prepare_grouped<true>(plan.bn, plan.cluster)
-                                  : prepare_grouped<false>(plan.bn, plan.cluster);
-    if (pe != cudaSuccess || func == nullptr) return false;
+    void *func = nullptr;
+    if (grouped_op(GroupedOp::kFunc, plan, h.b_kn, &func) != cudaSuccess ||
+        grouped_op(GroupedOp::kPrepare, plan, h.b_kn, nullptr) != cudaSuccess || func == nullptr)
+        return false;
     cudaLaunchAttributeValue old = {}, one = {};
     if (cudaGraphKernelNodeGetAttribute(st.node, cudaLaunchAttributeClusterDimension, &old) != cudaSuccess) {
         (void)cudaGetLastError();

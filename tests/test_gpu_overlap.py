@@ -638,3 +638,48 @@ def test_whole_k_calls_bitwise(grouping, shape, fused):
             P = S * M * N
             assert bitwise(it["ws"][:P], w[:P])
     assert sk.splitk_get_device_status() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    (96, 512, 512, 4, 128),       # clusters of 4
+    (256, 1024, 2048, 2, 1024),   # the headline shape with F32 operands
+    (32, 512, 2048, 1, 2048),     # one split, eight chunks
+])
+@pytest.mark.parametrize("fused", [1, 3])
+def test_grouped_f32_calls_bitwise(grouping, shape, fused):
+    """F32 operands (3xTF32) group the same way: 12 independent calls, the
+    first launching with its usual plan, the second converting that launch
+    to the compact plan and joining it, up to 8 per launch.  Every output
+    (and kept partials) is the eager one, bit for bit."""
+    sk = grouping
+    M, N, K, S, kps = shape
+    dt = "f32"
+    if not sk.splitk_describe_launch(M, N, K, S, kps, dt, fused=fused)["fused_in_kernel"]:
+        pytest.skip("this shape runs the two kernels")
+    insts = instances(sk, M, N, K, S, kps, dt, 12)
+    for it in insts:
+        sk.gemm_bt(it["A"], it["B"], it["ref"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=fused)
+    torch.cuda.synchronize()
+    refs_ws = [it["ws"].clone() for it in insts]
+    seen = []
+
+    def body():
+        for it in insts:
+            sk.gemm_bt(it["A"], it["B"], it["out"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=fused)
+            seen.append(sk.splitk_last_launch())
+
+    g = capture(body)
+    assert [d["group"] for d in seen] == [1, 2, 3, 4, 5, 6, 7, 8, 1, 2, 3, 4], seen
+    assert all(d["compact"] == 1 for d in seen[1:]), seen
+    for _ in range(2):
+        for it in insts:
+            it["out"].fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        for it in insts:
+            assert bitwise(it["out"], it["ref"])
+    if fused == 3:
+        for it, w in zip(insts, refs_ws):
+            P = S * M * N
+            assert bitwise(it["ws"][:P], w[:P])
+    assert sk.splitk_get_device_status() == 0
