@@ -178,11 +178,7 @@ int gemm_bt_workspace_init(void *workspace, size_t workspace_bytes, void *stream
  *                 (too many splits for one cluster, or more tiles than
  *                 resident clusters), the call runs the two kernels of 0,
  *                 which measured faster there than summing through global
- *                 memory; so it does for F32 operands with M <= 32 or 8
- *                 splits or more where the cluster summing the splits would
- *                 be larger than the partial pass's own (measured faster
- *                 too).
- *                 splitk_describe_launch reports which;
+ *                 memory.  splitk_describe_launch reports which;
  *              3: as 1, and the workspace also holds the partials afterwards.
  * For a given shape, `out` (and the partials, where kept) are bitwise the
  * same for every value of `fused`. */

@@ -123,15 +123,18 @@ int run_partial_pass(const void *A, const void *B, float *P, float *out, int64_t
     if (out) writes[nw++] = splitk::span_of(out, static_cast<uint64_t>(M * N) * 4);
     splitk::ChainGuard chain(stream, reads, 2, writes, nw);
     // Inside a capture the launches of a run take the compact layout (two or
-    // three CTAs to an SM).  With grouping, the run's first launch takes the
-    // usual plan instead where the grouped kernels can run it: alone in a
+    // three CTAs to an SM).  With grouping, a fused run's first launch takes
+    // the usual plan instead where the grouped kernels can run it: alone in a
     // graph that is faster, and the next call converts it to the compact plan
     // when it joins (one call per graph on GB300: BF16 M256 N1024 K2048 S2
     // 14.3 -> 10.4 us, M96 N512 K2048 S4 10.5 -> 9.6; graphs of eight and
-    // forty unchanged).
+    // forty unchanged).  A partial pass of the two-kernel call keeps the
+    // compact layout: a reduce follows it, so nothing joins it, and the next
+    // partial passes share the SMs with it (graphs of eight such calls: 4.89
+    // against 5.11 us per call).
     const bool compact = chain.capturing() && (chain.overlap() || chain.fresh());
     TilePlan plan;
-    if (compact && !chain.overlap() && splitk::grouping_enabled()) {
+    if (compact && !chain.overlap() && fused && splitk::grouping_enabled()) {
         plan = splitk::plan_tc(M, N, K, S, kps, fused, pr.f32, false);
         if (!splitk::head_groupable(pr, plan)) plan = splitk::plan_tc(M, N, K, S, kps, fused, pr.f32, true);
     } else {
@@ -213,23 +216,20 @@ bool fused_possible(int dtype, bool b_kn) { return !(dtype == SPLITK_F32 && b_kn
 
 }  // namespace
 
-// Whether gemm_bt(fused != 0) sums the splits inside its launch.  It does
-// where the tile plan holds all of a tile's splits in one resident cluster,
-// except for F32 operands (3xTF32) with M <= 32 or 8 splits or more, where
-// the cluster that sums the splits is larger than the partial pass's own
-// (every split's chunks, against one split's): its exchange moves the whole
-// 128-row accumulator, of which at most 32 rows are live for M <= 32, and
-// the F32 stages leave little room for the receive slots; on GB300 the two
-// kernels measured faster (M32 N512 K2048, 2 to 8 splits: 5.6-5.8 against
-// 7.0-7.2 us; M96 N512 K512, 8 splits: 4.0 against 4.5 us).
+// Whether gemm_bt(fused != 0) sums the splits inside its launch: where the
+// tile plan holds all of a tile's splits in one resident cluster.  (F32
+// operands with M <= 32 or 8 splits or more once ran the two kernels there,
+// which measured faster before the F32 launches grouped; on GB300 the fused
+// call now wins for them as well, eagerly (M32 N512 K2048, 2 to 8 splits:
+// 9.5 against 11.0-11.3 us; M96 N512 K512 S8 5.5 against 7.4; M256 N1024
+// K2048 S8 14.5 both ways) and in graphs of eight (4.1 against 4.9; 2.1
+// against 4.0).)
 bool splitk::fused_in_kernel(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, int dtype, bool b_kn)
 {
     if (!fused_possible(dtype, b_kn)) return false;
     const bool x3 = dtype == SPLITK_F32;
     const TilePlan f = splitk::plan_tc(M, N, K, S, kps, true, x3);
-    if (f.split_sum != 2) return false;
-    if (x3 && (M <= 32 || S >= 8) && f.cluster > splitk::plan_tc(M, N, K, S, kps, false, x3).cluster) return false;
-    return true;
+    return f.split_sum == 2;
 }
 
 namespace {

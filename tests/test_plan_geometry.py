@@ -399,22 +399,21 @@ def test_fused_routing(lib):
     """gemm_bt(fused=1) sums the splits in its launch only where one resident
     cluster holds all of a tile's splits and chunks; elsewhere it runs the two
     kernels (the same chunks, so the same result bit for bit), which measured
-    faster on GB300 than summing through global memory.  F32 operands with
-    M <= 32 or 8 splits or more also run the two kernels where the summing
-    cluster would be larger than the partial pass's own."""
+    faster on GB300 than summing through global memory; F32 operands follow
+    the same rule."""
     sk = lib
     fused_in_kernel = [
         (256, 1024, 2048, 2, 1024, "bf16"), (256, 1024, 2048, 4, 512, "bf16"), (96, 512, 2048, 4, 512, "bf16"),
         (256, 512, 2048, 4, 512, "bf16"), (32, 64, 128, 2, 64, "bf16"), (32, 512, 2048, 8, 256, "f16"),
         (96, 512, 512, 2, 256, "f32"), (32, 512, 2048, 1, 2048, "f32"),
+        (32, 512, 2048, 2, 1024, "f32"), (32, 512, 2048, 8, 256, "f32"), (96, 512, 512, 8, 64, "f32"),
     ]
     two_kernels = [
         (256, 1024, 2048, 8, 256, "bf16"), (256, 1024, 2048, 16, 128, "bf16"),   # more than one cluster holds
         (96, 512, 2048, 16, 128, "bf16"), (32, 512, 2048, 16, 128, "f16"),
         (64, 128, 160, 3, 64, "bf16"),                                          # three splits
         (4096, 8192, 4096, 2, 2048, "bf16"),                                    # more tiles than resident clusters
-        (32, 512, 2048, 2, 1024, "f32"), (32, 512, 2048, 8, 256, "f32"),        # F32, M <= 32
-        (96, 512, 512, 8, 64, "f32"),                                           # F32, 8 splits
+        (32, 512, 2048, 16, 128, "f32"),
     ]
     for c in fused_in_kernel:
         d = sk.splitk_describe_launch(*c, fused=1)
