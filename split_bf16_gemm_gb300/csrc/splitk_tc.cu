@@ -1111,11 +1111,11 @@ struct StageChoice {
 // buffered, or all in flight, within `limit` bytes of shared memory, for a
 // cluster of q.
 StageChoice pick_stages(int bn, int nkb, bool can3d, int q, int share, bool x3 = false, int tm = kTileM,
-                        size_t limit = kSmemLimit, bool rir = false)
+                        size_t limit = kSmemLimit, bool rir = false, int max_kbs = kMaxKbs)
 {
     StageChoice r;
     for (int cand : {kMaxKbs, 2, 1}) {
-        if (!can3d && cand > 1) continue;
+        if ((!can3d && cand > 1) || cand > max_kbs) continue;
         if (g_override_kbs && cand != std::min(g_override_kbs, can3d ? kMaxKbs : 1)) continue;
         const int want = (nkb + cand - 1) / cand;
         int st = std::min(want, kMaxStages);
@@ -1398,13 +1398,17 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
         const int cols = cbn * cpc;   // tensor-memory columns of a CTA
         const int cshare = share_for(cbn, qc);
         const int cnkb = nkb * cpc;   // k-blocks of a CTA
+        // with several chunks a stage holds k-blocks of one chunk: at most
+        // the largest power of two dividing a chunk's k-blocks
+        const int mk = cpc > 1 ? std::min(kMaxKbs, nkb & -nkb) : kMaxKbs;
         const auto double_buffered = [&](const StageChoice &c) {
             return c.ok && c.stages >= std::min(2, (cnkb + c.kbs - 1) / c.kbs) && (cpc == 1 || nkb % c.kbs == 0);
         };
         StageChoice cc;
         if (qc <= 4 && cols <= 128 && (cctas > resident_clusters(1) / 2 || cpc > 1))
-            cc = pick_stages(cbn, cnkb, can3d, qc, cshare, x3, tm, kCompact3SmemLimit, qc > 1);
-        if (!double_buffered(cc)) cc = pick_stages(cbn, cnkb, can3d, qc, cshare, x3, tm, kCompactSmemLimit, qc > 1);
+            cc = pick_stages(cbn, cnkb, can3d, qc, cshare, x3, tm, kCompact3SmemLimit, qc > 1, mk);
+        if (!double_buffered(cc))
+            cc = pick_stages(cbn, cnkb, can3d, qc, cshare, x3, tm, kCompactSmemLimit, qc > 1, mk);
         if (!double_buffered(cc)) return false;
         // the staging area and the receive slots inside the ring, and the
         // shared memory the tensor-memory rule asks for (tmem_fits)
@@ -1466,7 +1470,8 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
         const int64_t cctas = row_tiles * (N / cbn);
         if (N % cbn || cols > 512 || (cols & (cols - 1)) || cctas > resident_clusters(1)) return false;
         const int cnkb = nkb * units;
-        StageChoice cc = pick_stages(cbn, cnkb, can3d, 1, share_for(cbn, 1), x3, tm, kSmemLimit, false);
+        StageChoice cc = pick_stages(cbn, cnkb, can3d, 1, share_for(cbn, 1), x3, tm, kSmemLimit, false,
+                                     std::min(kMaxKbs, nkb & -nkb));
         if (!cc.ok || cc.stages < std::min(2, (cnkb + cc.kbs - 1) / cc.kbs) || nkb % cc.kbs != 0) return false;
         p.compact = 1;
         p.bn = cbn;
