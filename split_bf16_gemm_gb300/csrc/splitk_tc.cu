@@ -315,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, Q <= 4 ? 3 : 2)
     float *const P = ops.P[grp];
     float *const out = ops.out[grp];
     // A CTA covers cpc consecutive (split, chunk) units, each summed in its
-    // own accumulator (cpc > 1 only for 16-bit, 128-row plans whose chunks
-    // are whole k-blocks of whole stages): one chunk, every chunk of a
+    // own accumulator (cpc > 1 only for 128-row plans whose chunks are whole
+    // k-blocks of whole stages): one chunk, two chunks or every chunk of a
     // split, or (whole_k) every chunk of every split, where the splits are
     // full and their chunks tile them.  The same products, chunk sums and
     // order as one CTA per chunk: the chunk sums (and with whole_k the split
@@ -1437,9 +1437,10 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
         return true;
     };
     // F32 (3xTF32) plans take the compact layout too (two CTAs per SM: their
-    // stages, with the lo halves, are twice as large), never merged: on
-    // GB300 F32 M96 N512 K512 went from 3.98 to 2.36 us per operation in
-    // graphs of eight, M256 N1024 K2048 S2 from 14.5 to 10.7 us.
+    // stages, with the lo halves, are twice as large): on GB300 F32 M96 N512
+    // K512 went from 3.98 to 2.36 us per operation in graphs of eight, M256
+    // N1024 K2048 S2 from 14.5 to 10.7 us.  They merge pairs of chunks like
+    // the 16-bit plans (64-column tiles; the 128-column ones do not fit).
     //
     // A fused plan of 64-column tiles and two chunks first tries 128-column
     // tiles with both chunks in a CTA (two 128-column accumulators, two CTAs
@@ -1491,7 +1492,7 @@ TilePlan plan_tc_uncached(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kp
         return true;
     };
     if (compact && tm == kTileM && bn <= 128) {
-        const bool mergeable = !x3 && split_sum == 2 && chunks > 1 && can3d && chunk_len % kBlockK == 0;
+        const bool mergeable = split_sum == 2 && chunks > 1 && can3d && chunk_len % kb_elems == 0;
         const bool whole = whole_ok && !x3 && split_sum == 2 && S > 1 && can3d && chunk_len % kBlockK == 0 &&
                            K == S * kps && kps == static_cast<int64_t>(chunks) * chunk_len;
         if (!(mergeable && bn == 64 && try_compact(2, 128)) && !(mergeable && bn == 64 && try_compact(2, 64)))
@@ -1579,12 +1580,13 @@ cudaError_t check_plan(const GemmProblem &pr, const TilePlan &plan)
     // memory columns in all), its chunks whole k-blocks of whole stages
     // (or every chunk of every split: full splits that the chunks tile, no cluster)
     const bool whole_k = plan.cpc > plan.chunks;
+    const int kbe = plan.x3 ? 32 : kBlockK;   // elements of a k-block
+    const bool pair = plan.cpc == 2 && plan.chunks % 2 == 0;
+    const bool whole = whole_k && !plan.x3 && plan.cpc == pr.S * plan.chunks && plan.cluster == 1 &&
+                       pr.K == pr.S * pr.kps && pr.kps == static_cast<int64_t>(plan.chunks) * plan.chunk_len;
     const bool cpc_ok = plan.cpc == 1 ||
-                        (((plan.cpc == 2 && plan.chunks % 2 == 0) || (whole_k && plan.cpc == pr.S * plan.chunks && plan.cluster == 1 &&
-                                                      pr.K == pr.S * pr.kps &&
-                                                      pr.kps == static_cast<int64_t>(plan.chunks) * plan.chunk_len)) &&
-                         !plan.x3 && plan.tile_m == kTileM && tmem_fits(plan.bn * plan.cpc, plan.smem_bytes) &&
-                         plan.chunk_len % kBlockK == 0 && (plan.chunk_len / kBlockK) % plan.kbs == 0 &&
+                        ((pair || whole) && plan.tile_m == kTileM && tmem_fits(plan.bn * plan.cpc, plan.smem_bytes) &&
+                         plan.chunk_len % kbe == 0 && (plan.chunk_len / kbe) % plan.kbs == 0 &&
                          static_cast<int64_t>(plan.grid.z) * plan.cpc == pr.S * plan.chunks);
     if (!cpc_ok) return note_error(cudaErrorInvalidConfiguration, "chunks per CTA out of range");
     if (plan.cluster > kMaxChunks || plan.stages > kMaxStages || plan.kbs < 1 || plan.kbs > kMaxKbs ||

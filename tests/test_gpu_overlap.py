@@ -423,8 +423,9 @@ def test_long_run_starts_a_new_window(lib):
 @pytest.mark.parametrize("fused", [0, 1])
 def test_f32_calls_overlap_bitwise(lib, shape, fused):
     """F32 operands (3xTF32) in graphs: the calls after the first overlap and
-    take the compact layout (two CTAs per SM, one chunk per CTA), and every
-    output is the eager one, bit for bit."""
+    take the compact layout (two CTAs per SM, a pair of chunks per CTA where
+    a split has two or more), and every output is the eager one, bit for
+    bit."""
     sk = lib
     M, N, K, S, kps = shape
     dt = "f32"
@@ -441,7 +442,10 @@ def test_f32_calls_overlap_bitwise(lib, shape, fused):
 
     g = capture(body)
     assert seen[0]["overlap"] == 0 and all(d["overlap"] == 2 for d in seen[1:]), seen
-    assert all(d["chunks_per_block"] == 1 for d in seen), seen
+    plan = sk.splitk_describe_launch(M, N, K, S, kps, dt, fused=fused)
+    cpc = 2 if plan["fused_in_kernel"] and plan["chunks"] % 2 == 0 else 1
+    assert plan["compact_chunks_per_block"] == cpc, plan
+    assert all(d["chunks_per_block"] == cpc for d in seen), seen
     if M * N <= 256 * 1024:
         assert all(d["compact"] == 1 for d in seen), seen
     for _ in range(2):

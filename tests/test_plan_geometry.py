@@ -204,7 +204,7 @@ def check_plan(sk, M, N, K, S, kps, fused, dt, bn=0, ch=0, kbs=0):
         # two consecutive chunks of a split in one block: only where the
         # chunks are whole stages of whole k-blocks, from 64-column tiles
         # (widened to 128 or not)
-        mergeable = not x3 and SS == 2 and C > 1 and can3d and CL % 64 == 0
+        mergeable = SS == 2 and C > 1 and can3d and CL % kb_elems == 0
         assert CB == BN or (CB == 128 and BN == 64 and cpc == 2 and mergeable), (BN, CB, cpc)
         assert cpc in (1, 2) and (cpc == 1 or (mergeable and BN == 64 and C % 2 == 0))
         assert qc == Q // cpc and d["compact_grid_z"] == S * C // cpc and d["compact_grid_z"] % qc == 0
