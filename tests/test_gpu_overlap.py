@@ -601,6 +601,8 @@ def test_grouped_kn_bitwise(grouping):
 @pytest.mark.parametrize("shape", [
     (128, 2048, 4096, 4, 1024),   # 16 whole-K blocks a call, one chunk per split
     (512, 1024, 4096, 2, 2048),   # 32 a call, two chunks per split
+    (224, 2048, 4096, 4, 1024),   # an M tail: the second row tile has 96 live rows
+    (96, 4096, 4096, 2, 2048),    # M below one tile
 ])
 @pytest.mark.parametrize("fused", [1, 3])
 def test_whole_k_calls_bitwise(grouping, shape, fused):
@@ -686,4 +688,32 @@ def test_grouped_f32_calls_bitwise(grouping, shape, fused):
         for it, w in zip(insts, refs_ws):
             P = S * M * N
             assert bitwise(it["ws"][:P], w[:P])
+    assert sk.splitk_get_device_status() == 0
+
+
+def test_whole_k_kn_bitwise(grouping):
+    """Whole-K blocks reading the [K,N] weight (MN-major operand), with an M
+    tail: bitwise the [N,K] path's eager results."""
+    sk = grouping
+    M, N, K, S, kps, dt = 352, 1024, 4096, 2, 2048, "bf16"
+    insts = instances(sk, M, N, K, S, kps, dt, 8)
+    for it in insts:
+        it["W"] = it["B"].t().contiguous()
+        sk.gemm_bt(it["A"], it["B"], it["ref"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=1)
+    torch.cuda.synchronize()
+    seen = []
+
+    def body():
+        for it in insts:
+            sk.gemm_kn(it["A"], it["W"], it["out"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=1)
+            seen.append(sk.splitk_last_launch())
+
+    g = capture(body)
+    C = sk.splitk_describe_launch(M, N, K, S, kps, dt, fused=1)["chunks"]
+    assert all(d["chunks_per_block"] == S * C and d["cluster"] == 1 for d in seen[1:]), seen
+    assert [d["group"] for d in seen] == list(range(1, 9)), seen
+    g.replay()
+    torch.cuda.synchronize()
+    for it in insts:
+        assert bitwise(it["out"], it["ref"])
     assert sk.splitk_get_device_status() == 0

@@ -356,6 +356,8 @@ def test_plan_geometry_random_and_large(lib):
     ((512, 1024, 4096, 2, 2048), True),
     ((128, 4096, 4096, 2, 2048), True),
     ((128, 4096, 8192, 4, 2048), True),
+    ((224, 2048, 4096, 4, 1024), True),    # an M tail
+    ((96, 4096, 4096, 2, 2048), True),     # M below one tile
     ((256, 1024, 1536, 2, 1024), False),   # the last split short: not full splits
     ((96, 512, 2048, 4, 512), False),      # 2 chunks x 4 splits: 1024 columns
 ])
