@@ -1161,19 +1161,20 @@ double model_us(int64_t M, int64_t N, int64_t S, int bn, int chunks, int64_t chu
 }  // namespace
 
 // Estimated microseconds per call of one tensor-core launch in a stream of
-// such calls inside a graph (where independent calls overlap): each CTA lives
-// for its loads (per-CTA TMA intake ~92 GB/s), its exchange over distributed
-// shared memory (~11 GB/s per CTA, contended) and its stores (~1.5 TB/s), and
-// the GPU keeps 148 x (CTAs per SM) of them at once -- the compact layout's
-// two or three for fused calls (with every chunk of a split in one CTA where
-// the plan allows it), otherwise what shared memory allows, at most two (the
-// reduce's blocks share the SMs with the partial pass) -- plus a fixed
-// 1.29 us.  Fitted on GB300 to 106 measured candidates (BF16, 12 shapes from
-// M32 N64 K128 to M8192 N8192 K8192, fused and two kernels, 1 to 16 splits):
-// median error 8%, at most 1.4x.
+// such calls inside a graph (where independent calls overlap): the layout a
+// graph gives it (compact, and for a fused call that follows another, merged
+// chunks or whole-K blocks), each CTA living for its loads (per-CTA TMA
+// intake ~99 GB/s), its exchange over distributed shared memory (~7.5 GB/s
+// per CTA, contended) and its stores (~77 GB/s), the GPU keeping 148 x (CTAs
+// per SM) of them at once -- three, two or one by the compact plan's shared
+// memory, otherwise what shared memory allows, at most two -- plus a fixed
+// 1.53 us, less 0.17 us per doubling of the cluster.  Fitted on GB300 to 110
+// measured candidates (BF16, 12 shapes from M32 N64 K128 to M8192 N8192
+// K8192, fused and two kernels, 1 to 16 splits, graphs of the same call):
+// median error 6%, at most 1.42x.
 double estimate_tc_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3)
 {
-    const TilePlan p = plan_tc(M, N, K, S, kps, fused, x3, fused);
+    const TilePlan p = plan_tc(M, N, K, S, kps, fused, x3, true, fused);
     const double elem = x3 ? 4.0 : 2.0;
     const double ctas = static_cast<double>(p.grid.x) * p.grid.y * p.grid.z;
     const double acc = static_cast<double>(kTileM) * p.bn * 4;
@@ -1181,12 +1182,13 @@ double estimate_tc_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, b
     const double exchange = p.cluster > 1 ? acc * (p.cluster - 1) / p.cluster : 0.0;
     const double store = acc / p.cluster;
     int per_sm;
-    if (fused && p.compact)
-        per_sm = p.smem_bytes <= kCompact3SmemLimit + 1024 ? 3 : 2;
+    if (p.compact)
+        per_sm = p.smem_bytes <= kCompact3SmemLimit + 1024 ? 3 : (p.smem_bytes <= kCompactSmemLimit + 1024 ? 2 : 1);
     else
         per_sm = std::max(1, std::min(2, static_cast<int>((228 * 1024) / (p.smem_bytes + 1024 + 256))));
-    const double cta_us = load / 9.235e4 + exchange / 1.108e4 + store / 1.535e6;
-    return 1.287 + cta_us * ctas / (static_cast<double>(resident_clusters(1)) * per_sm);
+    const double cta_us = load / 9.864e4 + exchange / 7.468e3 + store / 7.665e4;
+    return 1.534 - 0.1686 * std::log2(static_cast<double>(p.cluster)) +
+           cta_us * ctas / (static_cast<double>(resident_clusters(1)) * per_sm);
 }
 
 namespace {

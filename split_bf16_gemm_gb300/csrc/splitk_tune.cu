@@ -53,12 +53,12 @@ int elem_size(int dtype)
 
 // Estimated microseconds per gemm_bt call in a graph of such calls: the
 // tensor-core launch, plus for the two-kernel path (fused == 0, or a fused
-// call that runs the two kernels) the reduce: 0.95 us, its bytes at ~3.0 TB/s
-// and 0.062 us per split (fitted with the launch model in splitk_tc.cu).
+// call that runs the two kernels) the reduce: 0.90 us, its bytes at ~3.2 TB/s
+// and 0.047 us per split (fitted with the launch model in splitk_tc.cu).
 double estimate_us(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, int dtype, int fused)
 {
     const bool in_kernel = fused != 0 && splitk::fused_in_kernel(M, N, K, S, kps, dtype, false);
-    const double reduce = 0.953 + static_cast<double>(S + 1) * M * N * 4 / 2.978e6 + 0.0623 * static_cast<double>(S);
+    const double reduce = 0.9016 + static_cast<double>(S + 1) * M * N * 4 / 3.192e6 + 0.0473 * static_cast<double>(S);
     return splitk::estimate_tc_us(M, N, K, S, kps, in_kernel, dtype == SPLITK_F32) + (in_kernel ? 0.0 : reduce);
 }
 
