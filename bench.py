@@ -71,8 +71,10 @@ def code_of(text: str) -> str:
 
 def kernel_traffic(ops_per_launch=1):
     """DRAM bytes per launch of the tensor-core kernel from the committed ncu
-    record, or None when the kernel's code changed since it was taken or the
-    record's launches computed another number of operations."""
+    record, or None when the kernel's code changed since it was taken (the
+    record's sources without comments, each up to the record's end-of-device-
+    code marker where it has one) or the record's launches computed another
+    number of operations."""
     import hashlib
 
     path = os.path.join(ROOT, "profiles", "tc_splitk_traffic.txt")
@@ -85,9 +87,13 @@ def kernel_traffic(ops_per_launch=1):
                 k, v = line.split("=", 1)
                 rec[k.strip()] = v.strip()
     h = hashlib.sha256()
+    cut = rec.get("device_code_ends_at", "")
     for src in rec.get("sources", "").split():
         with open(os.path.join(ROOT, src)) as f:
-            h.update(code_of(f.read()).encode())
+            text = code_of(f.read())
+        if cut and cut in text:   # the device code only: the host planner below may change
+            text = text[:text.index(cut)]
+        h.update(text.encode())
     if h.hexdigest() != rec.get("code_sha256") or int(rec.get("ops_per_launch", 1)) != ops_per_launch:
         return None
     return int(rec["dram_bytes_per_launch"])
