@@ -64,8 +64,8 @@ constexpr int kMaxGroup = 8;   // independent calls one launch may compute (grap
 // x3: F32 operands as 3xTF32 (else 16-bit operands).
 // compact: the layout that lets two or three CTAs share an SM, where that
 // plan exists (plan.compact says whether it was taken).
-// A fused compact plan may give each CTA all the chunks of its split
-// (plan.cpc > 1); with whole_k, for a launch that follows another, every
+// A fused compact plan may give each CTA two consecutive chunks of its split
+// (plan.cpc == 2); with whole_k, for a launch that follows another, every
 // chunk of every split (plan.cpc > plan.chunks, no cluster) where the
 // compact plan would take more than half the SMs.
 TilePlan plan_tc(int64_t M, int64_t N, int64_t K, int64_t S, int64_t kps, bool fused, bool x3 = false,

@@ -8,9 +8,9 @@
 // "Launch contract and correctness").  Optionally the same launch also sums
 // the splits into out[m,n] (the pages' separate accumulation pass, fused).
 //
-// One CTA (256 threads, 8 warps) owns a TM x BN output tile of one K-chunk, or
-// of both chunks of its split, each in its own accumulator (TM = 128, or 256
-// as below):
+// One CTA (256 threads, 8 warps) owns a TM x BN output tile of one K-chunk, of
+// two consecutive chunks of its split, or (whole-K) of every chunk of every
+// split, each chunk in its own accumulator (TM = 128, or 256 as below):
 //   thread 0       TMA producer: per stage, kbs 64-wide k-blocks of A (TM
 //                  rows) and of B (BN rows), 128-byte swizzled, into a ring
 //                  of `stages` buffers; the first stages go out before tensor
@@ -55,7 +55,10 @@
 // before one CTA of the grid finishes (the grids still finish in launch
 // order).  Consecutive independent operations then run side by side, two or
 // three CTAs to an SM in the compact layout (a ring cut to fit, that also
-// receives the peers' shares), where a CTA may take both chunks of its split.
+// receives the peers' shares), where a CTA may take two chunks of its split
+// or, for large shapes, the whole K range; consecutive calls of one shape may
+// also join one launch of the grouped kernel (G problems, found from
+// blockIdx.y), whose graph node the host rewrites as calls join it.
 //
 // Every mbarrier wait has a time limit; on time-out the kernel records a bit
 // in g_device_status, drains its own loads in flight, still sends and awaits
@@ -112,7 +115,7 @@ struct TcArgs {
                            // wait before the first store; 2: load and store at once, wait
                            // before finishing (no launch in flight reads or writes the outputs)
     int recv_in_ring;      // the peers' shares land in the stage ring, once its MMAs are done
-    int cpc;               // chunks per CTA: 1, or every chunk of a split, each in its own accumulator
+    int cpc;               // chunks per CTA: 1, 2, or (whole-K) every chunk of every split, each in its own accumulator
 };
 
 // Part j of `parts` (whole 128-byte lines) of [p, p + bytes) into L2, one

@@ -6,14 +6,15 @@ launch that can still be running writes what the new one reads (overlap 1);
 it also stores before that grid ends only where none of them reads or
 writes what the new one writes (overlap 2), and every launch still waits for
 the previous grid before it finishes.  A fused launch that overlaps may give
-each thread block all the chunks of its split (chunks_per_block > 1), or
-where the splits are full, after the first call, every chunk of every split
-(no cluster), with the same sums.  Each test captures a sequence of calls, checks which launches
-overlapped (splitk_last_launch, read right after each call), replays the
-graph several times and compares every output bitwise with the same calls
-made eagerly, where each launch waits for the one before it.  The eager results themselves are pinned to the
-F64 oracle by test_gpu_parity.py; the headline case is checked against the
-oracle here too.
+each thread block two consecutive chunks of its split (chunks_per_block 2),
+or where the splits are full, after the first call, every chunk of every
+split (no cluster), with the same sums; consecutive calls of one shape may
+join one launch (group).  Each test captures a sequence of calls, checks
+which launches overlapped (splitk_last_launch, read right after each call),
+replays the graph several times and compares every output bitwise with the
+same calls made eagerly, where each launch waits for the one before it.  The
+eager results themselves are pinned to the F64 oracle by test_gpu_parity.py;
+the headline case is checked against the oracle here too.
 """
 import numpy as np
 import pytest
