@@ -718,3 +718,73 @@ def test_whole_k_kn_bitwise(grouping):
     for it in insts:
         assert bitwise(it["out"], it["ref"])
     assert sk.splitk_get_device_status() == 0
+
+
+def random_graph_cases(n, seed=77):
+    """Seeded shapes for graphs of independent calls: full splits (K = S * kps,
+    where whole-K blocks may apply) and short last splits, 1 to 8 splits, all
+    three element types, both weight layouts for 16-bit operands."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    cases = []
+    while len(cases) < n:
+        M = 32 * int(rng.integers(1, 17))          # 32 .. 512
+        N = 64 * int(rng.integers(1, 33))          # 64 .. 2048
+        S = int(rng.choice([1, 2, 3, 4, 8]))
+        kps = 64 * int(rng.integers(1, 33))        # 64 .. 2048
+        short = 32 * int(rng.integers(0, kps // 32)) if rng.integers(0, 2) else 0
+        K = S * kps - short
+        if (S - 1) * kps >= K:
+            continue
+        dt = ("bf16", "f16", "f32")[int(rng.integers(0, 3))]
+        kn = dt != "f32" and bool(rng.integers(0, 2))
+        fused = (1, 3)[int(rng.integers(0, 2))]
+        cases.append((M, N, K, S, kps, dt, kn, fused))
+    return cases
+
+
+GRAPH_CASES = random_graph_cases(16) + [
+    (224, 2048, 4096, 4, 1024, "bf16", True, 3),   # whole-K blocks: [K,N] weight, kept partials, M tail
+    (512, 1024, 4096, 2, 2048, "f16", False, 1),
+    (96, 4096, 4096, 2, 2048, "bf16", True, 1),
+    (352, 1024, 4096, 2, 2048, "f16", True, 3),
+]
+
+
+@pytest.mark.parametrize("case", GRAPH_CASES,
+                         ids=[f"{c[5]}{'-kn' if c[6] else ''}-M{c[0]}N{c[1]}K{c[2]}S{c[3]}-f{c[7]}" for c in GRAPH_CASES])
+def test_random_graphs_bitwise(grouping, case):
+    """Six independent calls of a random shape captured into one graph
+    (grouping on: joined launches, merged chunks, whole-K blocks and the
+    conversion of a run's first launch wherever the planner takes them):
+    every output, and the partials kept with fused=3, bitwise the same calls
+    made eagerly."""
+    sk = grouping
+    M, N, K, S, kps, dt, kn, fused = case
+    insts = instances(sk, M, N, K, S, kps, dt, 6, seed0=M + N + K)
+    call = sk.gemm_kn if kn else sk.gemm_bt
+    for it in insts:
+        if kn:
+            it["B"] = it["B"].t().contiguous()   # the [K,N] weight itself
+        call(it["A"], it["B"], it["ref"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=fused)
+    torch.cuda.synchronize()
+    refs_ws = [it["ws"].clone() for it in insts]
+    seen = []
+
+    def body():
+        for it in insts:
+            call(it["A"], it["B"], it["out"], it["ws"], it["nb"], M, N, K, S, kps, dt, fused=fused)
+            seen.append(sk.splitk_last_launch())
+
+    g = capture(body)
+    assert all(d["capturing"] == 1 for d in seen), seen
+    for _ in range(2):
+        for it in insts:
+            it["out"].fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        for i, it in enumerate(insts):
+            assert bitwise(it["out"], it["ref"]), (i, seen[i])
+    if fused == 3:
+        for it, w in zip(insts, refs_ws):
+            assert bitwise(it["ws"][:S * M * N], w[:S * M * N])
+    assert sk.splitk_get_device_status() == 0
