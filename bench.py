@@ -88,11 +88,14 @@ def kernel_traffic(ops_per_launch=1):
                 rec[k.strip()] = v.strip()
     h = hashlib.sha256()
     cut = rec.get("device_code_ends_at", "")
+    constants_only = set(rec.get("constants_only", "").split())
     for src in rec.get("sources", "").split():
         with open(os.path.join(ROOT, src)) as f:
             text = code_of(f.read())
         if cut and cut in text:   # the device code only: the host planner below may change
             text = text[:text.index(cut)]
+        if src in constants_only:  # a host header: only the constants the kernel is built from
+            text = "\n".join(line for line in text.splitlines() if line.startswith("constexpr"))
         h.update(text.encode())
     if h.hexdigest() != rec.get("code_sha256") or int(rec.get("ops_per_launch", 1)) != ops_per_launch:
         return None

@@ -146,12 +146,17 @@ int run_partial_pass(const void *A, const void *B, float *P, float *out, int64_t
     // a call that touches nothing in flight, with the same shape and plan as
     // the launch before it, joins that launch (no node added)
     int group = 1, mode = pr.overlap ? (pr.store_early ? 2 : 1) : 0;
+    bool broken = false;
     if (pr.store_early && splitk::grouping_enabled() &&
-        splitk::join_group(pr, plan, chain.capture_id(), chain.dep_node(), &group, &mode)) {
+        splitk::join_group(pr, plan, chain.capture_id(), chain.dep_node(), &group, &mode, &broken)) {
         chain.commit_joined();
         splitk::note_launch({mode, plan.compact, 1, plan.bn, plan.chunks, plan.stages, plan.kbs,
                              static_cast<int>(plan.smem_bytes), plan.cpc, plan.cluster, group});
         return SPLITK_OK;
+    }
+    if (broken) {   // the captured graph holds an inconsistent node (last error says which)
+        chain.commit(false, false);
+        return SPLITK_ERR_CUDA;
     }
     const cudaError_t err = chain.capturing() && splitk::grouping_enabled()
                                 ? splitk::launch_tc_grouped(pr, plan, stream, chain.capture_id())

@@ -88,7 +88,7 @@ bool head_groupable(const GemmProblem &p, const TilePlan &plan);
 // current dependency), if it has the same shape and plan and room; returns
 // whether it did (and the launch's problem count in *group_size).
 bool join_group(const GemmProblem &p, const TilePlan &plan, unsigned long long capture, cudaGraphNode_t dep,
-                int *group_size, int *mode);
+                int *group_size, int *mode, bool *broken);
 // One launch computing n (1..kMaxGroup) independent problems of one shape
 // with the plan (compact, groupable), outside a capture: the grouped kernel
 // with every problem given at once.

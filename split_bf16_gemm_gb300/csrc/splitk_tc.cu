@@ -1836,7 +1836,7 @@ namespace {
 // node gets that plan's kernel, cluster size, grid and shared memory and both
 // problems.  Where a step fails the node is left as it was (its cluster
 // attribute restored) and the call launches on its own.
-bool convert_head(GroupState &st, const GemmProblem &pr, const TilePlan &plan)
+bool convert_head(GroupState &st, const GemmProblem &pr, const TilePlan &plan, bool *broken)
 {
     if (st.n != 1 || !groupable(pr, plan)) return false;
     const GemmProblem &h = st.head;
@@ -1855,17 +1855,15 @@ bool convert_head(GroupState &st, const GemmProblem &pr, const TilePlan &plan)
     if (grouped_op(GroupedOp::kFunc, plan, h.b_kn, &func) != cudaSuccess ||
         grouped_op(GroupedOp::kPrepare, plan, h.b_kn, nullptr) != cudaSuccess || func == nullptr)
         return false;
-    cudaLaunchAttributeValue old = {}, one = {};
-    if (cudaGraphKernelNodeGetAttribute(st.node, cudaLaunchAttributeClusterDimension, &old) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return false;
-    }
-    one.clusterDim.x = one.clusterDim.y = 1;
-    one.clusterDim.z = static_cast<unsigned>(plan.cluster);
-    if (cudaGraphKernelNodeSetAttribute(st.node, cudaLaunchAttributeClusterDimension, &one) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return false;
-    }
+    // the node's launch before: restored if the cluster attribute cannot be
+    // changed after the parameters were
+    cudaKernelNodeParams before = {};
+    before.func = st.func;
+    before.gridDim = dim3(st.plan.grid.x, st.plan.grid.y * static_cast<unsigned>(st.n), st.plan.grid.z);
+    before.blockDim = dim3(kThreads, 1, 1);
+    before.sharedMemBytes = static_cast<unsigned>(st.smem);
+    void *before_params[2] = {&st.ops, &st.args};
+    before.kernelParams = before_params;
     cudaKernelNodeParams kp = {};
     kp.func = func;
     kp.gridDim = dim3(plan.grid.x, plan.grid.y * 2u, plan.grid.z);
@@ -1874,11 +1872,22 @@ bool convert_head(GroupState &st, const GemmProblem &pr, const TilePlan &plan)
     void *params[2] = {&ops, &a};
     kp.kernelParams = params;
     kp.extra = nullptr;
-    if (cudaGraphKernelNodeSetParams(st.node, &kp) != cudaSuccess) {
+    if (cudaGraphKernelNodeSetParams(st.node, &kp) != cudaSuccess) {   // the node is as it was
         (void)cudaGetLastError();
-        if (cudaGraphKernelNodeSetAttribute(st.node, cudaLaunchAttributeClusterDimension, &old) != cudaSuccess)
-            (void)cudaGetLastError();
         st.valid = false;
+        return false;
+    }
+    cudaLaunchAttributeValue one = {};
+    one.clusterDim.x = one.clusterDim.y = 1;
+    one.clusterDim.z = static_cast<unsigned>(plan.cluster);
+    if (cudaGraphKernelNodeSetAttribute(st.node, cudaLaunchAttributeClusterDimension, &one) != cudaSuccess) {
+        (void)cudaGetLastError();
+        st.valid = false;
+        if (cudaGraphKernelNodeSetParams(st.node, &before) != cudaSuccess) {
+            (void)cudaGetLastError();
+            *broken = true;   // new kernel, old cluster size: the capture must not be used
+            note_error(cudaErrorUnknown, "grouped launch: graph node left with a mismatched cluster size");
+        }
         return false;
     }
     st.plan = plan;
@@ -1893,8 +1902,9 @@ bool convert_head(GroupState &st, const GemmProblem &pr, const TilePlan &plan)
 }  // namespace
 
 bool join_group(const GemmProblem &pr, const TilePlan &plan, unsigned long long capture, cudaGraphNode_t dep,
-                int *group_size, int *mode)
+                int *group_size, int *mode, bool *broken)
 {
+    *broken = false;
     if (!groupable(pr, plan) || capture == 0 || dep == nullptr) return false;
     if (check_plan(pr, plan) != cudaSuccess) return false;
     std::lock_guard<std::mutex> lock(g_group_mu);
@@ -1907,7 +1917,7 @@ bool join_group(const GemmProblem &pr, const TilePlan &plan, unsigned long long 
                             st->keep_p == (pr.P != nullptr) && (st->head.out != nullptr) == (pr.out != nullptr);
     if (!same_shape) return false;
     if (!same_plan(st->plan, plan)) {
-        if (!convert_head(*st, pr, plan)) return false;
+        if (!convert_head(*st, pr, plan, broken)) return false;
         st->stamp = ++g_group_clock;
         if (group_size) *group_size = st->n;
         if (mode) *mode = st->overlap ? (st->store_early ? 2 : 1) : 0;
