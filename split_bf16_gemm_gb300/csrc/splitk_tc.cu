@@ -1835,7 +1835,8 @@ namespace {
 // that launch to its own plan (compact, or whole-K blocks) and joins it: the
 // node gets that plan's kernel, cluster size, grid and shared memory and both
 // problems.  Where a step fails the node is left as it was (its cluster
-// attribute restored) and the call launches on its own.
+// attribute restored) and the call launches on its own; should the restore
+// itself fail, *broken tells the caller, whose call then fails.
 bool convert_head(GroupState &st, const GemmProblem &pr, const TilePlan &plan, bool *broken)
 {
     if (st.n != 1 || !groupable(pr, plan)) return false;
@@ -1855,15 +1856,20 @@ bool convert_head(GroupState &st, const GemmProblem &pr, const TilePlan &plan, b
     if (grouped_op(GroupedOp::kFunc, plan, h.b_kn, &func) != cudaSuccess ||
         grouped_op(GroupedOp::kPrepare, plan, h.b_kn, nullptr) != cudaSuccess || func == nullptr)
         return false;
-    // the node's launch before: restored if the cluster attribute cannot be
-    // changed after the parameters were
-    cudaKernelNodeParams before = {};
-    before.func = st.func;
-    before.gridDim = dim3(st.plan.grid.x, st.plan.grid.y * static_cast<unsigned>(st.n), st.plan.grid.z);
-    before.blockDim = dim3(kThreads, 1, 1);
-    before.sharedMemBytes = static_cast<unsigned>(st.smem);
-    void *before_params[2] = {&st.ops, &st.args};
-    before.kernelParams = before_params;
+    // The cluster size first: the new size divides the launch's current grid
+    // (a cluster holds the splits and chunks of a tile, fewer of them once
+    // merged), so the node is valid in between; the new parameters then.
+    cudaLaunchAttributeValue old = {}, one = {};
+    if (cudaGraphKernelNodeGetAttribute(st.node, cudaLaunchAttributeClusterDimension, &old) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    one.clusterDim.x = one.clusterDim.y = 1;
+    one.clusterDim.z = static_cast<unsigned>(plan.cluster);
+    if (cudaGraphKernelNodeSetAttribute(st.node, cudaLaunchAttributeClusterDimension, &one) != cudaSuccess) {
+        (void)cudaGetLastError();   // the node is as it was
+        return false;
+    }
     cudaKernelNodeParams kp = {};
     kp.func = func;
     kp.gridDim = dim3(plan.grid.x, plan.grid.y * 2u, plan.grid.z);
@@ -1872,20 +1878,12 @@ bool convert_head(GroupState &st, const GemmProblem &pr, const TilePlan &plan, b
     void *params[2] = {&ops, &a};
     kp.kernelParams = params;
     kp.extra = nullptr;
-    if (cudaGraphKernelNodeSetParams(st.node, &kp) != cudaSuccess) {   // the node is as it was
+    if (cudaGraphKernelNodeSetParams(st.node, &kp) != cudaSuccess) {
         (void)cudaGetLastError();
         st.valid = false;
-        return false;
-    }
-    cudaLaunchAttributeValue one = {};
-    one.clusterDim.x = one.clusterDim.y = 1;
-    one.clusterDim.z = static_cast<unsigned>(plan.cluster);
-    if (cudaGraphKernelNodeSetAttribute(st.node, cudaLaunchAttributeClusterDimension, &one) != cudaSuccess) {
-        (void)cudaGetLastError();
-        st.valid = false;
-        if (cudaGraphKernelNodeSetParams(st.node, &before) != cudaSuccess) {
+        if (cudaGraphKernelNodeSetAttribute(st.node, cudaLaunchAttributeClusterDimension, &old) != cudaSuccess) {
             (void)cudaGetLastError();
-            *broken = true;   // new kernel, old cluster size: the capture must not be used
+            *broken = true;   // old kernel, new cluster size: the capture must not be used
             note_error(cudaErrorUnknown, "grouped launch: graph node left with a mismatched cluster size");
         }
         return false;
