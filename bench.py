@@ -514,10 +514,22 @@ def run_ours(args, rank, world, dev, torch, dist):
         sk.splitk_reduce(inst["ws"], inst["out"], SPLITS, M, N, stream=stream)
 
     torch.cuda.synchronize()
-    graphs = [capture(torch, stream, lambda grp=grp: [op(i) for i in grp]) for grp in groups]
+    # each call's tensor-core launch as captured: a call that starts a launch
+    # reports group 1, one that joins the launch before it a larger group
+    joined = []
+
+    def op_recorded(inst):
+        op(inst)
+        joined.append(sk.splitk_last_launch()["group"])
+
+    graphs = [capture(torch, stream, lambda grp=grp: [op_recorded(i) for i in grp]) for grp in groups]
     # the operations the last captured launch computes: a step's calls join
     # one launch where they can (group), so a launch is a whole step
-    ops_per_launch = sk.splitk_last_launch()["group"]
+    ops_per_launch = joined[-1]
+    # kernels one step launches: the tensor-core launches the step's calls
+    # started, plus a reduce per call where the splits are summed apart
+    tc_per_step = sum(1 for g in joined[-pack:] if g == 1)
+    launches_per_step = tc_per_step + (pack if plan["kernels_per_call"] == 2 else 0)
 
     # sanity before timing: the fused and two-kernel paths agree bitwise
     inst = pool[0]
@@ -665,6 +677,7 @@ def run_ours(args, rank, world, dev, torch, dist):
                    "l2": f"inputs larger than L2: {n_inst} distinct instances, "
                          f"{n_inst * (M * K + N * K) * 2 / 1e6:.0f} MB of A+B, cycled",
                    "timing": "CUDA graph per step, CUDA events on the launching stream",
+                   "launches_per_step": launches_per_step,
                    "plan": plan},
         "tflops": round(FLOPS_PER_OP / (us_per_op * 1e-6) / 1e12 / 1, 2),
         "op_roofline": {
@@ -715,7 +728,7 @@ def run_ours(args, rank, world, dev, torch, dist):
                    "before_timing": {"outputs": before[1], "max_scaled_err": float(f"{before[0]:.3e}")},
                    "after_timing": {"outputs": after[1], "max_scaled_err": float(f"{after[0]:.3e}")}},
         "configs": configs,
-        "gpu_launches": args.steps * pack * plan["kernels_per_call"],
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
     }
     return line
