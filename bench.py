@@ -630,6 +630,30 @@ def run_ours(args, rank, world, dev, torch, dist):
     for inst in pool:
         del inst["W"]
 
+    # the same operations eagerly (no graph): one gemm_bt call each, or a
+    # step's calls as one gemm_bt_batch call (grouped launches)
+    ptrs = [tuple(sk.pointer_array([i[k] for i in grp]) for k in ("A", "B", "out")) for grp in groups]
+    eager_us = {}
+    for name in ("calls", "batch"):
+        def eager_step(g):
+            if name == "batch":
+                sk.gemm_bt_batch(*ptrs[g], pack, pool[0]["ws"], nbytes, M, N, K, SPLITS, KPS, DTYPE, fused=fused,
+                                 stream=stream)
+            else:
+                for inst in groups[g]:
+                    op(inst)
+        for g in range(len(groups)):
+            eager_step(g)
+        torch.cuda.synchronize()
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for r in range(reps):
+                eager_step(r % len(groups))
+            stop.record(stream)
+        stop.synchronize()
+        eager_us[name] = round(start.elapsed_time(stop) * 1e3 / (reps * pack), 4)
+
     # weight preparation (B = W^T), a one-shot cost outside the operation
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     prep_n = 24
@@ -715,6 +739,8 @@ def run_ours(args, rank, world, dev, torch, dist):
                    "the grid finishes; kernels_us.fused_op_every_launch_waits is the same graphs with "
                    "that turned off",
         "e2e": e2e,
+        "eager": {"what": "the same operations outside a graph: one gemm_bt per operation (every launch waits "
+                           "for the one before), or each step's 8 as one gemm_bt_batch call", "us": eager_us},
         "kn_layout": {"what": "the same operations with the weight in its [K,N] layout (gemm_kn, MN-major B)",
                       "us": kn_us},
         "prepare": {"what": "weight preparation B[N,K] = W[K,N]^T (one-shot, outside the operation); "

@@ -229,6 +229,31 @@ int gemm_bt_noalloc(const void *A, const void *B, float *out, int64_t M,
                     int64_t N, int64_t K, int64_t splits, int64_t k_per_split,
                     int dtype, int fused, void *stream);
 
+/* `count` independent operations out_i = gemm_bt(A_i, B_i) of one shape on
+ * device buffers, enqueued on `stream` in as few launches as the plan
+ * allows.  The pages time eight complete operations per replay ("pack 8":
+ * "Aligned shared rows for pipelined NAX on CUDA", section "Measurement
+ * protocol"); outside a graph capture this call gives such a pack the
+ * grouped launches a capture would.
+ *   A, B, out   host arrays of `count` DEVICE pointers: activations [M,K],
+ *               prepared weights [N,K] (entries may repeat, as may A's) and
+ *               outputs [M,N] F32, each fully overwritten
+ *   workspace   device, >= gemm_bt_workspace_bytes() bytes: scratch for the
+ *               operations that run the two kernels, used one after another
+ *   count       1 .. 65536
+ *   fused       0 or 1 (as for gemm_bt; fused = 1 calls whose splits are
+ *               summed inside the launch run up to 8 to a launch, BF16/F16
+ *               with a compact plan; everything else one gemm_bt each)
+ * Every result is bitwise that of gemm_bt(fused) on the same operands.
+ * Returns as gemm_bt's validation would for each operation, plus
+ * SPLITK_ERR_CONFIG for count outside [1, 65536] or fused not 0 or 1, and
+ * SPLITK_ERR_ALIAS when an output overlaps another output, an input or the
+ * workspace; nothing is enqueued unless every operation passes. */
+int gemm_bt_batch(const void *const *A, const void *const *B, float *const *out,
+                  int64_t count, void *workspace, size_t workspace_bytes,
+                  int64_t M, int64_t N, int64_t K, int64_t splits,
+                  int64_t k_per_split, int dtype, int fused, void *stream);
+
 /* Device staging bytes gemm_bt_host_batch needs for `count` operations of
  * this shape: count A slots [M,K], count output slots [M,N] F32 and one
  * gemm_bt workspace.  Returns 0 for a rejected geometry or element type, or

@@ -8,7 +8,7 @@ F32); this package is its build step and a thin ctypes binding.
 """
 from ._build import LIB_PATH, build  # noqa: F401
 from .binding import (  # noqa: F401
-    BF16, F16, F32, SplitKError, dtype_code, gemm_bt, gemm_bt_host_batch, gemm_bt_host_staging_bytes,
+    BF16, F16, F32, SplitKError, dtype_code, gemm_bt, gemm_bt_batch, gemm_bt_host_batch, gemm_bt_host_staging_bytes,
     gemm_bt_noalloc, gemm_bt_workspace_bytes, gemm_bt_workspace_init, gemm_kn, gemm_splitk_kn, pointer_array,
     gemm_splitk_bt,
     lib, splitk_check_geometry, splitk_describe_launch, splitk_get_device_status, splitk_reduce,

@@ -28,6 +28,7 @@ EXPORTS = (
     "gemm_bt_workspace_init", "gemm_bt_noalloc", "splitk_prepare_bt",
     "gemm_bt_host_staging_bytes", "gemm_bt_host_batch", "splitk_choose_splits", "splitk_autotune_splits",
     "gemm_splitk_kn", "gemm_kn", "splitk_set_overlap", "splitk_last_launch", "splitk_selftest_kernel_timeout",
+    "gemm_bt_batch",
 )
 NOALLOC_MAX_BYTES = 32 << 20   # SPLITK_NOALLOC_MAX_BYTES
 
@@ -60,6 +61,7 @@ def lib() -> ctypes.CDLL:
             L.gemm_bt_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i32]
             L.gemm_bt_workspace_bytes.restype = sz
             L.gemm_bt.argtypes = [vp, vp, vp, vp, sz, i64, i64, i64, i64, i64, i32, i32, vp]
+            L.gemm_bt_batch.argtypes = [vp, vp, vp, i64, vp, sz, i64, i64, i64, i64, i64, i32, i32, vp]
             L.gemm_splitk_kn.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, vp]
             L.gemm_kn.argtypes = [vp, vp, vp, vp, sz, i64, i64, i64, i64, i64, i32, i32, vp]
             L.splitk_get_device_status.argtypes = [vp]
@@ -221,6 +223,17 @@ def gemm_bt_host_batch(A_host, B, out_host, count, staging, staging_bytes, M, N,
                                     _ptr(staging), staging_bytes, M, N, K, splits, k_per_split,
                                     dtype_code(dtype), fused, ops_per_copy, _stream(stream)),
            "gemm_bt_host_batch")
+
+
+def gemm_bt_batch(A, B, out, count, workspace, workspace_bytes, M, N, K, splits, k_per_split, dtype, fused=0,
+                  stream=None) -> None:
+    """`count` operations out[i] = gemm_bt(A[i], B[i]) of one shape; A, B and
+    out: sequences of device tensors (or addresses), or prebuilt
+    pointer_array()s."""
+    arrs = [x if isinstance(x, ctypes.Array) else pointer_array(x) for x in (A, B, out)]
+    _check(lib().gemm_bt_batch(*(ctypes.cast(a, ctypes.c_void_p) for a in arrs), count, _ptr(workspace),
+                               workspace_bytes, M, N, K, splits, k_per_split, dtype_code(dtype), fused,
+                               _stream(stream)), "gemm_bt_batch")
 
 
 SPLIT_CANDIDATES = (1, 2, 4, 8, 16)

@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <vector>
 #include <cstdio>
 
 #include "splitk.h"
@@ -371,6 +372,58 @@ int gemm_bt(const void *A, const void *B, float *out, void *workspace, size_t wo
             int64_t K, int64_t splits, int64_t k_per_split, int dtype, int fused, void *stream)
 {
     return gemm_impl(A, B, out, workspace, workspace_bytes, M, N, K, splits, k_per_split, dtype, fused, false, stream);
+}
+
+int gemm_bt_batch(const void *const *A, const void *const *B, float *const *out, int64_t count, void *workspace,
+                  size_t workspace_bytes, int64_t M, int64_t N, int64_t K, int64_t splits, int64_t k_per_split,
+                  int dtype, int fused, void *stream)
+{
+    if (count < 1 || count > (int64_t(1) << 16) || (fused != 0 && fused != 1)) return SPLITK_ERR_CONFIG;
+    if (!A || !B || !out) return SPLITK_ERR_NULL;
+    // every operation as gemm_bt would check it, then the outputs against one
+    // another, every input and the workspace (sorted ranges: an output may
+    // overlap nothing; inputs may overlap inputs)
+    std::vector<std::pair<Range, bool>> ranges;   // (bytes, is an output)
+    ranges.reserve(static_cast<size_t>(count) * 3 + 1);
+    const int e = elem_bytes(dtype);
+    for (int64_t i = 0; i < count; ++i) {
+        const int st = splitk::check_gemm_bt(A[i], B[i], out[i], workspace, workspace_bytes, M, N, K, splits,
+                                             k_per_split, dtype, fused);
+        if (st != SPLITK_OK) return st;
+        ranges.push_back({range_of(A[i], static_cast<uint64_t>(M * K) * e), false});
+        ranges.push_back({range_of(B[i], static_cast<uint64_t>(N * K) * e), false});
+        ranges.push_back({range_of(out[i], static_cast<uint64_t>(M * N) * 4), true});
+    }
+    ranges.push_back({range_of(workspace, gemm_bt_workspace_bytes(M, N, K, splits, k_per_split, fused)), true});
+    std::sort(ranges.begin(), ranges.end(),
+              [](const std::pair<Range, bool> &x, const std::pair<Range, bool> &y) { return x.first.lo < y.first.lo; });
+    // sweep: the furthest end seen so far, and whether an output reaches it
+    uint64_t reach = 0, out_reach = 0;
+    for (size_t i = 0; i < ranges.size(); ++i) {
+        const Range &r = ranges[i].first;
+        if (r.hi <= r.lo) continue;
+        if (i > 0 && (r.lo < out_reach || (ranges[i].second && r.lo < reach))) return SPLITK_ERR_ALIAS;
+        reach = std::max(reach, r.hi);
+        if (ranges[i].second) out_reach = std::max(out_reach, r.hi);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool batch = fused == 1 && dtype != SPLITK_F32 &&
+                       splitk::fused_in_kernel(M, N, K, splits, k_per_split, dtype, false) &&
+                       splitk::batch_possible(M, N, K, splits, k_per_split);
+    for (int64_t i = 0; i < count;) {
+        const int64_t n = batch ? std::min<int64_t>(count - i, splitk::kMaxGroup) : 1;
+        int st;
+        if (n > 1) {
+            st = splitk::run_fused_batch(A + i, B + i, out + i, static_cast<int>(n), M, N, K, splits, k_per_split,
+                                         dtype, s);
+        } else {
+            st = gemm_impl(A[i], B[i], out[i], workspace, workspace_bytes, M, N, K, splits, k_per_split, dtype, fused,
+                           false, stream);
+        }
+        if (st != SPLITK_OK) return st;
+        i += n;
+    }
+    return SPLITK_OK;
 }
 
 int gemm_kn(const void *A, const void *W, float *out, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,

@@ -624,6 +624,41 @@ def test_kn_every_tiling(lib, orc, case):
     assert len(seen) > 4
 
 
+BATCH_CASES = [(256, 1024, 2048, 2, 1024, "bf16", 1, 13), (96, 512, 2048, 4, 512, "f16", 1, 3),
+               (32, 512, 2048, 1, 2048, "f32", 1, 2), (256, 1024, 2048, 2, 1024, "bf16", 0, 4),
+               (160, 192, 320, 3, 128, "bf16", 1, 5)]
+
+
+@pytest.mark.parametrize("case", BATCH_CASES, ids=[f"{c[5]}-M{c[0]}N{c[1]}K{c[2]}S{c[3]}-f{c[6]}x{c[7]}"
+                                                    for c in BATCH_CASES])
+def test_batch_matches_single_calls(lib, case):
+    """gemm_bt_batch: every output bitwise the gemm_bt result for its
+    operands (one weight repeated for half the operations), guards intact;
+    fused 16-bit calls whose plan groups run up to 8 to a launch."""
+    sk = lib
+    M, N, K, S, kps, dt, fused, count = case
+    cs = [oracle_case(M, N, K, S, kps, dt, "uniform", 100 + i) for i in range(count)]
+    As = [device_operand(c[0].A, dt) for c in cs]
+    Bs = [device_operand(c[0].B, dt) for c in cs]
+    Bs = [Bs[i] if i % 2 == 0 else Bs[0] for i in range(count)]   # repeated weights
+    ws, nbytes = workspace(M, N, K, S, kps)
+    refs = []
+    for A, B in zip(As, Bs):
+        o = Guarded(M * N)
+        sk.gemm_bt(A, B, o.data, ws.data, nbytes, M, N, K, S, kps, dt, fused=fused)
+        refs.append(o.numpy().copy())
+    outs = [Guarded(M * N) for _ in range(count)]
+    sk.gemm_bt_batch(As, Bs, [o.data for o in outs], count, ws.data, nbytes, M, N, K, S, kps, dt, fused=fused)
+    torch.cuda.synchronize()
+    assert sk.splitk_get_device_status() == 0
+    plan = sk.splitk_describe_launch(M, N, K, S, kps, dt, fused=fused)
+    if fused and dt != "f32" and plan["fused_in_kernel"] and plan["compact"]:
+        assert sk.splitk_last_launch()["group"] == (count - 1) % 8 + 1
+    for o, r in zip(outs, refs):
+        assert np.array_equal(o.numpy().view(np.uint32), r.view(np.uint32))
+        assert o.guards_intact()
+
+
 @pytest.mark.parametrize("nstreams,opc", [(1, 1), (2, 0), (2, 4)])
 def test_host_batch_alternating_staging_in_flight(lib, nstreams, opc):
     """Six batches over two alternating staging buffers, on one stream or two

@@ -287,6 +287,41 @@ def test_host_batch_rejections(L):
     assert call(M=48, A=0) == bd.ERR_SHAPE
 
 
+def test_batch_rejections(L):
+    """gemm_bt_batch checks every operation and the outputs against one
+    another, every input and the workspace before it touches CUDA (no GPU
+    here)."""
+    M, N, K, S, kps = 32, 64, 128, 2, 64
+    a_bytes, o_bytes = M * K * 2, M * N * 4                     # 8 KiB each
+    need = sk.gemm_bt_workspace_bytes(M, N, K, S, kps)
+
+    def call(A=(A0, A0 + a_bytes), B=(B0, B0), O=(O0, O0 + o_bytes), count=2, ws=W0, wsb=need, fused=1,
+             dtype=bd.BF16, **kw):
+        g = dict(GOOD, **kw)
+        arrs = [ctypes.cast(bd.pointer_array(list(x)), ctypes.c_void_p) if x is not None else None
+                for x in (A, B, O)]
+        return L.gemm_bt_batch(*arrs, count, ws, wsb, g["M"], g["N"], g["K"], g["S"], g["kps"], dtype, fused,
+                               None)
+
+    assert call(count=0) == bd.ERR_CONFIG
+    assert call(count=(1 << 16) + 1) == bd.ERR_CONFIG
+    assert call(fused=2) == bd.ERR_CONFIG
+    assert call(fused=3) == bd.ERR_CONFIG
+    assert call(A=None) == bd.ERR_NULL
+    assert call(O=None) == bd.ERR_NULL
+    assert call(B=(B0, 0)) == bd.ERR_NULL
+    assert call(M=48) == bd.ERR_SHAPE
+    assert call(S=3) == bd.ERR_SPLIT
+    assert call(dtype=5) == bd.ERR_DTYPE
+    assert call(O=(O0, O0 + 8)) == bd.ERR_ALIGN
+    assert call(wsb=need - 16) == bd.ERR_WORKSPACE
+    assert call(O=(O0, O0 + o_bytes - 16)) == bd.ERR_ALIAS            # two outputs overlap
+    assert call(O=(O0, A0 + 64)) == bd.ERR_ALIAS                      # an output over another call's input
+    assert call(A=(A0, O0 + 256)) == bd.ERR_ALIAS                     # an input over another call's output
+    assert call(O=(O0, W0 + 16)) == bd.ERR_ALIAS                      # an output over the workspace
+    assert call(M=48, A=None) == bd.ERR_NULL                          # the arrays first
+
+
 def test_choose_splits_is_legal(L, orc):
     """The model's choice is always a legal geometry drawn from the candidates:
     the largest candidate whose estimate is within 2% of the smallest."""
