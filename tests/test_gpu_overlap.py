@@ -19,7 +19,7 @@ the headline case is checked against the oracle here too.
 import numpy as np
 import pytest
 
-from harness import TOL_FINAL, device_operand, max_scaled_error, oracle_case
+from harness import TOL_FINAL, TOL_PARTIAL, device_operand, max_scaled_error, oracle_case
 
 pytestmark = pytest.mark.gpu
 
@@ -752,12 +752,15 @@ GRAPH_CASES = random_graph_cases(16) + [
 
 @pytest.mark.parametrize("case", GRAPH_CASES,
                          ids=[f"{c[5]}{'-kn' if c[6] else ''}-M{c[0]}N{c[1]}K{c[2]}S{c[3]}-f{c[7]}" for c in GRAPH_CASES])
-def test_random_graphs_bitwise(grouping, case):
+def test_random_graphs_bitwise(grouping, orc, case):
     """Six independent calls of a random shape captured into one graph
     (grouping on: joined launches, merged chunks, whole-K blocks and the
     conversion of a run's first launch wherever the planner takes them):
     every output, and the partials kept with fused=3, bitwise the same calls
-    made eagerly."""
+    made eagerly, and the first call's at 300 seeded points within the
+    pages' tolerances of the oracle."""
+    import splitk_inputs as gen
+
     sk = grouping
     M, N, K, S, kps, dt, kn, fused = case
     insts = instances(sk, M, N, K, S, kps, dt, 6, seed0=M + N + K)
@@ -788,3 +791,20 @@ def test_random_graphs_bitwise(grouping, case):
         for it, w in zip(insts, refs_ws):
             assert bitwise(it["ws"][:S * M * N], w[:S * M * N])
     assert sk.splitk_get_device_status() == 0
+    # the first call against the oracle at seeded points (split -1: the output)
+    ops = gen.uniform(M, N, K, dt, seed=M + N + K)
+    rng = np.random.Generator(np.random.PCG64(K))
+    npts = 300
+    sp = rng.integers(-1, S if fused == 3 else 0, npts)
+    m, n = rng.integers(0, M, npts), rng.integers(0, N, npts)
+    sp[:4] = -1
+    m[:4], n[:4] = [0, M - 1, 0, M - 1], [0, 0, N - 1, N - 1]   # the zero first row, the x4 last row
+    val, bound = orc.points(ops.A, ops.B, dt, kps, S, sp, m, n)
+    got = insts[0]["out"].cpu().numpy()[m, n]
+    if fused == 3:
+        P0 = insts[0]["ws"][:S * M * N].view(S, M, N).cpu().numpy()
+        got = np.where(sp >= 0, P0[np.maximum(sp, 0), m, n], got)
+    part = sp >= 0
+    assert max_scaled_error(got[~part], val[~part], bound[~part]) <= TOL_FINAL[dt]
+    if part.any():
+        assert max_scaled_error(got[part], val[part], bound[part]) <= TOL_PARTIAL
