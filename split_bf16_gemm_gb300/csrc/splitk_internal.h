@@ -59,6 +59,13 @@ constexpr int kMaxStages = 8;
 constexpr int kMaxKbs = 4;     // k-blocks in one pipeline stage (one TMA box per operand)
 constexpr int kMaxChunks = 8;  // portable cluster size
 constexpr int kMaxGroup = 8;   // independent calls one launch may compute (graph capture)
+constexpr size_t kSmemLimit = 226 * 1024;   // dynamic shared memory of a CTA; leaves room for static shared memory
+
+// Whether a CTA with `smem` bytes of dynamic shared memory may allocate `cols`
+// tensor-memory columns: the rule that keeps every mix of these kernels'
+// CTAs that fits an SM by shared memory within its 512 columns
+// (splitk_plan.cu).
+bool tmem_fits(int cols, size_t smem);
 
 // Tile choice for a shape (automatic, or the process-wide override).
 // x3: F32 operands as 3xTF32 (else 16-bit operands).
