@@ -145,7 +145,8 @@ int run_partial_pass(const void *A, const void *B, float *P, float *out, int64_t
     pr.overlap = chain.overlap();
     pr.store_early = chain.store_early();
     // a call that touches nothing in flight, with the same shape and plan as
-    // the launch before it, joins that launch (no node added)
+    // the launch before it, joins that launch (no node added); the first such
+    // call after a run's first launch may convert that launch to its own plan
     int group = 1, mode = pr.overlap ? (pr.store_early ? 2 : 1) : 0;
     bool broken = false;
     if (pr.store_early && splitk::grouping_enabled() &&
