@@ -322,6 +322,38 @@ def test_batch_rejections(L):
     assert call(M=48, A=None) == bd.ERR_NULL                          # the arrays first
 
 
+def test_batch_alias_rule(L):
+    """gemm_bt_batch's overlap check against brute force on seeded random
+    layouts: every layout where some output overlaps another output, an input
+    or the workspace is rejected with ERR_ALIAS before any device work.
+    (Layouts that pass would launch on these made-up addresses, so they are
+    not called: the GPU tests run the accepted layouts on real buffers.)"""
+    import numpy as np
+
+    M, N, K, S, kps = 32, 64, 128, 2, 64
+    a_bytes, b_bytes, o_bytes = M * K * 2, N * K * 2, M * N * 4
+    ws_bytes = sk.gemm_bt_workspace_bytes(M, N, K, S, kps)
+    rng = np.random.Generator(np.random.PCG64(11))
+    seen = {True: 0, False: 0}
+    for _ in range(300):
+        count = int(rng.integers(1, 5))
+        slot = lambda: 0x10000000 + 1024 * int(rng.integers(0, 160))   # 16-byte aligned, often overlapping
+        A = [slot() for _ in range(count)]
+        B = [slot() for _ in range(count)]
+        O = [slot() for _ in range(count)]
+        W = slot()
+        ranges = [(a, a + a_bytes, False) for a in A] + [(b, b + b_bytes, False) for b in B] + \
+                 [(o, o + o_bytes, True) for o in O] + [(W, W + ws_bytes, True)]
+        alias = any(r[2] and q is not r and r[0] < q[1] and q[0] < r[1] for r in ranges for q in ranges)
+        seen[alias] += 1
+        if not alias:
+            continue
+        arrs = [ctypes.cast(bd.pointer_array(x), ctypes.c_void_p) for x in (A, B, O)]
+        st = L.gemm_bt_batch(*arrs, count, W, ws_bytes, M, N, K, S, kps, bd.BF16, 1, None)
+        assert st == bd.ERR_ALIAS, (A, B, O, W, st)
+    assert seen[True] > 20, seen
+
+
 def test_choose_splits_is_legal(L, orc):
     """The model's choice is always a legal geometry drawn from the candidates:
     the largest candidate whose estimate is within 2% of the smallest."""
