@@ -42,8 +42,9 @@
  * failed) or the launch itself failed (SPLITK_ERR_CUDA).  No exception and no
  * abort crosses the ABI.  Every wait inside a kernel has a time limit; a wait
  * that runs out sets a device status word, which splitk_get_device_status()
- * reads.  The three compute entry points (gemm_splitk_bt, splitk_reduce,
- * gemm_bt) may be captured into a CUDA graph.
+ * reads.  The compute entry points (gemm_splitk_bt, splitk_reduce, gemm_bt,
+ * their [K,N] forms, gemm_bt_batch and gemm_bt_noalloc after its first call)
+ * may be captured into a CUDA graph.
  *
  * Consecutive launches inside a graph: every launch is a programmatic
  * dependent of the one before it on its stream.  Eagerly, each launch waits
@@ -56,16 +57,17 @@
  * grid only before its first store ("overlap"); if none of them reads or
  * writes what the new launch writes either, it also stores at once and
  * waits only before it finishes, so the grids still finish in launch order.
- * Such a fused launch may also give each thread block all the chunks of its
- * split (or two consecutive chunks), each in its own accumulator, added in
- * pairs inside the block (the owner adds a split's chunks in pairs too),
- * or, for large shapes with full splits, every chunk of every split.
+ * Such a fused launch may also give each thread block two consecutive chunks
+ * of its split (all of them where a split has two), each in its own
+ * accumulator, added inside the block (the owner adds a split's chunks in
+ * pairs too), or, for large shapes with full splits, every chunk of every
+ * split.
  * A call that may store early and has the same shape and plan as the launch
  * before it joins that launch instead of adding one: the launch's graph
  * node then computes both calls (up to 8), whose blocks may run in any
  * order; the first such call after a run's first launch may also switch
- * that launch to its own (whole-K) plan.  Its results are bitwise those of
- * the same launch without overlap.
+ * that launch to its own plan (compact, or whole-K).  Its results are
+ * bitwise those of the same launch without overlap.
  * Launches that read what an
  * earlier one writes (a chain of GEMMs, the reduce after the partial pass),
  * launches after another kernel or a copy, and launches outside a capture
