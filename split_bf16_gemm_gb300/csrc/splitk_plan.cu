@@ -7,7 +7,7 @@
 // The operation it plans is the partial pass (and optionally the split sum)
 // of the pages "Aligned shared rows for pipelined NAX on CUDA" and "Wider
 // consecutive-weight NAX GEMM" (sections "Contract and correctness" /
-// "Launch contract and correctness"); the tiling is this build's own.
+// "Launch contract and correctness"); the tiling is the library's own.
 
 #include <algorithm>
 #include <cmath>
